@@ -1,0 +1,270 @@
+/*
+ * Exact-attention oracle: plain, slow, fp64 CPU code.
+ *
+ * TEST INFRASTRUCTURE ONLY. Nothing on the product path may link, load or
+ * call this file; only the tests, the smoke check and the CPU-baseline leg of
+ * the benchmark do. It shares no code, header or constant with the CUDA
+ * library.
+ *
+ * What it computes is the plain definition of scaled dot-product attention,
+ * one query row at a time, with no tiling:
+ *   S = scale * Q K^T                      (tutorial page "research-attention",
+ *                                           section 01, first equation)
+ *   P = row-softmax(S)                     (same section, second equation)
+ *   O = P V                                (same section, third equation)
+ *   L_i = log sum_j exp(S_ij) = m_i + log l_i
+ *                                          (same page, section 04: the saved
+ *                                           statistic L = m + log(l))
+ * With a causal mask, S_ij = -inf for key j > query i (standard lower
+ * triangle; the pages only name the mask as an experiment parameter, section
+ * 06 of the same page).
+ *
+ * Backward, for an upstream gradient dO and no gradient through L (blog page
+ * "Flash Attention 原理与实现", section "Backward 的 Tiling 策略", written out):
+ *   dV = P^T dO
+ *   dP = dO V^T
+ *   D_i = sum_c dO_ic O_ic
+ *   dS = P o (dP - D)            (softmax gradient, row-wise)
+ *   dQ = scale * dS K
+ *   dK = scale * dS^T Q
+ * The factor `scale` in dQ/dK makes these the true derivatives of O(Q,K,V);
+ * the finite-difference tests pin it.
+ *
+ * Layout: every matrix is contiguous [B][H][N][d] (row-major), L is [B][H][N].
+ * All arithmetic is double precision; the max is subtracted before exp, as
+ * the tutorial's section 02 prescribes.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+static double dot(const double *a, const double *b, int d) {
+  double s = 0.0;
+  for (int c = 0; c < d; ++c) s += a[c] * b[c];
+  return s;
+}
+
+/* Number of keys query row i may see. */
+static int visible_keys(int i, int N, int causal) { return causal ? i + 1 : N; }
+
+/* One query row of one head: scores s[0..nk), probabilities p, output o, and
+ * the log-sum-exp. q is the query row, k/v point at the head's [N][d] keys and
+ * values. Returns L_i. */
+static double row_forward(const double *q, const double *k, const double *v,
+                          int nk, int d, double scale, double *s, double *p,
+                          double *o) {
+  double m = -INFINITY;
+  for (int j = 0; j < nk; ++j) {
+    s[j] = scale * dot(q, k + (size_t)j * d, d);
+    if (s[j] > m) m = s[j];
+  }
+  double l = 0.0;
+  for (int j = 0; j < nk; ++j) {
+    p[j] = exp(s[j] - m);
+    l += p[j];
+  }
+  for (int j = 0; j < nk; ++j) p[j] /= l;
+  for (int c = 0; c < d; ++c) o[c] = 0.0;
+  for (int j = 0; j < nk; ++j) {
+    const double *vj = v + (size_t)j * d;
+    for (int c = 0; c < d; ++c) o[c] += p[j] * vj[c];
+  }
+  return m + log(l);
+}
+
+/* Forward over all heads and rows. */
+void oracle_fwd(const double *q, const double *k, const double *v, double *o,
+                double *lse, int B, int H, int N, int d, double scale,
+                int causal) {
+  const int64_t rows = (int64_t)B * H * N;
+#pragma omp parallel
+  {
+    double *s = (double *)malloc(sizeof(double) * (size_t)N);
+    double *p = (double *)malloc(sizeof(double) * (size_t)N);
+#pragma omp for schedule(dynamic, 16)
+    for (int64_t r = 0; r < rows; ++r) {
+      const int64_t bh = r / N;
+      const int i = (int)(r % N);
+      const size_t head = (size_t)bh * N * d;
+      lse[r] = row_forward(q + (size_t)r * d, k + head, v + head,
+                           visible_keys(i, N, causal), d, scale, s, p,
+                           o + (size_t)r * d);
+    }
+    free(s);
+    free(p);
+  }
+}
+
+/* Full softmax matrix P of one head (small N only; for invariant tests). */
+void oracle_probs(const double *q, const double *k, int N, int d, double scale,
+                  int causal, double *P) {
+  double *s = (double *)malloc(sizeof(double) * (size_t)N);
+  double *o = (double *)malloc(sizeof(double) * (size_t)d);
+  double *vz = (double *)calloc((size_t)N * d, sizeof(double));
+  for (int i = 0; i < N; ++i) {
+    double *prow = P + (size_t)i * N;
+    int nk = visible_keys(i, N, causal);
+    row_forward(q + (size_t)i * d, k, vz, nk, d, scale, s, prow, o);
+    for (int j = nk; j < N; ++j) prow[j] = 0.0;
+  }
+  free(s);
+  free(o);
+  free(vz);
+}
+
+/* Backward of one head: q,k,v,dO are that head's [N][d] blocks. dk, dv are
+ * accumulated into (caller zeroes them); dq rows are written. Row-at-a-time
+ * with O(N) scratch. */
+static void head_backward(const double *q, const double *k, const double *v,
+                          const double *dO, double *dq, double *dk, double *dv,
+                          int N, int d, double scale, int causal, double *s,
+                          double *p, double *o) {
+  for (int i = 0; i < N; ++i) {
+    const double *qi = q + (size_t)i * d;
+    const double *doi = dO + (size_t)i * d;
+    const int nk = visible_keys(i, N, causal);
+    row_forward(qi, k, v, nk, d, scale, s, p, o);
+    const double Di = dot(doi, o, d);
+    double *dqi = dq + (size_t)i * d;
+    for (int c = 0; c < d; ++c) dqi[c] = 0.0;
+    for (int j = 0; j < nk; ++j) {
+      const double *kj = k + (size_t)j * d;
+      const double dPij = dot(doi, v + (size_t)j * d, d);
+      const double dSij = p[j] * (dPij - Di);
+      double *dkj = dk + (size_t)j * d;
+      double *dvj = dv + (size_t)j * d;
+      for (int c = 0; c < d; ++c) {
+        dqi[c] += scale * dSij * kj[c];
+        dkj[c] += scale * dSij * qi[c];
+        dvj[c] += p[j] * doi[c];
+      }
+    }
+  }
+}
+
+/* Backward over all heads. Outputs dq, dk, dv are overwritten. */
+void oracle_bwd(const double *q, const double *k, const double *v,
+                const double *dO, double *dq, double *dk, double *dv, int B,
+                int H, int N, int d, double scale, int causal) {
+  const int64_t heads = (int64_t)B * H;
+  const size_t hs = (size_t)N * d;
+#pragma omp parallel
+  {
+    double *s = (double *)malloc(sizeof(double) * (size_t)N);
+    double *p = (double *)malloc(sizeof(double) * (size_t)N);
+    double *o = (double *)malloc(sizeof(double) * (size_t)d);
+#pragma omp for schedule(dynamic, 1)
+    for (int64_t bh = 0; bh < heads; ++bh) {
+      const size_t off = (size_t)bh * hs;
+      memset(dk + off, 0, sizeof(double) * hs);
+      memset(dv + off, 0, sizeof(double) * hs);
+      head_backward(q + off, k + off, v + off, dO + off, dq + off, dk + off,
+                    dv + off, N, d, scale, causal, s, p, o);
+    }
+    free(s);
+    free(p);
+    free(o);
+  }
+}
+
+/* Sampled query rows of one head: O_i, L_i and dQ_i for rows[0..nrows).
+ * q,k,v,dO are the head's [N][d] blocks. Each row costs O(N d). */
+void oracle_query_rows(const double *q, const double *k, const double *v,
+                       const double *dO, int N, int d, double scale, int causal,
+                       const int64_t *rows, int nrows, double *o_out,
+                       double *lse_out, double *dq_out) {
+#pragma omp parallel
+  {
+    double *s = (double *)malloc(sizeof(double) * (size_t)N);
+    double *p = (double *)malloc(sizeof(double) * (size_t)N);
+#pragma omp for schedule(dynamic, 1)
+    for (int r = 0; r < nrows; ++r) {
+      const int i = (int)rows[r];
+      const double *qi = q + (size_t)i * d;
+      const double *doi = dO + (size_t)i * d;
+      double *oi = o_out + (size_t)r * d;
+      const int nk = visible_keys(i, N, causal);
+      lse_out[r] = row_forward(qi, k, v, nk, d, scale, s, p, oi);
+      const double Di = dot(doi, oi, d);
+      double *dqi = dq_out + (size_t)r * d;
+      for (int c = 0; c < d; ++c) dqi[c] = 0.0;
+      for (int j = 0; j < nk; ++j) {
+        const double dSij = p[j] * (dot(doi, v + (size_t)j * d, d) - Di);
+        const double *kj = k + (size_t)j * d;
+        for (int c = 0; c < d; ++c) dqi[c] += scale * dSij * kj[c];
+      }
+    }
+    free(s);
+    free(p);
+  }
+}
+
+/* Sampled key rows of one head: dK_j and dV_j for keys[0..nkeys).
+ * Every query row that sees one of the keys contributes, so each such row is
+ * run forward in full (its P row and D_i), then its terms for the sampled keys
+ * are added. Rows are split over threads with private partial sums that are
+ * added at the end. */
+void oracle_key_rows(const double *q, const double *k, const double *v,
+                     const double *dO, int N, int d, double scale, int causal,
+                     const int64_t *keys, int nkeys, double *dk_out,
+                     double *dv_out) {
+  int64_t jmin = N;
+  for (int t = 0; t < nkeys; ++t)
+    if (keys[t] < jmin) jmin = keys[t];
+  const int first_row = causal ? (int)jmin : 0;
+  const size_t acc = (size_t)nkeys * d;
+  memset(dk_out, 0, sizeof(double) * acc);
+  memset(dv_out, 0, sizeof(double) * acc);
+#pragma omp parallel
+  {
+    double *s = (double *)malloc(sizeof(double) * (size_t)N);
+    double *p = (double *)malloc(sizeof(double) * (size_t)N);
+    double *o = (double *)malloc(sizeof(double) * (size_t)d);
+    double *pk = (double *)calloc(acc, sizeof(double));
+    double *pv = (double *)calloc(acc, sizeof(double));
+#pragma omp for schedule(dynamic, 8)
+    for (int i = first_row; i < N; ++i) {
+      const double *qi = q + (size_t)i * d;
+      const double *doi = dO + (size_t)i * d;
+      const int nk = visible_keys(i, N, causal);
+      row_forward(qi, k, v, nk, d, scale, s, p, o);
+      const double Di = dot(doi, o, d);
+      for (int t = 0; t < nkeys; ++t) {
+        const int j = (int)keys[t];
+        if (j >= nk) continue;
+        const double dSij = p[j] * (dot(doi, v + (size_t)j * d, d) - Di);
+        double *a = pk + (size_t)t * d;
+        double *b = pv + (size_t)t * d;
+        for (int c = 0; c < d; ++c) {
+          a[c] += scale * dSij * qi[c];
+          b[c] += p[j] * doi[c];
+        }
+      }
+    }
+#pragma omp critical
+    {
+      for (size_t x = 0; x < acc; ++x) {
+        dk_out[x] += pk[x];
+        dv_out[x] += pv[x];
+      }
+    }
+    free(s);
+    free(p);
+    free(o);
+    free(pk);
+    free(pv);
+  }
+}
+
+/* Threads the OpenMP runtime will use (1 without OpenMP). */
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}

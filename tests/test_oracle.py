@@ -1,0 +1,411 @@
+"""Pins for the fp64 CPU oracle: the pages' worked examples, closed forms,
+invariants and finite differences. None of these compares the oracle with a
+retyped copy of itself.
+
+Sources:
+  * tutorial page "research-attention", section 03: single-row demo (scores
+    [1,2,0,3], tile size 2) with its printed state after the first tile and its
+    printed result;
+  * LLaMA 3 notes page "Flash Attention", the 4-token d=2 example (Q=K=V=X,
+    scale 1/sqrt(2)) with its printed softmax row, denominator, numerators and
+    outputs of tokens 0 and 1;
+  * tutorial section 02 (the recurrence, "one division at the end") and
+    section 04 (L = m + log l);
+  * blog page "Flash Attention 原理与实现", section "Backward 的 Tiling 策略"
+    (the gradient products), checked by central finite differences.
+"""
+import json
+import math
+import os
+import shutil
+import subprocess
+import tempfile
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle.online_softmax import tiled_row
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+# ---------------------------------------------------------------- worked examples
+
+def test_tutorial_single_row_full_attention():
+    """The demo row as full attention: q=[1,0], k_j=[s_j,0], scale 1, so every
+    query row has scores [1,2,0,3]; the page prints [0.795176, 2.200684]."""
+    g = _golden("tutorial_single_row.json")
+    s = np.array(g["scores"])
+    N = len(s)
+    q = np.tile([1.0, 0.0], (N, 1))[None, None]
+    k = np.stack([s, np.zeros(N)], axis=1)[None, None]
+    v = np.array(g["values"])[None, None]
+    o, lse = oracle.attention_fwd(q, k, v, scale=1.0, causal=False)
+    half_ulp = 0.5 * 10.0 ** (-g["printed_output_decimals"])
+    for i in range(N):
+        assert np.max(np.abs(o[0, 0, i] - np.array(g["printed_output"]))) <= half_ulp
+    # L is the log of the one-shot denominator: sum_j e^{s_j}
+    assert abs(lse[0, 0, 0] - math.log(sum(math.exp(x) for x in s))) < 1e-12
+
+
+def test_tutorial_recurrence_states_and_result():
+    g = _golden("tutorial_single_row.json")
+    o, L, states = tiled_row(g["scores"], g["values"], g["tile"])
+    half_ulp = 0.5 * 10.0 ** (-g["state_decimals"])
+    st = states[0]
+    assert st.m == g["state_after_first_tile"]["m"]
+    assert abs(st.l - g["state_after_first_tile"]["l"]) <= half_ulp
+    assert np.max(np.abs(np.array(st.u) - g["state_after_first_tile"]["u"])) <= half_ulp
+    assert np.max(np.abs(np.array(o) - g["printed_output"])) <= half_ulp
+    # the page's own check: tiled vs one-shot within 1e-12
+    s = np.array(g["scores"])
+    q = np.tile([1.0, 0.0], (4, 1))[None, None]
+    k = np.stack([s, np.zeros(4)], axis=1)[None, None]
+    o_ref, lse_ref = oracle.attention_fwd(q, k, np.array(g["values"])[None, None], 1.0)
+    assert np.max(np.abs(np.array(o) - o_ref[0, 0, 0])) < g["tiled_vs_one_shot_bound"]
+    assert abs(L - lse_ref[0, 0, 0]) < 1e-12
+
+
+def test_llama_notes_four_tokens():
+    g = _golden("llama_notes_four_tokens.json")
+    X = np.array(g["X"])
+    scale = 1.0 / math.sqrt(X.shape[1])
+    x4 = X[None, None]
+    o, lse = oracle.attention_fwd(x4, x4, x4, scale)
+    o, lse = o[0, 0], lse[0, 0]
+    assert np.max(np.abs(o[0] - g["output_token0"])) <= g["tol_outputs"]
+    assert np.max(np.abs(o[1] - g["output_token1"])) <= g["tol_outputs"]
+    P = oracle.softmax_probs(X, X, scale)
+    assert np.max(np.abs(P[0] - g["softmax_row0"])) <= g["tol_softmax"]
+    # the page's denominator and numerators carry no max shift: den = e^L, num = O * den
+    den0 = math.exp(lse[0])
+    assert abs(den0 - g["denominator_row0"]) <= g["tol_sums"]
+    assert np.max(np.abs(o[0] * den0 - g["numerators_row0"])) <= g["tol_sums"]
+    den1 = math.exp(lse[1])
+    assert np.max(np.abs(o[1] * den1 - g["numerators_row1"])) <= g["tol_sums"]
+    # "symmetric queries give symmetric outputs" (summary of the same section)
+    assert np.max(np.abs(o[1] - o[0][::-1])) < 1e-12
+
+
+# ---------------------------------------------------------------- invariants
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_every_tile_size_matches_one_shot(seed):
+    """Tutorial section 03: tiling yields the same exact attention for any block size."""
+    r = _rng(seed)
+    N, d = 13, 3
+    q = r.standard_normal((1, 1, N, d))
+    k = r.standard_normal((1, 1, N, d)) * 3.0
+    v = r.standard_normal((1, 1, N, d))
+    for causal in (False, True):
+        o_ref, lse_ref = oracle.attention_fwd(q, k, v, 0.7, causal)
+        for i in range(N):
+            s = [0.7 * float(np.dot(q[0, 0, i], k[0, 0, j])) if (not causal or j <= i) else -math.inf
+                 for j in range(N)]
+            for tile in range(1, N + 1):
+                o_t, L_t, _ = tiled_row(s, v[0, 0].tolist(), tile)
+                assert np.max(np.abs(np.array(o_t) - o_ref[0, 0, i])) < 1e-12
+                assert abs(L_t - lse_ref[0, 0, i]) < 1e-12
+
+
+def test_fully_masked_leading_tile_keeps_state():
+    """A tile that is all -inf before any finite score leaves (m, l, u) at its start."""
+    o, L, states = tiled_row([-math.inf, -math.inf, 0.5, 1.5], [[1, 0], [0, 1], [2, 0], [0, 2]], 2)
+    assert states[0].m == -math.inf and states[0].l == 0.0 and states[0].u == [0.0, 0.0]
+    w = np.exp(np.array([0.5, 1.5]) - 1.5)
+    ref = (w[0] * np.array([2, 0]) + w[1] * np.array([0, 2])) / w.sum()
+    assert np.max(np.abs(np.array(o) - ref)) < 1e-15
+
+
+def test_probability_rows_sum_to_one_and_mask():
+    r = _rng(3)
+    N, d = 37, 8
+    q, k = r.standard_normal((N, d)), r.standard_normal((N, d))
+    for causal in (False, True):
+        P = oracle.softmax_probs(q, k, 0.4, causal)
+        assert np.max(np.abs(P.sum(axis=1) - 1.0)) < 1e-12
+        assert (P >= 0).all()
+        if causal:
+            assert np.all(P[np.triu_indices(N, 1)] == 0.0)
+            assert np.all(P[np.tril_indices(N)] > 0.0)
+
+
+def test_key_permutation_permutes_probability_columns_only():
+    r = _rng(4)
+    N, d = 20, 5
+    q, k, v = (r.standard_normal((1, 1, N, d)) for _ in range(3))
+    perm = r.permutation(N)
+    o1, l1 = oracle.attention_fwd(q, k, v, 0.5)
+    o2, l2 = oracle.attention_fwd(q, k[:, :, perm], v[:, :, perm], 0.5)
+    assert np.max(np.abs(o1 - o2)) < 1e-12 and np.max(np.abs(l1 - l2)) < 1e-12
+    P1 = oracle.softmax_probs(q[0, 0], k[0, 0], 0.5)
+    P2 = oracle.softmax_probs(q[0, 0], k[0, 0, perm], 0.5)
+    assert np.max(np.abs(P1[:, perm] - P2)) < 1e-15
+
+
+def test_batch_and_head_independence():
+    """Heads never mix: each (b, h) slice equals the same slice computed alone."""
+    r = _rng(5)
+    q, k, v, dO = (r.standard_normal((2, 3, 9, 4)) for _ in range(4))
+    o, lse = oracle.attention_fwd(q, k, v, 0.6, True)
+    dq, dk, dv = oracle.attention_bwd(q, k, v, dO, 0.6, True)
+    for b in range(2):
+        for h in range(3):
+            sl = (slice(b, b + 1), slice(h, h + 1))
+            o1, l1 = oracle.attention_fwd(q[sl], k[sl], v[sl], 0.6, True)
+            g1 = oracle.attention_bwd(q[sl], k[sl], v[sl], dO[sl], 0.6, True)
+            assert np.array_equal(o1[0, 0], o[b, h]) and np.array_equal(l1[0, 0], lse[b, h])
+            for a, full in zip(g1, (dq, dk, dv)):
+                assert np.array_equal(a[0, 0], full[b, h])
+
+
+# ---------------------------------------------------------------- closed forms
+
+def test_single_key_returns_value():
+    r = _rng(6)
+    q, k, v = (r.standard_normal((1, 2, 1, 6)) for _ in range(3))
+    o, lse = oracle.attention_fwd(q, k, v, 0.3)
+    assert np.array_equal(o, v)
+    assert np.max(np.abs(lse - 0.3 * np.sum(q * k, axis=-1))) < 1e-15
+
+
+def test_causal_first_row_sees_only_itself():
+    r = _rng(7)
+    q, k, v = (r.standard_normal((1, 1, 11, 4)) for _ in range(3))
+    o, lse = oracle.attention_fwd(q, k, v, 0.9, True)
+    assert np.array_equal(o[0, 0, 0], v[0, 0, 0])
+    assert abs(lse[0, 0, 0] - 0.9 * np.dot(q[0, 0, 0], k[0, 0, 0])) < 1e-15
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_zero_queries_average_values(causal):
+    r = _rng(8)
+    N, d = 17, 3
+    q = np.zeros((1, 1, N, d))
+    k, v, dO = (r.standard_normal((1, 1, N, d)) for _ in range(3))
+    o, lse = oracle.attention_fwd(q, k, v, 1.0, causal)
+    _, _, dv = oracle.attention_bwd(q, k, v, dO, 1.0, causal)
+    for i in range(N):
+        n = i + 1 if causal else N
+        assert np.max(np.abs(o[0, 0, i] - v[0, 0, :n].mean(axis=0))) < 1e-14
+        assert abs(lse[0, 0, i] - math.log(n)) < 1e-14
+    for j in range(N):
+        if causal:
+            ref = sum(dO[0, 0, i] / (i + 1) for i in range(j, N))
+        else:
+            ref = dO[0, 0].sum(axis=0) / N
+        assert np.max(np.abs(dv[0, 0, j] - ref)) < 1e-13
+
+
+def test_constant_score_shift_moves_lse_only():
+    """Adding c to every score of a row: P and O unchanged, L grows by c
+    (tutorial section 02: a common base leaves the ratio unchanged)."""
+    r = _rng(9)
+    N, d, c = 12, 4, 2.5
+    q, k, v = (r.standard_normal((1, 1, N, d)) for _ in range(3))
+    scale = 0.5
+    q2 = np.concatenate([q, np.full((1, 1, N, 1), c / scale)], axis=-1)
+    k2 = np.concatenate([k, np.ones((1, 1, N, 1))], axis=-1)
+    for causal in (False, True):
+        o1, l1 = oracle.attention_fwd(q, k, v, scale, causal)
+        v2 = np.concatenate([v, np.zeros((1, 1, N, 1))], axis=-1)
+        o2, l2 = oracle.attention_fwd(q2, k2, v2, scale, causal)
+        assert np.max(np.abs(o1 - o2[..., :d])) < 1e-13
+        assert np.max(np.abs(l2 - l1 - c)) < 1e-12
+
+
+def test_large_scores_stay_finite():
+    """Scores near 1e4: max subtraction keeps every exp argument <= 0 (blog,
+    pitfalls item 4; tutorial section 02)."""
+    r = _rng(10)
+    q = r.standard_normal((1, 1, 16, 4)) * 100
+    k = r.standard_normal((1, 1, 16, 4)) * 100
+    v, dO = r.standard_normal((1, 1, 16, 4)), r.standard_normal((1, 1, 16, 4))
+    o, lse = oracle.attention_fwd(q, k, v, 1.0, False)
+    g = oracle.attention_bwd(q, k, v, dO, 1.0, False)
+    assert np.abs(lse).max() > 1e3
+    assert np.isfinite(o).all() and np.isfinite(lse).all()
+    assert all(np.isfinite(x).all() for x in g)
+    # every output is a convex combination of value rows
+    assert (o <= v.max(axis=2, keepdims=True) + 1e-12).all()
+    assert (o >= v.min(axis=2, keepdims=True) - 1e-12).all()
+
+
+# ---------------------------------------------------------------- backward
+
+def _loss(q, k, v, dO, scale, causal):
+    o, _ = oracle.attention_fwd(q, k, v, scale, causal)
+    return float(np.sum(o * dO))
+
+
+@pytest.mark.parametrize("N", [1, 2, 3, 5, 8])
+@pytest.mark.parametrize("d", [1, 2, 4])
+@pytest.mark.parametrize("causal", [False, True])
+def test_gradients_match_central_differences(N, d, causal):
+    r = _rng(100 + 10 * N + d)
+    q, k, v, dO = (r.standard_normal((1, 1, N, d)) for _ in range(4))
+    scale = 0.8
+    grads = oracle.attention_bwd(q, k, v, dO, scale, causal)
+    h = 1e-6
+    for which, g in zip(range(3), grads):
+        num = np.zeros_like(g)
+        base = [q, k, v]
+        for idx in np.ndindex(g.shape):
+            plus = [x.copy() for x in base]
+            minus = [x.copy() for x in base]
+            plus[which][idx] += h
+            minus[which][idx] -= h
+            num[idx] = (_loss(*plus, dO, scale, causal) - _loss(*minus, dO, scale, causal)) / (2 * h)
+        err = np.max(np.abs(num - g)) / max(1.0, np.max(np.abs(g)))
+        assert err <= 1e-6, (which, err)
+
+
+def test_gradient_sum_rules():
+    """Softmax rows sum to 1, so each row of dS sums to 0: sum_j dK_j = 0 and
+    sum_j dV_j = sum_i dO_i."""
+    r = _rng(11)
+    q, k, v, dO = (r.standard_normal((2, 2, 33, 6)) for _ in range(4))
+    for causal in (False, True):
+        _, dk, dv = oracle.attention_bwd(q, k, v, dO, 0.4, causal)
+        assert np.max(np.abs(dk.sum(axis=2))) < 1e-12
+        assert np.max(np.abs(dv.sum(axis=2) - dO.sum(axis=2))) < 1e-12
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_against_torch_autograd_fp64(causal):
+    """An independent route: torch's fp64 softmax/matmul and autograd."""
+    torch = pytest.importorskip("torch")
+    r = _rng(12)
+    B, H, N, d = 2, 3, 40, 16
+    q, k, v, dO = (r.standard_normal((B, H, N, d)) for _ in range(4))
+    scale = 1 / math.sqrt(d)
+    tq, tk, tv = (torch.tensor(x, requires_grad=True) for x in (q, k, v))
+    s = torch.matmul(tq, tk.transpose(-1, -2)) * scale
+    if causal:
+        s = s.masked_fill(torch.triu(torch.ones(N, N, dtype=torch.bool), 1), float("-inf"))
+    o_t = torch.matmul(torch.softmax(s, dim=-1), tv)
+    o_t.backward(torch.tensor(dO))
+    o, lse = oracle.attention_fwd(q, k, v, scale, causal)
+    grads = oracle.attention_bwd(q, k, v, dO, scale, causal)
+    assert np.max(np.abs(o - o_t.detach().numpy())) < 1e-12
+    assert np.max(np.abs(lse - torch.logsumexp(s, dim=-1).detach().numpy())) < 1e-12
+    for g, t in zip(grads, (tq, tk, tv)):
+        assert np.max(np.abs(g - t.grad.numpy())) < 1e-11
+
+
+# ---------------------------------------------------------------- sampled-row entry points
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_sampled_rows_match_full(causal):
+    r = _rng(13)
+    N, d = 70, 8
+    q, k, v, dO = (r.standard_normal((1, 1, N, d)) for _ in range(4))
+    o, lse = oracle.attention_fwd(q, k, v, 0.35, causal)
+    dq, dk, dv = oracle.attention_bwd(q, k, v, dO, 0.35, causal)
+    rows = [0, 1, 17, 42, 69]
+    o_r, l_r, dq_r = oracle.query_rows(q[0, 0], k[0, 0], v[0, 0], dO[0, 0], rows, 0.35, causal)
+    assert np.max(np.abs(o_r - o[0, 0, rows])) < 1e-13
+    assert np.max(np.abs(l_r - lse[0, 0, rows])) < 1e-13
+    assert np.max(np.abs(dq_r - dq[0, 0, rows])) < 1e-13
+    keys = [0, 5, 33, 69]
+    dk_r, dv_r = oracle.key_rows(q[0, 0], k[0, 0], v[0, 0], dO[0, 0], keys, 0.35, causal)
+    assert np.max(np.abs(dk_r - dk[0, 0, keys])) < 1e-12
+    assert np.max(np.abs(dv_r - dv[0, 0, keys])) < 1e-12
+
+
+# ---------------------------------------------------------------- planted mistakes
+
+MUTATIONS = {
+    "dK without scale": ("dkj[c] += scale * dSij * qi[c];", "dkj[c] += dSij * qi[c];"),
+    "dS with wrong sign of D": ("p[j] * (dPij - Di)", "p[j] * (dPij + Di)"),
+    "dV transposed operand": ("dvj[c] += p[j] * doi[c];", "dvj[c] += p[j] * qi[c];"),
+    "causal sees one key too many": ("return causal ? i + 1 : N;",
+                                     "return causal ? (i + 2 < N ? i + 2 : N) : N;"),
+    "L without the max": ("return m + log(l);", "return log(l);"),
+    "softmax not normalised": ("for (int j = 0; j < nk; ++j) p[j] /= l;", ""),
+}
+
+
+class _Lib:
+    """ctypes view of a (possibly mutated) oracle build."""
+
+    def __init__(self, so):
+        import ctypes
+        self.P = ctypes.c_void_p
+        self.lib = ctypes.CDLL(so)
+        self.lib.oracle_fwd.argtypes = [self.P] * 5 + [ctypes.c_int] * 4 + [ctypes.c_double, ctypes.c_int]
+        self.lib.oracle_bwd.argtypes = [self.P] * 7 + [ctypes.c_int] * 4 + [ctypes.c_double, ctypes.c_int]
+
+    def fwd(self, q, k, v, scale, causal):
+        B, H, N, d = q.shape
+        o = np.empty_like(q); lse = np.empty(q.shape[:3])
+        self.lib.oracle_fwd(*(x.ctypes.data_as(self.P) for x in (q, k, v, o, lse)), B, H, N, d, scale, int(causal))
+        return o, lse
+
+    def bwd(self, q, k, v, dO, scale, causal):
+        B, H, N, d = q.shape
+        g = [np.empty_like(q) for _ in range(3)]
+        self.lib.oracle_bwd(*(x.ctypes.data_as(self.P) for x in (q, k, v, dO, *g)), B, H, N, d, scale, int(causal))
+        return g
+
+
+def _pins_hold(lib):
+    """The forward pins (tutorial row with its L, causal row 0) and the
+    finite-difference pin of the backward, run against ``lib``."""
+    g = _golden("tutorial_single_row.json")
+    s = np.array(g["scores"])
+    q = np.tile([1.0, 0.0], (4, 1))[None, None]
+    k = np.stack([s, np.zeros(4)], axis=1)[None, None]
+    o, lse = lib.fwd(q, k, np.array(g["values"])[None, None], 1.0, False)
+    if np.max(np.abs(o[0, 0, 0] - g["printed_output"])) > 5e-7:
+        return False
+    if abs(lse[0, 0, 0] - math.log(np.exp(s).sum())) > 1e-12:
+        return False
+    r = _rng(14)
+    q, k, v, dO = (r.standard_normal((1, 1, 5, 3)) for _ in range(4))
+    o, lse = lib.fwd(q, k, v, 0.8, True)
+    if not np.array_equal(o[0, 0, 0], v[0, 0, 0]) or abs(lse[0, 0, 0] - 0.8 * q[0, 0, 0] @ k[0, 0, 0]) > 1e-14:
+        return False
+    h = 1e-6
+    for causal in (False, True):
+        grads = lib.bwd(q, k, v, dO, 0.8, causal)
+        for which in range(3):
+            for idx in np.ndindex(q.shape):
+                plus = [q.copy(), k.copy(), v.copy()]
+                minus = [q.copy(), k.copy(), v.copy()]
+                plus[which][idx] += h
+                minus[which][idx] -= h
+                num = (np.sum(lib.fwd(*plus, 0.8, causal)[0] * dO)
+                       - np.sum(lib.fwd(*minus, 0.8, causal)[0] * dO)) / (2 * h)
+                if abs(num - grads[which][idx]) > 1e-6 * max(1.0, np.abs(grads[which]).max()):
+                    return False
+    return True
+
+
+@pytest.mark.skipif(shutil.which("gcc") is None, reason="needs gcc")
+def test_planted_mistakes_are_caught():
+    """The pins hold for the real oracle, and each plausible slip planted in a
+    copy of its source (a dropped factor, a wrong sign, a transposed operand, an
+    off-by-one mask, a lost term) makes at least one of them fail."""
+    src = open(os.path.join(os.path.dirname(oracle.__file__), "oracle.c")).read()
+    assert _pins_hold(_Lib(oracle.build()))
+    with tempfile.TemporaryDirectory() as tmp:
+        for n, (name, (old, new)) in enumerate(MUTATIONS.items()):
+            assert old in src, name
+            path = os.path.join(tmp, f"mutant{n}.c")
+            with open(path, "w") as f:
+                f.write(src.replace(old, new))
+            so = path[:-2] + ".so"
+            subprocess.check_call(["gcc", "-O1", "-std=c11", "-fPIC", "-shared", "-fopenmp",
+                                   path, "-o", so, "-lm"])
+            assert not _pins_hold(_Lib(so)), name
