@@ -1,0 +1,334 @@
+"""Benchmark: exact attention forward + backward on GB300.
+
+One step = one forward and one backward pass (every kernel of the path) over
+the bf16 B=8 H=32 N=4096 d=128 non-causal workload, inputs resident in HBM.
+The metric is whole-job TFLOP/s with FLOPs counted as 4*B*H*N^2*d for the
+forward and 2.5x that for the backward (halved under a causal mask).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0). Multi-GPU runs come from torchrun, one process
+per GPU; every (batch, head) is independent, so each rank runs its own copy
+of the workload (weak scaling, no collective on the data path).
+
+--impl reference times the fp64 CPU oracle on this machine's host cores on a
+bounded sample of the same workload (whole heads, full N), in the same metric.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd/bwd TFLOP/s at B8 H32 N4096 d128 bf16; % of BF16 tensor peak"
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"bf16_tflops": p["bf16_tflops"], "bf16_tflops_sustained": p.get("bf16_tflops_sustained"),
+                "hbm_gbs": p["hbm_gbs"], "source": "measured"}
+    return {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0,
+            "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def cpu_baseline(w, heads: int):
+    """Oracle fwd+bwd on `heads` whole heads of the workload (full N)."""
+    import torch
+
+    import oracle
+    from exact_attention_97_gb300.inputs import make_qkv_do
+
+    q, k, v, dO = make_qkv_do(1, heads, w.N, w.d, w.seed, torch.bfloat16)
+    f64 = lambda t: t.float().double().numpy()  # noqa: E731
+    q, k, v, dO = f64(q), f64(k), f64(v), f64(dO)
+    oracle.build()
+    t0 = time.perf_counter()
+    oracle.attention_fwd(q, k, v, w.scale, w.causal)
+    oracle.attention_bwd(q, k, v, dO, w.scale, w.causal)
+    dt = time.perf_counter() - t0
+    flops = (w.flops_fwd() + w.flops_bwd()) / (w.B * w.H) * heads
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"{heads} whole heads (full N={w.N}, d={w.d}) of the workload, fwd+bwd, fp64, "
+                      f"{dt:.1f} s wall"}
+
+
+def run_reference(args, w):
+    world, rank, _ = _dist()
+    if rank != 0:
+        return 0
+    import oracle
+    times = []
+    base = None
+    for step in range(args.warmup + args.steps):
+        b = cpu_baseline(w, args.ref_heads)
+        if step >= args.warmup:
+            times.append(b)
+        base = b
+    vals = [b["value"] for b in times]
+    value = statistics.median(vals)
+    flops_step = (w.flops_fwd() + w.flops_bwd()) / (w.B * w.H) * args.ref_heads
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": flops_step / (value * 1e12) * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
+                   "sample_heads_per_step": args.ref_heads},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.num_threads(),
+                         "kind": "oracle", "sample": base["sample"]},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, w):
+    import torch
+    import torch.distributed as dist
+
+    import exact_attention_97_gb300 as fa
+    from exact_attention_97_gb300.inputs import make_qkv_do
+
+    world, rank, local = _dist()
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    fa.load()
+
+    # inputs: seeded host tensors, pinned copies for the end-to-end leg, device copies
+    q_h, k_h, v_h, do_h = (t.pin_memory() for t in make_qkv_do(w.B, w.H, w.N, w.d, w.seed, torch.bfloat16))
+    q, k, v, dO = (t.to(dev) for t in (q_h, k_h, v_h, do_h))
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.N), device=dev, dtype=torch.float32)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    need = fa.fa_bwd_workspace_size(w.B, w.H, w.N, w.d, fa.FA_BF16)
+    ws = torch.empty(need, device=dev, dtype=torch.uint8)
+    stream = torch.cuda.current_stream()
+
+    launches = [0]
+
+    def step():
+        fa.attention_forward(q, k, v, w.scale, w.causal, out=o, lse=lse)
+        n = fa.fa_last_launch_count()
+        fa.attention_backward(q, k, v, o, lse, dO, w.scale, w.causal, workspace=ws, grads=(dq, dk, dv))
+        launches[0] += n + fa.fa_last_launch_count()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if fa.fa_device_status() != 0:
+        raise RuntimeError("kernel pipeline timeout during warm-up")
+
+    # per-kernel events: pair 2s = forward kernel of step s, 2s+1 = backward main pass
+    pairs = 2 * args.steps
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * pairs)]
+    for e in evs:
+        e.record(stream)  # creates the underlying CUDA event
+    handles = (ctypes.c_void_p * (2 * pairs))(*[e.cuda_event for e in evs])
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    sampler = ClockSampler(local)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.3)
+    fa.fa_set_kernel_timing(handles, pairs)
+    launches[0] = 0
+    start.record(stream)
+    for _ in range(args.steps):
+        step()
+    stop.record(stream)
+    torch.cuda.synchronize()
+    fa.fa_set_kernel_timing(None, 0)
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    if fa.fa_device_status() != 0:
+        raise RuntimeError("kernel pipeline timeout in the timed region")
+    ms = start.elapsed_time(stop)
+    fwd_ms = [evs[4 * s].elapsed_time(evs[4 * s + 1]) for s in range(args.steps)]
+    bwd_ms = [evs[4 * s + 2].elapsed_time(evs[4 * s + 3]) for s in range(args.steps)]
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    flops_step = w.flops_fwd() + w.flops_bwd()
+    value = flops_step * world * args.steps / (ms * 1e-3) / 1e12
+    peaks = _peaks()
+    fwd_avg, bwd_avg = statistics.mean(fwd_ms), statistics.mean(bwd_ms)
+    fwd_tf = w.flops_fwd() / (fwd_avg * 1e-3) / 1e12
+    bwd_tf = w.flops_bwd() / (bwd_avg * 1e-3) / 1e12
+    dominant = "bwd_main" if bwd_avg * 1 >= fwd_avg else "fwd"
+    achieved = bwd_tf if dominant == "bwd_main" else fwd_tf
+    roofline = {"bound": "tensor", "kernel": "bwd_main_kernel<128>" if dominant == "bwd_main" else "fwd_bf16_kernel<128>",
+                "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": achieved / peaks["bf16_tflops"], "traffic": args.traffic,
+                "peak_source": peaks["source"] + " burst bf16 (cuBLAS)"}
+
+    # end to end through the public API: pinned host inputs in, results back to pinned host
+    e2e = None
+    if not args.no_e2e:
+        out_h = [torch.empty_like(q_h).pin_memory() for _ in range(4)]
+
+        def e2e_step():
+            qd, kd, vd, dod = (t.to(dev, non_blocking=True) for t in (q_h, k_h, v_h, do_h))
+            od, ld = fa.attention_forward(qd, kd, vd, w.scale, w.causal)
+            g = fa.attention_backward(qd, kd, vd, od, ld, dod, w.scale, w.causal, workspace=ws)
+            for dst, src in zip(out_h, (od, *g)):
+                dst.copy_(src, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        e2e_steps = max(3, min(args.steps, 10))
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if world > 1:
+            dist.barrier()
+        a.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ems = a.elapsed_time(b)
+        if world > 1:
+            t = torch.tensor([ems], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ems = float(t.item())
+        bytes_in = sum(t.numel() * t.element_size() for t in (q_h, k_h, v_h, do_h))
+        bytes_out = sum(t.numel() * t.element_size() for t in out_h)
+        e2e = {"value": flops_step * world * e2e_steps / (ems * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": bytes_in, "d2h_bytes_per_step": bytes_out,
+               "ms_per_step": ems / e2e_steps}
+
+    base = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        base = cpu_baseline(w, args.cpu_heads)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
+                       "inputs": "i.i.d. N(0,1), seeds Q=0 K=1 V=2 dO=3",
+                       "l2": "inputs larger than L2 (each of Q, K, V, dO is "
+                             f"{q.numel() * 2 / 1e6:.0f} MB vs 129 MB L2)",
+                       "parallelism": f"{world} independent replica(s), no collective"},
+            "pct_of_peak": value / (peaks["bf16_tflops"] * world) * 100.0,
+            "fwd": {"ms": fwd_avg, "tflops": fwd_tf, "frac": fwd_tf / peaks["bf16_tflops"]},
+            "bwd_main": {"ms": bwd_avg, "tflops": bwd_tf, "frac": bwd_tf / peaks["bf16_tflops"]},
+            "roofline": roofline,
+            "cpu_baseline": base,
+            "e2e": e2e,
+            "gpu_launches": launches[0],
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=None, help="workload name (default: the headline)")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-heads", type=int, default=8, help="heads in the CPU-baseline sample")
+    ap.add_argument("--ref-heads", type=int, default=2, help="heads per step of --impl reference")
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="DRAM bytes per launch of the dominant kernel from an ncu capture")
+    args = ap.parse_args()
+    from exact_attention_97_gb300.inputs import HEADLINE, WORKLOADS
+    w = WORKLOADS[args.workload or HEADLINE]
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

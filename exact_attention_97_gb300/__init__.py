@@ -1,0 +1,100 @@
+"""Exact scaled dot-product attention for GB300 (sm_103a).
+
+O = softmax(scale * Q K^T) V, computed tile by tile with the online-softmax
+recurrence (never materialising the N x N matrix) and the per-row
+log-sum-exp L saved for a backward pass that recomputes the probabilities.
+
+The work is done by libfa.so (C ABI in include/fa.h). This package is a thin
+binding: ``fa_fwd`` / ``fa_bwd`` / ``fa_fwd_f32`` / ``fa_bwd_f32`` take raw
+device pointers exactly like the C functions, and ``attention_forward`` /
+``attention_backward`` accept torch CUDA tensors, allocate outputs and the
+backward workspace with torch, and pass pointers through. torch supplies
+device memory and streams only.
+"""
+from __future__ import annotations
+
+import math
+
+from ._lib import (FA_BF16, FA_F32, FAError, fa_bwd, fa_bwd_f32, fa_bwd_workspace_size,
+                   fa_device_status, fa_fwd, fa_fwd_f32, fa_last_launch_count,
+                   fa_set_kernel_timing, fa_status_string, lib_path, load)
+
+__all__ = [
+    "FA_BF16", "FA_F32", "FAError", "fa_fwd", "fa_bwd", "fa_fwd_f32", "fa_bwd_f32",
+    "fa_bwd_workspace_size", "fa_status_string", "fa_device_status", "fa_last_launch_count",
+    "fa_set_kernel_timing",
+    "attention_forward", "attention_backward", "lib_path", "load",
+]
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _check(name, t, shape, dtype):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _stream_handle(stream):
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def attention_forward(q, k, v, scale=None, causal=False, out=None, lse=None, stream=None):
+    """(O, L) for [B, H, N, d] CUDA tensors q, k, v (all bf16 or all float32).
+
+    bf16 needs d in {64, 128}; float32 takes 1 <= d <= 128. L is float32
+    [B, H, N], the natural-log log-sum-exp of the scaled scores.
+    """
+    torch = _torch()
+    B, H, N, d = q.shape
+    dt = q.dtype
+    if dt not in (torch.bfloat16, torch.float32):
+        raise ValueError("q must be bfloat16 or float32")
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _check(name, t, (B, H, N, d), dt)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    with torch.cuda.device(q.device):
+        o = torch.empty_like(q) if out is None else out
+        lse = torch.empty((B, H, N), device=q.device, dtype=torch.float32) if lse is None else lse
+        _check("out", o, (B, H, N, d), dt)
+        _check("lse", lse, (B, H, N), torch.float32)
+        fn = fa_fwd if dt == torch.bfloat16 else fa_fwd_f32
+        fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N, d, scale,
+           int(bool(causal)), _stream_handle(stream))
+    return o, lse
+
+
+def attention_backward(q, k, v, o, lse, dO, scale=None, causal=False, workspace=None, stream=None,
+                       grads=None):
+    """(dQ, dK, dV) for upstream gradient dO, given the forward's O and L."""
+    torch = _torch()
+    B, H, N, d = q.shape
+    dt = q.dtype
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dO", dO)):
+        _check(name, t, (B, H, N, d), dt)
+    _check("lse", lse, (B, H, N), torch.float32)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    kind = FA_BF16 if dt == torch.bfloat16 else FA_F32
+    need = fa_bwd_workspace_size(B, H, N, d, kind)
+    with torch.cuda.device(q.device):
+        if workspace is None:
+            workspace = torch.empty(need, device=q.device, dtype=torch.uint8)
+        if workspace.numel() * workspace.element_size() < need:
+            raise ValueError(f"workspace needs {need} bytes")
+        dq, dk, dv = grads if grads is not None else (torch.empty_like(q), torch.empty_like(k),
+                                                      torch.empty_like(v))
+        fn = fa_bwd if kind == FA_BF16 else fa_bwd_f32
+        fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), dO.data_ptr(),
+           dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d, scale, int(bool(causal)),
+           workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    return dq, dk, dv

@@ -1,0 +1,112 @@
+"""ctypes binding of libfa.so: same entry-point names as include/fa.h,
+argument marshalling only. Every computation runs in the library's kernels;
+there is no other code path, and a missing library is an error.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build as _build
+
+_lock = threading.Lock()
+_lib = None
+
+c_int, c_float, c_size_t, c_void_p = ctypes.c_int, ctypes.c_float, ctypes.c_size_t, ctypes.c_void_p
+
+# name -> (restype, argtypes); mirrors include/fa.h
+_SIGNATURES = {
+    "fa_fwd": (c_int, [c_void_p] * 5 + [c_int] * 4 + [c_float, c_int, c_void_p]),
+    "fa_bwd": (c_int, [c_void_p] * 9 + [c_int] * 4 + [c_float, c_int, c_void_p, c_size_t, c_void_p]),
+    "fa_fwd_f32": (c_int, [c_void_p] * 5 + [c_int] * 4 + [c_float, c_int, c_void_p]),
+    "fa_bwd_f32": (c_int, [c_void_p] * 9 + [c_int] * 4 + [c_float, c_int, c_void_p, c_size_t, c_void_p]),
+    "fa_bwd_workspace_size": (c_size_t, [c_int] * 5),
+    "fa_status_string": (ctypes.c_char_p, [c_int]),
+    "fa_last_cuda_error": (c_int, []),
+    "fa_device_status": (c_int, []),
+    "fa_last_launch_count": (c_int, []),
+    "fa_set_kernel_timing": (c_int, [c_void_p, c_int]),
+}
+
+FA_BF16, FA_F32 = 0, 1
+STATUS = {0: "FA_OK", 1: "FA_ERR_NULL", 2: "FA_ERR_SHAPE", 3: "FA_ERR_UNSUPPORTED",
+          4: "FA_ERR_ALIGN", 5: "FA_ERR_WORKSPACE", 6: "FA_ERR_LAUNCH", 7: "FA_ERR_TIMEOUT",
+          8: "FA_ERR_ARCH", 9: "FA_ERR_ARG"}
+
+
+class FAError(RuntimeError):
+    def __init__(self, fn: str, status: int, msg: str, cuda_error: int = 0):
+        super().__init__(f"{fn} returned {STATUS.get(status, status)} ({msg})"
+                         + (f", CUDA error {cuda_error}" if cuda_error else ""))
+        self.status = status
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = True):
+    """Load libfa.so (building it first when asked and nvcc is present)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.LIB
+            if not os.path.exists(path) or (build_if_missing and not _build.up_to_date()):
+                if not build_if_missing:
+                    raise RuntimeError(f"libfa.so not built at {path}")
+                _build.build()
+            lib = ctypes.CDLL(path)
+            for name, (res, args) in _SIGNATURES.items():
+                fn = getattr(lib, name)
+                fn.restype, fn.argtypes = res, args
+            _lib = lib
+    return _lib
+
+
+def _call(name: str, *args) -> int:
+    lib = load()
+    st = getattr(lib, name)(*args)
+    if st != 0:
+        raise FAError(name, st, lib.fa_status_string(st).decode(), lib.fa_last_cuda_error())
+    return st
+
+
+def fa_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, stream):
+    return _call("fa_fwd", q, k, v, o, lse, B, H, N, d, float(scale), int(causal), stream)
+
+
+def fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, scale, causal, workspace, workspace_bytes, stream):
+    return _call("fa_bwd", q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, float(scale), int(causal),
+                 workspace, workspace_bytes, stream)
+
+
+def fa_fwd_f32(q, k, v, o, lse, B, H, N, d, scale, causal, stream):
+    return _call("fa_fwd_f32", q, k, v, o, lse, B, H, N, d, float(scale), int(causal), stream)
+
+
+def fa_bwd_f32(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, scale, causal, workspace, workspace_bytes,
+               stream):
+    return _call("fa_bwd_f32", q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, float(scale), int(causal),
+                 workspace, workspace_bytes, stream)
+
+
+def fa_bwd_workspace_size(B, H, N, d, dtype) -> int:
+    return int(load().fa_bwd_workspace_size(B, H, N, d, dtype))
+
+
+def fa_status_string(status: int) -> str:
+    return load().fa_status_string(status).decode()
+
+
+def fa_device_status() -> int:
+    return int(load().fa_device_status())
+
+
+def fa_last_launch_count() -> int:
+    return int(load().fa_last_launch_count())
+
+
+def fa_set_kernel_timing(events, n_pairs: int) -> int:
+    """events: a ctypes array of 2*n_pairs cudaEvent_t handles (or None)."""
+    return int(load().fa_set_kernel_timing(events, n_pairs))

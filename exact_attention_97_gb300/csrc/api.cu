@@ -1,0 +1,323 @@
+// api.cu -- the exported C ABI (include/fa.h): argument checks, tensor-map
+// construction and kernel launches. Nothing here allocates device memory or
+// synchronises, except fa_device_status, which is documented to.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "../../include/fa.h"
+#include "kernels.h"
+
+namespace {
+
+using namespace fa;
+
+// Kernels record FA_ERR_TIMEOUT here when they give up on a wait.
+__device__ int g_fa_status = 0;
+
+thread_local int t_last_cuda_error = 0;
+thread_local int t_last_launches = 0;
+thread_local void **t_events = nullptr;
+thread_local int t_event_pairs = 0;
+thread_local int t_event_next = 0;
+
+constexpr int kMaxDevices = 64;
+struct DeviceInfo {
+  bool ready = false;
+  int ok_arch = 0;
+  int num_sms = 0;
+  int *status = nullptr;
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mutex;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+std::once_flag g_encode_once;
+
+int record(cudaError_t e) {
+  t_last_cuda_error = static_cast<int>(e);
+  return e == cudaSuccess ? kOk : kErrLaunch;
+}
+
+// Looks up (once per device) whether the current device is sm_103, its SM
+// count and the address of the status word.
+int current_device(DeviceInfo **out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return record(e);
+  if (dev < 0 || dev >= kMaxDevices) return kErrArch;
+  std::lock_guard<std::mutex> lock(g_dev_mutex);
+  DeviceInfo &d = g_dev[dev];
+  if (!d.ready) {
+    int major = 0, minor = 0, sms = 0;
+    if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return record(e);
+    d.ok_arch = (major == 10 && minor == 3);
+    d.num_sms = sms;
+    if (d.ok_arch) {
+      void *p = nullptr;
+      if ((e = cudaGetSymbolAddress(&p, g_fa_status)) != cudaSuccess) return record(e);
+      d.status = static_cast<int *>(p);
+    }
+    d.ready = true;
+  }
+  if (!d.ok_arch) return kErrArch;
+  *out = &d;
+  return kOk;
+}
+
+int get_encoder() {
+  std::call_once(g_encode_once, [] {
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  });
+  return g_encode ? kOk : kErrLaunch;
+}
+
+// 3-D bf16 map over a contiguous [BH][N][d] tensor: dims {d, N, BH}, box
+// {64, 128, 1}, 128-byte swizzle; rows past N (inside a head) read as zero.
+int make_map(CUtensorMap *map, const void *ptr, int BH, int N, int d) {
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                        static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
+                           static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(d) * 2};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    t_last_cuda_error = static_cast<int>(r);
+    return kErrLaunch;
+  }
+  return kOk;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int check_shape(int B, int H, int N, int d, int dmax) {
+  if (B < 1 || H < 1 || N < 1 || d < 1 || d > dmax) return kErrShape;
+  const double elems = static_cast<double>(B) * H * N * d;
+  if (elems >= 1099511627776.0) return kErrShape;  // 2^40
+  if (static_cast<long long>(B) * H > 65535) return kErrUnsupported;  // grid.y limit
+  return kOk;
+}
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Workspace layout.
+//   f32:  D [B*H*N] fp32.
+//   bf16: dQ accumulator [B*H*N*d] fp32, then L*log2(e) and D, each
+//         [B*H][Np] fp32 with Np = 128*ceil(N/128) (padding rows hold +inf / 0).
+struct BwdWorkspace {
+  size_t acc = 0, lp = 0, dp = 0, total = 0;  // byte offsets and size
+};
+
+BwdWorkspace ws_layout(int B, int H, int N, int d, int dtype) {
+  BwdWorkspace w;
+  const size_t rows = static_cast<size_t>(B) * H * N;
+  if (dtype == FA_F32) {
+    w.total = round_up(rows * sizeof(float), 256);
+    return w;
+  }
+  const size_t prow = static_cast<size_t>(B) * H * ((static_cast<size_t>(N) + 127) / 128 * 128);
+  w.acc = 0;
+  w.lp = round_up(rows * d * sizeof(float), 256);
+  w.dp = w.lp + round_up(prow * sizeof(float), 256);
+  w.total = w.dp + round_up(prow * sizeof(float), 256);
+  return w;
+}
+
+size_t ws_bytes(int B, int H, int N, int d, int dtype) {
+  if (check_shape(B, H, N, d, 128) != kOk) return 0;
+  return ws_layout(B, H, N, d, dtype).total;
+}
+
+}  // namespace
+
+namespace fa {
+void timing_begin(cudaStream_t stream) {
+  if (t_events && t_event_next < t_event_pairs)
+    cudaEventRecord(static_cast<cudaEvent_t>(t_events[2 * t_event_next]), stream);
+}
+void timing_end(cudaStream_t stream) {
+  if (t_events && t_event_next < t_event_pairs) {
+    cudaEventRecord(static_cast<cudaEvent_t>(t_events[2 * t_event_next + 1]), stream);
+    ++t_event_next;
+  }
+}
+}  // namespace fa
+
+extern "C" {
+
+int fa_set_kernel_timing(void **events, int n_pairs) {
+  if (n_pairs == -1) return t_event_next;
+  if (n_pairs < 0) return FA_ERR_ARG;
+  t_events = (events && n_pairs > 0) ? events : nullptr;
+  t_event_pairs = t_events ? n_pairs : 0;
+  t_event_next = 0;
+  return FA_OK;
+}
+
+const char *fa_status_string(int status) {
+  switch (status) {
+    case FA_OK: return "ok";
+    case FA_ERR_NULL: return "a required pointer is NULL";
+    case FA_ERR_SHAPE: return "B, H, N or d out of range";
+    case FA_ERR_UNSUPPORTED: return "shape not supported by this build";
+    case FA_ERR_ALIGN: return "pointer not aligned as required";
+    case FA_ERR_WORKSPACE: return "workspace missing or too small";
+    case FA_ERR_LAUNCH: return "CUDA launch or tensor-map call failed";
+    case FA_ERR_TIMEOUT: return "a kernel gave up waiting on a pipeline barrier";
+    case FA_ERR_ARCH: return "current device is not sm_103";
+    case FA_ERR_ARG: return "invalid argument";
+    default: return "unknown status";
+  }
+}
+
+int fa_last_cuda_error(void) { return t_last_cuda_error; }
+int fa_last_launch_count(void) { return t_last_launches; }
+
+size_t fa_bwd_workspace_size(int B, int H, int N, int d, int dtype) {
+  if (dtype != FA_BF16 && dtype != FA_F32) return 0;
+  return ws_bytes(B, H, N, d, dtype);
+}
+
+int fa_device_status(void) {
+  DeviceInfo *dev = nullptr;
+  int st = current_device(&dev);
+  if (st != kOk) return st;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return record(e);
+  int v = 0;
+  if ((e = cudaMemcpy(&v, dev->status, sizeof(int), cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return record(e);
+  const int zero = 0;
+  if ((e = cudaMemcpy(dev->status, &zero, sizeof(int), cudaMemcpyHostToDevice)) != cudaSuccess)
+    return record(e);
+  return v;
+}
+
+int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int N,
+           int d, float scale, int causal, fa_stream_t stream) {
+  if (!q || !k || !v || !o || !lse) return FA_ERR_NULL;
+  int st = check_shape(B, H, N, d, 128);
+  if (st != kOk) return st;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (!isfinite(scale)) return FA_ERR_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
+    return FA_ERR_ALIGN;
+  DeviceInfo *dev = nullptr;
+  if ((st = current_device(&dev)) != kOk) return st;
+  if ((st = get_encoder()) != kOk) return st;
+  CUtensorMap tq, tk, tv;
+  const int BH = B * H;
+  if ((st = make_map(&tq, q, BH, N, d)) != kOk || (st = make_map(&tk, k, BH, N, d)) != kOk ||
+      (st = make_map(&tv, v, BH, N, d)) != kOk)
+    return st;
+  int launches = 0;
+  cudaError_t e = launch_fwd_bf16(tq, tk, tv, o, lse, B, H, N, d, scale, causal ? 1 : 0,
+                                  dev->status, dev->num_sms, reinterpret_cast<cudaStream_t>(stream),
+                                  &launches);
+  if (e != cudaSuccess) return record(e);
+  t_last_launches = launches;
+  return FA_OK;
+}
+
+int fa_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
+           const void *dO, void *dq, void *dk, void *dv, int B, int H, int N, int d, float scale,
+           int causal, void *workspace, size_t workspace_bytes, fa_stream_t stream) {
+  if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return FA_ERR_NULL;
+  int st = check_shape(B, H, N, d, 128);
+  if (st != kOk) return st;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (!isfinite(scale)) return FA_ERR_ARG;
+  const void *ptrs[] = {q, k, v, o, dO, dq, dk, dv};
+  for (const void *p : ptrs)
+    if (!aligned(p, 16)) return FA_ERR_ALIGN;
+  if (!aligned(lse, 4)) return FA_ERR_ALIGN;
+  const size_t need = ws_bytes(B, H, N, d, FA_BF16);
+  if (!workspace || workspace_bytes < need) return FA_ERR_WORKSPACE;
+  if (!aligned(workspace, 256)) return FA_ERR_ALIGN;
+  DeviceInfo *dev = nullptr;
+  if ((st = current_device(&dev)) != kOk) return st;
+  if ((st = get_encoder()) != kOk) return st;
+  CUtensorMap tq, tk, tv, tdo;
+  const int BH = B * H;
+  if ((st = make_map(&tq, q, BH, N, d)) != kOk || (st = make_map(&tk, k, BH, N, d)) != kOk ||
+      (st = make_map(&tv, v, BH, N, d)) != kOk || (st = make_map(&tdo, dO, BH, N, d)) != kOk)
+    return st;
+  const BwdWorkspace w = ws_layout(B, H, N, d, FA_BF16);
+  char *ws = static_cast<char *>(workspace);
+  int launches = 0;
+  cudaError_t e = launch_bwd_bf16(tq, tk, tv, tdo, o, dO, lse, dq, dk, dv,
+                                  reinterpret_cast<float *>(ws + w.acc),
+                                  reinterpret_cast<float *>(ws + w.lp),
+                                  reinterpret_cast<float *>(ws + w.dp), B, H, N, d, scale,
+                                  causal ? 1 : 0, dev->status, dev->num_sms,
+                                  reinterpret_cast<cudaStream_t>(stream), &launches);
+  if (e != cudaSuccess) return record(e);
+  t_last_launches = launches;
+  return FA_OK;
+}
+
+int fa_fwd_f32(const float *q, const float *k, const float *v, float *o, float *lse, int B, int H,
+               int N, int d, float scale, int causal, fa_stream_t stream) {
+  if (!q || !k || !v || !o || !lse) return FA_ERR_NULL;
+  int st = check_shape(B, H, N, d, 128);
+  if (st != kOk) return st;
+  if (!isfinite(scale)) return FA_ERR_ARG;
+  const void *ptrs[] = {q, k, v, o, lse};
+  for (const void *p : ptrs)
+    if (!aligned(p, 4)) return FA_ERR_ALIGN;
+  DeviceInfo *dev = nullptr;
+  if ((st = current_device(&dev)) != kOk) return st;
+  int launches = 0;
+  cudaError_t e = launch_fwd_f32(q, k, v, o, lse, B, H, N, d, scale, causal ? 1 : 0,
+                                 reinterpret_cast<cudaStream_t>(stream), &launches);
+  if (e != cudaSuccess) return record(e);
+  t_last_launches = launches;
+  return FA_OK;
+}
+
+int fa_bwd_f32(const float *q, const float *k, const float *v, const float *o, const float *lse,
+               const float *dO, float *dq, float *dk, float *dv, int B, int H, int N, int d,
+               float scale, int causal, void *workspace, size_t workspace_bytes,
+               fa_stream_t stream) {
+  if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return FA_ERR_NULL;
+  int st = check_shape(B, H, N, d, 128);
+  if (st != kOk) return st;
+  if (!isfinite(scale)) return FA_ERR_ARG;
+  const void *ptrs[] = {q, k, v, o, lse, dO, dq, dk, dv};
+  for (const void *p : ptrs)
+    if (!aligned(p, 4)) return FA_ERR_ALIGN;
+  const size_t need = ws_bytes(B, H, N, d, FA_F32);
+  if (!workspace || workspace_bytes < need) return FA_ERR_WORKSPACE;
+  if (!aligned(workspace, 256)) return FA_ERR_ALIGN;
+  DeviceInfo *dev = nullptr;
+  if ((st = current_device(&dev)) != kOk) return st;
+  int launches = 0;
+  cudaError_t e = launch_bwd_f32(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, scale,
+                                 causal ? 1 : 0, static_cast<float *>(workspace),
+                                 reinterpret_cast<cudaStream_t>(stream), &launches);
+  if (e != cudaSuccess) return record(e);
+  t_last_launches = launches;
+  return FA_OK;
+}
+
+}  // extern "C"

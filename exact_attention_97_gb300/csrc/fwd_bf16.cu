@@ -1,0 +1,331 @@
+// fwd_bf16.cu -- exact attention forward on the sm_103a tensor cores.
+//
+// What it computes (pages): the tiled loop of "Flash Attention 原理与实现",
+// section "Forward 的 Tiling 策略" -- for each block Q_i of query rows, walk
+// the key/value blocks K_j, V_j, form S_ij = Q_i K_j^T, fold it into the
+// running row state and divide by l once at the end -- with the state update
+// of the "research-attention" tutorial, section 02:
+//     m' = max(m, rowmax S),  alpha = exp(m - m'),  p = exp(s - m'),
+//     l' = alpha l + rowsum p, u' = alpha u + p V,   o = u / l,
+// and the saved statistic L = m + ln l of its section 04.
+//
+// GB300 design (one CTA = one 128-row query tile of one (batch, head)):
+//   warp 0      TMA producer: Q once, then K_j and V_j into a ring of kStages
+//               shared-memory stages (128-byte swizzle, 3-D tensor maps so
+//               rows past N read as zero).
+//   warp 1      MMA issuer (one thread): S_j = Q K_j^T into tensor memory
+//               (TMEM), double-buffered so S_{j+1} runs while row statistics
+//               of S_j are computed; then O += P_j V_j with P_j read straight
+//               from TMEM (A operand in TMEM, B = V_j in shared memory).
+//   warp 2      allocates / frees the 512 TMEM columns.
+//   warps 4-7   softmax: thread t owns row t of the tile (= TMEM lane t).
+//               Loads its 128 scores, applies the mask, takes the row max,
+//               writes P = 2^(s*c - m*c) (c = scale*log2 e) back as bf16 over
+//               the S columns, and keeps l. The running max is only moved
+//               when it grows by more than 2^8: any common base leaves u/l
+//               unchanged (tutorial section 02), so the O rescale in TMEM
+//               (ld, multiply, st) is skipped on most tiles. The epilogue
+//               divides by l, stores O as bf16 and L = m*scale + ln l.
+//
+// TMEM columns: S buffer 0 = [0,128), S buffer 1 = [128,256), O = [256,256+d).
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "kernels.h"
+#include "sm103.cuh"
+
+namespace fa {
+namespace {
+
+constexpr int kBlockM = 128;   // query rows per tile (= TMEM lanes)
+constexpr int kBlockN = 128;   // keys per tile
+constexpr int kStages = 3;     // K and V ring depth
+constexpr int kThreads = 256;  // 8 warps
+constexpr float kRescaleLog2 = 8.0f;  // move the running max only past 2^8
+constexpr float kLn2 = 0.69314718055994531f;
+
+template <int D>
+struct FwdSmem {
+  static constexpr int kTileBytes = kBlockN * D * 2;  // one 128 x D bf16 tile
+  static constexpr int kSubBytes = kBlockN * 128;     // one 128 x 64 sub-tile
+  static constexpr int kQ = 0;
+  static constexpr int kK = kQ + kTileBytes;
+  static constexpr int kV = kK + kStages * kTileBytes;
+  static constexpr int kBytes = kV + kStages * kTileBytes;
+  static constexpr int kAlloc = kBytes + 1024;  // slack for 1024-byte alignment
+};
+
+__device__ __forceinline__ void load_tile(uint8_t *dst, const CUtensorMap *map, uint64_t *bar,
+                                          int D, int row, int bh) {
+  for (int x = 0; x < D; x += 64) tma_load_3d(dst + (x / 64) * (kBlockN * 128), map, bar, x, row, bh);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ,
+                    const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, __nv_bfloat16 *__restrict__ o,
+                    float *__restrict__ lse, int N, float scale, float scale_log2, int causal,
+                    int *status) {
+  using L = FwdSmem<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~static_cast<uintptr_t>(1023));
+  __shared__ uint64_t q_full, k_full[kStages], k_empty[kStages], v_full[kStages],
+      v_empty[kStages], s_full[2], p_ready[2], o_done, drain;
+  __shared__ uint32_t tmem_base_s;
+  __shared__ int abort_flag;
+
+  const int warp = warp_id(), lane = lane_id();
+  const int n_qtiles = (N + kBlockM - 1) / kBlockM;
+  // causal: longest rows first so the last wave holds the short tiles
+  const int qtile = causal ? (n_qtiles - 1 - static_cast<int>(blockIdx.x)) : blockIdx.x;
+  const int bh = blockIdx.y;
+  const int n_ktiles_all = (N + kBlockN - 1) / kBlockN;
+  const int n_ktiles = causal ? min(n_ktiles_all, qtile + 1) : n_ktiles_all;
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(&q_full, 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+      mbar_init(&v_full[s], 1);
+      mbar_init(&v_empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&s_full[b], 1);
+      mbar_init(&p_ready[b], 4 * 32);
+    }
+    mbar_init(&o_done, 1);
+    mbar_init(&drain, 1);
+    fence_mbar_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(&tmem_base_s, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_s;
+  const uint32_t tmem_O = tmem + 256;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      mbar_arrive_expect_tx(&q_full, L::kTileBytes);
+      load_tile(smem + L::kQ, &tmQ, &q_full, D, qtile * kBlockM, bh);
+      int issued = 0;
+      for (int j = 0; j < n_ktiles; ++j) {
+        const int st = j % kStages;
+        const uint32_t ph = ((j / kStages) & 1) ^ 1;  // parity of the previous use
+        if (j >= kStages && !mbar_wait(&k_empty[st], ph, &abort_flag)) break;
+        mbar_arrive_expect_tx(&k_full[st], L::kTileBytes);
+        load_tile(smem + L::kK + st * L::kTileBytes, &tmK, &k_full[st], D, j * kBlockN, bh);
+        if (j >= kStages && !mbar_wait(&v_empty[st], ph, &abort_flag)) {
+          ++issued;
+          break;
+        }
+        mbar_arrive_expect_tx(&v_full[st], L::kTileBytes);
+        load_tile(smem + L::kV + st * L::kTileBytes, &tmV, &v_full[st], D, j * kBlockN, bh);
+        ++issued;
+      }
+      // teardown: every issued copy must land before the CTA's memory is released
+      mbar_wait_drain(&q_full, 0);
+      for (int j = max(0, issued - kStages); j < issued; ++j) {
+        mbar_wait_drain(&k_full[j % kStages], (j / kStages) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    // -------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = idesc_bf16(kBlockM, kBlockN, false, false);
+      constexpr uint32_t idesc_o = idesc_bf16(kBlockM, D, false, true);
+      const uint32_t q_addr = smem_u32(smem + L::kQ);
+      bool ok = mbar_wait(&q_full, 0, &abort_flag);
+      auto issue_pv = [&](int jj) -> bool {
+        const int sb = jj & 1, st = jj % kStages;
+        if (!mbar_wait(&p_ready[sb], (jj >> 1) & 1, &abort_flag)) return false;
+        if (!mbar_wait(&v_full[st], (jj / kStages) & 1, &abort_flag)) return false;
+        tc_fence_after();
+        const uint32_t v_addr = smem_u32(smem + L::kV + st * L::kTileBytes);
+#pragma unroll
+        for (int kk = 0; kk < kBlockN / 16; ++kk) {
+          const uint64_t bdesc = sdesc_sw128(v_addr + kk * 2048, L::kSubBytes, 1024);
+          mma_ts(tmem_O, tmem + sb * 128 + kk * 8, bdesc, idesc_o, (jj > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(&v_empty[st]);
+        mma_commit(&o_done);
+        return true;
+      };
+      for (int j = 0; ok && j < n_ktiles; ++j) {
+        const int st = j % kStages, sb = j & 1;
+        if (!mbar_wait(&k_full[st], (j / kStages) & 1, &abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t k_addr = smem_u32(smem + L::kK + st * L::kTileBytes);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk / 4) * L::kSubBytes + (kk % 4) * 32;
+          const uint64_t adesc = sdesc_sw128(q_addr + off, 16, 1024);
+          const uint64_t bdesc = sdesc_sw128(k_addr + off, 16, 1024);
+          mma_ss(tmem + sb * 128, adesc, bdesc, idesc_s, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&s_full[sb]);
+        mma_commit(&k_empty[st]);
+        if (j > 0 && !issue_pv(j - 1)) ok = false;
+      }
+      if (ok) issue_pv(n_ktiles - 1);
+      // teardown: all issued MMAs finish before TMEM is released
+      mma_commit(&drain);
+      mbar_wait_drain(&drain, 0);
+    }
+  } else if (warp >= 4) {
+    // ----------------------------------------------------------------- softmax
+    const int wq = warp - 4;                 // TMEM lane quarter of this warp
+    const int r_local = wq * 32 + lane;      // row within the tile
+    const int row = qtile * kBlockM + r_local;
+    const uint32_t lane_addr = static_cast<uint32_t>(wq * 32) << 16;
+    float m_used = -INFINITY, l_sum = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_ktiles; ++j) {
+      const int sb = j & 1;
+      if (!mbar_wait_warp(&s_full[sb], (j >> 1) & 1, &abort_flag)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float s[kBlockN];
+#pragma unroll
+      for (int ch = 0; ch < kBlockN / 32; ++ch) {
+        uint32_t r[32];
+        tmem_ld32(tmem + lane_addr + sb * 128 + ch * 32, r);
+#pragma unroll
+        for (int t = 0; t < 32; ++t) s[ch * 32 + t] = __uint_as_float(r[t]);
+      }
+      const int key0 = j * kBlockN;
+      int limit = N - key0;                              // keys >= N are masked
+      if (causal) limit = min(limit, row - key0 + 1);    // keys > row are masked
+      if (limit < kBlockN) {
+#pragma unroll
+        for (int t = 0; t < kBlockN; ++t)
+          if (t >= limit) s[t] = -INFINITY;
+      }
+      float mx = s[0];
+#pragma unroll
+      for (int t = 1; t < kBlockN; ++t) mx = fmaxf(mx, s[t]);
+      if (j == 0) {
+        m_used = mx;
+      } else {
+        const bool need = (mx - m_used) * scale_log2 > kRescaleLog2;
+        if (__any_sync(0xffffffffu, need)) {
+          // O must hold P_{j-1} V_{j-1} before it is rescaled
+          if (!mbar_wait_warp(&o_done, (j - 1) & 1, &abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const float alpha = need ? ex2_approx((m_used - mx) * scale_log2) : 1.f;
+          if (need) {
+            l_sum *= alpha;
+            m_used = mx;
+          }
+#pragma unroll 1
+          for (int ch = 0; ch < D / 32; ++ch) {
+            uint32_t r[32];
+            tmem_ld32(tmem_O + lane_addr + ch * 32, r);
+#pragma unroll
+            for (int t = 0; t < 32; ++t) r[t] = __float_as_uint(__uint_as_float(r[t]) * alpha);
+            tmem_st32(tmem_O + lane_addr + ch * 32, r);
+          }
+        }
+      }
+      const float neg = -m_used * scale_log2;
+      float rs = 0.f;
+#pragma unroll
+      for (int ch = 0; ch < kBlockN / 32; ++ch) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int t = 0; t < 16; ++t) {
+          const float p0 = ex2_approx(fmaf(s[ch * 32 + 2 * t], scale_log2, neg));
+          const float p1 = ex2_approx(fmaf(s[ch * 32 + 2 * t + 1], scale_log2, neg));
+          rs += p0 + p1;
+          pk[t] = pack_bf16x2(p0, p1);
+        }
+        tmem_st16(tmem + lane_addr + sb * 128 + ch * 16, pk);
+      }
+      l_sum += rs;
+      tc_fence_before();
+      mbar_arrive(&p_ready[sb]);
+    }
+    // ---------------------------------------------------------------- epilogue
+    if (ok && mbar_wait_warp(&o_done, (n_ktiles - 1) & 1, &abort_flag)) {
+      tc_fence_after();
+      const float inv_l = 1.f / l_sum;
+      const bool store = row < N;
+      __nv_bfloat16 *orow = o + (static_cast<size_t>(bh) * N + row) * D;
+#pragma unroll 1
+      for (int ch = 0; ch < D / 32; ++ch) {
+        uint32_t r[32];
+        tmem_ld32(tmem_O + lane_addr + ch * 32, r);
+        uint32_t pk[16];
+#pragma unroll
+        for (int t = 0; t < 16; ++t)
+          pk[t] = pack_bf16x2(__uint_as_float(r[2 * t]) * inv_l, __uint_as_float(r[2 * t + 1]) * inv_l);
+        if (store) {
+          uint4 *dst = reinterpret_cast<uint4 *>(orow + ch * 32);
+#pragma unroll
+          for (int t = 0; t < 4; ++t)
+            dst[t] = make_uint4(pk[4 * t], pk[4 * t + 1], pk[4 * t + 2], pk[4 * t + 3]);
+        }
+      }
+      if (store) lse[static_cast<size_t>(bh) * N + row] = (m_used * scale_log2 + log2f(l_sum)) * kLn2;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+  if (threadIdx.x == 0 && abort_flag) atomicExch(status, kErrTimeout);
+}
+
+template <int D>
+cudaError_t launch(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtensorMap &tmV, void *o,
+                   float *lse, int B, int H, int N, float scale, int causal, int *status,
+                   cudaStream_t stream) {
+  using L = FwdSmem<D>;
+  auto kern = fwd_bf16_kernel<D>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+  if (e != cudaSuccess) return e;
+  dim3 grid((N + kBlockM - 1) / kBlockM, B * H);
+  timing_begin(stream);
+  kern<<<grid, kThreads, L::kAlloc, stream>>>(tmQ, tmK, tmV, static_cast<__nv_bfloat16 *>(o), lse,
+                                               N, scale, scale * 1.4426950408889634f, causal,
+                                               status);
+  timing_end(stream);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_bf16(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtensorMap &tmV,
+                            void *o, float *lse, int B, int H, int N, int d, float scale,
+                            int causal, int *status, int num_sms, cudaStream_t stream,
+                            int *launches) {
+  (void)num_sms;
+  *launches += 1;
+  if (d == 64) return launch<64>(tmQ, tmK, tmV, o, lse, B, H, N, scale, causal, status, stream);
+  return launch<128>(tmQ, tmK, tmV, o, lse, B, H, N, scale, causal, status, stream);
+}
+
+}  // namespace fa

@@ -1,0 +1,55 @@
+// kernels.h -- internal launchers behind the C ABI (not exported).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace fa {
+
+// Error codes shared with include/fa.h (kept numerically identical).
+enum : int {
+  kOk = 0,
+  kErrNull = 1,
+  kErrShape = 2,
+  kErrUnsupported = 3,
+  kErrAlign = 4,
+  kErrWorkspace = 5,
+  kErrLaunch = 6,
+  kErrTimeout = 7,
+  kErrArch = 8,
+  kErrArg = 9
+};
+
+// Benchmark timing hook: records the next free event pair (if any) around a
+// main kernel. `begin` records the first event, `end` the second and advances.
+void timing_begin(cudaStream_t stream);
+void timing_end(cudaStream_t stream);
+
+cudaError_t launch_fwd_f32(const float *q, const float *k, const float *v, float *o, float *lse,
+                           int B, int H, int N, int d, float scale, int causal,
+                           cudaStream_t stream, int *launches);
+
+cudaError_t launch_bwd_f32(const float *q, const float *k, const float *v, const float *o,
+                           const float *lse, const float *dO, float *dq, float *dk, float *dv,
+                           int B, int H, int N, int d, float scale, int causal, float *D,
+                           cudaStream_t stream, int *launches);
+
+// bf16 tensor-core forward. tmQ/tmK/tmV are 3-D tensor maps {d, N, B*H} with
+// a {64, 128, 1} box and 128-byte swizzle.
+cudaError_t launch_fwd_bf16(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtensorMap &tmV,
+                            void *o, float *lse, int B, int H, int N, int d, float scale,
+                            int causal, int *status, int num_sms, cudaStream_t stream,
+                            int *launches);
+
+// bf16 tensor-core backward (three kernels). dq_acc is [B*H*N*d] fp32; Lp and
+// Dp are [B*H][Np] fp32 with Np = 128*ceil(N/128); all three live in the
+// caller's workspace.
+cudaError_t launch_bwd_bf16(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtensorMap &tmV,
+                            const CUtensorMap &tmdO, const void *o, const void *dO,
+                            const float *lse, void *dq, void *dk, void *dv, float *dq_acc,
+                            float *Lp, float *Dp, int B, int H, int N, int d, float scale,
+                            int causal, int *status, int num_sms, cudaStream_t stream,
+                            int *launches);
+
+}  // namespace fa

@@ -1,0 +1,157 @@
+/*
+ * fa.h -- C ABI of the exact-attention library (libfa.so), GB300 / sm_103a.
+ *
+ * The library computes exact scaled dot-product attention
+ *     O = softmax(scale * Q K^T) V
+ * tile by tile with the online-softmax recurrence, never materialising the
+ * N x N score or probability matrix, and saves the per-row log-sum-exp
+ *     L_i = m_i + ln l_i
+ * for the backward pass, which recomputes the probabilities from Q, K and L.
+ *
+ * Sources of each operation (page title and section):
+ *   - problem statement, S = QK^T/sqrt(d), P = softmax(S), O = PV:
+ *     "research-attention" tutorial, section 01 equations;
+ *   - running state (m, l, u) and its merge with alpha = exp(m - m'):
+ *     same tutorial, section 02;
+ *   - saved statistic L = m + log(l) and rebuilding P = exp(s - L):
+ *     same tutorial, section 04;
+ *   - tiled forward loop and the final division O_i / l_i:
+ *     "Flash Attention 原理与实现", section "Forward 的 Tiling 策略";
+ *   - backward by recomputation, dV = P^T dO, dP = dO V^T, dS from the
+ *     softmax gradient, dQ = dS K, dK = dS^T Q, with cross-block accumulation
+ *     of dQ by atomic adds: same blog, section "Backward 的 Tiling 策略" and
+ *     item 3 of "实际实现中的注意事项".
+ *
+ * Conventions shared by every entry point
+ *   Layout     Q, K, V, O, dO, dQ, dK, dV are contiguous [B][H][N][d] arrays
+ *              of the entry point's element type (bf16 for fa_fwd/fa_bwd,
+ *              float for the _f32 twins); lse is a contiguous [B][H][N] float
+ *              array holding the natural-log log-sum-exp of the scaled scores.
+ *              Q and K/V share the sequence length N.
+ *   Mask       causal != 0 lets query i see keys j <= i; causal == 0 lets
+ *              every query see all N keys.
+ *   Scale      any finite float; callers usually pass 1/sqrt(d). dQ and dK
+ *              are the true derivatives and therefore carry the factor scale.
+ *   Memory     every pointer is a DEVICE pointer owned by the caller. The
+ *              library never allocates, frees or synchronises; all work is
+ *              enqueued on `stream` (0 = legacy default stream) and returns
+ *              immediately.
+ *   Errors     argument errors return a non-zero fa_status and launch
+ *              nothing. FA_ERR_LAUNCH reports a CUDA launch error (the CUDA
+ *              error is left for cudaGetLastError-style inspection via
+ *              fa_last_cuda_error). A kernel that gives up on an internal
+ *              wait (it never traps) records FA_ERR_TIMEOUT in a device
+ *              status word read by fa_device_status.
+ *   Supported  bf16: d in {64, 128}, N >= 1 (ragged tails are masked),
+ *              every pointer 16-byte aligned.
+ *              f32: 1 <= d <= 128, N >= 1, every pointer 4-byte aligned.
+ *              B, H >= 1; B*H*N*d must be below 2^40 elements.
+ */
+#ifndef FA_H
+#define FA_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t / CUstream. */
+typedef struct CUstream_st *fa_stream_t;
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_NULL = 1,        /* a required pointer is NULL */
+  FA_ERR_SHAPE = 2,       /* B, H, N or d out of range, or sizes overflow */
+  FA_ERR_UNSUPPORTED = 3, /* valid shape this build has no kernel for */
+  FA_ERR_ALIGN = 4,       /* pointer not aligned as required */
+  FA_ERR_WORKSPACE = 5,   /* workspace NULL or smaller than fa_bwd_workspace_size */
+  FA_ERR_LAUNCH = 6,      /* a CUDA launch or tensor-map call failed */
+  FA_ERR_TIMEOUT = 7,     /* a kernel gave up waiting on a pipeline barrier */
+  FA_ERR_ARCH = 8,        /* current device is not sm_103 */
+  FA_ERR_ARG = 9          /* other invalid argument (non-finite scale, dtype) */
+} fa_status;
+
+typedef enum { FA_BF16 = 0, FA_F32 = 1 } fa_dtype;
+
+/*
+ * Forward, bf16 in / bf16 out.
+ *   q, k, v  [B][H][N][d] bf16, read only.
+ *   o        [B][H][N][d] bf16, written: O = softmax(scale*QK^T) V.
+ *   lse      [B][H][N] float, written: L_i = ln sum_j exp(scale q_i.k_j).
+ * Arithmetic: bf16 operands, fp32 accumulation; probabilities are rounded to
+ * bf16 before the P.V product.
+ */
+int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+           int B, int H, int N, int d, float scale, int causal,
+           fa_stream_t stream);
+
+/*
+ * Backward, bf16 in / bf16 out, for upstream gradient dO.
+ *   q, k, v, o, dO   [B][H][N][d] bf16, read only (o as written by fa_fwd).
+ *   lse              [B][H][N] float from fa_fwd, read only.
+ *   dq, dk, dv       [B][H][N][d] bf16, written.
+ *   workspace        device scratch of at least
+ *                    fa_bwd_workspace_size(B, H, N, d, FA_BF16) bytes, 256-byte
+ *                    aligned, owned by the caller; holds the fp32 dQ
+ *                    accumulator and the row terms D_i = sum_c dO_ic O_ic.
+ *                    Its contents on entry are ignored.
+ * Three kernels run on `stream`: D_i and zeroing of the accumulator, the main
+ * pass (one CTA per key block, dQ added with fp32 atomics), and the dQ
+ * conversion. Atomic accumulation makes dQ's rounding order vary run to run.
+ */
+int fa_bwd(const void *q, const void *k, const void *v, const void *o,
+           const float *lse, const void *dO, void *dq, void *dk, void *dv,
+           int B, int H, int N, int d, float scale, int causal,
+           void *workspace, size_t workspace_bytes, fa_stream_t stream);
+
+/* Forward with float tensors (all fp32 arithmetic, exact expf). Same
+ * arguments and layout as fa_fwd with float element type. */
+int fa_fwd_f32(const float *q, const float *k, const float *v, float *o,
+               float *lse, int B, int H, int N, int d, float scale, int causal,
+               fa_stream_t stream);
+
+/* Backward with float tensors. dk and dv are accumulated with fp32 atomics
+ * after being cleared on `stream`. workspace as for fa_bwd (dtype FA_F32). */
+int fa_bwd_f32(const float *q, const float *k, const float *v, const float *o,
+               const float *lse, const float *dO, float *dq, float *dk,
+               float *dv, int B, int H, int N, int d, float scale, int causal,
+               void *workspace, size_t workspace_bytes, fa_stream_t stream);
+
+/* Bytes of workspace fa_bwd / fa_bwd_f32 need for this shape (0 on invalid
+ * shape). dtype is an fa_dtype. */
+size_t fa_bwd_workspace_size(int B, int H, int N, int d, int dtype);
+
+/* Static description of a status code; never NULL. */
+const char *fa_status_string(int status);
+
+/* The cudaError_t of the last failed CUDA call made by this library on the
+ * calling host thread (0 if none). */
+int fa_last_cuda_error(void);
+
+/* Reads and clears the device status word that kernels set when they give up
+ * on a wait (FA_OK or FA_ERR_TIMEOUT). Synchronises the current device. */
+int fa_device_status(void);
+
+/* Number of kernels the most recent successful fa_* call on this host thread
+ * enqueued. */
+int fa_last_launch_count(void);
+
+/*
+ * Per-kernel timing for benchmarks (no counterpart on the pages; it only
+ * measures). `events` holds 2*n_pairs cudaEvent_t handles created by the
+ * caller with timing enabled. After this call, each fa_fwd / fa_bwd on this
+ * host thread records events[2i] on its stream just before its main kernel
+ * (the forward kernel, or the backward's main pass) and events[2i+1] just
+ * after it, for i = 0, 1, ... up to n_pairs - 1; later calls record nothing.
+ * Pass NULL / 0 to switch it off. Returns FA_ERR_ARG for n_pairs < 0.
+ * Returns the number of pairs used so far when called with n_pairs == -1
+ * (events ignored).
+ */
+int fa_set_kernel_timing(void **events, int n_pairs);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H */

@@ -116,59 +116,80 @@ void oracle_probs(const double *q, const double *k, int N, int d, double scale,
   free(vz);
 }
 
-/* Backward of one head: q,k,v,dO are that head's [N][d] blocks. dk, dv are
- * accumulated into (caller zeroes them); dq rows are written. Row-at-a-time
- * with O(N) scratch. */
-static void head_backward(const double *q, const double *k, const double *v,
-                          const double *dO, double *dq, double *dk, double *dv,
-                          int N, int d, double scale, int causal, double *s,
-                          double *p, double *o) {
-  for (int i = 0; i < N; ++i) {
-    const double *qi = q + (size_t)i * d;
-    const double *doi = dO + (size_t)i * d;
-    const int nk = visible_keys(i, N, causal);
-    row_forward(qi, k, v, nk, d, scale, s, p, o);
-    const double Di = dot(doi, o, d);
-    double *dqi = dq + (size_t)i * d;
-    for (int c = 0; c < d; ++c) dqi[c] = 0.0;
-    for (int j = 0; j < nk; ++j) {
-      const double *kj = k + (size_t)j * d;
-      const double dPij = dot(doi, v + (size_t)j * d, d);
-      const double dSij = p[j] * (dPij - Di);
-      double *dkj = dk + (size_t)j * d;
-      double *dvj = dv + (size_t)j * d;
-      for (int c = 0; c < d; ++c) {
-        dqi[c] += scale * dSij * kj[c];
-        dkj[c] += scale * dSij * qi[c];
-        dvj[c] += p[j] * doi[c];
-      }
-    }
-  }
-}
-
-/* Backward over all heads. Outputs dq, dk, dv are overwritten. */
+/* Backward over all heads. Outputs dq, dk, dv are overwritten.
+ * Heads are processed one after another; inside a head the query rows are
+ * split statically over threads. Each thread runs its rows forward in full
+ * (S row, P row, O row, D_i), writes dQ_i, and adds its rows' terms of dK and
+ * dV into private [N][d] sums, which are then added together in thread order
+ * (so the result does not depend on scheduling). */
 void oracle_bwd(const double *q, const double *k, const double *v,
                 const double *dO, double *dq, double *dk, double *dv, int B,
                 int H, int N, int d, double scale, int causal) {
   const int64_t heads = (int64_t)B * H;
   const size_t hs = (size_t)N * d;
-#pragma omp parallel
-  {
-    double *s = (double *)malloc(sizeof(double) * (size_t)N);
-    double *p = (double *)malloc(sizeof(double) * (size_t)N);
-    double *o = (double *)malloc(sizeof(double) * (size_t)d);
-#pragma omp for schedule(dynamic, 1)
-    for (int64_t bh = 0; bh < heads; ++bh) {
-      const size_t off = (size_t)bh * hs;
-      memset(dk + off, 0, sizeof(double) * hs);
-      memset(dv + off, 0, sizeof(double) * hs);
-      head_backward(q + off, k + off, v + off, dO + off, dq + off, dk + off,
-                    dv + off, N, d, scale, causal, s, p, o);
+  int nthr = 1;
+#ifdef _OPENMP
+  nthr = omp_get_max_threads();
+#endif
+  double *part = (double *)malloc(sizeof(double) * 2 * hs * (size_t)nthr);
+  for (int64_t bh = 0; bh < heads; ++bh) {
+    const size_t off = (size_t)bh * hs;
+    const double *qh = q + off, *kh = k + off, *vh = v + off, *doh = dO + off;
+    double *dqh = dq + off;
+    int used = 1;
+#pragma omp parallel num_threads(nthr)
+    {
+      int t = 0;
+#ifdef _OPENMP
+      t = omp_get_thread_num();
+#pragma omp single
+      used = omp_get_num_threads();
+#endif
+      double *pk = part + (size_t)t * 2 * hs;
+      double *pv = pk + hs;
+      memset(pk, 0, sizeof(double) * 2 * hs);
+      double *s = (double *)malloc(sizeof(double) * (size_t)N);
+      double *p = (double *)malloc(sizeof(double) * (size_t)N);
+      double *o = (double *)malloc(sizeof(double) * (size_t)d);
+#pragma omp for schedule(static)
+      for (int i = 0; i < N; ++i) {
+        const double *qi = qh + (size_t)i * d;
+        const double *doi = doh + (size_t)i * d;
+        const int nk = visible_keys(i, N, causal);
+        row_forward(qi, kh, vh, nk, d, scale, s, p, o);
+        const double Di = dot(doi, o, d);
+        double *dqi = dqh + (size_t)i * d;
+        for (int c = 0; c < d; ++c) dqi[c] = 0.0;
+        for (int j = 0; j < nk; ++j) {
+          const double *kj = kh + (size_t)j * d;
+          const double dPij = dot(doi, vh + (size_t)j * d, d);
+          const double dSij = p[j] * (dPij - Di);
+          double *dkj = pk + (size_t)j * d;
+          double *dvj = pv + (size_t)j * d;
+          for (int c = 0; c < d; ++c) {
+            dqi[c] += scale * dSij * kj[c];
+            dkj[c] += scale * dSij * qi[c];
+            dvj[c] += p[j] * doi[c];
+          }
+        }
+      }
+      free(s);
+      free(p);
+      free(o);
     }
-    free(s);
-    free(p);
-    free(o);
+    double *dkh = dk + off, *dvh = dv + off;
+    memset(dkh, 0, sizeof(double) * hs);
+    memset(dvh, 0, sizeof(double) * hs);
+    for (int t = 0; t < used; ++t) {
+      const double *pk = part + (size_t)t * 2 * hs;
+      const double *pv = pk + hs;
+      for (size_t x = 0; x < hs; ++x) {
+        dkh[x] += pk[x];
+        dvh[x] += pv[x];
+      }
+    }
   }
+  free(part);
 }
 
 /* Sampled query rows of one head: O_i, L_i and dQ_i for rows[0..nrows).

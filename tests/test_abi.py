@@ -1,0 +1,136 @@
+"""Host-side checks of the C ABI, no GPU needed: the library builds, loads and
+exports every function include/fa.h declares; the pure host functions answer;
+argument errors come back as status codes before any device work."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import exact_attention_97_gb300 as fa
+from exact_attention_97_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fa.h")
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return _lib.load()
+
+
+def test_header_declares_the_entry_points():
+    names = _declared()
+    for n in ["fa_fwd", "fa_bwd", "fa_fwd_f32", "fa_bwd_f32", "fa_bwd_workspace_size",
+              "fa_status_string"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", _lib.lib_path()], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (fa_[a-z0-9_]+)", out))
+    for name in _declared():
+        assert name in exported, name
+        assert getattr(lib, name) is not None
+    assert set(_declared()) <= set(_lib._SIGNATURES)
+
+
+def test_status_strings(lib):
+    for code in range(10):
+        s = fa.fa_status_string(code)
+        assert s and s != "unknown status"
+    assert fa.fa_status_string(1234) == "unknown status"
+
+
+def test_workspace_size_layout():
+    # bf16: dQ accumulator (B*H*N*d fp32), then padded L and D rows (B*H*ceil(N/128)*128 each)
+    def r256(x):
+        return (x + 255) // 256 * 256
+    for B, H, N, d in [(1, 1, 1, 64), (2, 3, 300, 128), (8, 32, 4096, 128), (1, 32, 65536, 128)]:
+        prow = B * H * ((N + 127) // 128 * 128)
+        want = r256(B * H * N * d * 4) + 2 * r256(prow * 4)
+        assert fa.fa_bwd_workspace_size(B, H, N, d, fa.FA_BF16) == want
+        assert fa.fa_bwd_workspace_size(B, H, N, d, fa.FA_F32) == r256(B * H * N * 4)
+    assert fa.fa_bwd_workspace_size(0, 1, 1, 64, fa.FA_BF16) == 0
+    assert fa.fa_bwd_workspace_size(1, 1, 1, 129, fa.FA_BF16) == 0
+    assert fa.fa_bwd_workspace_size(1, 1, 1, 64, 7) == 0
+
+
+P = 0x10000  # a fake, 16-byte aligned "device pointer": never dereferenced, validation fails first
+
+
+def _fwd(lib, q=P, k=P, v=P, o=P, lse=P, B=1, H=1, N=128, d=64, scale=0.125, causal=0):
+    return lib.fa_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, None)
+
+
+def _bwd(lib, ws=P, ws_bytes=1 << 40, B=1, H=1, N=128, d=64, scale=0.125, ptr=P, **kw):
+    ptrs = [kw.get(n, ptr) for n in ("q", "k", "v", "o", "lse", "dO", "dq", "dk", "dv")]
+    return lib.fa_bwd(*ptrs, B, H, N, d, scale, 0, ws, ws_bytes, None)
+
+
+def test_fwd_argument_errors(lib):
+    assert _fwd(lib, q=None) == 1
+    assert _fwd(lib, lse=None) == 1
+    assert _fwd(lib, N=0) == 2
+    assert _fwd(lib, B=-1) == 2
+    assert _fwd(lib, d=0) == 2
+    assert _fwd(lib, d=256) == 2
+    assert _fwd(lib, d=96) == 3          # valid head size without a bf16 kernel
+    assert _fwd(lib, B=300, H=300) == 3  # more than 65535 heads
+    assert _fwd(lib, N=1 << 30, B=4, H=4, d=128) == 2  # 2^40 elements
+    assert _fwd(lib, q=P + 8) == 4       # TMA needs 16-byte aligned bases
+    assert _fwd(lib, lse=P + 2) == 4
+    assert _fwd(lib, scale=float("nan")) == 9
+    assert _fwd(lib, scale=float("inf")) == 9
+
+
+def test_bwd_argument_errors(lib):
+    assert _bwd(lib, dk=None) == 1
+    assert _bwd(lib, N=-3) == 2
+    assert _bwd(lib, d=80) == 3
+    assert _bwd(lib, dv=P + 4) == 4
+    assert _bwd(lib, ws=None) == 5
+    need = fa.fa_bwd_workspace_size(1, 1, 128, 64, fa.FA_BF16)
+    assert _bwd(lib, ws_bytes=need - 1) == 5
+    assert _bwd(lib, ws=P + 16, ws_bytes=need) == 4  # workspace must be 256-byte aligned
+    assert _bwd(lib, scale=float("-inf")) == 9
+
+
+def test_f32_argument_errors(lib):
+    args = [P] * 5
+    assert lib.fa_fwd_f32(None, *args[1:], 1, 1, 4, 2, 1.0, 0, None) == 1
+    assert lib.fa_fwd_f32(*args, 1, 1, 4, 129, 1.0, 0, None) == 2
+    assert lib.fa_fwd_f32(P + 2, *args[1:], 1, 1, 4, 2, 1.0, 0, None) == 4
+    ptrs = [P] * 9
+    assert lib.fa_bwd_f32(*ptrs, 1, 1, 4, 2, 1.0, 0, None, 0, None) == 5
+
+
+def test_no_cpu_fallback_in_the_binding():
+    """The binding only marshals arguments: it never imports the oracle or
+    computes attention itself."""
+    import ast
+    bad_calls = {"softmax", "matmul", "einsum", "bmm", "mm", "scaled_dot_product_attention", "exp"}
+    pkg = os.path.join(ROOT, "exact_attention_97_gb300")
+    for fn in os.listdir(pkg):
+        if not fn.endswith(".py"):
+            continue
+        tree = ast.parse(open(os.path.join(pkg, fn)).read())
+        for node in ast.walk(tree):
+            if isinstance(node, ast.Import):
+                assert not any(a.name.split(".")[0] == "oracle" for a in node.names), fn
+            if isinstance(node, ast.ImportFrom):
+                assert (node.module or "").split(".")[0] != "oracle", fn
+            if isinstance(node, ast.Call):
+                f = node.func
+                name = f.attr if isinstance(f, ast.Attribute) else getattr(f, "id", "")
+                assert name not in bad_calls, (fn, name)
+            if isinstance(node, ast.BinOp):
+                assert not isinstance(node.op, ast.MatMult), fn

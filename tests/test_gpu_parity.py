@@ -1,0 +1,218 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle on the
+same seeded inputs, element by element.
+
+Small cases compare every element of O, L, dQ, dK and dV with the full oracle.
+At the full workload sizes the oracle checks whole sampled heads plus sampled
+query rows (O, L, dQ) and key rows (dK, dV); the causal N=65536 case checks
+sampled rows and, over every key, the sum rules that hold at any size.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from exact_attention_97_gb300.inputs import WORKLOADS, make_qkv_do, sample_indices
+
+from parity import check, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _np(t):
+    return t.float().double().numpy()
+
+
+def _full_ref(q, k, v, dO, scale, causal):
+    o, lse = oracle.attention_fwd(q, k, v, scale, causal)
+    dq, dk, dv = oracle.attention_bwd(q, k, v, dO, scale, causal)
+    return {"o": o, "lse": lse, "dq": dq, "dk": dk, "dv": dv}
+
+
+def _as_dict(res):
+    return dict(zip(("o", "lse", "dq", "dk", "dv"), res))
+
+
+# ------------------------------------------------------------ worked examples (fp32 path)
+
+def test_tutorial_row_on_gpu():
+    g = json.load(open(os.path.join(GOLDEN, "tutorial_single_row.json")))
+    s = torch.tensor(g["scores"], dtype=torch.float32)
+    q = torch.tensor([[1.0, 0.0]] * 4).view(1, 1, 4, 2)
+    k = torch.stack([s, torch.zeros(4)], dim=1).view(1, 1, 4, 2)
+    v = torch.tensor(g["values"]).view(1, 1, 4, 2)
+    dO = torch.ones_like(v)
+    got = _as_dict(run_gpu(q, k, v, dO, 1.0, False))
+    check("tutorial_row_f32", "f32", got, _full_ref(_np(q), _np(k), _np(v), _np(dO), 1.0, False))
+    for i in range(4):
+        assert np.max(np.abs(got["o"][0, 0, i] - g["printed_output"])) <= 5e-7 + 1e-6
+
+
+def test_llama_notes_example_on_gpu():
+    g = json.load(open(os.path.join(GOLDEN, "llama_notes_four_tokens.json")))
+    X = torch.tensor(g["X"], dtype=torch.float32).view(1, 1, 4, 2)
+    scale = 1.0 / math.sqrt(2.0)
+    dO = torch.tensor([[1.0, -1.0], [0.5, 2.0], [-1.0, 0.0], [0.25, 0.25]]).view(1, 1, 4, 2)
+    for causal in (False, True):
+        got = _as_dict(run_gpu(X, X, X, dO, scale, causal))
+        check(f"llama_notes_f32_causal{int(causal)}", "f32", got,
+              _full_ref(_np(X), _np(X), _np(X), _np(dO), scale, causal))
+    got = _as_dict(run_gpu(X, X, X, dO, scale, False))
+    assert np.max(np.abs(got["o"][0, 0, 0] - g["output_token0"])) <= g["tol_outputs"]
+    assert np.max(np.abs(got["o"][0, 0, 1] - g["output_token1"])) <= g["tol_outputs"]
+    assert abs(math.exp(got["lse"][0, 0, 0]) - g["denominator_row0"]) <= g["tol_sums"]
+
+
+# ------------------------------------------------------------ fp32 path
+
+def test_f32_B1_H2_N256_d64():
+    w = WORKLOADS["f32_B1_H2_N256_d64"]
+    q, k, v, dO = make_qkv_do(w.B, w.H, w.N, w.d, w.seed, torch.float32)
+    got = _as_dict(run_gpu(q, k, v, dO, w.scale, w.causal))
+    check(w.name, "f32", got, _full_ref(_np(q), _np(k), _np(v), _np(dO), w.scale, w.causal))
+
+
+@pytest.mark.parametrize("d", [1, 3, 17, 64, 100, 128])
+@pytest.mark.parametrize("N", [1, 5, 33, 130])
+@pytest.mark.parametrize("causal", [False, True])
+def test_f32_ragged(d, N, causal):
+    q, k, v, dO = make_qkv_do(2, 1, N, d, seed=7 * d + N, dtype=torch.float32)
+    got = _as_dict(run_gpu(q, k, v, dO, 1.0 / math.sqrt(d), causal))
+    check(f"f32_ragged_N{N}_d{d}_c{int(causal)}", "f32", got,
+          _full_ref(_np(q), _np(k), _np(v), _np(dO), 1.0 / math.sqrt(d), causal))
+
+
+# ------------------------------------------------------------ bf16 tensor-core path, full oracle
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("N", [1, 4, 127, 128, 129, 300])
+@pytest.mark.parametrize("causal", [False, True])
+def test_bf16_small_and_ragged(d, N, causal):
+    q, k, v, dO = make_qkv_do(1, 2, N, d, seed=1000 + N + d, dtype=torch.bfloat16)
+    scale = 1.0 / math.sqrt(d)
+    got = _as_dict(run_gpu(q, k, v, dO, scale, causal))
+    check(f"bf16_small_N{N}_d{d}_c{int(causal)}", "bf16", got,
+          _full_ref(_np(q), _np(k), _np(v), _np(dO), scale, causal))
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_bf16_scale_and_large_scores(d):
+    """Scores far from the unit range (the running max moves by many 2^8
+    steps): a large scale and queries scaled up."""
+    q, k, v, dO = make_qkv_do(1, 2, 700, d, seed=55, dtype=torch.float32)
+    q = (q * 4).to(torch.bfloat16)
+    k, v, dO = (x.to(torch.bfloat16) for x in (k, v, dO))
+    for causal in (False, True):
+        got = _as_dict(run_gpu(q, k, v, dO, 0.5, causal))
+        check(f"bf16_large_scores_d{d}_c{int(causal)}", "bf16", got,
+              _full_ref(_np(q), _np(k), _np(v), _np(dO), 0.5, causal))
+
+
+def test_bf16_causal_B1_H8_N1024_d64():
+    w = WORKLOADS["bf16_causal_B1_H8_N1024_d64"]
+    q, k, v, dO = make_qkv_do(w.B, w.H, w.N, w.d, w.seed, torch.bfloat16)
+    got = _as_dict(run_gpu(q, k, v, dO, w.scale, w.causal))
+    check(w.name, "bf16", got, _full_ref(_np(q), _np(k), _np(v), _np(dO), w.scale, w.causal))
+
+
+# ------------------------------------------------------------ full-size workloads, sampled
+
+def _head_ref(q, k, v, dO, b, h, scale, causal, rows=None, keys=None):
+    """Oracle for one head: O, L, dQ at `rows` and dK, dV at `keys` (all if None)."""
+    N = q.shape[2]
+    qh, kh, vh, doh = (_np(x[b, h]) for x in (q, k, v, dO))
+    rows = np.arange(N) if rows is None else np.asarray(rows)
+    keys = np.arange(N) if keys is None else np.asarray(keys)
+    o, lse, dq = oracle.query_rows(qh, kh, vh, doh, rows, scale, causal)
+    dk, dv = oracle.key_rows(qh, kh, vh, doh, keys, scale, causal)
+    return {"o": o, "lse": lse, "dq": dq, "dk": dk, "dv": dv}, rows, keys
+
+
+def _sampled_check(name, w, q, k, v, dO, got, heads, n_rows=64):
+    B, H, N = w.B, w.H, w.N
+    # whole heads
+    for (b, h) in heads:
+        ref, rows, keys = _head_ref(q, k, v, dO, b, h, w.scale, w.causal)
+        g = {"o": got["o"][b, h], "lse": got["lse"][b, h], "dq": got["dq"][b, h],
+             "dk": got["dk"][b, h], "dv": got["dv"][b, h]}
+        check(f"{name}_head{b}_{h}", "bf16", g, ref)
+    # seeded query rows spread over all heads
+    flat = sample_indices(B * H * N, n_rows, seed=99).numpy()
+    o_r, l_r, dq_r = [], [], []
+    for idx in flat:
+        b, h, i = idx // (H * N), (idx // N) % H, idx % N
+        ref, _, _ = _head_ref(q, k, v, dO, b, h, w.scale, w.causal, rows=[i], keys=[])
+        o_r.append((got["o"][b, h, i], ref["o"][0]))
+        l_r.append((got["lse"][b, h, i], ref["lse"][0]))
+        dq_r.append((got["dq"][b, h, i], ref["dq"][0]))
+    g = {"o": np.array([a for a, _ in o_r]), "lse": np.array([a for a, _ in l_r]),
+         "dq": np.array([a for a, _ in dq_r])}
+    r = {"o": np.array([b for _, b in o_r]), "lse": np.array([b for _, b in l_r]),
+         "dq": np.array([b for _, b in dq_r])}
+    check(f"{name}_rows", "bf16", g, r)
+
+
+def test_bf16_B4_H16_N4096_d64():
+    w = WORKLOADS["bf16_B4_H16_N4096_d64"]
+    q, k, v, dO = make_qkv_do(w.B, w.H, w.N, w.d, w.seed, torch.bfloat16)
+    got = _as_dict(run_gpu(q, k, v, dO, w.scale, w.causal))
+    _sampled_check(w.name, w, q, k, v, dO, got, heads=[(0, 0), (3, 15)])
+
+
+def test_bf16_B8_H32_N4096_d128():
+    w = WORKLOADS["bf16_B8_H32_N4096_d128"]
+    q, k, v, dO = make_qkv_do(w.B, w.H, w.N, w.d, w.seed, torch.bfloat16)
+    got = _as_dict(run_gpu(q, k, v, dO, w.scale, w.causal))
+    _sampled_check(w.name, w, q, k, v, dO, got, heads=[(0, 0), (7, 31)])
+
+
+def test_bf16_causal_B1_H32_N65536_d128():
+    w = WORKLOADS["bf16_causal_B1_H32_N65536_d128"]
+    q, k, v, dO = make_qkv_do(w.B, w.H, w.N, w.d, w.seed, torch.bfloat16)
+    got = _as_dict(run_gpu(q, k, v, dO, w.scale, w.causal))
+    N = w.N
+    # 256 seeded query rows over all heads: O, L, dQ (each row costs O(N d))
+    flat = sample_indices(w.H * N, 256, seed=5).numpy()
+    by_head = {}
+    for idx in flat:
+        by_head.setdefault(int(idx // N), []).append(int(idx % N))
+    g, r = {"o": [], "lse": [], "dq": []}, {"o": [], "lse": [], "dq": []}
+    for h, rows in by_head.items():
+        qh, kh, vh, doh = (_np(x[0, h]) for x in (q, k, v, dO))
+        o, lse, dq = oracle.query_rows(qh, kh, vh, doh, rows, w.scale, True)
+        g["o"].append(got["o"][0, h, rows]); r["o"].append(o)
+        g["lse"].append(got["lse"][0, h, rows]); r["lse"].append(lse)
+        g["dq"].append(got["dq"][0, h, rows]); r["dq"].append(dq)
+    check(w.name + "_rows", "bf16", {k_: np.concatenate(v_) for k_, v_ in g.items()},
+          {k_: np.concatenate(v_) for k_, v_ in r.items()})
+    # 256 key rows: 64 seeded keys in the last 4096 positions of 4 heads (a key's
+    # gradient needs every later query's L and D, so late keys keep this bounded)
+    gk, rk = {"dk": [], "dv": []}, {"dk": [], "dv": []}
+    for h in (0, 9, 22, 31):
+        keys = (N - 4096 + sample_indices(4096, 64, seed=h).numpy()).tolist()
+        qh, kh, vh, doh = (_np(x[0, h]) for x in (q, k, v, dO))
+        dk, dv = oracle.key_rows(qh, kh, vh, doh, keys, w.scale, True)
+        gk["dk"].append(got["dk"][0, h, keys]); rk["dk"].append(dk)
+        gk["dv"].append(got["dv"][0, h, keys]); rk["dv"].append(dv)
+    check(w.name + "_keys", "bf16", {k_: np.concatenate(v_) for k_, v_ in gk.items()},
+          {k_: np.concatenate(v_) for k_, v_ in rk.items()})
+    # any-size properties over every key of every head: rows of P sum to one, so
+    # sum_j dK_j = 0 and sum_j dV_j = sum_i dO_i
+    dk_sum = got["dk"].sum(axis=2)
+    dv_sum = got["dv"].sum(axis=2)
+    do_sum = _np(dO).sum(axis=2)
+    assert np.max(np.abs(dk_sum)) <= 1e-2 * np.max(np.abs(got["dk"]).sum(axis=2))
+    assert np.max(np.abs(dv_sum - do_sum)) <= 1e-2 * np.max(np.abs(got["dv"]).sum(axis=2))
+
+
+def test_repeated_calls_are_stable():
+    """The same call twice gives the same O and L (no state leaks between calls)."""
+    q, k, v, dO = make_qkv_do(2, 3, 333, 128, seed=3, dtype=torch.bfloat16)
+    a = run_gpu(q, k, v, dO, 0.1, True, backward=False)
+    b = run_gpu(q, k, v, dO, 0.1, True, backward=False)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
