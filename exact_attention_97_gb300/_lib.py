@@ -27,6 +27,7 @@ _SIGNATURES = {
     "fa_device_status": (c_int, []),
     "fa_last_launch_count": (c_int, []),
     "fa_set_kernel_timing": (c_int, [c_void_p, c_int]),
+    "fa_bwd_static_scratch": (c_int, [c_void_p] * 9 + [c_int] * 4 + [c_float, c_int, c_void_p]),
 }
 
 FA_BF16, FA_F32 = 0, 1

@@ -321,3 +321,80 @@ int fa_bwd_f32(const float *q, const float *k, const float *v, const float *o, c
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// fa_bwd_static_scratch: fa_bwd without a caller-supplied workspace.
+//
+// Some callers cannot allocate device memory when they call the backward
+// pass: a host framework that reserves the GPU's memory up front in its own
+// pool and lets nothing else call cudaMalloc, a plug-in whose fixed calling
+// convention has no slot for a workspace pointer, or a latency-bound path that
+// may not allocate after start-up (cudaMalloc can synchronise the device).
+// For them the scratch lives in the file-scope array below, which every GPU
+// that loads this library holds until the process exits.
+// ---------------------------------------------------------------------------
+namespace {
+
+static __device__ __align__(256) unsigned char g_static_scratch[FA_STATIC_SCRATCH_BYTES];
+
+unsigned char *g_static_scratch_ptr[kMaxDevices] = {};
+std::mutex g_static_scratch_mutex;
+
+// Device address of the static scratch on the current device, looked up once
+// per device (the host-side name is only a stand-in for the device array).
+int static_scratch(unsigned char **out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return record(e);
+  if (dev < 0 || dev >= kMaxDevices) return kErrArch;
+  std::lock_guard<std::mutex> lock(g_static_scratch_mutex);
+  if (!g_static_scratch_ptr[dev]) {
+    void *p = nullptr;
+    if ((e = cudaGetSymbolAddress(&p, g_static_scratch)) != cudaSuccess) return record(e);
+    g_static_scratch_ptr[dev] = static_cast<unsigned char *>(p);
+  }
+  *out = g_static_scratch_ptr[dev];
+  return kOk;
+}
+
+}  // namespace
+
+extern "C" int fa_bwd_static_scratch(const void *q, const void *k, const void *v, const void *o,
+                                     const float *lse, const void *dO, void *dq, void *dk, void *dv,
+                                     int B, int H, int N, int d, float scale, int causal,
+                                     fa_stream_t stream) {
+  if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return FA_ERR_NULL;
+  int st = check_shape(B, H, N, d, 128);
+  if (st != kOk) return st;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (!isfinite(scale)) return FA_ERR_ARG;
+  const void *ptrs[] = {q, k, v, o, dO, dq, dk, dv};
+  for (const void *p : ptrs)
+    if (!aligned(p, 16)) return FA_ERR_ALIGN;
+  if (!aligned(lse, 4)) return FA_ERR_ALIGN;
+  const BwdWorkspace w = ws_layout(B, H, N, d, FA_BF16);
+  if (w.total > static_cast<size_t>(FA_STATIC_SCRATCH_BYTES)) return FA_ERR_WORKSPACE;
+  DeviceInfo *dev = nullptr;
+  if ((st = current_device(&dev)) != kOk) return st;
+  unsigned char *ws = nullptr;
+  if ((st = static_scratch(&ws)) != kOk) return st;
+  if ((st = get_encoder()) != kOk) return st;
+  CUtensorMap tq, tk, tv, tdo;
+  const int BH = B * H;
+  if ((st = make_map(&tq, q, BH, N, d)) != kOk || (st = make_map(&tk, k, BH, N, d)) != kOk ||
+      (st = make_map(&tv, v, BH, N, d)) != kOk || (st = make_map(&tdo, dO, BH, N, d)) != kOk)
+    return st;
+  // The first kernel of the pass rewrites every scratch byte it later reads
+  // (zeroed dQ accumulator, L and D rows), so the previous call's contents
+  // never leak into this one.
+  int launches = 0;
+  cudaError_t e = launch_bwd_bf16(tq, tk, tv, tdo, o, dO, lse, dq, dk, dv,
+                                  reinterpret_cast<float *>(ws + w.acc),
+                                  reinterpret_cast<float *>(ws + w.lp),
+                                  reinterpret_cast<float *>(ws + w.dp), B, H, N, d, scale,
+                                  causal ? 1 : 0, dev->status, dev->num_sms,
+                                  reinterpret_cast<cudaStream_t>(stream), &launches);
+  if (e != cudaSuccess) return record(e);
+  t_last_launches = launches;
+  return FA_OK;
+}

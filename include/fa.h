@@ -150,6 +150,41 @@ int fa_last_launch_count(void);
  */
 int fa_set_kernel_timing(void **events, int n_pairs);
 
+/*
+ * fa_bwd_static_scratch -- the bf16 backward pass for callers that cannot
+ * allocate device memory (no counterpart on the pages; the method is the
+ * same as fa_bwd's, only the scratch memory differs).
+ *
+ * Who needs it: code that runs under a host framework which reserves the
+ * GPU's memory up front in its own pool and allows no other cudaMalloc, a
+ * plug-in whose fixed calling convention has no slot for a workspace, or a
+ * latency-bound path that may not allocate after start-up (cudaMalloc can
+ * synchronise the device).
+ *
+ * Arguments, layout and results are those of fa_bwd without the workspace
+ * pair. Instead of a caller buffer the pass uses one static device array of
+ * FA_STATIC_SCRATCH_BYTES that this library holds on every GPU that loads it,
+ * until the process exits; the call itself allocates nothing (no cudaMalloc,
+ * no cudaFree, no allocating library routine).
+ *   Limit   returns FA_ERR_WORKSPACE, launching nothing, when
+ *           fa_bwd_workspace_size(B, H, N, d, FA_BF16) exceeds
+ *           FA_STATIC_SCRATCH_BYTES (e.g. B*H*N*d of about 4M elements).
+ *   Set-up  the first call on a device looks up the array's device address
+ *           (cudaGetSymbolAddress); make that first call before any stream
+ *           capture.
+ *   Sharing every call on a device uses the same array, which keeps the last
+ *           call's contents; the pass rewrites every byte it reads before
+ *           reading it. Calls whose kernels overlap on the GPU (different
+ *           streams, or host threads, with no ordering between them) race on
+ *           the array and give wrong gradients: order them.
+ */
+#define FA_STATIC_SCRATCH_BYTES (16u * 1024u * 1024u)
+
+int fa_bwd_static_scratch(const void *q, const void *k, const void *v,
+                          const void *o, const float *lse, const void *dO,
+                          void *dq, void *dk, void *dv, int B, int H, int N,
+                          int d, float scale, int causal, fa_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
