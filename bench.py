@@ -314,6 +314,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=None, help="workload name (default: the headline)")
+    ap.add_argument("--shape", default=None,
+                    help="B,H,N,d[,causal]: a smaller bf16 case of the same kernels (profiling)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-heads", type=int, default=8, help="heads in the CPU-baseline sample")
@@ -321,8 +323,13 @@ def main():
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per launch of the dominant kernel from an ncu capture")
     args = ap.parse_args()
-    from exact_attention_97_gb300.inputs import HEADLINE, WORKLOADS
+    from exact_attention_97_gb300.inputs import HEADLINE, WORKLOADS, Workload
     w = WORKLOADS[args.workload or HEADLINE]
+    if args.shape:
+        vals = [int(x) for x in args.shape.split(",")]
+        B, H, N, d = vals[:4]
+        causal = bool(vals[4]) if len(vals) > 4 else False
+        w = Workload(f"bf16{'_causal' if causal else ''}_B{B}_H{H}_N{N}_d{d}", "bf16", B, H, N, d, causal)
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":

@@ -56,9 +56,12 @@ def build(force: bool = False, verbose: bool = False) -> str:
     os.makedirs(BUILD, exist_ok=True)
     cc = nvcc()
 
+    # tuning knobs (e.g. "-DFA_FWD_POLY_PAIRS=2") for sweeps; empty by default
+    extra = os.environ.get("FA_NVCC_DEFINES", "").split()
+
     def compile_one(src):
         obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
-        cmd = [cc, *ARCH, *NVCC_FLAGS, "-c", src, "-o", obj]
+        cmd = [cc, *ARCH, *NVCC_FLAGS, *extra, "-c", src, "-o", obj]
         if verbose:
             cmd.insert(1, "-Xptxas=-v")
         r = subprocess.run(cmd, capture_output=True, text=True)

@@ -61,7 +61,9 @@ struct BwdCfg {
   static constexpr int kQ = kV + kTileBytes;
   static constexpr int kDO = kQ + kStages * kTileBytes;
   static constexpr int kDS = kDO + kStages * kTileBytes;  // only used when !kDsInDo
-  static constexpr int kBytes = kDS + (kDsInDo ? 0 : kBlk * kBlk * 2);
+  static constexpr int kStage = kDS + (kDsInDo ? 0 : kBlk * kBlk * 2);  // dQ staging (d = 128)
+  static constexpr int kStageRows = 32;                                 // query rows per chunk
+  static constexpr int kBytes = kStage + (kDsInDo ? kStageRows * D * 4 : 0);
   static constexpr int kAlloc = kBytes + 1024;
   // TMEM columns
   static constexpr uint32_t tS = 0, tDP = 128, tDV = 256, tDK = 256 + D, tDQ = (D == 128) ? 128 : 384;
@@ -78,7 +80,7 @@ __device__ __forceinline__ float bf16hi(uint32_t v) { return __uint_as_float(v &
 
 // ------------------------------------------------------------------ kernel 1
 // Per query row of a head padded to Np = 128*ceil(N/128) rows:
-//   Lp = L * log2(e) (so the main kernel forms p = 2^(s*c - Lp)), +inf past N;
+//   Lp = -L * log2(e) (so the main kernel forms p = 2^(s*c + Lp)), -inf past N;
 //   Dp = sum_c dO_ic O_ic, 0 past N;
 // and zeroing of the fp32 dQ accumulator rows. One group of D/8 threads per
 // row, 16-byte loads.
@@ -115,7 +117,7 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16 *__re
   for (int off = kTpr / 2; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
   if (pr < prow_total && part == 0) {
     Dp[pr] = real ? s : 0.f;
-    Lp[pr] = real ? lse[r] * kLog2e : INFINITY;
+    Lp[pr] = real ? -lse[r] * kLog2e : -INFINITY;
   }
 }
 
@@ -136,6 +138,11 @@ __global__ void __launch_bounds__(256) bwd_dq_kernel(const float *__restrict__ d
 }
 
 // ------------------------------------------------------------------ kernel 2
+#ifndef FA_BWD_POLY_PAIRS
+#define FA_BWD_POLY_PAIRS 0
+#endif
+constexpr int kBwdPolyPairs = FA_BWD_POLY_PAIRS;  // of every 8 exp pairs, this many on the FMA pipe
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ,
@@ -151,7 +158,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
   __shared__ uint64_t kv_full, qd_full[NST], qd_empty[NST], s_full, dp_full, p_ready, ds_ready,
-      ds_free, dq_full, dq_free, dkdv_done, drain;
+      ds_free, dq_full, dq_free, dkdv_done, drain, stage_full, stage_free;
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_flag;
   __shared__ __align__(16) float Lst[NST][kBlk], Dst[NST][kBlk];  // per stage, filled by bulk copy
@@ -180,6 +187,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&dq_free, 128);
     mbar_init(&dkdv_done, 1);
     mbar_init(&drain, 1);
+    mbar_init(&stage_full, 128);
+    mbar_init(&stage_free, 1);
     fence_mbar_init();
   }
   if (warp == 2) {
@@ -220,22 +229,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // -------------------------------------------------------------- MMA issuer
+    // Order per tile t: dP_t, dV_t, S_{t+1}, dK_t, dQ_t. S_{t+1} goes ahead of
+    // dK_t and dQ_t so that P_{t+1} is built while those two run.
     if (lane == 0) {
       constexpr uint32_t id_s = idesc_bf16(kBlk, kBlk, false, false);   // S^T, dP^T
       constexpr uint32_t id_kv = idesc_bf16(kBlk, D, false, true);      // dV, dK
       constexpr uint32_t id_dq =
           (D == 128) ? idesc_bf16(D, kBlk, true, true) : idesc_bf16(kBlk, D, true, true);
       const uint32_t k_addr = smem_u32(smem + C::kK), v_addr = smem_u32(smem + C::kV);
-      bool ok = mbar_wait(&kv_full, 0, &abort_flag);
-      for (int t = 0; ok && t < n_tiles; ++t) {
+      auto issue_s = [&](int t) -> bool {  // S^T_t = K Q_t^T into the S columns
         const int st = t % NST;
-        const uint32_t ph = t & 1;
-        const uint32_t q_addr = smem_u32(smem + C::kQ + st * C::kTileBytes);
-        const uint32_t do_addr = smem_u32(smem + C::kDO + st * C::kTileBytes);
-        const uint32_t ds_addr = C::kDsInDo ? do_addr : smem_u32(smem + C::kDS);
-        if (!mbar_wait(&qd_full[st], (t / NST) & 1, &abort_flag)) { ok = false; break; }
+        if (!mbar_wait(&qd_full[st], (t / NST) & 1, &abort_flag)) return false;
         tc_fence_after();
-        // S^T = K Q^T
+        const uint32_t q_addr = smem_u32(smem + C::kQ + st * C::kTileBytes);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk / 4) * C::kSubBytes + (kk % 4) * 32;
@@ -243,6 +249,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                  sdesc_sw128(q_addr + off, 16, 1024), id_s, kk > 0);
         }
         mma_commit(&s_full);
+        return true;
+      };
+      bool ok = mbar_wait(&kv_full, 0, &abort_flag) && issue_s(0);
+      for (int t = 0; ok && t < n_tiles; ++t) {
+        const int st = t % NST;
+        const uint32_t ph = t & 1;
+        const uint32_t q_addr = smem_u32(smem + C::kQ + st * C::kTileBytes);
+        const uint32_t do_addr = smem_u32(smem + C::kDO + st * C::kTileBytes);
+        const uint32_t ds_addr = C::kDsInDo ? do_addr : smem_u32(smem + C::kDS);
         // dP^T = V dO^T; with d = 128 its columns held dQ^T of the last tile
         if (C::kDsInDo && t > 0) {
           if (!mbar_wait(&dq_free, (t - 1) & 1, &abort_flag)) { ok = false; break; }
@@ -263,9 +278,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_ts(tmem + C::tDV, tmem + C::tS + kk * 8, sdesc_sw128(do_addr + kk * 2048, C::kSubBytes, 1024),
                  id_kv, (t > 0 || kk > 0) ? 1u : 0u);
         if (C::kDsInDo) mma_commit(&ds_free);  // dO buffer may now take dS^T
-        // dK += dS^T Q
         if (!mbar_wait(&ds_ready, ph, &abort_flag)) { ok = false; break; }
         tc_fence_after();
+        // the S columns are free again (P_t read by dV_t and by the dS pass)
+        if (t + 1 < n_tiles && !issue_s(t + 1)) { ok = false; break; }
+        // dK += dS^T Q
 #pragma unroll
         for (int kk = 0; kk < kBlk / 16; ++kk) {
           const uint32_t off = (kk / 4) * C::kSubBytes + (kk % 4) * 32;
@@ -300,69 +317,82 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int kr = wq * 32 + lane;  // key row within the block (TMEM lane)
     const int key = kb * kBlk + kr;
     const uint32_t lane_addr = static_cast<uint32_t>(wq * 32) << 16;
+    const uint64_t cc = f2_pack(scale_log2, scale_log2);
     bool ok = true;
     for (int t = 0; t < n_tiles; ++t) {
       const uint32_t ph = t & 1;
       const int st = t % NST;
       const int q0 = (i_first + t) * kBlk;
-      // L and D of this query tile arrive with Q and dO
+      // -L log2(e) and D of this query tile arrive with Q and dO
       if (!mbar_wait_warp(&qd_full[st], (t / NST) & 1, &abort_flag)) { ok = false; break; }
-      const float *Lt = Lst[st];
-      const float *Dt = Dst[st];
+      const float2 *L2 = reinterpret_cast<const float2 *>(Lst[st]);
+      const float2 *D2 = reinterpret_cast<const float2 *>(Dst[st]);
       // queries below qmin see nothing of this key (causal); keys past N see nothing
       const int qmin = (key >= N) ? (q0 + kBlk) : (causal ? key : 0);
       if (!mbar_wait_warp(&s_full, ph, &abort_flag)) { ok = false; break; }
       tc_fence_after();
+      // P^T = 2^(s c - L log2 e), in two halves of 64 query columns; half h is
+      // written as 32 packed pairs into columns [32h, 32h+32), over scores
+      // that have already been read
 #pragma unroll
-      for (int ch = 0; ch < kBlk / 32; ++ch) {
-        uint32_t r[32];
-        tmem_ld32(tmem + lane_addr + C::tS + ch * 32, r);
-        uint32_t pk[16];
+      for (int h = 0; h < 2; ++h) {
+        uint32_t r[64];
+        tmem_ld64(tmem + lane_addr + C::tS + h * 64, r);
+        uint32_t pk[32];
 #pragma unroll
-        for (int u = 0; u < 16; ++u) {
-          const int c0 = ch * 32 + 2 * u;
-          float p0 = ex2_approx(fmaf(__uint_as_float(r[2 * u]), scale_log2, -Lt[c0]));
-          float p1 = ex2_approx(fmaf(__uint_as_float(r[2 * u + 1]), scale_log2, -Lt[c0 + 1]));
+        for (int u = 0; u < 32; ++u) {
+          const int c0 = h * 64 + 2 * u;
+          const float2 nl = L2[c0 / 2];
+          const uint64_t x2 =
+              f2_fma(f2_pack(__uint_as_float(r[2 * u]), __uint_as_float(r[2 * u + 1])), cc, f2_pack(nl.x, nl.y));
+          float p0, p1;
+          if ((u & 7) < kBwdPolyPairs) {
+            f2_unpack(ex2_poly2(x2), p0, p1);
+          } else {
+            float x0, x1;
+            f2_unpack(x2, x0, x1);
+            p0 = ex2_approx(x0);
+            p1 = ex2_approx(x1);
+          }
           if (q0 + c0 < qmin) p0 = 0.f;
           if (q0 + c0 + 1 < qmin) p1 = 0.f;
           pk[u] = pack_bf16x2(p0, p1);
         }
-        tmem_st16(tmem + lane_addr + C::tS + ch * 16, pk);
+        tmem_st32(tmem + lane_addr + C::tS + h * 32, pk);
       }
       tc_fence_before();
       mbar_arrive(&p_ready);
-      // dS^T = P^T o (dP^T - D)
+      // dS^T = P^T o (dP^T - D), in the same two halves
       if (!mbar_wait_warp(&dp_full, ph, &abort_flag)) { ok = false; break; }
       tc_fence_after();
-      uint32_t ds[kBlk / 2];
+      uint8_t *dsb = C::kDsInDo ? (smem + C::kDO + st * C::kTileBytes) : (smem + C::kDS);
 #pragma unroll
-      for (int ch = 0; ch < kBlk / 32; ++ch) {
-        uint32_t r[32];
-        tmem_ld32(tmem + lane_addr + C::tDP + ch * 32, r);
-        uint32_t pp[16];
-        tmem_ld16(tmem + lane_addr + C::tS + ch * 16, pp);  // 16 packed P pairs
+      for (int h = 0; h < 2; ++h) {
+        uint32_t r[64], pp[32];
+        tmem_ld64(tmem + lane_addr + C::tDP + h * 64, r);
+        tmem_ld32(tmem + lane_addr + C::tS + h * 32, pp);
+        uint32_t ds[32];
 #pragma unroll
-        for (int u = 0; u < 16; ++u) {
-          const int c0 = ch * 32 + 2 * u;
-          const float d0 = bf16lo(pp[u]) * (__uint_as_float(r[2 * u]) - Dt[c0]);
-          const float d1 = bf16hi(pp[u]) * (__uint_as_float(r[2 * u + 1]) - Dt[c0 + 1]);
-          ds[ch * 16 + u] = pack_bf16x2(d0, d1);
+        for (int u = 0; u < 32; ++u) {
+          const float2 dd = D2[h * 32 + u];
+          const float d0 = bf16lo(pp[u]) * (__uint_as_float(r[2 * u]) - dd.x);
+          const float d1 = bf16hi(pp[u]) * (__uint_as_float(r[2 * u + 1]) - dd.y);
+          ds[u] = pack_bf16x2(d0, d1);
+        }
+        if (h == 0) {
+          // the buffer dS^T goes to must be free of its last tensor-core reader
+          const uint32_t fph = C::kDsInDo ? ph : ((t - 1) & 1);
+          if ((C::kDsInDo || t > 0) && !mbar_wait_warp(&ds_free, fph, &abort_flag)) { ok = false; break; }
+          tc_fence_after();
+        }
+        // row kr of dS^T, queries [64h, 64h+64): one 128-byte swizzled row of sub-tile h
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          uint4 *dst = reinterpret_cast<uint4 *>(dsb + h * C::kSubBytes + kr * 128 + ((c ^ (kr & 7)) << 4));
+          *dst = make_uint4(ds[4 * c], ds[4 * c + 1], ds[4 * c + 2], ds[4 * c + 3]);
         }
       }
-      // the buffer dS^T goes to must be free of its last tensor-core reader
-      const uint32_t fph = C::kDsInDo ? ph : ((t - 1) & 1);
-      if ((C::kDsInDo || t > 0) && !mbar_wait_warp(&ds_free, fph, &abort_flag)) { ok = false; break; }
-      tc_fence_after();
-      {
-        uint8_t *dsb = C::kDsInDo ? (smem + C::kDO + st * C::kTileBytes) : (smem + C::kDS);
-#pragma unroll
-        for (int c16 = 0; c16 < kBlk / 8; ++c16) {
-          const int sub = c16 >> 3, chunk = c16 & 7;
-          uint4 *dst = reinterpret_cast<uint4 *>(dsb + sub * C::kSubBytes + kr * 128 +
-                                                 ((chunk ^ (kr & 7)) << 4));
-          *dst = make_uint4(ds[4 * c16], ds[4 * c16 + 1], ds[4 * c16 + 2], ds[4 * c16 + 3]);
-        }
-      }
+      if (!ok) break;
       fence_proxy_async_smem();
       mbar_arrive(&ds_ready);
     }
@@ -386,27 +416,47 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp >= 8) {
-    // ------------------------------------------------------- dQ atomics, dK
+    // ------------------------------------------------------- dQ drain, dK
     const int wq = warp - 8;
     const uint32_t lane_addr = static_cast<uint32_t>(wq * 32) << 16;
+    const bool issuer = (warp == 8 && lane == 0);
     bool ok = true;
+    int chunks = 0;  // staging chunks handed to the copy engine so far
     for (int t = 0; t < n_tiles; ++t) {
       const int q0 = (i_first + t) * kBlk;
+      const int nq = min(kBlk, N - q0);
       if (!mbar_wait_warp(&dq_full, t & 1, &abort_flag)) { ok = false; break; }
       tc_fence_after();
       if (D == 128) {
-        // lane = head dimension c, columns = queries
+        // lane = head dimension c, columns = queries. Read the whole tile,
+        // release the TMEM columns, then push it to the fp32 accumulator in
+        // 32-row chunks through the staging buffer and bulk reduce-adds.
+        uint32_t r[128];
+        tmem_ld128(tmem + lane_addr + C::tDQ, r);
+        tc_fence_before();
+        mbar_arrive(&dq_free);
         const int c = wq * 32 + lane;
-        float *base = dq_acc + (static_cast<size_t>(bh) * N + q0) * D + c;
-        const int nq = min(kBlk, N - q0);
-#pragma unroll 1
-        for (int ch = 0; ch < kBlk / 32; ++ch) {
-          uint32_t r[32];
-          tmem_ld32(tmem + lane_addr + C::tDQ + ch * 32, r);
+        float *stage = reinterpret_cast<float *>(smem + C::kStage);
 #pragma unroll
-          for (int u = 0; u < 32; ++u)
-            if (ch * 32 + u < nq) atomicAdd(base + static_cast<size_t>(ch * 32 + u) * D, __uint_as_float(r[u]));
+        for (int ch = 0; ch < kBlk / C::kStageRows; ++ch) {
+          const int rows = min(C::kStageRows, nq - ch * C::kStageRows);
+          if (rows <= 0) break;
+          if (chunks > 0 && !mbar_wait_warp(&stage_free, (chunks - 1) & 1, &abort_flag)) { ok = false; break; }
+#pragma unroll
+          for (int u = 0; u < C::kStageRows; ++u) stage[u * D + c] = __uint_as_float(r[ch * C::kStageRows + u]);
+          fence_proxy_async_smem();
+          mbar_arrive(&stage_full);
+          if (issuer) {
+            if (!mbar_wait(&stage_full, chunks & 1, &abort_flag)) { ok = false; break; }
+            bulk_reduce_add_f32(dq_acc + (static_cast<size_t>(bh) * N + q0 + ch * C::kStageRows) * D, stage,
+                                static_cast<uint32_t>(rows) * D * 4);
+            bulk_commit();
+            bulk_wait_read_all();
+            mbar_arrive(&stage_free);
+          }
+          ++chunks;
         }
+        if (!ok) break;
       } else {
         // lane = query row, columns = head dimension
         const int q = q0 + wq * 32 + lane;
@@ -422,10 +472,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                        __uint_as_float(r[4 * u + 2]), __uint_as_float(r[4 * u + 3])));
           }
         }
+        tc_fence_before();
+        mbar_arrive(&dq_free);
       }
-      tc_fence_before();
-      mbar_arrive(&dq_free);
     }
+    if (issuer) bulk_wait_all();  // every reduce-add has landed before the CTA ends
     // epilogue: dK rows (times scale)
     if (ok && mbar_wait_warp(&dkdv_done, 0, &abort_flag)) {
       tc_fence_after();

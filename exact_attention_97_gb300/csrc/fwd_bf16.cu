@@ -43,6 +43,10 @@ constexpr int kBlockN = 128;   // keys per tile
 constexpr int kStages = 3;     // K and V ring depth
 constexpr int kThreads = 256;  // 8 warps
 constexpr float kRescaleLog2 = 8.0f;  // move the running max only past 2^8
+#ifndef FA_FWD_POLY_PAIRS
+#define FA_FWD_POLY_PAIRS 0
+#endif
+constexpr int kPolyPairs = FA_FWD_POLY_PAIRS;  // of every 8 exp pairs, this many on the FMA pipe
 constexpr float kLn2 = 0.69314718055994531f;
 
 template <int D>
@@ -202,25 +206,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
-      float s[kBlockN];
-#pragma unroll
-      for (int ch = 0; ch < kBlockN / 32; ++ch) {
-        uint32_t r[32];
-        tmem_ld32(tmem + lane_addr + sb * 128 + ch * 32, r);
-#pragma unroll
-        for (int t = 0; t < 32; ++t) s[ch * 32 + t] = __uint_as_float(r[t]);
-      }
+      uint32_t sr[kBlockN];
+      tmem_ld128(tmem + lane_addr + sb * 128, sr);
       const int key0 = j * kBlockN;
       int limit = N - key0;                              // keys >= N are masked
       if (causal) limit = min(limit, row - key0 + 1);    // keys > row are masked
       if (limit < kBlockN) {
 #pragma unroll
         for (int t = 0; t < kBlockN; ++t)
-          if (t >= limit) s[t] = -INFINITY;
+          if (t >= limit) sr[t] = __float_as_uint(-INFINITY);
       }
-      float mx = s[0];
+      // row max: four independent chains of 3-input max
+      float mx;
+      {
+        float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
 #pragma unroll
-      for (int t = 1; t < kBlockN; ++t) mx = fmaxf(mx, s[t]);
+        for (int t = 0; t < kBlockN; t += 8) {
+          m0 = fmax3(m0, __uint_as_float(sr[t]), __uint_as_float(sr[t + 1]));
+          m1 = fmax3(m1, __uint_as_float(sr[t + 2]), __uint_as_float(sr[t + 3]));
+          m2 = fmax3(m2, __uint_as_float(sr[t + 4]), __uint_as_float(sr[t + 5]));
+          m3 = fmax3(m3, __uint_as_float(sr[t + 6]), __uint_as_float(sr[t + 7]));
+        }
+        mx = fmax3(m0, m1, fmaxf(m2, m3));
+      }
       if (j == 0) {
         m_used = mx;
       } else {
@@ -247,19 +255,39 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+      // P = 2^(s*c - m*c), two columns at a time; in every group of 8 pairs the
+      // first kPolyPairs go through the FMA-pipe polynomial, the rest through ex2
       const float neg = -m_used * scale_log2;
-      float rs = 0.f;
+      const uint64_t cc = f2_pack(scale_log2, scale_log2), nn = f2_pack(neg, neg);
+      uint64_t acc0 = 0, acc1 = 0, acc2 = 0, acc3 = 0;  // packed partial row sums (+0.0f pairs)
+      uint32_t pk[kBlockN / 2];
 #pragma unroll
-      for (int ch = 0; ch < kBlockN / 32; ++ch) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int t = 0; t < 16; ++t) {
-          const float p0 = ex2_approx(fmaf(s[ch * 32 + 2 * t], scale_log2, neg));
-          const float p1 = ex2_approx(fmaf(s[ch * 32 + 2 * t + 1], scale_log2, neg));
-          rs += p0 + p1;
-          pk[t] = pack_bf16x2(p0, p1);
+      for (int u = 0; u < kBlockN / 2; ++u) {
+        const uint64_t x2 = f2_fma(f2_pack(__uint_as_float(sr[2 * u]), __uint_as_float(sr[2 * u + 1])), cc, nn);
+        uint64_t p2;
+        if ((u & 7) < kPolyPairs) {
+          p2 = ex2_poly2(x2);
+        } else {
+          float x0, x1;
+          f2_unpack(x2, x0, x1);
+          p2 = f2_pack(ex2_approx(x0), ex2_approx(x1));
         }
-        tmem_st16(tmem + lane_addr + sb * 128 + ch * 16, pk);
+        switch (u & 3) {
+          case 0: acc0 = f2_add(acc0, p2); break;
+          case 1: acc1 = f2_add(acc1, p2); break;
+          case 2: acc2 = f2_add(acc2, p2); break;
+          default: acc3 = f2_add(acc3, p2); break;
+        }
+        float p0, p1;
+        f2_unpack(p2, p0, p1);
+        pk[u] = pack_bf16x2(p0, p1);
+      }
+      tmem_st64(tmem + lane_addr + sb * 128, pk);
+      float rs;
+      {
+        float a0, a1;
+        f2_unpack(f2_add(f2_add(acc0, acc1), f2_add(acc2, acc3)), a0, a1);
+        rs = a0 + a1;
       }
       l_sum += rs;
       tc_fence_before();
