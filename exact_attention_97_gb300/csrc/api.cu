@@ -122,13 +122,14 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Workspace layout.
 //   f32:  D [B*H*N] fp32.
-//   bf16: dQ accumulator [B*H*N*d] fp32, then L*log2(e) and D, each
-//         [B*H][Np] fp32 with Np = 128*ceil(N/128) (padding rows hold +inf / 0).
+//   bf16: -L*log2(e) and D, each [B*H][Np] fp32 with Np = 128*ceil(N/128)
+//         (padding rows hold -inf / 0).
 struct BwdWorkspace {
-  size_t acc = 0, lp = 0, dp = 0, total = 0;  // byte offsets and size
+  size_t lp = 0, dp = 0, total = 0;  // byte offsets and size
 };
 
 BwdWorkspace ws_layout(int B, int H, int N, int d, int dtype) {
+  (void)d;
   BwdWorkspace w;
   const size_t rows = static_cast<size_t>(B) * H * N;
   if (dtype == FA_F32) {
@@ -136,9 +137,8 @@ BwdWorkspace ws_layout(int B, int H, int N, int d, int dtype) {
     return w;
   }
   const size_t prow = static_cast<size_t>(B) * H * ((static_cast<size_t>(N) + 127) / 128 * 128);
-  w.acc = 0;
-  w.lp = round_up(rows * d * sizeof(float), 256);
-  w.dp = w.lp + round_up(prow * sizeof(float), 256);
+  w.lp = 0;
+  w.dp = round_up(prow * sizeof(float), 256);
   w.total = w.dp + round_up(prow * sizeof(float), 256);
   return w;
 }
@@ -266,7 +266,6 @@ int fa_bwd(const void *q, const void *k, const void *v, const void *o, const flo
   char *ws = static_cast<char *>(workspace);
   int launches = 0;
   cudaError_t e = launch_bwd_bf16(tq, tk, tv, tdo, o, dO, lse, dq, dk, dv,
-                                  reinterpret_cast<float *>(ws + w.acc),
                                   reinterpret_cast<float *>(ws + w.lp),
                                   reinterpret_cast<float *>(ws + w.dp), B, H, N, d, scale,
                                   causal ? 1 : 0, dev->status, dev->num_sms,
@@ -385,11 +384,10 @@ extern "C" int fa_bwd_static_scratch(const void *q, const void *k, const void *v
       (st = make_map(&tv, v, BH, N, d)) != kOk || (st = make_map(&tdo, dO, BH, N, d)) != kOk)
     return st;
   // The first kernel of the pass rewrites every scratch byte it later reads
-  // (zeroed dQ accumulator, L and D rows), so the previous call's contents
+  // (the L and D rows, padding included), so the previous call's contents
   // never leak into this one.
   int launches = 0;
   cudaError_t e = launch_bwd_bf16(tq, tk, tv, tdo, o, dO, lse, dq, dk, dv,
-                                  reinterpret_cast<float *>(ws + w.acc),
                                   reinterpret_cast<float *>(ws + w.lp),
                                   reinterpret_cast<float *>(ws + w.dp), B, H, N, d, scale,
                                   causal ? 1 : 0, dev->status, dev->num_sms,

@@ -42,14 +42,13 @@ cudaError_t launch_fwd_bf16(const CUtensorMap &tmQ, const CUtensorMap &tmK, cons
                             int causal, int *status, int num_sms, cudaStream_t stream,
                             int *launches);
 
-// bf16 tensor-core backward (three kernels). dq_acc is [B*H*N*d] fp32; Lp and
-// Dp are [B*H][Np] fp32 with Np = 128*ceil(N/128); all three live in the
-// caller's workspace.
+// bf16 tensor-core backward (three kernels: row terms, dK/dV pass, dQ pass).
+// Lp and Dp are [B*H][Np] fp32 with Np = 128*ceil(N/128), in the caller's
+// workspace.
 cudaError_t launch_bwd_bf16(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtensorMap &tmV,
-                            const CUtensorMap &tmdO, const void *o, const void *dO,
-                            const float *lse, void *dq, void *dk, void *dv, float *dq_acc,
-                            float *Lp, float *Dp, int B, int H, int N, int d, float scale,
-                            int causal, int *status, int num_sms, cudaStream_t stream,
+                            const CUtensorMap &tmdO, const void *o, const void *dO, const float *lse,
+                            void *dq, void *dk, void *dv, float *Lp, float *Dp, int B, int H, int N, int d,
+                            float scale, int causal, int *status, int num_sms, cudaStream_t stream,
                             int *launches);
 
 }  // namespace fa

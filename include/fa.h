@@ -18,9 +18,10 @@
  *   - tiled forward loop and the final division O_i / l_i:
  *     "Flash Attention 原理与实现", section "Forward 的 Tiling 策略";
  *   - backward by recomputation, dV = P^T dO, dP = dO V^T, dS from the
- *     softmax gradient, dQ = dS K, dK = dS^T Q, with cross-block accumulation
- *     of dQ by atomic adds: same blog, section "Backward 的 Tiling 策略" and
- *     item 3 of "实际实现中的注意事项".
+ *     softmax gradient, dQ = dS K, dK = dS^T Q: same blog, section
+ *     "Backward 的 Tiling 策略"; dQ is gathered across key blocks by local
+ *     accumulation (one of the two ways item 3 of "实际实现中的注意事项"
+ *     names) rather than by atomic adds.
  *
  * Conventions shared by every entry point
  *   Layout     Q, K, V, O, dO, dQ, dK, dV are contiguous [B][H][N][d] arrays
@@ -93,12 +94,14 @@ int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
  *   dq, dk, dv       [B][H][N][d] bf16, written.
  *   workspace        device scratch of at least
  *                    fa_bwd_workspace_size(B, H, N, d, FA_BF16) bytes, 256-byte
- *                    aligned, owned by the caller; holds the fp32 dQ
- *                    accumulator and the row terms D_i = sum_c dO_ic O_ic.
- *                    Its contents on entry are ignored.
- * Three kernels run on `stream`: D_i and zeroing of the accumulator, the main
- * pass (one CTA per key block, dQ added with fp32 atomics), and the dQ
- * conversion. Atomic accumulation makes dQ's rounding order vary run to run.
+ *                    aligned, owned by the caller; holds the per-row terms
+ *                    -L*log2(e) and D_i = sum_c dO_ic O_ic, padded to whole
+ *                    128-row tiles (8 bytes per padded row). Its contents on
+ *                    entry are ignored.
+ * Three kernels run on `stream`: the row terms; a pass over key blocks that
+ * forms dK and dV; a pass over query tiles that forms dQ. Both passes
+ * recompute S and dP, so no partial sums go through global memory and the
+ * result does not depend on scheduling.
  */
 int fa_bwd(const void *q, const void *k, const void *v, const void *o,
            const float *lse, const void *dO, void *dq, void *dk, void *dv,
@@ -168,7 +171,8 @@ int fa_set_kernel_timing(void **events, int n_pairs);
  * no cudaFree, no allocating library routine).
  *   Limit   returns FA_ERR_WORKSPACE, launching nothing, when
  *           fa_bwd_workspace_size(B, H, N, d, FA_BF16) exceeds
- *           FA_STATIC_SCRATCH_BYTES (e.g. B*H*N*d of about 4M elements).
+ *           FA_STATIC_SCRATCH_BYTES, i.e. past about 2M padded query rows
+ *           (B*H*128*ceil(N/128) > 2,097,152).
  *   Set-up  the first call on a device looks up the array's device address
  *           (cudaGetSymbolAddress); make that first call before any stream
  *           capture.

@@ -82,7 +82,7 @@ def test_static_scratch_backward_matches_workspace_backward():
 
 def test_static_scratch_refuses_problems_beyond_its_size():
     lib = _lib.load()
-    B, H, N, d = 1, 32, 4096, 128  # needs far more than the static array
+    B, H, N, d = 1, 64, 65536, 128  # 4M padded rows: twice what the static array holds
     assert fa.fa_bwd_workspace_size(B, H, N, d, fa.FA_BF16) > STATIC_BYTES
     p = 0x10000  # never dereferenced: the size check fails before any device work
     st = lib.fa_bwd_static_scratch(*([p] * 9), B, H, N, d, ctypes.c_float(0.1), 0, None)
