@@ -344,16 +344,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ------------------------------------------------------------------ kernel 3
+// K_j is needed until dQ_j, V_j only until dP_j, so they have rings of their
+// own (K one deeper) and loaders of their own: the next K blocks can be in
+// flight while dQ of the current one runs.
 template <int D>
 struct DqCfg {
-  static constexpr int kStages = (D == 128) ? 2 : 3;
+  static constexpr int kKStages = (D == 128) ? 3 : 4;
+  static constexpr int kVStages = (D == 128) ? 2 : 3;
   static constexpr int kTileBytes = kBlk * D * 2;
   static constexpr int kSubBytes = kBlk * 128;
   static constexpr int kQ = 0;
   static constexpr int kDO = kQ + kTileBytes;
   static constexpr int kK = kDO + kTileBytes;
-  static constexpr int kV = kK + kStages * kTileBytes;
-  static constexpr int kBytes = kV + kStages * kTileBytes;
+  static constexpr int kV = kK + kKStages * kTileBytes;
+  static constexpr int kBytes = kV + kVStages * kTileBytes;
   static constexpr int kAlloc = kBytes + 1024;
   static constexpr uint32_t tS = 0, tDP = 256, tDQ = 384;  // S buffers at 0 and 128
 };
@@ -366,11 +370,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                   __nv_bfloat16 *__restrict__ dq, int N, float scale, float scale_log2, int causal,
                   int *status) {
   using C = DqCfg<D>;
-  constexpr int NST = C::kStages;
+  constexpr int KS = C::kKStages, VS = C::kVStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
-  __shared__ uint64_t qd_full, kv_full[NST], kv_empty[NST], s_full[2], dp_full, ds_ready, done, drain;
+  __shared__ uint64_t qd_full, k_full[KS], k_empty[KS], v_full[VS], v_empty[VS], s_full[2], dp_full,
+      ds_ready, done, drain;
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_flag;
 
@@ -385,9 +390,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     abort_flag = 0;
     mbar_init(&qd_full, 1);
-    for (int s = 0; s < NST; ++s) {
-      mbar_init(&kv_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
+    for (int s = 0; s < KS; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+    }
+    for (int s = 0; s < VS; ++s) {
+      mbar_init(&v_full[s], 1);
+      mbar_init(&v_empty[s], 1);
     }
     mbar_init(&s_full[0], 1);
     mbar_init(&s_full[1], 1);
@@ -407,27 +416,38 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = tmem_base_s;
 
   if (warp == 0) {
-    // ---------------------------------------------------------------- producer
+    // ------------------------------------------------------- loader: Q, dO, K
     if (lane == 0) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
-      tma_prefetch_desc(&tmV);
       tma_prefetch_desc(&tmdO);
       mbar_arrive_expect_tx(&qd_full, 2 * C::kTileBytes);
       load_rows(smem + C::kQ, &tmQ, &qd_full, D, qt * kBlk, bh);
       load_rows(smem + C::kDO, &tmdO, &qd_full, D, qt * kBlk, bh);
       int issued = 0;
       for (int j = 0; j < n_kb; ++j) {
-        const int st = j % NST;
-        if (j >= NST && !mbar_wait(&kv_empty[st], ((j / NST) & 1) ^ 1, &abort_flag)) break;
-        mbar_arrive_expect_tx(&kv_full[st], 2 * C::kTileBytes);
-        load_rows(smem + C::kK + st * C::kTileBytes, &tmK, &kv_full[st], D, j * kBlk, bh);
-        load_rows(smem + C::kV + st * C::kTileBytes, &tmV, &kv_full[st], D, j * kBlk, bh);
+        const int st = j % KS;
+        if (j >= KS && !mbar_wait(&k_empty[st], ((j / KS) & 1) ^ 1, &abort_flag)) break;
+        mbar_arrive_expect_tx(&k_full[st], C::kTileBytes);
+        load_rows(smem + C::kK + st * C::kTileBytes, &tmK, &k_full[st], D, j * kBlk, bh);
         ++issued;
       }
       mbar_wait_drain(&qd_full, 0);
-      for (int j = max(0, issued - NST); j < issued; ++j)
-        mbar_wait_drain(&kv_full[j % NST], (j / NST) & 1);
+      for (int j = max(0, issued - KS); j < issued; ++j) mbar_wait_drain(&k_full[j % KS], (j / KS) & 1);
+    }
+  } else if (warp == 3) {
+    // ---------------------------------------------------------------- loader: V
+    if (lane == 0) {
+      tma_prefetch_desc(&tmV);
+      int issued = 0;
+      for (int j = 0; j < n_kb; ++j) {
+        const int st = j % VS;
+        if (j >= VS && !mbar_wait(&v_empty[st], ((j / VS) & 1) ^ 1, &abort_flag)) break;
+        mbar_arrive_expect_tx(&v_full[st], C::kTileBytes);
+        load_rows(smem + C::kV + st * C::kTileBytes, &tmV, &v_full[st], D, j * kBlk, bh);
+        ++issued;
+      }
+      for (int j = max(0, issued - VS); j < issued; ++j) mbar_wait_drain(&v_full[j % VS], (j / VS) & 1);
     }
   } else if (warp == 1) {
     // -------------------------------------------------------------- MMA issuer
@@ -437,8 +457,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t id_q = idesc_bf16(kBlk, D, false, true);      // dQ
       const uint32_t q_addr = smem_u32(smem + C::kQ), do_addr = smem_u32(smem + C::kDO);
       auto issue_s = [&](int j) -> bool {  // S_j = Q K_j^T into buffer j&1
-        const int st = j % NST;
-        if (!mbar_wait(&kv_full[st], (j / NST) & 1, &abort_flag)) return false;
+        const int st = j % KS;
+        if (!mbar_wait(&k_full[st], (j / KS) & 1, &abort_flag)) return false;
         tc_fence_after();
         const uint32_t k_addr = smem_u32(smem + C::kK + st * C::kTileBytes);
 #pragma unroll
@@ -450,8 +470,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(&s_full[j & 1]);
         return true;
       };
-      auto issue_dp = [&](int j) {  // dP_j = dO V_j^T (K_j and V_j landed together)
-        const uint32_t v_addr = smem_u32(smem + C::kV + (j % NST) * C::kTileBytes);
+      auto issue_dp = [&](int j) -> bool {  // dP_j = dO V_j^T
+        const int st = j % VS;
+        if (!mbar_wait(&v_full[st], (j / VS) & 1, &abort_flag)) return false;
+        tc_fence_after();
+        const uint32_t v_addr = smem_u32(smem + C::kV + st * C::kTileBytes);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk / 4) * C::kSubBytes + (kk % 4) * 32;
@@ -459,12 +482,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                  id_s, kk > 0);
         }
         mma_commit(&dp_full);
+        mma_commit(&v_empty[st]);
+        return true;
       };
-      bool ok = mbar_wait(&qd_full, 0, &abort_flag) && issue_s(0);
-      if (ok) issue_dp(0);
+      bool ok = mbar_wait(&qd_full, 0, &abort_flag) && issue_s(0) && issue_dp(0);
       if (ok && n_kb > 1) ok = issue_s(1);
       for (int j = 0; ok && j < n_kb; ++j) {
-        const int st = j % NST;
+        const int st = j % KS;
         if (!mbar_wait(&ds_ready, j & 1, &abort_flag)) { ok = false; break; }
         tc_fence_after();
         // dQ += dS_j K_j : A = dS_j (bf16 in TMEM), B = K_j (MN-major)
@@ -473,8 +497,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kk = 0; kk < kBlk / 16; ++kk)
           mma_ts(tmem + C::tDQ, tmem + C::tS + (j & 1) * 128 + a_col(kk),
                  sdesc_sw128(k_addr + kk * 2048, C::kSubBytes, 1024), id_q, (j > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&kv_empty[st]);
-        if (j + 1 < n_kb) issue_dp(j + 1);  // dP_j has been read into dS_j
+        mma_commit(&k_empty[st]);
+        if (j + 1 < n_kb && !issue_dp(j + 1)) { ok = false; break; }  // dP_j has been read into dS_j
         // buffer j&1 still holds dS_j, which the dQ_j MMA above reads first
         if (j + 2 < n_kb && !issue_s(j + 2)) { ok = false; break; }
       }

@@ -10,14 +10,17 @@
 // and the saved statistic L = m + ln l of its section 04.
 //
 // GB300 design (one CTA = one 128-row query tile of one (batch, head)):
-//   warp 0      TMA producer: Q once, then K_j and V_j into a ring of kStages
-//               shared-memory stages (128-byte swizzle, 3-D tensor maps so
-//               rows past N read as zero).
-//   warp 1      MMA issuer (one thread): S_j = Q K_j^T into tensor memory
-//               (TMEM), double-buffered so S_{j+1} runs while row statistics
-//               of S_j are computed; then O += P_j V_j with P_j read straight
-//               from TMEM (A operand in TMEM, B = V_j in shared memory).
-//   warp 2      allocates / frees the 512 TMEM columns.
+//   warp 0      loader: Q once, then K_j into a ring of kStages shared-memory
+//               stages (128-byte swizzle, 3-D tensor maps so rows past N read
+//               as zero).
+//   warp 2      loader of V_j (its own ring); also allocates and frees the
+//               512 tensor-memory (TMEM) columns.
+//   warp 1      MMA issuer for S_j = Q K_j^T into one of three TMEM buffers,
+//               so S_{j+1} and S_{j+2} can run while row statistics of S_j
+//               are computed.
+//   warp 3      MMA issuer for O += P_j V_j, with P_j read straight from TMEM
+//               (A operand in TMEM, B = V_j in shared memory). Two issuing
+//               threads keep the tensor pipe fed while either waits.
 //   warps 4-7   softmax: thread t owns row t of the tile (= TMEM lane t).
 //               Loads its 128 scores, applies the mask, takes the row max,
 //               writes P = 2^(s*c - m*c) (c = scale*log2 e) back as bf16 over
@@ -27,7 +30,7 @@
 //               (ld, multiply, st) is skipped on most tiles. The epilogue
 //               divides by l, stores O as bf16 and L = m*scale + ln l.
 //
-// TMEM columns: S buffer 0 = [0,128), S buffer 1 = [128,256), O = [256,256+d).
+// TMEM columns: S buffers [0,128), [128,256), [256,384); O = [384, 384+d).
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
@@ -41,6 +44,7 @@ namespace {
 constexpr int kBlockM = 128;   // query rows per tile (= TMEM lanes)
 constexpr int kBlockN = 128;   // keys per tile
 constexpr int kStages = 3;     // K and V ring depth
+constexpr int kSBuf = 3;       // S buffers in TMEM (3 x 128 columns, O after them)
 constexpr int kThreads = 256;  // 8 warps
 constexpr float kRescaleLog2 = 8.0f;  // move the running max only past 2^8
 #ifndef FA_FWD_POLY_PAIRS
@@ -77,7 +81,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
   __shared__ uint64_t q_full, k_full[kStages], k_empty[kStages], v_full[kStages],
-      v_empty[kStages], s_full[2], p_ready[2], o_done, drain;
+      v_empty[kStages], s_full[kSBuf], p_ready[kSBuf], pv_done[kSBuf], drain_s, drain_pv;
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_flag;
 
@@ -98,12 +102,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&v_full[s], 1);
       mbar_init(&v_empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < kSBuf; ++b) {
       mbar_init(&s_full[b], 1);
       mbar_init(&p_ready[b], 4 * 32);
+      mbar_init(&pv_done[b], 1);
     }
-    mbar_init(&o_done, 1);
-    mbar_init(&drain, 1);
+    mbar_init(&drain_s, 1);
+    mbar_init(&drain_pv, 1);
     fence_mbar_init();
   }
   if (warp == 2) {
@@ -114,82 +119,91 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base_s;
-  const uint32_t tmem_O = tmem + 256;
+  const uint32_t tmem_O = tmem + kSBuf * 128;
 
   if (warp == 0) {
-    // ---------------------------------------------------------------- producer
+    // ------------------------------------------------------------ loader: Q, K
     if (lane == 0) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
-      tma_prefetch_desc(&tmV);
       mbar_arrive_expect_tx(&q_full, L::kTileBytes);
       load_tile(smem + L::kQ, &tmQ, &q_full, D, qtile * kBlockM, bh);
       int issued = 0;
       for (int j = 0; j < n_ktiles; ++j) {
         const int st = j % kStages;
-        const uint32_t ph = ((j / kStages) & 1) ^ 1;  // parity of the previous use
-        if (j >= kStages && !mbar_wait(&k_empty[st], ph, &abort_flag)) break;
+        if (j >= kStages && !mbar_wait(&k_empty[st], ((j / kStages) & 1) ^ 1, &abort_flag)) break;
         mbar_arrive_expect_tx(&k_full[st], L::kTileBytes);
         load_tile(smem + L::kK + st * L::kTileBytes, &tmK, &k_full[st], D, j * kBlockN, bh);
-        if (j >= kStages && !mbar_wait(&v_empty[st], ph, &abort_flag)) {
-          ++issued;
-          break;
-        }
-        mbar_arrive_expect_tx(&v_full[st], L::kTileBytes);
-        load_tile(smem + L::kV + st * L::kTileBytes, &tmV, &v_full[st], D, j * kBlockN, bh);
         ++issued;
       }
       // teardown: every issued copy must land before the CTA's memory is released
       mbar_wait_drain(&q_full, 0);
-      for (int j = max(0, issued - kStages); j < issued; ++j) {
+      for (int j = max(0, issued - kStages); j < issued; ++j)
         mbar_wait_drain(&k_full[j % kStages], (j / kStages) & 1);
+    }
+  } else if (warp == 2) {
+    // ---------------------------------------------------------------- loader: V
+    if (lane == 0) {
+      tma_prefetch_desc(&tmV);
+      int issued = 0;
+      for (int j = 0; j < n_ktiles; ++j) {
+        const int st = j % kStages;
+        if (j >= kStages && !mbar_wait(&v_empty[st], ((j / kStages) & 1) ^ 1, &abort_flag)) break;
+        mbar_arrive_expect_tx(&v_full[st], L::kTileBytes);
+        load_tile(smem + L::kV + st * L::kTileBytes, &tmV, &v_full[st], D, j * kBlockN, bh);
+        ++issued;
       }
+      for (int j = max(0, issued - kStages); j < issued; ++j)
+        mbar_wait_drain(&v_full[j % kStages], (j / kStages) & 1);
     }
   } else if (warp == 1) {
-    // -------------------------------------------------------------- MMA issuer
+    // ------------------------------------------------------ MMA issuer: S = Q K^T
+    // S_j goes to buffer j % 3 once P_{j-3} (which lived there) has been used.
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16(kBlockM, kBlockN, false, false);
-      constexpr uint32_t idesc_o = idesc_bf16(kBlockM, D, false, true);
       const uint32_t q_addr = smem_u32(smem + L::kQ);
       bool ok = mbar_wait(&q_full, 0, &abort_flag);
-      auto issue_pv = [&](int jj) -> bool {
-        const int sb = jj & 1, st = jj % kStages;
-        if (!mbar_wait(&p_ready[sb], (jj >> 1) & 1, &abort_flag)) return false;
-        if (!mbar_wait(&v_full[st], (jj / kStages) & 1, &abort_flag)) return false;
-        tc_fence_after();
-        const uint32_t v_addr = smem_u32(smem + L::kV + st * L::kTileBytes);
-#pragma unroll
-        for (int kk = 0; kk < kBlockN / 16; ++kk) {
-          const uint64_t bdesc = sdesc_sw128(v_addr + kk * 2048, L::kSubBytes, 1024);
-          mma_ts(tmem_O, tmem + sb * 128 + kk * 8, bdesc, idesc_o, (jj > 0 || kk > 0) ? 1u : 0u);
-        }
-        mma_commit(&v_empty[st]);
-        mma_commit(&o_done);
-        return true;
-      };
       for (int j = 0; ok && j < n_ktiles; ++j) {
-        const int st = j % kStages, sb = j & 1;
-        if (!mbar_wait(&k_full[st], (j / kStages) & 1, &abort_flag)) {
-          ok = false;
-          break;
-        }
+        const int st = j % kStages, sb = j % kSBuf;
+        if (j >= kSBuf && !mbar_wait(&pv_done[sb], ((j / kSBuf) - 1) & 1, &abort_flag)) { ok = false; break; }
+        if (!mbar_wait(&k_full[st], (j / kStages) & 1, &abort_flag)) { ok = false; break; }
         tc_fence_after();
         const uint32_t k_addr = smem_u32(smem + L::kK + st * L::kTileBytes);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk / 4) * L::kSubBytes + (kk % 4) * 32;
-          const uint64_t adesc = sdesc_sw128(q_addr + off, 16, 1024);
-          const uint64_t bdesc = sdesc_sw128(k_addr + off, 16, 1024);
-          mma_ss(tmem + sb * 128, adesc, bdesc, idesc_s, kk > 0 ? 1u : 0u);
+          mma_ss(tmem + sb * 128, sdesc_sw128(q_addr + off, 16, 1024), sdesc_sw128(k_addr + off, 16, 1024),
+                 idesc_s, kk > 0 ? 1u : 0u);
         }
         mma_commit(&s_full[sb]);
         mma_commit(&k_empty[st]);
-        if (j > 0 && !issue_pv(j - 1)) ok = false;
       }
-      if (ok) issue_pv(n_ktiles - 1);
       // teardown: all issued MMAs finish before TMEM is released
-      mma_commit(&drain);
-      mbar_wait_drain(&drain, 0);
+      mma_commit(&drain_s);
+      mbar_wait_drain(&drain_s, 0);
+    }
+  } else if (warp == 3) {
+    // ---------------------------------------------------- MMA issuer: O += P V
+    // A second issuing thread, so the tensor pipe always has one of the two
+    // streams queued while the other waits on its barriers.
+    if (lane == 0) {
+      constexpr uint32_t idesc_o = idesc_bf16(kBlockM, D, false, true);
+      bool ok = true;
+      for (int j = 0; ok && j < n_ktiles; ++j) {
+        const int st = j % kStages, sb = j % kSBuf;
+        if (!mbar_wait(&p_ready[sb], (j / kSBuf) & 1, &abort_flag)) { ok = false; break; }
+        if (!mbar_wait(&v_full[st], (j / kStages) & 1, &abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t v_addr = smem_u32(smem + L::kV + st * L::kTileBytes);
+#pragma unroll
+        for (int kk = 0; kk < kBlockN / 16; ++kk)
+          mma_ts(tmem_O, tmem + sb * 128 + kk * 8, sdesc_sw128(v_addr + kk * 2048, L::kSubBytes, 1024), idesc_o,
+                 (j > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&v_empty[st]);
+        mma_commit(&pv_done[sb]);
+      }
+      mma_commit(&drain_pv);
+      mbar_wait_drain(&drain_pv, 0);
     }
   } else if (warp >= 4) {
     // ----------------------------------------------------------------- softmax
@@ -200,8 +214,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     float m_used = -INFINITY, l_sum = 0.f;
     bool ok = true;
     for (int j = 0; j < n_ktiles; ++j) {
-      const int sb = j & 1;
-      if (!mbar_wait_warp(&s_full[sb], (j >> 1) & 1, &abort_flag)) {
+      const int sb = j % kSBuf;
+      if (!mbar_wait_warp(&s_full[sb], (j / kSBuf) & 1, &abort_flag)) {
         ok = false;
         break;
       }
@@ -234,8 +248,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else {
         const bool need = (mx - m_used) * scale_log2 > kRescaleLog2;
         if (__any_sync(0xffffffffu, need)) {
-          // O must hold P_{j-1} V_{j-1} before it is rescaled
-          if (!mbar_wait_warp(&o_done, (j - 1) & 1, &abort_flag)) {
+          // O must hold P_{j-1} V_{j-1} before it is rescaled. Wait on that
+          // product's own buffer barrier: its previous phase (P_{j-4} V_{j-4})
+          // is known complete because S_{j-1} was only issued after it, so
+          // the parity cannot be matched by a stale phase.
+          if (!mbar_wait_warp(&pv_done[(j - 1) % kSBuf], ((j - 1) / kSBuf) & 1, &abort_flag)) {
             ok = false;
             break;
           }
@@ -294,7 +311,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(&p_ready[sb]);
     }
     // ---------------------------------------------------------------- epilogue
-    if (ok && mbar_wait_warp(&o_done, (n_ktiles - 1) & 1, &abort_flag)) {
+    // the last P V (and, issued in order before it, every other one) is done
+    if (ok && mbar_wait_warp(&pv_done[(n_ktiles - 1) % kSBuf], ((n_ktiles - 1) / kSBuf) & 1, &abort_flag)) {
       tc_fence_after();
       const float inv_l = 1.f / l_sum;
       const bool store = row < N;
