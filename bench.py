@@ -32,6 +32,25 @@ if ROOT not in sys.path:
 
 METRIC = "attention fwd/bwd TFLOP/s at B8 H32 N4096 d128 bf16; % of BF16 tensor peak"
 
+# DRAM bytes per launch of the dominant kernel at the headline size, from the
+# ncu capture summarised in profiles/ncu_full_fwd_dkdv_dq_bf16_B2_H32_N4096_d128.md
+# (a quarter-size case, scaled by the number of heads). Only valid for the
+# kernel source it was measured on: reported as null once that file changes.
+MEASURED_TRAFFIC = {"workload": "bf16_B8_H32_N4096_d128", "kernel": "bwd_dkdv_kernel<128>",
+                    "bytes": 4 * (270.698752e6 + 104.478720e6),
+                    "source": "exact_attention_97_gb300/csrc/bwd_bf16.cu", "sha256_16": "67de7b080a14fcc4"}
+
+
+def _measured_traffic(kernel: str, workload: str):
+    import hashlib
+    m = MEASURED_TRAFFIC
+    if kernel != m["kernel"] or workload != m["workload"]:
+        return None
+    with open(os.path.join(ROOT, m["source"]), "rb") as f:
+        if hashlib.sha256(f.read()).hexdigest()[:16] != m["sha256_16"]:
+            return None
+    return m["bytes"]
+
 
 def _peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -182,11 +201,20 @@ def run_ours(args, w):
     stream = torch.cuda.current_stream()
 
     launches = [0]
+    marks = []  # (fwd start, bwd start, bwd end) events per timed step, on the launch stream
 
-    def step():
+    def step(mark=False):
+        if mark:
+            m = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+            m[0].record(stream)
         fa.attention_forward(q, k, v, w.scale, w.causal, out=o, lse=lse)
         n = fa.fa_last_launch_count()
+        if mark:
+            m[1].record(stream)
         fa.attention_backward(q, k, v, o, lse, dO, w.scale, w.causal, workspace=ws, grads=(dq, dk, dv))
+        if mark:
+            m[2].record(stream)
+            marks.append(m)
         launches[0] += n + fa.fa_last_launch_count()
 
     for _ in range(args.warmup):
@@ -195,8 +223,9 @@ def run_ours(args, w):
     if fa.fa_device_status() != 0:
         raise RuntimeError("kernel pipeline timeout during warm-up")
 
-    # per-kernel events: pair 2s = forward kernel of step s, 2s+1 = backward main pass
-    pairs = 2 * args.steps
+    # per-kernel events recorded by the library around each tensor-core kernel:
+    # per step, pair 3s = forward, 3s+1 = dK/dV pass, 3s+2 = dQ pass
+    pairs = 3 * args.steps
     evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * pairs)]
     for e in evs:
         e.record(stream)  # creates the underlying CUDA event
@@ -213,7 +242,7 @@ def run_ours(args, w):
     launches[0] = 0
     start.record(stream)
     for _ in range(args.steps):
-        step()
+        step(mark=True)
     stop.record(stream)
     torch.cuda.synchronize()
     fa.fa_set_kernel_timing(None, 0)
@@ -223,8 +252,14 @@ def run_ours(args, w):
     if fa.fa_device_status() != 0:
         raise RuntimeError("kernel pipeline timeout in the timed region")
     ms = start.elapsed_time(stop)
-    fwd_ms = [evs[4 * s].elapsed_time(evs[4 * s + 1]) for s in range(args.steps)]
-    bwd_ms = [evs[4 * s + 2].elapsed_time(evs[4 * s + 3]) for s in range(args.steps)]
+
+    def pair_ms(i):
+        return statistics.mean(evs[2 * (3 * s + i)].elapsed_time(evs[2 * (3 * s + i) + 1])
+                               for s in range(args.steps))
+
+    k_fwd, k_dkdv, k_dq = pair_ms(0), pair_ms(1), pair_ms(2)
+    fwd_call = statistics.mean(m[0].elapsed_time(m[1]) for m in marks)
+    bwd_call = statistics.mean(m[1].elapsed_time(m[2]) for m in marks)
     if world > 1:
         t = torch.tensor([ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -233,15 +268,30 @@ def run_ours(args, w):
     flops_step = w.flops_fwd() + w.flops_bwd()
     value = flops_step * world * args.steps / (ms * 1e-3) / 1e12
     peaks = _peaks()
-    fwd_avg, bwd_avg = statistics.mean(fwd_ms), statistics.mean(bwd_ms)
-    fwd_tf = w.flops_fwd() / (fwd_avg * 1e-3) / 1e12
-    bwd_tf = w.flops_bwd() / (bwd_avg * 1e-3) / 1e12
-    dominant = "bwd_main" if bwd_avg * 1 >= fwd_avg else "fwd"
-    achieved = bwd_tf if dominant == "bwd_main" else fwd_tf
-    roofline = {"bound": "tensor", "kernel": "bwd_main_kernel<128>" if dominant == "bwd_main" else "fwd_bf16_kernel<128>",
-                "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": achieved / peaks["bf16_tflops"], "traffic": args.traffic,
-                "peak_source": peaks["source"] + " burst bf16 (cuBLAS)"}
+    peak = peaks["bf16_tflops"]
+    F = w.flops_fwd()  # two contractions (QK^T, PV) over the pairs in the mask
+
+    def tf(flops, t_ms):
+        return flops / (t_ms * 1e-3) / 1e12
+
+    # Algorithmic flops per kernel: the backward's five contractions are split
+    # as S, dP, dV, dK in the dK/dV pass (2F) and dQ in the dQ pass (F/2); the
+    # dQ pass also recomputes S and dP (executed 3F/2).
+    kernels = {
+        "fwd_bf16_kernel": {"ms": k_fwd, "algo_tflops": tf(F, k_fwd), "frac": tf(F, k_fwd) / peak},
+        "bwd_dkdv_kernel": {"ms": k_dkdv, "algo_tflops": tf(2 * F, k_dkdv), "frac": tf(2 * F, k_dkdv) / peak},
+        "bwd_dq_kernel": {"ms": k_dq, "algo_tflops": tf(0.5 * F, k_dq), "executed_tflops": tf(1.5 * F, k_dq),
+                          "executed_frac": tf(1.5 * F, k_dq) / peak},
+    }
+    dom = max(("fwd_bf16_kernel", F, k_fwd), ("bwd_dkdv_kernel", 2 * F, k_dkdv),
+              ("bwd_dq_kernel", 0.5 * F, k_dq), key=lambda x: x[2])
+    achieved = tf(dom[1], dom[2])
+    roofline = {"bound": "tensor", "kernel": f"{dom[0]}<{w.d}>", "achieved": achieved, "peak": peak,
+                "unit": "TFLOP/s", "frac": achieved / peak,
+                "traffic": args.traffic if args.traffic is not None else _measured_traffic(f"{dom[0]}<{w.d}>", w.name),
+                "peak_source": peaks["source"] + " burst bf16 (cuBLAS), of measured"}
+    fwd_tf = tf(w.flops_fwd(), fwd_call)
+    bwd_tf = tf(w.flops_bwd(), bwd_call)
 
     # end to end through the public API: pinned host inputs in, results back to pinned host
     e2e = None
@@ -292,9 +342,10 @@ def run_ours(args, w):
                        "l2": "inputs larger than L2 (each of Q, K, V, dO is "
                              f"{q.numel() * 2 / 1e6:.0f} MB vs 129 MB L2)",
                        "parallelism": f"{world} independent replica(s), no collective"},
-            "pct_of_peak": value / (peaks["bf16_tflops"] * world) * 100.0,
-            "fwd": {"ms": fwd_avg, "tflops": fwd_tf, "frac": fwd_tf / peaks["bf16_tflops"]},
-            "bwd_main": {"ms": bwd_avg, "tflops": bwd_tf, "frac": bwd_tf / peaks["bf16_tflops"]},
+            "pct_of_peak": value / (peak * world) * 100.0,
+            "fwd": {"ms": fwd_call, "tflops": fwd_tf, "frac": fwd_tf / peak},
+            "bwd": {"ms": bwd_call, "tflops": bwd_tf, "frac": bwd_tf / peak},
+            "kernels": kernels,
             "roofline": roofline,
             "cpu_baseline": base,
             "e2e": e2e,

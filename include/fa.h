@@ -143,13 +143,14 @@ int fa_last_launch_count(void);
 /*
  * Per-kernel timing for benchmarks (no counterpart on the pages; it only
  * measures). `events` holds 2*n_pairs cudaEvent_t handles created by the
- * caller with timing enabled. After this call, each fa_fwd / fa_bwd on this
- * host thread records events[2i] on its stream just before its main kernel
- * (the forward kernel, or the backward's main pass) and events[2i+1] just
- * after it, for i = 0, 1, ... up to n_pairs - 1; later calls record nothing.
- * Pass NULL / 0 to switch it off. Returns FA_ERR_ARG for n_pairs < 0.
- * Returns the number of pairs used so far when called with n_pairs == -1
- * (events ignored).
+ * caller with timing enabled. After this call, every tensor-core kernel that
+ * fa_fwd / fa_bwd launch on this host thread is bracketed by the next free
+ * pair: events[2i] is recorded on the call's stream just before the kernel
+ * and events[2i+1] just after it. fa_fwd uses one pair (the forward kernel),
+ * fa_bwd two (the dK/dV pass, then the dQ pass); once all n_pairs are used,
+ * nothing more is recorded. Pass NULL / 0 to switch it off. Returns
+ * FA_ERR_ARG for n_pairs < -1, and the number of pairs used so far when
+ * called with n_pairs == -1 (events ignored).
  */
 int fa_set_kernel_timing(void **events, int n_pairs);
 
