@@ -47,10 +47,6 @@ constexpr int kStages = 3;     // K and V ring depth
 constexpr int kSBuf = 3;       // S buffers in TMEM (3 x 128 columns, O after them)
 constexpr int kThreads = 256;  // 8 warps
 constexpr float kRescaleLog2 = 8.0f;  // move the running max only past 2^8
-#ifndef FA_FWD_POLY_PAIRS
-#define FA_FWD_POLY_PAIRS 0
-#endif
-constexpr int kPolyPairs = FA_FWD_POLY_PAIRS;  // of every 8 exp pairs, this many on the FMA pipe
 constexpr float kLn2 = 0.69314718055994531f;
 
 template <int D>
@@ -272,8 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      // P = 2^(s*c - m*c), two columns at a time; in every group of 8 pairs the
-      // first kPolyPairs go through the FMA-pipe polynomial, the rest through ex2
+      // P = 2^(s*c - m*c), two columns at a time
       const float neg = -m_used * scale_log2;
       const uint64_t cc = f2_pack(scale_log2, scale_log2), nn = f2_pack(neg, neg);
       uint64_t acc0 = 0, acc1 = 0, acc2 = 0, acc3 = 0;  // packed partial row sums (+0.0f pairs)
@@ -281,14 +276,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int u = 0; u < kBlockN / 2; ++u) {
         const uint64_t x2 = f2_fma(f2_pack(__uint_as_float(sr[2 * u]), __uint_as_float(sr[2 * u + 1])), cc, nn);
-        uint64_t p2;
-        if ((u & 7) < kPolyPairs) {
-          p2 = ex2_poly2(x2);
-        } else {
-          float x0, x1;
-          f2_unpack(x2, x0, x1);
-          p2 = f2_pack(ex2_approx(x0), ex2_approx(x1));
-        }
+        float x0, x1;
+        f2_unpack(x2, x0, x1);
+        const uint64_t p2 = f2_pack(ex2_approx(x0), ex2_approx(x1));
         switch (u & 3) {
           case 0: acc0 = f2_add(acc0, p2); break;
           case 1: acc1 = f2_add(acc1, p2); break;

@@ -349,32 +349,6 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
-// 2^x on the FMA pipe, for x in [-125, 64]: 2^x = 2^n * 2^f with n = round(x)
-// (taken from the low mantissa bits of x + 1.5*2^23) and f = x - n in
-// [-1/2, 1/2]; 2^f is the degree-3 polynomial with the least maximum relative
-// error on that interval (Remez exchange, exp2_poly_fit.py; 7.5e-5 relative,
-// well inside bf16's 2^-9), and 2^n is added to the result's exponent field.
-// Used for a share of the softmax exponentials so that they do not all queue
-// on the special-function unit. Works on two values at once.
-__device__ __forceinline__ uint64_t ex2_poly2(uint64_t x2) {
-  constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
-  float x0, x1;
-  f2_unpack(x2, x0, x1);
-  x2 = f2_pack(fmaxf(x0, -125.f), fmaxf(x1, -125.f));
-  const uint64_t t2 = f2_add(x2, f2_pack(kMagic, kMagic));
-  const uint64_t n2 = f2_add(t2, f2_pack(-kMagic, -kMagic));
-  const uint64_t f2 = f2_fma(n2, f2_pack(-1.f, -1.f), x2);
-  uint64_t p2 = f2_fma(f2_pack(0.0551716685f, 0.0551716685f), f2, f2_pack(0.242611125f, 0.242611125f));
-  p2 = f2_fma(p2, f2, f2_pack(0.693260968f, 0.693260968f));
-  p2 = f2_fma(p2, f2, f2_pack(0.999928057f, 0.999928057f));
-  float p0, p1, t0, t1;
-  f2_unpack(p2, p0, p1);
-  f2_unpack(t2, t0, t1);
-  const uint32_t r0 = __float_as_uint(p0) + (__float_as_uint(t0) << 23);
-  const uint32_t r1 = __float_as_uint(p1) + (__float_as_uint(t1) << 23);
-  return f2_pack(__uint_as_float(r0), __uint_as_float(r1));
-}
-
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
