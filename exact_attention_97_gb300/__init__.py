@@ -15,12 +15,13 @@ from __future__ import annotations
 
 import math
 
-from ._lib import (FA_BF16, FA_F32, FAError, fa_bwd, fa_bwd_f32, fa_bwd_workspace_size,
-                   fa_device_status, fa_fwd, fa_fwd_f32, fa_last_launch_count,
-                   fa_set_kernel_timing, fa_status_string, lib_path, load)
+from ._lib import (FA_BF16, FA_F16, FA_F32, FAError, fa_bwd, fa_bwd_f16, fa_bwd_f32,
+                   fa_bwd_workspace_size, fa_device_status, fa_fwd, fa_fwd_f16, fa_fwd_f32,
+                   fa_last_launch_count, fa_set_kernel_timing, fa_status_string, lib_path, load)
 
 __all__ = [
-    "FA_BF16", "FA_F32", "FAError", "fa_fwd", "fa_bwd", "fa_fwd_f32", "fa_bwd_f32",
+    "FA_BF16", "FA_F16", "FA_F32", "FAError", "fa_fwd", "fa_bwd", "fa_fwd_f16", "fa_bwd_f16",
+    "fa_fwd_f32", "fa_bwd_f32",
     "fa_bwd_workspace_size", "fa_status_string", "fa_device_status", "fa_last_launch_count",
     "fa_set_kernel_timing",
     "attention_forward", "attention_backward", "lib_path", "load",
@@ -50,16 +51,16 @@ def _stream_handle(stream):
 
 
 def attention_forward(q, k, v, scale=None, causal=False, out=None, lse=None, stream=None):
-    """(O, L) for [B, H, N, d] CUDA tensors q, k, v (all bf16 or all float32).
+    """(O, L) for [B, H, N, d] CUDA tensors q, k, v (all bf16, all f16 or all float32).
 
-    bf16 needs d in {64, 128}; float32 takes 1 <= d <= 128. L is float32
+    bf16 and f16 need d in {64, 128}; float32 takes 1 <= d <= 128. L is float32
     [B, H, N], the natural-log log-sum-exp of the scaled scores.
     """
     torch = _torch()
     B, H, N, d = q.shape
     dt = q.dtype
-    if dt not in (torch.bfloat16, torch.float32):
-        raise ValueError("q must be bfloat16 or float32")
+    if dt not in (torch.bfloat16, torch.float16, torch.float32):
+        raise ValueError("q must be bfloat16, float16 or float32")
     for name, t in (("q", q), ("k", k), ("v", v)):
         _check(name, t, (B, H, N, d), dt)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
@@ -68,7 +69,7 @@ def attention_forward(q, k, v, scale=None, causal=False, out=None, lse=None, str
         lse = torch.empty((B, H, N), device=q.device, dtype=torch.float32) if lse is None else lse
         _check("out", o, (B, H, N, d), dt)
         _check("lse", lse, (B, H, N), torch.float32)
-        fn = fa_fwd if dt == torch.bfloat16 else fa_fwd_f32
+        fn = {torch.bfloat16: fa_fwd, torch.float16: fa_fwd_f16, torch.float32: fa_fwd_f32}[dt]
         fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N, d, scale,
            int(bool(causal)), _stream_handle(stream))
     return o, lse
@@ -84,7 +85,7 @@ def attention_backward(q, k, v, o, lse, dO, scale=None, causal=False, workspace=
         _check(name, t, (B, H, N, d), dt)
     _check("lse", lse, (B, H, N), torch.float32)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    kind = FA_BF16 if dt == torch.bfloat16 else FA_F32
+    kind = {torch.bfloat16: FA_BF16, torch.float16: FA_F16, torch.float32: FA_F32}[dt]
     need = fa_bwd_workspace_size(B, H, N, d, kind)
     with torch.cuda.device(q.device):
         if workspace is None:
@@ -93,7 +94,7 @@ def attention_backward(q, k, v, o, lse, dO, scale=None, causal=False, workspace=
             raise ValueError(f"workspace needs {need} bytes")
         dq, dk, dv = grads if grads is not None else (torch.empty_like(q), torch.empty_like(k),
                                                       torch.empty_like(v))
-        fn = fa_bwd if kind == FA_BF16 else fa_bwd_f32
+        fn = {FA_BF16: fa_bwd, FA_F16: fa_bwd_f16, FA_F32: fa_bwd_f32}[kind]
         fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), dO.data_ptr(),
            dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d, scale, int(bool(causal)),
            workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream_handle(stream))

@@ -19,6 +19,8 @@ c_int, c_float, c_size_t, c_void_p = ctypes.c_int, ctypes.c_float, ctypes.c_size
 _SIGNATURES = {
     "fa_fwd": (c_int, [c_void_p] * 5 + [c_int] * 4 + [c_float, c_int, c_void_p]),
     "fa_bwd": (c_int, [c_void_p] * 9 + [c_int] * 4 + [c_float, c_int, c_void_p, c_size_t, c_void_p]),
+    "fa_fwd_f16": (c_int, [c_void_p] * 5 + [c_int] * 4 + [c_float, c_int, c_void_p]),
+    "fa_bwd_f16": (c_int, [c_void_p] * 9 + [c_int] * 4 + [c_float, c_int, c_void_p, c_size_t, c_void_p]),
     "fa_fwd_f32": (c_int, [c_void_p] * 5 + [c_int] * 4 + [c_float, c_int, c_void_p]),
     "fa_bwd_f32": (c_int, [c_void_p] * 9 + [c_int] * 4 + [c_float, c_int, c_void_p, c_size_t, c_void_p]),
     "fa_bwd_workspace_size": (c_size_t, [c_int] * 5),
@@ -30,7 +32,7 @@ _SIGNATURES = {
     "fa_bwd_static_scratch": (c_int, [c_void_p] * 9 + [c_int] * 4 + [c_float, c_int, c_void_p]),
 }
 
-FA_BF16, FA_F32 = 0, 1
+FA_BF16, FA_F32, FA_F16 = 0, 1, 2
 STATUS = {0: "FA_OK", 1: "FA_ERR_NULL", 2: "FA_ERR_SHAPE", 3: "FA_ERR_UNSUPPORTED",
           4: "FA_ERR_ALIGN", 5: "FA_ERR_WORKSPACE", 6: "FA_ERR_LAUNCH", 7: "FA_ERR_TIMEOUT",
           8: "FA_ERR_ARCH", 9: "FA_ERR_ARG"}
@@ -79,6 +81,15 @@ def fa_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, stream):
 
 def fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, scale, causal, workspace, workspace_bytes, stream):
     return _call("fa_bwd", q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, float(scale), int(causal),
+                 workspace, workspace_bytes, stream)
+
+
+def fa_fwd_f16(q, k, v, o, lse, B, H, N, d, scale, causal, stream):
+    return _call("fa_fwd_f16", q, k, v, o, lse, B, H, N, d, float(scale), int(causal), stream)
+
+
+def fa_bwd_f16(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, scale, causal, workspace, workspace_bytes, stream):
+    return _call("fa_bwd_f16", q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, float(scale), int(causal),
                  workspace, workspace_bytes, stream)
 
 

@@ -88,16 +88,18 @@ int get_encoder() {
   return g_encode ? kOk : kErrLaunch;
 }
 
-// 3-D bf16 map over a contiguous [BH][N][d] tensor: dims {d, N, BH}, box
-// {64, 128, 1}, 128-byte swizzle; rows past N (inside a head) read as zero.
-int make_map(CUtensorMap *map, const void *ptr, int BH, int N, int d) {
+// 3-D map over a contiguous [BH][N][d] 16-bit tensor (bf16, or f16 when
+// `f16`): dims {d, N, BH}, box {64, 128, 1}, 128-byte swizzle; rows past N
+// (inside a head) read as zero.
+int make_map(CUtensorMap *map, const void *ptr, int BH, int N, int d, bool f16) {
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
                         static_cast<cuuint64_t>(BH)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
                            static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(d) * 2};
   cuuint32_t box[3] = {64, 128, 1};
   cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims,
+  CUresult r = g_encode(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                        const_cast<void *>(ptr), dims,
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -194,7 +196,8 @@ int fa_last_cuda_error(void) { return t_last_cuda_error; }
 int fa_last_launch_count(void) { return t_last_launches; }
 
 size_t fa_bwd_workspace_size(int B, int H, int N, int d, int dtype) {
-  if (dtype != FA_BF16 && dtype != FA_F32) return 0;
+  if (dtype != FA_BF16 && dtype != FA_F32 && dtype != FA_F16) return 0;
+  if (dtype == FA_F16) dtype = FA_BF16;  // same layout
   return ws_bytes(B, H, N, d, dtype);
 }
 
@@ -213,8 +216,13 @@ int fa_device_status(void) {
   return v;
 }
 
-int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int N,
-           int d, float scale, int causal, fa_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Shared body of fa_fwd / fa_fwd_f16.
+int fwd16(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int N, int d,
+          float scale, int causal, fa_stream_t stream, bool f16) {
   if (!q || !k || !v || !o || !lse) return FA_ERR_NULL;
   int st = check_shape(B, H, N, d, 128);
   if (st != kOk) return st;
@@ -227,21 +235,21 @@ int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int
   if ((st = get_encoder()) != kOk) return st;
   CUtensorMap tq, tk, tv;
   const int BH = B * H;
-  if ((st = make_map(&tq, q, BH, N, d)) != kOk || (st = make_map(&tk, k, BH, N, d)) != kOk ||
-      (st = make_map(&tv, v, BH, N, d)) != kOk)
+  if ((st = make_map(&tq, q, BH, N, d, f16)) != kOk || (st = make_map(&tk, k, BH, N, d, f16)) != kOk ||
+      (st = make_map(&tv, v, BH, N, d, f16)) != kOk)
     return st;
   int launches = 0;
-  cudaError_t e = launch_fwd_bf16(tq, tk, tv, o, lse, B, H, N, d, scale, causal ? 1 : 0,
-                                  dev->status, dev->num_sms, reinterpret_cast<cudaStream_t>(stream),
-                                  &launches);
+  cudaError_t e = launch_fwd_16(tq, tk, tv, o, lse, B, H, N, d, scale, causal ? 1 : 0, f16, dev->status,
+                                dev->num_sms, reinterpret_cast<cudaStream_t>(stream), &launches);
   if (e != cudaSuccess) return record(e);
   t_last_launches = launches;
   return FA_OK;
 }
 
-int fa_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
-           const void *dO, void *dq, void *dk, void *dv, int B, int H, int N, int d, float scale,
-           int causal, void *workspace, size_t workspace_bytes, fa_stream_t stream) {
+// Shared body of fa_bwd / fa_bwd_f16.
+int bwd16(const void *q, const void *k, const void *v, const void *o, const float *lse, const void *dO,
+          void *dq, void *dk, void *dv, int B, int H, int N, int d, float scale, int causal, void *workspace,
+          size_t workspace_bytes, fa_stream_t stream, bool f16) {
   if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return FA_ERR_NULL;
   int st = check_shape(B, H, N, d, 128);
   if (st != kOk) return st;
@@ -259,20 +267,46 @@ int fa_bwd(const void *q, const void *k, const void *v, const void *o, const flo
   if ((st = get_encoder()) != kOk) return st;
   CUtensorMap tq, tk, tv, tdo;
   const int BH = B * H;
-  if ((st = make_map(&tq, q, BH, N, d)) != kOk || (st = make_map(&tk, k, BH, N, d)) != kOk ||
-      (st = make_map(&tv, v, BH, N, d)) != kOk || (st = make_map(&tdo, dO, BH, N, d)) != kOk)
+  if ((st = make_map(&tq, q, BH, N, d, f16)) != kOk || (st = make_map(&tk, k, BH, N, d, f16)) != kOk ||
+      (st = make_map(&tv, v, BH, N, d, f16)) != kOk || (st = make_map(&tdo, dO, BH, N, d, f16)) != kOk)
     return st;
   const BwdWorkspace w = ws_layout(B, H, N, d, FA_BF16);
   char *ws = static_cast<char *>(workspace);
   int launches = 0;
-  cudaError_t e = launch_bwd_bf16(tq, tk, tv, tdo, o, dO, lse, dq, dk, dv,
-                                  reinterpret_cast<float *>(ws + w.lp),
-                                  reinterpret_cast<float *>(ws + w.dp), B, H, N, d, scale,
-                                  causal ? 1 : 0, dev->status, dev->num_sms,
-                                  reinterpret_cast<cudaStream_t>(stream), &launches);
+  cudaError_t e = launch_bwd_16(tq, tk, tv, tdo, o, dO, lse, dq, dk, dv, reinterpret_cast<float *>(ws + w.lp),
+                                reinterpret_cast<float *>(ws + w.dp), B, H, N, d, scale, causal ? 1 : 0, f16,
+                                dev->status, dev->num_sms, reinterpret_cast<cudaStream_t>(stream), &launches);
   if (e != cudaSuccess) return record(e);
   t_last_launches = launches;
   return FA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int N, int d,
+           float scale, int causal, fa_stream_t stream) {
+  return fwd16(q, k, v, o, lse, B, H, N, d, scale, causal, stream, false);
+}
+
+int fa_fwd_f16(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int N, int d,
+               float scale, int causal, fa_stream_t stream) {
+  return fwd16(q, k, v, o, lse, B, H, N, d, scale, causal, stream, true);
+}
+
+int fa_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse, const void *dO,
+           void *dq, void *dk, void *dv, int B, int H, int N, int d, float scale, int causal, void *workspace,
+           size_t workspace_bytes, fa_stream_t stream) {
+  return bwd16(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, scale, causal, workspace, workspace_bytes, stream,
+               false);
+}
+
+int fa_bwd_f16(const void *q, const void *k, const void *v, const void *o, const float *lse, const void *dO,
+               void *dq, void *dk, void *dv, int B, int H, int N, int d, float scale, int causal,
+               void *workspace, size_t workspace_bytes, fa_stream_t stream) {
+  return bwd16(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, scale, causal, workspace, workspace_bytes, stream,
+               true);
 }
 
 int fa_fwd_f32(const float *q, const float *k, const float *v, float *o, float *lse, int B, int H,
@@ -380,18 +414,16 @@ extern "C" int fa_bwd_static_scratch(const void *q, const void *k, const void *v
   if ((st = get_encoder()) != kOk) return st;
   CUtensorMap tq, tk, tv, tdo;
   const int BH = B * H;
-  if ((st = make_map(&tq, q, BH, N, d)) != kOk || (st = make_map(&tk, k, BH, N, d)) != kOk ||
-      (st = make_map(&tv, v, BH, N, d)) != kOk || (st = make_map(&tdo, dO, BH, N, d)) != kOk)
+  if ((st = make_map(&tq, q, BH, N, d, false)) != kOk || (st = make_map(&tk, k, BH, N, d, false)) != kOk ||
+      (st = make_map(&tv, v, BH, N, d, false)) != kOk || (st = make_map(&tdo, dO, BH, N, d, false)) != kOk)
     return st;
   // The first kernel of the pass rewrites every scratch byte it later reads
   // (the L and D rows, padding included), so the previous call's contents
   // never leak into this one.
   int launches = 0;
-  cudaError_t e = launch_bwd_bf16(tq, tk, tv, tdo, o, dO, lse, dq, dk, dv,
-                                  reinterpret_cast<float *>(ws + w.lp),
-                                  reinterpret_cast<float *>(ws + w.dp), B, H, N, d, scale,
-                                  causal ? 1 : 0, dev->status, dev->num_sms,
-                                  reinterpret_cast<cudaStream_t>(stream), &launches);
+  cudaError_t e = launch_bwd_16(tq, tk, tv, tdo, o, dO, lse, dq, dk, dv, reinterpret_cast<float *>(ws + w.lp),
+                                reinterpret_cast<float *>(ws + w.dp), B, H, N, d, scale, causal ? 1 : 0, false,
+                                dev->status, dev->num_sms, reinterpret_cast<cudaStream_t>(stream), &launches);
   if (e != cudaSuccess) return record(e);
   t_last_launches = launches;
   return FA_OK;

@@ -1,4 +1,5 @@
-// bwd_bf16.cu -- exact attention backward on the sm_103a tensor cores.
+// bwd_tc.cu -- exact attention backward on the sm_103a tensor cores, for
+// 16-bit inputs (bf16 or f16; the element type is a template parameter).
 //
 // What it computes (pages): backward by recomputation, "Flash Attention
 // 原理与实现", section "Backward 的 Tiling 策略": the probabilities are rebuilt
@@ -19,12 +20,12 @@
 //   2. bwd_dkdv  one CTA per (batch*head, 128-key block); query tiles of 128
 //                rows stream through a TMA ring. Keys on the TMEM lanes:
 //                  S^T = K Q^T, dP^T = V dO^T          (TMEM)
-//                  dV += P^T dO   (P^T written over S^T as bf16, A from TMEM)
-//                  dK += dS^T Q   (dS^T written over dP^T as bf16, A from TMEM)
+//                  dV += P^T dO   (P^T written over S^T in 16 bits, A from TMEM)
+//                  dK += dS^T Q   (dS^T written over dP^T in 16 bits, A from TMEM)
 //   3. bwd_dq    one CTA per (batch*head, 128-row query tile); key blocks
 //                stream through a TMA ring. Queries on the TMEM lanes:
 //                  S = Q K^T (double-buffered), dP = dO V^T   (TMEM)
-//                  dQ += dS K     (dS read from TMEM as bf16)
+//                  dQ += dS K     (dS read from TMEM in 16 bits)
 // In both passes two warpgroups split the 128 columns of S and dP (64 each)
 // for the elementwise work; one warp loads, one thread issues the MMAs.
 #include <cuda_runtime.h>
@@ -46,16 +47,14 @@ __device__ __forceinline__ void load_rows(uint8_t *dst, const CUtensorMap *map, 
   for (int x = 0; x < D; x += 64) tma_load_3d(dst + (x / 64) * (kBlk * 128), map, bar, x, row, bh);
 }
 
-__device__ __forceinline__ float bf16lo(uint32_t v) { return __uint_as_float(v << 16); }
-__device__ __forceinline__ float bf16hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 
-// TMEM column of k-step kk (16 keys or queries) of a bf16 A operand that the
+// TMEM column of k-step kk (16 keys or queries) of a 16-bit A operand that the
 // two warpgroups wrote as packed pairs: warpgroup h (operand columns
 // 64h..64h+63) writes 32 columns at 64h, inside the 64 score columns it read.
 __device__ __forceinline__ uint32_t a_col(int kk) { return (kk >> 2) * 64 + (kk & 3) * 8; }
 
-// Stores 16 packed columns (32 bf16) of a row to global memory when `ok`.
-__device__ __forceinline__ void store_row32(__nv_bfloat16 *dst, const uint32_t (&pk)[16], bool ok) {
+// Stores 16 packed columns (32 elements) of a row to global memory when `ok`.
+__device__ __forceinline__ void store_row32(uint16_t *dst, const uint32_t (&pk)[16], bool ok) {
   if (!ok) return;
   uint4 *d4 = reinterpret_cast<uint4 *>(dst);
 #pragma unroll
@@ -67,9 +66,9 @@ __device__ __forceinline__ void store_row32(__nv_bfloat16 *dst, const uint32_t (
 //   Lp = -L * log2(e) (so the passes form p = 2^(s*c + Lp)), -inf past N;
 //   Dp = sum_c dO_ic O_ic, 0 past N.
 // One group of D/8 threads per row, 16-byte loads.
-template <int D>
-__global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16 *__restrict__ o,
-                                                       const __nv_bfloat16 *__restrict__ dO,
+template <int D, bool F16>
+__global__ void __launch_bounds__(256) bwd_prep_kernel(const uint16_t *__restrict__ o,
+                                                       const uint16_t *__restrict__ dO,
                                                        const float *__restrict__ lse,
                                                        float *__restrict__ Lp, float *__restrict__ Dp,
                                                        int N, int Np, int64_t prow_total) {
@@ -88,8 +87,8 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16 *__re
     const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
-      s = fmaf(bf16lo(av[t]), bf16lo(bv[t]), s);
-      s = fmaf(bf16hi(av[t]), bf16hi(bv[t]), s);
+      s = fmaf(Elt<F16>::lo(av[t]), Elt<F16>::lo(bv[t]), s);
+      s = fmaf(Elt<F16>::hi(av[t]), Elt<F16>::hi(bv[t]), s);
     }
   }
 #pragma unroll
@@ -105,7 +104,7 @@ template <int D>
 struct DkdvCfg {
   static constexpr int kStages = (D == 128) ? 2 : 3;
   static constexpr int kTileBytes = kBlk * D * 2;
-  static constexpr int kSubBytes = kBlk * 128;  // 128 rows x 64 bf16
+  static constexpr int kSubBytes = kBlk * 128;  // 128 rows x 64 16-bit elements
   static constexpr int kK = 0;
   static constexpr int kV = kK + kTileBytes;
   static constexpr int kQ = kV + kTileBytes;
@@ -115,14 +114,15 @@ struct DkdvCfg {
   static constexpr uint32_t tS = 0, tDP = 128, tDV = 256, tDK = 256 + D;  // TMEM columns
 };
 
-template <int D>
+template <int D, bool F16>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                     const float *__restrict__ Lp, const float *__restrict__ Dp,
-                    __nv_bfloat16 *__restrict__ dk, __nv_bfloat16 *__restrict__ dv, int N,
+                    uint16_t *__restrict__ dk, uint16_t *__restrict__ dv, int N,
                     float scale, float scale_log2, int causal, int *status) {
   using C = DkdvCfg<D>;
+  using E = Elt<F16>;
   constexpr int NST = C::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -198,8 +198,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // t+1 (so P_{t+1} is formed while the rest runs), dK_t, then dP of t+1
     // (which overwrites the columns dK_t reads, so it must come after).
     if (lane == 0) {
-      constexpr uint32_t id_s = idesc_bf16(kBlk, kBlk, false, false);  // S^T, dP^T
-      constexpr uint32_t id_kv = idesc_bf16(kBlk, D, false, true);     // dV, dK
+      constexpr uint32_t id_s = idesc_16(kBlk, kBlk, false, false, F16);  // S^T, dP^T
+      constexpr uint32_t id_kv = idesc_16(kBlk, D, false, true, F16);     // dV, dK
       const uint32_t k_addr = smem_u32(smem + C::kK), v_addr = smem_u32(smem + C::kV);
       auto issue_s = [&](int t) -> bool {  // S^T_t = K Q_t^T
         const int st = t % NST;
@@ -289,13 +289,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
           if (q0 + 2 * u < qmin) p0 = 0.f;
           if (q0 + 2 * u + 1 < qmin) p1 = 0.f;
-          pk[u] = pack_bf16x2(p0, p1);
+          pk[u] = E::pack(p0, p1);
         }
         tmem_st32(tmem + lane_addr + C::tS + h * 64, pk);
       }
       tc_fence_before();
       mbar_arrive(&p_ready);
-      // dS^T = P^T o (dP^T - D), with P as rounded for dV; written as bf16
+      // dS^T = P^T o (dP^T - D), with P as rounded for dV; written in 16 bits
       // pairs over the dP^T columns this warpgroup has just read
       if (!mbar_wait_warp(&dp_full, ph, &abort_flag)) { ok = false; break; }
       tc_fence_after();
@@ -306,9 +306,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int u = 0; u < 32; ++u) {
           const float2 dd = D2[u];
-          const float d0 = bf16lo(pk[u]) * (__uint_as_float(r[2 * u]) - dd.x);
-          const float d1 = bf16hi(pk[u]) * (__uint_as_float(r[2 * u + 1]) - dd.y);
-          ds[u] = pack_bf16x2(d0, d1);
+          const float d0 = E::lo(pk[u]) * (__uint_as_float(r[2 * u]) - dd.x);
+          const float d1 = E::hi(pk[u]) * (__uint_as_float(r[2 * u + 1]) - dd.y);
+          ds[u] = E::pack(d0, d1);
         }
         tmem_st32(tmem + lane_addr + C::tDP + h * 64, ds);
       }
@@ -320,7 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const uint32_t col = h ? C::tDK : C::tDV;
       const float mul = h ? scale : 1.f;
-      __nv_bfloat16 *out = (h ? dk : dv) + (static_cast<size_t>(bh) * N + key) * D;
+      uint16_t *out = (h ? dk : dv) + (static_cast<size_t>(bh) * N + key) * D;
 #pragma unroll 1
       for (int ch = 0; ch < D / 32; ++ch) {
         uint32_t r[32];
@@ -328,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t pk2[16];
 #pragma unroll
         for (int u = 0; u < 16; ++u)
-          pk2[u] = pack_bf16x2(__uint_as_float(r[2 * u]) * mul, __uint_as_float(r[2 * u + 1]) * mul);
+          pk2[u] = E::pack(__uint_as_float(r[2 * u]) * mul, __uint_as_float(r[2 * u + 1]) * mul);
         store_row32(out + ch * 32, pk2, key < N);
       }
     }
@@ -362,14 +362,15 @@ struct DqCfg {
   static constexpr uint32_t tS = 0, tDP = 256, tDQ = 384;  // S buffers at 0 and 128
 };
 
-template <int D>
+template <int D, bool F16>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                   const float *__restrict__ Lp, const float *__restrict__ Dp,
-                  __nv_bfloat16 *__restrict__ dq, int N, float scale, float scale_log2, int causal,
+                  uint16_t *__restrict__ dq, int N, float scale, float scale_log2, int causal,
                   int *status) {
   using C = DqCfg<D>;
+  using E = Elt<F16>;
   constexpr int KS = C::kKStages, VS = C::kVStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -453,8 +454,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // -------------------------------------------------------------- MMA issuer
     // Order: S_0, dP_0, S_1, then per key block j: dQ_j, dP_{j+1}, S_{j+2}.
     if (lane == 0) {
-      constexpr uint32_t id_s = idesc_bf16(kBlk, kBlk, false, false);  // S, dP
-      constexpr uint32_t id_q = idesc_bf16(kBlk, D, false, true);      // dQ
+      constexpr uint32_t id_s = idesc_16(kBlk, kBlk, false, false, F16);  // S, dP
+      constexpr uint32_t id_q = idesc_16(kBlk, D, false, true, F16);      // dQ
       const uint32_t q_addr = smem_u32(smem + C::kQ), do_addr = smem_u32(smem + C::kDO);
       auto issue_s = [&](int j) -> bool {  // S_j = Q K_j^T into buffer j&1
         const int st = j % KS;
@@ -491,7 +492,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int st = j % KS;
         if (!mbar_wait(&ds_ready, j & 1, &abort_flag)) { ok = false; break; }
         tc_fence_after();
-        // dQ += dS_j K_j : A = dS_j (bf16 in TMEM), B = K_j (MN-major)
+        // dQ += dS_j K_j : A = dS_j (16-bit in TMEM), B = K_j (MN-major)
         const uint32_t k_addr = smem_u32(smem + C::kK + st * C::kTileBytes);
 #pragma unroll
         for (int kk = 0; kk < kBlk / 16; ++kk)
@@ -551,7 +552,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int u = 0; u < 32; ++u) {
           const float d0 = p[2 * u] * (__uint_as_float(rr[2 * u]) - drow);
           const float d1 = p[2 * u + 1] * (__uint_as_float(rr[2 * u + 1]) - drow);
-          ds[u] = pack_bf16x2(d0, d1);
+          ds[u] = E::pack(d0, d1);
         }
         tmem_st32(tmem + lane_addr + sb, ds);  // over scores already read
       }
@@ -561,7 +562,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // epilogue: dQ = scale * accumulator; warpgroup h stores head columns [hD/2, hD/2 + D/2)
     if (ok && mbar_wait_warp(&done, 0, &abort_flag)) {
       tc_fence_after();
-      __nv_bfloat16 *out = dq + (static_cast<size_t>(bh) * N + q) * D + h * (D / 2);
+      uint16_t *out = dq + (static_cast<size_t>(bh) * N + q) * D + h * (D / 2);
 #pragma unroll 1
       for (int ch = 0; ch < D / 64; ++ch) {
         uint32_t rr[32];
@@ -569,7 +570,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t pk2[16];
 #pragma unroll
         for (int u = 0; u < 16; ++u)
-          pk2[u] = pack_bf16x2(__uint_as_float(rr[2 * u]) * scale, __uint_as_float(rr[2 * u + 1]) * scale);
+          pk2[u] = E::pack(__uint_as_float(rr[2 * u]) * scale, __uint_as_float(rr[2 * u + 1]) * scale);
         store_row32(out + ch * 32, pk2, q < N);
       }
     }
@@ -584,7 +585,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0 && abort_flag) atomicExch(status, kErrTimeout);
 }
 
-template <int D>
+template <int D, bool F16>
 cudaError_t launch(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtensorMap &tmV,
                    const CUtensorMap &tmdO, const void *o, const void *dO, const float *lse, void *dq,
                    void *dk, void *dv, float *Lp, float *Dp, int B, int H, int N, float scale, int causal,
@@ -595,15 +596,15 @@ cudaError_t launch(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtenso
   {
     const int64_t prows = static_cast<int64_t>(B) * H * Np;
     const int64_t threads = prows * (D / 8);
-    bwd_prep_kernel<D><<<static_cast<unsigned>((threads + 255) / 256), 256, 0, stream>>>(
-        static_cast<const __nv_bfloat16 *>(o), static_cast<const __nv_bfloat16 *>(dO), lse, Lp, Dp, N, Np,
+    bwd_prep_kernel<D, F16><<<static_cast<unsigned>((threads + 255) / 256), 256, 0, stream>>>(
+        static_cast<const uint16_t *>(o), static_cast<const uint16_t *>(dO), lse, Lp, Dp, N, Np,
         prows);
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const dim3 grid(n_tiles, B * H);
-  auto kdkdv = bwd_dkdv_kernel<D>;
-  auto kdq = bwd_dq_kernel<D>;
+  auto kdkdv = bwd_dkdv_kernel<D, F16>;
+  auto kdq = bwd_dq_kernel<D, F16>;
   if ((e = cudaFuncSetAttribute(kdkdv, cudaFuncAttributeMaxDynamicSharedMemorySize, DkdvCfg<D>::kAlloc)) !=
           cudaSuccess ||
       (e = cudaFuncSetAttribute(kdq, cudaFuncAttributeMaxDynamicSharedMemorySize, DqCfg<D>::kAlloc)) !=
@@ -611,14 +612,14 @@ cudaError_t launch(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtenso
     return e;
   timing_begin(stream);
   kdkdv<<<grid, kThreads, DkdvCfg<D>::kAlloc, stream>>>(tmQ, tmK, tmV, tmdO, Lp, Dp,
-                                                         static_cast<__nv_bfloat16 *>(dk),
-                                                         static_cast<__nv_bfloat16 *>(dv), N, scale,
+                                                         static_cast<uint16_t *>(dk),
+                                                         static_cast<uint16_t *>(dv), N, scale,
                                                          scale_log2, causal, status);
   timing_end(stream);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   timing_begin(stream);
   kdq<<<grid, kThreads, DqCfg<D>::kAlloc, stream>>>(tmQ, tmK, tmV, tmdO, Lp, Dp,
-                                                     static_cast<__nv_bfloat16 *>(dq), N, scale, scale_log2,
+                                                     static_cast<uint16_t *>(dq), N, scale, scale_log2,
                                                      causal, status);
   timing_end(stream);
   return cudaGetLastError();
@@ -626,18 +627,25 @@ cudaError_t launch(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtenso
 
 }  // namespace
 
-cudaError_t launch_bwd_bf16(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtensorMap &tmV,
-                            const CUtensorMap &tmdO, const void *o, const void *dO, const float *lse,
-                            void *dq, void *dk, void *dv, float *Lp, float *Dp, int B, int H, int N, int d,
-                            float scale, int causal, int *status, int num_sms, cudaStream_t stream,
-                            int *launches) {
+cudaError_t launch_bwd_16(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtensorMap &tmV,
+                          const CUtensorMap &tmdO, const void *o, const void *dO, const float *lse,
+                          void *dq, void *dk, void *dv, float *Lp, float *Dp, int B, int H, int N, int d,
+                          float scale, int causal, bool f16, int *status, int num_sms, cudaStream_t stream,
+                          int *launches) {
   (void)num_sms;
   *launches += 3;
+  if (f16) {
+    if (d == 64)
+      return launch<64, true>(tmQ, tmK, tmV, tmdO, o, dO, lse, dq, dk, dv, Lp, Dp, B, H, N, scale, causal,
+                              status, stream);
+    return launch<128, true>(tmQ, tmK, tmV, tmdO, o, dO, lse, dq, dk, dv, Lp, Dp, B, H, N, scale, causal,
+                             status, stream);
+  }
   if (d == 64)
-    return launch<64>(tmQ, tmK, tmV, tmdO, o, dO, lse, dq, dk, dv, Lp, Dp, B, H, N, scale, causal, status,
-                      stream);
-  return launch<128>(tmQ, tmK, tmV, tmdO, o, dO, lse, dq, dk, dv, Lp, Dp, B, H, N, scale, causal, status,
-                     stream);
+    return launch<64, false>(tmQ, tmK, tmV, tmdO, o, dO, lse, dq, dk, dv, Lp, Dp, B, H, N, scale, causal,
+                             status, stream);
+  return launch<128, false>(tmQ, tmK, tmV, tmdO, o, dO, lse, dq, dk, dv, Lp, Dp, B, H, N, scale, causal,
+                            status, stream);
 }
 
 }  // namespace fa

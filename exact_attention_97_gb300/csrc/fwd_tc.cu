@@ -1,4 +1,5 @@
-// fwd_bf16.cu -- exact attention forward on the sm_103a tensor cores.
+// fwd_tc.cu -- exact attention forward on the sm_103a tensor cores, for 16-bit
+// inputs (bf16 or f16; the element type is a template parameter).
 //
 // What it computes (pages): the tiled loop of "Flash Attention 原理与实现",
 // section "Forward 的 Tiling 策略" -- for each block Q_i of query rows, walk
@@ -65,14 +66,15 @@ __device__ __forceinline__ void load_tile(uint8_t *dst, const CUtensorMap *map, 
   for (int x = 0; x < D; x += 64) tma_load_3d(dst + (x / 64) * (kBlockN * 128), map, bar, x, row, bh);
 }
 
-template <int D>
+template <int D, bool F16>
 __global__ void __launch_bounds__(kThreads, 1)
-    fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ,
+    fwd_kernel(const __grid_constant__ CUtensorMap tmQ,
                     const __grid_constant__ CUtensorMap tmK,
-                    const __grid_constant__ CUtensorMap tmV, __nv_bfloat16 *__restrict__ o,
+                    const __grid_constant__ CUtensorMap tmV, uint16_t *__restrict__ o,
                     float *__restrict__ lse, int N, float scale, float scale_log2, int causal,
                     int *status) {
   using L = FwdSmem<D>;
+  using E = Elt<F16>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
@@ -156,7 +158,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------ MMA issuer: S = Q K^T
     // S_j goes to buffer j % 3 once P_{j-3} (which lived there) has been used.
     if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_bf16(kBlockM, kBlockN, false, false);
+      constexpr uint32_t idesc_s = idesc_16(kBlockM, kBlockN, false, false, F16);
       const uint32_t q_addr = smem_u32(smem + L::kQ);
       bool ok = mbar_wait(&q_full, 0, &abort_flag);
       for (int j = 0; ok && j < n_ktiles; ++j) {
@@ -183,7 +185,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // A second issuing thread, so the tensor pipe always has one of the two
     // streams queued while the other waits on its barriers.
     if (lane == 0) {
-      constexpr uint32_t idesc_o = idesc_bf16(kBlockM, D, false, true);
+      constexpr uint32_t idesc_o = idesc_16(kBlockM, D, false, true, F16);
       bool ok = true;
       for (int j = 0; ok && j < n_ktiles; ++j) {
         const int st = j % kStages, sb = j % kSBuf;
@@ -287,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         float p0, p1;
         f2_unpack(p2, p0, p1);
-        pk[u] = pack_bf16x2(p0, p1);
+        pk[u] = E::pack(p0, p1);
       }
       tmem_st64(tmem + lane_addr + sb * 128, pk);
       float rs;
@@ -306,7 +308,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const float inv_l = 1.f / l_sum;
       const bool store = row < N;
-      __nv_bfloat16 *orow = o + (static_cast<size_t>(bh) * N + row) * D;
+      uint16_t *orow = o + (static_cast<size_t>(bh) * N + row) * D;
 #pragma unroll 1
       for (int ch = 0; ch < D / 32; ++ch) {
         uint32_t r[32];
@@ -314,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t pk[16];
 #pragma unroll
         for (int t = 0; t < 16; ++t)
-          pk[t] = pack_bf16x2(__uint_as_float(r[2 * t]) * inv_l, __uint_as_float(r[2 * t + 1]) * inv_l);
+          pk[t] = E::pack(__uint_as_float(r[2 * t]) * inv_l, __uint_as_float(r[2 * t + 1]) * inv_l);
         if (store) {
           uint4 *dst = reinterpret_cast<uint4 *>(orow + ch * 32);
 #pragma unroll
@@ -335,17 +337,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0 && abort_flag) atomicExch(status, kErrTimeout);
 }
 
-template <int D>
+template <int D, bool F16>
 cudaError_t launch(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtensorMap &tmV, void *o,
                    float *lse, int B, int H, int N, float scale, int causal, int *status,
                    cudaStream_t stream) {
   using L = FwdSmem<D>;
-  auto kern = fwd_bf16_kernel<D>;
+  auto kern = fwd_kernel<D, F16>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (e != cudaSuccess) return e;
   dim3 grid((N + kBlockM - 1) / kBlockM, B * H);
   timing_begin(stream);
-  kern<<<grid, kThreads, L::kAlloc, stream>>>(tmQ, tmK, tmV, static_cast<__nv_bfloat16 *>(o), lse,
+  kern<<<grid, kThreads, L::kAlloc, stream>>>(tmQ, tmK, tmV, static_cast<uint16_t *>(o), lse,
                                                N, scale, scale * 1.4426950408889634f, causal,
                                                status);
   timing_end(stream);
@@ -354,14 +356,17 @@ cudaError_t launch(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtenso
 
 }  // namespace
 
-cudaError_t launch_fwd_bf16(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtensorMap &tmV,
-                            void *o, float *lse, int B, int H, int N, int d, float scale,
-                            int causal, int *status, int num_sms, cudaStream_t stream,
-                            int *launches) {
+cudaError_t launch_fwd_16(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtensorMap &tmV,
+                          void *o, float *lse, int B, int H, int N, int d, float scale, int causal,
+                          bool f16, int *status, int num_sms, cudaStream_t stream, int *launches) {
   (void)num_sms;
   *launches += 1;
-  if (d == 64) return launch<64>(tmQ, tmK, tmV, o, lse, B, H, N, scale, causal, status, stream);
-  return launch<128>(tmQ, tmK, tmV, o, lse, B, H, N, scale, causal, status, stream);
+  if (f16) {
+    if (d == 64) return launch<64, true>(tmQ, tmK, tmV, o, lse, B, H, N, scale, causal, status, stream);
+    return launch<128, true>(tmQ, tmK, tmV, o, lse, B, H, N, scale, causal, status, stream);
+  }
+  if (d == 64) return launch<64, false>(tmQ, tmK, tmV, o, lse, B, H, N, scale, causal, status, stream);
+  return launch<128, false>(tmQ, tmK, tmV, o, lse, B, H, N, scale, causal, status, stream);
 }
 
 }  // namespace fa

@@ -35,20 +35,20 @@ cudaError_t launch_bwd_f32(const float *q, const float *k, const float *v, const
                            int B, int H, int N, int d, float scale, int causal, float *D,
                            cudaStream_t stream, int *launches);
 
-// bf16 tensor-core forward. tmQ/tmK/tmV are 3-D tensor maps {d, N, B*H} with
-// a {64, 128, 1} box and 128-byte swizzle.
-cudaError_t launch_fwd_bf16(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtensorMap &tmV,
-                            void *o, float *lse, int B, int H, int N, int d, float scale,
-                            int causal, int *status, int num_sms, cudaStream_t stream,
-                            int *launches);
+// 16-bit tensor-core forward (bf16, or f16 when `f16`). tmQ/tmK/tmV are 3-D
+// tensor maps {d, N, B*H} of that element type with a {64, 128, 1} box and
+// 128-byte swizzle.
+cudaError_t launch_fwd_16(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtensorMap &tmV,
+                          void *o, float *lse, int B, int H, int N, int d, float scale, int causal,
+                          bool f16, int *status, int num_sms, cudaStream_t stream, int *launches);
 
-// bf16 tensor-core backward (three kernels: row terms, dK/dV pass, dQ pass).
-// Lp and Dp are [B*H][Np] fp32 with Np = 128*ceil(N/128), in the caller's
-// workspace.
-cudaError_t launch_bwd_bf16(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtensorMap &tmV,
-                            const CUtensorMap &tmdO, const void *o, const void *dO, const float *lse,
-                            void *dq, void *dk, void *dv, float *Lp, float *Dp, int B, int H, int N, int d,
-                            float scale, int causal, int *status, int num_sms, cudaStream_t stream,
-                            int *launches);
+// 16-bit tensor-core backward (three kernels: row terms, dK/dV pass, dQ
+// pass). Lp and Dp are [B*H][Np] fp32 with Np = 128*ceil(N/128), in the
+// caller's workspace.
+cudaError_t launch_bwd_16(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtensorMap &tmV,
+                          const CUtensorMap &tmdO, const void *o, const void *dO, const float *lse,
+                          void *dq, void *dk, void *dv, float *Lp, float *Dp, int B, int H, int N, int d,
+                          float scale, int causal, bool f16, int *status, int num_sms, cudaStream_t stream,
+                          int *launches);
 
 }  // namespace fa

@@ -280,14 +280,15 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
 
 // ------------------------------------------------------------------- tcgen05
 
-// Instruction descriptor for kind::f16 with bf16 A and B, fp32 accumulator.
-//   bits 4-5 D format (1 = f32), 7-9 A format (1 = bf16), 10-12 B format,
-//   bit 15 A is MN-major, bit 16 B is MN-major, bits 17-22 N/8, 24-28 M/16.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major,
-                                                  bool b_mn_major) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn_major ? 1u : 0u) << 15) |
-         ((b_mn_major ? 1u : 0u) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
-         (static_cast<uint32_t>(M >> 4) << 24);
+// Instruction descriptor for kind::f16 with 16-bit A and B, fp32 accumulator.
+//   bits 4-5 D format (1 = f32), 7-9 A format and 10-12 B format (0 = f16,
+//   1 = bf16; A and B always share it), bit 15 A is MN-major, bit 16 B is
+//   MN-major, bits 17-22 N/8, 24-28 M/16.
+__host__ __device__ constexpr uint32_t idesc_16(int M, int N, bool a_mn_major, bool b_mn_major,
+                                                bool f16) {
+  return (1u << 4) | ((f16 ? 0u : 1u) << 7) | ((f16 ? 0u : 1u) << 10) |
+         ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
+         (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
 // Shared-memory matrix descriptor, 128-byte swizzle (the layout TMA writes
@@ -354,6 +355,36 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
 }
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ float f16_to_f32(uint32_t h) {
+  float f;
+  asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.f32.f16 %0, t;\n\t}" : "=f"(f) : "r"(h));
+  return f;
+}
+
+// The 16-bit element type of a kernel instance: bf16 (F16 = false) or f16.
+// pack() rounds two floats to a packed pair (nearest even), lo()/hi() widen
+// the low / high half of a packed pair back to float.
+template <bool F16>
+struct Elt;
+template <>
+struct Elt<false> {
+  __device__ static __forceinline__ uint32_t pack(float lo, float hi) { return pack_bf16x2(lo, hi); }
+  __device__ static __forceinline__ float lo(uint32_t v) { return __uint_as_float(v << 16); }
+  __device__ static __forceinline__ float hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+};
+template <>
+struct Elt<true> {
+  __device__ static __forceinline__ uint32_t pack(float lo, float hi) { return pack_f16x2(lo, hi); }
+  __device__ static __forceinline__ float lo(uint32_t v) { return f16_to_f32(v & 0xFFFFu); }
+  __device__ static __forceinline__ float hi(uint32_t v) { return f16_to_f32(v >> 16); }
+};
 
 __device__ __forceinline__ int warp_id() { return threadIdx.x >> 5; }
 __device__ __forceinline__ int lane_id() { return threadIdx.x & 31; }

@@ -43,8 +43,8 @@
  *              fa_last_cuda_error). A kernel that gives up on an internal
  *              wait (it never traps) records FA_ERR_TIMEOUT in a device
  *              status word read by fa_device_status.
- *   Supported  bf16: d in {64, 128}, N >= 1 (ragged tails are masked),
- *              every pointer 16-byte aligned.
+ *   Supported  bf16 and f16: d in {64, 128}, N >= 1 (ragged tails are
+ *              masked), every pointer 16-byte aligned.
  *              f32: 1 <= d <= 128, N >= 1, every pointer 4-byte aligned.
  *              B, H >= 1; B*H*N*d must be below 2^40 elements.
  */
@@ -73,7 +73,7 @@ typedef enum {
   FA_ERR_ARG = 9          /* other invalid argument (non-finite scale, dtype) */
 } fa_status;
 
-typedef enum { FA_BF16 = 0, FA_F32 = 1 } fa_dtype;
+typedef enum { FA_BF16 = 0, FA_F32 = 1, FA_F16 = 2 } fa_dtype;
 
 /*
  * Forward, bf16 in / bf16 out.
@@ -108,6 +108,18 @@ int fa_bwd(const void *q, const void *k, const void *v, const void *o,
            int B, int H, int N, int d, float scale, int causal,
            void *workspace, size_t workspace_bytes, fa_stream_t stream);
 
+/* Forward and backward with IEEE half (f16) tensors: same kernels, arguments,
+ * layout, workspace and errors as fa_fwd / fa_bwd with f16 in place of bf16;
+ * P and dS are rounded to f16 before their products. fp16 inputs are the
+ * blog's own setting (its pitfalls items on FP16 training and overflow). */
+int fa_fwd_f16(const void *q, const void *k, const void *v, void *o, float *lse,
+               int B, int H, int N, int d, float scale, int causal,
+               fa_stream_t stream);
+int fa_bwd_f16(const void *q, const void *k, const void *v, const void *o,
+               const float *lse, const void *dO, void *dq, void *dk, void *dv,
+               int B, int H, int N, int d, float scale, int causal,
+               void *workspace, size_t workspace_bytes, fa_stream_t stream);
+
 /* Forward with float tensors (all fp32 arithmetic, exact expf). Same
  * arguments and layout as fa_fwd with float element type. */
 int fa_fwd_f32(const float *q, const float *k, const float *v, float *o,
@@ -121,8 +133,8 @@ int fa_bwd_f32(const float *q, const float *k, const float *v, const float *o,
                float *dv, int B, int H, int N, int d, float scale, int causal,
                void *workspace, size_t workspace_bytes, fa_stream_t stream);
 
-/* Bytes of workspace fa_bwd / fa_bwd_f32 need for this shape (0 on invalid
- * shape). dtype is an fa_dtype. */
+/* Bytes of workspace fa_bwd / fa_bwd_f16 / fa_bwd_f32 need for this shape (0
+ * on invalid shape). dtype is an fa_dtype. */
 size_t fa_bwd_workspace_size(int B, int H, int N, int d, int dtype);
 
 /* Static description of a status code; never NULL. */

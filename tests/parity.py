@@ -5,6 +5,7 @@ Tolerances (the method's stated bar, per tensor over all checked elements):
   float32 inputs: O, L and every gradient max-abs <= 1e-4 (L's bound is a
                   reading: the stated 1e-4 for fp32 outputs is applied to it);
   bf16 inputs:    O max-abs <= 2e-2, L max-abs <= 1e-3,
+  (f16 inputs are held to the bf16 bar; the method states none for them)
                   each gradient max|g - g_ref| <= 5e-2 * max|g_ref|, with an
                   absolute floor of 1e-4 (the fp32 bar) for degenerate cases
                   whose exact gradient is zero (N = 1: dS = P (dP - D) = 0).

@@ -59,6 +59,7 @@ def test_workspace_size_layout():
         want = 2 * r256(prow * 4)
         assert fa.fa_bwd_workspace_size(B, H, N, d, fa.FA_BF16) == want
         assert fa.fa_bwd_workspace_size(B, H, N, d, fa.FA_F32) == r256(B * H * N * 4)
+        assert fa.fa_bwd_workspace_size(B, H, N, d, fa.FA_F16) == want
     assert fa.fa_bwd_workspace_size(0, 1, 1, 64, fa.FA_BF16) == 0
     assert fa.fa_bwd_workspace_size(1, 1, 1, 129, fa.FA_BF16) == 0
     assert fa.fa_bwd_workspace_size(1, 1, 1, 64, 7) == 0
@@ -102,6 +103,16 @@ def test_bwd_argument_errors(lib):
     assert _bwd(lib, ws_bytes=need - 1) == 5
     assert _bwd(lib, ws=P + 16, ws_bytes=need) == 4  # workspace must be 256-byte aligned
     assert _bwd(lib, scale=float("-inf")) == 9
+
+
+def test_f16_argument_errors(lib):
+    args = [P] * 5
+    assert lib.fa_fwd_f16(None, *args[1:], 1, 1, 128, 64, 0.125, 0, None) == 1
+    assert lib.fa_fwd_f16(*args, 1, 1, 128, 96, 0.125, 0, None) == 3
+    assert lib.fa_fwd_f16(P + 8, *args[1:], 1, 1, 128, 64, 0.125, 0, None) == 4
+    ptrs = [P] * 9
+    assert lib.fa_bwd_f16(*ptrs, 1, 1, 128, 64, 0.125, 0, None, 0, None) == 5
+    assert lib.fa_bwd_f16(*ptrs, 1, 1, 128, 64, float("nan"), 0, P, 1 << 30, None) == 9
 
 
 def test_f32_argument_errors(lib):

@@ -113,6 +113,30 @@ def test_bf16_scale_and_large_scores(d):
               _full_ref(_np(q), _np(k), _np(v), _np(dO), 0.5, causal))
 
 
+# ------------------------------------------------------------ f16 inputs (same kernels, f16 operands)
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("N", [1, 127, 300])
+@pytest.mark.parametrize("causal", [False, True])
+def test_f16_small_and_ragged(d, N, causal):
+    q, k, v, dO = make_qkv_do(1, 2, N, d, seed=2000 + N + d, dtype=torch.float16)
+    scale = 1.0 / math.sqrt(d)
+    got = _as_dict(run_gpu(q, k, v, dO, scale, causal))
+    check(f"f16_small_N{N}_d{d}_c{int(causal)}", "bf16", got,
+          _full_ref(_np(q), _np(k), _np(v), _np(dO), scale, causal))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_f16_B2_H4_N1024_d128_and_large_scores(causal):
+    q, k, v, dO = make_qkv_do(2, 4, 1024, 128, seed=31, dtype=torch.float32)
+    q = q * 3  # scores several units wide, so the running max moves
+    q, k, v, dO = (x.to(torch.float16) for x in (q, k, v, dO))
+    scale = 1.0 / math.sqrt(128)
+    got = _as_dict(run_gpu(q, k, v, dO, scale, causal))
+    check(f"f16_B2_H4_N1024_d128_c{int(causal)}", "bf16", got,
+          _full_ref(_np(q), _np(k), _np(v), _np(dO), scale, causal))
+
+
 def test_bf16_causal_B1_H8_N1024_d64():
     w = WORKLOADS["bf16_causal_B1_H8_N1024_d64"]
     q, k, v, dO = make_qkv_do(w.B, w.H, w.N, w.d, w.seed, torch.bfloat16)
