@@ -56,6 +56,8 @@ def _load():
             P = ctypes.c_void_p
             i, dbl = ctypes.c_int, ctypes.c_double
             lib.oracle_fwd.argtypes = [P, P, P, P, P, i, i, i, i, dbl, i]
+            lib.oracle_fwd_kv.argtypes = [P, P, P, P, P, i, i, i, i, i, dbl, i]
+            lib.oracle_bwd_kv.argtypes = [P, P, P, P, P, P, P, i, i, i, i, i, dbl, i]
             lib.oracle_bwd.argtypes = [P, P, P, P, P, P, P, i, i, i, i, dbl, i]
             lib.oracle_probs.argtypes = [P, P, i, i, dbl, i, P]
             lib.oracle_query_rows.argtypes = [P, P, P, P, i, i, dbl, i, P, i, P, P, P]
@@ -98,6 +100,32 @@ def attention_bwd(q, k, v, dO, scale: float, causal: bool = False):
     dq, dk, dv = np.empty_like(q), np.empty_like(q), np.empty_like(q)
     _load().oracle_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(dO), _ptr(dq), _ptr(dk), _ptr(dv),
                        B, H, N, d, float(scale), int(bool(causal)))
+    return dq, dk, dv
+
+
+def attention_fwd_kv(q, k, v, scale: float, causal: bool = False):
+    """O [B,H,Nq,d] and L [B,H,Nq] for q [B,H,Nq,d] and k, v [B,H,Nk,d].
+
+    Causal: query i sees key j iff j <= i + (Nk - Nq) (bottom-right aligned).
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    o = np.empty_like(q)
+    lse = np.empty((B, H, Nq), dtype=np.float64)
+    _load().oracle_fwd_kv(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Nq, Nk, d,
+                          float(scale), int(bool(causal)))
+    return o, lse
+
+
+def attention_bwd_kv(q, k, v, dO, scale: float, causal: bool = False):
+    """(dQ [B,H,Nq,d], dK [B,H,Nk,d], dV [B,H,Nk,d]) for the Nq x Nk problem."""
+    q, k, v, dO = _f64(q), _f64(k), _f64(v), _f64(dO)
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    dq, dk, dv = np.empty_like(q), np.empty_like(k), np.empty_like(v)
+    _load().oracle_bwd_kv(_ptr(q), _ptr(k), _ptr(v), _ptr(dO), _ptr(dq), _ptr(dk), _ptr(dv),
+                          B, H, Nq, Nk, d, float(scale), int(bool(causal)))
     return dq, dk, dv
 
 

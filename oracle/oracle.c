@@ -17,7 +17,9 @@
  *                                           statistic L = m + log(l))
  * With a causal mask, S_ij = -inf for key j > query i (standard lower
  * triangle; the pages only name the mask as an experiment parameter, section
- * 06 of the same page).
+ * 06 of the same page). With Nq queries and Nk >= Nq keys the triangle is
+ * aligned at the bottom right: query i sees key j iff j <= i + (Nk - Nq), so
+ * the last query sees every key (the decode / prefill reading).
  *
  * Backward, for an upstream gradient dO and no gradient through L (blog page
  * "Flash Attention 原理与实现", section "Backward 的 Tiling 策略", written out):
@@ -30,7 +32,8 @@
  * The factor `scale` in dQ/dK makes these the true derivatives of O(Q,K,V);
  * the finite-difference tests pin it.
  *
- * Layout: every matrix is contiguous [B][H][N][d] (row-major), L is [B][H][N].
+ * Layout: every matrix is contiguous [B][H][rows][d] (row-major) with Nq rows
+ * for Q, O, dO, dQ and Nk rows for K, V, dK, dV; L is [B][H][Nq].
  * All arithmetic is double precision; the max is subtracted before exp, as
  * the tutorial's section 02 prescribes.
  */
@@ -48,8 +51,12 @@ static double dot(const double *a, const double *b, int d) {
   return s;
 }
 
-/* Number of keys query row i may see. */
-static int visible_keys(int i, int N, int causal) { return causal ? i + 1 : N; }
+/* Number of keys query row i may see (a prefix of the keys). */
+static int visible_keys(int i, int Nq, int Nk, int causal) {
+  if (!causal) return Nk;
+  const int n = i + 1 + (Nk - Nq);
+  return n < Nk ? n : Nk;
+}
 
 /* One query row of one head: scores s[0..nk), probabilities p, output o, and
  * the log-sum-exp. q is the query row, k/v point at the head's [N][d] keys and
@@ -76,27 +83,34 @@ static double row_forward(const double *q, const double *k, const double *v,
   return m + log(l);
 }
 
-/* Forward over all heads and rows. */
-void oracle_fwd(const double *q, const double *k, const double *v, double *o,
-                double *lse, int B, int H, int N, int d, double scale,
-                int causal) {
-  const int64_t rows = (int64_t)B * H * N;
+/* Forward over all heads and rows, Nq queries and Nk keys per head. */
+void oracle_fwd_kv(const double *q, const double *k, const double *v, double *o,
+                   double *lse, int B, int H, int Nq, int Nk, int d, double scale,
+                   int causal) {
+  const int64_t rows = (int64_t)B * H * Nq;
 #pragma omp parallel
   {
-    double *s = (double *)malloc(sizeof(double) * (size_t)N);
-    double *p = (double *)malloc(sizeof(double) * (size_t)N);
+    double *s = (double *)malloc(sizeof(double) * (size_t)Nk);
+    double *p = (double *)malloc(sizeof(double) * (size_t)Nk);
 #pragma omp for schedule(dynamic, 16)
     for (int64_t r = 0; r < rows; ++r) {
-      const int64_t bh = r / N;
-      const int i = (int)(r % N);
-      const size_t head = (size_t)bh * N * d;
-      lse[r] = row_forward(q + (size_t)r * d, k + head, v + head,
-                           visible_keys(i, N, causal), d, scale, s, p,
+      const int64_t bh = r / Nq;
+      const int i = (int)(r % Nq);
+      const size_t khead = (size_t)bh * Nk * d;
+      lse[r] = row_forward(q + (size_t)r * d, k + khead, v + khead,
+                           visible_keys(i, Nq, Nk, causal), d, scale, s, p,
                            o + (size_t)r * d);
     }
     free(s);
     free(p);
   }
+}
+
+/* Forward with Nq = Nk = N. */
+void oracle_fwd(const double *q, const double *k, const double *v, double *o,
+                double *lse, int B, int H, int N, int d, double scale,
+                int causal) {
+  oracle_fwd_kv(q, k, v, o, lse, B, H, N, N, d, scale, causal);
 }
 
 /* Full softmax matrix P of one head (small N only; for invariant tests). */
@@ -107,7 +121,7 @@ void oracle_probs(const double *q, const double *k, int N, int d, double scale,
   double *vz = (double *)calloc((size_t)N * d, sizeof(double));
   for (int i = 0; i < N; ++i) {
     double *prow = P + (size_t)i * N;
-    int nk = visible_keys(i, N, causal);
+    int nk = visible_keys(i, N, N, causal);
     row_forward(q + (size_t)i * d, k, vz, nk, d, scale, s, prow, o);
     for (int j = nk; j < N; ++j) prow[j] = 0.0;
   }
@@ -116,26 +130,27 @@ void oracle_probs(const double *q, const double *k, int N, int d, double scale,
   free(vz);
 }
 
-/* Backward over all heads. Outputs dq, dk, dv are overwritten.
+/* Backward over all heads, Nq queries and Nk keys per head. Outputs dq, dk,
+ * dv are overwritten.
  * Heads are processed one after another; inside a head the query rows are
  * split statically over threads. Each thread runs its rows forward in full
  * (S row, P row, O row, D_i), writes dQ_i, and adds its rows' terms of dK and
  * dV into private [N][d] sums, which are then added together in thread order
  * (so the result does not depend on scheduling). */
-void oracle_bwd(const double *q, const double *k, const double *v,
-                const double *dO, double *dq, double *dk, double *dv, int B,
-                int H, int N, int d, double scale, int causal) {
+void oracle_bwd_kv(const double *q, const double *k, const double *v,
+                   const double *dO, double *dq, double *dk, double *dv, int B,
+                   int H, int Nq, int Nk, int d, double scale, int causal) {
   const int64_t heads = (int64_t)B * H;
-  const size_t hs = (size_t)N * d;
+  const size_t qs = (size_t)Nq * d, hs = (size_t)Nk * d;
   int nthr = 1;
 #ifdef _OPENMP
   nthr = omp_get_max_threads();
 #endif
   double *part = (double *)malloc(sizeof(double) * 2 * hs * (size_t)nthr);
   for (int64_t bh = 0; bh < heads; ++bh) {
-    const size_t off = (size_t)bh * hs;
-    const double *qh = q + off, *kh = k + off, *vh = v + off, *doh = dO + off;
-    double *dqh = dq + off;
+    const size_t qoff = (size_t)bh * qs, off = (size_t)bh * hs;
+    const double *qh = q + qoff, *kh = k + off, *vh = v + off, *doh = dO + qoff;
+    double *dqh = dq + qoff;
     int used = 1;
 #pragma omp parallel num_threads(nthr)
     {
@@ -148,14 +163,14 @@ void oracle_bwd(const double *q, const double *k, const double *v,
       double *pk = part + (size_t)t * 2 * hs;
       double *pv = pk + hs;
       memset(pk, 0, sizeof(double) * 2 * hs);
-      double *s = (double *)malloc(sizeof(double) * (size_t)N);
-      double *p = (double *)malloc(sizeof(double) * (size_t)N);
+      double *s = (double *)malloc(sizeof(double) * (size_t)Nk);
+      double *p = (double *)malloc(sizeof(double) * (size_t)Nk);
       double *o = (double *)malloc(sizeof(double) * (size_t)d);
 #pragma omp for schedule(static)
-      for (int i = 0; i < N; ++i) {
+      for (int i = 0; i < Nq; ++i) {
         const double *qi = qh + (size_t)i * d;
         const double *doi = doh + (size_t)i * d;
-        const int nk = visible_keys(i, N, causal);
+        const int nk = visible_keys(i, Nq, Nk, causal);
         row_forward(qi, kh, vh, nk, d, scale, s, p, o);
         const double Di = dot(doi, o, d);
         double *dqi = dqh + (size_t)i * d;
@@ -192,6 +207,13 @@ void oracle_bwd(const double *q, const double *k, const double *v,
   free(part);
 }
 
+/* Backward with Nq = Nk = N. */
+void oracle_bwd(const double *q, const double *k, const double *v,
+                const double *dO, double *dq, double *dk, double *dv, int B,
+                int H, int N, int d, double scale, int causal) {
+  oracle_bwd_kv(q, k, v, dO, dq, dk, dv, B, H, N, N, d, scale, causal);
+}
+
 /* Sampled query rows of one head: O_i, L_i and dQ_i for rows[0..nrows).
  * q,k,v,dO are the head's [N][d] blocks. Each row costs O(N d). */
 void oracle_query_rows(const double *q, const double *k, const double *v,
@@ -208,7 +230,7 @@ void oracle_query_rows(const double *q, const double *k, const double *v,
       const double *qi = q + (size_t)i * d;
       const double *doi = dO + (size_t)i * d;
       double *oi = o_out + (size_t)r * d;
-      const int nk = visible_keys(i, N, causal);
+      const int nk = visible_keys(i, N, N, causal);
       lse_out[r] = row_forward(qi, k, v, nk, d, scale, s, p, oi);
       const double Di = dot(doi, oi, d);
       double *dqi = dq_out + (size_t)r * d;
@@ -251,7 +273,7 @@ void oracle_key_rows(const double *q, const double *k, const double *v,
     for (int i = first_row; i < N; ++i) {
       const double *qi = q + (size_t)i * d;
       const double *doi = dO + (size_t)i * d;
-      const int nk = visible_keys(i, N, causal);
+      const int nk = visible_keys(i, N, N, causal);
       row_forward(qi, k, v, nk, d, scale, s, p, o);
       const double Di = dot(doi, o, d);
       for (int t = 0; t < nkeys; ++t) {

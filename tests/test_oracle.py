@@ -303,6 +303,69 @@ def test_against_torch_autograd_fp64(causal):
         assert np.max(np.abs(g - t.grad.numpy())) < 1e-11
 
 
+# ---------------------------------------------------------------- Nq queries, Nk keys
+
+def _square_with_prefix(r, Nq, Nk, d):
+    """A square Nk x Nk problem whose last Nq query rows are the Nq x Nk one;
+    the leading rows get zero upstream gradient, so they add nothing to dK, dV."""
+    q = r.standard_normal((1, 2, Nq, d))
+    k, v = (r.standard_normal((1, 2, Nk, d)) for _ in range(2))
+    dO = r.standard_normal((1, 2, Nq, d))
+    q_full = np.concatenate([r.standard_normal((1, 2, Nk - Nq, d)), q], axis=2)
+    dO_full = np.concatenate([np.zeros((1, 2, Nk - Nq, d)), dO], axis=2)
+    return q, k, v, dO, q_full, dO_full
+
+
+@pytest.mark.parametrize("Nq,Nk", [(1, 9), (4, 9), (9, 9), (7, 20)])
+def test_kv_bottom_right_causal_is_the_last_rows_of_the_square_problem(Nq, Nk):
+    """Bottom-right alignment means exactly this: the Nq queries are the last
+    Nq rows of the causal Nk x Nk problem on the same keys."""
+    r = _rng(40 + Nq + Nk)
+    q, k, v, dO, q_full, dO_full = _square_with_prefix(r, Nq, Nk, 3)
+    o, lse = oracle.attention_fwd_kv(q, k, v, 0.7, True)
+    o_sq, lse_sq = oracle.attention_fwd(q_full, k, v, 0.7, True)
+    assert np.max(np.abs(o - o_sq[:, :, Nk - Nq:])) < 1e-13
+    assert np.max(np.abs(lse - lse_sq[:, :, Nk - Nq:])) < 1e-13
+    dq, dk, dv = oracle.attention_bwd_kv(q, k, v, dO, 0.7, True)
+    dq_sq, dk_sq, dv_sq = oracle.attention_bwd(q_full, k, v, dO_full, 0.7, True)
+    assert np.max(np.abs(dq - dq_sq[:, :, Nk - Nq:])) < 1e-12
+    assert np.max(np.abs(dk - dk_sq)) < 1e-12 and np.max(np.abs(dv - dv_sq)) < 1e-12
+
+
+def test_kv_single_query_decode_sees_every_key():
+    r = _rng(41)
+    q = r.standard_normal((1, 1, 1, 4))
+    k, v = (r.standard_normal((1, 1, 13, 4)) for _ in range(2))
+    oc, lc = oracle.attention_fwd_kv(q, k, v, 0.5, True)
+    on, ln = oracle.attention_fwd_kv(q, k, v, 0.5, False)
+    assert np.max(np.abs(oc - on)) < 1e-15 and np.max(np.abs(lc - ln)) < 1e-15
+    s = 0.5 * (k[0, 0] @ q[0, 0, 0])
+    w = np.exp(s - s.max())
+    assert np.max(np.abs(on[0, 0, 0] - (w / w.sum()) @ v[0, 0])) < 1e-14
+
+
+@pytest.mark.parametrize("Nq,Nk,causal", [(3, 5, True), (3, 5, False), (5, 3, False), (2, 2, True)])
+def test_kv_gradients_match_central_differences(Nq, Nk, causal):
+    r = _rng(200 + 10 * Nq + Nk)
+    q = r.standard_normal((1, 1, Nq, 2))
+    k, v = (r.standard_normal((1, 1, Nk, 2)) for _ in range(2))
+    dO = r.standard_normal((1, 1, Nq, 2))
+    grads = oracle.attention_bwd_kv(q, k, v, dO, 0.9, causal)
+    h = 1e-6
+
+    def loss(qq, kk, vv):
+        return float(np.sum(oracle.attention_fwd_kv(qq, kk, vv, 0.9, causal)[0] * dO))
+
+    for which, g in enumerate(grads):
+        for idx in np.ndindex(g.shape):
+            plus = [q.copy(), k.copy(), v.copy()]
+            minus = [q.copy(), k.copy(), v.copy()]
+            plus[which][idx] += h
+            minus[which][idx] -= h
+            num = (loss(*plus) - loss(*minus)) / (2 * h)
+            assert abs(num - g[idx]) <= 1e-6 * max(1.0, np.abs(g).max())
+
+
 # ---------------------------------------------------------------- sampled-row entry points
 
 @pytest.mark.parametrize("causal", [False, True])
@@ -329,8 +392,8 @@ MUTATIONS = {
     "dK without scale": ("dkj[c] += scale * dSij * qi[c];", "dkj[c] += dSij * qi[c];"),
     "dS with wrong sign of D": ("p[j] * (dPij - Di)", "p[j] * (dPij + Di)"),
     "dV transposed operand": ("dvj[c] += p[j] * doi[c];", "dvj[c] += p[j] * qi[c];"),
-    "causal sees one key too many": ("return causal ? i + 1 : N;",
-                                     "return causal ? (i + 2 < N ? i + 2 : N) : N;"),
+    "causal sees one key too many": ("const int n = i + 1 + (Nk - Nq);", "const int n = i + 2 + (Nk - Nq);"),
+    "causal aligned top-left": ("const int n = i + 1 + (Nk - Nq);", "const int n = i + 1;"),
     "L without the max": ("return m + log(l);", "return log(l);"),
     "softmax not normalised": ("for (int j = 0; j < nk; ++j) p[j] /= l;", ""),
 }
@@ -345,11 +408,20 @@ class _Lib:
         self.lib = ctypes.CDLL(so)
         self.lib.oracle_fwd.argtypes = [self.P] * 5 + [ctypes.c_int] * 4 + [ctypes.c_double, ctypes.c_int]
         self.lib.oracle_bwd.argtypes = [self.P] * 7 + [ctypes.c_int] * 4 + [ctypes.c_double, ctypes.c_int]
+        self.lib.oracle_fwd_kv.argtypes = [self.P] * 5 + [ctypes.c_int] * 5 + [ctypes.c_double, ctypes.c_int]
 
     def fwd(self, q, k, v, scale, causal):
         B, H, N, d = q.shape
         o = np.empty_like(q); lse = np.empty(q.shape[:3])
         self.lib.oracle_fwd(*(x.ctypes.data_as(self.P) for x in (q, k, v, o, lse)), B, H, N, d, scale, int(causal))
+        return o, lse
+
+    def fwd_kv(self, q, k, v, scale, causal):
+        B, H, Nq, d = q.shape
+        Nk = k.shape[2]
+        o = np.empty_like(q); lse = np.empty(q.shape[:3])
+        self.lib.oracle_fwd_kv(*(x.ctypes.data_as(self.P) for x in (q, k, v, o, lse)), B, H, Nq, Nk, d, scale,
+                               int(causal))
         return o, lse
 
     def bwd(self, q, k, v, dO, scale, causal):
@@ -375,6 +447,12 @@ def _pins_hold(lib):
     q, k, v, dO = (r.standard_normal((1, 1, 5, 3)) for _ in range(4))
     o, lse = lib.fwd(q, k, v, 0.8, True)
     if not np.array_equal(o[0, 0, 0], v[0, 0, 0]) or abs(lse[0, 0, 0] - 0.8 * q[0, 0, 0] @ k[0, 0, 0]) > 1e-14:
+        return False
+    # bottom-right causal alignment: the kv problem is the tail of the square one
+    qf = r.standard_normal((1, 1, 7, 3))
+    kf, vf = r.standard_normal((1, 1, 7, 3)), r.standard_normal((1, 1, 7, 3))
+    o_kv, _ = lib.fwd_kv(np.ascontiguousarray(qf[:, :, 4:]), kf, vf, 0.8, True)
+    if np.max(np.abs(o_kv - lib.fwd(qf, kf, vf, 0.8, True)[0][:, :, 4:])) > 1e-12:
         return False
     h = 1e-6
     for causal in (False, True):
