@@ -128,25 +128,27 @@ def _dist():
 
 
 def cpu_baseline(w, heads: int):
-    """Oracle fwd+bwd on `heads` whole heads of the workload (full N)."""
+    """Oracle fwd+bwd on `heads` whole heads of the workload (full N and Nk)."""
     import torch
 
     import oracle
     from exact_attention_97_gb300.inputs import make_qkv_do
 
-    q, k, v, dO = make_qkv_do(1, heads, w.N, w.d, w.seed, torch.bfloat16)
+    dt = torch.float16 if w.dtype == "f16" else torch.bfloat16
+    q, _, _, dO = make_qkv_do(1, heads, w.N, w.d, w.seed, dt)
+    _, k, v, _ = make_qkv_do(1, heads, w.n_keys, w.d, w.seed, dt)
     f64 = lambda t: t.float().double().numpy()  # noqa: E731
     q, k, v, dO = f64(q), f64(k), f64(v), f64(dO)
     oracle.build()
     t0 = time.perf_counter()
-    oracle.attention_fwd(q, k, v, w.scale, w.causal)
-    oracle.attention_bwd(q, k, v, dO, w.scale, w.causal)
-    dt = time.perf_counter() - t0
+    oracle.attention_fwd_kv(q, k, v, w.scale, w.causal)
+    oracle.attention_bwd_kv(q, k, v, dO, w.scale, w.causal)
+    dt_s = time.perf_counter() - t0
     flops = (w.flops_fwd() + w.flops_bwd()) / (w.B * w.H) * heads
-    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(),
+    return {"value": flops / dt_s / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(),
             "kind": "oracle",
-            "sample": f"{heads} whole heads (full N={w.N}, d={w.d}) of the workload, fwd+bwd, fp64, "
-                      f"{dt:.1f} s wall"}
+            "sample": f"{heads} whole heads (full N={w.N}, Nk={w.n_keys}, d={w.d}) of the workload, fwd+bwd, "
+                      f"fp64, {dt_s:.1f} s wall"}
 
 
 def run_reference(args, w):
@@ -194,11 +196,14 @@ def run_ours(args, w):
     fa.load()
 
     # inputs: seeded host tensors, pinned copies for the end-to-end leg, device copies
-    q_h, k_h, v_h, do_h = (t.pin_memory() for t in make_qkv_do(w.B, w.H, w.N, w.d, w.seed, torch.bfloat16))
+    dt = torch.float16 if w.dtype == "f16" else torch.bfloat16
+    q_h, _, _, do_h = make_qkv_do(w.B, w.H, w.N, w.d, w.seed, dt)
+    _, k_h, v_h, _ = make_qkv_do(w.B, w.H, w.n_keys, w.d, w.seed, dt)
+    q_h, k_h, v_h, do_h = (t.pin_memory() for t in (q_h, k_h, v_h, do_h))
     q, k, v, dO = (t.to(dev) for t in (q_h, k_h, v_h, do_h))
     o = torch.empty_like(q)
     lse = torch.empty((w.B, w.H, w.N), device=dev, dtype=torch.float32)
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     need = fa.fa_bwd_workspace_size(w.B, w.H, w.N, w.d, fa.FA_BF16)
     ws = torch.empty(need, device=dev, dtype=torch.uint8)
     stream = torch.cuda.current_stream()
@@ -299,7 +304,7 @@ def run_ours(args, w):
     # end to end through the public API: pinned host inputs in, results back to pinned host
     e2e = None
     if not args.no_e2e:
-        out_h = [torch.empty_like(q_h).pin_memory() for _ in range(4)]
+        out_h = [torch.empty_like(t).pin_memory() for t in (q_h, q_h, k_h, v_h)]
 
         def e2e_step():
             qd, kd, vd, dod = (t.to(dev, non_blocking=True) for t in (q_h, k_h, v_h, do_h))
@@ -339,8 +344,9 @@ def run_ours(args, w):
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
+            "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "Nk": w.n_keys, "d": w.d,
+                       "causal": w.causal,
                        "inputs": "i.i.d. N(0,1), seeds Q=0 K=1 V=2 dO=3",
                        "l2": "inputs larger than L2 (each of Q, K, V, dO is "
                              f"{q.numel() * 2 / 1e6:.0f} MB vs 129 MB L2)",
@@ -369,7 +375,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=None, help="workload name (default: the headline)")
     ap.add_argument("--shape", default=None,
-                    help="B,H,N,d[,causal]: a smaller bf16 case of the same kernels (profiling)")
+                    help="B,H,N,d[,causal]: another case of the same kernels (profiling, other shapes)")
+    ap.add_argument("--nk", type=int, default=0, help="key/value rows per head for --shape (default N)")
+    ap.add_argument("--dtype", choices=["bf16", "f16"], default="bf16", help="16-bit input type for --shape")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-heads", type=int, default=8, help="heads in the CPU-baseline sample")
@@ -383,7 +391,9 @@ def main():
         vals = [int(x) for x in args.shape.split(",")]
         B, H, N, d = vals[:4]
         causal = bool(vals[4]) if len(vals) > 4 else False
-        w = Workload(f"bf16{'_causal' if causal else ''}_B{B}_H{H}_N{N}_d{d}", "bf16", B, H, N, d, causal)
+        kv = f"_Nk{args.nk}" if args.nk else ""
+        w = Workload(f"{args.dtype}{'_causal' if causal else ''}_B{B}_H{H}_N{N}{kv}_d{d}", args.dtype, B, H, N, d,
+                     causal, Nk=args.nk)
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":

@@ -15,13 +15,13 @@ from __future__ import annotations
 
 import math
 
-from ._lib import (FA_BF16, FA_F16, FA_F32, FAError, fa_bwd, fa_bwd_f16, fa_bwd_f32,
-                   fa_bwd_workspace_size, fa_device_status, fa_fwd, fa_fwd_f16, fa_fwd_f32,
+from ._lib import (FA_BF16, FA_F16, FA_F32, FAError, fa_bwd, fa_bwd_f16, fa_bwd_f32, fa_bwd_kv,
+                   fa_bwd_workspace_size, fa_device_status, fa_fwd, fa_fwd_f16, fa_fwd_f32, fa_fwd_kv,
                    fa_last_launch_count, fa_set_kernel_timing, fa_status_string, lib_path, load)
 
 __all__ = [
     "FA_BF16", "FA_F16", "FA_F32", "FAError", "fa_fwd", "fa_bwd", "fa_fwd_f16", "fa_bwd_f16",
-    "fa_fwd_f32", "fa_bwd_f32",
+    "fa_fwd_f32", "fa_bwd_f32", "fa_fwd_kv", "fa_bwd_kv",
     "fa_bwd_workspace_size", "fa_status_string", "fa_device_status", "fa_last_launch_count",
     "fa_set_kernel_timing",
     "attention_forward", "attention_backward", "lib_path", "load",
@@ -51,27 +51,36 @@ def _stream_handle(stream):
 
 
 def attention_forward(q, k, v, scale=None, causal=False, out=None, lse=None, stream=None):
-    """(O, L) for [B, H, N, d] CUDA tensors q, k, v (all bf16, all f16 or all float32).
+    """(O, L) for CUDA tensors q [B, H, Nq, d] and k, v [B, H, Nk, d] (all bf16, all f16 or all float32).
 
-    bf16 and f16 need d in {64, 128}; float32 takes 1 <= d <= 128. L is float32
-    [B, H, N], the natural-log log-sum-exp of the scaled scores.
+    bf16 and f16 need d in {64, 128}; float32 takes 1 <= d <= 128 and Nk == Nq. L is
+    float32 [B, H, Nq], the natural-log log-sum-exp of the scaled scores. With Nk != Nq
+    the causal mask is aligned bottom-right (query i sees keys j <= i + Nk - Nq).
     """
     torch = _torch()
     B, H, N, d = q.shape
+    Nk = k.shape[2]
     dt = q.dtype
     if dt not in (torch.bfloat16, torch.float16, torch.float32):
         raise ValueError("q must be bfloat16, float16 or float32")
-    for name, t in (("q", q), ("k", k), ("v", v)):
-        _check(name, t, (B, H, N, d), dt)
+    _check("q", q, (B, H, N, d), dt)
+    for name, t in (("k", k), ("v", v)):
+        _check(name, t, (B, H, Nk, d), dt)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     with torch.cuda.device(q.device):
         o = torch.empty_like(q) if out is None else out
         lse = torch.empty((B, H, N), device=q.device, dtype=torch.float32) if lse is None else lse
         _check("out", o, (B, H, N, d), dt)
         _check("lse", lse, (B, H, N), torch.float32)
-        fn = {torch.bfloat16: fa_fwd, torch.float16: fa_fwd_f16, torch.float32: fa_fwd_f32}[dt]
-        fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N, d, scale,
-           int(bool(causal)), _stream_handle(stream))
+        ptrs = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr())
+        if Nk != N:
+            if dt == torch.float32:
+                raise ValueError("float32 needs k and v with as many rows as q")
+            fa_fwd_kv(*ptrs, B, H, N, Nk, d, scale, int(bool(causal)),
+                      FA_F16 if dt == torch.float16 else FA_BF16, _stream_handle(stream))
+        else:
+            fn = {torch.bfloat16: fa_fwd, torch.float16: fa_fwd_f16, torch.float32: fa_fwd_f32}[dt]
+            fn(*ptrs, B, H, N, d, scale, int(bool(causal)), _stream_handle(stream))
     return o, lse
 
 
@@ -80,9 +89,12 @@ def attention_backward(q, k, v, o, lse, dO, scale=None, causal=False, workspace=
     """(dQ, dK, dV) for upstream gradient dO, given the forward's O and L."""
     torch = _torch()
     B, H, N, d = q.shape
+    Nk = k.shape[2]
     dt = q.dtype
-    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dO", dO)):
+    for name, t in (("q", q), ("o", o), ("dO", dO)):
         _check(name, t, (B, H, N, d), dt)
+    for name, t in (("k", k), ("v", v)):
+        _check(name, t, (B, H, Nk, d), dt)
     _check("lse", lse, (B, H, N), torch.float32)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     kind = {torch.bfloat16: FA_BF16, torch.float16: FA_F16, torch.float32: FA_F32}[dt]
@@ -94,8 +106,14 @@ def attention_backward(q, k, v, o, lse, dO, scale=None, causal=False, workspace=
             raise ValueError(f"workspace needs {need} bytes")
         dq, dk, dv = grads if grads is not None else (torch.empty_like(q), torch.empty_like(k),
                                                       torch.empty_like(v))
-        fn = {FA_BF16: fa_bwd, FA_F16: fa_bwd_f16, FA_F32: fa_bwd_f32}[kind]
-        fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), dO.data_ptr(),
-           dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d, scale, int(bool(causal)),
-           workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream_handle(stream))
+        ptrs = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), dO.data_ptr(),
+                dq.data_ptr(), dk.data_ptr(), dv.data_ptr())
+        ws = (workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream_handle(stream))
+        if Nk != N:
+            if kind == FA_F32:
+                raise ValueError("float32 needs k and v with as many rows as q")
+            fa_bwd_kv(*ptrs, B, H, N, Nk, d, scale, int(bool(causal)), kind, *ws)
+        else:
+            fn = {FA_BF16: fa_bwd, FA_F16: fa_bwd_f16, FA_F32: fa_bwd_f32}[kind]
+            fn(*ptrs, B, H, N, d, scale, int(bool(causal)), *ws)
     return dq, dk, dv

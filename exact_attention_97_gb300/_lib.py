@@ -21,6 +21,8 @@ _SIGNATURES = {
     "fa_bwd": (c_int, [c_void_p] * 9 + [c_int] * 4 + [c_float, c_int, c_void_p, c_size_t, c_void_p]),
     "fa_fwd_f16": (c_int, [c_void_p] * 5 + [c_int] * 4 + [c_float, c_int, c_void_p]),
     "fa_bwd_f16": (c_int, [c_void_p] * 9 + [c_int] * 4 + [c_float, c_int, c_void_p, c_size_t, c_void_p]),
+    "fa_fwd_kv": (c_int, [c_void_p] * 5 + [c_int] * 5 + [c_float, c_int, c_int, c_void_p]),
+    "fa_bwd_kv": (c_int, [c_void_p] * 9 + [c_int] * 5 + [c_float, c_int, c_int, c_void_p, c_size_t, c_void_p]),
     "fa_fwd_f32": (c_int, [c_void_p] * 5 + [c_int] * 4 + [c_float, c_int, c_void_p]),
     "fa_bwd_f32": (c_int, [c_void_p] * 9 + [c_int] * 4 + [c_float, c_int, c_void_p, c_size_t, c_void_p]),
     "fa_bwd_workspace_size": (c_size_t, [c_int] * 5),
@@ -91,6 +93,16 @@ def fa_fwd_f16(q, k, v, o, lse, B, H, N, d, scale, causal, stream):
 def fa_bwd_f16(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, scale, causal, workspace, workspace_bytes, stream):
     return _call("fa_bwd_f16", q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, float(scale), int(causal),
                  workspace, workspace_bytes, stream)
+
+
+def fa_fwd_kv(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, dtype, stream):
+    return _call("fa_fwd_kv", q, k, v, o, lse, B, H, Nq, Nk, d, float(scale), int(causal), int(dtype), stream)
+
+
+def fa_bwd_kv(q, k, v, o, lse, dO, dq, dk, dv, B, H, Nq, Nk, d, scale, causal, dtype, workspace,
+              workspace_bytes, stream):
+    return _call("fa_bwd_kv", q, k, v, o, lse, dO, dq, dk, dv, B, H, Nq, Nk, d, float(scale), int(causal),
+                 int(dtype), workspace, workspace_bytes, stream)
 
 
 def fa_fwd_f32(q, k, v, o, lse, B, H, N, d, scale, causal, stream):

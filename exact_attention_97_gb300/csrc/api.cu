@@ -220,12 +220,14 @@ int fa_device_status(void) {
 
 namespace {
 
-// Shared body of fa_fwd / fa_fwd_f16.
-int fwd16(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int N, int d,
-          float scale, int causal, fa_stream_t stream, bool f16) {
+// Shared body of fa_fwd / fa_fwd_f16 / fa_fwd_kv: N query rows, Nk key rows.
+int fwd16(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int N, int Nk,
+          int d, float scale, int causal, fa_stream_t stream, bool f16) {
   if (!q || !k || !v || !o || !lse) return FA_ERR_NULL;
   int st = check_shape(B, H, N, d, 128);
+  if (st == kOk) st = check_shape(B, H, Nk, d, 128);
   if (st != kOk) return st;
+  if (causal && Nk < N) return FA_ERR_SHAPE;  // leading queries would see no key
   if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
   if (!isfinite(scale)) return FA_ERR_ARG;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
@@ -235,24 +237,26 @@ int fwd16(const void *q, const void *k, const void *v, void *o, float *lse, int 
   if ((st = get_encoder()) != kOk) return st;
   CUtensorMap tq, tk, tv;
   const int BH = B * H;
-  if ((st = make_map(&tq, q, BH, N, d, f16)) != kOk || (st = make_map(&tk, k, BH, N, d, f16)) != kOk ||
-      (st = make_map(&tv, v, BH, N, d, f16)) != kOk)
+  if ((st = make_map(&tq, q, BH, N, d, f16)) != kOk || (st = make_map(&tk, k, BH, Nk, d, f16)) != kOk ||
+      (st = make_map(&tv, v, BH, Nk, d, f16)) != kOk)
     return st;
   int launches = 0;
-  cudaError_t e = launch_fwd_16(tq, tk, tv, o, lse, B, H, N, d, scale, causal ? 1 : 0, f16, dev->status,
+  cudaError_t e = launch_fwd_16(tq, tk, tv, o, lse, B, H, N, Nk, d, scale, causal ? 1 : 0, f16, dev->status,
                                 dev->num_sms, reinterpret_cast<cudaStream_t>(stream), &launches);
   if (e != cudaSuccess) return record(e);
   t_last_launches = launches;
   return FA_OK;
 }
 
-// Shared body of fa_bwd / fa_bwd_f16.
+// Shared body of fa_bwd / fa_bwd_f16 / fa_bwd_kv: N query rows, Nk key rows.
 int bwd16(const void *q, const void *k, const void *v, const void *o, const float *lse, const void *dO,
-          void *dq, void *dk, void *dv, int B, int H, int N, int d, float scale, int causal, void *workspace,
-          size_t workspace_bytes, fa_stream_t stream, bool f16) {
+          void *dq, void *dk, void *dv, int B, int H, int N, int Nk, int d, float scale, int causal,
+          void *workspace, size_t workspace_bytes, fa_stream_t stream, bool f16) {
   if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return FA_ERR_NULL;
   int st = check_shape(B, H, N, d, 128);
+  if (st == kOk) st = check_shape(B, H, Nk, d, 128);
   if (st != kOk) return st;
+  if (causal && Nk < N) return FA_ERR_SHAPE;
   if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
   if (!isfinite(scale)) return FA_ERR_ARG;
   const void *ptrs[] = {q, k, v, o, dO, dq, dk, dv};
@@ -267,14 +271,14 @@ int bwd16(const void *q, const void *k, const void *v, const void *o, const floa
   if ((st = get_encoder()) != kOk) return st;
   CUtensorMap tq, tk, tv, tdo;
   const int BH = B * H;
-  if ((st = make_map(&tq, q, BH, N, d, f16)) != kOk || (st = make_map(&tk, k, BH, N, d, f16)) != kOk ||
-      (st = make_map(&tv, v, BH, N, d, f16)) != kOk || (st = make_map(&tdo, dO, BH, N, d, f16)) != kOk)
+  if ((st = make_map(&tq, q, BH, N, d, f16)) != kOk || (st = make_map(&tk, k, BH, Nk, d, f16)) != kOk ||
+      (st = make_map(&tv, v, BH, Nk, d, f16)) != kOk || (st = make_map(&tdo, dO, BH, N, d, f16)) != kOk)
     return st;
   const BwdWorkspace w = ws_layout(B, H, N, d, FA_BF16);
   char *ws = static_cast<char *>(workspace);
   int launches = 0;
   cudaError_t e = launch_bwd_16(tq, tk, tv, tdo, o, dO, lse, dq, dk, dv, reinterpret_cast<float *>(ws + w.lp),
-                                reinterpret_cast<float *>(ws + w.dp), B, H, N, d, scale, causal ? 1 : 0, f16,
+                                reinterpret_cast<float *>(ws + w.dp), B, H, N, Nk, d, scale, causal ? 1 : 0, f16,
                                 dev->status, dev->num_sms, reinterpret_cast<cudaStream_t>(stream), &launches);
   if (e != cudaSuccess) return record(e);
   t_last_launches = launches;
@@ -287,26 +291,40 @@ extern "C" {
 
 int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int N, int d,
            float scale, int causal, fa_stream_t stream) {
-  return fwd16(q, k, v, o, lse, B, H, N, d, scale, causal, stream, false);
+  return fwd16(q, k, v, o, lse, B, H, N, N, d, scale, causal, stream, false);
 }
 
 int fa_fwd_f16(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int N, int d,
                float scale, int causal, fa_stream_t stream) {
-  return fwd16(q, k, v, o, lse, B, H, N, d, scale, causal, stream, true);
+  return fwd16(q, k, v, o, lse, B, H, N, N, d, scale, causal, stream, true);
+}
+
+int fa_fwd_kv(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int Nq, int Nk,
+              int d, float scale, int causal, int dtype, fa_stream_t stream) {
+  if (dtype != FA_BF16 && dtype != FA_F16) return dtype == FA_F32 ? FA_ERR_UNSUPPORTED : FA_ERR_ARG;
+  return fwd16(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, stream, dtype == FA_F16);
 }
 
 int fa_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse, const void *dO,
            void *dq, void *dk, void *dv, int B, int H, int N, int d, float scale, int causal, void *workspace,
            size_t workspace_bytes, fa_stream_t stream) {
-  return bwd16(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, scale, causal, workspace, workspace_bytes, stream,
+  return bwd16(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, N, d, scale, causal, workspace, workspace_bytes, stream,
                false);
 }
 
 int fa_bwd_f16(const void *q, const void *k, const void *v, const void *o, const float *lse, const void *dO,
                void *dq, void *dk, void *dv, int B, int H, int N, int d, float scale, int causal,
                void *workspace, size_t workspace_bytes, fa_stream_t stream) {
-  return bwd16(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, scale, causal, workspace, workspace_bytes, stream,
+  return bwd16(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, N, d, scale, causal, workspace, workspace_bytes, stream,
                true);
+}
+
+int fa_bwd_kv(const void *q, const void *k, const void *v, const void *o, const float *lse, const void *dO,
+              void *dq, void *dk, void *dv, int B, int H, int Nq, int Nk, int d, float scale, int causal,
+              int dtype, void *workspace, size_t workspace_bytes, fa_stream_t stream) {
+  if (dtype != FA_BF16 && dtype != FA_F16) return dtype == FA_F32 ? FA_ERR_UNSUPPORTED : FA_ERR_ARG;
+  return bwd16(q, k, v, o, lse, dO, dq, dk, dv, B, H, Nq, Nk, d, scale, causal, workspace, workspace_bytes,
+               stream, dtype == FA_F16);
 }
 
 int fa_fwd_f32(const float *q, const float *k, const float *v, float *o, float *lse, int B, int H,
@@ -422,7 +440,7 @@ extern "C" int fa_bwd_static_scratch(const void *q, const void *k, const void *v
   // never leak into this one.
   int launches = 0;
   cudaError_t e = launch_bwd_16(tq, tk, tv, tdo, o, dO, lse, dq, dk, dv, reinterpret_cast<float *>(ws + w.lp),
-                                reinterpret_cast<float *>(ws + w.dp), B, H, N, d, scale, causal ? 1 : 0, false,
+                                reinterpret_cast<float *>(ws + w.dp), B, H, N, N, d, scale, causal ? 1 : 0, false,
                                 dev->status, dev->num_sms, reinterpret_cast<cudaStream_t>(stream), &launches);
   if (e != cudaSuccess) return record(e);
   t_last_launches = launches;

@@ -119,7 +119,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                     const float *__restrict__ Lp, const float *__restrict__ Dp,
-                    uint16_t *__restrict__ dk, uint16_t *__restrict__ dv, int N,
+                    uint16_t *__restrict__ dk, uint16_t *__restrict__ dv, int N, int Nk,
                     float scale, float scale_log2, int causal, int *status) {
   using C = DkdvCfg<D>;
   using E = Elt<F16>;
@@ -138,7 +138,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int kb = blockIdx.x;  // low blocks see the most query tiles under the causal mask
   const int Np = n_tiles_all * kBlk;
   const int bh = blockIdx.y;
-  const int i_first = causal ? kb : 0;
+  // N query rows, Nk >= N keys under the causal mask; key j is seen by the
+  // queries i >= j - (Nk - N) (bottom-right alignment)
+  const int off = Nk - N;
+  const int i_first = causal ? max(0, kb * kBlk - off) / kBlk : 0;
   const int n_tiles = n_tiles_all - i_first;
 
   if (threadIdx.x == 0) {
@@ -272,7 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float2 *L2 = reinterpret_cast<const float2 *>(Lst[st] + h * 64);
       const float2 *D2 = reinterpret_cast<const float2 *>(Dst[st] + h * 64);
       // queries below qmin see nothing of this key (causal); keys past N see nothing
-      const int qmin = (key >= N) ? (q0 + 64) : (causal ? key : 0);
+      const int qmin = (key >= Nk) ? (q0 + 64) : (causal ? key - off : 0);
       if (!mbar_wait_warp(&s_full, ph, &abort_flag)) { ok = false; break; }
       tc_fence_after();
       uint32_t pk[32];
@@ -320,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const uint32_t col = h ? C::tDK : C::tDV;
       const float mul = h ? scale : 1.f;
-      uint16_t *out = (h ? dk : dv) + (static_cast<size_t>(bh) * N + key) * D;
+      uint16_t *out = (h ? dk : dv) + (static_cast<size_t>(bh) * Nk + key) * D;
 #pragma unroll 1
       for (int ch = 0; ch < D / 32; ++ch) {
         uint32_t r[32];
@@ -329,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int u = 0; u < 16; ++u)
           pk2[u] = E::pack(__uint_as_float(r[2 * u]) * mul, __uint_as_float(r[2 * u + 1]) * mul);
-        store_row32(out + ch * 32, pk2, key < N);
+        store_row32(out + ch * 32, pk2, key < Nk);
       }
     }
   }
@@ -367,7 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                   const float *__restrict__ Lp, const float *__restrict__ Dp,
-                  uint16_t *__restrict__ dq, int N, float scale, float scale_log2, int causal,
+                  uint16_t *__restrict__ dq, int N, int Nk, float scale, float scale_log2, int causal,
                   int *status) {
   using C = DqCfg<D>;
   using E = Elt<F16>;
@@ -386,7 +389,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int qt = causal ? (n_tiles - 1 - static_cast<int>(blockIdx.x)) : blockIdx.x;
   const int bh = blockIdx.y;
   const int Np = n_tiles * kBlk;
-  const int n_kb = causal ? min(n_tiles, qt + 1) : n_tiles;
+  const int off = Nk - N;  // bottom-right causal alignment, as in the forward
+  const int n_kb_all = (Nk + kBlk - 1) / kBlk;
+  const int n_kb = causal ? min(n_kb_all, (qt * kBlk + kBlk - 1 + off) / kBlk + 1) : n_kb_all;
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
@@ -517,7 +522,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const size_t prow = static_cast<size_t>(bh) * Np + q;
     const float nl = Lp[prow], drow = Dp[prow];
     const uint64_t cc = f2_pack(scale_log2, scale_log2), nn = f2_pack(nl, nl);
-    const int kvis = causal ? min(N, q + 1) : N;  // keys below kvis are visible
+    const int kvis = causal ? min(Nk, q + 1 + off) : Nk;  // keys below kvis are visible
     bool ok = true;
     for (int j = 0; j < n_kb; ++j) {
       const uint32_t sb = C::tS + (j & 1) * 128 + h * 64;
@@ -588,8 +593,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int D, bool F16>
 cudaError_t launch(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtensorMap &tmV,
                    const CUtensorMap &tmdO, const void *o, const void *dO, const float *lse, void *dq,
-                   void *dk, void *dv, float *Lp, float *Dp, int B, int H, int N, float scale, int causal,
-                   int *status, cudaStream_t stream) {
+                   void *dk, void *dv, float *Lp, float *Dp, int B, int H, int N, int Nk, float scale,
+                   int causal, int *status, cudaStream_t stream) {
   const int n_tiles = (N + kBlk - 1) / kBlk;
   const int Np = n_tiles * kBlk;
   const float scale_log2 = scale * kLog2e;
@@ -602,7 +607,7 @@ cudaError_t launch(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtenso
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const dim3 grid(n_tiles, B * H);
+  const dim3 grid_kv((Nk + kBlk - 1) / kBlk, B * H), grid_q(n_tiles, B * H);
   auto kdkdv = bwd_dkdv_kernel<D, F16>;
   auto kdq = bwd_dq_kernel<D, F16>;
   if ((e = cudaFuncSetAttribute(kdkdv, cudaFuncAttributeMaxDynamicSharedMemorySize, DkdvCfg<D>::kAlloc)) !=
@@ -611,15 +616,15 @@ cudaError_t launch(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtenso
           cudaSuccess)
     return e;
   timing_begin(stream);
-  kdkdv<<<grid, kThreads, DkdvCfg<D>::kAlloc, stream>>>(tmQ, tmK, tmV, tmdO, Lp, Dp,
-                                                         static_cast<uint16_t *>(dk),
-                                                         static_cast<uint16_t *>(dv), N, scale,
+  kdkdv<<<grid_kv, kThreads, DkdvCfg<D>::kAlloc, stream>>>(tmQ, tmK, tmV, tmdO, Lp, Dp,
+                                                            static_cast<uint16_t *>(dk),
+                                                            static_cast<uint16_t *>(dv), N, Nk, scale,
                                                          scale_log2, causal, status);
   timing_end(stream);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   timing_begin(stream);
-  kdq<<<grid, kThreads, DqCfg<D>::kAlloc, stream>>>(tmQ, tmK, tmV, tmdO, Lp, Dp,
-                                                     static_cast<uint16_t *>(dq), N, scale, scale_log2,
+  kdq<<<grid_q, kThreads, DqCfg<D>::kAlloc, stream>>>(tmQ, tmK, tmV, tmdO, Lp, Dp,
+                                                       static_cast<uint16_t *>(dq), N, Nk, scale, scale_log2,
                                                      causal, status);
   timing_end(stream);
   return cudaGetLastError();
@@ -629,22 +634,22 @@ cudaError_t launch(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtenso
 
 cudaError_t launch_bwd_16(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtensorMap &tmV,
                           const CUtensorMap &tmdO, const void *o, const void *dO, const float *lse,
-                          void *dq, void *dk, void *dv, float *Lp, float *Dp, int B, int H, int N, int d,
+                          void *dq, void *dk, void *dv, float *Lp, float *Dp, int B, int H, int N, int Nk, int d,
                           float scale, int causal, bool f16, int *status, int num_sms, cudaStream_t stream,
                           int *launches) {
   (void)num_sms;
   *launches += 3;
   if (f16) {
     if (d == 64)
-      return launch<64, true>(tmQ, tmK, tmV, tmdO, o, dO, lse, dq, dk, dv, Lp, Dp, B, H, N, scale, causal,
+      return launch<64, true>(tmQ, tmK, tmV, tmdO, o, dO, lse, dq, dk, dv, Lp, Dp, B, H, N, Nk, scale, causal,
                               status, stream);
-    return launch<128, true>(tmQ, tmK, tmV, tmdO, o, dO, lse, dq, dk, dv, Lp, Dp, B, H, N, scale, causal,
+    return launch<128, true>(tmQ, tmK, tmV, tmdO, o, dO, lse, dq, dk, dv, Lp, Dp, B, H, N, Nk, scale, causal,
                              status, stream);
   }
   if (d == 64)
-    return launch<64, false>(tmQ, tmK, tmV, tmdO, o, dO, lse, dq, dk, dv, Lp, Dp, B, H, N, scale, causal,
+    return launch<64, false>(tmQ, tmK, tmV, tmdO, o, dO, lse, dq, dk, dv, Lp, Dp, B, H, N, Nk, scale, causal,
                              status, stream);
-  return launch<128, false>(tmQ, tmK, tmV, tmdO, o, dO, lse, dq, dk, dv, Lp, Dp, B, H, N, scale, causal,
+  return launch<128, false>(tmQ, tmK, tmV, tmdO, o, dO, lse, dq, dk, dv, Lp, Dp, B, H, N, Nk, scale, causal,
                             status, stream);
 }
 

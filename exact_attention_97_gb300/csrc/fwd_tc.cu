@@ -71,7 +71,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ,
                     const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, uint16_t *__restrict__ o,
-                    float *__restrict__ lse, int N, float scale, float scale_log2, int causal,
+                    float *__restrict__ lse, int N, int Nk, float scale, float scale_log2, int causal,
                     int *status) {
   using L = FwdSmem<D>;
   using E = Elt<F16>;
@@ -88,8 +88,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   // causal: longest rows first so the last wave holds the short tiles
   const int qtile = causal ? (n_qtiles - 1 - static_cast<int>(blockIdx.x)) : blockIdx.x;
   const int bh = blockIdx.y;
-  const int n_ktiles_all = (N + kBlockN - 1) / kBlockN;
-  const int n_ktiles = causal ? min(n_ktiles_all, qtile + 1) : n_ktiles_all;
+  // N query rows, Nk >= N keys under the causal mask; query i sees keys up to
+  // i + (Nk - N) (bottom-right alignment; with Nk = N the usual triangle)
+  const int off = Nk - N;
+  const int n_ktiles_all = (Nk + kBlockN - 1) / kBlockN;
+  const int n_ktiles =
+      causal ? min(n_ktiles_all, (qtile * kBlockM + kBlockM - 1 + off) / kBlockN + 1) : n_ktiles_all;
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
@@ -221,8 +225,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t sr[kBlockN];
       tmem_ld128(tmem + lane_addr + sb * 128, sr);
       const int key0 = j * kBlockN;
-      int limit = N - key0;                              // keys >= N are masked
-      if (causal) limit = min(limit, row - key0 + 1);    // keys > row are masked
+      int limit = Nk - key0;                                  // keys >= Nk are masked
+      if (causal) limit = min(limit, row + off - key0 + 1);   // keys > row + off are masked
       if (limit < kBlockN) {
 #pragma unroll
         for (int t = 0; t < kBlockN; ++t)
@@ -339,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int D, bool F16>
 cudaError_t launch(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtensorMap &tmV, void *o,
-                   float *lse, int B, int H, int N, float scale, int causal, int *status,
+                   float *lse, int B, int H, int N, int Nk, float scale, int causal, int *status,
                    cudaStream_t stream) {
   using L = FwdSmem<D>;
   auto kern = fwd_kernel<D, F16>;
@@ -348,7 +352,7 @@ cudaError_t launch(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtenso
   dim3 grid((N + kBlockM - 1) / kBlockM, B * H);
   timing_begin(stream);
   kern<<<grid, kThreads, L::kAlloc, stream>>>(tmQ, tmK, tmV, static_cast<uint16_t *>(o), lse,
-                                               N, scale, scale * 1.4426950408889634f, causal,
+                                               N, Nk, scale, scale * 1.4426950408889634f, causal,
                                                status);
   timing_end(stream);
   return cudaGetLastError();
@@ -357,16 +361,16 @@ cudaError_t launch(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtenso
 }  // namespace
 
 cudaError_t launch_fwd_16(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtensorMap &tmV,
-                          void *o, float *lse, int B, int H, int N, int d, float scale, int causal,
+                          void *o, float *lse, int B, int H, int N, int Nk, int d, float scale, int causal,
                           bool f16, int *status, int num_sms, cudaStream_t stream, int *launches) {
   (void)num_sms;
   *launches += 1;
   if (f16) {
-    if (d == 64) return launch<64, true>(tmQ, tmK, tmV, o, lse, B, H, N, scale, causal, status, stream);
-    return launch<128, true>(tmQ, tmK, tmV, o, lse, B, H, N, scale, causal, status, stream);
+    if (d == 64) return launch<64, true>(tmQ, tmK, tmV, o, lse, B, H, N, Nk, scale, causal, status, stream);
+    return launch<128, true>(tmQ, tmK, tmV, o, lse, B, H, N, Nk, scale, causal, status, stream);
   }
-  if (d == 64) return launch<64, false>(tmQ, tmK, tmV, o, lse, B, H, N, scale, causal, status, stream);
-  return launch<128, false>(tmQ, tmK, tmV, o, lse, B, H, N, scale, causal, status, stream);
+  if (d == 64) return launch<64, false>(tmQ, tmK, tmV, o, lse, B, H, N, Nk, scale, causal, status, stream);
+  return launch<128, false>(tmQ, tmK, tmV, o, lse, B, H, N, Nk, scale, causal, status, stream);
 }
 
 }  // namespace fa

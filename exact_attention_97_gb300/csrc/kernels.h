@@ -35,11 +35,12 @@ cudaError_t launch_bwd_f32(const float *q, const float *k, const float *v, const
                            int B, int H, int N, int d, float scale, int causal, float *D,
                            cudaStream_t stream, int *launches);
 
+// N query rows and Nk key rows per head (causal: bottom-right aligned, Nk >= N).
 // 16-bit tensor-core forward (bf16, or f16 when `f16`). tmQ/tmK/tmV are 3-D
 // tensor maps {d, N, B*H} of that element type with a {64, 128, 1} box and
 // 128-byte swizzle.
 cudaError_t launch_fwd_16(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtensorMap &tmV,
-                          void *o, float *lse, int B, int H, int N, int d, float scale, int causal,
+                          void *o, float *lse, int B, int H, int N, int Nk, int d, float scale, int causal,
                           bool f16, int *status, int num_sms, cudaStream_t stream, int *launches);
 
 // 16-bit tensor-core backward (three kernels: row terms, dK/dV pass, dQ
@@ -47,7 +48,7 @@ cudaError_t launch_fwd_16(const CUtensorMap &tmQ, const CUtensorMap &tmK, const 
 // caller's workspace.
 cudaError_t launch_bwd_16(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtensorMap &tmV,
                           const CUtensorMap &tmdO, const void *o, const void *dO, const float *lse,
-                          void *dq, void *dk, void *dv, float *Lp, float *Dp, int B, int H, int N, int d,
+                          void *dq, void *dk, void *dv, float *Lp, float *Dp, int B, int H, int N, int Nk, int d,
                           float scale, int causal, bool f16, int *status, int num_sms, cudaStream_t stream,
                           int *launches);
 

@@ -27,6 +27,21 @@ class Workload:
     d: int
     causal: bool
     seed: int = 0
+    Nk: int = 0  # key/value rows per head; 0 means N (the square problem)
+
+    @property
+    def n_keys(self) -> int:
+        return self.Nk or self.N
+
+    def pairs_per_head(self) -> float:
+        """(query, key) pairs inside the mask: Nq*Nk, or under the causal mask
+        aligned bottom-right (query i sees keys j <= i + Nk - Nq) the sum of
+        min(Nk, i + 1 + Nk - Nq) over the Nq queries."""
+        nq, nk = self.N, self.n_keys
+        if not self.causal:
+            return float(nq) * nk
+        off = nk - nq
+        return float(nq) * off + nq * (nq + 1) / 2.0
 
     @property
     def scale(self) -> float:
@@ -37,9 +52,13 @@ class Workload:
         return torch.bfloat16 if self.dtype == "bf16" else torch.float32
 
     def flops_fwd(self) -> float:
-        """4*B*H*N^2*d (two contractions), halved under the causal mask."""
-        f = 4.0 * self.B * self.H * self.N * self.N * self.d
-        return f / 2 if self.causal else f
+        """4*d per (query, key) pair in the mask (two contractions): 4*B*H*N^2*d for
+        the square problem, halved under the causal mask (the N/2 diagonal term of
+        the exact pair count is dropped, as in the usual convention)."""
+        if self.n_keys == self.N:
+            f = 4.0 * self.B * self.H * self.N * self.N * self.d
+            return f / 2 if self.causal else f
+        return 4.0 * self.B * self.H * self.d * self.pairs_per_head()
 
     def flops_bwd(self) -> float:
         """2.5x the forward count (five contractions instead of two)."""

@@ -120,6 +120,28 @@ int fa_bwd_f16(const void *q, const void *k, const void *v, const void *o,
                int B, int H, int N, int d, float scale, int causal,
                void *workspace, size_t workspace_bytes, fa_stream_t stream);
 
+/*
+ * Forward and backward with Nq query rows against Nk key/value rows per head
+ * (decode and chunked-prefill shapes; the blog's setting is a 64K-token
+ * inference service, and the tutorial's section 06 lists query and key
+ * lengths as separate parameters). Q, O, dO, dQ are [B][H][Nq][d]; K, V, dK,
+ * dV are [B][H][Nk][d]; lse is [B][H][Nq]. dtype is FA_BF16 or FA_F16
+ * (FA_F32 returns FA_ERR_UNSUPPORTED). With causal != 0 the mask is aligned
+ * at the bottom right: query i sees key j iff j <= i + (Nk - Nq), so the
+ * queries act as the last Nq rows of the square problem; that requires
+ * Nk >= Nq (else FA_ERR_SHAPE). The backward's workspace is
+ * fa_bwd_workspace_size(B, H, Nq, d, dtype) bytes. Everything else is as for
+ * fa_fwd / fa_bwd; fa_fwd(...) is fa_fwd_kv(..., N, N, ..., FA_BF16, ...).
+ */
+int fa_fwd_kv(const void *q, const void *k, const void *v, void *o, float *lse,
+              int B, int H, int Nq, int Nk, int d, float scale, int causal,
+              int dtype, fa_stream_t stream);
+int fa_bwd_kv(const void *q, const void *k, const void *v, const void *o,
+              const float *lse, const void *dO, void *dq, void *dk, void *dv,
+              int B, int H, int Nq, int Nk, int d, float scale, int causal,
+              int dtype, void *workspace, size_t workspace_bytes,
+              fa_stream_t stream);
+
 /* Forward with float tensors (all fp32 arithmetic, exact expf). Same
  * arguments and layout as fa_fwd with float element type. */
 int fa_fwd_f32(const float *q, const float *k, const float *v, float *o,

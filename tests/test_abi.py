@@ -115,6 +115,19 @@ def test_f16_argument_errors(lib):
     assert lib.fa_bwd_f16(*ptrs, 1, 1, 128, 64, float("nan"), 0, P, 1 << 30, None) == 9
 
 
+def test_kv_argument_errors(lib):
+    args = [P] * 5
+    # causal with fewer keys than queries: the leading queries would see nothing
+    assert lib.fa_fwd_kv(*args, 1, 1, 300, 200, 64, 0.125, 1, fa.FA_BF16, None) == 2
+    assert lib.fa_fwd_kv(*args, 1, 1, 300, 0, 64, 0.125, 0, fa.FA_BF16, None) == 2
+    assert lib.fa_fwd_kv(*args, 1, 1, 300, 200, 64, 0.125, 0, fa.FA_F32, None) == 3
+    assert lib.fa_fwd_kv(*args, 1, 1, 300, 200, 64, 0.125, 0, 7, None) == 9
+    ptrs = [P] * 9
+    assert lib.fa_bwd_kv(*ptrs, 1, 1, 100, 64, 64, 0.125, 1, fa.FA_F16, P, 1 << 30, None) == 2
+    need = fa.fa_bwd_workspace_size(1, 1, 100, 64, fa.FA_F16)
+    assert lib.fa_bwd_kv(*ptrs, 1, 1, 100, 640, 64, 0.125, 1, fa.FA_F16, P, need - 16, None) == 5
+
+
 def test_f32_argument_errors(lib):
     args = [P] * 5
     assert lib.fa_fwd_f32(None, *args[1:], 1, 1, 4, 2, 1.0, 0, None) == 1

@@ -137,6 +137,48 @@ def test_f16_B2_H4_N1024_d128_and_large_scores(causal):
           _full_ref(_np(q), _np(k), _np(v), _np(dO), scale, causal))
 
 
+# ------------------------------------------------------------ Nq queries against Nk keys
+
+def _run_gpu_kv(q, k, v, dO, scale, causal):
+    import exact_attention_97_gb300 as fa
+    dev = torch.device("cuda")
+    qd, kd, vd, dod = (x.to(dev) for x in (q, k, v, dO))
+    nan = float("nan")
+    o = torch.full_like(qd, nan)
+    lse = torch.full(tuple(q.shape[:3]), nan, device=dev, dtype=torch.float32)
+    fa.attention_forward(qd, kd, vd, scale, causal, out=o, lse=lse)
+    grads = (torch.full_like(qd, nan), torch.full_like(kd, nan), torch.full_like(vd, nan))
+    fa.attention_backward(qd, kd, vd, o, lse, dod, scale, causal, grads=grads)
+    torch.cuda.synchronize()
+    assert fa.fa_device_status() == 0
+    return dict(zip(("o", "lse", "dq", "dk", "dv"), (t.float().cpu().double().numpy() for t in (o, lse, *grads))))
+
+
+@pytest.mark.parametrize("Nq,Nk,causal", [(1, 300, True), (1, 300, False), (128, 1000, True), (100, 640, True),
+                                          (257, 511, True), (300, 130, False), (640, 641, True)])
+@pytest.mark.parametrize("d", [64, 128])
+def test_bf16_kv_lengths(Nq, Nk, causal, d):
+    """Decode / chunked-prefill shapes: causal mask aligned bottom-right."""
+    q, _, _, dO = make_qkv_do(1, 2, Nq, d, seed=300 + Nq, dtype=torch.bfloat16)
+    _, k, v, _ = make_qkv_do(1, 2, Nk, d, seed=400 + Nk, dtype=torch.bfloat16)
+    scale = 1.0 / math.sqrt(d)
+    got = _run_gpu_kv(q, k, v, dO, scale, causal)
+    o, lse = oracle.attention_fwd_kv(_np(q), _np(k), _np(v), scale, causal)
+    dq, dk, dv = oracle.attention_bwd_kv(_np(q), _np(k), _np(v), _np(dO), scale, causal)
+    check(f"bf16_kv_Nq{Nq}_Nk{Nk}_d{d}_c{int(causal)}", "bf16", got,
+          {"o": o, "lse": lse, "dq": dq, "dk": dk, "dv": dv})
+
+
+def test_f16_kv_lengths():
+    q, _, _, dO = make_qkv_do(2, 2, 200, 128, seed=5, dtype=torch.float16)
+    _, k, v, _ = make_qkv_do(2, 2, 777, 128, seed=6, dtype=torch.float16)
+    scale = 1.0 / math.sqrt(128)
+    got = _run_gpu_kv(q, k, v, dO, scale, True)
+    o, lse = oracle.attention_fwd_kv(_np(q), _np(k), _np(v), scale, True)
+    dq, dk, dv = oracle.attention_bwd_kv(_np(q), _np(k), _np(v), _np(dO), scale, True)
+    check("f16_kv_Nq200_Nk777_d128_c1", "bf16", got, {"o": o, "lse": lse, "dq": dq, "dk": dk, "dv": dv})
+
+
 def test_bf16_causal_B1_H8_N1024_d64():
     w = WORKLOADS["bf16_causal_B1_H8_N1024_d64"]
     q, k, v, dO = make_qkv_do(w.B, w.H, w.N, w.d, w.seed, torch.bfloat16)
