@@ -10,10 +10,13 @@
 //     l' = alpha l + rowsum p, u' = alpha u + p V,   o = u / l,
 // and the saved statistic L = m + ln l of its section 04.
 //
-// GB300 design (one CTA = one 128-row query tile of one (batch, head)):
-//   warp 0      loader: Q once, then K_j into a ring of kStages shared-memory
-//               stages (128-byte swizzle, 3-D tensor maps so rows past N read
-//               as zero).
+// GB300 design: a persistent grid, one CTA per SM, each CTA walking a static
+// list of 128-row query tiles (see FwdSched); within a CTA:
+//   warp 0      loader: Q of each tile, then K_j into a ring of kStages
+//               shared-memory stages (128-byte swizzle, 3-D tensor maps so
+//               rows past N read as zero). The rings and barrier phases run
+//               on across tiles, so the next tile's loads and S MMAs overlap
+//               the current tile's last P V products and its epilogue.
 //   warp 2      loader of V_j (its own ring); also allocates and frees the
 //               512 tensor-memory (TMEM) columns.
 //   warp 1      MMA issuer for S_j = Q K_j^T into one of three TMEM buffers,
@@ -36,7 +39,10 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <algorithm>
+
 #include "kernels.h"
+#include "tile_sched.h"
 #include "sm103.cuh"
 
 namespace fa {
@@ -44,20 +50,30 @@ namespace {
 
 constexpr int kBlockM = 128;   // query rows per tile (= TMEM lanes)
 constexpr int kBlockN = 128;   // keys per tile
-constexpr int kStages = 3;     // K and V ring depth
+constexpr int kStages = 3;     // K ring depth
 constexpr int kSBuf = 3;       // S buffers in TMEM (3 x 128 columns, O after them)
 constexpr int kThreads = 256;  // 8 warps
 constexpr float kRescaleLog2 = 8.0f;  // move the running max only past 2^8
 constexpr float kLn2 = 0.69314718055994531f;
 
+#ifndef FA_FWD_QBUF
+#define FA_FWD_QBUF 2
+#endif
+
+// Shared memory: kQBuf query tiles (two let the next tile's Q land while the
+// current tile still runs), the K ring and the V ring. At d = 128 two Q
+// buffers and three K stages leave room for two V stages under the 227 KB
+// limit.
 template <int D>
 struct FwdSmem {
+  static constexpr int kQBuf = FA_FWD_QBUF;
+  static constexpr int kVStages = (D == 128 && kQBuf == 2) ? 2 : 3;
   static constexpr int kTileBytes = kBlockN * D * 2;  // one 128 x D bf16 tile
   static constexpr int kSubBytes = kBlockN * 128;     // one 128 x 64 sub-tile
   static constexpr int kQ = 0;
-  static constexpr int kK = kQ + kTileBytes;
+  static constexpr int kK = kQ + kQBuf * kTileBytes;
   static constexpr int kV = kK + kStages * kTileBytes;
-  static constexpr int kBytes = kV + kStages * kTileBytes;
+  static constexpr int kBytes = kV + kVStages * kTileBytes;
   static constexpr int kAlloc = kBytes + 1024;  // slack for 1024-byte alignment
 };
 
@@ -71,36 +87,43 @@ __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ,
                     const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, uint16_t *__restrict__ o,
-                    float *__restrict__ lse, int N, int Nk, float scale, float scale_log2, int causal,
-                    int *status) {
+                    float *__restrict__ lse, int N, int Nk, const __grid_constant__ TileSched sched, float scale,
+                    float scale_log2, int causal, int *status) {
   using L = FwdSmem<D>;
   using E = Elt<F16>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
-  __shared__ uint64_t q_full, k_full[kStages], k_empty[kStages], v_full[kStages],
-      v_empty[kStages], s_full[kSBuf], p_ready[kSBuf], pv_done[kSBuf], drain_s, drain_pv;
+  constexpr int kQBuf = L::kQBuf, kVStages = L::kVStages;
+  __shared__ uint64_t q_full[kQBuf], q_empty[kQBuf], k_full[kStages], k_empty[kStages], v_full[kVStages],
+      v_empty[kVStages], s_full[kSBuf], p_ready[kSBuf], pv_done[kSBuf], drain_s, drain_pv;
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_flag;
 
   const int warp = warp_id(), lane = lane_id();
-  const int n_qtiles = (N + kBlockM - 1) / kBlockM;
-  // causal: longest rows first so the last wave holds the short tiles
-  const int qtile = causal ? (n_qtiles - 1 - static_cast<int>(blockIdx.x)) : blockIdx.x;
-  const int bh = blockIdx.y;
+  const int n_qtiles = sched.nt;
+  // schedule rank 0 is a head's most expensive query tile (the last one
+  // under the causal mask)
+  auto qtile_of = [&](int rank) { return causal ? n_qtiles - 1 - rank : rank; };
   // N query rows, Nk >= N keys under the causal mask; query i sees keys up to
   // i + (Nk - N) (bottom-right alignment; with Nk = N the usual triangle)
   const int off = Nk - N;
   const int n_ktiles_all = (Nk + kBlockN - 1) / kBlockN;
-  const int n_ktiles =
-      causal ? min(n_ktiles_all, (qtile * kBlockM + kBlockM - 1 + off) / kBlockN + 1) : n_ktiles_all;
+  auto ktiles = [&](int qtile) {
+    return causal ? min(n_ktiles_all, (qtile * kBlockM + kBlockM - 1 + off) / kBlockN + 1) : n_ktiles_all;
+  };
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
-    mbar_init(&q_full, 1);
+    for (int b = 0; b < kQBuf; ++b) {
+      mbar_init(&q_full[b], 1);
+      mbar_init(&q_empty[b], 1);
+    }
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&k_empty[s], 1);
+    }
+    for (int s = 0; s < kVStages; ++s) {
       mbar_init(&v_full[s], 1);
       mbar_init(&v_empty[s], 1);
     }
@@ -123,62 +146,109 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = tmem_base_s;
   const uint32_t tmem_O = tmem + kSBuf * 128;
 
+  // Every role walks the same item sequence. Key tiles are counted across
+  // items (kt), so the K/V rings, the S buffers and their barrier phases run
+  // on without a break from one item to the next; `it` counts items (phase of
+  // q_full / q_empty).
   if (warp == 0) {
     // ------------------------------------------------------------ loader: Q, K
+    // Q of item `it` goes into buffer it % kQBuf once every S MMA of the item
+    // that used it before has completed (q_empty); it is also prefetched into
+    // L2 one item ahead.
     if (lane == 0) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
-      mbar_arrive_expect_tx(&q_full, L::kTileBytes);
-      load_tile(smem + L::kQ, &tmQ, &q_full, D, qtile * kBlockM, bh);
-      int issued = 0;
-      for (int j = 0; j < n_ktiles; ++j) {
-        const int st = j % kStages;
-        if (j >= kStages && !mbar_wait(&k_empty[st], ((j / kStages) & 1) ^ 1, &abort_flag)) break;
-        mbar_arrive_expect_tx(&k_full[st], L::kTileBytes);
-        load_tile(smem + L::kK + st * L::kTileBytes, &tmK, &k_full[st], D, j * kBlockN, bh);
-        ++issued;
+      bool ok = true;
+      int kt = 0, it = 0, rank, bh;
+      for (int k = 0; ok; ++k) {
+        const int step = sched_item(sched, blockIdx.x, k, rank, bh);
+        if (step == kDone) break;
+        if (step == kSkip) continue;
+        const int qtile = qtile_of(rank);
+        {  // L2 prefetch of the next item's Q
+          int nr, nbh, ns, k2 = k + 1;
+          while ((ns = sched_item(sched, blockIdx.x, k2, nr, nbh)) == kSkip) ++k2;
+          if (ns == kItem)
+            for (int x = 0; x < D; x += 64) tma_prefetch_l2_3d(&tmQ, x, qtile_of(nr) * kBlockM, nbh);
+        }
+        const int qb = it % kQBuf;
+        if (it >= kQBuf && !mbar_wait(&q_empty[qb], ((it / kQBuf) & 1) ^ 1, &abort_flag)) { ok = false; break; }
+        mbar_arrive_expect_tx(&q_full[qb], L::kTileBytes);
+        load_tile(smem + L::kQ + qb * L::kTileBytes, &tmQ, &q_full[qb], D, qtile * kBlockM, bh);
+        const int nk = ktiles(qtile);
+        for (int j = 0; j < nk; ++j, ++kt) {
+          const int st = kt % kStages;
+          if (kt >= kStages && !mbar_wait(&k_empty[st], ((kt / kStages) & 1) ^ 1, &abort_flag)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&k_full[st], L::kTileBytes);
+          load_tile(smem + L::kK + st * L::kTileBytes, &tmK, &k_full[st], D, j * kBlockN, bh);
+        }
+        ++it;  // this item's Q load was issued
       }
       // teardown: every issued copy must land before the CTA's memory is released
-      mbar_wait_drain(&q_full, 0);
-      for (int j = max(0, issued - kStages); j < issued; ++j)
-        mbar_wait_drain(&k_full[j % kStages], (j / kStages) & 1);
+      for (int i = max(0, it - kQBuf); i < it; ++i) mbar_wait_drain(&q_full[i % kQBuf], (i / kQBuf) & 1);
+      for (int j = max(0, kt - kStages); j < kt; ++j) mbar_wait_drain(&k_full[j % kStages], (j / kStages) & 1);
     }
   } else if (warp == 2) {
     // ---------------------------------------------------------------- loader: V
     if (lane == 0) {
       tma_prefetch_desc(&tmV);
-      int issued = 0;
-      for (int j = 0; j < n_ktiles; ++j) {
-        const int st = j % kStages;
-        if (j >= kStages && !mbar_wait(&v_empty[st], ((j / kStages) & 1) ^ 1, &abort_flag)) break;
-        mbar_arrive_expect_tx(&v_full[st], L::kTileBytes);
-        load_tile(smem + L::kV + st * L::kTileBytes, &tmV, &v_full[st], D, j * kBlockN, bh);
-        ++issued;
+      bool ok = true;
+      int kt = 0, rank, bh;
+      for (int k = 0; ok; ++k) {
+        const int step = sched_item(sched, blockIdx.x, k, rank, bh);
+        if (step == kDone) break;
+        if (step == kSkip) continue;
+        const int nk = ktiles(qtile_of(rank));
+        for (int j = 0; j < nk; ++j, ++kt) {
+          const int st = kt % kVStages;
+          if (kt >= kVStages && !mbar_wait(&v_empty[st], ((kt / kVStages) & 1) ^ 1, &abort_flag)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&v_full[st], L::kTileBytes);
+          load_tile(smem + L::kV + st * L::kTileBytes, &tmV, &v_full[st], D, j * kBlockN, bh);
+        }
       }
-      for (int j = max(0, issued - kStages); j < issued; ++j)
-        mbar_wait_drain(&v_full[j % kStages], (j / kStages) & 1);
+      for (int j = max(0, kt - kVStages); j < kt; ++j) mbar_wait_drain(&v_full[j % kVStages], (j / kVStages) & 1);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------ MMA issuer: S = Q K^T
-    // S_j goes to buffer j % 3 once P_{j-3} (which lived there) has been used.
+    // S of key tile kt goes to buffer kt % 3 once P V of tile kt - 3 (which
+    // used that buffer) has completed.
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_16(kBlockM, kBlockN, false, false, F16);
-      const uint32_t q_addr = smem_u32(smem + L::kQ);
-      bool ok = mbar_wait(&q_full, 0, &abort_flag);
-      for (int j = 0; ok && j < n_ktiles; ++j) {
-        const int st = j % kStages, sb = j % kSBuf;
-        if (j >= kSBuf && !mbar_wait(&pv_done[sb], ((j / kSBuf) - 1) & 1, &abort_flag)) { ok = false; break; }
-        if (!mbar_wait(&k_full[st], (j / kStages) & 1, &abort_flag)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t k_addr = smem_u32(smem + L::kK + st * L::kTileBytes);
+      bool ok = true;
+      int kt = 0, it = 0;
+      int rank, bh;
+      for (int k = 0; ok; ++k) {
+        const int step = sched_item(sched, blockIdx.x, k, rank, bh);
+        if (step == kDone) break;
+        if (step == kSkip) continue;
+        const int qtile = qtile_of(rank);
+        const int nk = ktiles(qtile);
+        const int qb = it % kQBuf;
+        const uint32_t q_addr = smem_u32(smem + L::kQ + qb * L::kTileBytes);
+        if (!mbar_wait(&q_full[qb], (it / kQBuf) & 1, &abort_flag)) { ok = false; break; }
+        for (int j = 0; j < nk; ++j, ++kt) {
+          const int st = kt % kStages, sb = kt % kSBuf;
+          if (kt >= kSBuf && !mbar_wait(&pv_done[sb], ((kt / kSBuf) - 1) & 1, &abort_flag)) { ok = false; break; }
+          if (!mbar_wait(&k_full[st], (kt / kStages) & 1, &abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t k_addr = smem_u32(smem + L::kK + st * L::kTileBytes);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk / 4) * L::kSubBytes + (kk % 4) * 32;
-          mma_ss(tmem + sb * 128, sdesc_sw128(q_addr + off, 16, 1024), sdesc_sw128(k_addr + off, 16, 1024),
-                 idesc_s, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk / 4) * L::kSubBytes + (kk % 4) * 32;
+            mma_ss(tmem + sb * 128, sdesc_sw128(q_addr + off, 16, 1024), sdesc_sw128(k_addr + off, 16, 1024),
+                   idesc_s, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(&s_full[sb]);
+          mma_commit(&k_empty[st]);
         }
-        mma_commit(&s_full[sb]);
-        mma_commit(&k_empty[st]);
+        mma_commit(&q_empty[qb]);  // this Q buffer is free once the item's S MMAs are done
+        ++it;
       }
       // teardown: all issued MMAs finish before TMEM is released
       mma_commit(&drain_s);
@@ -187,22 +257,33 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 3) {
     // ---------------------------------------------------- MMA issuer: O += P V
     // A second issuing thread, so the tensor pipe always has one of the two
-    // streams queued while the other waits on its barriers.
+    // streams queued while the other waits on its barriers. The first P V of
+    // an item overwrites O: its P is only marked ready after the softmax warps
+    // have read the previous item's O out of TMEM.
     if (lane == 0) {
       constexpr uint32_t idesc_o = idesc_16(kBlockM, D, false, true, F16);
       bool ok = true;
-      for (int j = 0; ok && j < n_ktiles; ++j) {
-        const int st = j % kStages, sb = j % kSBuf;
-        if (!mbar_wait(&p_ready[sb], (j / kSBuf) & 1, &abort_flag)) { ok = false; break; }
-        if (!mbar_wait(&v_full[st], (j / kStages) & 1, &abort_flag)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t v_addr = smem_u32(smem + L::kV + st * L::kTileBytes);
+      int kt = 0;
+      int rank, bh;
+      for (int k = 0; ok; ++k) {
+        const int step = sched_item(sched, blockIdx.x, k, rank, bh);
+        if (step == kDone) break;
+        if (step == kSkip) continue;
+        const int qtile = qtile_of(rank);
+        const int nk = ktiles(qtile);
+        for (int j = 0; j < nk; ++j, ++kt) {
+          const int st = kt % kVStages, sb = kt % kSBuf;
+          if (!mbar_wait(&p_ready[sb], (kt / kSBuf) & 1, &abort_flag)) { ok = false; break; }
+          if (!mbar_wait(&v_full[st], (kt / kVStages) & 1, &abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t v_addr = smem_u32(smem + L::kV + st * L::kTileBytes);
 #pragma unroll
-        for (int kk = 0; kk < kBlockN / 16; ++kk)
-          mma_ts(tmem_O, tmem + sb * 128 + kk * 8, sdesc_sw128(v_addr + kk * 2048, L::kSubBytes, 1024), idesc_o,
-                 (j > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&v_empty[st]);
-        mma_commit(&pv_done[sb]);
+          for (int kk = 0; kk < kBlockN / 16; ++kk)
+            mma_ts(tmem_O, tmem + sb * 128 + kk * 8, sdesc_sw128(v_addr + kk * 2048, L::kSubBytes, 1024),
+                   idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(&v_empty[st]);
+          mma_commit(&pv_done[sb]);
+        }
       }
       mma_commit(&drain_pv);
       mbar_wait_drain(&drain_pv, 0);
@@ -211,104 +292,117 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ----------------------------------------------------------------- softmax
     const int wq = warp - 4;                 // TMEM lane quarter of this warp
     const int r_local = wq * 32 + lane;      // row within the tile
-    const int row = qtile * kBlockM + r_local;
     const uint32_t lane_addr = static_cast<uint32_t>(wq * 32) << 16;
-    float m_used = -INFINITY, l_sum = 0.f;
     bool ok = true;
-    for (int j = 0; j < n_ktiles; ++j) {
-      const int sb = j % kSBuf;
-      if (!mbar_wait_warp(&s_full[sb], (j / kSBuf) & 1, &abort_flag)) {
+    int kt = 0;
+    int rank, bh;
+    for (int k = 0; ok; ++k) {
+      const int step = sched_item(sched, blockIdx.x, k, rank, bh);
+      if (step == kDone) break;
+      if (step == kSkip) continue;
+      const int qtile = qtile_of(rank);
+      const int nk = ktiles(qtile);
+      const int row = qtile * kBlockM + r_local;
+      float m_used = -INFINITY, l_sum = 0.f;
+      for (int j = 0; j < nk; ++j, ++kt) {
+        const int sb = kt % kSBuf;
+        if (!mbar_wait_warp(&s_full[sb], (kt / kSBuf) & 1, &abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t sr[kBlockN];
+        tmem_ld128(tmem + lane_addr + sb * 128, sr);
+        const int key0 = j * kBlockN;
+        int limit = Nk - key0;                                  // keys >= Nk are masked
+        if (causal) limit = min(limit, row + off - key0 + 1);   // keys > row + off are masked
+        if (limit < kBlockN) {
+#pragma unroll
+          for (int t = 0; t < kBlockN; ++t)
+            if (t >= limit) sr[t] = __float_as_uint(-INFINITY);
+        }
+        // row max: four independent chains of 3-input max
+        float mx;
+        {
+          float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
+#pragma unroll
+          for (int t = 0; t < kBlockN; t += 8) {
+            m0 = fmax3(m0, __uint_as_float(sr[t]), __uint_as_float(sr[t + 1]));
+            m1 = fmax3(m1, __uint_as_float(sr[t + 2]), __uint_as_float(sr[t + 3]));
+            m2 = fmax3(m2, __uint_as_float(sr[t + 4]), __uint_as_float(sr[t + 5]));
+            m3 = fmax3(m3, __uint_as_float(sr[t + 6]), __uint_as_float(sr[t + 7]));
+          }
+          mx = fmax3(m0, m1, fmaxf(m2, m3));
+        }
+        if (j == 0) {
+          m_used = mx;
+        } else {
+          const bool need = (mx - m_used) * scale_log2 > kRescaleLog2;
+          if (__any_sync(0xffffffffu, need)) {
+            // O must hold P_{kt-1} V_{kt-1} before it is rescaled. Wait on
+            // that product's own buffer barrier: its previous phase (tile
+            // kt - 4) is known complete because S of tile kt - 1 was only
+            // issued after it, so a stale phase cannot match the parity.
+            if (!mbar_wait_warp(&pv_done[(kt - 1) % kSBuf], ((kt - 1) / kSBuf) & 1, &abort_flag)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const float alpha = need ? ex2_approx((m_used - mx) * scale_log2) : 1.f;
+            if (need) {
+              l_sum *= alpha;
+              m_used = mx;
+            }
+#pragma unroll 1
+            for (int ch = 0; ch < D / 32; ++ch) {
+              uint32_t r[32];
+              tmem_ld32(tmem_O + lane_addr + ch * 32, r);
+#pragma unroll
+              for (int t = 0; t < 32; ++t) r[t] = __float_as_uint(__uint_as_float(r[t]) * alpha);
+              tmem_st32(tmem_O + lane_addr + ch * 32, r);
+            }
+          }
+        }
+        // P = 2^(s*c - m*c), two columns at a time
+        const float neg = -m_used * scale_log2;
+        const uint64_t cc = f2_pack(scale_log2, scale_log2), nn = f2_pack(neg, neg);
+        uint64_t acc0 = 0, acc1 = 0, acc2 = 0, acc3 = 0;  // packed partial row sums (+0.0f pairs)
+        uint32_t pk[kBlockN / 2];
+#pragma unroll
+        for (int w = 0; w < kBlockN / 2; ++w) {
+          const uint64_t x2 = f2_fma(f2_pack(__uint_as_float(sr[2 * w]), __uint_as_float(sr[2 * w + 1])), cc, nn);
+          float x0, x1;
+          f2_unpack(x2, x0, x1);
+          const uint64_t p2 = f2_pack(ex2_approx(x0), ex2_approx(x1));
+          switch (w & 3) {
+            case 0: acc0 = f2_add(acc0, p2); break;
+            case 1: acc1 = f2_add(acc1, p2); break;
+            case 2: acc2 = f2_add(acc2, p2); break;
+            default: acc3 = f2_add(acc3, p2); break;
+          }
+          float p0, p1;
+          f2_unpack(p2, p0, p1);
+          pk[w] = E::pack(p0, p1);
+        }
+        tmem_st64(tmem + lane_addr + sb * 128, pk);
+        float rs;
+        {
+          float a0, a1;
+          f2_unpack(f2_add(f2_add(acc0, acc1), f2_add(acc2, acc3)), a0, a1);
+          rs = a0 + a1;
+        }
+        l_sum += rs;
+        tc_fence_before();
+        mbar_arrive(&p_ready[sb]);
+      }
+      // -------------------------------------------------------------- epilogue
+      // the item's last P V (and, issued in order before it, every other
+      // one) is done; the next item's first P V waits for this warp's next
+      // p_ready arrival, which comes after these TMEM reads
+      if (!ok || !mbar_wait_warp(&pv_done[(kt - 1) % kSBuf], ((kt - 1) / kSBuf) & 1, &abort_flag)) {
         ok = false;
         break;
       }
-      tc_fence_after();
-      uint32_t sr[kBlockN];
-      tmem_ld128(tmem + lane_addr + sb * 128, sr);
-      const int key0 = j * kBlockN;
-      int limit = Nk - key0;                                  // keys >= Nk are masked
-      if (causal) limit = min(limit, row + off - key0 + 1);   // keys > row + off are masked
-      if (limit < kBlockN) {
-#pragma unroll
-        for (int t = 0; t < kBlockN; ++t)
-          if (t >= limit) sr[t] = __float_as_uint(-INFINITY);
-      }
-      // row max: four independent chains of 3-input max
-      float mx;
-      {
-        float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
-#pragma unroll
-        for (int t = 0; t < kBlockN; t += 8) {
-          m0 = fmax3(m0, __uint_as_float(sr[t]), __uint_as_float(sr[t + 1]));
-          m1 = fmax3(m1, __uint_as_float(sr[t + 2]), __uint_as_float(sr[t + 3]));
-          m2 = fmax3(m2, __uint_as_float(sr[t + 4]), __uint_as_float(sr[t + 5]));
-          m3 = fmax3(m3, __uint_as_float(sr[t + 6]), __uint_as_float(sr[t + 7]));
-        }
-        mx = fmax3(m0, m1, fmaxf(m2, m3));
-      }
-      if (j == 0) {
-        m_used = mx;
-      } else {
-        const bool need = (mx - m_used) * scale_log2 > kRescaleLog2;
-        if (__any_sync(0xffffffffu, need)) {
-          // O must hold P_{j-1} V_{j-1} before it is rescaled. Wait on that
-          // product's own buffer barrier: its previous phase (P_{j-4} V_{j-4})
-          // is known complete because S_{j-1} was only issued after it, so
-          // the parity cannot be matched by a stale phase.
-          if (!mbar_wait_warp(&pv_done[(j - 1) % kSBuf], ((j - 1) / kSBuf) & 1, &abort_flag)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const float alpha = need ? ex2_approx((m_used - mx) * scale_log2) : 1.f;
-          if (need) {
-            l_sum *= alpha;
-            m_used = mx;
-          }
-#pragma unroll 1
-          for (int ch = 0; ch < D / 32; ++ch) {
-            uint32_t r[32];
-            tmem_ld32(tmem_O + lane_addr + ch * 32, r);
-#pragma unroll
-            for (int t = 0; t < 32; ++t) r[t] = __float_as_uint(__uint_as_float(r[t]) * alpha);
-            tmem_st32(tmem_O + lane_addr + ch * 32, r);
-          }
-        }
-      }
-      // P = 2^(s*c - m*c), two columns at a time
-      const float neg = -m_used * scale_log2;
-      const uint64_t cc = f2_pack(scale_log2, scale_log2), nn = f2_pack(neg, neg);
-      uint64_t acc0 = 0, acc1 = 0, acc2 = 0, acc3 = 0;  // packed partial row sums (+0.0f pairs)
-      uint32_t pk[kBlockN / 2];
-#pragma unroll
-      for (int u = 0; u < kBlockN / 2; ++u) {
-        const uint64_t x2 = f2_fma(f2_pack(__uint_as_float(sr[2 * u]), __uint_as_float(sr[2 * u + 1])), cc, nn);
-        float x0, x1;
-        f2_unpack(x2, x0, x1);
-        const uint64_t p2 = f2_pack(ex2_approx(x0), ex2_approx(x1));
-        switch (u & 3) {
-          case 0: acc0 = f2_add(acc0, p2); break;
-          case 1: acc1 = f2_add(acc1, p2); break;
-          case 2: acc2 = f2_add(acc2, p2); break;
-          default: acc3 = f2_add(acc3, p2); break;
-        }
-        float p0, p1;
-        f2_unpack(p2, p0, p1);
-        pk[u] = E::pack(p0, p1);
-      }
-      tmem_st64(tmem + lane_addr + sb * 128, pk);
-      float rs;
-      {
-        float a0, a1;
-        f2_unpack(f2_add(f2_add(acc0, acc1), f2_add(acc2, acc3)), a0, a1);
-        rs = a0 + a1;
-      }
-      l_sum += rs;
-      tc_fence_before();
-      mbar_arrive(&p_ready[sb]);
-    }
-    // ---------------------------------------------------------------- epilogue
-    // the last P V (and, issued in order before it, every other one) is done
-    if (ok && mbar_wait_warp(&pv_done[(n_ktiles - 1) % kSBuf], ((n_ktiles - 1) / kSBuf) & 1, &abort_flag)) {
       tc_fence_after();
       const float inv_l = 1.f / l_sum;
       const bool store = row < N;
@@ -344,16 +438,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int D, bool F16>
 cudaError_t launch(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtensorMap &tmV, void *o,
                    float *lse, int B, int H, int N, int Nk, float scale, int causal, int *status,
-                   cudaStream_t stream) {
+                   int num_sms, cudaStream_t stream) {
   using L = FwdSmem<D>;
   auto kern = fwd_kernel<D, F16>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (e != cudaSuccess) return e;
-  dim3 grid((N + kBlockM - 1) / kBlockM, B * H);
+  // persistent grid: at most one CTA per SM, each walking its static list of
+  // query tiles; a tile costs its key tiles plus about one for its epilogue
+  const int BH = B * H, nt = (N + kBlockM - 1) / kBlockM;
+  const int n_ktiles_all = (Nk + kBlockN - 1) / kBlockN, off = Nk - N;
+  const TileSched sched = sched_cached(0, BH, N, Nk, causal != 0, nt, num_sms, [&](int rank) {
+    const int qtile = nt - 1 - rank;
+    const int nk = causal ? std::min(n_ktiles_all, (qtile * kBlockM + kBlockM - 1 + off) / kBlockN + 1)
+                          : n_ktiles_all;
+    return static_cast<long long>(nk) + 1;
+  });
   timing_begin(stream);
-  kern<<<grid, kThreads, L::kAlloc, stream>>>(tmQ, tmK, tmV, static_cast<uint16_t *>(o), lse,
-                                               N, Nk, scale, scale * 1.4426950408889634f, causal,
-                                               status);
+  kern<<<sched.G, kThreads, L::kAlloc, stream>>>(tmQ, tmK, tmV, static_cast<uint16_t *>(o), lse,
+                                                  N, Nk, sched, scale, scale * 1.4426950408889634f, causal,
+                                                  status);
   timing_end(stream);
   return cudaGetLastError();
 }
@@ -363,14 +466,13 @@ cudaError_t launch(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtenso
 cudaError_t launch_fwd_16(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtensorMap &tmV,
                           void *o, float *lse, int B, int H, int N, int Nk, int d, float scale, int causal,
                           bool f16, int *status, int num_sms, cudaStream_t stream, int *launches) {
-  (void)num_sms;
   *launches += 1;
   if (f16) {
-    if (d == 64) return launch<64, true>(tmQ, tmK, tmV, o, lse, B, H, N, Nk, scale, causal, status, stream);
-    return launch<128, true>(tmQ, tmK, tmV, o, lse, B, H, N, Nk, scale, causal, status, stream);
+    if (d == 64) return launch<64, true>(tmQ, tmK, tmV, o, lse, B, H, N, Nk, scale, causal, status, num_sms, stream);
+    return launch<128, true>(tmQ, tmK, tmV, o, lse, B, H, N, Nk, scale, causal, status, num_sms, stream);
   }
-  if (d == 64) return launch<64, false>(tmQ, tmK, tmV, o, lse, B, H, N, Nk, scale, causal, status, stream);
-  return launch<128, false>(tmQ, tmK, tmV, o, lse, B, H, N, Nk, scale, causal, status, stream);
+  if (d == 64) return launch<64, false>(tmQ, tmK, tmV, o, lse, B, H, N, Nk, scale, causal, status, num_sms, stream);
+  return launch<128, false>(tmQ, tmK, tmV, o, lse, B, H, N, Nk, scale, causal, status, num_sms, stream);
 }
 
 }  // namespace fa
