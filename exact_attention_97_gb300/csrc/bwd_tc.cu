@@ -17,22 +17,29 @@
 // Three kernels on one stream:
 //   1. bwd_prep  per query row, padded to whole 128-row tiles:
 //                -L*log2(e) (-inf past N) and D_i = dO_i . O_i (0 past N).
-//   2. bwd_dkdv  one CTA per (batch*head, 128-key block); query tiles of 128
+//   2. bwd_dkdv  per (batch*head, 128-key block) item; query tiles of 128
 //                rows stream through a TMA ring. Keys on the TMEM lanes:
 //                  S^T = K Q^T, dP^T = V dO^T          (TMEM)
 //                  dV += P^T dO   (P^T written over S^T in 16 bits, A from TMEM)
 //                  dK += dS^T Q   (dS^T written over dP^T in 16 bits, A from TMEM)
-//   3. bwd_dq    one CTA per (batch*head, 128-row query tile); key blocks
+//   3. bwd_dq    per (batch*head, 128-row query tile) item; key blocks
 //                stream through a TMA ring. Queries on the TMEM lanes:
 //                  S = Q K^T (double-buffered), dP = dO V^T   (TMEM)
 //                  dQ += dS K     (dS read from TMEM in 16 bits)
 // In both passes two warpgroups split the 128 columns of S and dP (64 each)
-// for the elementwise work; one warp loads, one thread issues the MMAs.
+// for the elementwise work; one warp loads, one thread issues the MMAs. Both
+// passes are persistent: at most one CTA per SM walks a static list of items
+// (tile_sched.h), and the rings and barrier phases carry over from item to
+// item, so the next item's loads and first MMAs overlap the current item's
+// last products and its epilogue.
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
 
+#include <algorithm>
+
 #include "kernels.h"
+#include "tile_sched.h"
 #include "sm103.cuh"
 
 namespace fa {
@@ -120,33 +127,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                     const float *__restrict__ Lp, const float *__restrict__ Dp,
                     uint16_t *__restrict__ dk, uint16_t *__restrict__ dv, int N, int Nk,
-                    float scale, float scale_log2, int causal, int *status) {
+                    const __grid_constant__ TileSched sched, float scale, float scale_log2, int causal,
+                    int *status) {
   using C = DkdvCfg<D>;
   using E = Elt<F16>;
   constexpr int NST = C::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
-  __shared__ uint64_t kv_full, qd_full[NST], qd_empty[NST], s_full, dp_full, p_ready, ds_ready, done,
-      drain;
+  __shared__ uint64_t k_full, k_empty, v_full, v_empty, qd_full[NST], qd_empty[NST], s_full, dp_full, p_ready,
+      ds_ready, done, drain;
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_flag;
   __shared__ __align__(16) float Lst[NST][kBlk], Dst[NST][kBlk];  // per stage, by bulk copy
 
   const int warp = warp_id(), lane = lane_id();
   const int n_tiles_all = (N + kBlk - 1) / kBlk;
-  const int kb = blockIdx.x;  // low blocks see the most query tiles under the causal mask
   const int Np = n_tiles_all * kBlk;
-  const int bh = blockIdx.y;
   // N query rows, Nk >= N keys under the causal mask; key j is seen by the
-  // queries i >= j - (Nk - N) (bottom-right alignment)
+  // queries i >= j - (Nk - N) (bottom-right alignment). Schedule rank r is
+  // key block r: low blocks see the most query tiles.
   const int off = Nk - N;
-  const int i_first = causal ? max(0, kb * kBlk - off) / kBlk : 0;
-  const int n_tiles = n_tiles_all - i_first;
+  auto first_tile = [&](int kb) { return causal ? max(0, kb * kBlk - off) / kBlk : 0; };
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
-    mbar_init(&kv_full, 1);
+    mbar_init(&k_full, 1);
+    mbar_init(&k_empty, 1);
+    mbar_init(&v_full, 1);
+    mbar_init(&v_empty, 1);
     for (int s = 0; s < NST; ++s) {
       mbar_init(&qd_full[s], 1);
       mbar_init(&qd_empty[s], 1);
@@ -168,45 +177,70 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_base_s;
 
+  // Every role walks the same items (key blocks); query tiles are counted
+  // across items (g) for the ring and the per-tile barriers, items (it) for
+  // the K, V and `done` barriers.
   if (warp == 0) {
     // ---------------------------------------------------------------- producer
+    // K of the next block loads as soon as the last S^T MMA of the current
+    // one has completed, V after its last dP^T; query tiles stream on.
     if (lane == 0) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
       tma_prefetch_desc(&tmdO);
-      mbar_arrive_expect_tx(&kv_full, 2 * C::kTileBytes);
-      load_rows(smem + C::kK, &tmK, &kv_full, D, kb * kBlk, bh);
-      load_rows(smem + C::kV, &tmV, &kv_full, D, kb * kBlk, bh);
-      int issued = 0;
-      for (int t = 0; t < n_tiles; ++t) {
-        const int st = t % NST;
-        if (t >= NST && !mbar_wait(&qd_empty[st], ((t / NST) & 1) ^ 1, &abort_flag)) break;
-        const int row = (i_first + t) * kBlk;
+      bool ok = true;
+      int g = 0, it = 0, kb, bh;
+      auto load_qd = [&](int row) -> bool {
+        const int st = g % NST;
+        if (g >= NST && !mbar_wait(&qd_empty[st], ((g / NST) & 1) ^ 1, &abort_flag)) return false;
         mbar_arrive_expect_tx(&qd_full[st], 2 * C::kTileBytes + 2 * kBlk * 4);
         load_rows(smem + C::kQ + st * C::kTileBytes, &tmQ, &qd_full[st], D, row, bh);
         load_rows(smem + C::kDO + st * C::kTileBytes, &tmdO, &qd_full[st], D, row, bh);
         const size_t prow = static_cast<size_t>(bh) * Np + row;
         bulk_load(Lst[st], Lp + prow, kBlk * 4, &qd_full[st]);
         bulk_load(Dst[st], Dp + prow, kBlk * 4, &qd_full[st]);
-        ++issued;
+        ++g;
+        return true;
+      };
+      int kdone = 0, vdone = 0;  // K / V loads issued
+      for (int k = 0; ok; ++k) {
+        const int step = sched_item(sched, blockIdx.x, k, kb, bh);
+        if (step == kDone) break;
+        if (step == kSkip) continue;
+        const int i_first = first_tile(kb), n_tiles = n_tiles_all - i_first;
+        if (it > 0 && !mbar_wait(&k_empty, (it - 1) & 1, &abort_flag)) break;
+        mbar_arrive_expect_tx(&k_full, C::kTileBytes);
+        load_rows(smem + C::kK, &tmK, &k_full, D, kb * kBlk, bh);
+        ++kdone;
+        if (!load_qd(i_first * kBlk)) break;
+        if (it > 0 && !mbar_wait(&v_empty, (it - 1) & 1, &abort_flag)) break;
+        mbar_arrive_expect_tx(&v_full, C::kTileBytes);
+        load_rows(smem + C::kV, &tmV, &v_full, D, kb * kBlk, bh);
+        ++vdone;
+        for (int t = 1; t < n_tiles; ++t)
+          if (!load_qd((i_first + t) * kBlk)) { ok = false; break; }
+        ++it;
       }
-      mbar_wait_drain(&kv_full, 0);
-      for (int t = max(0, issued - NST); t < issued; ++t)
-        mbar_wait_drain(&qd_full[t % NST], (t / NST) & 1);
+      if (kdone > 0) mbar_wait_drain(&k_full, (kdone - 1) & 1);
+      if (vdone > 0) mbar_wait_drain(&v_full, (vdone - 1) & 1);
+      for (int t = max(0, g - NST); t < g; ++t) mbar_wait_drain(&qd_full[t % NST], (t / NST) & 1);
     }
   } else if (warp == 1) {
     // -------------------------------------------------------------- MMA issuer
     // Per tile t: dV_t once P_t is in TMEM; once dS_t is in TMEM, S of tile
     // t+1 (so P_{t+1} is formed while the rest runs), dK_t, then dP of t+1
-    // (which overwrites the columns dK_t reads, so it must come after).
+    // (which overwrites the columns dK_t reads, so it must come after). The
+    // first dV / dK of a block overwrite the accumulators: they wait for P_0
+    // and dS_0, which the elementwise warps only produce after storing the
+    // previous block's dV and dK.
     if (lane == 0) {
       constexpr uint32_t id_s = idesc_16(kBlk, kBlk, false, false, F16);  // S^T, dP^T
       constexpr uint32_t id_kv = idesc_16(kBlk, D, false, true, F16);     // dV, dK
       const uint32_t k_addr = smem_u32(smem + C::kK), v_addr = smem_u32(smem + C::kV);
-      auto issue_s = [&](int t) -> bool {  // S^T_t = K Q_t^T
-        const int st = t % NST;
-        if (!mbar_wait(&qd_full[st], (t / NST) & 1, &abort_flag)) return false;
+      auto issue_s = [&](int gt) -> bool {  // S^T = K Q^T of global tile gt
+        const int st = gt % NST;
+        if (!mbar_wait(&qd_full[st], (gt / NST) & 1, &abort_flag)) return false;
         tc_fence_after();
         const uint32_t q_addr = smem_u32(smem + C::kQ + st * C::kTileBytes);
 #pragma unroll
@@ -218,8 +252,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(&s_full);
         return true;
       };
-      auto issue_dp = [&](int t) {  // dP^T_t = V dO_t^T (tile t already landed)
-        const uint32_t do_addr = smem_u32(smem + C::kDO + (t % NST) * C::kTileBytes);
+      auto issue_dp = [&](int gt) {  // dP^T = V dO^T (tile gt already landed)
+        const uint32_t do_addr = smem_u32(smem + C::kDO + (gt % NST) * C::kTileBytes);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk / 4) * C::kSubBytes + (kk % 4) * 32;
@@ -228,33 +262,53 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mma_commit(&dp_full);
       };
-      bool ok = mbar_wait(&kv_full, 0, &abort_flag) && issue_s(0);
-      if (ok) issue_dp(0);
-      for (int t = 0; ok && t < n_tiles; ++t) {
-        const int st = t % NST;
-        const uint32_t ph = t & 1;
-        const uint32_t q_addr = smem_u32(smem + C::kQ + st * C::kTileBytes);
-        const uint32_t do_addr = smem_u32(smem + C::kDO + st * C::kTileBytes);
-        // dV += P^T dO
-        if (!mbar_wait(&p_ready, ph, &abort_flag)) { ok = false; break; }
+      bool ok = true;
+      int g = 0, it = 0, kb, bh;
+      for (int k = 0; ok; ++k) {
+        const int step = sched_item(sched, blockIdx.x, k, kb, bh);
+        if (step == kDone) break;
+        if (step == kSkip) continue;
+        const int n_tiles = n_tiles_all - first_tile(kb);
+        if (!mbar_wait(&k_full, it & 1, &abort_flag) || !issue_s(g)) break;
+        if (n_tiles == 1) mma_commit(&k_empty);
+        if (!mbar_wait(&v_full, it & 1, &abort_flag)) break;
         tc_fence_after();
+        issue_dp(g);
+        if (n_tiles == 1) mma_commit(&v_empty);
+        for (int t = 0; t < n_tiles; ++t, ++g) {
+          const int st = g % NST;
+          const uint32_t ph = g & 1;
+          const uint32_t q_addr = smem_u32(smem + C::kQ + st * C::kTileBytes);
+          const uint32_t do_addr = smem_u32(smem + C::kDO + st * C::kTileBytes);
+          // dV += P^T dO
+          if (!mbar_wait(&p_ready, ph, &abort_flag)) { ok = false; break; }
+          tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < kBlk / 16; ++kk)
-          mma_ts(tmem + C::tDV, tmem + C::tS + a_col(kk), sdesc_sw128(do_addr + kk * 2048, C::kSubBytes, 1024),
-                 id_kv, (t > 0 || kk > 0) ? 1u : 0u);
-        if (!mbar_wait(&ds_ready, ph, &abort_flag)) { ok = false; break; }
-        tc_fence_after();
-        // the S columns are free: P_t went to dV_t (issued above)
-        if (t + 1 < n_tiles && !issue_s(t + 1)) { ok = false; break; }
-        // dK += dS^T Q
+          for (int kk = 0; kk < kBlk / 16; ++kk)
+            mma_ts(tmem + C::tDV, tmem + C::tS + a_col(kk), sdesc_sw128(do_addr + kk * 2048, C::kSubBytes, 1024),
+                   id_kv, (t > 0 || kk > 0) ? 1u : 0u);
+          if (!mbar_wait(&ds_ready, ph, &abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          // the S columns are free: P_t went to dV_t (issued above)
+          if (t + 1 < n_tiles) {
+            if (!issue_s(g + 1)) { ok = false; break; }
+            if (t + 2 == n_tiles) mma_commit(&k_empty);  // the block's last S^T
+          }
+          // dK += dS^T Q
 #pragma unroll
-        for (int kk = 0; kk < kBlk / 16; ++kk)
-          mma_ts(tmem + C::tDK, tmem + C::tDP + a_col(kk), sdesc_sw128(q_addr + kk * 2048, C::kSubBytes, 1024),
-                 id_kv, (t > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&qd_empty[st]);
-        if (t + 1 < n_tiles) issue_dp(t + 1);  // after dK_t has read dS_t from these columns
+          for (int kk = 0; kk < kBlk / 16; ++kk)
+            mma_ts(tmem + C::tDK, tmem + C::tDP + a_col(kk), sdesc_sw128(q_addr + kk * 2048, C::kSubBytes, 1024),
+                   id_kv, (t > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(&qd_empty[st]);
+          if (t + 1 < n_tiles) {  // after dK_t has read dS_t from these columns
+            issue_dp(g + 1);
+            if (t + 2 == n_tiles) mma_commit(&v_empty);  // the block's last dP^T
+          }
+        }
+        if (!ok) break;
+        mma_commit(&done);
+        ++it;
       }
-      if (ok) mma_commit(&done);
       mma_commit(&drain);
       mbar_wait_drain(&drain, 0);
     }
@@ -263,63 +317,73 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int h = (warp >= 8) ? 1 : 0;
     const int wq = warp & 3;
     const int kr = wq * 32 + lane;  // key row within the block (TMEM lane)
-    const int key = kb * kBlk + kr;
     const uint32_t lane_addr = static_cast<uint32_t>(wq * 32) << 16;
     const uint64_t cc = f2_pack(scale_log2, scale_log2);
     bool ok = true;
-    for (int t = 0; t < n_tiles; ++t) {
-      const uint32_t ph = t & 1;
-      const int st = t % NST;
-      const int q0 = (i_first + t) * kBlk + h * 64;  // first query of this warpgroup's columns
-      if (!mbar_wait_warp(&qd_full[st], (t / NST) & 1, &abort_flag)) { ok = false; break; }
-      const float2 *L2 = reinterpret_cast<const float2 *>(Lst[st] + h * 64);
-      const float2 *D2 = reinterpret_cast<const float2 *>(Dst[st] + h * 64);
-      // queries below qmin see nothing of this key (causal); keys past N see nothing
-      const int qmin = (key >= Nk) ? (q0 + 64) : (causal ? key - off : 0);
-      if (!mbar_wait_warp(&s_full, ph, &abort_flag)) { ok = false; break; }
-      tc_fence_after();
-      uint32_t pk[32];
-      {
-        uint32_t r[64];
-        tmem_ld64(tmem + lane_addr + C::tS + h * 64, r);
+    int g = 0, it = 0, kb, bh;
+    for (int k = 0; ok; ++k) {
+      const int step = sched_item(sched, blockIdx.x, k, kb, bh);
+      if (step == kDone) break;
+      if (step == kSkip) continue;
+      const int i_first = first_tile(kb), n_tiles = n_tiles_all - i_first;
+      const int key = kb * kBlk + kr;
+      // queries below qmin see nothing of this key (causal); keys past Nk see nothing
+      const int qmin0 = causal ? key - off : 0;
+      for (int t = 0; t < n_tiles; ++t, ++g) {
+        const uint32_t ph = g & 1;
+        const int st = g % NST;
+        const int q0 = (i_first + t) * kBlk + h * 64;  // first query of this warpgroup's columns
+        const int qmin = (key >= Nk) ? (q0 + 64) : qmin0;
+        if (!mbar_wait_warp(&qd_full[st], (g / NST) & 1, &abort_flag)) { ok = false; break; }
+        const float2 *L2 = reinterpret_cast<const float2 *>(Lst[st] + h * 64);
+        const float2 *D2 = reinterpret_cast<const float2 *>(Dst[st] + h * 64);
+        if (!mbar_wait_warp(&s_full, ph, &abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        uint32_t pk[32];
+        {
+          uint32_t r[64];
+          tmem_ld64(tmem + lane_addr + C::tS + h * 64, r);
 #pragma unroll
-        for (int u = 0; u < 32; ++u) {
-          const float2 nl = L2[u];
-          const uint64_t x2 =
-              f2_fma(f2_pack(__uint_as_float(r[2 * u]), __uint_as_float(r[2 * u + 1])), cc, f2_pack(nl.x, nl.y));
-          float x0, x1;
-          f2_unpack(x2, x0, x1);
-          float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-          if (q0 + 2 * u < qmin) p0 = 0.f;
-          if (q0 + 2 * u + 1 < qmin) p1 = 0.f;
-          pk[u] = E::pack(p0, p1);
+          for (int u = 0; u < 32; ++u) {
+            const float2 nl = L2[u];
+            const uint64_t x2 =
+                f2_fma(f2_pack(__uint_as_float(r[2 * u]), __uint_as_float(r[2 * u + 1])), cc, f2_pack(nl.x, nl.y));
+            float x0, x1;
+            f2_unpack(x2, x0, x1);
+            float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+            if (q0 + 2 * u < qmin) p0 = 0.f;
+            if (q0 + 2 * u + 1 < qmin) p1 = 0.f;
+            pk[u] = E::pack(p0, p1);
+          }
+          tmem_st32(tmem + lane_addr + C::tS + h * 64, pk);
         }
-        tmem_st32(tmem + lane_addr + C::tS + h * 64, pk);
-      }
-      tc_fence_before();
-      mbar_arrive(&p_ready);
-      // dS^T = P^T o (dP^T - D), with P as rounded for dV; written in 16 bits
-      // pairs over the dP^T columns this warpgroup has just read
-      if (!mbar_wait_warp(&dp_full, ph, &abort_flag)) { ok = false; break; }
-      tc_fence_after();
-      {
-        uint32_t r[64];
-        tmem_ld64(tmem + lane_addr + C::tDP + h * 64, r);
-        uint32_t ds[32];
+        tc_fence_before();
+        mbar_arrive(&p_ready);
+        // dS^T = P^T o (dP^T - D), with P as rounded for dV; written in 16 bits
+        // pairs over the dP^T columns this warpgroup has just read
+        if (!mbar_wait_warp(&dp_full, ph, &abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        {
+          uint32_t r[64];
+          tmem_ld64(tmem + lane_addr + C::tDP + h * 64, r);
+          uint32_t ds[32];
 #pragma unroll
-        for (int u = 0; u < 32; ++u) {
-          const float2 dd = D2[u];
-          const float d0 = E::lo(pk[u]) * (__uint_as_float(r[2 * u]) - dd.x);
-          const float d1 = E::hi(pk[u]) * (__uint_as_float(r[2 * u + 1]) - dd.y);
-          ds[u] = E::pack(d0, d1);
+          for (int u = 0; u < 32; ++u) {
+            const float2 dd = D2[u];
+            const float d0 = E::lo(pk[u]) * (__uint_as_float(r[2 * u]) - dd.x);
+            const float d1 = E::hi(pk[u]) * (__uint_as_float(r[2 * u + 1]) - dd.y);
+            ds[u] = E::pack(d0, d1);
+          }
+          tmem_st32(tmem + lane_addr + C::tDP + h * 64, ds);
         }
-        tmem_st32(tmem + lane_addr + C::tDP + h * 64, ds);
+        tc_fence_before();
+        mbar_arrive(&ds_ready);
       }
-      tc_fence_before();
-      mbar_arrive(&ds_ready);
-    }
-    // epilogue: warpgroup 0 stores dV, warpgroup 1 stores dK (times scale)
-    if (ok && mbar_wait_warp(&done, 0, &abort_flag)) {
+      // epilogue: warpgroup 0 stores dV, warpgroup 1 stores dK (times scale)
+      if (!ok || !mbar_wait_warp(&done, it & 1, &abort_flag)) {
+        ok = false;
+        break;
+      }
       tc_fence_after();
       const uint32_t col = h ? C::tDK : C::tDV;
       const float mul = h ? scale : 1.f;
@@ -334,6 +398,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           pk2[u] = E::pack(__uint_as_float(r[2 * u]) * mul, __uint_as_float(r[2 * u + 1]) * mul);
         store_row32(out + ch * 32, pk2, key < Nk);
       }
+      ++it;
     }
   }
 
@@ -370,32 +435,37 @@ __global__ void __launch_bounds__(kThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                   const float *__restrict__ Lp, const float *__restrict__ Dp,
-                  uint16_t *__restrict__ dq, int N, int Nk, float scale, float scale_log2, int causal,
-                  int *status) {
+                  uint16_t *__restrict__ dq, int N, int Nk, const __grid_constant__ TileSched sched, float scale,
+                  float scale_log2, int causal, int *status) {
   using C = DqCfg<D>;
   using E = Elt<F16>;
   constexpr int KS = C::kKStages, VS = C::kVStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
-  __shared__ uint64_t qd_full, k_full[KS], k_empty[KS], v_full[VS], v_empty[VS], s_full[2], dp_full,
-      ds_ready, done, drain;
+  __shared__ uint64_t q_full, q_empty, do_full, do_empty, k_full[KS], k_empty[KS], v_full[VS], v_empty[VS],
+      s_full[2], dp_full, ds_ready, done, drain;
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_flag;
 
   const int warp = warp_id(), lane = lane_id();
   const int n_tiles = (N + kBlk - 1) / kBlk;
-  // causal: longest rows first so the last wave holds the short tiles
-  const int qt = causal ? (n_tiles - 1 - static_cast<int>(blockIdx.x)) : blockIdx.x;
-  const int bh = blockIdx.y;
   const int Np = n_tiles * kBlk;
   const int off = Nk - N;  // bottom-right causal alignment, as in the forward
   const int n_kb_all = (Nk + kBlk - 1) / kBlk;
-  const int n_kb = causal ? min(n_kb_all, (qt * kBlk + kBlk - 1 + off) / kBlk + 1) : n_kb_all;
+  // schedule rank 0 is a head's most expensive query tile (the last one
+  // under the causal mask)
+  auto qtile_of = [&](int rank) { return causal ? n_tiles - 1 - rank : rank; };
+  auto kblocks = [&](int qt) {
+    return causal ? min(n_kb_all, (qt * kBlk + kBlk - 1 + off) / kBlk + 1) : n_kb_all;
+  };
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
-    mbar_init(&qd_full, 1);
+    mbar_init(&q_full, 1);
+    mbar_init(&q_empty, 1);
+    mbar_init(&do_full, 1);
+    mbar_init(&do_empty, 1);
     for (int s = 0; s < KS; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&k_empty[s], 1);
@@ -421,64 +491,93 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_base_s;
 
+  // Every role walks the same items (query tiles); key blocks are counted
+  // across items (g) for the K/V rings, the S buffers and the per-block
+  // barriers, items (it) for the Q, dO and `done` barriers.
   if (warp == 0) {
     // ------------------------------------------------------- loader: Q, dO, K
+    // Q of the next tile loads once the last S MMA of the current one has
+    // completed, dO once its last dP MMA has; the K ring runs on.
     if (lane == 0) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmdO);
-      mbar_arrive_expect_tx(&qd_full, 2 * C::kTileBytes);
-      load_rows(smem + C::kQ, &tmQ, &qd_full, D, qt * kBlk, bh);
-      load_rows(smem + C::kDO, &tmdO, &qd_full, D, qt * kBlk, bh);
-      int issued = 0;
-      for (int j = 0; j < n_kb; ++j) {
-        const int st = j % KS;
-        if (j >= KS && !mbar_wait(&k_empty[st], ((j / KS) & 1) ^ 1, &abort_flag)) break;
-        mbar_arrive_expect_tx(&k_full[st], C::kTileBytes);
-        load_rows(smem + C::kK + st * C::kTileBytes, &tmK, &k_full[st], D, j * kBlk, bh);
-        ++issued;
+      bool ok = true;
+      int g = 0, nq = 0, ndo = 0, rank, bh;  // K blocks, Q tiles, dO tiles issued
+      for (int k = 0; ok; ++k) {
+        const int step = sched_item(sched, blockIdx.x, k, rank, bh);
+        if (step == kDone) break;
+        if (step == kSkip) continue;
+        const int qt = qtile_of(rank), n_kb = kblocks(qt);
+        if (nq > 0 && !mbar_wait(&q_empty, (nq - 1) & 1, &abort_flag)) break;
+        mbar_arrive_expect_tx(&q_full, C::kTileBytes);
+        load_rows(smem + C::kQ, &tmQ, &q_full, D, qt * kBlk, bh);
+        ++nq;
+        for (int j = 0; j < n_kb; ++j, ++g) {
+          const int st = g % KS;
+          if (g >= KS && !mbar_wait(&k_empty[st], ((g / KS) & 1) ^ 1, &abort_flag)) { ok = false; break; }
+          mbar_arrive_expect_tx(&k_full[st], C::kTileBytes);
+          load_rows(smem + C::kK + st * C::kTileBytes, &tmK, &k_full[st], D, j * kBlk, bh);
+          if (j == 0) {  // dO after the first K block: S_0 needs Q and K_0 first
+            if (ndo > 0 && !mbar_wait(&do_empty, (ndo - 1) & 1, &abort_flag)) { ok = false; ++g; break; }
+            mbar_arrive_expect_tx(&do_full, C::kTileBytes);
+            load_rows(smem + C::kDO, &tmdO, &do_full, D, qt * kBlk, bh);
+            ++ndo;
+          }
+        }
       }
-      mbar_wait_drain(&qd_full, 0);
-      for (int j = max(0, issued - KS); j < issued; ++j) mbar_wait_drain(&k_full[j % KS], (j / KS) & 1);
+      // teardown: every issued copy must land before the CTA's memory is released
+      if (nq > 0) mbar_wait_drain(&q_full, (nq - 1) & 1);
+      if (ndo > 0) mbar_wait_drain(&do_full, (ndo - 1) & 1);
+      for (int j = max(0, g - KS); j < g; ++j) mbar_wait_drain(&k_full[j % KS], (j / KS) & 1);
     }
   } else if (warp == 3) {
     // ---------------------------------------------------------------- loader: V
     if (lane == 0) {
       tma_prefetch_desc(&tmV);
-      int issued = 0;
-      for (int j = 0; j < n_kb; ++j) {
-        const int st = j % VS;
-        if (j >= VS && !mbar_wait(&v_empty[st], ((j / VS) & 1) ^ 1, &abort_flag)) break;
-        mbar_arrive_expect_tx(&v_full[st], C::kTileBytes);
-        load_rows(smem + C::kV + st * C::kTileBytes, &tmV, &v_full[st], D, j * kBlk, bh);
-        ++issued;
+      bool ok = true;
+      int g = 0, rank, bh;
+      for (int k = 0; ok; ++k) {
+        const int step = sched_item(sched, blockIdx.x, k, rank, bh);
+        if (step == kDone) break;
+        if (step == kSkip) continue;
+        const int n_kb = kblocks(qtile_of(rank));
+        for (int j = 0; j < n_kb; ++j, ++g) {
+          const int st = g % VS;
+          if (g >= VS && !mbar_wait(&v_empty[st], ((g / VS) & 1) ^ 1, &abort_flag)) { ok = false; break; }
+          mbar_arrive_expect_tx(&v_full[st], C::kTileBytes);
+          load_rows(smem + C::kV + st * C::kTileBytes, &tmV, &v_full[st], D, j * kBlk, bh);
+        }
       }
-      for (int j = max(0, issued - VS); j < issued; ++j) mbar_wait_drain(&v_full[j % VS], (j / VS) & 1);
+      for (int j = max(0, g - VS); j < g; ++j) mbar_wait_drain(&v_full[j % VS], (j / VS) & 1);
     }
   } else if (warp == 1) {
     // -------------------------------------------------------------- MMA issuer
-    // Order: S_0, dP_0, S_1, then per key block j: dQ_j, dP_{j+1}, S_{j+2}.
+    // Per tile: S_0, dP_0, S_1, then per key block j: dQ_j, dP_{j+1}, S_{j+2}.
+    // The first dQ of a tile overwrites the accumulator: it waits for dS_0,
+    // which the elementwise warps only produce after storing the previous
+    // tile's dQ.
     if (lane == 0) {
       constexpr uint32_t id_s = idesc_16(kBlk, kBlk, false, false, F16);  // S, dP
       constexpr uint32_t id_q = idesc_16(kBlk, D, false, true, F16);      // dQ
       const uint32_t q_addr = smem_u32(smem + C::kQ), do_addr = smem_u32(smem + C::kDO);
-      auto issue_s = [&](int j) -> bool {  // S_j = Q K_j^T into buffer j&1
-        const int st = j % KS;
-        if (!mbar_wait(&k_full[st], (j / KS) & 1, &abort_flag)) return false;
+      auto issue_s = [&](int gj) -> bool {  // S of global block gj = Q K^T into buffer gj&1
+        const int st = gj % KS;
+        if (!mbar_wait(&k_full[st], (gj / KS) & 1, &abort_flag)) return false;
         tc_fence_after();
         const uint32_t k_addr = smem_u32(smem + C::kK + st * C::kTileBytes);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk / 4) * C::kSubBytes + (kk % 4) * 32;
-          mma_ss(tmem + C::tS + (j & 1) * 128, sdesc_sw128(q_addr + off, 16, 1024),
+          mma_ss(tmem + C::tS + (gj & 1) * 128, sdesc_sw128(q_addr + off, 16, 1024),
                  sdesc_sw128(k_addr + off, 16, 1024), id_s, kk > 0);
         }
-        mma_commit(&s_full[j & 1]);
+        mma_commit(&s_full[gj & 1]);
         return true;
       };
-      auto issue_dp = [&](int j) -> bool {  // dP_j = dO V_j^T
-        const int st = j % VS;
-        if (!mbar_wait(&v_full[st], (j / VS) & 1, &abort_flag)) return false;
+      auto issue_dp = [&](int gj) -> bool {  // dP = dO V^T
+        const int st = gj % VS;
+        if (!mbar_wait(&v_full[st], (gj / VS) & 1, &abort_flag)) return false;
         tc_fence_after();
         const uint32_t v_addr = smem_u32(smem + C::kV + st * C::kTileBytes);
 #pragma unroll
@@ -491,24 +590,46 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(&v_empty[st]);
         return true;
       };
-      bool ok = mbar_wait(&qd_full, 0, &abort_flag) && issue_s(0) && issue_dp(0);
-      if (ok && n_kb > 1) ok = issue_s(1);
-      for (int j = 0; ok && j < n_kb; ++j) {
-        const int st = j % KS;
-        if (!mbar_wait(&ds_ready, j & 1, &abort_flag)) { ok = false; break; }
-        tc_fence_after();
-        // dQ += dS_j K_j : A = dS_j (16-bit in TMEM), B = K_j (MN-major)
-        const uint32_t k_addr = smem_u32(smem + C::kK + st * C::kTileBytes);
+      bool ok = true;
+      int g = 0, it = 0, rank, bh;
+      for (int k = 0; ok; ++k) {
+        const int step = sched_item(sched, blockIdx.x, k, rank, bh);
+        if (step == kDone) break;
+        if (step == kSkip) continue;
+        const int n_kb = kblocks(qtile_of(rank));
+        if (!mbar_wait(&q_full, it & 1, &abort_flag) || !issue_s(g)) break;
+        if (n_kb == 1) mma_commit(&q_empty);
+        if (!mbar_wait(&do_full, it & 1, &abort_flag) || !issue_dp(g)) break;
+        if (n_kb == 1) mma_commit(&do_empty);
+        if (n_kb > 1) {
+          if (!issue_s(g + 1)) break;
+          if (n_kb == 2) mma_commit(&q_empty);
+        }
+        for (int j = 0; j < n_kb; ++j, ++g) {
+          const int st = g % KS;
+          if (!mbar_wait(&ds_ready, g & 1, &abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          // dQ += dS_j K_j : A = dS_j (16-bit in TMEM), B = K_j (MN-major)
+          const uint32_t k_addr = smem_u32(smem + C::kK + st * C::kTileBytes);
 #pragma unroll
-        for (int kk = 0; kk < kBlk / 16; ++kk)
-          mma_ts(tmem + C::tDQ, tmem + C::tS + (j & 1) * 128 + a_col(kk),
-                 sdesc_sw128(k_addr + kk * 2048, C::kSubBytes, 1024), id_q, (j > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&k_empty[st]);
-        if (j + 1 < n_kb && !issue_dp(j + 1)) { ok = false; break; }  // dP_j has been read into dS_j
-        // buffer j&1 still holds dS_j, which the dQ_j MMA above reads first
-        if (j + 2 < n_kb && !issue_s(j + 2)) { ok = false; break; }
+          for (int kk = 0; kk < kBlk / 16; ++kk)
+            mma_ts(tmem + C::tDQ, tmem + C::tS + (g & 1) * 128 + a_col(kk),
+                   sdesc_sw128(k_addr + kk * 2048, C::kSubBytes, 1024), id_q, (j > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(&k_empty[st]);
+          if (j + 1 < n_kb) {  // dP_j has been read into dS_j
+            if (!issue_dp(g + 1)) { ok = false; break; }
+            if (j + 2 == n_kb) mma_commit(&do_empty);  // the tile's last dP
+          }
+          // buffer g&1 still holds dS_j, which the dQ_j MMA above reads first
+          if (j + 2 < n_kb) {
+            if (!issue_s(g + 2)) { ok = false; break; }
+            if (j + 3 == n_kb) mma_commit(&q_empty);  // the tile's last S
+          }
+        }
+        if (!ok) break;
+        mma_commit(&done);
+        ++it;
       }
-      if (ok) mma_commit(&done);
       mma_commit(&drain);
       mbar_wait_drain(&drain, 0);
     }
@@ -517,55 +638,65 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int h = (warp >= 8) ? 1 : 0;
     const int wq = warp & 3;
     const int r = wq * 32 + lane;  // query row within the tile (TMEM lane)
-    const int q = qt * kBlk + r;
     const uint32_t lane_addr = static_cast<uint32_t>(wq * 32) << 16;
-    const size_t prow = static_cast<size_t>(bh) * Np + q;
-    const float nl = Lp[prow], drow = Dp[prow];
-    const uint64_t cc = f2_pack(scale_log2, scale_log2), nn = f2_pack(nl, nl);
-    const int kvis = causal ? min(Nk, q + 1 + off) : Nk;  // keys below kvis are visible
+    const uint64_t cc = f2_pack(scale_log2, scale_log2);
     bool ok = true;
-    for (int j = 0; j < n_kb; ++j) {
-      const uint32_t sb = C::tS + (j & 1) * 128 + h * 64;
-      const int limit = kvis - (j * kBlk + h * 64);  // columns at or past limit are masked
-      if (!mbar_wait_warp(&s_full[j & 1], (j >> 1) & 1, &abort_flag)) { ok = false; break; }
-      tc_fence_after();
-      float p[64];
-      {
-        uint32_t rr[64];
-        tmem_ld64(tmem + lane_addr + sb, rr);
+    int g = 0, it = 0, rank, bh;
+    for (int k = 0; ok; ++k) {
+      const int step = sched_item(sched, blockIdx.x, k, rank, bh);
+      if (step == kDone) break;
+      if (step == kSkip) continue;
+      const int qt = qtile_of(rank), n_kb = kblocks(qt);
+      const int q = qt * kBlk + r;
+      const size_t prow = static_cast<size_t>(bh) * Np + q;
+      const float nl = Lp[prow], drow = Dp[prow];
+      const uint64_t nn = f2_pack(nl, nl);
+      const int kvis = causal ? min(Nk, q + 1 + off) : Nk;  // keys below kvis are visible
+      for (int j = 0; j < n_kb; ++j, ++g) {
+        const uint32_t sb = C::tS + (g & 1) * 128 + h * 64;
+        const int limit = kvis - (j * kBlk + h * 64);  // columns at or past limit are masked
+        if (!mbar_wait_warp(&s_full[g & 1], (g >> 1) & 1, &abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        float p[64];
+        {
+          uint32_t rr[64];
+          tmem_ld64(tmem + lane_addr + sb, rr);
 #pragma unroll
-        for (int u = 0; u < 32; ++u) {
-          const uint64_t x2 = f2_fma(f2_pack(__uint_as_float(rr[2 * u]), __uint_as_float(rr[2 * u + 1])), cc, nn);
-          float x0, x1;
-          f2_unpack(x2, x0, x1);
-          p[2 * u] = ex2_approx(x0);
-          p[2 * u + 1] = ex2_approx(x1);
-        }
-        if (limit < 64) {
+          for (int u = 0; u < 32; ++u) {
+            const uint64_t x2 = f2_fma(f2_pack(__uint_as_float(rr[2 * u]), __uint_as_float(rr[2 * u + 1])), cc, nn);
+            float x0, x1;
+            f2_unpack(x2, x0, x1);
+            p[2 * u] = ex2_approx(x0);
+            p[2 * u + 1] = ex2_approx(x1);
+          }
+          if (limit < 64) {
 #pragma unroll
-          for (int u = 0; u < 64; ++u)
-            if (u >= limit) p[u] = 0.f;
+            for (int u = 0; u < 64; ++u)
+              if (u >= limit) p[u] = 0.f;
+          }
         }
+        if (!mbar_wait_warp(&dp_full, g & 1, &abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        {
+          uint32_t rr[64];
+          tmem_ld64(tmem + lane_addr + C::tDP + h * 64, rr);
+          uint32_t ds[32];
+#pragma unroll
+          for (int u = 0; u < 32; ++u) {
+            const float d0 = p[2 * u] * (__uint_as_float(rr[2 * u]) - drow);
+            const float d1 = p[2 * u + 1] * (__uint_as_float(rr[2 * u + 1]) - drow);
+            ds[u] = E::pack(d0, d1);
+          }
+          tmem_st32(tmem + lane_addr + sb, ds);  // over scores already read
+        }
+        tc_fence_before();
+        mbar_arrive(&ds_ready);
       }
-      if (!mbar_wait_warp(&dp_full, j & 1, &abort_flag)) { ok = false; break; }
-      tc_fence_after();
-      {
-        uint32_t rr[64];
-        tmem_ld64(tmem + lane_addr + C::tDP + h * 64, rr);
-        uint32_t ds[32];
-#pragma unroll
-        for (int u = 0; u < 32; ++u) {
-          const float d0 = p[2 * u] * (__uint_as_float(rr[2 * u]) - drow);
-          const float d1 = p[2 * u + 1] * (__uint_as_float(rr[2 * u + 1]) - drow);
-          ds[u] = E::pack(d0, d1);
-        }
-        tmem_st32(tmem + lane_addr + sb, ds);  // over scores already read
+      // epilogue: dQ = scale * accumulator; warpgroup h stores head columns [hD/2, hD/2 + D/2)
+      if (!ok || !mbar_wait_warp(&done, it & 1, &abort_flag)) {
+        ok = false;
+        break;
       }
-      tc_fence_before();
-      mbar_arrive(&ds_ready);
-    }
-    // epilogue: dQ = scale * accumulator; warpgroup h stores head columns [hD/2, hD/2 + D/2)
-    if (ok && mbar_wait_warp(&done, 0, &abort_flag)) {
       tc_fence_after();
       uint16_t *out = dq + (static_cast<size_t>(bh) * N + q) * D + h * (D / 2);
 #pragma unroll 1
@@ -578,6 +709,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           pk2[u] = E::pack(__uint_as_float(rr[2 * u]) * scale, __uint_as_float(rr[2 * u + 1]) * scale);
         store_row32(out + ch * 32, pk2, q < N);
       }
+      ++it;
     }
   }
 
@@ -594,7 +726,7 @@ template <int D, bool F16>
 cudaError_t launch(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtensorMap &tmV,
                    const CUtensorMap &tmdO, const void *o, const void *dO, const float *lse, void *dq,
                    void *dk, void *dv, float *Lp, float *Dp, int B, int H, int N, int Nk, float scale,
-                   int causal, int *status, cudaStream_t stream) {
+                   int causal, int *status, int num_sms, cudaStream_t stream) {
   const int n_tiles = (N + kBlk - 1) / kBlk;
   const int Np = n_tiles * kBlk;
   const float scale_log2 = scale * kLog2e;
@@ -607,7 +739,19 @@ cudaError_t launch(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtenso
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const dim3 grid_kv((Nk + kBlk - 1) / kBlk, B * H), grid_q(n_tiles, B * H);
+  // persistent grids: at most one CTA per SM, each walking its static list of
+  // key blocks (dK/dV pass) or query tiles (dQ pass); an item costs the tiles
+  // it visits plus about one for its epilogue
+  const int BH = B * H, off = Nk - N, n_kb_all = (Nk + kBlk - 1) / kBlk;
+  const TileSched sched_kv = sched_cached(1, BH, N, Nk, causal != 0, n_kb_all, num_sms, [&](int kb) {
+    const int i_first = causal ? std::max(0, kb * kBlk - off) / kBlk : 0;
+    return static_cast<long long>(n_tiles - i_first) + 1;
+  });
+  const TileSched sched_q = sched_cached(2, BH, N, Nk, causal != 0, n_tiles, num_sms, [&](int rank) {
+    const int qt = n_tiles - 1 - rank;
+    const int nkb = causal ? std::min(n_kb_all, (qt * kBlk + kBlk - 1 + off) / kBlk + 1) : n_kb_all;
+    return static_cast<long long>(nkb) + 1;
+  });
   auto kdkdv = bwd_dkdv_kernel<D, F16>;
   auto kdq = bwd_dq_kernel<D, F16>;
   if ((e = cudaFuncSetAttribute(kdkdv, cudaFuncAttributeMaxDynamicSharedMemorySize, DkdvCfg<D>::kAlloc)) !=
@@ -616,16 +760,16 @@ cudaError_t launch(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtenso
           cudaSuccess)
     return e;
   timing_begin(stream);
-  kdkdv<<<grid_kv, kThreads, DkdvCfg<D>::kAlloc, stream>>>(tmQ, tmK, tmV, tmdO, Lp, Dp,
-                                                            static_cast<uint16_t *>(dk),
-                                                            static_cast<uint16_t *>(dv), N, Nk, scale,
-                                                         scale_log2, causal, status);
+  kdkdv<<<sched_kv.G, kThreads, DkdvCfg<D>::kAlloc, stream>>>(tmQ, tmK, tmV, tmdO, Lp, Dp,
+                                                               static_cast<uint16_t *>(dk),
+                                                               static_cast<uint16_t *>(dv), N, Nk, sched_kv,
+                                                               scale, scale_log2, causal, status);
   timing_end(stream);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   timing_begin(stream);
-  kdq<<<grid_q, kThreads, DqCfg<D>::kAlloc, stream>>>(tmQ, tmK, tmV, tmdO, Lp, Dp,
-                                                       static_cast<uint16_t *>(dq), N, Nk, scale, scale_log2,
-                                                     causal, status);
+  kdq<<<sched_q.G, kThreads, DqCfg<D>::kAlloc, stream>>>(tmQ, tmK, tmV, tmdO, Lp, Dp,
+                                                          static_cast<uint16_t *>(dq), N, Nk, sched_q, scale,
+                                                          scale_log2, causal, status);
   timing_end(stream);
   return cudaGetLastError();
 }
@@ -637,20 +781,19 @@ cudaError_t launch_bwd_16(const CUtensorMap &tmQ, const CUtensorMap &tmK, const 
                           void *dq, void *dk, void *dv, float *Lp, float *Dp, int B, int H, int N, int Nk, int d,
                           float scale, int causal, bool f16, int *status, int num_sms, cudaStream_t stream,
                           int *launches) {
-  (void)num_sms;
   *launches += 3;
   if (f16) {
     if (d == 64)
       return launch<64, true>(tmQ, tmK, tmV, tmdO, o, dO, lse, dq, dk, dv, Lp, Dp, B, H, N, Nk, scale, causal,
-                              status, stream);
+                              status, num_sms, stream);
     return launch<128, true>(tmQ, tmK, tmV, tmdO, o, dO, lse, dq, dk, dv, Lp, Dp, B, H, N, Nk, scale, causal,
-                             status, stream);
+                             status, num_sms, stream);
   }
   if (d == 64)
     return launch<64, false>(tmQ, tmK, tmV, tmdO, o, dO, lse, dq, dk, dv, Lp, Dp, B, H, N, Nk, scale, causal,
-                             status, stream);
+                             status, num_sms, stream);
   return launch<128, false>(tmQ, tmK, tmV, tmdO, o, dO, lse, dq, dk, dv, Lp, Dp, B, H, N, Nk, scale, causal,
-                            status, stream);
+                            status, num_sms, stream);
 }
 
 }  // namespace fa
