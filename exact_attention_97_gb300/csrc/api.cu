@@ -110,6 +110,26 @@ int make_map(CUtensorMap *map, const void *ptr, int BH, int N, int d, bool f16) 
   return kOk;
 }
 
+// Map for the backward's dK / dV stores: 32-row x 16-column boxes with a
+// 32-byte swizzle, written from per-warp staging buffers. Rows past `N` in a
+// box are not written.
+int make_store_map(CUtensorMap *map, void *ptr, int BH, int N, int d, bool f16) {
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                        static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
+                           static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(d) * 2};
+  cuuint32_t box[3] = {16, 32, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, ptr,
+                        dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B,
+                        CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    t_last_cuda_error = static_cast<int>(r);
+    return kErrLaunch;
+  }
+  return kOk;
+}
+
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 int check_shape(int B, int H, int N, int d, int dmax) {
@@ -269,15 +289,17 @@ int bwd16(const void *q, const void *k, const void *v, const void *o, const floa
   DeviceInfo *dev = nullptr;
   if ((st = current_device(&dev)) != kOk) return st;
   if ((st = get_encoder()) != kOk) return st;
-  CUtensorMap tq, tk, tv, tdo;
+  CUtensorMap tq, tk, tv, tdo, tdk, tdv;
   const int BH = B * H;
   if ((st = make_map(&tq, q, BH, N, d, f16)) != kOk || (st = make_map(&tk, k, BH, Nk, d, f16)) != kOk ||
-      (st = make_map(&tv, v, BH, Nk, d, f16)) != kOk || (st = make_map(&tdo, dO, BH, N, d, f16)) != kOk)
+      (st = make_map(&tv, v, BH, Nk, d, f16)) != kOk || (st = make_map(&tdo, dO, BH, N, d, f16)) != kOk ||
+      (st = make_store_map(&tdk, dk, BH, Nk, d, f16)) != kOk ||
+      (st = make_store_map(&tdv, dv, BH, Nk, d, f16)) != kOk)
     return st;
   const BwdWorkspace w = ws_layout(B, H, N, d, FA_BF16);
   char *ws = static_cast<char *>(workspace);
   int launches = 0;
-  cudaError_t e = launch_bwd_16(tq, tk, tv, tdo, o, dO, lse, dq, dk, dv, reinterpret_cast<float *>(ws + w.lp),
+  cudaError_t e = launch_bwd_16(tq, tk, tv, tdo, tdk, tdv, o, dO, lse, dq, dk, dv, reinterpret_cast<float *>(ws + w.lp),
                                 reinterpret_cast<float *>(ws + w.dp), B, H, N, Nk, d, scale, causal ? 1 : 0, f16,
                                 dev->status, dev->num_sms, reinterpret_cast<cudaStream_t>(stream), &launches);
   if (e != cudaSuccess) return record(e);
@@ -430,16 +452,18 @@ extern "C" int fa_bwd_static_scratch(const void *q, const void *k, const void *v
   unsigned char *ws = nullptr;
   if ((st = static_scratch(&ws)) != kOk) return st;
   if ((st = get_encoder()) != kOk) return st;
-  CUtensorMap tq, tk, tv, tdo;
+  CUtensorMap tq, tk, tv, tdo, tdk, tdv;
   const int BH = B * H;
   if ((st = make_map(&tq, q, BH, N, d, false)) != kOk || (st = make_map(&tk, k, BH, N, d, false)) != kOk ||
-      (st = make_map(&tv, v, BH, N, d, false)) != kOk || (st = make_map(&tdo, dO, BH, N, d, false)) != kOk)
+      (st = make_map(&tv, v, BH, N, d, false)) != kOk || (st = make_map(&tdo, dO, BH, N, d, false)) != kOk ||
+      (st = make_store_map(&tdk, dk, BH, N, d, false)) != kOk ||
+      (st = make_store_map(&tdv, dv, BH, N, d, false)) != kOk)
     return st;
   // The first kernel of the pass rewrites every scratch byte it later reads
   // (the L and D rows, padding included), so the previous call's contents
   // never leak into this one.
   int launches = 0;
-  cudaError_t e = launch_bwd_16(tq, tk, tv, tdo, o, dO, lse, dq, dk, dv, reinterpret_cast<float *>(ws + w.lp),
+  cudaError_t e = launch_bwd_16(tq, tk, tv, tdo, tdk, tdv, o, dO, lse, dq, dk, dv, reinterpret_cast<float *>(ws + w.lp),
                                 reinterpret_cast<float *>(ws + w.dp), B, H, N, N, d, scale, causal ? 1 : 0, false,
                                 dev->status, dev->num_sms, reinterpret_cast<cudaStream_t>(stream), &launches);
   if (e != cudaSuccess) return record(e);

@@ -116,7 +116,10 @@ struct DkdvCfg {
   static constexpr int kV = kK + kTileBytes;
   static constexpr int kQ = kV + kTileBytes;
   static constexpr int kDO = kQ + kStages * kTileBytes;
-  static constexpr int kBytes = kDO + kStages * kTileBytes;
+  // epilogue staging: per storing warp, two 32-row x 16-column buffers
+  static constexpr int kStgBuf = 32 * 16 * 2;
+  static constexpr int kStg = kDO + kStages * kTileBytes;
+  static constexpr int kBytes = kStg + 8 * 2 * kStgBuf;
   static constexpr int kAlloc = kBytes + 1024;
   static constexpr uint32_t tS = 0, tDP = 128, tDV = 256, tDK = 256 + D;  // TMEM columns
 };
@@ -125,8 +128,8 @@ template <int D, bool F16>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
-                    const float *__restrict__ Lp, const float *__restrict__ Dp,
-                    uint16_t *__restrict__ dk, uint16_t *__restrict__ dv, int N, int Nk,
+                    const __grid_constant__ CUtensorMap tmdK, const __grid_constant__ CUtensorMap tmdV,
+                    const float *__restrict__ Lp, const float *__restrict__ Dp, int N, int Nk,
                     const __grid_constant__ TileSched sched, float scale, float scale_log2, int causal,
                     int *status) {
   using C = DkdvCfg<D>;
@@ -183,7 +186,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ---------------------------------------------------------------- producer
     // K of the next block loads as soon as the last S^T MMA of the current
-    // one has completed, V after its last dP^T; query tiles stream on.
+    // one has completed, V after its last dP^T (both prefetched into L2 one
+    // block ahead); query tiles stream on.
     if (lane == 0) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
@@ -209,6 +213,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (step == kDone) break;
         if (step == kSkip) continue;
         const int i_first = first_tile(kb), n_tiles = n_tiles_all - i_first;
+        {  // the next block's K and V are read once: start them towards L2 now
+          int nkb, nbh, ns, k2 = k + 1;
+          while ((ns = sched_item(sched, blockIdx.x, k2, nkb, nbh)) == kSkip) ++k2;
+          if (ns == kItem)
+            for (int x = 0; x < D; x += 64) {
+              tma_prefetch_l2_3d(&tmK, x, nkb * kBlk, nbh);
+              tma_prefetch_l2_3d(&tmV, x, nkb * kBlk, nbh);
+            }
+        }
         if (it > 0 && !mbar_wait(&k_empty, (it - 1) & 1, &abort_flag)) break;
         mbar_arrive_expect_tx(&k_full, C::kTileBytes);
         load_rows(smem + C::kK, &tmK, &k_full, D, kb * kBlk, bh);
@@ -379,29 +392,54 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         mbar_arrive(&ds_ready);
       }
-      // epilogue: warpgroup 0 stores dV, warpgroup 1 stores dK (times scale)
+      // epilogue: warpgroup 0 stores dV, warpgroup 1 stores dK (times scale).
+      // Each warp stages 32 rows x 16 columns at a time in shared memory (the
+      // layout of the store map's 32-byte swizzle: the two 16-byte halves of
+      // row r swap when bit 2 of r is set) and one lane writes the box with a
+      // TMA store, alternating two buffers; rows past Nk are not written.
       if (!ok || !mbar_wait_warp(&done, it & 1, &abort_flag)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const uint32_t col = h ? C::tDK : C::tDV;
-      const float mul = h ? scale : 1.f;
-      uint16_t *out = (h ? dk : dv) + (static_cast<size_t>(bh) * Nk + key) * D;
+      {
+        const uint32_t col = h ? C::tDK : C::tDV;
+        const float mul = h ? scale : 1.f;
+        const CUtensorMap *map = h ? &tmdK : &tmdV;
+        uint8_t *stg = smem + C::kStg + (warp - 4) * 2 * C::kStgBuf;
+        const int row0 = kb * kBlk + wq * 32;
+        const int sw = (lane >> 2) & 1;
 #pragma unroll 1
-      for (int ch = 0; ch < D / 32; ++ch) {
-        uint32_t r[32];
-        tmem_ld32(tmem + lane_addr + col + ch * 32, r);
-        uint32_t pk2[16];
+        for (int ch = 0; ch < D / 16; ++ch) {
+          uint8_t *buf = stg + (ch & 1) * C::kStgBuf;
+          if (lane == 0) {
+            if (ch == 0) bulk_wait_read_all();  // the previous block's stores have read both buffers
+            else bulk_wait_read_le1();          // the store of chunk ch - 2 has read this buffer
+          }
+          __syncwarp();
+          uint32_t r[16];
+          tmem_ld16(tmem + lane_addr + col + ch * 16, r);
+          uint32_t pk2[8];
 #pragma unroll
-        for (int u = 0; u < 16; ++u)
-          pk2[u] = E::pack(__uint_as_float(r[2 * u]) * mul, __uint_as_float(r[2 * u + 1]) * mul);
-        store_row32(out + ch * 32, pk2, key < Nk);
+          for (int u = 0; u < 8; ++u)
+            pk2[u] = E::pack(__uint_as_float(r[2 * u]) * mul, __uint_as_float(r[2 * u + 1]) * mul);
+          uint4 *row = reinterpret_cast<uint4 *>(buf + lane * 32);
+          row[sw] = make_uint4(pk2[0], pk2[1], pk2[2], pk2[3]);
+          row[sw ^ 1] = make_uint4(pk2[4], pk2[5], pk2[6], pk2[7]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0 && row0 < Nk) {
+            tma_store_3d(map, buf, ch * 16, row0, bh);
+            bulk_commit();
+          }
+        }
       }
       ++it;
     }
   }
 
+  // the staged dK / dV stores complete before the CTA's shared memory goes
+  if (warp >= 4 && lane == 0) bulk_wait_all();
   tc_fence_before();
   __syncthreads();
   if (warp == 2) {
@@ -497,7 +535,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------- loader: Q, dO, K
     // Q of the next tile loads once the last S MMA of the current one has
-    // completed, dO once its last dP MMA has; the K ring runs on.
+    // completed, dO once its last dP MMA has (both prefetched into L2 one
+    // tile ahead); the K ring runs on.
     if (lane == 0) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
@@ -509,6 +548,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (step == kDone) break;
         if (step == kSkip) continue;
         const int qt = qtile_of(rank), n_kb = kblocks(qt);
+        {  // the next tile's Q and dO are read once: start them towards L2 now
+          int nr, nbh, ns, k2 = k + 1;
+          while ((ns = sched_item(sched, blockIdx.x, k2, nr, nbh)) == kSkip) ++k2;
+          if (ns == kItem)
+            for (int x = 0; x < D; x += 64) {
+              tma_prefetch_l2_3d(&tmQ, x, qtile_of(nr) * kBlk, nbh);
+              tma_prefetch_l2_3d(&tmdO, x, qtile_of(nr) * kBlk, nbh);
+            }
+        }
         if (nq > 0 && !mbar_wait(&q_empty, (nq - 1) & 1, &abort_flag)) break;
         mbar_arrive_expect_tx(&q_full, C::kTileBytes);
         load_rows(smem + C::kQ, &tmQ, &q_full, D, qt * kBlk, bh);
@@ -724,7 +772,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int D, bool F16>
 cudaError_t launch(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtensorMap &tmV,
-                   const CUtensorMap &tmdO, const void *o, const void *dO, const float *lse, void *dq,
+                   const CUtensorMap &tmdO, const CUtensorMap &tmdK, const CUtensorMap &tmdV, const void *o,
+                   const void *dO, const float *lse, void *dq,
                    void *dk, void *dv, float *Lp, float *Dp, int B, int H, int N, int Nk, float scale,
                    int causal, int *status, int num_sms, cudaStream_t stream) {
   const int n_tiles = (N + kBlk - 1) / kBlk;
@@ -760,10 +809,8 @@ cudaError_t launch(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtenso
           cudaSuccess)
     return e;
   timing_begin(stream);
-  kdkdv<<<sched_kv.G, kThreads, DkdvCfg<D>::kAlloc, stream>>>(tmQ, tmK, tmV, tmdO, Lp, Dp,
-                                                               static_cast<uint16_t *>(dk),
-                                                               static_cast<uint16_t *>(dv), N, Nk, sched_kv,
-                                                               scale, scale_log2, causal, status);
+  kdkdv<<<sched_kv.G, kThreads, DkdvCfg<D>::kAlloc, stream>>>(tmQ, tmK, tmV, tmdO, tmdK, tmdV, Lp, Dp, N, Nk,
+                                                               sched_kv, scale, scale_log2, causal, status);
   timing_end(stream);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   timing_begin(stream);
@@ -777,22 +824,23 @@ cudaError_t launch(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtenso
 }  // namespace
 
 cudaError_t launch_bwd_16(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtensorMap &tmV,
-                          const CUtensorMap &tmdO, const void *o, const void *dO, const float *lse,
+                          const CUtensorMap &tmdO, const CUtensorMap &tmdK, const CUtensorMap &tmdV,
+                          const void *o, const void *dO, const float *lse,
                           void *dq, void *dk, void *dv, float *Lp, float *Dp, int B, int H, int N, int Nk, int d,
                           float scale, int causal, bool f16, int *status, int num_sms, cudaStream_t stream,
                           int *launches) {
   *launches += 3;
   if (f16) {
     if (d == 64)
-      return launch<64, true>(tmQ, tmK, tmV, tmdO, o, dO, lse, dq, dk, dv, Lp, Dp, B, H, N, Nk, scale, causal,
+      return launch<64, true>(tmQ, tmK, tmV, tmdO, tmdK, tmdV, o, dO, lse, dq, dk, dv, Lp, Dp, B, H, N, Nk, scale, causal,
                               status, num_sms, stream);
-    return launch<128, true>(tmQ, tmK, tmV, tmdO, o, dO, lse, dq, dk, dv, Lp, Dp, B, H, N, Nk, scale, causal,
+    return launch<128, true>(tmQ, tmK, tmV, tmdO, tmdK, tmdV, o, dO, lse, dq, dk, dv, Lp, Dp, B, H, N, Nk, scale, causal,
                              status, num_sms, stream);
   }
   if (d == 64)
-    return launch<64, false>(tmQ, tmK, tmV, tmdO, o, dO, lse, dq, dk, dv, Lp, Dp, B, H, N, Nk, scale, causal,
+    return launch<64, false>(tmQ, tmK, tmV, tmdO, tmdK, tmdV, o, dO, lse, dq, dk, dv, Lp, Dp, B, H, N, Nk, scale, causal,
                              status, num_sms, stream);
-  return launch<128, false>(tmQ, tmK, tmV, tmdO, o, dO, lse, dq, dk, dv, Lp, Dp, B, H, N, Nk, scale, causal,
+  return launch<128, false>(tmQ, tmK, tmV, tmdO, tmdK, tmdV, o, dO, lse, dq, dk, dv, Lp, Dp, B, H, N, Nk, scale, causal,
                             status, num_sms, stream);
 }
 

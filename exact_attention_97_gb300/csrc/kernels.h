@@ -45,9 +45,11 @@ cudaError_t launch_fwd_16(const CUtensorMap &tmQ, const CUtensorMap &tmK, const 
 
 // 16-bit tensor-core backward (three kernels: row terms, dK/dV pass, dQ
 // pass). Lp and Dp are [B*H][Np] fp32 with Np = 128*ceil(N/128), in the
-// caller's workspace.
+// caller's workspace. tmdK / tmdV are store maps {d, Nk, B*H} of dk / dv with
+// a {16, 32, 1} box and 32-byte swizzle.
 cudaError_t launch_bwd_16(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtensorMap &tmV,
-                          const CUtensorMap &tmdO, const void *o, const void *dO, const float *lse,
+                          const CUtensorMap &tmdO, const CUtensorMap &tmdK, const CUtensorMap &tmdV,
+                          const void *o, const void *dO, const float *lse,
                           void *dq, void *dk, void *dv, float *Lp, float *Dp, int B, int H, int N, int Nk, int d,
                           float scale, int causal, bool f16, int *status, int num_sms, cudaStream_t stream,
                           int *launches);

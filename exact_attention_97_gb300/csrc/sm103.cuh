@@ -104,6 +104,15 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, u
       : "memory");
 }
 
+// 3-D tiled store shared -> global, tracked as a bulk group of the issuing
+// thread. Box elements outside the tensor are not written.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, const void *src, int x, int y, int z) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+
 // Prefetch one tile of a 3-D tensor map into L2 (no shared-memory copy, no
 // completion to wait for).
 __device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap *map, int x, int y, int z) {
@@ -126,6 +135,8 @@ __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t b
 // Element-wise fp32 add of `bytes` of shared memory into global memory, done
 // by the copy engine (16-byte aligned addresses, size a multiple of 16).
 // Tracked as one bulk group: commit, then wait for the source to be read.
+// (Bulk groups are per issuing thread; the waits below cover that thread's
+// groups only.)
 __device__ __forceinline__ void bulk_reduce_add_f32(float *dst, const void *src, uint32_t bytes) {
   asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(
                    reinterpret_cast<uint64_t>(dst)),
@@ -135,6 +146,9 @@ __device__ __forceinline__ void bulk_reduce_add_f32(float *dst, const void *src,
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_read_all() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_read_le1() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
 }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
