@@ -248,7 +248,7 @@ int fwd16(const void *q, const void *k, const void *v, void *o, float *lse, int 
   if (st == kOk) st = check_shape(B, H, Nk, d, 128);
   if (st != kOk) return st;
   if (causal && Nk < N) return FA_ERR_SHAPE;  // leading queries would see no key
-  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (d != 64 && d != 96 && d != 128) return FA_ERR_UNSUPPORTED;
   if (!isfinite(scale)) return FA_ERR_ARG;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
     return FA_ERR_ALIGN;
@@ -277,7 +277,7 @@ int bwd16(const void *q, const void *k, const void *v, const void *o, const floa
   if (st == kOk) st = check_shape(B, H, Nk, d, 128);
   if (st != kOk) return st;
   if (causal && Nk < N) return FA_ERR_SHAPE;
-  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (d != 64 && d != 96 && d != 128) return FA_ERR_UNSUPPORTED;
   if (!isfinite(scale)) return FA_ERR_ARG;
   const void *ptrs[] = {q, k, v, o, dO, dq, dk, dv};
   for (const void *p : ptrs)
@@ -439,7 +439,7 @@ extern "C" int fa_bwd_static_scratch(const void *q, const void *k, const void *v
   if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return FA_ERR_NULL;
   int st = check_shape(B, H, N, d, 128);
   if (st != kOk) return st;
-  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (d != 64 && d != 96 && d != 128) return FA_ERR_UNSUPPORTED;
   if (!isfinite(scale)) return FA_ERR_ARG;
   const void *ptrs[] = {q, k, v, o, dO, dq, dk, dv};
   for (const void *p : ptrs)

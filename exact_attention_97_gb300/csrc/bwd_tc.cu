@@ -60,26 +60,21 @@ __device__ __forceinline__ void load_rows(uint8_t *dst, const CUtensorMap *map, 
 // 64h..64h+63) writes 32 columns at 64h, inside the 64 score columns it read.
 __device__ __forceinline__ uint32_t a_col(int kk) { return (kk >> 2) * 64 + (kk & 3) * 8; }
 
-// Stores 16 packed columns (32 elements) of a row to global memory when `ok`.
-__device__ __forceinline__ void store_row32(uint16_t *dst, const uint32_t (&pk)[16], bool ok) {
-  if (!ok) return;
-  uint4 *d4 = reinterpret_cast<uint4 *>(dst);
-#pragma unroll
-  for (int u = 0; u < 4; ++u) d4[u] = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
-}
-
 // ------------------------------------------------------------------ kernel 1
 // Per query row of a head padded to Np = 128*ceil(N/128) rows:
 //   Lp = -L * log2(e) (so the passes form p = 2^(s*c + Lp)), -inf past N;
 //   Dp = sum_c dO_ic O_ic, 0 past N.
-// One group of D/8 threads per row, 16-byte loads.
+// One group of prep_tpr(D) threads per row (D/8 rounded up to a power of
+// two), one 16-byte load of O and of dO per thread that has one.
+__host__ __device__ constexpr int prep_tpr(int D) { return D / 8 <= 8 ? 8 : (D / 8 <= 16 ? 16 : 32); }
+
 template <int D, bool F16>
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const uint16_t *__restrict__ o,
                                                        const uint16_t *__restrict__ dO,
                                                        const float *__restrict__ lse,
                                                        float *__restrict__ Lp, float *__restrict__ Dp,
                                                        int N, int Np, int64_t prow_total) {
-  constexpr int kTpr = D / 8;  // threads per row
+  constexpr int kTpr = prep_tpr(D);  // threads per row
   const int64_t gid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t pr = gid / kTpr;  // padded row index
   const int part = static_cast<int>(gid % kTpr);
@@ -88,7 +83,7 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const uint16_t *__restric
   const bool real = pr < prow_total && i < N;
   const int64_t r = bh * N + i;  // unpadded row
   float s = 0.f;
-  if (real) {
+  if (real && part < D / 8) {
     const uint4 a = *reinterpret_cast<const uint4 *>(o + r * D + part * 8);
     const uint4 b = *reinterpret_cast<const uint4 *>(dO + r * D + part * 8);
     const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
@@ -109,8 +104,9 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const uint16_t *__restric
 // ------------------------------------------------------------------ kernel 2
 template <int D>
 struct DkdvCfg {
-  static constexpr int kStages = (D == 128) ? 2 : 3;
-  static constexpr int kTileBytes = kBlk * D * 2;
+  static constexpr int kDP = (D + 63) / 64 * 64;  // whole 64-column TMA boxes per row
+  static constexpr int kStages = (kDP == 128) ? 2 : 3;
+  static constexpr int kTileBytes = kBlk * kDP * 2;
   static constexpr int kSubBytes = kBlk * 128;  // 128 rows x 64 16-bit elements
   static constexpr int kK = 0;
   static constexpr int kV = kK + kTileBytes;
@@ -455,9 +451,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 // flight while dQ of the current one runs.
 template <int D>
 struct DqCfg {
-  static constexpr int kKStages = (D == 128) ? 3 : 4;
-  static constexpr int kVStages = (D == 128) ? 2 : 3;
-  static constexpr int kTileBytes = kBlk * D * 2;
+  static constexpr int kDP = (D + 63) / 64 * 64;  // whole 64-column TMA boxes per row
+  static constexpr int kKStages = (kDP == 128) ? 3 : 4;
+  static constexpr int kVStages = (kDP == 128) ? 2 : 3;
+  static constexpr int kTileBytes = kBlk * kDP * 2;
   static constexpr int kSubBytes = kBlk * 128;
   static constexpr int kQ = 0;
   static constexpr int kDO = kQ + kTileBytes;
@@ -740,7 +737,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         mbar_arrive(&ds_ready);
       }
-      // epilogue: dQ = scale * accumulator; warpgroup h stores head columns [hD/2, hD/2 + D/2)
+      // epilogue: dQ = scale * accumulator; warpgroup h stores head columns
+      // [hD/2, hD/2 + D/2), 16 at a time
       if (!ok || !mbar_wait_warp(&done, it & 1, &abort_flag)) {
         ok = false;
         break;
@@ -748,14 +746,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       uint16_t *out = dq + (static_cast<size_t>(bh) * N + q) * D + h * (D / 2);
 #pragma unroll 1
-      for (int ch = 0; ch < D / 64; ++ch) {
-        uint32_t rr[32];
-        tmem_ld32(tmem + lane_addr + C::tDQ + h * (D / 2) + ch * 32, rr);
-        uint32_t pk2[16];
+      for (int ch = 0; ch < D / 32; ++ch) {
+        uint32_t rr[16];
+        tmem_ld16(tmem + lane_addr + C::tDQ + h * (D / 2) + ch * 16, rr);
+        uint32_t pk2[8];
 #pragma unroll
-        for (int u = 0; u < 16; ++u)
+        for (int u = 0; u < 8; ++u)
           pk2[u] = E::pack(__uint_as_float(rr[2 * u]) * scale, __uint_as_float(rr[2 * u + 1]) * scale);
-        store_row32(out + ch * 32, pk2, q < N);
+        if (q < N) {
+          uint4 *d4 = reinterpret_cast<uint4 *>(out + ch * 16);
+          d4[0] = make_uint4(pk2[0], pk2[1], pk2[2], pk2[3]);
+          d4[1] = make_uint4(pk2[4], pk2[5], pk2[6], pk2[7]);
+        }
       }
       ++it;
     }
@@ -781,7 +783,7 @@ cudaError_t launch(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtenso
   const float scale_log2 = scale * kLog2e;
   {
     const int64_t prows = static_cast<int64_t>(B) * H * Np;
-    const int64_t threads = prows * (D / 8);
+    const int64_t threads = prows * prep_tpr(D);
     bwd_prep_kernel<D, F16><<<static_cast<unsigned>((threads + 255) / 256), 256, 0, stream>>>(
         static_cast<const uint16_t *>(o), static_cast<const uint16_t *>(dO), lse, Lp, Dp, N, Np,
         prows);
@@ -830,18 +832,18 @@ cudaError_t launch_bwd_16(const CUtensorMap &tmQ, const CUtensorMap &tmK, const 
                           float scale, int causal, bool f16, int *status, int num_sms, cudaStream_t stream,
                           int *launches) {
   *launches += 3;
+#define FA_BWD_LAUNCH(DD, FF)                                                                                  \
+  return launch<DD, FF>(tmQ, tmK, tmV, tmdO, tmdK, tmdV, o, dO, lse, dq, dk, dv, Lp, Dp, B, H, N, Nk, scale, \
+                        causal, status, num_sms, stream)
   if (f16) {
-    if (d == 64)
-      return launch<64, true>(tmQ, tmK, tmV, tmdO, tmdK, tmdV, o, dO, lse, dq, dk, dv, Lp, Dp, B, H, N, Nk, scale, causal,
-                              status, num_sms, stream);
-    return launch<128, true>(tmQ, tmK, tmV, tmdO, tmdK, tmdV, o, dO, lse, dq, dk, dv, Lp, Dp, B, H, N, Nk, scale, causal,
-                             status, num_sms, stream);
+    if (d == 64) FA_BWD_LAUNCH(64, true);
+    if (d == 96) FA_BWD_LAUNCH(96, true);
+    FA_BWD_LAUNCH(128, true);
   }
-  if (d == 64)
-    return launch<64, false>(tmQ, tmK, tmV, tmdO, tmdK, tmdV, o, dO, lse, dq, dk, dv, Lp, Dp, B, H, N, Nk, scale, causal,
-                             status, num_sms, stream);
-  return launch<128, false>(tmQ, tmK, tmV, tmdO, tmdK, tmdV, o, dO, lse, dq, dk, dv, Lp, Dp, B, H, N, Nk, scale, causal,
-                            status, num_sms, stream);
+  if (d == 64) FA_BWD_LAUNCH(64, false);
+  if (d == 96) FA_BWD_LAUNCH(96, false);
+  FA_BWD_LAUNCH(128, false);
+#undef FA_BWD_LAUNCH
 }
 
 }  // namespace fa

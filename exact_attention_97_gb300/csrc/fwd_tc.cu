@@ -61,14 +61,16 @@ constexpr float kLn2 = 0.69314718055994531f;
 #endif
 
 // Shared memory: kQBuf query tiles (two let the next tile's Q land while the
-// current tile still runs), the K ring and the V ring. At d = 128 two Q
+// current tile still runs), the K ring and the V ring. At d = 96 and 128 two Q
 // buffers and three K stages leave room for two V stages under the 227 KB
 // limit.
 template <int D>
 struct FwdSmem {
+  // a row of a tile is whole 64-column TMA boxes; columns past D read as zero
+  static constexpr int kDP = (D + 63) / 64 * 64;
   static constexpr int kQBuf = FA_FWD_QBUF;
-  static constexpr int kVStages = (D == 128 && kQBuf == 2) ? 2 : 3;
-  static constexpr int kTileBytes = kBlockN * D * 2;  // one 128 x D bf16 tile
+  static constexpr int kVStages = (kDP == 128 && kQBuf == 2) ? 2 : 3;
+  static constexpr int kTileBytes = kBlockN * kDP * 2;  // one 128 x kDP 16-bit tile
   static constexpr int kSubBytes = kBlockN * 128;     // one 128 x 64 sub-tile
   static constexpr int kQ = 0;
   static constexpr int kK = kQ + kQBuf * kTileBytes;
@@ -469,9 +471,11 @@ cudaError_t launch_fwd_16(const CUtensorMap &tmQ, const CUtensorMap &tmK, const 
   *launches += 1;
   if (f16) {
     if (d == 64) return launch<64, true>(tmQ, tmK, tmV, o, lse, B, H, N, Nk, scale, causal, status, num_sms, stream);
+    if (d == 96) return launch<96, true>(tmQ, tmK, tmV, o, lse, B, H, N, Nk, scale, causal, status, num_sms, stream);
     return launch<128, true>(tmQ, tmK, tmV, o, lse, B, H, N, Nk, scale, causal, status, num_sms, stream);
   }
   if (d == 64) return launch<64, false>(tmQ, tmK, tmV, o, lse, B, H, N, Nk, scale, causal, status, num_sms, stream);
+  if (d == 96) return launch<96, false>(tmQ, tmK, tmV, o, lse, B, H, N, Nk, scale, causal, status, num_sms, stream);
   return launch<128, false>(tmQ, tmK, tmV, o, lse, B, H, N, Nk, scale, causal, status, num_sms, stream);
 }
 

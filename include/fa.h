@@ -43,7 +43,7 @@
  *              fa_last_cuda_error). A kernel that gives up on an internal
  *              wait (it never traps) records FA_ERR_TIMEOUT in a device
  *              status word read by fa_device_status.
- *   Supported  bf16 and f16: d in {64, 128}, N >= 1 (ragged tails are
+ *   Supported  bf16 and f16: d in {64, 96, 128}, N >= 1 (ragged tails are
  *              masked), every pointer 16-byte aligned.
  *              f32: 1 <= d <= 128, N >= 1, every pointer 4-byte aligned.
  *              B, H >= 1; B*H*N*d must be below 2^40 elements.

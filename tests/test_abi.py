@@ -84,7 +84,7 @@ def test_fwd_argument_errors(lib):
     assert _fwd(lib, B=-1) == 2
     assert _fwd(lib, d=0) == 2
     assert _fwd(lib, d=256) == 2
-    assert _fwd(lib, d=96) == 3          # valid head size without a bf16 kernel
+    assert _fwd(lib, d=80) == 3          # valid head size without a bf16 kernel
     assert _fwd(lib, B=300, H=300) == 3  # more than 65535 heads
     assert _fwd(lib, N=1 << 30, B=4, H=4, d=128) == 2  # 2^40 elements
     assert _fwd(lib, q=P + 8) == 4       # TMA needs 16-byte aligned bases
@@ -108,7 +108,7 @@ def test_bwd_argument_errors(lib):
 def test_f16_argument_errors(lib):
     args = [P] * 5
     assert lib.fa_fwd_f16(None, *args[1:], 1, 1, 128, 64, 0.125, 0, None) == 1
-    assert lib.fa_fwd_f16(*args, 1, 1, 128, 96, 0.125, 0, None) == 3
+    assert lib.fa_fwd_f16(*args, 1, 1, 128, 80, 0.125, 0, None) == 3
     assert lib.fa_fwd_f16(P + 8, *args[1:], 1, 1, 128, 64, 0.125, 0, None) == 4
     ptrs = [P] * 9
     assert lib.fa_bwd_f16(*ptrs, 1, 1, 128, 64, 0.125, 0, None, 0, None) == 5

@@ -89,7 +89,7 @@ def test_f32_ragged(d, N, causal):
 
 # ------------------------------------------------------------ bf16 tensor-core path, full oracle
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 96, 128])
 @pytest.mark.parametrize("N", [1, 4, 127, 128, 129, 300])
 @pytest.mark.parametrize("causal", [False, True])
 def test_bf16_small_and_ragged(d, N, causal):
@@ -100,7 +100,7 @@ def test_bf16_small_and_ragged(d, N, causal):
           _full_ref(_np(q), _np(k), _np(v), _np(dO), scale, causal))
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 96, 128])
 def test_bf16_scale_and_large_scores(d):
     """Scores far from the unit range (the running max moves by many 2^8
     steps): a large scale and queries scaled up."""
@@ -113,9 +113,20 @@ def test_bf16_scale_and_large_scores(d):
               _full_ref(_np(q), _np(k), _np(v), _np(dO), 0.5, causal))
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_bf16_B2_H4_N1000_d96(causal):
+    """Head size 96: tiles are padded to two 64-column boxes, products use
+    N = 96; many tiles per item and a ragged tail."""
+    q, k, v, dO = make_qkv_do(2, 4, 1000, 96, seed=96, dtype=torch.bfloat16)
+    scale = 1.0 / math.sqrt(96)
+    got = _as_dict(run_gpu(q, k, v, dO, scale, causal))
+    check(f"bf16_B2_H4_N1000_d96_c{int(causal)}", "bf16", got,
+          _full_ref(_np(q), _np(k), _np(v), _np(dO), scale, causal))
+
+
 # ------------------------------------------------------------ f16 inputs (same kernels, f16 operands)
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 96, 128])
 @pytest.mark.parametrize("N", [1, 127, 300])
 @pytest.mark.parametrize("causal", [False, True])
 def test_f16_small_and_ragged(d, N, causal):
@@ -156,7 +167,7 @@ def _run_gpu_kv(q, k, v, dO, scale, causal):
 
 @pytest.mark.parametrize("Nq,Nk,causal", [(1, 300, True), (1, 300, False), (128, 1000, True), (100, 640, True),
                                           (257, 511, True), (300, 130, False), (640, 641, True)])
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 96, 128])
 def test_bf16_kv_lengths(Nq, Nk, causal, d):
     """Decode / chunked-prefill shapes: causal mask aligned bottom-right."""
     q, _, _, dO = make_qkv_do(1, 2, Nq, d, seed=300 + Nq, dtype=torch.bfloat16)
