@@ -31,6 +31,7 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "attention fwd/bwd TFLOP/s at B8 H32 N4096 d128 bf16; % of BF16 tensor peak"
+METRIC_FWD = "attention forward TFLOP/s (forward-only run of the workload in config); % of BF16 tensor peak"
 
 # DRAM bytes per launch of the dominant kernel at the headline size, from the
 # ncu capture summarised in profiles/ncu_full_fwd_dkdv_dq_bf16_B2_H32_N4096_d128.md
@@ -219,11 +220,12 @@ def run_ours(args, w):
         n = fa.fa_last_launch_count()
         if mark:
             m[1].record(stream)
-        fa.attention_backward(q, k, v, o, lse, dO, w.scale, w.causal, workspace=ws, grads=(dq, dk, dv))
+        if not args.fwd_only:
+            fa.attention_backward(q, k, v, o, lse, dO, w.scale, w.causal, workspace=ws, grads=(dq, dk, dv))
         if mark:
             m[2].record(stream)
             marks.append(m)
-        launches[0] += n + fa.fa_last_launch_count()
+        launches[0] += n + (0 if args.fwd_only else fa.fa_last_launch_count())
 
     for _ in range(args.warmup):
         step()
@@ -232,8 +234,10 @@ def run_ours(args, w):
         raise RuntimeError("kernel pipeline timeout during warm-up")
 
     # per-kernel events recorded by the library around each tensor-core kernel:
-    # per step, pair 3s = forward, 3s+1 = dK/dV pass, 3s+2 = dQ pass
-    pairs = 3 * args.steps
+    # per step, pair 3s = forward, 3s+1 = dK/dV pass, 3s+2 = dQ pass (one pair
+    # per step with --fwd-only)
+    per = 1 if args.fwd_only else 3
+    pairs = per * args.steps
     evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * pairs)]
     for e in evs:
         e.record(stream)  # creates the underlying CUDA event
@@ -262,18 +266,19 @@ def run_ours(args, w):
     ms = start.elapsed_time(stop)
 
     def pair_ms(i):
-        return statistics.mean(evs[2 * (3 * s + i)].elapsed_time(evs[2 * (3 * s + i) + 1])
+        return statistics.mean(evs[2 * (per * s + i)].elapsed_time(evs[2 * (per * s + i) + 1])
                                for s in range(args.steps))
 
-    k_fwd, k_dkdv, k_dq = pair_ms(0), pair_ms(1), pair_ms(2)
+    k_fwd = pair_ms(0)
+    k_dkdv, k_dq = (None, None) if args.fwd_only else (pair_ms(1), pair_ms(2))
     fwd_call = statistics.mean(m[0].elapsed_time(m[1]) for m in marks)
-    bwd_call = statistics.mean(m[1].elapsed_time(m[2]) for m in marks)
+    bwd_call = None if args.fwd_only else statistics.mean(m[1].elapsed_time(m[2]) for m in marks)
     if world > 1:
         t = torch.tensor([ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms = float(t.item())
 
-    flops_step = w.flops_fwd() + w.flops_bwd()
+    flops_step = w.flops_fwd() + (0 if args.fwd_only else w.flops_bwd())
     value = flops_step * world * args.steps / (ms * 1e-3) / 1e12
     peaks = _peaks()
     peak = peaks["bf16_tflops"]
@@ -285,31 +290,33 @@ def run_ours(args, w):
     # Algorithmic flops per kernel: the backward's five contractions are split
     # as S, dP, dV, dK in the dK/dV pass (2F) and dQ in the dQ pass (F/2); the
     # dQ pass also recomputes S and dP (executed 3F/2).
-    kernels = {
-        "fwd_kernel": {"ms": k_fwd, "algo_tflops": tf(F, k_fwd), "frac": tf(F, k_fwd) / peak},
-        "bwd_dkdv_kernel": {"ms": k_dkdv, "algo_tflops": tf(2 * F, k_dkdv), "frac": tf(2 * F, k_dkdv) / peak},
-        "bwd_dq_kernel": {"ms": k_dq, "algo_tflops": tf(0.5 * F, k_dq), "executed_tflops": tf(1.5 * F, k_dq),
-                          "executed_frac": tf(1.5 * F, k_dq) / peak},
-    }
-    dom = max(("fwd_kernel", F, k_fwd), ("bwd_dkdv_kernel", 2 * F, k_dkdv),
-              ("bwd_dq_kernel", 0.5 * F, k_dq), key=lambda x: x[2])
+    kernels = {"fwd_kernel": {"ms": k_fwd, "algo_tflops": tf(F, k_fwd), "frac": tf(F, k_fwd) / peak}}
+    dom = ("fwd_kernel", F, k_fwd)
+    if not args.fwd_only:
+        kernels["bwd_dkdv_kernel"] = {"ms": k_dkdv, "algo_tflops": tf(2 * F, k_dkdv),
+                                      "frac": tf(2 * F, k_dkdv) / peak}
+        kernels["bwd_dq_kernel"] = {"ms": k_dq, "algo_tflops": tf(0.5 * F, k_dq),
+                                    "executed_tflops": tf(1.5 * F, k_dq), "executed_frac": tf(1.5 * F, k_dq) / peak}
+        dom = max(("fwd_kernel", F, k_fwd), ("bwd_dkdv_kernel", 2 * F, k_dkdv),
+                  ("bwd_dq_kernel", 0.5 * F, k_dq), key=lambda x: x[2])
     achieved = tf(dom[1], dom[2])
     roofline = {"bound": "tensor", "kernel": f"{dom[0]}<{w.d}>", "achieved": achieved, "peak": peak,
                 "unit": "TFLOP/s", "frac": achieved / peak,
                 "traffic": args.traffic if args.traffic is not None else _measured_traffic(f"{dom[0]}<{w.d}>", w.name),
                 "peak_source": peaks["source"] + " burst bf16 (cuBLAS), of measured"}
     fwd_tf = tf(w.flops_fwd(), fwd_call)
-    bwd_tf = tf(w.flops_bwd(), bwd_call)
+    bwd_tf = None if args.fwd_only else tf(w.flops_bwd(), bwd_call)
 
     # end to end through the public API: pinned host inputs in, results back to pinned host
     e2e = None
     if not args.no_e2e:
-        out_h = [torch.empty_like(t).pin_memory() for t in (q_h, q_h, k_h, v_h)]
+        out_h = [torch.empty_like(t).pin_memory() for t in ((q_h,) if args.fwd_only else (q_h, q_h, k_h, v_h))]
 
         def e2e_step():
             qd, kd, vd, dod = (t.to(dev, non_blocking=True) for t in (q_h, k_h, v_h, do_h))
             od, ld = fa.attention_forward(qd, kd, vd, w.scale, w.causal)
-            g = fa.attention_backward(qd, kd, vd, od, ld, dod, w.scale, w.causal, workspace=ws)
+            g = () if args.fwd_only else fa.attention_backward(qd, kd, vd, od, ld, dod, w.scale, w.causal,
+                                                               workspace=ws)
             for dst, src in zip(out_h, (od, *g)):
                 dst.copy_(src, non_blocking=True)
 
@@ -330,19 +337,20 @@ def run_ours(args, w):
             t = torch.tensor([ems], device=dev)
             dist.all_reduce(t, op=dist.ReduceOp.MAX)
             ems = float(t.item())
-        bytes_in = sum(t.numel() * t.element_size() for t in (q_h, k_h, v_h, do_h))
+        bytes_in = sum(t.numel() * t.element_size() for t in ((q_h, k_h, v_h) if args.fwd_only else
+                                                                (q_h, k_h, v_h, do_h)))
         bytes_out = sum(t.numel() * t.element_size() for t in out_h)
         e2e = {"value": flops_step * world * e2e_steps / (ems * 1e-3) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": bytes_in, "d2h_bytes_per_step": bytes_out,
                "ms_per_step": ems / e2e_steps}
 
     base = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.fwd_only:
         base = cpu_baseline(w, args.cpu_heads)
 
     if rank == 0:
         line = {
-            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "metric": METRIC_FWD if args.fwd_only else METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
             "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "Nk": w.n_keys, "d": w.d,
@@ -353,7 +361,7 @@ def run_ours(args, w):
                        "parallelism": f"{world} independent replica(s), no collective"},
             "pct_of_peak": value / (peak * world) * 100.0,
             "fwd": {"ms": fwd_call, "tflops": fwd_tf, "frac": fwd_tf / peak},
-            "bwd": {"ms": bwd_call, "tflops": bwd_tf, "frac": bwd_tf / peak},
+            "bwd": None if args.fwd_only else {"ms": bwd_call, "tflops": bwd_tf, "frac": bwd_tf / peak},
             "kernels": kernels,
             "roofline": roofline,
             "cpu_baseline": base,
@@ -378,6 +386,8 @@ def main():
                     help="B,H,N,d[,causal]: another case of the same kernels (profiling, other shapes)")
     ap.add_argument("--nk", type=int, default=0, help="key/value rows per head for --shape (default N)")
     ap.add_argument("--dtype", choices=["bf16", "f16"], default="bf16", help="16-bit input type for --shape")
+    ap.add_argument("--fwd-only", action="store_true",
+                    help="time the forward alone (head sizes with no backward kernel, e.g. d = 256)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-heads", type=int, default=8, help="heads in the CPU-baseline sample")

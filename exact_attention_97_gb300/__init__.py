@@ -53,7 +53,7 @@ def _stream_handle(stream):
 def attention_forward(q, k, v, scale=None, causal=False, out=None, lse=None, stream=None):
     """(O, L) for CUDA tensors q [B, H, Nq, d] and k, v [B, H, Nk, d] (all bf16, all f16 or all float32).
 
-    bf16 and f16 need d in {64, 96, 128}; float32 takes 1 <= d <= 128 and Nk == Nq. L is
+    bf16 and f16 need d in {64, 96, 128} (or 256 for the forward); float32 takes 1 <= d <= 128 and Nk == Nq. L is
     float32 [B, H, Nq], the natural-log log-sum-exp of the scaled scores. With Nk != Nq
     the causal mask is aligned bottom-right (query i sees keys j <= i + Nk - Nq).
     """

@@ -244,11 +244,11 @@ namespace {
 int fwd16(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int N, int Nk,
           int d, float scale, int causal, fa_stream_t stream, bool f16) {
   if (!q || !k || !v || !o || !lse) return FA_ERR_NULL;
-  int st = check_shape(B, H, N, d, 128);
-  if (st == kOk) st = check_shape(B, H, Nk, d, 128);
+  int st = check_shape(B, H, N, d, 256);
+  if (st == kOk) st = check_shape(B, H, Nk, d, 256);
   if (st != kOk) return st;
   if (causal && Nk < N) return FA_ERR_SHAPE;  // leading queries would see no key
-  if (d != 64 && d != 96 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (d != 64 && d != 96 && d != 128 && d != 256) return FA_ERR_UNSUPPORTED;
   if (!isfinite(scale)) return FA_ERR_ARG;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
     return FA_ERR_ALIGN;
@@ -273,11 +273,11 @@ int bwd16(const void *q, const void *k, const void *v, const void *o, const floa
           void *dq, void *dk, void *dv, int B, int H, int N, int Nk, int d, float scale, int causal,
           void *workspace, size_t workspace_bytes, fa_stream_t stream, bool f16) {
   if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return FA_ERR_NULL;
-  int st = check_shape(B, H, N, d, 128);
-  if (st == kOk) st = check_shape(B, H, Nk, d, 128);
+  int st = check_shape(B, H, N, d, 256);
+  if (st == kOk) st = check_shape(B, H, Nk, d, 256);
   if (st != kOk) return st;
   if (causal && Nk < N) return FA_ERR_SHAPE;
-  if (d != 64 && d != 96 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (d != 64 && d != 96 && d != 128) return FA_ERR_UNSUPPORTED;  // no d = 256 backward
   if (!isfinite(scale)) return FA_ERR_ARG;
   const void *ptrs[] = {q, k, v, o, dO, dq, dk, dv};
   for (const void *p : ptrs)

@@ -50,8 +50,6 @@ namespace {
 
 constexpr int kBlockM = 128;   // query rows per tile (= TMEM lanes)
 constexpr int kBlockN = 128;   // keys per tile
-constexpr int kStages = 3;     // K ring depth
-constexpr int kSBuf = 3;       // S buffers in TMEM (3 x 128 columns, O after them)
 constexpr int kThreads = 256;  // 8 warps
 constexpr float kRescaleLog2 = 8.0f;  // move the running max only past 2^8
 constexpr float kLn2 = 0.69314718055994531f;
@@ -60,28 +58,41 @@ constexpr float kLn2 = 0.69314718055994531f;
 #define FA_FWD_QBUF 2
 #endif
 
-// Shared memory: kQBuf query tiles (two let the next tile's Q land while the
-// current tile still runs), the K ring and the V ring. At d = 96 and 128 two Q
-// buffers and three K stages leave room for two V stages under the 227 KB
-// limit.
+// Shared memory and tensor memory by head size. A row of a tile is whole
+// 64-column TMA boxes (columns past D read as zero). K and V stream in units
+// of at most 128 columns: one unit per key tile up to d = 128, two at d = 256
+// (the score product then accumulates over both K units, and P V runs as two
+// N = 128 products, one per V unit). Shared memory holds kQBuf query tiles
+// (two let the next tile's Q land while the current tile still runs), the K
+// ring and the V ring, under the 227 KB limit: at d = 96 and 128, 2 Q + 3 K +
+// 2 V tiles; at d = 256, 1 Q tile + 3 K + 2 V units. Tensor memory holds
+// kSBuf score buffers of 128 columns and O after them (512 columns).
 template <int D>
 struct FwdSmem {
-  // a row of a tile is whole 64-column TMA boxes; columns past D read as zero
   static constexpr int kDP = (D + 63) / 64 * 64;
-  static constexpr int kQBuf = FA_FWD_QBUF;
-  static constexpr int kVStages = (kDP == 128 && kQBuf == 2) ? 2 : 3;
-  static constexpr int kTileBytes = kBlockN * kDP * 2;  // one 128 x kDP 16-bit tile
-  static constexpr int kSubBytes = kBlockN * 128;     // one 128 x 64 sub-tile
+  static constexpr int kUnits = kDP > 128 ? kDP / 128 : 1;  // K / V ring units per key tile
+  static constexpr int kUnitCols = kDP / kUnits;
+  static constexpr int kUnitBytes = kBlockN * kUnitCols * 2;
+  static constexpr int kQBytes = kBlockM * kDP * 2;
+  static constexpr int kSK = (kUnits == 1 ? D : kUnitCols) / 16;  // k-steps of S per unit
+  static constexpr int kPVN = kUnits == 1 ? D : kUnitCols;         // N of one P V product
+  static constexpr int kSBuf = kDP > 128 ? 2 : 3;
+  static constexpr int kQBuf = kDP > 128 ? 1 : FA_FWD_QBUF;
+  static constexpr int kKStages = 3;
+  static constexpr int kVStages = kDP > 128 ? 2 : ((kDP == 128 && kQBuf == 2) ? 2 : 3);
+  static constexpr int kSubBytes = kBlockN * 128;  // one 128-row x 64-column sub-tile
   static constexpr int kQ = 0;
-  static constexpr int kK = kQ + kQBuf * kTileBytes;
-  static constexpr int kV = kK + kStages * kTileBytes;
-  static constexpr int kBytes = kV + kVStages * kTileBytes;
+  static constexpr int kK = kQ + kQBuf * kQBytes;
+  static constexpr int kV = kK + kKStages * kUnitBytes;
+  static constexpr int kBytes = kV + kVStages * kUnitBytes;
   static constexpr int kAlloc = kBytes + 1024;  // slack for 1024-byte alignment
 };
 
-__device__ __forceinline__ void load_tile(uint8_t *dst, const CUtensorMap *map, uint64_t *bar,
-                                          int D, int row, int bh) {
-  for (int x = 0; x < D; x += 64) tma_load_3d(dst + (x / 64) * (kBlockN * 128), map, bar, x, row, bh);
+// Columns [c0, c1) of 128 rows starting at `row`, as 64-column boxes into
+// consecutive sub-tiles at dst.
+__device__ __forceinline__ void load_cols(uint8_t *dst, const CUtensorMap *map, uint64_t *bar, int c0, int c1,
+                                          int row, int bh) {
+  for (int x = c0; x < c1; x += 64) tma_load_3d(dst + ((x - c0) / 64) * (kBlockN * 128), map, bar, x, row, bh);
 }
 
 template <int D, bool F16>
@@ -96,7 +107,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
-  constexpr int kQBuf = L::kQBuf, kVStages = L::kVStages;
+  constexpr int kQBuf = L::kQBuf, kStages = L::kKStages, kVStages = L::kVStages, kSBuf = L::kSBuf;
+  constexpr int kUnits = L::kUnits, kUC = L::kUnitCols;
   __shared__ uint64_t q_full[kQBuf], q_empty[kQBuf], k_full[kStages], k_empty[kStages], v_full[kVStages],
       v_empty[kVStages], s_full[kSBuf], p_ready[kSBuf], pv_done[kSBuf], drain_s, drain_pv;
   __shared__ uint32_t tmem_base_s;
@@ -175,17 +187,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const int qb = it % kQBuf;
         if (it >= kQBuf && !mbar_wait(&q_empty[qb], ((it / kQBuf) & 1) ^ 1, &abort_flag)) { ok = false; break; }
-        mbar_arrive_expect_tx(&q_full[qb], L::kTileBytes);
-        load_tile(smem + L::kQ + qb * L::kTileBytes, &tmQ, &q_full[qb], D, qtile * kBlockM, bh);
-        const int nk = ktiles(qtile);
+        mbar_arrive_expect_tx(&q_full[qb], L::kQBytes);
+        load_cols(smem + L::kQ + qb * L::kQBytes, &tmQ, &q_full[qb], 0, D, qtile * kBlockM, bh);
+        const int nk = ktiles(qtile) * kUnits;  // K units of this item
         for (int j = 0; j < nk; ++j, ++kt) {
-          const int st = kt % kStages;
+          const int st = kt % kStages, c0 = (j % kUnits) * kUC;
           if (kt >= kStages && !mbar_wait(&k_empty[st], ((kt / kStages) & 1) ^ 1, &abort_flag)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&k_full[st], L::kTileBytes);
-          load_tile(smem + L::kK + st * L::kTileBytes, &tmK, &k_full[st], D, j * kBlockN, bh);
+          mbar_arrive_expect_tx(&k_full[st], L::kUnitBytes);
+          load_cols(smem + L::kK + st * L::kUnitBytes, &tmK, &k_full[st], c0, min(D, c0 + kUC),
+                    (j / kUnits) * kBlockN, bh);
         }
         ++it;  // this item's Q load was issued
       }
@@ -203,27 +216,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int step = sched_item(sched, blockIdx.x, k, rank, bh);
         if (step == kDone) break;
         if (step == kSkip) continue;
-        const int nk = ktiles(qtile_of(rank));
+        const int nk = ktiles(qtile_of(rank)) * kUnits;  // V units of this item
         for (int j = 0; j < nk; ++j, ++kt) {
-          const int st = kt % kVStages;
+          const int st = kt % kVStages, c0 = (j % kUnits) * kUC;
           if (kt >= kVStages && !mbar_wait(&v_empty[st], ((kt / kVStages) & 1) ^ 1, &abort_flag)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&v_full[st], L::kTileBytes);
-          load_tile(smem + L::kV + st * L::kTileBytes, &tmV, &v_full[st], D, j * kBlockN, bh);
+          mbar_arrive_expect_tx(&v_full[st], L::kUnitBytes);
+          load_cols(smem + L::kV + st * L::kUnitBytes, &tmV, &v_full[st], c0, min(D, c0 + kUC),
+                    (j / kUnits) * kBlockN, bh);
         }
       }
       for (int j = max(0, kt - kVStages); j < kt; ++j) mbar_wait_drain(&v_full[j % kVStages], (j / kVStages) & 1);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------ MMA issuer: S = Q K^T
-    // S of key tile kt goes to buffer kt % 3 once P V of tile kt - 3 (which
-    // used that buffer) has completed.
+    // S of key tile kt goes to buffer kt % kSBuf once P V of tile kt - kSBuf
+    // (which used that buffer) has completed; it accumulates over the tile's K
+    // units (ring position ku).
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_16(kBlockM, kBlockN, false, false, F16);
       bool ok = true;
-      int kt = 0, it = 0;
+      int kt = 0, it = 0, ku = 0;
       int rank, bh;
       for (int k = 0; ok; ++k) {
         const int step = sched_item(sched, blockIdx.x, k, rank, bh);
@@ -232,22 +247,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int qtile = qtile_of(rank);
         const int nk = ktiles(qtile);
         const int qb = it % kQBuf;
-        const uint32_t q_addr = smem_u32(smem + L::kQ + qb * L::kTileBytes);
+        const uint32_t q_addr = smem_u32(smem + L::kQ + qb * L::kQBytes);
         if (!mbar_wait(&q_full[qb], (it / kQBuf) & 1, &abort_flag)) { ok = false; break; }
         for (int j = 0; j < nk; ++j, ++kt) {
-          const int st = kt % kStages, sb = kt % kSBuf;
+          const int sb = kt % kSBuf;
           if (kt >= kSBuf && !mbar_wait(&pv_done[sb], ((kt / kSBuf) - 1) & 1, &abort_flag)) { ok = false; break; }
-          if (!mbar_wait(&k_full[st], (kt / kStages) & 1, &abort_flag)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t k_addr = smem_u32(smem + L::kK + st * L::kTileBytes);
+          for (int u = 0; u < kUnits; ++u, ++ku) {
+            const int st = ku % kStages;
+            if (!mbar_wait(&k_full[st], (ku / kStages) & 1, &abort_flag)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t k_addr = smem_u32(smem + L::kK + st * L::kUnitBytes);
+            const uint32_t qu_addr = q_addr + u * (kUC / 64) * L::kSubBytes;
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk / 4) * L::kSubBytes + (kk % 4) * 32;
-            mma_ss(tmem + sb * 128, sdesc_sw128(q_addr + off, 16, 1024), sdesc_sw128(k_addr + off, 16, 1024),
-                   idesc_s, kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < L::kSK; ++kk) {
+              const uint32_t off = (kk / 4) * L::kSubBytes + (kk % 4) * 32;
+              mma_ss(tmem + sb * 128, sdesc_sw128(qu_addr + off, 16, 1024), sdesc_sw128(k_addr + off, 16, 1024),
+                     idesc_s, (u > 0 || kk > 0) ? 1u : 0u);
+            }
+            mma_commit(&k_empty[st]);
           }
+          if (!ok) break;
           mma_commit(&s_full[sb]);
-          mma_commit(&k_empty[st]);
         }
         mma_commit(&q_empty[qb]);  // this Q buffer is free once the item's S MMAs are done
         ++it;
@@ -263,9 +283,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // an item overwrites O: its P is only marked ready after the softmax warps
     // have read the previous item's O out of TMEM.
     if (lane == 0) {
-      constexpr uint32_t idesc_o = idesc_16(kBlockM, D, false, true, F16);
+      constexpr uint32_t idesc_o = idesc_16(kBlockM, L::kPVN, false, true, F16);
       bool ok = true;
-      int kt = 0;
+      int kt = 0, vu = 0;
       int rank, bh;
       for (int k = 0; ok; ++k) {
         const int step = sched_item(sched, blockIdx.x, k, rank, bh);
@@ -274,16 +294,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int qtile = qtile_of(rank);
         const int nk = ktiles(qtile);
         for (int j = 0; j < nk; ++j, ++kt) {
-          const int st = kt % kVStages, sb = kt % kSBuf;
+          const int sb = kt % kSBuf;
           if (!mbar_wait(&p_ready[sb], (kt / kSBuf) & 1, &abort_flag)) { ok = false; break; }
-          if (!mbar_wait(&v_full[st], (kt / kVStages) & 1, &abort_flag)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t v_addr = smem_u32(smem + L::kV + st * L::kTileBytes);
+          for (int u = 0; u < kUnits; ++u, ++vu) {  // O columns [u kUC, (u+1) kUC) from V unit u
+            const int st = vu % kVStages;
+            if (!mbar_wait(&v_full[st], (vu / kVStages) & 1, &abort_flag)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t v_addr = smem_u32(smem + L::kV + st * L::kUnitBytes);
 #pragma unroll
-          for (int kk = 0; kk < kBlockN / 16; ++kk)
-            mma_ts(tmem_O, tmem + sb * 128 + kk * 8, sdesc_sw128(v_addr + kk * 2048, L::kSubBytes, 1024),
-                   idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(&v_empty[st]);
+            for (int kk = 0; kk < kBlockN / 16; ++kk)
+              mma_ts(tmem_O + u * kUC, tmem + sb * 128 + kk * 8,
+                     sdesc_sw128(v_addr + kk * 2048, L::kSubBytes, 1024), idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+            mma_commit(&v_empty[st]);
+          }
+          if (!ok) break;
           mma_commit(&pv_done[sb]);
         }
       }
@@ -472,10 +496,12 @@ cudaError_t launch_fwd_16(const CUtensorMap &tmQ, const CUtensorMap &tmK, const 
   if (f16) {
     if (d == 64) return launch<64, true>(tmQ, tmK, tmV, o, lse, B, H, N, Nk, scale, causal, status, num_sms, stream);
     if (d == 96) return launch<96, true>(tmQ, tmK, tmV, o, lse, B, H, N, Nk, scale, causal, status, num_sms, stream);
+    if (d == 256) return launch<256, true>(tmQ, tmK, tmV, o, lse, B, H, N, Nk, scale, causal, status, num_sms, stream);
     return launch<128, true>(tmQ, tmK, tmV, o, lse, B, H, N, Nk, scale, causal, status, num_sms, stream);
   }
   if (d == 64) return launch<64, false>(tmQ, tmK, tmV, o, lse, B, H, N, Nk, scale, causal, status, num_sms, stream);
   if (d == 96) return launch<96, false>(tmQ, tmK, tmV, o, lse, B, H, N, Nk, scale, causal, status, num_sms, stream);
+  if (d == 256) return launch<256, false>(tmQ, tmK, tmV, o, lse, B, H, N, Nk, scale, causal, status, num_sms, stream);
   return launch<128, false>(tmQ, tmK, tmV, o, lse, B, H, N, Nk, scale, causal, status, num_sms, stream);
 }
 

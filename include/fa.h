@@ -43,10 +43,13 @@
  *              fa_last_cuda_error). A kernel that gives up on an internal
  *              wait (it never traps) records FA_ERR_TIMEOUT in a device
  *              status word read by fa_device_status.
- *   Supported  bf16 and f16: d in {64, 96, 128}, N >= 1 (ragged tails are
- *              masked), every pointer 16-byte aligned.
+ *   Supported  bf16 and f16: d in {64, 96, 128} (the forward also takes
+ *              d = 256; the backward returns FA_ERR_UNSUPPORTED for it),
+ *              N >= 1 (ragged tails are masked), every pointer 16-byte
+ *              aligned.
  *              f32: 1 <= d <= 128, N >= 1, every pointer 4-byte aligned.
- *              B, H >= 1; B*H*N*d must be below 2^40 elements.
+ *              B, H >= 1; B*H*N*d must be below 2^40 elements; d above
+ *              256 (128 for f32) is FA_ERR_SHAPE.
  */
 #ifndef FA_H
 #define FA_H

@@ -83,8 +83,9 @@ def test_fwd_argument_errors(lib):
     assert _fwd(lib, N=0) == 2
     assert _fwd(lib, B=-1) == 2
     assert _fwd(lib, d=0) == 2
-    assert _fwd(lib, d=256) == 2
+    assert _fwd(lib, d=512) == 2
     assert _fwd(lib, d=80) == 3          # valid head size without a bf16 kernel
+    assert _fwd(lib, d=200) == 3
     assert _fwd(lib, B=300, H=300) == 3  # more than 65535 heads
     assert _fwd(lib, N=1 << 30, B=4, H=4, d=128) == 2  # 2^40 elements
     assert _fwd(lib, q=P + 8) == 4       # TMA needs 16-byte aligned bases
@@ -97,6 +98,8 @@ def test_bwd_argument_errors(lib):
     assert _bwd(lib, dk=None) == 1
     assert _bwd(lib, N=-3) == 2
     assert _bwd(lib, d=80) == 3
+    assert _bwd(lib, d=256) == 3  # the d = 256 kernel is forward only
+    assert _bwd(lib, d=512) == 2
     assert _bwd(lib, dv=P + 4) == 4
     assert _bwd(lib, ws=None) == 5
     need = fa.fa_bwd_workspace_size(1, 1, 128, 64, fa.FA_BF16)

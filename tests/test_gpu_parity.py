@@ -124,6 +124,40 @@ def test_bf16_B2_H4_N1000_d96(causal):
           _full_ref(_np(q), _np(k), _np(v), _np(dO), scale, causal))
 
 
+@pytest.mark.parametrize("N,causal", [(1, False), (300, False), (300, True), (700, True)])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+def test_fwd_d256(N, causal, dtype):
+    """Head size 256, forward only: K and V stream as two 128-column units
+    per key tile; the backward refuses d = 256."""
+    import exact_attention_97_gb300 as fa
+    q, k, v, dO = make_qkv_do(1, 3, N, 256, seed=256 + N, dtype=dtype)
+    scale = 1.0 / math.sqrt(256)
+    dev = torch.device("cuda")
+    qd, kd, vd = (x.to(dev) for x in (q, k, v))
+    o, lse = fa.attention_forward(qd, kd, vd, scale, causal)
+    torch.cuda.synchronize()
+    assert fa.fa_device_status() == 0
+    ro, rl = oracle.attention_fwd(_np(q), _np(k), _np(v), scale, causal)
+    check(f"fwd_d256_N{N}_c{int(causal)}_{str(dtype)[6:]}", "bf16",
+          {"o": o.float().cpu().double().numpy(), "lse": lse.cpu().double().numpy()}, {"o": ro, "lse": rl})
+    with pytest.raises(fa.FAError):
+        fa.attention_backward(qd, kd, vd, o, lse, dO.to(dev), scale, causal)
+
+
+def test_fwd_d256_kv():
+    import exact_attention_97_gb300 as fa
+    q, _, _, _ = make_qkv_do(2, 2, 130, 256, seed=7, dtype=torch.bfloat16)
+    _, k, v, _ = make_qkv_do(2, 2, 900, 256, seed=8, dtype=torch.bfloat16)
+    scale = 1.0 / math.sqrt(256)
+    dev = torch.device("cuda")
+    o, lse = fa.attention_forward(q.to(dev), k.to(dev), v.to(dev), scale, True)
+    torch.cuda.synchronize()
+    assert fa.fa_device_status() == 0
+    ro, rl = oracle.attention_fwd_kv(_np(q), _np(k), _np(v), scale, True)
+    check("fwd_d256_kv_Nq130_Nk900_c1", "bf16",
+          {"o": o.float().cpu().double().numpy(), "lse": lse.cpu().double().numpy()}, {"o": ro, "lse": rl})
+
+
 # ------------------------------------------------------------ f16 inputs (same kernels, f16 operands)
 
 @pytest.mark.parametrize("d", [64, 96, 128])
