@@ -56,7 +56,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
     os.makedirs(BUILD, exist_ok=True)
     cc = nvcc()
 
-    # tuning knobs (e.g. "-DFA_FWD_POLY_PAIRS=2") for sweeps; empty by default
+    # tuning knobs (e.g. "-DFA_FWD_QBUF=1") for sweeps; empty by default
     extra = os.environ.get("FA_NVCC_DEFINES", "").split()
 
     def compile_one(src):
