@@ -18,6 +18,10 @@ notes):
   * dQ and dK carry the factor ``scale`` (true derivatives; pinned by finite
     differences).
   * L is the natural-log log-sum-exp of the scaled scores.
+  * dropout (not on the pages beyond its probability and scope): Z is drawn
+    from Philox4x32-10, one byte per element, kept iff byte >= t with
+    t = round(256 p); kept probabilities are scaled by 256 / (256 - t); L is
+    the undropped log-sum-exp (see oracle.c for the counter layout).
 """
 from __future__ import annotations
 
@@ -63,6 +67,11 @@ def _load():
             lib.oracle_query_rows.argtypes = [P, P, P, P, i, i, dbl, i, P, i, P, P, P]
             lib.oracle_key_rows.argtypes = [P, P, P, P, i, i, dbl, i, P, i, P, P]
             lib.oracle_num_threads.restype = i
+            u32, u64 = ctypes.c_uint32, ctypes.c_uint64
+            lib.oracle_philox4x32_10.argtypes = [P, P, P]
+            lib.oracle_dropout_mask.argtypes = [u64, u32, i, ctypes.c_int64, i, i, P]
+            lib.oracle_fwd_dropout_kv.argtypes = [P, P, P, P, P, i, i, i, i, i, dbl, i, u64, u32, i]
+            lib.oracle_bwd_dropout_kv.argtypes = [P, P, P, P, P, P, P, i, i, i, i, i, dbl, i, u64, u32, i]
             _lib = lib
     return _lib
 
@@ -160,3 +169,53 @@ def key_rows(q, k, v, dO, keys, scale: float, causal: bool = False):
     _load().oracle_key_rows(_ptr(q), _ptr(k), _ptr(v), _ptr(dO), N, d, float(scale),
                             int(bool(causal)), _ptr(keys), n, _ptr(dk), _ptr(dv))
     return dk, dv
+
+
+# ------------------------------------------------------------------ dropout
+
+def dropout_threshold(p: float) -> int:
+    """t = round(256 p), the byte threshold for dropout probability p in [0, 1)."""
+    if not 0.0 <= p < 1.0:
+        raise ValueError("dropout probability must be in [0, 1)")
+    return min(255, int(round(256.0 * p)))
+
+
+def philox4x32_10(counter, key):
+    """The four 32-bit output words of Philox4x32-10 for a 4-word counter and a
+    2-word key."""
+    c = np.ascontiguousarray(np.asarray(counter, dtype=np.uint32))
+    k = np.ascontiguousarray(np.asarray(key, dtype=np.uint32))
+    out = np.empty(4, dtype=np.uint32)
+    _load().oracle_philox4x32_10(_ptr(c), _ptr(k), _ptr(out))
+    return out
+
+
+def dropout_mask(seed: int, offset: int, t: int, head: int, Nq: int, Nk: int) -> np.ndarray:
+    """Keep mask [Nq, Nk] (1 = kept) of head index `head` (= b * H + h)."""
+    m = np.empty((Nq, Nk), dtype=np.uint8)
+    _load().oracle_dropout_mask(int(seed), int(offset), int(t), int(head), Nq, Nk, _ptr(m))
+    return m
+
+
+def attention_fwd_dropout_kv(q, k, v, scale: float, causal: bool, seed: int, offset: int, t: int):
+    """O and L of attention with dropout on P (byte threshold t); q [B,H,Nq,d], k, v [B,H,Nk,d]."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    o = np.empty_like(q)
+    lse = np.empty((B, H, Nq), dtype=np.float64)
+    _load().oracle_fwd_dropout_kv(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Nq, Nk, d,
+                                  float(scale), int(bool(causal)), int(seed), int(offset), int(t))
+    return o, lse
+
+
+def attention_bwd_dropout_kv(q, k, v, dO, scale: float, causal: bool, seed: int, offset: int, t: int):
+    """(dQ, dK, dV) of the dropout forward with the same seed, offset and t."""
+    q, k, v, dO = _f64(q), _f64(k), _f64(v), _f64(dO)
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    dq, dk, dv = np.empty_like(q), np.empty_like(k), np.empty_like(v)
+    _load().oracle_bwd_dropout_kv(_ptr(q), _ptr(k), _ptr(v), _ptr(dO), _ptr(dq), _ptr(dk), _ptr(dv),
+                                  B, H, Nq, Nk, d, float(scale), int(bool(causal)), int(seed), int(offset),
+                                  int(t))
+    return dq, dk, dv

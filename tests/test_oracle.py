@@ -487,3 +487,198 @@ def test_planted_mistakes_are_caught():
             subprocess.check_call(["gcc", "-O1", "-std=c11", "-fPIC", "-shared", "-fopenmp",
                                    path, "-o", so, "-lm"])
             assert not _pins_hold(_Lib(so)), name
+
+
+# ---------------------------------------------------------------- dropout
+
+def test_philox_known_answers():
+    """The oracle's Philox4x32-10 reproduces the generator's published
+    known-answer vectors (tests/golden/philox4x32_10_known_answers.json)."""
+    g = _golden("philox4x32_10_known_answers.json")
+    for vec in g["vectors"]:
+        ctr = [int(x, 16) for x in vec["counter"]]
+        key = [int(x, 16) for x in vec["key"]]
+        want = [int(x, 16) for x in vec["output"]]
+        assert list(oracle.philox4x32_10(ctr, key)) == want
+
+
+def _curand():
+    import ctypes
+    import ctypes.util
+    for name in ("libcurand.so", "libcurand.so.10", ctypes.util.find_library("curand"),
+                 "/usr/local/cuda/lib64/libcurand.so"):
+        if not name:
+            continue
+        try:
+            return ctypes.CDLL(name)
+        except OSError:
+            continue
+    return None
+
+
+def test_philox_matches_curand_host_generator():
+    """cuRAND's host-side Philox4_32_10 generator (legacy ordering) emits, for
+    seed s, the blocks f(counter = (0, 0, i, 0), key = (s_lo, s_hi)) for
+    i = 0, 1, ...; an implementation independent of the oracle's."""
+    import ctypes
+    lib = _curand()
+    if lib is None:
+        pytest.skip("no cuRAND library")
+    gen = ctypes.c_void_p()
+    if lib.curandCreateGeneratorHost(ctypes.byref(gen), 161) != 0:  # CURAND_RNG_PSEUDO_PHILOX4_32_10
+        pytest.skip("cuRAND host generator unavailable")
+    try:
+        assert lib.curandSetGeneratorOrdering(gen, 103) == 0  # CURAND_ORDERING_PSEUDO_LEGACY
+        for seed in (0, 1, 0x0123456789ABCDEF, 0xFFFFFFFF00000001):
+            assert lib.curandSetPseudoRandomGeneratorSeed(gen, ctypes.c_ulonglong(seed)) == 0
+            assert lib.curandSetGeneratorOffset(gen, ctypes.c_ulonglong(0)) == 0
+            buf = (ctypes.c_uint * 64)()
+            assert lib.curandGenerate(gen, buf, 64) == 0
+            key = [seed & 0xFFFFFFFF, seed >> 32]
+            for i in range(16):
+                assert list(buf[4 * i:4 * i + 4]) == list(oracle.philox4x32_10([0, 0, i, 0], key)), (seed, i)
+    finally:
+        lib.curandDestroyGenerator(gen)
+
+
+def test_dropout_mask_layout_and_rate():
+    """The mask is the documented byte of the documented Philox call, does not
+    depend on the problem's shape, and keeps about 1 - t/256 of the entries."""
+    seed, off, t = 0x9E3779B97F4A7C15, 7, 77
+    m = oracle.dropout_mask(seed, off, t, 5, 64, 96)
+    for (i, j) in [(0, 0), (1, 2), (3, 95), (17, 40), (63, 63)]:
+        w = oracle.philox4x32_10([j // 4, i // 4, 5, off], [seed & 0xFFFFFFFF, seed >> 32])
+        assert m[i, j] == int(((int(w[i % 4]) >> (8 * (j % 4))) & 0xFF) >= t)
+    assert np.array_equal(oracle.dropout_mask(seed, off, t, 5, 20, 30), m[:20, :30])
+    big = np.stack([oracle.dropout_mask(seed, off, t, h, 256, 256) for h in range(4)])
+    keep = 1.0 - t / 256.0
+    sigma = math.sqrt(keep * (1 - keep) / big.size)
+    assert abs(big.mean() - keep) < 5 * sigma
+    assert not np.array_equal(big[0], big[1])                                  # heads differ
+    assert not np.array_equal(oracle.dropout_mask(seed, off + 1, t, 5, 64, 96), m)  # offsets differ
+    assert oracle.dropout_mask(seed, off, 0, 5, 64, 96).all()                  # t = 0 keeps everything
+
+
+def test_dropout_with_zero_probability_is_plain_attention():
+    r = _rng(40)
+    q, dO = (r.standard_normal((1, 2, 9, 5)) for _ in range(2))
+    k, v = (r.standard_normal((1, 2, 13, 5)) for _ in range(2))
+    for causal in (False, True):
+        o, lse = oracle.attention_fwd_kv(q, k, v, 0.7, causal)
+        od, lsed = oracle.attention_fwd_dropout_kv(q, k, v, 0.7, causal, 11, 0, 0)
+        assert np.max(np.abs(od - o)) < 1e-14 and np.max(np.abs(lsed - lse)) == 0
+        g = oracle.attention_bwd_kv(q, k, v, dO, 0.7, causal)
+        gd = oracle.attention_bwd_dropout_kv(q, k, v, dO, 0.7, causal, 11, 0, 0)
+        for a, b in zip(g, gd):
+            assert np.max(np.abs(a - b)) < 1e-13
+
+
+def test_dropout_is_unbiased():
+    """E[O] over masks equals the undropped O: the kept entries are scaled by
+    256 / (256 - t). Mean over 2000 seeds, checked to 5 standard errors."""
+    r = _rng(41)
+    q, k, v = (r.standard_normal((1, 1, 3, 4)) for _ in range(3))
+    o, _ = oracle.attention_fwd(q, k, v, 0.9, False)
+    t = 64
+    samples = np.stack([oracle.attention_fwd_dropout_kv(q, k, v, 0.9, False, s, 3, t)[0] for s in range(2000)])
+    se = samples.std(axis=0) / math.sqrt(len(samples))
+    assert np.all(np.abs(samples.mean(axis=0) - o) < 5 * se + 1e-12)
+
+
+def test_dropout_backward_finite_differences():
+    """With the mask fixed by (seed, offset, t), the dropout forward is a smooth
+    function of Q, K, V; the oracle's dropout backward matches central
+    differences of sum(O * dO), dropped entries' -P*D terms included."""
+    r = _rng(42)
+    q, dO = (r.standard_normal((1, 1, 6, 3)) for _ in range(2))
+    k, v = (r.standard_normal((1, 1, 8, 3)) for _ in range(2))
+    h, args = 1e-6, (0.8, True, 1234, 5, 90)
+    assert oracle.dropout_mask(1234, 5, 90, 0, 6, 8).min() == 0  # some entries are dropped
+    grads = oracle.attention_bwd_dropout_kv(q, k, v, dO, *args)
+    for which, x in enumerate((q, k, v)):
+        for idx in np.ndindex(x.shape):
+            xs = [q.copy(), k.copy(), v.copy()]
+            xs[which][idx] += h
+            up = np.sum(oracle.attention_fwd_dropout_kv(*xs, *args)[0] * dO)
+            xs[which][idx] -= 2 * h
+            dn = np.sum(oracle.attention_fwd_dropout_kv(*xs, *args)[0] * dO)
+            assert abs((up - dn) / (2 * h) - grads[which][idx]) < 1e-6 * max(1.0, np.abs(grads[which]).max())
+
+
+DROPOUT_MUTATIONS = {
+    "Philox multiplier swapped": ("(uint64_t)0xD2511F53u * c[0]", "(uint64_t)0xCD9E8D57u * c[0]"),
+    "Philox key schedule dropped": ("    k[0] += 0x9E3779B9u;\n", ""),
+    "kept entries not rescaled": ("o[c] += p[j] * inv_keep * vj[c];", "o[c] += p[j] * vj[c];"),
+    "dropped entries lose -P D": ("const double dSij = p[j] * (dPij - Di);\n          const double pdij",
+                                  "const double dSij = z ? p[j] * (dPij - Di) : 0.0;\n          const double pdij"),
+    "dV with the undropped P": ("dvj[c] += pdij * doi[c];", "dvj[c] += p[j] * doi[c];"),
+    "dP mask not applied": ("const double dPij = z ? dot(doi, vh + (size_t)j * d, d) * inv_keep : 0.0;",
+                            "const double dPij = dot(doi, vh + (size_t)j * d, d) * inv_keep;"),
+}
+
+
+def _dropout_pins_hold(so):
+    """The dropout pins above, run against a (possibly mutated) oracle build."""
+    import ctypes
+    P, i, dbl, u32, u64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_double, ctypes.c_uint32, ctypes.c_uint64
+    lib = ctypes.CDLL(so)
+    lib.oracle_philox4x32_10.argtypes = [P, P, P]
+    lib.oracle_fwd_dropout_kv.argtypes = [P, P, P, P, P, i, i, i, i, i, dbl, i, u64, u32, i]
+    lib.oracle_bwd_dropout_kv.argtypes = [P, P, P, P, P, P, P, i, i, i, i, i, dbl, i, u64, u32, i]
+
+    def fwd(q, k, v, scale, causal, seed, off, t):
+        o = np.empty_like(q); lse = np.empty(q.shape[:3])
+        lib.oracle_fwd_dropout_kv(*(x.ctypes.data_as(P) for x in (q, k, v, o, lse)), *q.shape[:3], k.shape[2],
+                                  q.shape[3], scale, int(causal), seed, off, t)
+        return o
+
+    def bwd(q, k, v, dO, scale, causal, seed, off, t):
+        g = [np.empty_like(q), np.empty_like(k), np.empty_like(v)]
+        lib.oracle_bwd_dropout_kv(*(x.ctypes.data_as(P) for x in (q, k, v, dO, *g)), *q.shape[:3], k.shape[2],
+                                  q.shape[3], scale, int(causal), seed, off, t)
+        return g
+
+    for vec in _golden("philox4x32_10_known_answers.json")["vectors"]:
+        c = np.array([int(x, 16) for x in vec["counter"]], dtype=np.uint32)
+        kk = np.array([int(x, 16) for x in vec["key"]], dtype=np.uint32)
+        out = np.empty(4, dtype=np.uint32)
+        lib.oracle_philox4x32_10(c.ctypes.data_as(P), kk.ctypes.data_as(P), out.ctypes.data_as(P))
+        if list(out) != [int(x, 16) for x in vec["output"]]:
+            return False
+    r = _rng(41)
+    q, k, v = (r.standard_normal((1, 1, 3, 4)) for _ in range(3))
+    o, _ = oracle.attention_fwd(q, k, v, 0.9, False)
+    samples = np.stack([fwd(q, k, v, 0.9, False, s, 3, 64) for s in range(2000)])
+    if not np.all(np.abs(samples.mean(axis=0) - o) < 5 * samples.std(axis=0) / math.sqrt(2000) + 1e-12):
+        return False
+    r = _rng(42)
+    q, dO = (r.standard_normal((1, 1, 6, 3)) for _ in range(2))
+    k, v = (r.standard_normal((1, 1, 8, 3)) for _ in range(2))
+    h, args = 1e-6, (0.8, True, 1234, 5, 90)
+    grads = bwd(q, k, v, dO, *args)
+    for which, x in enumerate((q, k, v)):
+        for idx in np.ndindex(x.shape):
+            xs = [q.copy(), k.copy(), v.copy()]
+            xs[which][idx] += h
+            up = np.sum(fwd(*xs, *args) * dO)
+            xs[which][idx] -= 2 * h
+            dn = np.sum(fwd(*xs, *args) * dO)
+            if abs((up - dn) / (2 * h) - grads[which][idx]) > 1e-6 * max(1.0, np.abs(grads[which]).max()):
+                return False
+    return True
+
+
+@pytest.mark.skipif(shutil.which("gcc") is None, reason="needs gcc")
+def test_planted_dropout_mistakes_are_caught():
+    src = open(os.path.join(os.path.dirname(oracle.__file__), "oracle.c")).read()
+    assert _dropout_pins_hold(oracle.build())
+    with tempfile.TemporaryDirectory() as tmp:
+        for n, (name, (old, new)) in enumerate(DROPOUT_MUTATIONS.items()):
+            assert src.count(old) == 1, name
+            path = os.path.join(tmp, f"dmutant{n}.c")
+            with open(path, "w") as f:
+                f.write(src.replace(old, new))
+            so = path[:-2] + ".so"
+            subprocess.check_call(["gcc", "-O1", "-std=c11", "-fPIC", "-shared", "-fopenmp",
+                                   path, "-o", so, "-lm"])
+            assert not _dropout_pins_hold(so), name
