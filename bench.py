@@ -209,6 +209,7 @@ def run_ours(args, w):
     ws = torch.empty(need, device=dev, dtype=torch.uint8)
     stream = torch.cuda.current_stream()
 
+    drop = {"dropout_p": args.dropout, "seed": 1234, "offset": 0} if args.dropout else {}
     launches = [0]
     marks = []  # (fwd start, bwd start, bwd end) events per timed step, on the launch stream
 
@@ -216,12 +217,12 @@ def run_ours(args, w):
         if mark:
             m = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
             m[0].record(stream)
-        fa.attention_forward(q, k, v, w.scale, w.causal, out=o, lse=lse)
+        fa.attention_forward(q, k, v, w.scale, w.causal, out=o, lse=lse, **drop)
         n = fa.fa_last_launch_count()
         if mark:
             m[1].record(stream)
         if not args.fwd_only:
-            fa.attention_backward(q, k, v, o, lse, dO, w.scale, w.causal, workspace=ws, grads=(dq, dk, dv))
+            fa.attention_backward(q, k, v, o, lse, dO, w.scale, w.causal, workspace=ws, grads=(dq, dk, dv), **drop)
         if mark:
             m[2].record(stream)
             marks.append(m)
@@ -314,9 +315,9 @@ def run_ours(args, w):
 
         def e2e_step():
             qd, kd, vd, dod = (t.to(dev, non_blocking=True) for t in (q_h, k_h, v_h, do_h))
-            od, ld = fa.attention_forward(qd, kd, vd, w.scale, w.causal)
+            od, ld = fa.attention_forward(qd, kd, vd, w.scale, w.causal, **drop)
             g = () if args.fwd_only else fa.attention_backward(qd, kd, vd, od, ld, dod, w.scale, w.causal,
-                                                               workspace=ws)
+                                                               workspace=ws, **drop)
             for dst, src in zip(out_h, (od, *g)):
                 dst.copy_(src, non_blocking=True)
 
@@ -345,7 +346,7 @@ def run_ours(args, w):
                "ms_per_step": ems / e2e_steps}
 
     base = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.fwd_only:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.fwd_only and not args.dropout:
         base = cpu_baseline(w, args.cpu_heads)
 
     if rank == 0:
@@ -354,7 +355,7 @@ def run_ours(args, w):
             "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
             "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "Nk": w.n_keys, "d": w.d,
-                       "causal": w.causal,
+                       "causal": w.causal, "dropout": args.dropout,
                        "inputs": "i.i.d. N(0,1), seeds Q=0 K=1 V=2 dO=3",
                        "l2": "inputs larger than L2 (each of Q, K, V, dO is "
                              f"{q.numel() * 2 / 1e6:.0f} MB vs 129 MB L2)",
@@ -388,6 +389,8 @@ def main():
     ap.add_argument("--dtype", choices=["bf16", "f16"], default="bf16", help="16-bit input type for --shape")
     ap.add_argument("--fwd-only", action="store_true",
                     help="time the forward alone (head sizes with no backward kernel, e.g. d = 256)")
+    ap.add_argument("--dropout", type=float, default=0.0,
+                    help="dropout probability on the attention probabilities (Philox mask, seed 1234)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-heads", type=int, default=8, help="heads in the CPU-baseline sample")

@@ -15,13 +15,13 @@ from __future__ import annotations
 
 import math
 
-from ._lib import (FA_BF16, FA_F16, FA_F32, FAError, fa_bwd, fa_bwd_f16, fa_bwd_f32, fa_bwd_kv,
-                   fa_bwd_workspace_size, fa_device_status, fa_fwd, fa_fwd_f16, fa_fwd_f32, fa_fwd_kv,
-                   fa_last_launch_count, fa_set_kernel_timing, fa_status_string, lib_path, load)
+from ._lib import (FA_BF16, FA_F16, FA_F32, FAError, fa_bwd, fa_bwd_dropout, fa_bwd_f16, fa_bwd_f32, fa_bwd_kv,
+                   fa_bwd_workspace_size, fa_device_status, fa_fwd, fa_fwd_dropout, fa_fwd_f16, fa_fwd_f32,
+                   fa_fwd_kv, fa_last_launch_count, fa_set_kernel_timing, fa_status_string, lib_path, load)
 
 __all__ = [
     "FA_BF16", "FA_F16", "FA_F32", "FAError", "fa_fwd", "fa_bwd", "fa_fwd_f16", "fa_bwd_f16",
-    "fa_fwd_f32", "fa_bwd_f32", "fa_fwd_kv", "fa_bwd_kv",
+    "fa_fwd_f32", "fa_bwd_f32", "fa_fwd_kv", "fa_bwd_kv", "fa_fwd_dropout", "fa_bwd_dropout",
     "fa_bwd_workspace_size", "fa_status_string", "fa_device_status", "fa_last_launch_count",
     "fa_set_kernel_timing",
     "attention_forward", "attention_backward", "lib_path", "load",
@@ -50,12 +50,16 @@ def _stream_handle(stream):
     return s.cuda_stream
 
 
-def attention_forward(q, k, v, scale=None, causal=False, out=None, lse=None, stream=None):
+def attention_forward(q, k, v, scale=None, causal=False, out=None, lse=None, stream=None,
+                      dropout_p=0.0, seed=0, offset=0):
     """(O, L) for CUDA tensors q [B, H, Nq, d] and k, v [B, H, Nk, d] (all bf16, all f16 or all float32).
 
     bf16 and f16 need d in {64, 96, 128} (or 256 for the forward); float32 takes 1 <= d <= 128 and Nk == Nq. L is
     float32 [B, H, Nq], the natural-log log-sum-exp of the scaled scores. With Nk != Nq
     the causal mask is aligned bottom-right (query i sees keys j <= i + Nk - Nq).
+    dropout_p > 0 (bf16 / f16 only) drops attention probabilities with the
+    Philox mask of fa_fwd_dropout, keyed by (seed, offset); pass the same
+    three values to attention_backward.
     """
     torch = _torch()
     B, H, N, d = q.shape
@@ -73,7 +77,13 @@ def attention_forward(q, k, v, scale=None, causal=False, out=None, lse=None, str
         _check("out", o, (B, H, N, d), dt)
         _check("lse", lse, (B, H, N), torch.float32)
         ptrs = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr())
-        if Nk != N:
+        if dropout_p:
+            if dt == torch.float32:
+                raise ValueError("dropout needs bfloat16 or float16 inputs")
+            fa_fwd_dropout(*ptrs, B, H, N, Nk, d, scale, int(bool(causal)),
+                           FA_F16 if dt == torch.float16 else FA_BF16, dropout_p, seed, offset,
+                           _stream_handle(stream))
+        elif Nk != N:
             if dt == torch.float32:
                 raise ValueError("float32 needs k and v with as many rows as q")
             fa_fwd_kv(*ptrs, B, H, N, Nk, d, scale, int(bool(causal)),
@@ -85,8 +95,9 @@ def attention_forward(q, k, v, scale=None, causal=False, out=None, lse=None, str
 
 
 def attention_backward(q, k, v, o, lse, dO, scale=None, causal=False, workspace=None, stream=None,
-                       grads=None):
-    """(dQ, dK, dV) for upstream gradient dO, given the forward's O and L."""
+                       grads=None, dropout_p=0.0, seed=0, offset=0):
+    """(dQ, dK, dV) for upstream gradient dO, given the forward's O and L (and
+    the forward's dropout_p, seed and offset)."""
     torch = _torch()
     B, H, N, d = q.shape
     Nk = k.shape[2]
@@ -109,7 +120,11 @@ def attention_backward(q, k, v, o, lse, dO, scale=None, causal=False, workspace=
         ptrs = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), dO.data_ptr(),
                 dq.data_ptr(), dk.data_ptr(), dv.data_ptr())
         ws = (workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream_handle(stream))
-        if Nk != N:
+        if dropout_p:
+            if kind == FA_F32:
+                raise ValueError("dropout needs bfloat16 or float16 inputs")
+            fa_bwd_dropout(*ptrs, B, H, N, Nk, d, scale, int(bool(causal)), kind, dropout_p, seed, offset, *ws)
+        elif Nk != N:
             if kind == FA_F32:
                 raise ValueError("float32 needs k and v with as many rows as q")
             fa_bwd_kv(*ptrs, B, H, N, Nk, d, scale, int(bool(causal)), kind, *ws)

@@ -242,7 +242,7 @@ namespace {
 
 // Shared body of fa_fwd / fa_fwd_f16 / fa_fwd_kv: N query rows, Nk key rows.
 int fwd16(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int N, int Nk,
-          int d, float scale, int causal, fa_stream_t stream, bool f16) {
+          int d, float scale, int causal, fa_stream_t stream, bool f16, const Dropout *drop = nullptr) {
   if (!q || !k || !v || !o || !lse) return FA_ERR_NULL;
   int st = check_shape(B, H, N, d, 256);
   if (st == kOk) st = check_shape(B, H, Nk, d, 256);
@@ -261,7 +261,7 @@ int fwd16(const void *q, const void *k, const void *v, void *o, float *lse, int 
       (st = make_map(&tv, v, BH, Nk, d, f16)) != kOk)
     return st;
   int launches = 0;
-  cudaError_t e = launch_fwd_16(tq, tk, tv, o, lse, B, H, N, Nk, d, scale, causal ? 1 : 0, f16, dev->status,
+  cudaError_t e = launch_fwd_16(tq, tk, tv, o, lse, B, H, N, Nk, d, scale, causal ? 1 : 0, f16, drop, dev->status,
                                 dev->num_sms, reinterpret_cast<cudaStream_t>(stream), &launches);
   if (e != cudaSuccess) return record(e);
   t_last_launches = launches;
@@ -271,7 +271,7 @@ int fwd16(const void *q, const void *k, const void *v, void *o, float *lse, int 
 // Shared body of fa_bwd / fa_bwd_f16 / fa_bwd_kv: N query rows, Nk key rows.
 int bwd16(const void *q, const void *k, const void *v, const void *o, const float *lse, const void *dO,
           void *dq, void *dk, void *dv, int B, int H, int N, int Nk, int d, float scale, int causal,
-          void *workspace, size_t workspace_bytes, fa_stream_t stream, bool f16) {
+          void *workspace, size_t workspace_bytes, fa_stream_t stream, bool f16, const Dropout *drop = nullptr) {
   if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return FA_ERR_NULL;
   int st = check_shape(B, H, N, d, 256);
   if (st == kOk) st = check_shape(B, H, Nk, d, 256);
@@ -301,7 +301,7 @@ int bwd16(const void *q, const void *k, const void *v, const void *o, const floa
   int launches = 0;
   cudaError_t e = launch_bwd_16(tq, tk, tv, tdo, tdk, tdv, o, dO, lse, dq, dk, dv, reinterpret_cast<float *>(ws + w.lp),
                                 reinterpret_cast<float *>(ws + w.dp), B, H, N, Nk, d, scale, causal ? 1 : 0, f16,
-                                dev->status, dev->num_sms, reinterpret_cast<cudaStream_t>(stream), &launches);
+                                drop, dev->status, dev->num_sms, reinterpret_cast<cudaStream_t>(stream), &launches);
   if (e != cudaSuccess) return record(e);
   t_last_launches = launches;
   return FA_OK;
@@ -347,6 +347,41 @@ int fa_bwd_kv(const void *q, const void *k, const void *v, const void *o, const 
   if (dtype != FA_BF16 && dtype != FA_F16) return dtype == FA_F32 ? FA_ERR_UNSUPPORTED : FA_ERR_ARG;
   return bwd16(q, k, v, o, lse, dO, dq, dk, dv, B, H, Nq, Nk, d, scale, causal, workspace, workspace_bytes,
                stream, dtype == FA_F16);
+}
+
+// Dropout parameters: p in [0, 1) to a byte threshold t = round(256 p).
+static int make_dropout(float p, unsigned long long seed, unsigned int offset, Dropout *dr) {
+  if (!(p >= 0.f && p < 1.f)) return FA_ERR_ARG;
+  int t = static_cast<int>(lrint(256.0 * static_cast<double>(p)));
+  if (t > 255) t = 255;
+  dr->k0 = static_cast<uint32_t>(seed);
+  dr->k1 = static_cast<uint32_t>(seed >> 32);
+  dr->offset = offset;
+  dr->t = static_cast<uint32_t>(t);
+  dr->inv_keep = static_cast<float>(256.0 / (256.0 - t));
+  return FA_OK;
+}
+
+int fa_fwd_dropout(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int Nq,
+                   int Nk, int d, float scale, int causal, int dtype, float p_drop, unsigned long long seed,
+                   unsigned int offset, fa_stream_t stream) {
+  if (dtype != FA_BF16 && dtype != FA_F16) return dtype == FA_F32 ? FA_ERR_UNSUPPORTED : FA_ERR_ARG;
+  Dropout dr;
+  const int st = make_dropout(p_drop, seed, offset, &dr);
+  if (st != FA_OK) return st;
+  return fwd16(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, stream, dtype == FA_F16, &dr);
+}
+
+int fa_bwd_dropout(const void *q, const void *k, const void *v, const void *o, const float *lse, const void *dO,
+                   void *dq, void *dk, void *dv, int B, int H, int Nq, int Nk, int d, float scale, int causal,
+                   int dtype, float p_drop, unsigned long long seed, unsigned int offset, void *workspace,
+                   size_t workspace_bytes, fa_stream_t stream) {
+  if (dtype != FA_BF16 && dtype != FA_F16) return dtype == FA_F32 ? FA_ERR_UNSUPPORTED : FA_ERR_ARG;
+  Dropout dr;
+  const int st = make_dropout(p_drop, seed, offset, &dr);
+  if (st != FA_OK) return st;
+  return bwd16(q, k, v, o, lse, dO, dq, dk, dv, B, H, Nq, Nk, d, scale, causal, workspace, workspace_bytes,
+               stream, dtype == FA_F16, &dr);
 }
 
 int fa_fwd_f32(const float *q, const float *k, const float *v, float *o, float *lse, int B, int H,
@@ -465,7 +500,7 @@ extern "C" int fa_bwd_static_scratch(const void *q, const void *k, const void *v
   int launches = 0;
   cudaError_t e = launch_bwd_16(tq, tk, tv, tdo, tdk, tdv, o, dO, lse, dq, dk, dv, reinterpret_cast<float *>(ws + w.lp),
                                 reinterpret_cast<float *>(ws + w.dp), B, H, N, N, d, scale, causal ? 1 : 0, false,
-                                dev->status, dev->num_sms, reinterpret_cast<cudaStream_t>(stream), &launches);
+                                nullptr, dev->status, dev->num_sms, reinterpret_cast<cudaStream_t>(stream), &launches);
   if (e != cudaSuccess) return record(e);
   t_last_launches = launches;
   return FA_OK;

@@ -120,14 +120,14 @@ struct DkdvCfg {
   static constexpr uint32_t tS = 0, tDP = 128, tDV = 256, tDK = 256 + D;  // TMEM columns
 };
 
-template <int D, bool F16>
+template <int D, bool F16, bool DROP>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                     const __grid_constant__ CUtensorMap tmdK, const __grid_constant__ CUtensorMap tmdV,
                     const float *__restrict__ Lp, const float *__restrict__ Dp, int N, int Nk,
                     const __grid_constant__ TileSched sched, float scale, float scale_log2, int causal,
-                    int *status) {
+                    const Dropout drop, int *status) {
   using C = DkdvCfg<D>;
   using E = Elt<F16>;
   constexpr int NST = C::kStages;
@@ -343,6 +343,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int st = g % NST;
         const int q0 = (i_first + t) * kBlk + h * 64;  // first query of this warpgroup's columns
         const int qmin = (key >= Nk) ? (q0 + 64) : qmin0;
+        uint32_t keep[2];  // dropout: keep bits of this key for the 64 queries, drawn while S^T is in flight
+        if constexpr (DROP) dropout_col_bits<2>(drop, static_cast<uint32_t>(bh), key, q0, keep);
         if (!mbar_wait_warp(&qd_full[st], (g / NST) & 1, &abort_flag)) { ok = false; break; }
         const float2 *L2 = reinterpret_cast<const float2 *>(Lst[st] + h * 64);
         const float2 *D2 = reinterpret_cast<const float2 *>(Dst[st] + h * 64);
@@ -364,7 +366,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (q0 + 2 * u + 1 < qmin) p1 = 0.f;
             pk[u] = E::pack(p0, p1);
           }
-          tmem_st32(tmem + lane_addr + C::tS + h * 64, pk);
+          if constexpr (DROP) {  // dV takes P o Z / (1 - p); pk keeps P for dS
+            uint32_t pkd[32];
+#pragma unroll
+            for (int u = 0; u < 32; ++u) {
+              const uint32_t kb = keep[u >> 4] >> ((2 * u) & 31);
+              pkd[u] = E::pack((kb & 1u) ? E::lo(pk[u]) * drop.inv_keep : 0.f,
+                               (kb & 2u) ? E::hi(pk[u]) * drop.inv_keep : 0.f);
+            }
+            tmem_st32(tmem + lane_addr + C::tS + h * 64, pkd);
+          } else {
+            tmem_st32(tmem + lane_addr + C::tS + h * 64, pk);
+          }
         }
         tc_fence_before();
         mbar_arrive(&p_ready);
@@ -379,8 +392,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int u = 0; u < 32; ++u) {
             const float2 dd = D2[u];
-            const float d0 = E::lo(pk[u]) * (__uint_as_float(r[2 * u]) - dd.x);
-            const float d1 = E::hi(pk[u]) * (__uint_as_float(r[2 * u + 1]) - dd.y);
+            float dp0 = __uint_as_float(r[2 * u]), dp1 = __uint_as_float(r[2 * u + 1]);
+            if constexpr (DROP) {  // dP = (dO V^T) o Z / (1 - p)
+              const uint32_t kb = keep[u >> 4] >> ((2 * u) & 31);
+              dp0 = (kb & 1u) ? dp0 * drop.inv_keep : 0.f;
+              dp1 = (kb & 2u) ? dp1 * drop.inv_keep : 0.f;
+            }
+            const float d0 = E::lo(pk[u]) * (dp0 - dd.x);
+            const float d1 = E::hi(pk[u]) * (dp1 - dd.y);
             ds[u] = E::pack(d0, d1);
           }
           tmem_st32(tmem + lane_addr + C::tDP + h * 64, ds);
@@ -465,13 +484,13 @@ struct DqCfg {
   static constexpr uint32_t tS = 0, tDP = 256, tDQ = 384;  // S buffers at 0 and 128
 };
 
-template <int D, bool F16>
+template <int D, bool F16, bool DROP>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                   const float *__restrict__ Lp, const float *__restrict__ Dp,
                   uint16_t *__restrict__ dq, int N, int Nk, const __grid_constant__ TileSched sched, float scale,
-                  float scale_log2, int causal, int *status) {
+                  float scale_log2, int causal, const Dropout drop, int *status) {
   using C = DqCfg<D>;
   using E = Elt<F16>;
   constexpr int KS = C::kKStages, VS = C::kVStages;
@@ -700,6 +719,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < n_kb; ++j, ++g) {
         const uint32_t sb = C::tS + (g & 1) * 128 + h * 64;
         const int limit = kvis - (j * kBlk + h * 64);  // columns at or past limit are masked
+        uint32_t keep[2];  // dropout: keep bits of this row for the 64 keys, drawn while S is in flight
+        if constexpr (DROP) dropout_row_bits<2>(drop, static_cast<uint32_t>(bh), q, j * kBlk + h * 64, keep);
         if (!mbar_wait_warp(&s_full[g & 1], (g >> 1) & 1, &abort_flag)) { ok = false; break; }
         tc_fence_after();
         float p[64];
@@ -728,8 +749,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t ds[32];
 #pragma unroll
           for (int u = 0; u < 32; ++u) {
-            const float d0 = p[2 * u] * (__uint_as_float(rr[2 * u]) - drow);
-            const float d1 = p[2 * u + 1] * (__uint_as_float(rr[2 * u + 1]) - drow);
+            float dp0 = __uint_as_float(rr[2 * u]), dp1 = __uint_as_float(rr[2 * u + 1]);
+            if constexpr (DROP) {  // dP = (dO V^T) o Z / (1 - p)
+              const uint32_t kb = keep[u >> 4] >> ((2 * u) & 31);
+              dp0 = (kb & 1u) ? dp0 * drop.inv_keep : 0.f;
+              dp1 = (kb & 2u) ? dp1 * drop.inv_keep : 0.f;
+            }
+            const float d0 = p[2 * u] * (dp0 - drow);
+            const float d1 = p[2 * u + 1] * (dp1 - drow);
             ds[u] = E::pack(d0, d1);
           }
           tmem_st32(tmem + lane_addr + sb, ds);  // over scores already read
@@ -772,12 +799,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0 && abort_flag) atomicExch(status, kErrTimeout);
 }
 
-template <int D, bool F16>
+template <int D, bool F16, bool DROP>
 cudaError_t launch(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtensorMap &tmV,
                    const CUtensorMap &tmdO, const CUtensorMap &tmdK, const CUtensorMap &tmdV, const void *o,
                    const void *dO, const float *lse, void *dq,
                    void *dk, void *dv, float *Lp, float *Dp, int B, int H, int N, int Nk, float scale,
-                   int causal, int *status, int num_sms, cudaStream_t stream) {
+                   int causal, const Dropout &drop, int *status, int num_sms, cudaStream_t stream) {
   const int n_tiles = (N + kBlk - 1) / kBlk;
   const int Np = n_tiles * kBlk;
   const float scale_log2 = scale * kLog2e;
@@ -803,8 +830,8 @@ cudaError_t launch(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtenso
     const int nkb = causal ? std::min(n_kb_all, (qt * kBlk + kBlk - 1 + off) / kBlk + 1) : n_kb_all;
     return static_cast<long long>(nkb) + 1;
   });
-  auto kdkdv = bwd_dkdv_kernel<D, F16>;
-  auto kdq = bwd_dq_kernel<D, F16>;
+  auto kdkdv = bwd_dkdv_kernel<D, F16, DROP>;
+  auto kdq = bwd_dq_kernel<D, F16, DROP>;
   if ((e = cudaFuncSetAttribute(kdkdv, cudaFuncAttributeMaxDynamicSharedMemorySize, DkdvCfg<D>::kAlloc)) !=
           cudaSuccess ||
       (e = cudaFuncSetAttribute(kdq, cudaFuncAttributeMaxDynamicSharedMemorySize, DqCfg<D>::kAlloc)) !=
@@ -812,29 +839,26 @@ cudaError_t launch(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtenso
     return e;
   timing_begin(stream);
   kdkdv<<<sched_kv.G, kThreads, DkdvCfg<D>::kAlloc, stream>>>(tmQ, tmK, tmV, tmdO, tmdK, tmdV, Lp, Dp, N, Nk,
-                                                               sched_kv, scale, scale_log2, causal, status);
+                                                               sched_kv, scale, scale_log2, causal, drop, status);
   timing_end(stream);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   timing_begin(stream);
   kdq<<<sched_q.G, kThreads, DqCfg<D>::kAlloc, stream>>>(tmQ, tmK, tmV, tmdO, Lp, Dp,
                                                           static_cast<uint16_t *>(dq), N, Nk, sched_q, scale,
-                                                          scale_log2, causal, status);
+                                                          scale_log2, causal, drop, status);
   timing_end(stream);
   return cudaGetLastError();
 }
 
-}  // namespace
-
-cudaError_t launch_bwd_16(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtensorMap &tmV,
-                          const CUtensorMap &tmdO, const CUtensorMap &tmdK, const CUtensorMap &tmdV,
-                          const void *o, const void *dO, const float *lse,
-                          void *dq, void *dk, void *dv, float *Lp, float *Dp, int B, int H, int N, int Nk, int d,
-                          float scale, int causal, bool f16, int *status, int num_sms, cudaStream_t stream,
-                          int *launches) {
-  *launches += 3;
+template <bool DROP>
+cudaError_t dispatch(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtensorMap &tmV,
+                     const CUtensorMap &tmdO, const CUtensorMap &tmdK, const CUtensorMap &tmdV, const void *o,
+                     const void *dO, const float *lse, void *dq, void *dk, void *dv, float *Lp, float *Dp, int B,
+                     int H, int N, int Nk, int d, float scale, int causal, bool f16, const Dropout &drop,
+                     int *status, int num_sms, cudaStream_t stream) {
 #define FA_BWD_LAUNCH(DD, FF)                                                                                  \
-  return launch<DD, FF>(tmQ, tmK, tmV, tmdO, tmdK, tmdV, o, dO, lse, dq, dk, dv, Lp, Dp, B, H, N, Nk, scale, \
-                        causal, status, num_sms, stream)
+  return launch<DD, FF, DROP>(tmQ, tmK, tmV, tmdO, tmdK, tmdV, o, dO, lse, dq, dk, dv, Lp, Dp, B, H, N, Nk,  \
+                              scale, causal, drop, status, num_sms, stream)
   if (f16) {
     if (d == 64) FA_BWD_LAUNCH(64, true);
     if (d == 96) FA_BWD_LAUNCH(96, true);
@@ -844,6 +868,22 @@ cudaError_t launch_bwd_16(const CUtensorMap &tmQ, const CUtensorMap &tmK, const 
   if (d == 96) FA_BWD_LAUNCH(96, false);
   FA_BWD_LAUNCH(128, false);
 #undef FA_BWD_LAUNCH
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_16(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtensorMap &tmV,
+                          const CUtensorMap &tmdO, const CUtensorMap &tmdK, const CUtensorMap &tmdV,
+                          const void *o, const void *dO, const float *lse,
+                          void *dq, void *dk, void *dv, float *Lp, float *Dp, int B, int H, int N, int Nk, int d,
+                          float scale, int causal, bool f16, const Dropout *drop, int *status, int num_sms,
+                          cudaStream_t stream, int *launches) {
+  *launches += 3;
+  if (drop)
+    return dispatch<true>(tmQ, tmK, tmV, tmdO, tmdK, tmdV, o, dO, lse, dq, dk, dv, Lp, Dp, B, H, N, Nk, d, scale,
+                          causal, f16, *drop, status, num_sms, stream);
+  return dispatch<false>(tmQ, tmK, tmV, tmdO, tmdK, tmdV, o, dO, lse, dq, dk, dv, Lp, Dp, B, H, N, Nk, d, scale,
+                         causal, f16, Dropout{}, status, num_sms, stream);
 }
 
 }  // namespace fa

@@ -95,13 +95,13 @@ __device__ __forceinline__ void load_cols(uint8_t *dst, const CUtensorMap *map, 
   for (int x = c0; x < c1; x += 64) tma_load_3d(dst + ((x - c0) / 64) * (kBlockN * 128), map, bar, x, row, bh);
 }
 
-template <int D, bool F16>
+template <int D, bool F16, bool DROP>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ,
                     const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, uint16_t *__restrict__ o,
                     float *__restrict__ lse, int N, int Nk, const __grid_constant__ TileSched sched, float scale,
-                    float scale_log2, int causal, int *status) {
+                    float scale_log2, int causal, const Dropout drop, int *status) {
   using L = FwdSmem<D>;
   using E = Elt<F16>;
   extern __shared__ uint8_t smem_raw[];
@@ -332,6 +332,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       float m_used = -INFINITY, l_sum = 0.f;
       for (int j = 0; j < nk; ++j, ++kt) {
         const int sb = kt % kSBuf;
+        uint32_t keep[4];  // dropout: keep bits of this row's 128 keys, drawn while S is in flight
+        if constexpr (DROP) dropout_row_bits<4>(drop, static_cast<uint32_t>(bh), row, j * kBlockN, keep);
         if (!mbar_wait_warp(&s_full[sb], (kt / kSBuf) & 1, &abort_flag)) {
           ok = false;
           break;
@@ -408,6 +410,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           float p0, p1;
           f2_unpack(p2, p0, p1);
+          if constexpr (DROP) {  // l keeps the undropped sum; P V gets P o Z / (1 - p)
+            const uint32_t kb = keep[w >> 4] >> ((2 * w) & 31);
+            p0 = (kb & 1u) ? p0 * drop.inv_keep : 0.f;
+            p1 = (kb & 2u) ? p1 * drop.inv_keep : 0.f;
+          }
           pk[w] = E::pack(p0, p1);
         }
         tmem_st64(tmem + lane_addr + sb * 128, pk);
@@ -461,12 +468,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0 && abort_flag) atomicExch(status, kErrTimeout);
 }
 
-template <int D, bool F16>
+template <int D, bool F16, bool DROP>
 cudaError_t launch(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtensorMap &tmV, void *o,
-                   float *lse, int B, int H, int N, int Nk, float scale, int causal, int *status,
-                   int num_sms, cudaStream_t stream) {
+                   float *lse, int B, int H, int N, int Nk, float scale, int causal, const Dropout &drop,
+                   int *status, int num_sms, cudaStream_t stream) {
   using L = FwdSmem<D>;
-  auto kern = fwd_kernel<D, F16>;
+  auto kern = fwd_kernel<D, F16, DROP>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (e != cudaSuccess) return e;
   // persistent grid: at most one CTA per SM, each walking its static list of
@@ -482,27 +489,42 @@ cudaError_t launch(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtenso
   timing_begin(stream);
   kern<<<sched.G, kThreads, L::kAlloc, stream>>>(tmQ, tmK, tmV, static_cast<uint16_t *>(o), lse,
                                                   N, Nk, sched, scale, scale * 1.4426950408889634f, causal,
-                                                  status);
+                                                  drop, status);
   timing_end(stream);
   return cudaGetLastError();
+}
+
+template <bool DROP>
+cudaError_t dispatch(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtensorMap &tmV, void *o, float *lse,
+                     int B, int H, int N, int Nk, int d, float scale, int causal, bool f16, const Dropout &drop,
+                     int *status, int num_sms, cudaStream_t stream) {
+#define FA_FWD_LAUNCH(DD, FF) \
+  return launch<DD, FF, DROP>(tmQ, tmK, tmV, o, lse, B, H, N, Nk, scale, causal, drop, status, num_sms, stream)
+  if (f16) {
+    if (d == 64) FA_FWD_LAUNCH(64, true);
+    if (d == 96) FA_FWD_LAUNCH(96, true);
+    if (d == 256) FA_FWD_LAUNCH(256, true);
+    FA_FWD_LAUNCH(128, true);
+  }
+  if (d == 64) FA_FWD_LAUNCH(64, false);
+  if (d == 96) FA_FWD_LAUNCH(96, false);
+  if (d == 256) FA_FWD_LAUNCH(256, false);
+  FA_FWD_LAUNCH(128, false);
+#undef FA_FWD_LAUNCH
 }
 
 }  // namespace
 
 cudaError_t launch_fwd_16(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtensorMap &tmV,
                           void *o, float *lse, int B, int H, int N, int Nk, int d, float scale, int causal,
-                          bool f16, int *status, int num_sms, cudaStream_t stream, int *launches) {
+                          bool f16, const Dropout *drop, int *status, int num_sms, cudaStream_t stream,
+                          int *launches) {
   *launches += 1;
-  if (f16) {
-    if (d == 64) return launch<64, true>(tmQ, tmK, tmV, o, lse, B, H, N, Nk, scale, causal, status, num_sms, stream);
-    if (d == 96) return launch<96, true>(tmQ, tmK, tmV, o, lse, B, H, N, Nk, scale, causal, status, num_sms, stream);
-    if (d == 256) return launch<256, true>(tmQ, tmK, tmV, o, lse, B, H, N, Nk, scale, causal, status, num_sms, stream);
-    return launch<128, true>(tmQ, tmK, tmV, o, lse, B, H, N, Nk, scale, causal, status, num_sms, stream);
-  }
-  if (d == 64) return launch<64, false>(tmQ, tmK, tmV, o, lse, B, H, N, Nk, scale, causal, status, num_sms, stream);
-  if (d == 96) return launch<96, false>(tmQ, tmK, tmV, o, lse, B, H, N, Nk, scale, causal, status, num_sms, stream);
-  if (d == 256) return launch<256, false>(tmQ, tmK, tmV, o, lse, B, H, N, Nk, scale, causal, status, num_sms, stream);
-  return launch<128, false>(tmQ, tmK, tmV, o, lse, B, H, N, Nk, scale, causal, status, num_sms, stream);
+  if (drop)
+    return dispatch<true>(tmQ, tmK, tmV, o, lse, B, H, N, Nk, d, scale, causal, f16, *drop, status, num_sms,
+                          stream);
+  return dispatch<false>(tmQ, tmK, tmV, o, lse, B, H, N, Nk, d, scale, causal, f16, Dropout{}, status, num_sms,
+                         stream);
 }
 
 }  // namespace fa

@@ -7,6 +7,17 @@
 
 namespace fa {
 
+// Dropout on the attention probabilities: element (i, j) of head h is kept
+// iff byte j mod 4 of word i mod 4 of Philox4x32-10 with counter
+// (j/4, i/4, h, offset) and key (k0, k1) is >= t; kept probabilities are
+// scaled by inv_keep = 256 / (256 - t).
+struct Dropout {
+  uint32_t k0, k1;  // the 64-bit seed, low word first
+  uint32_t offset;
+  uint32_t t;       // byte threshold, 0..255
+  float inv_keep;
+};
+
 // Error codes shared with include/fa.h (kept numerically identical).
 enum : int {
   kOk = 0,
@@ -41,7 +52,8 @@ cudaError_t launch_bwd_f32(const float *q, const float *k, const float *v, const
 // 128-byte swizzle.
 cudaError_t launch_fwd_16(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtensorMap &tmV,
                           void *o, float *lse, int B, int H, int N, int Nk, int d, float scale, int causal,
-                          bool f16, int *status, int num_sms, cudaStream_t stream, int *launches);
+                          bool f16, const Dropout *drop, int *status, int num_sms, cudaStream_t stream,
+                          int *launches);
 
 // 16-bit tensor-core backward (three kernels: row terms, dK/dV pass, dQ
 // pass). Lp and Dp are [B*H][Np] fp32 with Np = 128*ceil(N/128), in the
@@ -51,7 +63,7 @@ cudaError_t launch_bwd_16(const CUtensorMap &tmQ, const CUtensorMap &tmK, const 
                           const CUtensorMap &tmdO, const CUtensorMap &tmdK, const CUtensorMap &tmdV,
                           const void *o, const void *dO, const float *lse,
                           void *dq, void *dk, void *dv, float *Lp, float *Dp, int B, int H, int N, int Nk, int d,
-                          float scale, int causal, bool f16, int *status, int num_sms, cudaStream_t stream,
-                          int *launches);
+                          float scale, int causal, bool f16, const Dropout *drop, int *status, int num_sms,
+                          cudaStream_t stream, int *launches);
 
 }  // namespace fa

@@ -12,6 +12,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include "kernels.h"
+
 #ifndef FA_WAIT_LIMIT_CYCLES
 #define FA_WAIT_LIMIT_CYCLES (4ll * 1000 * 1000 * 1000)  // ~2 s at 2 GHz
 #endif
@@ -408,6 +410,102 @@ struct Elt<true> {
   __device__ static __forceinline__ float lo(uint32_t v) { return f16_to_f32(v & 0xFFFFu); }
   __device__ static __forceinline__ float hi(uint32_t v) { return f16_to_f32(v >> 16); }
 };
+
+// ------------------------------------------------------------------ dropout
+
+// Philox4x32-10, the counter-based generator of Salmon, Moraes, Dror and
+// Shaw ("Parallel random numbers: as easy as 1, 2, 3", SC 2011): ten rounds,
+// each two 32 x 32 -> 64-bit products of counter words 0 and 2 with the
+// paper's multipliers, a swap-and-xor of the halves with the key, and a Weyl
+// increment of the key.
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    // one widening multiply per product gives both halves
+    const uint64_t p0 = static_cast<uint64_t>(0xD2511F53u) * c.x;
+    const uint64_t p1 = static_cast<uint64_t>(0xCD9E8D57u) * c.z;
+    c = make_uint4(static_cast<uint32_t>(p1 >> 32) ^ c.y ^ k0, static_cast<uint32_t>(p1),
+                   static_cast<uint32_t>(p0 >> 32) ^ c.w ^ k1, static_cast<uint32_t>(p0));
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+  return c;
+}
+
+// Dropout on the attention probabilities (struct Dropout, kernels.h):
+// element (i, j) of head h (query i, key j) is kept iff byte j mod 4 of word
+// i mod 4 of philox4x32_10((j/4, i/4, h, offset), seed) is >= t.
+
+// Bits (>= t) of the four bytes of w, as a 4-bit value (byte b -> bit b).
+__device__ __forceinline__ uint32_t keep_nibble(uint32_t w, uint32_t t4) {
+  const uint32_t ge = __vcmpgeu4(w, t4);  // 0xFF in each byte that is >= t
+  return ((ge >> 7) & 1u) | ((ge >> 14) & 2u) | ((ge >> 21) & 4u) | ((ge >> 28) & 8u);
+}
+
+// The mask helpers below are warp-collective: the four lanes of a quad own
+// four consecutive rows (or keys) that share every Philox counter, so each
+// lane draws a quarter of the calls and the quad swaps 4-bit keep nibbles by
+// shuffle.
+
+// Keep bits of query row i (i mod 4 == lane mod 4) for the 32 * NW keys
+// starting at j0 (a multiple of 4): bit b of bits[w] is key j0 + 32 w + b.
+template <int NW>
+__device__ __forceinline__ void dropout_row_bits(const Dropout &dr, uint32_t h, int i, int j0, uint32_t (&bits)[NW]) {
+  const uint32_t t4 = dr.t * 0x01010101u;
+  const int lane = threadIdx.x & 31, quad = lane & ~3, me = lane & 3;
+#pragma unroll(NW > 2 ? 1 : NW)  // the four-word (forward) case stays rolled: its body is long
+  for (int w = 0; w < NW; ++w) {
+    uint32_t m = 0;
+#pragma unroll
+    for (int blk = 0; blk < 2; ++blk) {  // 16 keys: 4 calls, one per lane of the quad
+      const uint4 r = philox4x32_10(make_uint4(static_cast<uint32_t>(j0 / 4 + 8 * w + 4 * blk + me),
+                                               static_cast<uint32_t>(i / 4), h, dr.offset),
+                                    dr.k0, dr.k1);
+      // nibble r of `packed`: keep bits of row 4 (i/4) + r for this lane's 4 keys
+      const uint32_t packed = keep_nibble(r.x, t4) | (keep_nibble(r.y, t4) << 4) | (keep_nibble(r.z, t4) << 8) |
+                              (keep_nibble(r.w, t4) << 12);
+#pragma unroll
+      for (int src = 0; src < 4; ++src) {
+        const uint32_t v = __shfl_sync(0xffffffffu, packed, quad | src);
+        m |= ((v >> (4 * me)) & 0xFu) << (4 * (4 * blk + src));
+      }
+    }
+    bits[w] = m;
+  }
+}
+
+// Keep bits of key j (j mod 4 == lane mod 4) for the 32 * NW query rows
+// starting at i0 (a multiple of 4): bit b of bits[w] is row i0 + 32 w + b.
+template <int NW>
+__device__ __forceinline__ void dropout_col_bits(const Dropout &dr, uint32_t h, int j, int i0, uint32_t (&bits)[NW]) {
+  const uint32_t t4 = dr.t * 0x01010101u;
+  const int lane = threadIdx.x & 31, quad = lane & ~3, me = lane & 3;
+#pragma unroll(NW > 2 ? 1 : NW)  // the four-word (forward) case stays rolled: its body is long
+  for (int w = 0; w < NW; ++w) {
+    uint32_t m = 0;
+#pragma unroll
+    for (int blk = 0; blk < 2; ++blk) {  // 16 rows: 4 calls, one per lane of the quad
+      const uint4 r = philox4x32_10(make_uint4(static_cast<uint32_t>(j / 4),
+                                               static_cast<uint32_t>(i0 / 4 + 8 * w + 4 * blk + me), h, dr.offset),
+                                    dr.k0, dr.k1);
+      // nibble b of `packed`: keep bits of this call's 4 rows for key 4 (j/4) + b
+      const uint32_t g0 = __vcmpgeu4(r.x, t4), g1 = __vcmpgeu4(r.y, t4), g2 = __vcmpgeu4(r.z, t4),
+                     g3 = __vcmpgeu4(r.w, t4);
+      uint32_t packed = 0;
+#pragma unroll
+      for (int b = 0; b < 4; ++b)
+        packed |= (((g0 >> (8 * b + 7)) & 1u) | (((g1 >> (8 * b + 7)) & 1u) << 1) |
+                   (((g2 >> (8 * b + 7)) & 1u) << 2) | (((g3 >> (8 * b + 7)) & 1u) << 3))
+                  << (4 * b);
+#pragma unroll
+      for (int src = 0; src < 4; ++src) {
+        const uint32_t v = __shfl_sync(0xffffffffu, packed, quad | src);
+        m |= ((v >> (4 * me)) & 0xFu) << (4 * (4 * blk + src));
+      }
+    }
+    bits[w] = m;
+  }
+}
 
 __device__ __forceinline__ int warp_id() { return threadIdx.x >> 5; }
 __device__ __forceinline__ int lane_id() { return threadIdx.x & 31; }

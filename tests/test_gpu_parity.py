@@ -158,6 +158,132 @@ def test_fwd_d256_kv():
           {"o": o.float().cpu().double().numpy(), "lse": lse.cpu().double().numpy()}, {"o": ro, "lse": rl})
 
 
+# ------------------------------------------------------------ dropout
+
+def _drop_ref(q, k, v, dO, scale, causal, seed, offset, p):
+    t = oracle.dropout_threshold(p)
+    o, lse = oracle.attention_fwd_dropout_kv(_np(q), _np(k), _np(v), scale, causal, seed, offset, t)
+    ref = {"o": o, "lse": lse}
+    if dO is not None:
+        dq, dk, dv = oracle.attention_bwd_dropout_kv(_np(q), _np(k), _np(v), _np(dO), scale, causal, seed, offset, t)
+        ref.update(dq=dq, dk=dk, dv=dv)
+    return ref
+
+
+def _run_drop(q, k, v, dO, scale, causal, seed, offset, p):
+    import exact_attention_97_gb300 as fa
+    dev = torch.device("cuda")
+    qd, kd, vd = (x.to(dev) for x in (q, k, v))
+    o, lse = fa.attention_forward(qd, kd, vd, scale, causal, dropout_p=p, seed=seed, offset=offset)
+    got = {"o": o, "lse": lse}
+    if dO is not None:
+        dq, dk, dv = fa.attention_backward(qd, kd, vd, o, lse, dO.to(dev), scale, causal, dropout_p=p, seed=seed,
+                                           offset=offset)
+        got.update(dq=dq, dk=dk, dv=dv)
+    torch.cuda.synchronize()
+    assert fa.fa_device_status() == 0
+    return {key: t.float().cpu().double().numpy() for key, t in got.items()}
+
+
+def _mask(seed, offset, p, B, H, Nq, Nk, causal):
+    t = oracle.dropout_threshold(p)
+    m = np.stack([oracle.dropout_mask(seed, offset, t, h, Nq, Nk) for h in range(B * H)]).reshape(B, H, Nq, Nk)
+    if causal:
+        i = np.arange(Nq)[:, None]
+        j = np.arange(Nk)[None, :]
+        m = m * (j <= i + (Nk - Nq))
+    return m.astype(bool)
+
+
+@pytest.mark.parametrize("d,Nq,Nk,causal", [(128, 300, 128, False), (128, 100, 128, True), (256, 200, 256, False),
+                                            (256, 130, 256, True)])
+def test_dropout_forward_mask_is_exact(d, Nq, Nk, causal):
+    """With V the identity (value j = unit vector j, Nk <= d), O[i, j] is the
+    kept-and-scaled probability P[i, j] Z[i, j] / (1 - p): its zero pattern is
+    the mask, which must equal the oracle's bit for bit."""
+    seed, offset, p = 0x5EED5EED1234, 3, 0.3
+    q, k, _, _ = make_qkv_do(1, 3, Nq, d, seed=7, dtype=torch.float32)
+    _, k, _, _ = make_qkv_do(1, 3, Nk, d, seed=8, dtype=torch.float32)
+    q, k = (0.2 * q).to(torch.bfloat16), (0.2 * k).to(torch.bfloat16)  # scores near 0: no P underflows
+    v = torch.zeros(1, 3, Nk, d)
+    v[:, :, torch.arange(Nk), torch.arange(Nk)] = 1.0
+    v = v.to(torch.bfloat16)
+    got = _run_drop(q, k, v, None, 1.0 / math.sqrt(d), causal, seed, offset, p)
+    want = _mask(seed, offset, p, 1, 3, Nq, Nk, causal)
+    assert np.array_equal(got["o"][..., :Nk] != 0, want)
+    check(f"dropout_fwd_identity_d{d}_Nq{Nq}_c{int(causal)}", "bf16", got,
+          _drop_ref(q, k, v, None, 1.0 / math.sqrt(d), causal, seed, offset, p))
+
+
+@pytest.mark.parametrize("Nk", [128, 300, 513])
+def test_dropout_dkdv_mask_is_exact(Nk):
+    """dV = (P o Z / (1 - p))^T dO with dO the identity (Nq = d = 128): the
+    zero pattern of dV^T is the mask, drawn in the dK/dV pass's key-owner
+    layout, across several key blocks."""
+    seed, offset, p = 77, 11, 0.25
+    q, _, _, _ = make_qkv_do(1, 2, 128, 128, seed=9, dtype=torch.float32)
+    _, k, v, _ = make_qkv_do(1, 2, Nk, 128, seed=10, dtype=torch.float32)
+    q, k, v = (0.2 * q).to(torch.bfloat16), (0.2 * k).to(torch.bfloat16), v.to(torch.bfloat16)
+    dO = torch.eye(128).expand(1, 2, 128, 128).contiguous().to(torch.bfloat16)
+    got = _run_drop(q, k, v, dO, 1.0 / math.sqrt(128), False, seed, offset, p)
+    want = _mask(seed, offset, p, 1, 2, 128, Nk, False)
+    assert np.array_equal(np.swapaxes(got["dv"], 2, 3)[..., :128, :] != 0, want)
+    check(f"dropout_dkdv_identity_Nk{Nk}", "bf16", got,
+          _drop_ref(q, k, v, dO, 1.0 / math.sqrt(128), False, seed, offset, p))
+
+
+def test_dropout_dq_mask_is_exact():
+    """With K the identity (Nk = d = 128), every value and every dO row equal
+    to unit vector 0: dP = dO V^T = 1, D_i = sum_j Pd_ij, and dQ[i, j] =
+    scale P_ij (Z_ij / (1 - p) - D_i), positive exactly where Z_ij = 1."""
+    seed, offset, p = 2024, 0, 0.3
+    q, _, _, _ = make_qkv_do(1, 2, 300, 128, seed=12, dtype=torch.float32)
+    q = (0.2 * q).to(torch.bfloat16)
+    k = torch.eye(128).expand(1, 2, 128, 128).contiguous().to(torch.bfloat16)
+    v = torch.zeros(1, 2, 128, 128)
+    v[..., 0] = 1.0
+    dO = torch.zeros(1, 2, 300, 128)
+    dO[..., 0] = 1.0
+    v, dO = v.to(torch.bfloat16), dO.to(torch.bfloat16)
+    got = _run_drop(q, k, v, dO, 1.0 / math.sqrt(128), False, seed, offset, p)
+    want = _mask(seed, offset, p, 1, 2, 300, 128, False)
+    assert np.array_equal(got["dq"] > 0, want)
+    check("dropout_dq_identity", "bf16", got, _drop_ref(q, k, v, dO, 1.0 / math.sqrt(128), False, seed, offset, p))
+
+
+@pytest.mark.parametrize("d", [64, 96, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("p", [0.1, 0.5])
+def test_dropout_parity(d, causal, p):
+    q, k, v, dO = make_qkv_do(1, 2, 300, d, seed=500 + d, dtype=torch.bfloat16)
+    scale = 1.0 / math.sqrt(d)
+    got = _run_drop(q, k, v, dO, scale, causal, 99, 5, p)
+    check(f"dropout_d{d}_c{int(causal)}_p{p}", "bf16", got, _drop_ref(q, k, v, dO, scale, causal, 99, 5, p))
+
+
+def test_dropout_kv_f16_and_d256():
+    q, _, _, dO = make_qkv_do(2, 2, 200, 128, seed=5, dtype=torch.float16)
+    _, k, v, _ = make_qkv_do(2, 2, 777, 128, seed=6, dtype=torch.float16)
+    scale = 1.0 / math.sqrt(128)
+    got = _run_drop(q, k, v, dO, scale, True, 123456789, 1, 0.2)
+    check("dropout_f16_kv_Nq200_Nk777", "bf16", got, _drop_ref(q, k, v, dO, scale, True, 123456789, 1, 0.2))
+    q, k, v, _ = make_qkv_do(1, 2, 333, 256, seed=7, dtype=torch.bfloat16)
+    got = _run_drop(q, k, v, None, 1.0 / 16, True, 42, 0, 0.2)
+    check("dropout_fwd_d256", "bf16", got, _drop_ref(q, k, v, None, 1.0 / 16, True, 42, 0, 0.2))
+
+
+def test_dropout_zero_is_the_plain_path():
+    import exact_attention_97_gb300 as fa
+    q, k, v, dO = (x.cuda() for x in make_qkv_do(1, 2, 260, 128, seed=8, dtype=torch.bfloat16))
+    o, lse = fa.attention_forward(q, k, v, None, True)
+    od, lsed = fa.attention_forward(q, k, v, None, True, dropout_p=0.0001, seed=3)  # t = round(0.0256) = 0
+    assert torch.equal(o, od) and torch.equal(lse, lsed)
+    g = fa.attention_backward(q, k, v, o, lse, dO, None, True)
+    gd = fa.attention_backward(q, k, v, o, lse, dO, None, True, dropout_p=0.0001, seed=3)
+    for a, b in zip(g, gd):
+        assert torch.equal(a, b)
+
+
 # ------------------------------------------------------------ f16 inputs (same kernels, f16 operands)
 
 @pytest.mark.parametrize("d", [64, 96, 128])
