@@ -50,7 +50,9 @@ namespace {
 
 constexpr int kBlockM = 128;   // query rows per tile (= TMEM lanes)
 constexpr int kBlockN = 128;   // keys per tile
-constexpr int kThreads = 256;  // 8 warps
+constexpr int kThreads = 256;      // 8 warps
+constexpr int kThreadsDrop = 384;  // 12 warps with dropout: warps 8-11 draw the keep masks
+constexpr int kMaskSlots = 3;      // keep-mask ring (128 rows x 128 keys of bits each)
 constexpr float kRescaleLog2 = 8.0f;  // move the running max only past 2^8
 constexpr float kLn2 = 0.69314718055994531f;
 
@@ -67,7 +69,7 @@ constexpr float kLn2 = 0.69314718055994531f;
 // ring and the V ring, under the 227 KB limit: at d = 96 and 128, 2 Q + 3 K +
 // 2 V tiles; at d = 256, 1 Q tile + 3 K + 2 V units. Tensor memory holds
 // kSBuf score buffers of 128 columns and O after them (512 columns).
-template <int D>
+template <int D, bool DROP = false>
 struct FwdSmem {
   static constexpr int kDP = (D + 63) / 64 * 64;
   static constexpr int kUnits = kDP > 128 ? kDP / 128 : 1;  // K / V ring units per key tile
@@ -77,14 +79,18 @@ struct FwdSmem {
   static constexpr int kSK = (kUnits == 1 ? D : kUnitCols) / 16;  // k-steps of S per unit
   static constexpr int kPVN = kUnits == 1 ? D : kUnitCols;         // N of one P V product
   static constexpr int kSBuf = kDP > 128 ? 2 : 3;
-  static constexpr int kQBuf = kDP > 128 ? 1 : FA_FWD_QBUF;
-  static constexpr int kKStages = 3;
-  static constexpr int kVStages = kDP > 128 ? 2 : ((kDP == 128 && kQBuf == 2) ? 2 : 3);
+  // with dropout the keep-mask ring needs 6 KB: one Q buffer, and at d = 256
+  // a K ring of two units
+  static constexpr int kQBuf = (kDP > 128 || DROP) ? 1 : FA_FWD_QBUF;
+  static constexpr int kKStages = (kDP > 128 && DROP) ? 2 : 3;
+  static constexpr int kVStages = kDP > 128 ? 2 : ((kDP == 128 && (kQBuf == 2 || DROP)) ? 2 : 3);
   static constexpr int kSubBytes = kBlockN * 128;  // one 128-row x 64-column sub-tile
   static constexpr int kQ = 0;
   static constexpr int kK = kQ + kQBuf * kQBytes;
   static constexpr int kV = kK + kKStages * kUnitBytes;
-  static constexpr int kBytes = kV + kVStages * kUnitBytes;
+  static constexpr int kMask = kV + kVStages * kUnitBytes;
+  static constexpr int kMaskBytes = DROP ? kMaskSlots * kBlockM * 16 : 0;
+  static constexpr int kBytes = kMask + kMaskBytes;
   static constexpr int kAlloc = kBytes + 1024;  // slack for 1024-byte alignment
 };
 
@@ -96,13 +102,13 @@ __device__ __forceinline__ void load_cols(uint8_t *dst, const CUtensorMap *map, 
 }
 
 template <int D, bool F16, bool DROP>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ,
                     const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, uint16_t *__restrict__ o,
                     float *__restrict__ lse, int N, int Nk, const __grid_constant__ TileSched sched, float scale,
                     float scale_log2, int causal, const Dropout drop, int *status) {
-  using L = FwdSmem<D>;
+  using L = FwdSmem<D, DROP>;
   using E = Elt<F16>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -110,7 +116,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int kQBuf = L::kQBuf, kStages = L::kKStages, kVStages = L::kVStages, kSBuf = L::kSBuf;
   constexpr int kUnits = L::kUnits, kUC = L::kUnitCols;
   __shared__ uint64_t q_full[kQBuf], q_empty[kQBuf], k_full[kStages], k_empty[kStages], v_full[kVStages],
-      v_empty[kVStages], s_full[kSBuf], p_ready[kSBuf], pv_done[kSBuf], drain_s, drain_pv;
+      v_empty[kVStages], s_full[kSBuf], p_ready[kSBuf], pv_done[kSBuf], drain_s, drain_pv,
+      mask_full[kMaskSlots], mask_empty[kMaskSlots];
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_flag;
 
@@ -148,6 +155,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(&drain_s, 1);
     mbar_init(&drain_pv, 1);
+    for (int b = 0; b < kMaskSlots; ++b) {
+      mbar_init(&mask_full[b], 4 * 32);
+      mbar_init(&mask_empty[b], 4 * 32);
+    }
     fence_mbar_init();
   }
   if (warp == 2) {
@@ -164,6 +175,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   // items (kt), so the K/V rings, the S buffers and their barrier phases run
   // on without a break from one item to the next; `it` counts items (phase of
   // q_full / q_empty).
+  // With dropout, 12 warps share 384 x 168 registers: each warpgroup resizes
+  // its share at the top of its branch (loaders and issuers 56, softmax 232,
+  // keep masks 96 per thread: 49152 of the 64512).
+  if (warp < 4) {
+  if constexpr (DROP) setmaxnreg_dec<56>();
   if (warp == 0) {
     // ------------------------------------------------------------ loader: Q, K
     // Q of item `it` goes into buffer it % kQBuf once every S MMA of the item
@@ -314,7 +330,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit(&drain_pv);
       mbar_wait_drain(&drain_pv, 0);
     }
-  } else if (warp >= 4) {
+  }
+  } else if (warp < 8) {
+    if constexpr (DROP) setmaxnreg_inc<232>();
     // ----------------------------------------------------------------- softmax
     const int wq = warp - 4;                 // TMEM lane quarter of this warp
     const int r_local = wq * 32 + lane;      // row within the tile
@@ -332,8 +350,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       float m_used = -INFINITY, l_sum = 0.f;
       for (int j = 0; j < nk; ++j, ++kt) {
         const int sb = kt % kSBuf;
-        uint32_t keep[4];  // dropout: keep bits of this row's 128 keys, drawn while S is in flight
-        if constexpr (DROP) dropout_row_bits<4>(drop, static_cast<uint32_t>(bh), row, j * kBlockN, keep);
+        uint32_t keep[4];  // dropout: keep bits of this row's 128 keys, from the mask warps
+        if constexpr (DROP) {
+          const int ms = kt % kMaskSlots;
+          if (!mbar_wait_warp(&mask_full[ms], (kt / kMaskSlots) & 1, &abort_flag)) {
+            ok = false;
+            break;
+          }
+          const uint4 mv = *reinterpret_cast<const uint4 *>(smem + L::kMask + (ms * kBlockM + r_local) * 16);
+          keep[0] = mv.x;
+          keep[1] = mv.y;
+          keep[2] = mv.z;
+          keep[3] = mv.w;
+          mbar_arrive(&mask_empty[ms]);
+        }
         if (!mbar_wait_warp(&s_full[sb], (kt / kSBuf) & 1, &abort_flag)) {
           ok = false;
           break;
@@ -457,6 +487,37 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (store) lse[static_cast<size_t>(bh) * N + row] = (m_used * scale_log2 + log2f(l_sum)) * kLn2;
     }
+  } else {
+    if constexpr (DROP) {
+      setmaxnreg_dec<96>();
+      // ---------------------------------------------------------- keep masks
+      // Row r_local of every key tile, one tile ahead of the softmax warps at
+      // most kMaskSlots: the bits of Philox4x32-10 bytes >= t, in the layout
+      // the softmax reads (bit b of word w = key 32 w + b of the tile).
+      const int r_local = (warp - 8) * 32 + lane;
+      bool ok = true;
+      int kt = 0, rank, bh;
+      for (int k = 0; ok; ++k) {
+        const int step = sched_item(sched, blockIdx.x, k, rank, bh);
+        if (step == kDone) break;
+        if (step == kSkip) continue;
+        const int qtile = qtile_of(rank);
+        const int nk = ktiles(qtile), row = qtile * kBlockM + r_local;
+        for (int j = 0; j < nk; ++j, ++kt) {
+          const int ms = kt % kMaskSlots;
+          if (kt >= kMaskSlots &&
+              !mbar_wait_warp(&mask_empty[ms], ((kt / kMaskSlots) & 1) ^ 1, &abort_flag)) {
+            ok = false;
+            break;
+          }
+          uint32_t bits[4];
+          dropout_row_bits<4>(drop, static_cast<uint32_t>(bh), row, j * kBlockN, bits);
+          *reinterpret_cast<uint4 *>(smem + L::kMask + (ms * kBlockM + r_local) * 16) =
+              make_uint4(bits[0], bits[1], bits[2], bits[3]);
+          mbar_arrive(&mask_full[ms]);
+        }
+      }
+    }
   }
 
   tc_fence_before();
@@ -472,7 +533,7 @@ template <int D, bool F16, bool DROP>
 cudaError_t launch(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtensorMap &tmV, void *o,
                    float *lse, int B, int H, int N, int Nk, float scale, int causal, const Dropout &drop,
                    int *status, int num_sms, cudaStream_t stream) {
-  using L = FwdSmem<D>;
+  using L = FwdSmem<D, DROP>;
   auto kern = fwd_kernel<D, F16, DROP>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (e != cudaSuccess) return e;
@@ -487,7 +548,7 @@ cudaError_t launch(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtenso
     return static_cast<long long>(nk) + 1;
   });
   timing_begin(stream);
-  kern<<<sched.G, kThreads, L::kAlloc, stream>>>(tmQ, tmK, tmV, static_cast<uint16_t *>(o), lse,
+  kern<<<sched.G, DROP ? kThreadsDrop : kThreads, L::kAlloc, stream>>>(tmQ, tmK, tmV, static_cast<uint16_t *>(o), lse,
                                                   N, Nk, sched, scale, scale * 1.4426950408889634f, causal,
                                                   drop, status);
   timing_end(stream);

@@ -507,6 +507,18 @@ __device__ __forceinline__ void dropout_col_bits(const Dropout &dr, uint32_t h, 
   }
 }
 
+// Register rebalancing between warpgroups (all four warps of a warpgroup
+// execute the same one). The CTA's pool is its threads times the registers
+// per thread at launch; the requests of all warpgroups must fit in it.
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 __device__ __forceinline__ int warp_id() { return threadIdx.x >> 5; }
 __device__ __forceinline__ int lane_id() { return threadIdx.x & 31; }
 
