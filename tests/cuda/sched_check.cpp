@@ -67,6 +67,15 @@ static bool run(int N, int Nk, int BH, bool causal, int sms, double min_balance)
   return ok;
 }
 
+// The mode sched_make picks for a causal shape with the forward's costs.
+static bool expect_mode(int N, int Nk, int BH, int sms, int mode) {
+  const std::vector<long long> cost = fwd_costs(N, Nk, true);
+  const TileSched s = fa::sched_make(BH, static_cast<int>(cost.size()), cost.data(), true, sms);
+  const bool ok = s.mode == mode;
+  std::printf("%s mode %d %d %d %d\n", ok ? "ok" : "FAIL", N, Nk, BH, s.mode);
+  return ok;
+}
+
 int main() {
   bool ok = true;
   // balance floors where the schedule has enough work per CTA to balance
@@ -77,6 +86,10 @@ int main() {
   ok &= run(8192, 8192, 16, true, 152, 0.97);
   ok &= run(4096, 16384, 32, true, 152, 0.9);
   ok &= run(128, 8192, 2048, true, 152, 0.9);
+  // the shapes of the GPU schedule test: the mode each one exercises
+  ok &= expect_mode(2048, 2048, 48, 152, fa::kPairs);
+  ok &= expect_mode(1000, 4000, 40, 152, fa::kSnake);
+  ok &= expect_mode(1400, 1400, 60, 152, fa::kPairs);
   // coverage only: small, ragged and odd shapes, other SM counts
   const int Ns[] = {1, 100, 128, 129, 255, 256, 300, 1000, 1152, 2049};
   const int BHs[] = {1, 2, 3, 7, 19, 64};

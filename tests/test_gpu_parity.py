@@ -158,6 +158,26 @@ def test_fwd_d256_kv():
           {"o": o.float().cpu().double().numpy(), "lse": lse.cpu().double().numpy()}, {"o": ro, "lse": rl})
 
 
+# ------------------------------------------------------------ persistent schedule, several items per CTA
+
+@pytest.mark.parametrize("B,H,Nq,Nk,d", [
+    (2, 24, 2048, 2048, 64),   # pairs of query tiles / key blocks, then single tiles of the last 19 heads
+    (2, 20, 1000, 4000, 64),   # snake order over unequal causal costs (bottom-right mask)
+    (2, 30, 1400, 1400, 64),   # 11 tiles per head: pair units with an odd middle tile (empty slots)
+])
+def test_causal_schedules_with_several_items_per_cta(B, H, Nq, Nk, d):
+    """The host picks the schedule mode from exact tile costs (the CPU test
+    checks which one for these shapes); every item of every CTA must land
+    once, whatever the mode."""
+    q, _, _, dO = make_qkv_do(B, H, Nq, d, seed=600 + Nq, dtype=torch.bfloat16)
+    _, k, v, _ = make_qkv_do(B, H, Nk, d, seed=700 + Nk, dtype=torch.bfloat16)
+    scale = 1.0 / math.sqrt(d)
+    got = _run_gpu_kv(q, k, v, dO, scale, True)
+    o, lse = oracle.attention_fwd_kv(_np(q), _np(k), _np(v), scale, True)
+    dq, dk, dv = oracle.attention_bwd_kv(_np(q), _np(k), _np(v), _np(dO), scale, True)
+    check(f"sched_B{B}_H{H}_Nq{Nq}_Nk{Nk}_d{d}", "bf16", got, {"o": o, "lse": lse, "dq": dq, "dk": dk, "dv": dv})
+
+
 # ------------------------------------------------------------ dropout
 
 def _drop_ref(q, k, v, dO, scale, causal, seed, offset, p):
