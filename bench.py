@@ -188,6 +188,7 @@ def run_ours(args, w):
 
     import exact_attention_97_gb300 as fa
     from exact_attention_97_gb300.inputs import make_qkv_do
+    from exact_attention_97_gb300.shard import head_range, max_over_ranks
 
     world, rank, local = _dist()
     torch.cuda.set_device(local)
@@ -196,10 +197,15 @@ def run_ours(args, w):
     dev = torch.device("cuda", local)
     fa.load()
 
-    # inputs: seeded host tensors, pinned copies for the end-to-end leg, device copies
+    # inputs: seeded host tensors, pinned copies for the end-to-end leg, device copies.
+    # Weak scaling: the whole job is world x (B x H) independent heads; this
+    # rank owns its contiguous block of B x H of them, seeded by the block's
+    # offset (rank 0 keeps the workload's own seeds).
+    lo, _ = head_range(world * w.B * w.H, rank, world)
+    seed = w.seed + 4 * lo
     dt = torch.float16 if w.dtype == "f16" else torch.bfloat16
-    q_h, _, _, do_h = make_qkv_do(w.B, w.H, w.N, w.d, w.seed, dt)
-    _, k_h, v_h, _ = make_qkv_do(w.B, w.H, w.n_keys, w.d, w.seed, dt)
+    q_h, _, _, do_h = make_qkv_do(w.B, w.H, w.N, w.d, seed, dt)
+    _, k_h, v_h, _ = make_qkv_do(w.B, w.H, w.n_keys, w.d, seed, dt)
     q_h, k_h, v_h, do_h = (t.pin_memory() for t in (q_h, k_h, v_h, do_h))
     q, k, v, dO = (t.to(dev) for t in (q_h, k_h, v_h, do_h))
     o = torch.empty_like(q)
@@ -274,10 +280,7 @@ def run_ours(args, w):
     k_dkdv, k_dq = (None, None) if args.fwd_only else (pair_ms(1), pair_ms(2))
     fwd_call = statistics.mean(m[0].elapsed_time(m[1]) for m in marks)
     bwd_call = None if args.fwd_only else statistics.mean(m[1].elapsed_time(m[2]) for m in marks)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dev)
 
     flops_step = w.flops_fwd() + (0 if args.fwd_only else w.flops_bwd())
     value = flops_step * world * args.steps / (ms * 1e-3) / 1e12
@@ -334,10 +337,7 @@ def run_ours(args, w):
         b.record(stream)
         torch.cuda.synchronize()
         ems = a.elapsed_time(b)
-        if world > 1:
-            t = torch.tensor([ems], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ems = float(t.item())
+        ems = max_over_ranks(ems, dev)
         bytes_in = sum(t.numel() * t.element_size() for t in ((q_h, k_h, v_h) if args.fwd_only else
                                                                 (q_h, k_h, v_h, do_h)))
         bytes_out = sum(t.numel() * t.element_size() for t in out_h)
@@ -359,7 +359,7 @@ def run_ours(args, w):
                        "inputs": "i.i.d. N(0,1), seeds Q=0 K=1 V=2 dO=3",
                        "l2": "inputs larger than L2 (each of Q, K, V, dO is "
                              f"{q.numel() * 2 / 1e6:.0f} MB vs 129 MB L2)",
-                       "parallelism": f"{world} independent replica(s), no collective"},
+                       "parallelism": f"{world} rank(s), {w.B * w.H} heads each (heads sharded), no collective"},
             "pct_of_peak": value / (peak * world) * 100.0,
             "fwd": {"ms": fwd_call, "tflops": fwd_tf, "frac": fwd_tf / peak},
             "bwd": None if args.fwd_only else {"ms": bwd_call, "tflops": bwd_tf, "frac": bwd_tf / peak},
