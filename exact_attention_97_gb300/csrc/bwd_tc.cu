@@ -704,6 +704,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = wq * 32 + lane;  // query row within the tile (TMEM lane)
     const uint32_t lane_addr = static_cast<uint32_t>(wq * 32) << 16;
     const uint64_t cc = f2_pack(scale_log2, scale_log2);
+    // this row's -L log2(e) and D of item k (padded rows hold -inf and 0),
+    // loaded one item ahead so the epilogue hides their latency
+    auto row_terms = [&](int k, float &nl, float &drow) {
+      int rk, hb, st;
+      while ((st = sched_item(sched, blockIdx.x, k, rk, hb)) == kSkip) ++k;
+      if (st == kDone) return;
+      const size_t prow = static_cast<size_t>(hb) * Np + qtile_of(rk) * kBlk + r;
+      nl = Lp[prow];
+      drow = Dp[prow];
+    };
+    float nl_next = 0.f, drow_next = 0.f;
+    row_terms(0, nl_next, drow_next);
     bool ok = true;
     int g = 0, it = 0, rank, bh;
     for (int k = 0; ok; ++k) {
@@ -712,8 +724,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (step == kSkip) continue;
       const int qt = qtile_of(rank), n_kb = kblocks(qt);
       const int q = qt * kBlk + r;
-      const size_t prow = static_cast<size_t>(bh) * Np + q;
-      const float nl = Lp[prow], drow = Dp[prow];
+      const float nl = nl_next, drow = drow_next;
       const uint64_t nn = f2_pack(nl, nl);
       const int kvis = causal ? min(Nk, q + 1 + off) : Nk;  // keys below kvis are visible
       for (int j = 0; j < n_kb; ++j, ++g) {
@@ -764,6 +775,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         mbar_arrive(&ds_ready);
       }
+      if (ok) row_terms(k + 1, nl_next, drow_next);
       // epilogue: dQ = scale * accumulator; warpgroup h stores head columns
       // [hD/2, hD/2 + D/2), 16 at a time
       if (!ok || !mbar_wait_warp(&done, it & 1, &abort_flag)) {
