@@ -117,7 +117,7 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
   constexpr int kUnits = L::kUnits, kUC = L::kUnitCols;
   __shared__ uint64_t q_full[kQBuf], q_empty[kQBuf], k_full[kStages], k_empty[kStages], v_full[kVStages],
       v_empty[kVStages], s_full[kSBuf], p_ready[kSBuf], pv_done[kSBuf], drain_s, drain_pv,
-      mask_full[kMaskSlots], mask_empty[kMaskSlots];
+      mask_full[DROP ? kMaskSlots : 1], mask_empty[DROP ? kMaskSlots : 1];
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_flag;
 
@@ -155,9 +155,11 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
     }
     mbar_init(&drain_s, 1);
     mbar_init(&drain_pv, 1);
-    for (int b = 0; b < kMaskSlots; ++b) {
-      mbar_init(&mask_full[b], 4 * 32);
-      mbar_init(&mask_empty[b], 4 * 32);
+    if constexpr (DROP) {
+      for (int b = 0; b < kMaskSlots; ++b) {
+        mbar_init(&mask_full[b], 4 * 32);
+        mbar_init(&mask_empty[b], 4 * 32);
+      }
     }
     fence_mbar_init();
   }
@@ -175,12 +177,7 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
   // items (kt), so the K/V rings, the S buffers and their barrier phases run
   // on without a break from one item to the next; `it` counts items (phase of
   // q_full / q_empty).
-  // With dropout, 12 warps share 384 x 168 registers: each warpgroup resizes
-  // its share at the top of its branch (loaders and issuers 56, softmax 232,
-  // keep masks 96 per thread: 49152 of the 64512).
-  if (warp < 4) {
-  if constexpr (DROP) setmaxnreg_dec<56>();
-  if (warp == 0) {
+  auto role_k_loader = [&]() {
     // ------------------------------------------------------------ loader: Q, K
     // Q of item `it` goes into buffer it % kQBuf once every S MMA of the item
     // that used it before has completed (q_empty); it is also prefetched into
@@ -222,7 +219,8 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
       for (int i = max(0, it - kQBuf); i < it; ++i) mbar_wait_drain(&q_full[i % kQBuf], (i / kQBuf) & 1);
       for (int j = max(0, kt - kStages); j < kt; ++j) mbar_wait_drain(&k_full[j % kStages], (j / kStages) & 1);
     }
-  } else if (warp == 2) {
+  };
+  auto role_v_loader = [&]() {
     // ---------------------------------------------------------------- loader: V
     if (lane == 0) {
       tma_prefetch_desc(&tmV);
@@ -246,7 +244,8 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
       }
       for (int j = max(0, kt - kVStages); j < kt; ++j) mbar_wait_drain(&v_full[j % kVStages], (j / kVStages) & 1);
     }
-  } else if (warp == 1) {
+  };
+  auto role_s_issuer = [&]() {
     // ------------------------------------------------------ MMA issuer: S = Q K^T
     // S of key tile kt goes to buffer kt % kSBuf once P V of tile kt - kSBuf
     // (which used that buffer) has completed; it accumulates over the tile's K
@@ -292,7 +291,8 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
       mma_commit(&drain_s);
       mbar_wait_drain(&drain_s, 0);
     }
-  } else if (warp == 3) {
+  };
+  auto role_pv_issuer = [&]() {
     // ---------------------------------------------------- MMA issuer: O += P V
     // A second issuing thread, so the tensor pipe always has one of the two
     // streams queued while the other waits on its barriers. The first P V of
@@ -330,9 +330,8 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
       mma_commit(&drain_pv);
       mbar_wait_drain(&drain_pv, 0);
     }
-  }
-  } else if (warp < 8) {
-    if constexpr (DROP) setmaxnreg_inc<232>();
+  };
+  auto role_softmax = [&]() {
     // ----------------------------------------------------------------- softmax
     const int wq = warp - 4;                 // TMEM lane quarter of this warp
     const int r_local = wq * 32 + lane;      // row within the tile
@@ -487,9 +486,8 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
       }
       if (store) lse[static_cast<size_t>(bh) * N + row] = (m_used * scale_log2 + log2f(l_sum)) * kLn2;
     }
-  } else {
-    if constexpr (DROP) {
-      setmaxnreg_dec<96>();
+  };
+  auto role_masks = [&]() {
       // ---------------------------------------------------------- keep masks
       // Row r_local of every key tile, one tile ahead of the softmax warps at
       // most kMaskSlots: the bits of Philox4x32-10 bytes >= t, in the layout
@@ -517,7 +515,30 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
           mbar_arrive(&mask_full[ms]);
         }
       }
+  };
+  if constexpr (DROP) {
+    // 12 warps share 384 x 168 registers: each warpgroup resizes its share at
+    // the top of its branch (loaders and issuers 56, softmax 232, keep masks
+    // 96 per thread: 49152 of the 64512)
+    if (warp < 4) {
+      setmaxnreg_dec<56>();
+      if (warp == 0) role_k_loader();
+      else if (warp == 2) role_v_loader();
+      else if (warp == 1) role_s_issuer();
+      else role_pv_issuer();
+    } else if (warp < 8) {
+      setmaxnreg_inc<232>();
+      role_softmax();
+    } else {
+      setmaxnreg_dec<96>();
+      role_masks();
     }
+  } else {
+    if (warp == 0) role_k_loader();
+    else if (warp == 2) role_v_loader();
+    else if (warp == 1) role_s_issuer();
+    else if (warp == 3) role_pv_issuer();
+    else role_softmax();
   }
 
   tc_fence_before();
