@@ -31,7 +31,11 @@
 // passes are persistent: at most one CTA per SM walks a static list of items
 // (tile_sched.h), and the rings and barrier phases carry over from item to
 // item, so the next item's loads and first MMAs overlap the current item's
-// last products and its epilogue.
+// last products and its epilogue. The dK/dV pass writes its results through
+// per-warp shared-memory boxes and TMA stores. Head sizes 64, 96 and 128.
+// With dropout (DROP instances) both passes draw the keep bits of each tile
+// (Philox4x32-10, sm103.cuh) before its scores arrive: dV takes
+// P o Z / (1 - p), and dP is scaled by Z / (1 - p) before dS.
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>

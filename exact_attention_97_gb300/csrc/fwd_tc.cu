@@ -11,30 +11,36 @@
 // and the saved statistic L = m + ln l of its section 04.
 //
 // GB300 design: a persistent grid, one CTA per SM, each CTA walking a static
-// list of 128-row query tiles (see FwdSched); within a CTA:
-//   warp 0      loader: Q of each tile, then K_j into a ring of kStages
-//               shared-memory stages (128-byte swizzle, 3-D tensor maps so
-//               rows past N read as zero). The rings and barrier phases run
-//               on across tiles, so the next tile's loads and S MMAs overlap
-//               the current tile's last P V products and its epilogue.
+// list of 128-row query tiles (tile_sched.h); within a CTA:
+//   warp 0      loader: Q of each tile, then K_j into a ring of shared-memory
+//               stages (128-byte swizzle, 3-D tensor maps so rows past N read
+//               as zero). The rings and barrier phases run on across tiles,
+//               so the next tile's loads and S MMAs overlap the current
+//               tile's last P V products and its epilogue.
 //   warp 2      loader of V_j (its own ring); also allocates and frees the
 //               512 tensor-memory (TMEM) columns.
-//   warp 1      MMA issuer for S_j = Q K_j^T into one of three TMEM buffers,
-//               so S_{j+1} and S_{j+2} can run while row statistics of S_j
-//               are computed.
+//   warp 1      MMA issuer for S_j = Q K_j^T into one of the TMEM score
+//               buffers, so the next scores can run while row statistics of
+//               S_j are computed.
 //   warp 3      MMA issuer for O += P_j V_j, with P_j read straight from TMEM
 //               (A operand in TMEM, B = V_j in shared memory). Two issuing
 //               threads keep the tensor pipe fed while either waits.
 //   warps 4-7   softmax: thread t owns row t of the tile (= TMEM lane t).
 //               Loads its 128 scores, applies the mask, takes the row max,
-//               writes P = 2^(s*c - m*c) (c = scale*log2 e) back as bf16 over
-//               the S columns, and keeps l. The running max is only moved
-//               when it grows by more than 2^8: any common base leaves u/l
-//               unchanged (tutorial section 02), so the O rescale in TMEM
+//               writes P = 2^(s*c - m*c) (c = scale*log2 e) back as 16-bit
+//               pairs over the S columns, and keeps l. The running max is only
+//               moved when it grows by more than 2^8: any common base leaves
+//               u/l unchanged (tutorial section 02), so the O rescale in TMEM
 //               (ld, multiply, st) is skipped on most tiles. The epilogue
-//               divides by l, stores O as bf16 and L = m*scale + ln l.
+//               divides by l, stores O and L = m*scale + ln l.
+//   warps 8-11  (dropout instances only) draw each tile's keep bits
+//               (Philox4x32-10, sm103.cuh) into a shared ring one tile ahead;
+//               the softmax warps scale the kept P by 1 / (1 - p) for P V
+//               and keep the undropped l.
 //
-// TMEM columns: S buffers [0,128), [128,256), [256,384); O = [384, 384+d).
+// Head sizes 64, 96 and 128 use one K/V unit per key tile; 256 uses two
+// (FwdSmem). TMEM columns: score buffers of 128 columns, then O.
+
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
