@@ -311,18 +311,28 @@ def run_ours(args, w):
     fwd_tf = tf(w.flops_fwd(), fwd_call)
     bwd_tf = None if args.fwd_only else tf(w.flops_bwd(), bwd_call)
 
-    # end to end through the public API: pinned host inputs in, results back to pinned host
+    # end to end through the public API: pinned host inputs in, results back to pinned host.
+    # The training step goes through attention_step_host, which streams chunks of heads
+    # through the GPU (copy in, compute, copy out on three streams).
     e2e = None
     if not args.no_e2e:
-        out_h = [torch.empty_like(t).pin_memory() for t in ((q_h,) if args.fwd_only else (q_h, q_h, k_h, v_h))]
+        if args.fwd_only:
+            out_h = [torch.empty_like(q_h).pin_memory(),
+                     torch.empty((w.B, w.H, w.N), dtype=torch.float32).pin_memory()]
+        else:
+            out_h = [torch.empty_like(q_h).pin_memory(),
+                     torch.empty((w.B, w.H, w.N), dtype=torch.float32).pin_memory(),
+                     torch.empty_like(q_h).pin_memory(), torch.empty_like(k_h).pin_memory(),
+                     torch.empty_like(v_h).pin_memory()]
 
         def e2e_step():
-            qd, kd, vd, dod = (t.to(dev, non_blocking=True) for t in (q_h, k_h, v_h, do_h))
-            od, ld = fa.attention_forward(qd, kd, vd, w.scale, w.causal, **drop)
-            g = () if args.fwd_only else fa.attention_backward(qd, kd, vd, od, ld, dod, w.scale, w.causal,
-                                                               workspace=ws, **drop)
-            for dst, src in zip(out_h, (od, *g)):
-                dst.copy_(src, non_blocking=True)
+            if args.fwd_only:
+                qd, kd, vd = (t.to(dev, non_blocking=True) for t in (q_h, k_h, v_h))
+                od, ld = fa.attention_forward(qd, kd, vd, w.scale, w.causal, **drop)
+                for dst, src in zip(out_h, (od, ld)):
+                    dst.copy_(src, non_blocking=True)
+            else:
+                fa.attention_step_host(q_h, k_h, v_h, do_h, w.scale, w.causal, out=tuple(out_h), **drop)
 
         for _ in range(2):
             e2e_step()

@@ -24,7 +24,7 @@ __all__ = [
     "fa_fwd_f32", "fa_bwd_f32", "fa_fwd_kv", "fa_bwd_kv", "fa_fwd_dropout", "fa_bwd_dropout",
     "fa_bwd_workspace_size", "fa_status_string", "fa_device_status", "fa_last_launch_count",
     "fa_set_kernel_timing",
-    "attention_forward", "attention_backward", "lib_path", "load",
+    "attention_forward", "attention_backward", "attention_step_host", "lib_path", "load",
 ]
 
 
@@ -51,15 +51,16 @@ def _stream_handle(stream):
 
 
 def attention_forward(q, k, v, scale=None, causal=False, out=None, lse=None, stream=None,
-                      dropout_p=0.0, seed=0, offset=0):
+                      dropout_p=0.0, seed=0, offset=0, head_base=0):
     """(O, L) for CUDA tensors q [B, H, Nq, d] and k, v [B, H, Nk, d] (all bf16, all f16 or all float32).
 
     bf16 and f16 need d in {64, 96, 128} (or 256 for the forward); float32 takes 1 <= d <= 128 and Nk == Nq. L is
     float32 [B, H, Nq], the natural-log log-sum-exp of the scaled scores. With Nk != Nq
     the causal mask is aligned bottom-right (query i sees keys j <= i + Nk - Nq).
     dropout_p > 0 (bf16 / f16 only) drops attention probabilities with the
-    Philox mask of fa_fwd_dropout, keyed by (seed, offset); pass the same
-    three values to attention_backward.
+    Philox mask of fa_fwd_dropout, keyed by (seed, offset) and the heads'
+    global index (head_base + b * H + h); pass the same values to
+    attention_backward.
     """
     torch = _torch()
     B, H, N, d = q.shape
@@ -81,7 +82,7 @@ def attention_forward(q, k, v, scale=None, causal=False, out=None, lse=None, str
             if dt == torch.float32:
                 raise ValueError("dropout needs bfloat16 or float16 inputs")
             fa_fwd_dropout(*ptrs, B, H, N, Nk, d, scale, int(bool(causal)),
-                           FA_F16 if dt == torch.float16 else FA_BF16, dropout_p, seed, offset,
+                           FA_F16 if dt == torch.float16 else FA_BF16, dropout_p, seed, offset, head_base,
                            _stream_handle(stream))
         elif Nk != N:
             if dt == torch.float32:
@@ -95,7 +96,7 @@ def attention_forward(q, k, v, scale=None, causal=False, out=None, lse=None, str
 
 
 def attention_backward(q, k, v, o, lse, dO, scale=None, causal=False, workspace=None, stream=None,
-                       grads=None, dropout_p=0.0, seed=0, offset=0):
+                       grads=None, dropout_p=0.0, seed=0, offset=0, head_base=0):
     """(dQ, dK, dV) for upstream gradient dO, given the forward's O and L (and
     the forward's dropout_p, seed and offset)."""
     torch = _torch()
@@ -123,7 +124,8 @@ def attention_backward(q, k, v, o, lse, dO, scale=None, causal=False, workspace=
         if dropout_p:
             if kind == FA_F32:
                 raise ValueError("dropout needs bfloat16 or float16 inputs")
-            fa_bwd_dropout(*ptrs, B, H, N, Nk, d, scale, int(bool(causal)), kind, dropout_p, seed, offset, *ws)
+            fa_bwd_dropout(*ptrs, B, H, N, Nk, d, scale, int(bool(causal)), kind, dropout_p, seed, offset, head_base,
+                           *ws)
         elif Nk != N:
             if kind == FA_F32:
                 raise ValueError("float32 needs k and v with as many rows as q")
@@ -132,3 +134,6 @@ def attention_backward(q, k, v, o, lse, dO, scale=None, causal=False, workspace=
             fn = {FA_BF16: fa_bwd, FA_F16: fa_bwd_f16, FA_F32: fa_bwd_f32}[kind]
             fn(*ptrs, B, H, N, d, scale, int(bool(causal)), *ws)
     return dq, dk, dv
+
+
+from .pipeline import attention_step_host  # noqa: E402  (uses the functions above)

@@ -24,9 +24,10 @@ _SIGNATURES = {
     "fa_fwd_kv": (c_int, [c_void_p] * 5 + [c_int] * 5 + [c_float, c_int, c_int, c_void_p]),
     "fa_bwd_kv": (c_int, [c_void_p] * 9 + [c_int] * 5 + [c_float, c_int, c_int, c_void_p, c_size_t, c_void_p]),
     "fa_fwd_dropout": (c_int, [c_void_p] * 5 + [c_int] * 5 + [c_float, c_int, c_int, c_float, ctypes.c_ulonglong,
-                                                               ctypes.c_uint, c_void_p]),
+                                                               ctypes.c_uint, ctypes.c_uint, c_void_p]),
     "fa_bwd_dropout": (c_int, [c_void_p] * 9 + [c_int] * 5 + [c_float, c_int, c_int, c_float, ctypes.c_ulonglong,
-                                                               ctypes.c_uint, c_void_p, c_size_t, c_void_p]),
+                                                               ctypes.c_uint, ctypes.c_uint, c_void_p, c_size_t,
+                                                               c_void_p]),
     "fa_fwd_f32": (c_int, [c_void_p] * 5 + [c_int] * 4 + [c_float, c_int, c_void_p]),
     "fa_bwd_f32": (c_int, [c_void_p] * 9 + [c_int] * 4 + [c_float, c_int, c_void_p, c_size_t, c_void_p]),
     "fa_bwd_workspace_size": (c_size_t, [c_int] * 5),
@@ -109,15 +110,17 @@ def fa_bwd_kv(q, k, v, o, lse, dO, dq, dk, dv, B, H, Nq, Nk, d, scale, causal, d
                  int(dtype), workspace, workspace_bytes, stream)
 
 
-def fa_fwd_dropout(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, dtype, p_drop, seed, offset, stream):
+def fa_fwd_dropout(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, dtype, p_drop, seed, offset, head_base,
+                   stream):
     return _call("fa_fwd_dropout", q, k, v, o, lse, B, H, Nq, Nk, d, float(scale), int(causal), int(dtype),
-                 float(p_drop), int(seed), int(offset), stream)
+                 float(p_drop), int(seed), int(offset), int(head_base), stream)
 
 
 def fa_bwd_dropout(q, k, v, o, lse, dO, dq, dk, dv, B, H, Nq, Nk, d, scale, causal, dtype, p_drop, seed, offset,
-                   workspace, workspace_bytes, stream):
+                   head_base, workspace, workspace_bytes, stream):
     return _call("fa_bwd_dropout", q, k, v, o, lse, dO, dq, dk, dv, B, H, Nq, Nk, d, float(scale), int(causal),
-                 int(dtype), float(p_drop), int(seed), int(offset), workspace, workspace_bytes, stream)
+                 int(dtype), float(p_drop), int(seed), int(offset), int(head_base), workspace, workspace_bytes,
+                 stream)
 
 
 def fa_fwd_f32(q, k, v, o, lse, B, H, N, d, scale, causal, stream):

@@ -350,13 +350,15 @@ int fa_bwd_kv(const void *q, const void *k, const void *v, const void *o, const 
 }
 
 // Dropout parameters: p in [0, 1) to a byte threshold t = round(256 p).
-static int make_dropout(float p, unsigned long long seed, unsigned int offset, Dropout *dr) {
+static int make_dropout(float p, unsigned long long seed, unsigned int offset, unsigned int head_base,
+                        Dropout *dr) {
   if (!(p >= 0.f && p < 1.f)) return FA_ERR_ARG;
   int t = static_cast<int>(lrint(256.0 * static_cast<double>(p)));
   if (t > 255) t = 255;
   dr->k0 = static_cast<uint32_t>(seed);
   dr->k1 = static_cast<uint32_t>(seed >> 32);
   dr->offset = offset;
+  dr->head_base = head_base;
   dr->t = static_cast<uint32_t>(t);
   dr->inv_keep = static_cast<float>(256.0 / (256.0 - t));
   return FA_OK;
@@ -364,21 +366,21 @@ static int make_dropout(float p, unsigned long long seed, unsigned int offset, D
 
 int fa_fwd_dropout(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int Nq,
                    int Nk, int d, float scale, int causal, int dtype, float p_drop, unsigned long long seed,
-                   unsigned int offset, fa_stream_t stream) {
+                   unsigned int offset, unsigned int head_base, fa_stream_t stream) {
   if (dtype != FA_BF16 && dtype != FA_F16) return dtype == FA_F32 ? FA_ERR_UNSUPPORTED : FA_ERR_ARG;
   Dropout dr;
-  const int st = make_dropout(p_drop, seed, offset, &dr);
+  const int st = make_dropout(p_drop, seed, offset, head_base, &dr);
   if (st != FA_OK) return st;
   return fwd16(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, stream, dtype == FA_F16, &dr);
 }
 
 int fa_bwd_dropout(const void *q, const void *k, const void *v, const void *o, const float *lse, const void *dO,
                    void *dq, void *dk, void *dv, int B, int H, int Nq, int Nk, int d, float scale, int causal,
-                   int dtype, float p_drop, unsigned long long seed, unsigned int offset, void *workspace,
-                   size_t workspace_bytes, fa_stream_t stream) {
+                   int dtype, float p_drop, unsigned long long seed, unsigned int offset, unsigned int head_base,
+                   void *workspace, size_t workspace_bytes, fa_stream_t stream) {
   if (dtype != FA_BF16 && dtype != FA_F16) return dtype == FA_F32 ? FA_ERR_UNSUPPORTED : FA_ERR_ARG;
   Dropout dr;
-  const int st = make_dropout(p_drop, seed, offset, &dr);
+  const int st = make_dropout(p_drop, seed, offset, head_base, &dr);
   if (st != FA_OK) return st;
   return bwd16(q, k, v, o, lse, dO, dq, dk, dv, B, H, Nq, Nk, d, scale, causal, workspace, workspace_bytes,
                stream, dtype == FA_F16, &dr);

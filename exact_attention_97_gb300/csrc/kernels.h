@@ -9,11 +9,12 @@ namespace fa {
 
 // Dropout on the attention probabilities: element (i, j) of head h is kept
 // iff byte j mod 4 of word i mod 4 of Philox4x32-10 with counter
-// (j/4, i/4, h, offset) and key (k0, k1) is >= t; kept probabilities are
-// scaled by inv_keep = 256 / (256 - t).
+// (j/4, i/4, head_base + h, offset) and key (k0, k1) is >= t; kept
+// probabilities are scaled by inv_keep = 256 / (256 - t).
 struct Dropout {
   uint32_t k0, k1;  // the 64-bit seed, low word first
   uint32_t offset;
+  uint32_t head_base;  // index of the call's first head in a larger problem
   uint32_t t;       // byte threshold, 0..255
   float inv_keep;
 };

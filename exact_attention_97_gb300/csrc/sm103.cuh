@@ -434,7 +434,7 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1
 
 // Dropout on the attention probabilities (struct Dropout, kernels.h):
 // element (i, j) of head h (query i, key j) is kept iff byte j mod 4 of word
-// i mod 4 of philox4x32_10((j/4, i/4, h, offset), seed) is >= t.
+// i mod 4 of philox4x32_10((j/4, i/4, head_base + h, offset), seed) is >= t.
 
 // Bits (>= t) of the four bytes of w, as a 4-bit value (byte b -> bit b).
 __device__ __forceinline__ uint32_t keep_nibble(uint32_t w, uint32_t t4) {
@@ -459,7 +459,7 @@ __device__ __forceinline__ void dropout_row_bits(const Dropout &dr, uint32_t h, 
 #pragma unroll
     for (int blk = 0; blk < 2; ++blk) {  // 16 keys: 4 calls, one per lane of the quad
       const uint4 r = philox4x32_10(make_uint4(static_cast<uint32_t>(j0 / 4 + 8 * w + 4 * blk + me),
-                                               static_cast<uint32_t>(i / 4), h, dr.offset),
+                                               static_cast<uint32_t>(i / 4), dr.head_base + h, dr.offset),
                                     dr.k0, dr.k1);
       // nibble r of `packed`: keep bits of row 4 (i/4) + r for this lane's 4 keys
       const uint32_t packed = keep_nibble(r.x, t4) | (keep_nibble(r.y, t4) << 4) | (keep_nibble(r.z, t4) << 8) |
@@ -486,7 +486,8 @@ __device__ __forceinline__ void dropout_col_bits(const Dropout &dr, uint32_t h, 
 #pragma unroll
     for (int blk = 0; blk < 2; ++blk) {  // 16 rows: 4 calls, one per lane of the quad
       const uint4 r = philox4x32_10(make_uint4(static_cast<uint32_t>(j / 4),
-                                               static_cast<uint32_t>(i0 / 4 + 8 * w + 4 * blk + me), h, dr.offset),
+                                               static_cast<uint32_t>(i0 / 4 + 8 * w + 4 * blk + me),
+                                               dr.head_base + h, dr.offset),
                                     dr.k0, dr.k1);
       // nibble b of `packed`: keep bits of this call's 4 rows for key 4 (j/4) + b
       const uint32_t g0 = __vcmpgeu4(r.x, t4), g1 = __vcmpgeu4(r.y, t4), g2 = __vcmpgeu4(r.z, t4),

@@ -155,11 +155,15 @@ int fa_bwd_kv(const void *q, const void *k, const void *v, const void *o,
  *   Pd = P o Z / (1 - p'),  O = Pd V,  lse = the undropped log-sum-exp;
  *   backward with the same Z: dV = Pd^T dO, dP = (dO V^T) o Z / (1 - p'),
  *   dS = P o (dP - D), dQ = scale dS K, dK = scale dS^T Q.
- * Z_ij (query i, key j, head index h = b*H + head) is 1 iff byte (j mod 4)
- * of word (i mod 4) of Philox4x32-10 (Salmon et al., SC 2011) with counter
- * (j/4, i/4, h, offset) and key (seed low word, seed high word) is >= t,
+ * Z_ij (query i, key j, head index h = head_base + b*H + head) is 1 iff
+ * byte (j mod 4) of word (i mod 4) of Philox4x32-10 (Salmon et al., SC 2011)
+ * with counter (j/4, i/4, h, offset) and key (seed low word, seed high word)
+ * is >= t,
  * t = round(256 p_drop) capped at 255, and p' = t / 256. The same
- * (p_drop, seed, offset) must be passed to both calls. Arguments, layouts
+ * (p_drop, seed, offset, head_base) must be passed to both calls. head_base
+ * places the call's heads in a larger problem: a batch computed in pieces of
+ * heads (or sharded over GPUs) draws the same mask as one call on all of it
+ * when each piece passes the index of its first head. Arguments, layouts
  * and errors are as for fa_fwd_kv / fa_bwd_kv; p_drop outside [0, 1) or NaN
  * is FA_ERR_ARG. p_drop = 0 gives the plain results.
  */
@@ -167,14 +171,14 @@ int fa_fwd_dropout(const void *q, const void *k, const void *v, void *o,
                    float *lse, int B, int H, int Nq, int Nk, int d,
                    float scale, int causal, int dtype, float p_drop,
                    unsigned long long seed, unsigned int offset,
-                   fa_stream_t stream);
+                   unsigned int head_base, fa_stream_t stream);
 int fa_bwd_dropout(const void *q, const void *k, const void *v, const void *o,
                    const float *lse, const void *dO, void *dq, void *dk,
                    void *dv, int B, int H, int Nq, int Nk, int d, float scale,
                    int causal, int dtype, float p_drop,
                    unsigned long long seed, unsigned int offset,
-                   void *workspace, size_t workspace_bytes,
-                   fa_stream_t stream);
+                   unsigned int head_base, void *workspace,
+                   size_t workspace_bytes, fa_stream_t stream);
 
 /* Forward with float tensors (all fp32 arithmetic, exact expf). Same
  * arguments and layout as fa_fwd with float element type. */

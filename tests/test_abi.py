@@ -121,14 +121,15 @@ def test_f16_argument_errors(lib):
 def test_dropout_argument_errors(lib):
     args = [P] * 5
     for bad in (1.0, 1.5, -0.1, float("nan"), float("inf")):
-        assert lib.fa_fwd_dropout(*args, 1, 1, 128, 128, 64, 0.125, 0, fa.FA_BF16, bad, 1, 0, None) == 9
-    assert lib.fa_fwd_dropout(*args, 1, 1, 128, 128, 64, 0.125, 0, fa.FA_F32, 0.1, 1, 0, None) == 3
-    assert lib.fa_fwd_dropout(None, *args[1:], 1, 1, 128, 128, 64, 0.125, 0, fa.FA_BF16, 0.1, 1, 0, None) == 1
-    assert lib.fa_fwd_dropout(*args, 1, 1, 128, 128, 80, 0.125, 0, fa.FA_F16, 0.1, 1, 0, None) == 3
+        assert lib.fa_fwd_dropout(*args, 1, 1, 128, 128, 64, 0.125, 0, fa.FA_BF16, bad, 1, 0, 0, None) == 9
+    assert lib.fa_fwd_dropout(*args, 1, 1, 128, 128, 64, 0.125, 0, fa.FA_F32, 0.1, 1, 0, 0, None) == 3
+    assert lib.fa_fwd_dropout(None, *args[1:], 1, 1, 128, 128, 64, 0.125, 0, fa.FA_BF16, 0.1, 1, 0, 0, None) == 1
+    assert lib.fa_fwd_dropout(*args, 1, 1, 128, 128, 80, 0.125, 0, fa.FA_F16, 0.1, 1, 0, 0, None) == 3
     ptrs = [P] * 9
-    assert lib.fa_bwd_dropout(*ptrs, 1, 1, 128, 128, 64, 0.125, 0, fa.FA_BF16, 1.0, 1, 0, P, 1 << 30, None) == 9
-    assert lib.fa_bwd_dropout(*ptrs, 1, 1, 128, 128, 64, 0.125, 0, fa.FA_BF16, 0.2, 1, 0, None, 0, None) == 5
-    assert lib.fa_bwd_dropout(*ptrs, 1, 1, 128, 128, 256, 0.125, 0, fa.FA_BF16, 0.2, 1, 0, P, 1 << 30, None) == 3
+    assert lib.fa_bwd_dropout(*ptrs, 1, 1, 128, 128, 64, 0.125, 0, fa.FA_BF16, 1.0, 1, 0, 0, P, 1 << 30, None) == 9
+    assert lib.fa_bwd_dropout(*ptrs, 1, 1, 128, 128, 64, 0.125, 0, fa.FA_BF16, 0.2, 1, 0, 0, None, 0, None) == 5
+    assert lib.fa_bwd_dropout(*ptrs, 1, 1, 128, 128, 256, 0.125, 0, fa.FA_BF16, 0.2, 1, 0, 0, P, 1 << 30,
+                              None) == 3
 
 
 def test_kv_argument_errors(lib):

@@ -178,6 +178,31 @@ def test_causal_schedules_with_several_items_per_cta(B, H, Nq, Nk, d):
     check(f"sched_B{B}_H{H}_Nq{Nq}_Nk{Nk}_d{d}", "bf16", got, {"o": o, "lse": lse, "dq": dq, "dk": dk, "dv": dv})
 
 
+# ------------------------------------------------------------ host-resident training step
+
+@pytest.mark.parametrize("case", ["bf16_causal", "f16_kv", "dropout", "one_chunk"])
+def test_host_step_equals_device_path(case):
+    """attention_step_host streams chunks of heads through the GPU on three
+    streams; its results must equal the device-side calls bit for bit."""
+    import exact_attention_97_gb300 as fa
+    dt = torch.float16 if case == "f16_kv" else torch.bfloat16
+    Nk = 700 if case == "f16_kv" else 300
+    q, _, _, dO = make_qkv_do(2, 5, 300, 128, seed=77, dtype=dt)
+    _, k, v, _ = make_qkv_do(2, 5, Nk, 128, seed=78, dtype=dt)
+    kw = {"dropout_p": 0.2, "seed": 5, "offset": 1} if case == "dropout" else {}
+    chunks = 1 if case == "one_chunk" else 4
+    pin = [t.pin_memory() for t in (q, k, v, dO)]
+    res = fa.attention_step_host(*pin, None, True, chunks=chunks, **kw)
+    torch.cuda.current_stream().synchronize()
+    dev = [t.cuda() for t in (q, k, v, dO)]
+    o, lse = fa.attention_forward(*dev[:3], None, True, **kw)
+    g = fa.attention_backward(*dev[:3], o, lse, dev[3], None, True, **kw)
+    torch.cuda.synchronize()
+    assert fa.fa_device_status() == 0
+    for a, b in zip(res, (o, lse, *g)):
+        assert torch.equal(a, b.cpu())
+
+
 # ------------------------------------------------------------ dropout
 
 def _drop_ref(q, k, v, dO, scale, causal, seed, offset, p):
