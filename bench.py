@@ -308,6 +308,17 @@ def run_ours(args, w):
                 "unit": "TFLOP/s", "frac": achieved / peak,
                 "traffic": args.traffic if args.traffic is not None else _measured_traffic(f"{dom[0]}<{w.d}>", w.name),
                 "peak_source": peaks["source"] + " burst bf16 (cuBLAS), of measured"}
+    # Algorithmic HBM bytes per step (each tensor read or written once; L, D
+    # and the padded row terms as fp32): the bound of the small, latency-
+    # and launch-bound configurations.
+    e = 2  # bytes per 16-bit element
+    rows_q, rows_k = w.B * w.H * w.N, w.B * w.H * w.n_keys
+    bytes_fwd = (rows_q * 2 + rows_k * 2) * w.d * e + rows_q * 4             # Q, K, V in; O, L out
+    bytes_bwd = (rows_q * 4 + rows_k * 4) * w.d * e + rows_q * 4 * 3         # Q,K,V,O,dO in; dQ,dK,dV out; L, D
+    step_bytes = bytes_fwd + (0 if args.fwd_only else bytes_bwd)
+    hbm = {"achieved_gbs": step_bytes * args.steps / (ms * 1e-3) / 1e9, "peak_gbs": peaks["hbm_gbs"],
+           "frac": step_bytes * args.steps / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], "bytes_per_step": step_bytes,
+           "peak_source": peaks["source"] + " copy bandwidth, of " + peaks["source"]}
     fwd_tf = tf(w.flops_fwd(), fwd_call)
     bwd_tf = None if args.fwd_only else tf(w.flops_bwd(), bwd_call)
 
@@ -375,6 +386,7 @@ def run_ours(args, w):
             "bwd": None if args.fwd_only else {"ms": bwd_call, "tflops": bwd_tf, "frac": bwd_tf / peak},
             "kernels": kernels,
             "roofline": roofline,
+            "hbm": hbm,
             "cpu_baseline": base,
             "e2e": e2e,
             "gpu_launches": launches[0],

@@ -91,7 +91,7 @@ int get_encoder() {
 // 3-D map over a contiguous [BH][N][d] 16-bit tensor (bf16, or f16 when
 // `f16`): dims {d, N, BH}, box {64, 128, 1}, 128-byte swizzle; rows past N
 // (inside a head) read as zero.
-int make_map(CUtensorMap *map, const void *ptr, int BH, int N, int d, bool f16) {
+int encode_map(CUtensorMap *map, const void *ptr, int BH, int N, int d, bool f16) {
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
                         static_cast<cuuint64_t>(BH)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
@@ -113,7 +113,7 @@ int make_map(CUtensorMap *map, const void *ptr, int BH, int N, int d, bool f16) 
 // Map for the backward's dK / dV stores: 32-row x 16-column boxes with a
 // 32-byte swizzle, written from per-warp staging buffers. Rows past `N` in a
 // box are not written.
-int make_store_map(CUtensorMap *map, void *ptr, int BH, int N, int d, bool f16) {
+int encode_store_map(CUtensorMap *map, void *ptr, int BH, int N, int d, bool f16) {
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
                         static_cast<cuuint64_t>(BH)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
@@ -128,6 +128,50 @@ int make_store_map(CUtensorMap *map, void *ptr, int BH, int N, int d, bool f16) 
     return kErrLaunch;
   }
   return kOk;
+}
+
+// Tensor maps depend only on the address, the shape, the element type and
+// the box / swizzle kind, so repeated calls on the same buffers (a training
+// loop, a benchmark) reuse them: a small cache, first in first out, shared by
+// all threads. Encoding costs a driver call per map otherwise.
+struct MapKey {
+  const void *ptr;
+  int BH, N, d, f16, store;
+  bool operator==(const MapKey &o) const {
+    return ptr == o.ptr && BH == o.BH && N == o.N && d == o.d && f16 == o.f16 && store == o.store;
+  }
+};
+constexpr int kMapCache = 64;
+std::mutex g_map_mu;
+MapKey g_map_key[kMapCache];
+CUtensorMap g_map_val[kMapCache];
+int g_map_used = 0, g_map_next = 0;
+
+int cached_map(CUtensorMap *map, const void *ptr, int BH, int N, int d, bool f16, bool store) {
+  const MapKey key{ptr, BH, N, d, f16 ? 1 : 0, store ? 1 : 0};
+  {
+    std::lock_guard<std::mutex> lock(g_map_mu);
+    for (int i = 0; i < g_map_used; ++i)
+      if (g_map_key[i] == key) {
+        *map = g_map_val[i];
+        return kOk;
+      }
+  }
+  const int st = store ? encode_store_map(map, const_cast<void *>(ptr), BH, N, d, f16)
+                       : encode_map(map, ptr, BH, N, d, f16);
+  if (st != kOk) return st;
+  std::lock_guard<std::mutex> lock(g_map_mu);
+  g_map_key[g_map_next] = key;
+  g_map_val[g_map_next] = *map;
+  g_map_next = (g_map_next + 1) % kMapCache;
+  if (g_map_used < kMapCache) ++g_map_used;
+  return kOk;
+}
+int make_map(CUtensorMap *map, const void *ptr, int BH, int N, int d, bool f16) {
+  return cached_map(map, ptr, BH, N, d, f16, false);
+}
+int make_store_map(CUtensorMap *map, void *ptr, int BH, int N, int d, bool f16) {
+  return cached_map(map, ptr, BH, N, d, f16, true);
 }
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -182,6 +226,16 @@ void timing_end(cudaStream_t stream) {
     cudaEventRecord(static_cast<cudaEvent_t>(t_events[2 * t_event_next + 1]), stream);
     ++t_event_next;
   }
+}
+cudaError_t set_smem_once(const void *kernel, int bytes, std::atomic<unsigned long long> *done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+  if (bit && (done->load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit) done->fetch_or(bit, std::memory_order_release);
+  return e;
 }
 }  // namespace fa
 

@@ -848,10 +848,9 @@ cudaError_t launch(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtenso
   });
   auto kdkdv = bwd_dkdv_kernel<D, F16, DROP>;
   auto kdq = bwd_dq_kernel<D, F16, DROP>;
-  if ((e = cudaFuncSetAttribute(kdkdv, cudaFuncAttributeMaxDynamicSharedMemorySize, DkdvCfg<D>::kAlloc)) !=
-          cudaSuccess ||
-      (e = cudaFuncSetAttribute(kdq, cudaFuncAttributeMaxDynamicSharedMemorySize, DqCfg<D>::kAlloc)) !=
-          cudaSuccess)
+  static std::atomic<unsigned long long> smem_kv{0}, smem_q{0};
+  if ((e = set_smem_once(reinterpret_cast<const void *>(kdkdv), DkdvCfg<D>::kAlloc, &smem_kv)) != cudaSuccess ||
+      (e = set_smem_once(reinterpret_cast<const void *>(kdq), DqCfg<D>::kAlloc, &smem_q)) != cudaSuccess)
     return e;
   timing_begin(stream);
   kdkdv<<<sched_kv.G, kThreads, DkdvCfg<D>::kAlloc, stream>>>(tmQ, tmK, tmV, tmdO, tmdK, tmdV, Lp, Dp, N, Nk,

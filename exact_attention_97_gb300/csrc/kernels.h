@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace fa {
 
 // Dropout on the attention probabilities: element (i, j) of head h is kept
@@ -36,6 +38,11 @@ enum : int {
 // Benchmark timing hook: records the next free event pair (if any) around a
 // main kernel. `begin` records the first event, `end` the second and advances.
 void timing_begin(cudaStream_t stream);
+
+// Sets a kernel's dynamic shared-memory limit once per device: `done` is the
+// kernel instance's own mask of devices already set (bit = device ordinal;
+// ordinals past 63 are set on every call).
+cudaError_t set_smem_once(const void *kernel, int bytes, std::atomic<unsigned long long> *done);
 void timing_end(cudaStream_t stream);
 
 cudaError_t launch_fwd_f32(const float *q, const float *k, const float *v, float *o, float *lse,
