@@ -621,7 +621,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // -------------------------------------------------------------- MMA issuer
-    // Per tile: S_0, dP_0, S_1, then per key block j: dQ_j, dP_{j+1}, S_{j+2}.
+    // Per tile: S_0, dP_0, S_1, then per key block j: dP_{j+1}, dQ_j, S_{j+2}.
     // The first dQ of a tile overwrites the accumulator: it waits for dS_0,
     // which the elementwise warps only produce after storing the previous
     // tile's dQ.
@@ -677,6 +677,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int st = g % KS;
           if (!mbar_wait(&ds_ready, g & 1, &abort_flag)) { ok = false; break; }
           tc_fence_after();
+          // dP_j has been read into dS_j, so dP_{j+1} goes first: the
+          // elementwise warps' next dS then overlaps dQ_j and S_{j+2}
+          if (j + 1 < n_kb) {
+            if (!issue_dp(g + 1)) { ok = false; break; }
+            if (j + 2 == n_kb) mma_commit(&do_empty);  // the tile's last dP
+          }
           // dQ += dS_j K_j : A = dS_j (16-bit in TMEM), B = K_j (MN-major)
           const uint32_t k_addr = smem_u32(smem + C::kK + st * C::kTileBytes);
 #pragma unroll
@@ -684,10 +690,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_ts(tmem + C::tDQ, tmem + C::tS + (g & 1) * 128 + a_col(kk),
                    sdesc_sw128(k_addr + kk * 2048, C::kSubBytes, 1024), id_q, (j > 0 || kk > 0) ? 1u : 0u);
           mma_commit(&k_empty[st]);
-          if (j + 1 < n_kb) {  // dP_j has been read into dS_j
-            if (!issue_dp(g + 1)) { ok = false; break; }
-            if (j + 2 == n_kb) mma_commit(&do_empty);  // the tile's last dP
-          }
           // buffer g&1 still holds dS_j, which the dQ_j MMA above reads first
           if (j + 2 < n_kb) {
             if (!issue_s(g + 2)) { ok = false; break; }
@@ -781,27 +783,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (ok) row_terms(k + 1, nl_next, drow_next);
       // epilogue: dQ = scale * accumulator; warpgroup h stores head columns
-      // [hD/2, hD/2 + D/2), 16 at a time
+      // [hD/2, hD/2 + D/2) with whole-line row-segment stores
       if (!ok || !mbar_wait_warp(&done, it & 1, &abort_flag)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      uint16_t *out = dq + (static_cast<size_t>(bh) * N + q) * D + h * (D / 2);
-#pragma unroll 1
-      for (int ch = 0; ch < D / 32; ++ch) {
-        uint32_t rr[16];
-        tmem_ld16(tmem + lane_addr + C::tDQ + h * (D / 2) + ch * 16, rr);
-        uint32_t pk2[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-          pk2[u] = E::pack(__uint_as_float(rr[2 * u]) * scale, __uint_as_float(rr[2 * u + 1]) * scale);
-        if (q < N) {
-          uint4 *d4 = reinterpret_cast<uint4 *>(out + ch * 16);
-          d4[0] = make_uint4(pk2[0], pk2[1], pk2[2], pk2[3]);
-          d4[1] = make_uint4(pk2[4], pk2[5], pk2[6], pk2[7]);
-        }
-      }
+      store_tmem_rows<E, D / 2>(tmem + lane_addr + C::tDQ + h * (D / 2), scale,
+                                dq + (static_cast<size_t>(bh) * N + q) * D + h * (D / 2), D, N - q);
       ++it;
     }
   }

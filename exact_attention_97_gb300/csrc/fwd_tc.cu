@@ -473,24 +473,9 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
       }
       tc_fence_after();
       const float inv_l = 1.f / l_sum;
-      const bool store = row < N;
-      uint16_t *orow = o + (static_cast<size_t>(bh) * N + row) * D;
-#pragma unroll 1
-      for (int ch = 0; ch < D / 32; ++ch) {
-        uint32_t r[32];
-        tmem_ld32(tmem_O + lane_addr + ch * 32, r);
-        uint32_t pk[16];
-#pragma unroll
-        for (int t = 0; t < 16; ++t)
-          pk[t] = E::pack(__uint_as_float(r[2 * t]) * inv_l, __uint_as_float(r[2 * t + 1]) * inv_l);
-        if (store) {
-          uint4 *dst = reinterpret_cast<uint4 *>(orow + ch * 32);
-#pragma unroll
-          for (int t = 0; t < 4; ++t)
-            dst[t] = make_uint4(pk[4 * t], pk[4 * t + 1], pk[4 * t + 2], pk[4 * t + 3]);
-        }
-      }
-      if (store) lse[static_cast<size_t>(bh) * N + row] = (m_used * scale_log2 + log2f(l_sum)) * kLn2;
+      // O = accumulator / l, whole-line row-segment stores
+      store_tmem_rows<E, D>(tmem_O + lane_addr, inv_l, o + (static_cast<size_t>(bh) * N + row) * D, D, N - row);
+      if (row < N) lse[static_cast<size_t>(bh) * N + row] = (m_used * scale_log2 + log2f(l_sum)) * kLn2;
     }
   };
   auto role_masks = [&]() {

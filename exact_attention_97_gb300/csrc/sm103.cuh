@@ -523,4 +523,70 @@ __device__ __forceinline__ void setmaxnreg_dec() {
 __device__ __forceinline__ int warp_id() { return threadIdx.x >> 5; }
 __device__ __forceinline__ int lane_id() { return threadIdx.x & 31; }
 
+// ------------------------------------------------------- row-segment stores
+// An accumulator read from TMEM leaves each lane holding one row, and the
+// rows of a warp are 32 consecutive rows of the output, so a plain store from
+// every lane writes 32 cache lines per instruction. These helpers first
+// exchange 16-byte chunks inside groups of NC lanes (an NC x NC transpose in
+// log2(NC) xor-shuffle stages), so that lane p of a group holds chunk p of each
+// of the group's NC rows; store i then writes row i of every group, 32 / NC
+// rows of NC * 16 contiguous bytes, whole 128-byte lines when NC = 8.
+
+// w[4c .. 4c+3] is chunk c of the calling lane's row, which starts at `row`;
+// rows are `stride` elements apart, and only rows less than `rows_left` past
+// the calling lane's own are written. All 32 lanes must call it.
+template <int NC>
+__device__ __forceinline__ void store_row_chunks(uint32_t (&w)[4 * NC], uint16_t *row, int stride,
+                                                 int rows_left) {
+  const int p = lane_id() & (NC - 1);
+#pragma unroll
+  for (int m = 1; m < NC; m <<= 1) {
+    // after this stage a lane's chunk k has row bit m from k and chunk bit m
+    // from the lane: the lanes whose bit m differs from k's swap chunk k
+    const bool up = (p & m) != 0;
+#pragma unroll
+    for (int k0 = 0; k0 < NC; ++k0) {
+      if (k0 & m) continue;
+      const int k1 = k0 | m;
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const uint32_t send = up ? w[4 * k0 + t] : w[4 * k1 + t];
+        const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, m);
+        if (up)
+          w[4 * k0 + t] = recv;
+        else
+          w[4 * k1 + t] = recv;
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < NC; ++i)
+    if (i - p < rows_left)
+      *reinterpret_cast<uint4 *>(row + (i - p) * stride + p * 8) =
+          make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+}
+
+// Columns [C0, COLS) of this lane's TMEM row (fp32, from taddr + C0), times
+// `mul`, packed to 16-bit by E and stored at row[C0 ..] as above, in pieces of
+// 64, 32 or 16 columns. COLS - C0 must be a multiple of 16.
+template <class E, int COLS, int C0 = 0>
+__device__ __forceinline__ void store_tmem_rows(uint32_t taddr, float mul, uint16_t *row, int stride,
+                                                int rows_left) {
+  if constexpr (C0 < COLS) {
+    constexpr int kRem = COLS - C0;
+    constexpr int kNC = kRem >= 64 ? 8 : kRem >= 32 ? 4 : 2;  // 16-byte chunks in this piece
+    uint32_t w[4 * kNC];
+#pragma unroll
+    for (int c = 0; c < 8 * kNC; c += 16) {
+      uint32_t rr[16];
+      tmem_ld16(taddr + C0 + c, rr);
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        w[c / 2 + u] = E::pack(__uint_as_float(rr[2 * u]) * mul, __uint_as_float(rr[2 * u + 1]) * mul);
+    }
+    store_row_chunks<kNC>(w, row + C0, stride, rows_left);
+    store_tmem_rows<E, COLS, C0 + 8 * kNC>(taddr, mul, row, stride, rows_left);
+  }
+}
+
 }  // namespace fa
