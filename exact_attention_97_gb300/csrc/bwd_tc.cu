@@ -502,7 +502,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
   __shared__ uint64_t q_full, q_empty, do_full, do_empty, k_full[KS], k_empty[KS], v_full[VS], v_empty[VS],
-      s_full[2], dp_full, ds_ready, done, drain;
+      s_full[2], dp_full, ds_ready[2], sfree[2], done, drain, drain_q;
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_flag;
 
@@ -535,9 +535,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&s_full[0], 1);
     mbar_init(&s_full[1], 1);
     mbar_init(&dp_full, 1);
-    mbar_init(&ds_ready, 256);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&ds_ready[b], 256);
+      mbar_init(&sfree[b], 1);
+    }
     mbar_init(&done, 1);
     mbar_init(&drain, 1);
+    mbar_init(&drain_q, 1);
     fence_mbar_init();
   }
   if (warp == 2) {
@@ -620,16 +624,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = max(0, g - VS); j < g; ++j) mbar_wait_drain(&v_full[j % VS], (j / VS) & 1);
     }
   } else if (warp == 1) {
-    // -------------------------------------------------------------- MMA issuer
-    // Per tile: S_0, dP_0, S_1, then per key block j: dP_{j+1}, dQ_j, S_{j+2}.
-    // The first dQ of a tile overwrites the accumulator: it waits for dS_0,
-    // which the elementwise warps only produce after storing the previous
-    // tile's dQ.
+    // ------------------------------------------------------ MMA issuer: S, dP
+    // Per tile: S_0, dP_0, S_1, then per key block j: dP_{j+1}, S_{j+2}. The
+    // dQ products come from warp 2, so neither thread's barrier waits leave
+    // the tensor pipe idle. Two issuing threads give no order between their
+    // MMAs: S_{g+2} reuses the buffer of dS_g and so waits for dQ_g to
+    // complete (sfree), and dP_{g+1} reuses the dP columns, which the
+    // elementwise warps have read once dS_g is ready.
     if (lane == 0) {
       constexpr uint32_t id_s = idesc_16(kBlk, kBlk, false, false, F16);  // S, dP
-      constexpr uint32_t id_q = idesc_16(kBlk, D, false, true, F16);      // dQ
       const uint32_t q_addr = smem_u32(smem + C::kQ), do_addr = smem_u32(smem + C::kDO);
       auto issue_s = [&](int gj) -> bool {  // S of global block gj = Q K^T into buffer gj&1
+        if (gj >= 2 && !mbar_wait(&sfree[gj & 1], ((gj >> 1) - 1) & 1, &abort_flag)) return false;
         const int st = gj % KS;
         if (!mbar_wait(&k_full[st], (gj / KS) & 1, &abort_flag)) return false;
         tc_fence_after();
@@ -674,34 +680,56 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (n_kb == 2) mma_commit(&q_empty);
         }
         for (int j = 0; j < n_kb; ++j, ++g) {
-          const int st = g % KS;
-          if (!mbar_wait(&ds_ready, g & 1, &abort_flag)) { ok = false; break; }
-          tc_fence_after();
-          // dP_j has been read into dS_j, so dP_{j+1} goes first: the
-          // elementwise warps' next dS then overlaps dQ_j and S_{j+2}
-          if (j + 1 < n_kb) {
+          if (!mbar_wait(&ds_ready[g & 1], (g >> 1) & 1, &abort_flag)) { ok = false; break; }
+          if (j + 1 < n_kb) {  // dP_j has been read into dS_j
+            tc_fence_after();
             if (!issue_dp(g + 1)) { ok = false; break; }
             if (j + 2 == n_kb) mma_commit(&do_empty);  // the tile's last dP
           }
-          // dQ += dS_j K_j : A = dS_j (16-bit in TMEM), B = K_j (MN-major)
-          const uint32_t k_addr = smem_u32(smem + C::kK + st * C::kTileBytes);
-#pragma unroll
-          for (int kk = 0; kk < kBlk / 16; ++kk)
-            mma_ts(tmem + C::tDQ, tmem + C::tS + (g & 1) * 128 + a_col(kk),
-                   sdesc_sw128(k_addr + kk * 2048, C::kSubBytes, 1024), id_q, (j > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(&k_empty[st]);
-          // buffer g&1 still holds dS_j, which the dQ_j MMA above reads first
           if (j + 2 < n_kb) {
             if (!issue_s(g + 2)) { ok = false; break; }
             if (j + 3 == n_kb) mma_commit(&q_empty);  // the tile's last S
           }
         }
         if (!ok) break;
-        mma_commit(&done);
         ++it;
       }
       mma_commit(&drain);
       mbar_wait_drain(&drain, 0);
+    }
+  } else if (warp == 2) {
+    // ---------------------------------------------------- MMA issuer: dQ
+    // dQ += dS_j K_j per key block (A = dS_j, 16-bit in TMEM; B = K_j
+    // MN-major). The first of a tile overwrites the accumulator: it waits for
+    // dS_0, which the elementwise warps only produce after storing the
+    // previous tile's dQ.
+    if (lane == 0) {
+      constexpr uint32_t id_q = idesc_16(kBlk, D, false, true, F16);
+      bool ok = true;
+      int g = 0, rank, bh;
+      for (int k = 0; ok; ++k) {
+        const int step = sched_item(sched, blockIdx.x, k, rank, bh);
+        if (step == kDone) break;
+        if (step == kSkip) continue;
+        const int n_kb = kblocks(qtile_of(rank));
+        for (int j = 0; j < n_kb; ++j, ++g) {
+          const int st = g % KS;
+          if (!mbar_wait(&ds_ready[g & 1], (g >> 1) & 1, &abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t k_addr = smem_u32(smem + C::kK + st * C::kTileBytes);
+#pragma unroll
+          for (int kk = 0; kk < kBlk / 16; ++kk)
+            mma_ts(tmem + C::tDQ, tmem + C::tS + (g & 1) * 128 + a_col(kk),
+                   sdesc_sw128(k_addr + kk * 2048, C::kSubBytes, 1024), id_q, (j > 0 || kk > 0) ? 1u : 0u);
+          // S_g completed before dS_g existed, so K_g is free once dQ_g is
+          mma_commit(&k_empty[st]);
+          mma_commit(&sfree[g & 1]);
+        }
+        if (!ok) break;
+        mma_commit(&done);
+      }
+      mma_commit(&drain_q);
+      mbar_wait_drain(&drain_q, 0);
     }
   } else if (warp >= 4) {
     // ------------------------------------------ P, dS (warpgroup h: keys 64h..64h+63 of a block)
@@ -779,7 +807,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_st32(tmem + lane_addr + sb, ds);  // over scores already read
         }
         tc_fence_before();
-        mbar_arrive(&ds_ready);
+        mbar_arrive(&ds_ready[g & 1]);
       }
       if (ok) row_terms(k + 1, nl_next, drow_next);
       // epilogue: dQ = scale * accumulator; warpgroup h stores head columns
