@@ -27,12 +27,17 @@
 //                  S = Q K^T (double-buffered), dP = dO V^T   (TMEM)
 //                  dQ += dS K     (dS read from TMEM in 16 bits)
 // In both passes two warpgroups split the 128 columns of S and dP (64 each)
-// for the elementwise work; one warp loads, one thread issues the MMAs. Both
-// passes are persistent: at most one CTA per SM walks a static list of items
-// (tile_sched.h), and the rings and barrier phases carry over from item to
-// item, so the next item's loads and first MMAs overlap the current item's
-// last products and its epilogue. The dK/dV pass writes its results through
-// per-warp shared-memory boxes and TMA stores. Head sizes 64, 96 and 128.
+// for the elementwise work and one warp loads. Two threads issue the MMAs:
+// one the products of scores (S, dP), the other the accumulating ones (dV
+// and dK, or dQ), so that the barrier waits of either leave the tensor pipe
+// fed by the other; a product that overwrites TMEM columns another thread's
+// MMA reads waits for that MMA to complete. Both passes are persistent: at
+// most one CTA per SM walks a static list of items (tile_sched.h), and the
+// rings and barrier phases carry over from item to item, so the next item's
+// loads and first MMAs overlap the current item's last products and its
+// epilogue. The dK/dV pass writes its results through per-warp shared-memory
+// boxes and TMA stores, the dQ pass with whole-line row-segment stores. Head
+// sizes 64, 96 and 128.
 // With dropout (DROP instances) both passes draw the keep bits of each tile
 // (Philox4x32-10, sm103.cuh) before its scores arrive: dV takes
 // P o Z / (1 - p), and dP is scaled by Z / (1 - p) before dS.
@@ -41,6 +46,7 @@
 #include <stdint.h>
 
 #include <algorithm>
+#include <type_traits>
 
 #include "kernels.h"
 #include "tile_sched.h"
@@ -373,26 +379,40 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t keep[2];  // dropout: keep bits of this key for the 64 queries, drawn while S^T is in flight
         if constexpr (DROP) dropout_col_bits<2>(drop, static_cast<uint32_t>(bh), key, q0, keep);
         if (!mbar_wait_warp(&qd_full[st], (g / NST) & 1, &abort_flag)) { ok = false; break; }
-        const float2 *L2 = reinterpret_cast<const float2 *>(Lst[st] + h * 64);
-        const float2 *D2 = reinterpret_cast<const float2 *>(Dst[st] + h * 64);
+        const float4 *L4 = reinterpret_cast<const float4 *>(Lst[st] + h * 64);
+        const float4 *D4 = reinterpret_cast<const float4 *>(Dst[st] + h * 64);
         if (!mbar_wait_warp(&s_full, ph, &abort_flag)) { ok = false; break; }
         tc_fence_after();
         uint32_t pk[32];
         {
           uint32_t r[64];
           tmem_ld64(tmem + lane_addr + C::tS + h * 64, r);
+          // P of query columns q0 + 2u, q0 + 2u + 1; the mask test only where
+          // some of this row's 64 columns are masked (diagonal tiles, padding)
+          auto p_pairs = [&](auto masked) {
 #pragma unroll
-          for (int u = 0; u < 32; ++u) {
-            const float2 nl = L2[u];
-            const uint64_t x2 =
-                f2_fma(f2_pack(__uint_as_float(r[2 * u]), __uint_as_float(r[2 * u + 1])), cc, f2_pack(nl.x, nl.y));
-            float x0, x1;
-            f2_unpack(x2, x0, x1);
-            float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-            if (q0 + 2 * u < qmin) p0 = 0.f;
-            if (q0 + 2 * u + 1 < qmin) p1 = 0.f;
-            pk[u] = E::pack(p0, p1);
-          }
+            for (int u2 = 0; u2 < 16; ++u2) {
+              const float4 nl = L4[u2];
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                const int u = 2 * u2 + e;
+                const uint64_t x2 = f2_fma(f2_pack(__uint_as_float(r[2 * u]), __uint_as_float(r[2 * u + 1])), cc,
+                                           e ? f2_pack(nl.z, nl.w) : f2_pack(nl.x, nl.y));
+                float x0, x1;
+                f2_unpack(x2, x0, x1);
+                float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+                if constexpr (decltype(masked)::value) {
+                  if (q0 + 2 * u < qmin) p0 = 0.f;
+                  if (q0 + 2 * u + 1 < qmin) p1 = 0.f;
+                }
+                pk[u] = E::pack(p0, p1);
+              }
+            }
+          };
+          if (q0 < qmin)
+            p_pairs(std::true_type{});
+          else
+            p_pairs(std::false_type{});
           if constexpr (DROP) {  // dV takes P o Z / (1 - p); pk keeps P for dS
             uint32_t pkd[32];
 #pragma unroll
@@ -417,17 +437,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld64(tmem + lane_addr + C::tDP + h * 64, r);
           uint32_t ds[32];
 #pragma unroll
-          for (int u = 0; u < 32; ++u) {
-            const float2 dd = D2[u];
-            float dp0 = __uint_as_float(r[2 * u]), dp1 = __uint_as_float(r[2 * u + 1]);
-            if constexpr (DROP) {  // dP = (dO V^T) o Z / (1 - p)
-              const uint32_t kb = keep[u >> 4] >> ((2 * u) & 31);
-              dp0 = (kb & 1u) ? dp0 * drop.inv_keep : 0.f;
-              dp1 = (kb & 2u) ? dp1 * drop.inv_keep : 0.f;
+          for (int u2 = 0; u2 < 16; ++u2) {
+            const float4 dd = D4[u2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int u = 2 * u2 + e;
+              float dp0 = __uint_as_float(r[2 * u]), dp1 = __uint_as_float(r[2 * u + 1]);
+              if constexpr (DROP) {  // dP = (dO V^T) o Z / (1 - p)
+                const uint32_t kb = keep[u >> 4] >> ((2 * u) & 31);
+                dp0 = (kb & 1u) ? dp0 * drop.inv_keep : 0.f;
+                dp1 = (kb & 2u) ? dp1 * drop.inv_keep : 0.f;
+              }
+              const float d0 = E::lo(pk[u]) * (dp0 - (e ? dd.z : dd.x));
+              const float d1 = E::hi(pk[u]) * (dp1 - (e ? dd.w : dd.y));
+              ds[u] = E::pack(d0, d1);
             }
-            const float d0 = E::lo(pk[u]) * (dp0 - dd.x);
-            const float d1 = E::hi(pk[u]) * (dp1 - dd.y);
-            ds[u] = E::pack(d0, d1);
           }
           tmem_st32(tmem + lane_addr + C::tDP + h * 64, ds);
         }
