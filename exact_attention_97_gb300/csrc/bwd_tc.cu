@@ -448,8 +448,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 dp0 = (kb & 1u) ? dp0 * drop.inv_keep : 0.f;
                 dp1 = (kb & 2u) ? dp1 * drop.inv_keep : 0.f;
               }
-              const float d0 = E::lo(pk[u]) * (dp0 - (e ? dd.z : dd.x));
-              const float d1 = E::hi(pk[u]) * (dp1 - (e ? dd.w : dd.y));
+              float d0, d1;  // P (dP - D), two lanes at a time
+              f2_unpack(f2_mul(f2_pack(E::lo(pk[u]), E::hi(pk[u])),
+                               f2_sub(f2_pack(dp0, dp1), e ? f2_pack(dd.z, dd.w) : f2_pack(dd.x, dd.y))),
+                        d0, d1);
               ds[u] = E::pack(d0, d1);
             }
           }
@@ -806,7 +808,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int qt = qtile_of(rank), n_kb = kblocks(qt);
       const int q = qt * kBlk + r;
       const float nl = nl_next, drow = drow_next;
-      const uint64_t nn = f2_pack(nl, nl);
+      const uint64_t nn = f2_pack(nl, nl), dd2 = f2_pack(drow, drow);
       const int kvis = causal ? min(Nk, q + 1 + off) : Nk;  // keys below kvis are visible
       for (int j = 0; j < n_kb; ++j, ++g) {
         const uint32_t sb = C::tS + (g & 1) * 128 + h * 64;
@@ -847,8 +849,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               dp0 = (kb & 1u) ? dp0 * drop.inv_keep : 0.f;
               dp1 = (kb & 2u) ? dp1 * drop.inv_keep : 0.f;
             }
-            const float d0 = p[2 * u] * (dp0 - drow);
-            const float d1 = p[2 * u + 1] * (dp1 - drow);
+            float d0, d1;  // p (dP - D), two lanes at a time
+            f2_unpack(f2_mul(f2_pack(p[2 * u], p[2 * u + 1]), f2_sub(f2_pack(dp0, dp1), dd2)), d0, d1);
             ds[u] = E::pack(d0, d1);
           }
           tmem_st32(tmem + lane_addr + sb, ds);  // over scores already read
