@@ -384,6 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait_warp(&s_full, ph, &abort_flag)) { ok = false; break; }
         tc_fence_after();
         uint32_t pk[32];
+        float pf[64];  // P in fp32, for dS
         {
           uint32_t r[64];
           tmem_ld64(tmem + lane_addr + C::tS + h * 64, r);
@@ -405,7 +406,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                   if (q0 + 2 * u < qmin) p0 = 0.f;
                   if (q0 + 2 * u + 1 < qmin) p1 = 0.f;
                 }
-                pk[u] = E::pack(p0, p1);
+                pf[2 * u] = p0;
+                pf[2 * u + 1] = p1;
+                if constexpr (!DROP) pk[u] = E::pack(p0, p1);
               }
             }
           };
@@ -413,22 +416,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             p_pairs(std::true_type{});
           else
             p_pairs(std::false_type{});
-          if constexpr (DROP) {  // dV takes P o Z / (1 - p); pk keeps P for dS
-            uint32_t pkd[32];
+          if constexpr (DROP) {  // dV takes P o Z / (1 - p); dS takes P
 #pragma unroll
             for (int u = 0; u < 32; ++u) {
               const uint32_t kb = keep[u >> 4] >> ((2 * u) & 31);
-              pkd[u] = E::pack((kb & 1u) ? E::lo(pk[u]) * drop.inv_keep : 0.f,
-                               (kb & 2u) ? E::hi(pk[u]) * drop.inv_keep : 0.f);
+              pk[u] = E::pack((kb & 1u) ? pf[2 * u] * drop.inv_keep : 0.f,
+                              (kb & 2u) ? pf[2 * u + 1] * drop.inv_keep : 0.f);
             }
-            tmem_st32(tmem + lane_addr + C::tS + h * 64, pkd);
+            tmem_st32(tmem + lane_addr + C::tS + h * 64, pk);
           } else {
             tmem_st32(tmem + lane_addr + C::tS + h * 64, pk);
           }
         }
         tc_fence_before();
         mbar_arrive(&p_ready);
-        // dS^T = P^T o (dP^T - D), with P as rounded for dV; written in 16 bits
+        // dS^T = P^T o (dP^T - D); written in 16 bits
         // pairs over the dP^T columns this warpgroup has just read
         if (!mbar_wait_warp(&dp_full, ph, &abort_flag)) { ok = false; break; }
         tc_fence_after();
@@ -449,7 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 dp1 = (kb & 2u) ? dp1 * drop.inv_keep : 0.f;
               }
               float d0, d1;  // P (dP - D), two lanes at a time
-              f2_unpack(f2_mul(f2_pack(E::lo(pk[u]), E::hi(pk[u])),
+              f2_unpack(f2_mul(f2_pack(pf[2 * u], pf[2 * u + 1]),
                                f2_sub(f2_pack(dp0, dp1), e ? f2_pack(dd.z, dd.w) : f2_pack(dd.x, dd.y))),
                         d0, d1);
               ds[u] = E::pack(d0, d1);
