@@ -32,7 +32,8 @@
 //               moved when it grows by more than 2^8: any common base leaves
 //               u/l unchanged (tutorial section 02), so the O rescale in TMEM
 //               (ld, multiply, st) is skipped on most tiles. The epilogue
-//               divides by l, stores O and L = m*scale + ln l.
+//               divides by l and stores O with whole-line row-segment stores
+//               (store_tmem_rows, sm103.cuh), then L = m*scale + ln l.
 //   warps 8-11  (dropout instances only) draw each tile's keep bits
 //               (Philox4x32-10, sm103.cuh) into a shared ring one tile ahead;
 //               the softmax warps scale the kept P by 1 / (1 - p) for P V
