@@ -145,7 +145,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
   __shared__ uint64_t k_full, k_empty, v_full, v_empty, qd_full[NST], qd_empty[NST], s_full, dp_full, p_ready,
-      ds_ready, p_free, ds_free, done, drain, drain_kv;
+      ds_ready, done, drain, drain_kv;
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_flag;
   __shared__ __align__(16) float Lst[NST][kBlk], Dst[NST][kBlk];  // per stage, by bulk copy
@@ -167,15 +167,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&v_empty, 1);
     for (int s = 0; s < NST; ++s) {
       mbar_init(&qd_full[s], 1);
-      mbar_init(&qd_empty[s], 1);
+      mbar_init(&qd_empty[s], 2);  // the two issuing threads' last readers of the stage
     }
     mbar_init(&s_full, 1);
     mbar_init(&dp_full, 1);
     mbar_init(&p_ready, 256);
     mbar_init(&ds_ready, 256);
-    mbar_init(&p_free, 1);
-    mbar_init(&ds_free, 1);
-    mbar_init(&done, 1);
+    mbar_init(&done, 2);  // dV and dK, from the two issuing threads
     mbar_init(&drain, 1);
     mbar_init(&drain_kv, 1);
     fence_mbar_init();
@@ -249,17 +247,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int t = max(0, g - NST); t < g; ++t) mbar_wait_drain(&qd_full[t % NST], (t / NST) & 1);
     }
   } else if (warp == 1) {
-    // -------------------------------------------------- MMA issuer: S^T, dP^T
-    // S^T of tile t+1 overwrites the columns where P_t waits for dV_t, and
-    // dP^T of t+1 those where dS_t waits for dK_t; dV and dK come from warp 2,
-    // so these wait for that product to complete (p_free, ds_free) rather
-    // than relying on issue order. Neither thread's barrier waits then leave
-    // the tensor pipe idle.
+    // ------------------------------------------------ MMA issuer: S^T and dV
+    // Two threads issue, one per chain of products that reuse TMEM columns:
+    // this one S^T_t and dV_t (P_t is written over S^T_t's columns, and
+    // S^T_{t+1} overwrites them after dV_t has read them), warp 2 dP^T_t and
+    // dK_t (likewise with dS_t over dP^T_t). Within a thread, issue order is
+    // execution order, so a product that overwrites columns follows their
+    // reader without waiting for it to complete; the two chains share no
+    // TMEM columns. Q and dO stages are released by both threads (qd_empty
+    // counts two), and the block's accumulators are done once both are.
     if (lane == 0) {
-      constexpr uint32_t id_s = idesc_16(kBlk, kBlk, false, false, F16);  // S^T, dP^T
-      const uint32_t k_addr = smem_u32(smem + C::kK), v_addr = smem_u32(smem + C::kV);
+      constexpr uint32_t id_s = idesc_16(kBlk, kBlk, false, false, F16);  // S^T
+      constexpr uint32_t id_kv = idesc_16(kBlk, D, false, true, F16);     // dV
+      const uint32_t k_addr = smem_u32(smem + C::kK);
       auto issue_s = [&](int gt) -> bool {  // S^T = K Q^T of global tile gt
-        if (gt > 0 && !mbar_wait(&p_free, (gt - 1) & 1, &abort_flag)) return false;
         const int st = gt % NST;
         if (!mbar_wait(&qd_full[st], (gt / NST) & 1, &abort_flag)) return false;
         tc_fence_after();
@@ -273,10 +274,49 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(&s_full);
         return true;
       };
-      auto issue_dp = [&](int gt) -> bool {  // dP^T = V dO^T (tile gt has landed: its S^T waited)
-        if (gt > 0 && !mbar_wait(&ds_free, (gt - 1) & 1, &abort_flag)) return false;
+      bool ok = true;
+      int g = 0, it = 0, kb, bh;
+      for (int k = 0; ok; ++k) {
+        const int step = sched_item(sched, blockIdx.x, k, kb, bh);
+        if (step == kDone) break;
+        if (step == kSkip) continue;
+        const int n_tiles = n_tiles_all - first_tile(kb);
+        if (!mbar_wait(&k_full, it & 1, &abort_flag) || !issue_s(g)) break;
+        if (n_tiles == 1) mma_commit(&k_empty);
+        for (int t = 0; t < n_tiles; ++t, ++g) {
+          const int st = g % NST;
+          const uint32_t do_addr = smem_u32(smem + C::kDO + st * C::kTileBytes);
+          // dV += P^T dO
+          if (!mbar_wait(&p_ready, g & 1, &abort_flag)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < kBlk / 16; ++kk)
+            mma_ts(tmem + C::tDV, tmem + C::tS + a_col(kk), sdesc_sw128(do_addr + kk * 2048, C::kSubBytes, 1024),
+                   id_kv, (t > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(&qd_empty[st]);  // S^T_t completed before P_t existed; dV_t read dO_t
+          if (t + 1 < n_tiles) {      // over the columns dV_t has just read
+            if (!issue_s(g + 1)) { ok = false; break; }
+            if (t + 2 == n_tiles) mma_commit(&k_empty);  // the block's last S^T
+          }
+        }
+        if (!ok) break;
+        mma_commit(&done);
+        ++it;
+      }
+      mma_commit(&drain);
+      mbar_wait_drain(&drain, 0);
+    }
+  } else if (warp == 2) {
+    // ------------------------------------------------ MMA issuer: dP^T and dK
+    if (lane == 0) {
+      constexpr uint32_t id_s = idesc_16(kBlk, kBlk, false, false, F16);  // dP^T
+      constexpr uint32_t id_kv = idesc_16(kBlk, D, false, true, F16);     // dK
+      const uint32_t v_addr = smem_u32(smem + C::kV);
+      auto issue_dp = [&](int gt) -> bool {  // dP^T = V dO^T of global tile gt
+        const int st = gt % NST;
+        if (!mbar_wait(&qd_full[st], (gt / NST) & 1, &abort_flag)) return false;
         tc_fence_after();
-        const uint32_t do_addr = smem_u32(smem + C::kDO + (gt % NST) * C::kTileBytes);
+        const uint32_t do_addr = smem_u32(smem + C::kDO + st * C::kTileBytes);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk / 4) * C::kSubBytes + (kk % 4) * 32;
@@ -293,63 +333,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (step == kDone) break;
         if (step == kSkip) continue;
         const int n_tiles = n_tiles_all - first_tile(kb);
-        if (!mbar_wait(&k_full, it & 1, &abort_flag) || !issue_s(g)) break;
-        if (n_tiles == 1) mma_commit(&k_empty);
         if (!mbar_wait(&v_full, it & 1, &abort_flag) || !issue_dp(g)) break;
         if (n_tiles == 1) mma_commit(&v_empty);
-        for (int t = 0; t + 1 < n_tiles; ++t, ++g) {
-          if (!issue_s(g + 1)) { ok = false; break; }
-          if (t + 2 == n_tiles) mma_commit(&k_empty);  // the block's last S^T
-          if (!issue_dp(g + 1)) { ok = false; break; }
-          if (t + 2 == n_tiles) mma_commit(&v_empty);  // the block's last dP^T
-        }
-        if (!ok) break;
-        ++g;  // the block's last tile
-        ++it;
-      }
-      mma_commit(&drain);
-      mbar_wait_drain(&drain, 0);
-    }
-  } else if (warp == 2) {
-    // ------------------------------------------------------ MMA issuer: dV, dK
-    // Per tile t: dV_t += P_t^T dO_t once P_t is in TMEM, dK_t += dS_t^T Q_t
-    // once dS_t is. The first of a block overwrite the accumulators: they
-    // wait for P_0 and dS_0, which the elementwise warps only produce after
-    // storing the previous block's dV and dK.
-    if (lane == 0) {
-      constexpr uint32_t id_kv = idesc_16(kBlk, D, false, true, F16);  // dV, dK
-      bool ok = true;
-      int g = 0, kb, bh;
-      for (int k = 0; ok; ++k) {
-        const int step = sched_item(sched, blockIdx.x, k, kb, bh);
-        if (step == kDone) break;
-        if (step == kSkip) continue;
-        const int n_tiles = n_tiles_all - first_tile(kb);
         for (int t = 0; t < n_tiles; ++t, ++g) {
           const int st = g % NST;
-          const uint32_t ph = g & 1;
           const uint32_t q_addr = smem_u32(smem + C::kQ + st * C::kTileBytes);
-          const uint32_t do_addr = smem_u32(smem + C::kDO + st * C::kTileBytes);
-          if (!mbar_wait(&p_ready, ph, &abort_flag)) { ok = false; break; }
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < kBlk / 16; ++kk)
-            mma_ts(tmem + C::tDV, tmem + C::tS + a_col(kk), sdesc_sw128(do_addr + kk * 2048, C::kSubBytes, 1024),
-                   id_kv, (t > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(&p_free);
-          if (!mbar_wait(&ds_ready, ph, &abort_flag)) { ok = false; break; }
+          // dK += dS^T Q
+          if (!mbar_wait(&ds_ready, g & 1, &abort_flag)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < kBlk / 16; ++kk)
             mma_ts(tmem + C::tDK, tmem + C::tDP + a_col(kk), sdesc_sw128(q_addr + kk * 2048, C::kSubBytes, 1024),
                    id_kv, (t > 0 || kk > 0) ? 1u : 0u);
-          // S^T_t and dP^T_t completed before P_t and dS_t existed; this
-          // commit covers dV_t and dK_t, the tile's last readers of Q and dO
-          mma_commit(&qd_empty[st]);
-          mma_commit(&ds_free);
+          mma_commit(&qd_empty[st]);  // dP^T_t completed before dS_t existed; dK_t read Q_t
+          if (t + 1 < n_tiles) {      // over the columns dK_t has just read
+            if (!issue_dp(g + 1)) { ok = false; break; }
+            if (t + 2 == n_tiles) mma_commit(&v_empty);  // the block's last dP^T
+          }
         }
         if (!ok) break;
         mma_commit(&done);
+        ++it;
       }
       mma_commit(&drain_kv);
       mbar_wait_drain(&drain_kv, 0);
