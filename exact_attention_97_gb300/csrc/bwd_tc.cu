@@ -27,17 +27,17 @@
 //                  S = Q K^T (double-buffered), dP = dO V^T   (TMEM)
 //                  dQ += dS K     (dS read from TMEM in 16 bits)
 // In both passes two warpgroups split the 128 columns of S and dP (64 each)
-// for the elementwise work and one warp loads. Two threads issue the MMAs:
-// one the products of scores (S, dP), the other the accumulating ones (dV
-// and dK, or dQ), so that the barrier waits of either leave the tensor pipe
-// fed by the other; a product that overwrites TMEM columns another thread's
-// MMA reads waits for that MMA to complete. Both passes are persistent: at
-// most one CTA per SM walks a static list of items (tile_sched.h), and the
-// rings and barrier phases carry over from item to item, so the next item's
-// loads and first MMAs overlap the current item's last products and its
-// epilogue. The dK/dV pass writes its results through per-warp shared-memory
-// boxes and TMA stores, the dQ pass with whole-line row-segment stores. Head
-// sizes 64, 96 and 128.
+// for the elementwise work and one warp loads. Two threads issue the MMAs,
+// so that the barrier waits of either leave the tensor pipe fed by the
+// other: in the dK/dV pass one per chain of products that reuse TMEM columns
+// (S^T and dV; dP^T and dK), in the dQ pass one for S and dP and one for dQ,
+// where S_{j+2} waits for dQ_j to complete before overwriting dS_j. Both
+// passes are persistent: at most one CTA per SM walks a static list of items
+// (tile_sched.h), and the rings and barrier phases carry over from item to
+// item, so the next item's loads and first MMAs overlap the current item's
+// last products and its epilogue. The dK/dV pass writes its results through
+// per-warp shared-memory boxes and TMA stores, the dQ pass with whole-line
+// row-segment stores. Head sizes 64, 96 and 128.
 // With dropout (DROP instances) both passes draw the keep bits of each tile
 // (Philox4x32-10, sm103.cuh) before its scores arrive: dV takes
 // P o Z / (1 - p), and dP is scaled by Z / (1 - p) before dS.
