@@ -33,10 +33,10 @@ if ROOT not in sys.path:
 METRIC = "attention fwd/bwd TFLOP/s at B8 H32 N4096 d128 bf16; % of BF16 tensor peak"
 METRIC_FWD = "attention forward TFLOP/s (forward-only run of the workload in config); % of BF16 tensor peak"
 
-# DRAM bytes per launch of the dominant kernel at the headline size, from the
-# ncu capture summarised in profiles/ncu_full_fwd_dkdv_dq_bf16_B2_H32_N4096_d128.md
-# (a quarter-size case, scaled by the number of heads). Only valid for the
-# kernel source it was measured on: reported as null once that file changes.
+# DRAM bytes per launch of the dominant kernel at the headline size, from an
+# ncu capture of a quarter-size case of the same kernel (the traffic scales
+# with the number of heads). Only valid for the kernel source it was measured
+# on: reported as null once that file changes.
 MEASURED_TRAFFIC = {"workload": "bf16_B8_H32_N4096_d128", "kernel": "bwd_dkdv_kernel<128>",
                     "bytes": 4 * (270.937088e6 + 103.252480e6),
                     "source": "exact_attention_97_gb300/csrc/bwd_tc.cu", "sha256_16": "90c6224de6860c6d"}
@@ -121,6 +121,25 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def _host_info(local: int):
+    """Where the host side sits relative to the GPU (for reading e2e copy rates)."""
+    info = {"cpus_in_affinity": len(os.sched_getaffinity(0))}
+    try:
+        bus = subprocess.run(["nvidia-smi", f"--id={local}", "--query-gpu=pci.bus_id", "--format=csv,noheader"],
+                             capture_output=True, text=True, timeout=10).stdout.strip() or None
+        if bus:
+            dom = bus.lower()
+            if dom.count(":") == 2 and len(dom.split(":")[0]) == 8:
+                dom = dom[4:]
+            path = f"/sys/bus/pci/devices/{dom}/numa_node"
+            if os.path.exists(path):
+                info["gpu_numa_node"] = int(open(path).read().strip())
+            info["gpu_pci_bus_id"] = bus
+    except Exception as exc:  # informational only
+        info["error"] = str(exc)[:100]
+    return info
+
+
 def _dist():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -150,6 +169,43 @@ def cpu_baseline(w, heads: int):
             "kind": "oracle",
             "sample": f"{heads} whole heads (full N={w.N}, Nk={w.n_keys}, d={w.d}) of the workload, fwd+bwd, "
                       f"fp64, {dt_s:.1f} s wall"}
+
+
+def cpu_baseline_sampled_rows(w, rows: int = 256):
+    """Oracle on `rows` seeded query rows of a workload too large for whole
+    heads (the long causal one): O, L and dQ of each sampled row, as the parity
+    test computes them. The rate counts the flops those rows execute (S, O, dP
+    and dQ: 8 d per visible (query, key) pair); the full problem's time is a
+    linear extrapolation of its algorithmic flops at that rate."""
+    import torch
+
+    import oracle
+    from exact_attention_97_gb300.inputs import make_qkv_do, sample_indices
+
+    dt = torch.float16 if w.dtype == "f16" else torch.bfloat16
+    q, k, v, dO = make_qkv_do(w.B, w.H, w.N, w.d, w.seed, dt)
+    flat = sample_indices(w.B * w.H * w.N, rows, seed=5).numpy()
+    by_head = {}
+    for idx in flat:
+        by_head.setdefault(int(idx // w.N), []).append(int(idx % w.N))
+    oracle.build()
+    f64 = lambda t: t.float().double().numpy()  # noqa: E731
+    off = w.n_keys - w.N
+    t_total, flops = 0.0, 0.0
+    for bh, rr in by_head.items():
+        b, h = divmod(bh, w.H)
+        qh, kh, vh, doh = (f64(x[b, h]) for x in (q, k, v, dO))
+        t0 = time.perf_counter()
+        oracle.query_rows(qh, kh, vh, doh, rr, w.scale, w.causal)
+        t_total += time.perf_counter() - t0
+        flops += sum(8.0 * w.d * (min(w.n_keys, i + 1 + off) if w.causal else w.n_keys) for i in rr)
+    rate = flops / t_total
+    full = w.flops_fwd() + w.flops_bwd()
+    return {"value": rate / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{rows} seeded query rows of {w.name} (O, L, dQ at full N={w.N}), fp64, "
+                      f"{t_total:.2f} s wall; rate = executed flops (8 d per visible pair) / time",
+            "full_problem_s_extrapolated": full / rate,
+            "extrapolation": "linear: the workload's fwd+bwd algorithmic flops at the sample's rate"}
 
 
 def run_reference(args, w):
@@ -255,6 +311,7 @@ def run_ours(args, w):
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
+    torch.cuda.reset_peak_memory_stats(dev)
     sampler.start()
     time.sleep(0.3)
     fa.fa_set_kernel_timing(handles, pairs)
@@ -271,6 +328,7 @@ def run_ours(args, w):
     if fa.fa_device_status() != 0:
         raise RuntimeError("kernel pipeline timeout in the timed region")
     ms = start.elapsed_time(stop)
+    peak_mem = torch.cuda.max_memory_allocated(dev)
 
     def pair_ms(i):
         return statistics.mean(evs[2 * (per * s + i)].elapsed_time(evs[2 * (per * s + i) + 1])
@@ -283,6 +341,7 @@ def run_ours(args, w):
     # the headline value keeps the whole timed region
     fwd_call = statistics.median(m[0].elapsed_time(m[1]) for m in marks)
     bwd_call = None if args.fwd_only else statistics.median(m[1].elapsed_time(m[2]) for m in marks)
+    step_ms = sorted(m[0].elapsed_time(m[2]) for m in marks)  # whole step, per timed step
     ms = max_over_ranks(ms, dev)
 
     flops_step = w.flops_fwd() + (0 if args.fwd_only else w.flops_bwd())
@@ -325,6 +384,16 @@ def run_ours(args, w):
     fwd_tf = tf(w.flops_fwd(), fwd_call)
     bwd_tf = None if args.fwd_only else tf(w.flops_bwd(), bwd_call)
 
+    def quantile(xs, p):  # nearest-rank on sorted values
+        return xs[min(len(xs) - 1, max(0, int(round(p * (len(xs) - 1)))))]
+    spread = {"ms_median": statistics.median(step_ms), "ms_p10": quantile(step_ms, 0.1),
+              "ms_p90": quantile(step_ms, 0.9),
+              "value_median": tf(flops_step, statistics.median(step_ms)) * world,
+              "value_p10": tf(flops_step, quantile(step_ms, 0.9)) * world,
+              "value_p90": tf(flops_step, quantile(step_ms, 0.1)) * world,
+              "note": "per timed step, fwd start to bwd end on the launch stream (rank 0); value_p10 is "
+                      "the 10th-percentile throughput (from the 90th-percentile step time)"}
+
     # end to end through the public API: pinned host inputs in, results back to pinned host.
     # The training step goes through attention_step_host, which streams chunks of heads
     # through the GPU (copy in, compute, copy out on three streams).
@@ -365,13 +434,47 @@ def run_ours(args, w):
         bytes_in = sum(t.numel() * t.element_size() for t in ((q_h, k_h, v_h) if args.fwd_only else
                                                                 (q_h, k_h, v_h, do_h)))
         bytes_out = sum(t.numel() * t.element_size() for t in out_h)
+        # the link alone: each direction timed by itself on the same pinned
+        # buffers (whole tensors, one copy each), so the e2e time can be read
+        # against its copy-bound floor
+        ins_h = (q_h, k_h, v_h) if args.fwd_only else (q_h, k_h, v_h, do_h)
+        dev_in = [torch.empty_like(t, device=dev) for t in ins_h]
+        dev_out = [torch.empty_like(t, device=dev) for t in out_h]
+
+        def timed_copies(pairs, reps=3):
+            best = None
+            for _ in range(reps):
+                a2, b2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a2.record(stream)
+                for dst, src in pairs:
+                    dst.copy_(src, non_blocking=True)
+                b2.record(stream)
+                torch.cuda.synchronize()
+                t = a2.elapsed_time(b2)
+                best = t if best is None else min(best, t)
+            return best
+        h2d_ms = timed_copies(list(zip(dev_in, ins_h)))
+        d2h_ms = timed_copies(list(zip(out_h, dev_out)))
+        del dev_in, dev_out
+        h2d_gbs, d2h_gbs = bytes_in / (h2d_ms * 1e-3) / 1e9, bytes_out / (d2h_ms * 1e-3) / 1e9
         e2e = {"value": flops_step * world * e2e_steps / (ems * 1e-3) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": bytes_in, "d2h_bytes_per_step": bytes_out,
-               "ms_per_step": ems / e2e_steps}
+               "ms_per_step": ems / e2e_steps,
+               "h2d_gbs_alone": h2d_gbs, "d2h_gbs_alone": d2h_gbs,
+               "copy_ms_alone": {"h2d": h2d_ms, "d2h": d2h_ms},
+               "floor_ms": max(h2d_ms, d2h_ms, ms / args.steps),
+               "floor_note": "the step cannot beat the slower of: all inputs in, all outputs out (each at the "
+                             "bandwidth measured alone), the device-resident step; the chunked pipeline "
+                             "overlaps the three",
+               "host": _host_info(local)}
 
-    base = None
+    base, base_long = None, None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.fwd_only and not args.dropout:
         base = cpu_baseline(w, args.cpu_heads)
+        if not args.shape and not args.workload:
+            from exact_attention_97_gb300.inputs import WORKLOADS
+            wl = WORKLOADS["bf16_causal_B1_H32_N65536_d128"]
+            base_long = {wl.name: cpu_baseline_sampled_rows(wl)}
 
     if rank == 0:
         line = {
@@ -391,6 +494,11 @@ def run_ours(args, w):
             "roofline": roofline,
             "hbm": hbm,
             "cpu_baseline": base,
+            "cpu_baseline_other_workloads": base_long,
+            "spread": spread,
+            "peak_mem_bytes": peak_mem,
+            "peak_mem_note": "torch.cuda.max_memory_allocated over the timed region: inputs, outputs and the "
+                             f"backward workspace ({need} bytes); the library allocates nothing itself",
             "e2e": e2e,
             "gpu_launches": launches[0],
             "clocks": clocks,

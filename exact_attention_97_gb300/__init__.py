@@ -15,15 +15,18 @@ from __future__ import annotations
 
 import math
 
+import threading
+
 from ._lib import (FA_BF16, FA_F16, FA_F32, FAError, fa_bwd, fa_bwd_dropout, fa_bwd_f16, fa_bwd_f32, fa_bwd_kv,
                    fa_bwd_workspace_size, fa_device_status, fa_fwd, fa_fwd_dropout, fa_fwd_f16, fa_fwd_f32,
-                   fa_fwd_kv, fa_last_launch_count, fa_set_kernel_timing, fa_status_string, lib_path, load)
+                   fa_fwd_kv, fa_last_launch_count, fa_set_kernel_timing, fa_status_async, fa_status_string,
+                   fa_status_word, lib_path, load)
 
 __all__ = [
     "FA_BF16", "FA_F16", "FA_F32", "FAError", "fa_fwd", "fa_bwd", "fa_fwd_f16", "fa_bwd_f16",
     "fa_fwd_f32", "fa_bwd_f32", "fa_fwd_kv", "fa_bwd_kv", "fa_fwd_dropout", "fa_bwd_dropout",
     "fa_bwd_workspace_size", "fa_status_string", "fa_device_status", "fa_last_launch_count",
-    "fa_set_kernel_timing",
+    "fa_set_kernel_timing", "fa_status_async", "fa_status_word",
     "attention_forward", "attention_backward", "attention_step_host", "lib_path", "load",
 ]
 
@@ -50,8 +53,26 @@ def _stream_handle(stream):
     return s.cuda_stream
 
 
+_status_buf = threading.local()
+
+
+def _check_status(fn, stream):
+    """check=True: read the device status word on the call's stream (into a
+    per-thread page-locked int), wait for the stream, raise on a timeout."""
+    torch = _torch()
+    buf = getattr(_status_buf, "t", None)
+    if buf is None:
+        buf = _status_buf.t = torch.zeros(1, dtype=torch.int32).pin_memory()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    fa_status_async(buf.data_ptr(), s.cuda_stream)
+    s.synchronize()
+    st = int(buf[0])
+    if st != 0:
+        raise FAError(fn, st, fa_status_string(st))
+
+
 def attention_forward(q, k, v, scale=None, causal=False, out=None, lse=None, stream=None,
-                      dropout_p=0.0, seed=0, offset=0, head_base=0):
+                      dropout_p=0.0, seed=0, offset=0, head_base=0, check=False):
     """(O, L) for CUDA tensors q [B, H, Nq, d] and k, v [B, H, Nk, d] (all bf16, all f16 or all float32).
 
     bf16 and f16 need d in {64, 96, 128} (or 256 for the forward); float32 takes 1 <= d <= 128 and Nk == Nq. L is
@@ -61,6 +82,10 @@ def attention_forward(q, k, v, scale=None, causal=False, out=None, lse=None, str
     Philox mask of fa_fwd_dropout, keyed by (seed, offset) and the heads'
     global index (head_base + b * H + h); pass the same values to
     attention_backward.
+    check=True waits for the call's stream and raises FAError (status
+    FA_ERR_TIMEOUT) if a kernel of the library on this device gave up on a
+    pipeline wait since the status was last read; the results of such a call
+    are not valid.
     """
     torch = _torch()
     B, H, N, d = q.shape
@@ -92,13 +117,16 @@ def attention_forward(q, k, v, scale=None, causal=False, out=None, lse=None, str
         else:
             fn = {torch.bfloat16: fa_fwd, torch.float16: fa_fwd_f16, torch.float32: fa_fwd_f32}[dt]
             fn(*ptrs, B, H, N, d, scale, int(bool(causal)), _stream_handle(stream))
+        if check:
+            _check_status("attention_forward", stream)
     return o, lse
 
 
 def attention_backward(q, k, v, o, lse, dO, scale=None, causal=False, workspace=None, stream=None,
-                       grads=None, dropout_p=0.0, seed=0, offset=0, head_base=0):
+                       grads=None, dropout_p=0.0, seed=0, offset=0, head_base=0, check=False):
     """(dQ, dK, dV) for upstream gradient dO, given the forward's O and L (and
-    the forward's dropout_p, seed and offset)."""
+    the forward's dropout_p, seed and offset). check=True as for
+    attention_forward."""
     torch = _torch()
     B, H, N, d = q.shape
     Nk = k.shape[2]
@@ -133,6 +161,8 @@ def attention_backward(q, k, v, o, lse, dO, scale=None, causal=False, workspace=
         else:
             fn = {FA_BF16: fa_bwd, FA_F16: fa_bwd_f16, FA_F32: fa_bwd_f32}[kind]
             fn(*ptrs, B, H, N, d, scale, int(bool(causal)), *ws)
+        if check:
+            _check_status("attention_backward", stream)
     return dq, dk, dv
 
 

@@ -34,6 +34,8 @@ _SIGNATURES = {
     "fa_status_string": (ctypes.c_char_p, [c_int]),
     "fa_last_cuda_error": (c_int, []),
     "fa_device_status": (c_int, []),
+    "fa_status_async": (c_int, [c_void_p, c_void_p]),
+    "fa_status_word": (c_int, [ctypes.POINTER(c_void_p)]),
     "fa_last_launch_count": (c_int, []),
     "fa_set_kernel_timing": (c_int, [c_void_p, c_int]),
     "fa_bwd_static_scratch": (c_int, [c_void_p] * 9 + [c_int] * 4 + [c_float, c_int, c_void_p]),
@@ -143,6 +145,19 @@ def fa_status_string(status: int) -> str:
 
 def fa_device_status() -> int:
     return int(load().fa_device_status())
+
+
+def fa_status_async(dst, stream) -> int:
+    """Enqueue on `stream` a copy of the device status word into `dst` (a
+    device or page-locked host address) and clear the word; no synchronisation."""
+    return _call("fa_status_async", dst, stream)
+
+
+def fa_status_word() -> int:
+    """Device address of the current device's status word."""
+    p = c_void_p()
+    _call("fa_status_word", ctypes.byref(p))
+    return int(p.value or 0)
 
 
 def fa_last_launch_count() -> int:

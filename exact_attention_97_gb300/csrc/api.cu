@@ -26,14 +26,41 @@ thread_local int t_event_pairs = 0;
 thread_local int t_event_next = 0;
 
 constexpr int kMaxDevices = 64;
+// Per-device state, valid for one CUDA context: the status word's and the
+// static scratch's device addresses belong to the context that loaded this
+// library's module, so a new primary context (after cudaDeviceReset) makes
+// every entry look them up again (the epoch also re-arms set_smem_once).
 struct DeviceInfo {
   bool ready = false;
+  CUcontext ctx = nullptr;
   int ok_arch = 0;
   int num_sms = 0;
   int *status = nullptr;
+  unsigned char *scratch = nullptr;  // fa_bwd_static_scratch's array, looked up on first use
 };
 DeviceInfo g_dev[kMaxDevices];
+std::atomic<uint32_t> g_epoch[kMaxDevices];  // context epoch per device (0 = none yet)
+uint32_t g_epoch_next = 0;                   // under g_dev_mutex
 std::mutex g_dev_mutex;
+
+typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
+CtxGetCurrentFn g_ctx_get = nullptr;
+std::once_flag g_ctx_once;
+
+// The calling thread's current CUDA context (nullptr if none yet, or if the
+// driver entry point is unavailable).
+CUcontext current_context() {
+  std::call_once(g_ctx_once, [] {
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_get = reinterpret_cast<CtxGetCurrentFn>(fn);
+  });
+  CUcontext c = nullptr;
+  if (g_ctx_get && g_ctx_get(&c) != CUDA_SUCCESS) c = nullptr;
+  return c;
+}
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
@@ -47,8 +74,8 @@ int record(cudaError_t e) {
   return e == cudaSuccess ? kOk : kErrLaunch;
 }
 
-// Looks up (once per device) whether the current device is sm_103, its SM
-// count and the address of the status word.
+// Looks up whether the current device is sm_103, its SM count and the address
+// of the status word: once per device and context.
 int current_device(DeviceInfo **out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -56,6 +83,7 @@ int current_device(DeviceInfo **out) {
   if (dev < 0 || dev >= kMaxDevices) return kErrArch;
   std::lock_guard<std::mutex> lock(g_dev_mutex);
   DeviceInfo &d = g_dev[dev];
+  if (d.ready && d.ok_arch && current_context() != d.ctx) d.ready = false;  // the context was replaced
   if (!d.ready) {
     int major = 0, minor = 0, sms = 0;
     if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
@@ -64,11 +92,15 @@ int current_device(DeviceInfo **out) {
       return record(e);
     d.ok_arch = (major == 10 && minor == 3);
     d.num_sms = sms;
+    d.status = nullptr;
+    d.scratch = nullptr;
     if (d.ok_arch) {
-      void *p = nullptr;
+      void *p = nullptr;  // also brings up the context and this library's module
       if ((e = cudaGetSymbolAddress(&p, g_fa_status)) != cudaSuccess) return record(e);
       d.status = static_cast<int *>(p);
+      d.ctx = current_context();
     }
+    g_epoch[dev].store(++g_epoch_next, std::memory_order_release);
     d.ready = true;
   }
   if (!d.ok_arch) return kErrArch;
@@ -227,14 +259,15 @@ void timing_end(cudaStream_t stream) {
     ++t_event_next;
   }
 }
-cudaError_t set_smem_once(const void *kernel, int bytes, std::atomic<unsigned long long> *done) {
+cudaError_t set_smem_once(const void *kernel, int bytes, SmemOnce *done) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  const unsigned long long bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
-  if (bit && (done->load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  const bool known = dev >= 0 && dev < kMaxDevices;
+  const uint32_t epoch = known ? g_epoch[dev].load(std::memory_order_acquire) : 0u;
+  if (epoch != 0 && done->epoch[dev].load(std::memory_order_acquire) == epoch) return cudaSuccess;
   e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (e == cudaSuccess && bit) done->fetch_or(bit, std::memory_order_release);
+  if (e == cudaSuccess && epoch != 0) done->epoch[dev].store(epoch, std::memory_order_release);
   return e;
 }
 }  // namespace fa
@@ -273,6 +306,27 @@ size_t fa_bwd_workspace_size(int B, int H, int N, int d, int dtype) {
   if (dtype != FA_BF16 && dtype != FA_F32 && dtype != FA_F16) return 0;
   if (dtype == FA_F16) dtype = FA_BF16;  // same layout
   return ws_bytes(B, H, N, d, dtype);
+}
+
+int fa_status_async(int *dst, fa_stream_t stream) {
+  if (!dst) return FA_ERR_NULL;
+  if (!aligned(dst, 4)) return FA_ERR_ALIGN;
+  DeviceInfo *dev = nullptr;
+  int st = current_device(&dev);
+  if (st != kOk) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(dst, dev->status, sizeof(int), cudaMemcpyDefault, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(dev->status, 0, sizeof(int), s);
+  return e == cudaSuccess ? FA_OK : record(e);
+}
+
+int fa_status_word(int **dev_ptr) {
+  if (!dev_ptr) return FA_ERR_NULL;
+  DeviceInfo *dev = nullptr;
+  int st = current_device(&dev);
+  if (st != kOk) return st;
+  *dev_ptr = dev->status;
+  return FA_OK;
 }
 
 int fa_device_status(void) {
@@ -501,23 +555,21 @@ namespace {
 
 static __device__ __align__(256) unsigned char g_static_scratch[FA_STATIC_SCRATCH_BYTES];
 
-unsigned char *g_static_scratch_ptr[kMaxDevices] = {};
-std::mutex g_static_scratch_mutex;
-
 // Device address of the static scratch on the current device, looked up once
-// per device (the host-side name is only a stand-in for the device array).
+// per device and context (the host-side name is only a stand-in for the
+// device array).
 int static_scratch(unsigned char **out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return record(e);
-  if (dev < 0 || dev >= kMaxDevices) return kErrArch;
-  std::lock_guard<std::mutex> lock(g_static_scratch_mutex);
-  if (!g_static_scratch_ptr[dev]) {
+  DeviceInfo *dev = nullptr;
+  int st = current_device(&dev);
+  if (st != kOk) return st;
+  std::lock_guard<std::mutex> lock(g_dev_mutex);
+  if (!dev->scratch) {
     void *p = nullptr;
-    if ((e = cudaGetSymbolAddress(&p, g_static_scratch)) != cudaSuccess) return record(e);
-    g_static_scratch_ptr[dev] = static_cast<unsigned char *>(p);
+    cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
+    if (e != cudaSuccess) return record(e);
+    dev->scratch = static_cast<unsigned char *>(p);
   }
-  *out = g_static_scratch_ptr[dev];
+  *out = dev->scratch;
   return kOk;
 }
 
@@ -527,37 +579,18 @@ extern "C" int fa_bwd_static_scratch(const void *q, const void *k, const void *v
                                      const float *lse, const void *dO, void *dq, void *dk, void *dv,
                                      int B, int H, int N, int d, float scale, int causal,
                                      fa_stream_t stream) {
-  if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return FA_ERR_NULL;
-  int st = check_shape(B, H, N, d, 128);
-  if (st != kOk) return st;
-  if (d != 64 && d != 96 && d != 128) return FA_ERR_UNSUPPORTED;
-  if (!isfinite(scale)) return FA_ERR_ARG;
-  const void *ptrs[] = {q, k, v, o, dO, dq, dk, dv};
-  for (const void *p : ptrs)
-    if (!aligned(p, 16)) return FA_ERR_ALIGN;
-  if (!aligned(lse, 4)) return FA_ERR_ALIGN;
-  const BwdWorkspace w = ws_layout(B, H, N, d, FA_BF16);
-  if (w.total > static_cast<size_t>(FA_STATIC_SCRATCH_BYTES)) return FA_ERR_WORKSPACE;
-  DeviceInfo *dev = nullptr;
-  if ((st = current_device(&dev)) != kOk) return st;
+  // What differs from fa_bwd: the size limit, checked before any device work
+  // (an invalid shape falls through to fa_bwd's own checks), and the array.
+  const size_t need = ws_bytes(B, H, N, d, FA_BF16);
+  if (need > static_cast<size_t>(FA_STATIC_SCRATCH_BYTES)) return FA_ERR_WORKSPACE;
   unsigned char *ws = nullptr;
-  if ((st = static_scratch(&ws)) != kOk) return st;
-  if ((st = get_encoder()) != kOk) return st;
-  CUtensorMap tq, tk, tv, tdo, tdk, tdv;
-  const int BH = B * H;
-  if ((st = make_map(&tq, q, BH, N, d, false)) != kOk || (st = make_map(&tk, k, BH, N, d, false)) != kOk ||
-      (st = make_map(&tv, v, BH, N, d, false)) != kOk || (st = make_map(&tdo, dO, BH, N, d, false)) != kOk ||
-      (st = make_store_map(&tdk, dk, BH, N, d, false)) != kOk ||
-      (st = make_store_map(&tdv, dv, BH, N, d, false)) != kOk)
-    return st;
+  if (need != 0) {
+    const int st = static_scratch(&ws);
+    if (st != kOk) return st;
+  }
   // The first kernel of the pass rewrites every scratch byte it later reads
   // (the L and D rows, padding included), so the previous call's contents
   // never leak into this one.
-  int launches = 0;
-  cudaError_t e = launch_bwd_16(tq, tk, tv, tdo, tdk, tdv, o, dO, lse, dq, dk, dv, reinterpret_cast<float *>(ws + w.lp),
-                                reinterpret_cast<float *>(ws + w.dp), B, H, N, N, d, scale, causal ? 1 : 0, false,
-                                nullptr, dev->status, dev->num_sms, reinterpret_cast<cudaStream_t>(stream), &launches);
-  if (e != cudaSuccess) return record(e);
-  t_last_launches = launches;
-  return FA_OK;
+  return bwd16(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, N, d, scale, causal, ws, FA_STATIC_SCRATCH_BYTES,
+               stream, false);
 }

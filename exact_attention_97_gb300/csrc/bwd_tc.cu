@@ -920,7 +920,7 @@ cudaError_t launch(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtenso
   });
   auto kdkdv = bwd_dkdv_kernel<D, F16, DROP>;
   auto kdq = bwd_dq_kernel<D, F16, DROP>;
-  static std::atomic<unsigned long long> smem_kv{0}, smem_q{0};
+  static SmemOnce smem_kv, smem_q;
   if ((e = set_smem_once(reinterpret_cast<const void *>(kdkdv), DkdvCfg<D>::kAlloc, &smem_kv)) != cudaSuccess ||
       (e = set_smem_once(reinterpret_cast<const void *>(kdq), DqCfg<D>::kAlloc, &smem_q)) != cudaSuccess)
     return e;

@@ -548,7 +548,7 @@ cudaError_t launch(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtenso
                    int *status, int num_sms, cudaStream_t stream) {
   using L = FwdSmem<D, DROP>;
   auto kern = fwd_kernel<D, F16, DROP>;
-  static std::atomic<unsigned long long> smem_set{0};
+  static SmemOnce smem_set;
   cudaError_t e = set_smem_once(reinterpret_cast<const void *>(kern), L::kAlloc, &smem_set);
   if (e != cudaSuccess) return e;
   // persistent grid: at most one CTA per SM, each walking its static list of

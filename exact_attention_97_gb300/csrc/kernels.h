@@ -39,11 +39,20 @@ enum : int {
 // main kernel. `begin` records the first event, `end` the second and advances.
 void timing_begin(cudaStream_t stream);
 
-// Sets a kernel's dynamic shared-memory limit once per device: `done` is the
-// kernel instance's own mask of devices already set (bit = device ordinal;
-// ordinals past 63 are set on every call).
-cudaError_t set_smem_once(const void *kernel, int bytes, std::atomic<unsigned long long> *done);
 void timing_end(cudaStream_t stream);
+
+// A kernel instance's record of where its dynamic shared-memory limit has been
+// raised: per device ordinal, the context epoch it was set in (0 = never).
+// Function attributes belong to a context, so a device reset (a new primary
+// context, hence a new epoch) makes the library set them again.
+struct SmemOnce {
+  std::atomic<uint32_t> epoch[64];
+};
+
+// Sets a kernel's dynamic shared-memory limit once per device and context
+// (ordinals past 63 are set on every call). Call after the entry point has
+// looked up its device (the epoch comes from that lookup).
+cudaError_t set_smem_once(const void *kernel, int bytes, SmemOnce *done);
 
 cudaError_t launch_fwd_f32(const float *q, const float *k, const float *v, float *o, float *lse,
                            int B, int H, int N, int d, float scale, int causal,

@@ -208,6 +208,26 @@ int fa_last_cuda_error(void);
  * on a wait (FA_OK or FA_ERR_TIMEOUT). Synchronises the current device. */
 int fa_device_status(void);
 
+/*
+ * The same status, without synchronising: enqueues on `stream` a copy of the
+ * current device's status word into *dst, then clears the word. dst is device
+ * memory or page-locked host memory (cudaHostAlloc, torch pin_memory); it
+ * holds FA_OK or FA_ERR_TIMEOUT once the stream has reached the copy. The
+ * word is one per device, shared by every stream and host thread: a timeout
+ * recorded by any earlier kernel of this library on the device shows up in
+ * the next read. Returns FA_ERR_NULL / FA_ERR_ALIGN (dst not 4-byte aligned)
+ * or FA_ERR_LAUNCH if the copy cannot be enqueued.
+ */
+int fa_status_async(int *dst, fa_stream_t stream);
+
+/*
+ * Device address of the current device's status word, for callers that read
+ * it from their own stream-ordered work (their kernels, a captured graph).
+ * The library's kernels write FA_ERR_TIMEOUT there and nothing else; clear it
+ * by writing 0.
+ */
+int fa_status_word(int **dev_ptr);
+
 /* Number of kernels the most recent successful fa_* call on this host thread
  * enqueued. */
 int fa_last_launch_count(void);
@@ -254,6 +274,9 @@ int fa_set_kernel_timing(void **events, int n_pairs);
  *           reading it. Calls whose kernels overlap on the GPU (different
  *           streams, or host threads, with no ordering between them) race on
  *           the array and give wrong gradients: order them.
+ *   Reset   the looked-up address belongs to the device's current context;
+ *           after cudaDeviceReset the next call (on the new context) looks it
+ *           up again, so that call, too, should come before any capture.
  */
 #define FA_STATIC_SCRATCH_BYTES (16u * 1024u * 1024u)
 

@@ -133,7 +133,8 @@ void oracle_probs(const double *q, const double *k, int N, int d, double scale,
 /* Backward over all heads, Nq queries and Nk keys per head. Outputs dq, dk,
  * dv are overwritten.
  * Heads are processed one after another; inside a head the query rows are
- * split statically over threads. Each thread runs its rows forward in full
+ * dealt to threads in fixed chunks of 16 rows, round robin (so the long rows
+ * of a causal head are spread evenly). Each thread runs its rows forward in full
  * (S row, P row, O row, D_i), writes dQ_i, and adds its rows' terms of dK and
  * dV into private [N][d] sums, which are then added together in thread order
  * (so the result does not depend on scheduling). */
@@ -166,7 +167,7 @@ void oracle_bwd_kv(const double *q, const double *k, const double *v,
       double *s = (double *)malloc(sizeof(double) * (size_t)Nk);
       double *p = (double *)malloc(sizeof(double) * (size_t)Nk);
       double *o = (double *)malloc(sizeof(double) * (size_t)d);
-#pragma omp for schedule(static)
+#pragma omp for schedule(static, 16)
       for (int i = 0; i < Nq; ++i) {
         const double *qi = qh + (size_t)i * d;
         const double *doi = doh + (size_t)i * d;
@@ -441,7 +442,7 @@ void oracle_bwd_dropout_kv(const double *q, const double *k, const double *v, co
       double *s = (double *)malloc(sizeof(double) * (size_t)Nk);
       double *p = (double *)malloc(sizeof(double) * (size_t)Nk);
       double *o = (double *)malloc(sizeof(double) * (size_t)d);
-#pragma omp for schedule(static)
+#pragma omp for schedule(static, 16)
       for (int i = 0; i < Nq; ++i) {
         const double *qi = qh + (size_t)i * d;
         const double *doi = doh + (size_t)i * d;

@@ -43,3 +43,26 @@ extern "C" int run_wait_timeout(int *host_out) {
   cudaFree(d);
   return static_cast<int>(e);
 }
+
+// The same never-completed wait, and on giving up the kernel records the
+// library's timeout code (7, FA_ERR_TIMEOUT) in `status`, the library's
+// device status word passed in by address, as the attention kernels do when
+// they abort. Lets a test check that the status reaches the Python caller.
+__global__ void wait_timeout_status_kernel(int *status) {
+  __shared__ uint64_t never;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    fa::mbar_init(&never, 1);
+    fa::fence_mbar_init();
+  }
+  __syncthreads();
+  fa::mbar_wait_warp(&never, 0, &abort_flag);
+  __syncthreads();
+  if (threadIdx.x == 0 && abort_flag) atomicExch(status, 7);
+}
+
+extern "C" int run_wait_timeout_status(int *status_word) {
+  wait_timeout_status_kernel<<<2, 64>>>(status_word);
+  return static_cast<int>(cudaDeviceSynchronize());
+}

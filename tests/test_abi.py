@@ -154,6 +154,12 @@ def test_f32_argument_errors(lib):
     assert lib.fa_bwd_f32(*ptrs, 1, 1, 4, 2, 1.0, 0, None, 0, None) == 5
 
 
+def test_status_read_argument_errors(lib):
+    assert lib.fa_status_async(None, None) == 1
+    assert lib.fa_status_async(P + 2, None) == 4
+    assert lib.fa_status_word(None) == 1
+
+
 def test_no_cpu_fallback_in_the_binding():
     """The binding only marshals arguments: it never imports the oracle or
     computes attention itself."""

@@ -483,6 +483,19 @@ def test_bf16_causal_B1_H32_N65536_d128():
         gk["dv"].append(got["dv"][0, h, keys]); rk["dv"].append(dv)
     check(w.name + "_keys", "bf16", {k_: np.concatenate(v_) for k_, v_ in gk.items()},
           {k_: np.concatenate(v_) for k_, v_ in rk.items()})
+    # two whole heads: every key's dK and dV (and every row's dQ) against the
+    # full fp64 backward of the head. Early keys sum the contributions of up
+    # to 512 query tiles in the dK/dV pass's accumulators.
+    for h in (int(x) for x in sample_indices(w.H, 2, seed=65536).numpy()):
+        qh, kh, vh, doh = (_np(x[:, h:h + 1]) for x in (q, k, v, dO))
+        rdq, rdk, rdv = oracle.attention_bwd(qh, kh, vh, doh, w.scale, True)
+        check(f"{w.name}_whole_head{h}", "bf16",
+              {"dq": got["dq"][:, h:h + 1], "dk": got["dk"][:, h:h + 1], "dv": got["dv"][:, h:h + 1]},
+              {"dq": rdq, "dk": rdk, "dv": rdv})
+        # the earliest keys carry the longest sums: hold their block to the same bar
+        check(f"{w.name}_whole_head{h}_first_block", "bf16",
+              {"dk": got["dk"][0, h, :128], "dv": got["dv"][0, h, :128]},
+              {"dk": rdk[0, 0, :128], "dv": rdv[0, 0, :128]})
     # any-size properties over every key of every head: rows of P sum to one, so
     # sum_j dK_j = 0 and sum_j dV_j = sum_i dO_i
     dk_sum = got["dk"].sum(axis=2)

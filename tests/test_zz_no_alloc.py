@@ -6,12 +6,17 @@ cudaMalloc calls, their calling convention has no slot for a workspace
 pointer, or their latency budget rules out allocating after start-up. This
 entry point serves them from a static device array inside libfa.so.
 
-The test calls it through the C ABI twice in a row (different shapes and
-masks, so the second call runs over the first call's leftovers in the shared
-array) and checks each result against fa_bwd with a caller workspace, within
-the bf16 gradient tolerance the parity tests use. It also checks that the
-calls leave free device memory unchanged and that a problem too large for the
-array is refused before any launch. This file is collected last on purpose.
+What the tests check, through the C ABI:
+  * two calls in a row (the larger problem first) each match fa_bwd with a
+    caller workspace within the bf16 gradient tolerance of the parity tests,
+    and free device memory is the same before the first call (which also
+    looks up the array's address) and after the second;
+  * leftovers of an earlier call never reach a later one: a first call with a
+    NaN log-sum-exp leaves NaN in the array rows where the second call's
+    padding rows sit, and the second call's gradients are still finite and
+    correct (a padded row read before being rewritten would turn them NaN);
+  * a problem too large for the array is refused before any launch.
+This file is collected last on purpose.
 """
 import ctypes
 import math
@@ -62,22 +67,40 @@ def _compare(got, ref):
 def test_static_scratch_backward_matches_workspace_backward():
     lib = _lib.load()
     torch.cuda.init()
-    first = _case(1, 4, 1000, 64, False, seed=11)
-    second = _case(2, 3, 700, 128, True, seed=12)
+    first = _case(2, 3, 700, 128, True, seed=12)    # 6 heads x 768 padded rows
+    second = _case(1, 4, 1000, 64, False, seed=11)  # 4 heads x 1024 padded rows
     # outputs are allocated (by torch) before the calls and pre-filled with NaN
     g1 = [torch.full_like(first[0][0], float("nan")) for _ in range(3)]
     g2 = [torch.full_like(second[0][0], float("nan")) for _ in range(3)]
     torch.cuda.synchronize()
-    # first call on this device also looks up the static array's address
+    free_before = torch.cuda.mem_get_info()[0]
+    # the first call on this device also looks up the static array's address
     _static_call(lib, first[0], first[2], g1)
     torch.cuda.synchronize()
-    free_before = torch.cuda.mem_get_info()[0]
+    assert torch.cuda.mem_get_info()[0] == free_before
     _static_call(lib, second[0], second[2], g2)
     torch.cuda.synchronize()
     assert torch.cuda.mem_get_info()[0] == free_before
     assert fa.fa_device_status() == 0
     _compare(g1, first[1])
     _compare(g2, second[1])
+
+
+def test_static_scratch_leftovers_never_leak():
+    lib = _lib.load()
+    # poison: 1024 unpadded rows with L = NaN; the array's first 8 KB (its L
+    # and D rows) then hold NaN where the next call keeps L and D
+    ins, _, shape = _case(1, 1, 1024, 64, False, seed=21)
+    q, k, v, o, lse, dO = ins
+    junk = [torch.empty_like(q) for _ in range(3)]
+    _static_call(lib, (q, k, v, o, torch.full_like(lse, float("nan")), dO), shape, junk)
+    # 2 heads of 200 rows, padded to 256: rows 200..255 of each head are padding
+    ins2, ref2, shape2 = _case(1, 2, 200, 64, True, seed=22)
+    got = [torch.full_like(ins2[0], float("nan")) for _ in range(3)]
+    _static_call(lib, ins2, shape2, got)
+    torch.cuda.synchronize()
+    assert fa.fa_device_status() == 0
+    _compare(got, ref2)
 
 
 def test_static_scratch_refuses_problems_beyond_its_size():
