@@ -49,18 +49,25 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(p) <= t for p in _deps())
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile and link libfa.so; returns its path."""
-    if not force and up_to_date():
+def build(force: bool = False, verbose: bool = False, out_dir: str | None = None,
+          defines: tuple = ()) -> str:
+    """Compile and link libfa.so; returns its path.
+
+    out_dir / defines build a variant elsewhere (e.g. the two-CTA kernels,
+    ``defines=("-DFA_PAIR_KERNELS=1",)``) without touching the default library.
+    """
+    if out_dir is None and not force and up_to_date():
         return LIB
-    os.makedirs(BUILD, exist_ok=True)
+    build_dir = out_dir or BUILD
+    lib = os.path.join(build_dir, "libfa.so")
+    os.makedirs(build_dir, exist_ok=True)
     cc = nvcc()
 
     # tuning knobs (e.g. "-DFA_FWD_QBUF=1") for sweeps; empty by default
-    extra = os.environ.get("FA_NVCC_DEFINES", "").split()
+    extra = os.environ.get("FA_NVCC_DEFINES", "").split() + list(defines)
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
         cmd = [cc, *ARCH, *NVCC_FLAGS, *extra, "-c", src, "-o", obj]
         if verbose:
             cmd.insert(1, "-Xptxas=-v")
@@ -74,12 +81,12 @@ def build(force: bool = False, verbose: bool = False) -> str:
     srcs = _sources()
     with ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
         objs = list(ex.map(compile_one, srcs))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     r = subprocess.run([cc, *ARCH, "-shared", "-o", tmp, *objs], capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link of libfa.so failed:\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

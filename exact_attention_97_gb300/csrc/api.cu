@@ -121,14 +121,14 @@ int get_encoder() {
 }
 
 // 3-D map over a contiguous [BH][N][d] 16-bit tensor (bf16, or f16 when
-// `f16`): dims {d, N, BH}, box {64, 128, 1}, 128-byte swizzle; rows past N
-// (inside a head) read as zero.
-int encode_map(CUtensorMap *map, const void *ptr, int BH, int N, int d, bool f16) {
+// `f16`): dims {d, N, BH}, box {64, box_rows, 1}, 128-byte swizzle; rows past
+// N (inside a head) read as zero.
+int encode_map(CUtensorMap *map, const void *ptr, int BH, int N, int d, bool f16, int box_rows = 128) {
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
                         static_cast<cuuint64_t>(BH)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
                            static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(d) * 2};
-  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = g_encode(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
                         const_cast<void *>(ptr), dims,
@@ -168,7 +168,7 @@ int encode_store_map(CUtensorMap *map, void *ptr, int BH, int N, int d, bool f16
 // all threads. Encoding costs a driver call per map otherwise.
 struct MapKey {
   const void *ptr;
-  int BH, N, d, f16, store;
+  int BH, N, d, f16, store;  // store: 0 load map (128-row box), 1 store map, 2 load map with 64-row box
   bool operator==(const MapKey &o) const {
     return ptr == o.ptr && BH == o.BH && N == o.N && d == o.d && f16 == o.f16 && store == o.store;
   }
@@ -179,8 +179,8 @@ MapKey g_map_key[kMapCache];
 CUtensorMap g_map_val[kMapCache];
 int g_map_used = 0, g_map_next = 0;
 
-int cached_map(CUtensorMap *map, const void *ptr, int BH, int N, int d, bool f16, bool store) {
-  const MapKey key{ptr, BH, N, d, f16 ? 1 : 0, store ? 1 : 0};
+int cached_map(CUtensorMap *map, const void *ptr, int BH, int N, int d, bool f16, int kind) {
+  const MapKey key{ptr, BH, N, d, f16 ? 1 : 0, kind};
   {
     std::lock_guard<std::mutex> lock(g_map_mu);
     for (int i = 0; i < g_map_used; ++i)
@@ -189,8 +189,8 @@ int cached_map(CUtensorMap *map, const void *ptr, int BH, int N, int d, bool f16
         return kOk;
       }
   }
-  const int st = store ? encode_store_map(map, const_cast<void *>(ptr), BH, N, d, f16)
-                       : encode_map(map, ptr, BH, N, d, f16);
+  const int st = kind == 1 ? encode_store_map(map, const_cast<void *>(ptr), BH, N, d, f16)
+                           : encode_map(map, ptr, BH, N, d, f16, kind == 2 ? 64 : 128);
   if (st != kOk) return st;
   std::lock_guard<std::mutex> lock(g_map_mu);
   g_map_key[g_map_next] = key;
@@ -200,10 +200,14 @@ int cached_map(CUtensorMap *map, const void *ptr, int BH, int N, int d, bool f16
   return kOk;
 }
 int make_map(CUtensorMap *map, const void *ptr, int BH, int N, int d, bool f16) {
-  return cached_map(map, ptr, BH, N, d, f16, false);
+  return cached_map(map, ptr, BH, N, d, f16, 0);
 }
 int make_store_map(CUtensorMap *map, void *ptr, int BH, int N, int d, bool f16) {
-  return cached_map(map, ptr, BH, N, d, f16, true);
+  return cached_map(map, ptr, BH, N, d, f16, 1);
+}
+// 64-row boxes: the half tiles a CTA of a two-CTA (pair) kernel loads.
+int make_half_map(CUtensorMap *map, const void *ptr, int BH, int N, int d, bool f16) {
+  return cached_map(map, ptr, BH, N, d, f16, 2);
 }
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -259,6 +263,44 @@ void timing_end(cudaStream_t stream) {
     ++t_event_next;
   }
 }
+int max_pair_clusters(const void *kernel, int smem_bytes, int threads) {
+  struct Entry {
+    const void *kernel;
+    int dev, smem, threads, clusters;
+  };
+  static std::mutex mu;
+  static Entry cache[64];
+  static int used = 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < used; ++i)
+      if (cache[i].kernel == kernel && cache[i].dev == dev && cache[i].smem == smem_bytes &&
+          cache[i].threads == threads)
+        return cache[i].clusters;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(2, 1, 1);
+  cfg.blockDim = dim3(threads, 1, 1);
+  cfg.dynamicSmemBytes = smem_bytes;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) {
+    cudaGetLastError();  // a failed query is not sticky: leave no error for the next launch check
+    n = 0;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (used < 64) cache[used++] = Entry{kernel, dev, smem_bytes, threads, n};
+  return n;
+}
+
 cudaError_t set_smem_once(const void *kernel, int bytes, SmemOnce *done) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -363,14 +405,17 @@ int fwd16(const void *q, const void *k, const void *v, void *o, float *lse, int 
   DeviceInfo *dev = nullptr;
   if ((st = current_device(&dev)) != kOk) return st;
   if ((st = get_encoder()) != kOk) return st;
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, tkh;
   const int BH = B * H;
   if ((st = make_map(&tq, q, BH, N, d, f16)) != kOk || (st = make_map(&tk, k, BH, Nk, d, f16)) != kOk ||
       (st = make_map(&tv, v, BH, Nk, d, f16)) != kOk)
     return st;
+  const bool pair = FA_PAIR_KERNELS && d == 128 && !drop;  // the two-CTA kernel's K map has 64-row boxes
+  if (pair && (st = make_half_map(&tkh, k, BH, Nk, d, f16)) != kOk) return st;
   int launches = 0;
-  cudaError_t e = launch_fwd_16(tq, tk, tv, o, lse, B, H, N, Nk, d, scale, causal ? 1 : 0, f16, drop, dev->status,
-                                dev->num_sms, reinterpret_cast<cudaStream_t>(stream), &launches);
+  cudaError_t e = launch_fwd_16(tq, tk, pair ? &tkh : nullptr, tv, o, lse, B, H, N, Nk, d, scale, causal ? 1 : 0,
+                                f16, drop, dev->status, dev->num_sms, reinterpret_cast<cudaStream_t>(stream),
+                                &launches);
   if (e != cudaSuccess) return record(e);
   t_last_launches = launches;
   return FA_OK;
@@ -404,12 +449,21 @@ int bwd16(const void *q, const void *k, const void *v, const void *o, const floa
       (st = make_store_map(&tdk, dk, BH, Nk, d, f16)) != kOk ||
       (st = make_store_map(&tdv, dv, BH, Nk, d, f16)) != kOk)
     return st;
+  // the two-CTA kernels of d = 128 load half tiles (64-row boxes)
+  HalfMaps half;
+  const bool pair = FA_PAIR_KERNELS && d == 128 && !drop;
+  if (pair && ((st = make_half_map(&half.q, q, BH, N, d, f16)) != kOk ||
+               (st = make_half_map(&half.k, k, BH, Nk, d, f16)) != kOk ||
+               (st = make_half_map(&half.v, v, BH, Nk, d, f16)) != kOk ||
+               (st = make_half_map(&half.dO, dO, BH, N, d, f16)) != kOk))
+    return st;
   const BwdWorkspace w = ws_layout(B, H, N, d, FA_BF16);
   char *ws = static_cast<char *>(workspace);
   int launches = 0;
-  cudaError_t e = launch_bwd_16(tq, tk, tv, tdo, tdk, tdv, o, dO, lse, dq, dk, dv, reinterpret_cast<float *>(ws + w.lp),
-                                reinterpret_cast<float *>(ws + w.dp), B, H, N, Nk, d, scale, causal ? 1 : 0, f16,
-                                drop, dev->status, dev->num_sms, reinterpret_cast<cudaStream_t>(stream), &launches);
+  cudaError_t e = launch_bwd_16(tq, tk, tv, tdo, tdk, tdv, pair ? &half : nullptr, o, dO, lse, dq, dk, dv,
+                                reinterpret_cast<float *>(ws + w.lp), reinterpret_cast<float *>(ws + w.dp), B, H, N,
+                                Nk, d, scale, causal ? 1 : 0, f16, drop, dev->status, dev->num_sms,
+                                reinterpret_cast<cudaStream_t>(stream), &launches);
   if (e != cudaSuccess) return record(e);
   t_last_launches = launches;
   return FA_OK;

@@ -112,16 +112,28 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const uint16_t *__restric
 }
 
 // ------------------------------------------------------------------ kernel 2
-template <int D>
+//
+// PAIR (d = 128, no dropout): a two-CTA cluster runs key blocks 2u and 2u + 1
+// with M = 256 MMAs. Q_t and dO_t are each B of two products with different
+// splits, so a CTA (rank r) holds four 16 KB halves per query tile: the rows
+// 64r..64r+63 of Q and of dO (K-major, for S^T = K Q^T and dP^T = V dO^T) and
+// the head columns 64r..64r+63 of all 128 rows of Q and of dO (MN-major, for
+// dK += dS^T Q and dV += P^T dO). Same 64 KB per stage as one whole Q and dO.
+template <int D, bool PAIR = false>
 struct DkdvCfg {
+  static_assert(!PAIR || D == 128, "the pair kernel covers d = 128");
   static constexpr int kDP = (D + 63) / 64 * 64;  // whole 64-column TMA boxes per row
   static constexpr int kStages = (kDP == 128) ? 2 : 3;
   static constexpr int kTileBytes = kBlk * kDP * 2;
   static constexpr int kSubBytes = kBlk * 128;  // 128 rows x 64 16-bit elements
+  static constexpr int kHalfSub = kSubBytes / 2;  // 64 rows x 64 16-bit elements
   static constexpr int kK = 0;
   static constexpr int kV = kK + kTileBytes;
   static constexpr int kQ = kV + kTileBytes;
   static constexpr int kDO = kQ + kStages * kTileBytes;
+  // pair: offsets of the four halves inside a stage of 2 * kTileBytes at kQ
+  static constexpr int kPairStage = 2 * kTileBytes;
+  static constexpr int kQRows = 0, kQCols = kTileBytes / 2, kDORows = kTileBytes, kDOCols = kTileBytes + kTileBytes / 2;
   // epilogue staging: per storing warp, two 32-row x 16-column buffers
   static constexpr int kStgBuf = 32 * 16 * 2;
   static constexpr int kStg = kDO + kStages * kTileBytes;
@@ -130,22 +142,25 @@ struct DkdvCfg {
   static constexpr uint32_t tS = 0, tDP = 128, tDV = 256, tDK = 256 + D;  // TMEM columns
 };
 
-template <int D, bool F16, bool DROP>
+template <int D, bool F16, bool DROP, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                     const __grid_constant__ CUtensorMap tmdK, const __grid_constant__ CUtensorMap tmdV,
+                    const __grid_constant__ CUtensorMap tmQh, const __grid_constant__ CUtensorMap tmdOh,
                     const float *__restrict__ Lp, const float *__restrict__ Dp, int N, int Nk,
                     const __grid_constant__ TileSched sched, float scale, float scale_log2, int causal,
                     const Dropout drop, int *status) {
-  using C = DkdvCfg<D>;
+  static_assert(!(PAIR && DROP), "the pair kernel has no dropout");
+  using C = DkdvCfg<D, PAIR>;
   using E = Elt<F16>;
   constexpr int NST = C::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
-  __shared__ uint64_t k_full, k_empty, v_full, v_empty, qd_full[NST], qd_empty[NST], s_full, dp_full, p_ready,
-      ds_ready, done, drain, drain_kv;
+  // ld_full: the L and D rows of a stage (in each CTA; a pair's qd_full is rank 0's)
+  __shared__ uint64_t k_full, k_empty, v_full, v_empty, qd_full[NST], qd_empty[NST], ld_full[NST], s_full, dp_full,
+      p_ready, ds_ready, done, drain, drain_kv;
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_flag;
   __shared__ __align__(16) float Lst[NST][kBlk], Dst[NST][kBlk];  // per stage, by bulk copy
@@ -155,9 +170,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int Np = n_tiles_all * kBlk;
   // N query rows, Nk >= N keys under the causal mask; key j is seen by the
   // queries i >= j - (Nk - N) (bottom-right alignment). Schedule rank r is
-  // key block r: low blocks see the most query tiles.
+  // unit r (a key block, or with PAIR the block pair 2r, 2r + 1 whose block
+  // 2r + c runs on cluster rank c): low blocks see the most query tiles.
   const int off = Nk - N;
-  auto first_tile = [&](int kb) { return causal ? max(0, kb * kBlk - off) / kBlk : 0; };
+  const uint32_t crank = PAIR ? cluster_rank() : 0u;
+  const int cta = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  auto block_of = [&](int rank) { return PAIR ? 2 * rank + static_cast<int>(crank) : rank; };
+  // first query tile a unit visits: a pair starts at its lower block's (the
+  // upper block's keys see the tiles before their own first one masked)
+  auto first_tile = [&](int rank) {
+    const int kb = PAIR ? 2 * rank : rank;
+    return causal ? max(0, kb * kBlk - off) / kBlk : 0;
+  };
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
@@ -168,24 +192,46 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < NST; ++s) {
       mbar_init(&qd_full[s], 1);
       mbar_init(&qd_empty[s], 2);  // the two issuing threads' last readers of the stage
+      mbar_init(&ld_full[s], 1);
     }
     mbar_init(&s_full, 1);
     mbar_init(&dp_full, 1);
-    mbar_init(&p_ready, 256);
-    mbar_init(&ds_ready, 256);
+    mbar_init(&p_ready, PAIR ? 2 * 8 : 256);  // pair: one arrival per elementwise warp of each CTA
+    mbar_init(&ds_ready, PAIR ? 2 * 8 : 256);
     mbar_init(&done, 2);  // dV and dK, from the two issuing threads
     mbar_init(&drain, 1);
     mbar_init(&drain_kv, 1);
     fence_mbar_init();
   }
   if (warp == 2) {
-    tmem_alloc(&tmem_base_s, 512);
-    tmem_relinquish();
+    if constexpr (PAIR) {
+      tmem_alloc_pair(&tmem_base_s, 512);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(&tmem_base_s, 512);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
-  __syncthreads();
+  if constexpr (PAIR)
+    cluster_sync_all();  // the other CTA arrives on this one's barriers only once they exist
+  else
+    __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base_s;
+  // a pair's copies complete on rank 0's barriers, which only rank 0 drains
+  const bool drains = !PAIR || crank == 0;
+  // this CTA's K or V block on `bar` (rank 0's for a pair)
+  auto load_block = [&](uint32_t dst, const CUtensorMap *map, uint64_t *bar, int row, int bh) {
+    if constexpr (PAIR) {
+      if (crank == 0) mbar_arrive_expect_tx(bar, 2 * C::kTileBytes);
+      const uint32_t b0 = cluster_addr(bar, 0);
+      for (int x = 0; x < D; x += 64) tma_load_3d_pair(smem + dst + (x / 64) * C::kSubBytes, map, b0, x, row, bh);
+    } else {
+      mbar_arrive_expect_tx(bar, C::kTileBytes);
+      load_rows(smem + dst, map, bar, D, row, bh);
+    }
+  };
 
   // Every role walks the same items (key blocks); query tiles are counted
   // across items (g) for the ring and the per-tile barriers, items (it) for
@@ -201,50 +247,72 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tmV);
       tma_prefetch_desc(&tmdO);
       bool ok = true;
-      int g = 0, it = 0, kb, bh;
+      int g = 0, it = 0, rank, bh;
       auto load_qd = [&](int row) -> bool {
         const int st = g % NST;
         if (g >= NST && !mbar_wait(&qd_empty[st], ((g / NST) & 1) ^ 1, &abort_flag)) return false;
-        mbar_arrive_expect_tx(&qd_full[st], 2 * C::kTileBytes + 2 * kBlk * 4);
-        load_rows(smem + C::kQ + st * C::kTileBytes, &tmQ, &qd_full[st], D, row, bh);
-        load_rows(smem + C::kDO + st * C::kTileBytes, &tmdO, &qd_full[st], D, row, bh);
-        const size_t prow = static_cast<size_t>(bh) * Np + row;
-        bulk_load(Lst[st], Lp + prow, kBlk * 4, &qd_full[st]);
-        bulk_load(Dst[st], Dp + prow, kBlk * 4, &qd_full[st]);
+        if constexpr (PAIR) {
+          // rows 64r.. of Q and dO, and head columns 64r.. of all their rows,
+          // on rank 0's barrier; this CTA's L and D rows on its own
+          if (crank == 0) mbar_arrive_expect_tx(&qd_full[st], 2 * 2 * C::kTileBytes);
+          const uint32_t b0 = cluster_addr(&qd_full[st], 0);
+          uint8_t *stage = smem + C::kQ + st * C::kPairStage;
+          const int r64 = 64 * static_cast<int>(crank);
+          for (int x = 0; x < D; x += 64) {
+            tma_load_3d_pair(stage + C::kQRows + (x / 64) * C::kHalfSub, &tmQh, b0, x, row + r64, bh);
+            tma_load_3d_pair(stage + C::kDORows + (x / 64) * C::kHalfSub, &tmdOh, b0, x, row + r64, bh);
+          }
+          tma_load_3d_pair(stage + C::kQCols, &tmQ, b0, r64, row, bh);
+          tma_load_3d_pair(stage + C::kDOCols, &tmdO, b0, r64, row, bh);
+          mbar_arrive_expect_tx(&ld_full[st], 2 * kBlk * 4);
+          const size_t prow = static_cast<size_t>(bh) * Np + row;
+          bulk_load(Lst[st], Lp + prow, kBlk * 4, &ld_full[st]);
+          bulk_load(Dst[st], Dp + prow, kBlk * 4, &ld_full[st]);
+        } else {
+          mbar_arrive_expect_tx(&qd_full[st], 2 * C::kTileBytes + 2 * kBlk * 4);
+          load_rows(smem + C::kQ + st * C::kTileBytes, &tmQ, &qd_full[st], D, row, bh);
+          load_rows(smem + C::kDO + st * C::kTileBytes, &tmdO, &qd_full[st], D, row, bh);
+          const size_t prow = static_cast<size_t>(bh) * Np + row;
+          bulk_load(Lst[st], Lp + prow, kBlk * 4, &qd_full[st]);
+          bulk_load(Dst[st], Dp + prow, kBlk * 4, &qd_full[st]);
+        }
         ++g;
         return true;
       };
       int kdone = 0, vdone = 0;  // K / V loads issued
       for (int k = 0; ok; ++k) {
-        const int step = sched_item(sched, blockIdx.x, k, kb, bh);
+        const int step = sched_item(sched, cta, k, rank, bh);
         if (step == kDone) break;
         if (step == kSkip) continue;
-        const int i_first = first_tile(kb), n_tiles = n_tiles_all - i_first;
+        const int kb = block_of(rank);
+        const int i_first = first_tile(rank), n_tiles = n_tiles_all - i_first;
         {  // the next block's K and V are read once: start them towards L2 now
-          int nkb, nbh, ns, k2 = k + 1;
-          while ((ns = sched_item(sched, blockIdx.x, k2, nkb, nbh)) == kSkip) ++k2;
+          int nr, nbh, ns, k2 = k + 1;
+          while ((ns = sched_item(sched, cta, k2, nr, nbh)) == kSkip) ++k2;
           if (ns == kItem)
             for (int x = 0; x < D; x += 64) {
-              tma_prefetch_l2_3d(&tmK, x, nkb * kBlk, nbh);
-              tma_prefetch_l2_3d(&tmV, x, nkb * kBlk, nbh);
+              tma_prefetch_l2_3d(&tmK, x, block_of(nr) * kBlk, nbh);
+              tma_prefetch_l2_3d(&tmV, x, block_of(nr) * kBlk, nbh);
             }
         }
         if (it > 0 && !mbar_wait(&k_empty, (it - 1) & 1, &abort_flag)) break;
-        mbar_arrive_expect_tx(&k_full, C::kTileBytes);
-        load_rows(smem + C::kK, &tmK, &k_full, D, kb * kBlk, bh);
+        load_block(C::kK, &tmK, &k_full, kb * kBlk, bh);
         ++kdone;
         if (!load_qd(i_first * kBlk)) break;
         if (it > 0 && !mbar_wait(&v_empty, (it - 1) & 1, &abort_flag)) break;
-        mbar_arrive_expect_tx(&v_full, C::kTileBytes);
-        load_rows(smem + C::kV, &tmV, &v_full, D, kb * kBlk, bh);
+        load_block(C::kV, &tmV, &v_full, kb * kBlk, bh);
         ++vdone;
         for (int t = 1; t < n_tiles; ++t)
           if (!load_qd((i_first + t) * kBlk)) { ok = false; break; }
         ++it;
       }
-      if (kdone > 0) mbar_wait_drain(&k_full, (kdone - 1) & 1);
-      if (vdone > 0) mbar_wait_drain(&v_full, (vdone - 1) & 1);
-      for (int t = max(0, g - NST); t < g; ++t) mbar_wait_drain(&qd_full[t % NST], (t / NST) & 1);
+      if (drains) {
+        if (kdone > 0) mbar_wait_drain(&k_full, (kdone - 1) & 1);
+        if (vdone > 0) mbar_wait_drain(&v_full, (vdone - 1) & 1);
+        for (int t = max(0, g - NST); t < g; ++t) mbar_wait_drain(&qd_full[t % NST], (t / NST) & 1);
+      }
+      if constexpr (PAIR)  // this CTA's own L / D copies
+        for (int t = max(0, g - NST); t < g; ++t) mbar_wait_drain(&ld_full[t % NST], (t / NST) & 1);
     }
   } else if (warp == 1) {
     // ------------------------------------------------ MMA issuer: S^T and dV
@@ -256,106 +324,140 @@ __global__ void __launch_bounds__(kThreads, 1)
     // reader without waiting for it to complete; the two chains share no
     // TMEM columns. Q and dO stages are released by both threads (qd_empty
     // counts two), and the block's accumulators are done once both are.
-    if (lane == 0) {
-      constexpr uint32_t id_s = idesc_16(kBlk, kBlk, false, false, F16);  // S^T
-      constexpr uint32_t id_kv = idesc_16(kBlk, D, false, true, F16);     // dV
+    // With PAIR only rank 0 issues (M = 256 over both CTAs), and commits
+    // arrive on the barrier of that name in both CTAs.
+    if (lane == 0 && (!PAIR || crank == 0)) {
+      constexpr uint32_t id_s = idesc_16(PAIR ? 2 * kBlk : kBlk, kBlk, false, false, F16);  // S^T
+      constexpr uint32_t id_kv = idesc_16(PAIR ? 2 * kBlk : kBlk, D, false, true, F16);     // dV
       const uint32_t k_addr = smem_u32(smem + C::kK);
+      auto commit = [](uint64_t *bar) {
+        if constexpr (PAIR) mma_commit_pair_both(bar);
+        else mma_commit(bar);
+      };
       auto issue_s = [&](int gt) -> bool {  // S^T = K Q^T of global tile gt
         const int st = gt % NST;
         if (!mbar_wait(&qd_full[st], (gt / NST) & 1, &abort_flag)) return false;
         tc_fence_after();
-        const uint32_t q_addr = smem_u32(smem + C::kQ + st * C::kTileBytes);
+        const uint32_t q_addr = PAIR ? smem_u32(smem + C::kQ + st * C::kPairStage + C::kQRows)
+                                     : smem_u32(smem + C::kQ + st * C::kTileBytes);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk / 4) * C::kSubBytes + (kk % 4) * 32;
-          mma_ss(tmem + C::tS, sdesc_sw128(k_addr + off, 16, 1024), sdesc_sw128(q_addr + off, 16, 1024),
-                 id_s, kk > 0);
+          const uint32_t boff = (kk / 4) * (PAIR ? C::kHalfSub : C::kSubBytes) + (kk % 4) * 32;
+          if constexpr (PAIR)
+            mma_ss_pair(tmem + C::tS, sdesc_sw128(k_addr + off, 16, 1024), sdesc_sw128(q_addr + boff, 16, 1024),
+                        id_s, kk > 0);
+          else
+            mma_ss(tmem + C::tS, sdesc_sw128(k_addr + off, 16, 1024), sdesc_sw128(q_addr + boff, 16, 1024), id_s,
+                   kk > 0);
         }
-        mma_commit(&s_full);
+        commit(&s_full);
         return true;
       };
       bool ok = true;
-      int g = 0, it = 0, kb, bh;
+      int g = 0, it = 0, rank, bh;
       for (int k = 0; ok; ++k) {
-        const int step = sched_item(sched, blockIdx.x, k, kb, bh);
+        const int step = sched_item(sched, cta, k, rank, bh);
         if (step == kDone) break;
         if (step == kSkip) continue;
-        const int n_tiles = n_tiles_all - first_tile(kb);
+        const int n_tiles = n_tiles_all - first_tile(rank);
         if (!mbar_wait(&k_full, it & 1, &abort_flag) || !issue_s(g)) break;
-        if (n_tiles == 1) mma_commit(&k_empty);
+        if (n_tiles == 1) commit(&k_empty);
         for (int t = 0; t < n_tiles; ++t, ++g) {
           const int st = g % NST;
-          const uint32_t do_addr = smem_u32(smem + C::kDO + st * C::kTileBytes);
+          const uint32_t do_addr = PAIR ? smem_u32(smem + C::kQ + st * C::kPairStage + C::kDOCols)
+                                        : smem_u32(smem + C::kDO + st * C::kTileBytes);
           // dV += P^T dO
           if (!mbar_wait(&p_ready, g & 1, &abort_flag)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
-          for (int kk = 0; kk < kBlk / 16; ++kk)
-            mma_ts(tmem + C::tDV, tmem + C::tS + a_col(kk), sdesc_sw128(do_addr + kk * 2048, C::kSubBytes, 1024),
-                   id_kv, (t > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(&qd_empty[st]);  // S^T_t completed before P_t existed; dV_t read dO_t
-          if (t + 1 < n_tiles) {      // over the columns dV_t has just read
+          for (int kk = 0; kk < kBlk / 16; ++kk) {
+            const uint64_t bdesc = sdesc_sw128(do_addr + kk * 2048, C::kSubBytes, 1024);
+            if constexpr (PAIR)
+              mma_ts_pair(tmem + C::tDV, tmem + C::tS + a_col(kk), bdesc, id_kv, (t > 0 || kk > 0) ? 1u : 0u);
+            else
+              mma_ts(tmem + C::tDV, tmem + C::tS + a_col(kk), bdesc, id_kv, (t > 0 || kk > 0) ? 1u : 0u);
+          }
+          commit(&qd_empty[st]);  // S^T_t completed before P_t existed; dV_t read dO_t
+          if (t + 1 < n_tiles) {  // over the columns dV_t has just read
             if (!issue_s(g + 1)) { ok = false; break; }
-            if (t + 2 == n_tiles) mma_commit(&k_empty);  // the block's last S^T
+            if (t + 2 == n_tiles) commit(&k_empty);  // the block's last S^T
           }
         }
         if (!ok) break;
-        mma_commit(&done);
+        commit(&done);
         ++it;
       }
-      mma_commit(&drain);
+      if constexpr (PAIR) mma_commit_pair_local(&drain);
+      else mma_commit(&drain);
       mbar_wait_drain(&drain, 0);
     }
   } else if (warp == 2) {
     // ------------------------------------------------ MMA issuer: dP^T and dK
-    if (lane == 0) {
-      constexpr uint32_t id_s = idesc_16(kBlk, kBlk, false, false, F16);  // dP^T
-      constexpr uint32_t id_kv = idesc_16(kBlk, D, false, true, F16);     // dK
+    if (lane == 0 && (!PAIR || crank == 0)) {
+      constexpr uint32_t id_s = idesc_16(PAIR ? 2 * kBlk : kBlk, kBlk, false, false, F16);  // dP^T
+      constexpr uint32_t id_kv = idesc_16(PAIR ? 2 * kBlk : kBlk, D, false, true, F16);     // dK
       const uint32_t v_addr = smem_u32(smem + C::kV);
+      auto commit = [](uint64_t *bar) {
+        if constexpr (PAIR) mma_commit_pair_both(bar);
+        else mma_commit(bar);
+      };
       auto issue_dp = [&](int gt) -> bool {  // dP^T = V dO^T of global tile gt
         const int st = gt % NST;
         if (!mbar_wait(&qd_full[st], (gt / NST) & 1, &abort_flag)) return false;
         tc_fence_after();
-        const uint32_t do_addr = smem_u32(smem + C::kDO + st * C::kTileBytes);
+        const uint32_t do_addr = PAIR ? smem_u32(smem + C::kQ + st * C::kPairStage + C::kDORows)
+                                      : smem_u32(smem + C::kDO + st * C::kTileBytes);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk / 4) * C::kSubBytes + (kk % 4) * 32;
-          mma_ss(tmem + C::tDP, sdesc_sw128(v_addr + off, 16, 1024), sdesc_sw128(do_addr + off, 16, 1024),
-                 id_s, kk > 0);
+          const uint32_t boff = (kk / 4) * (PAIR ? C::kHalfSub : C::kSubBytes) + (kk % 4) * 32;
+          if constexpr (PAIR)
+            mma_ss_pair(tmem + C::tDP, sdesc_sw128(v_addr + off, 16, 1024), sdesc_sw128(do_addr + boff, 16, 1024),
+                        id_s, kk > 0);
+          else
+            mma_ss(tmem + C::tDP, sdesc_sw128(v_addr + off, 16, 1024), sdesc_sw128(do_addr + boff, 16, 1024), id_s,
+                   kk > 0);
         }
-        mma_commit(&dp_full);
+        commit(&dp_full);
         return true;
       };
       bool ok = true;
-      int g = 0, it = 0, kb, bh;
+      int g = 0, it = 0, rank, bh;
       for (int k = 0; ok; ++k) {
-        const int step = sched_item(sched, blockIdx.x, k, kb, bh);
+        const int step = sched_item(sched, cta, k, rank, bh);
         if (step == kDone) break;
         if (step == kSkip) continue;
-        const int n_tiles = n_tiles_all - first_tile(kb);
+        const int n_tiles = n_tiles_all - first_tile(rank);
         if (!mbar_wait(&v_full, it & 1, &abort_flag) || !issue_dp(g)) break;
-        if (n_tiles == 1) mma_commit(&v_empty);
+        if (n_tiles == 1) commit(&v_empty);
         for (int t = 0; t < n_tiles; ++t, ++g) {
           const int st = g % NST;
-          const uint32_t q_addr = smem_u32(smem + C::kQ + st * C::kTileBytes);
+          const uint32_t q_addr = PAIR ? smem_u32(smem + C::kQ + st * C::kPairStage + C::kQCols)
+                                       : smem_u32(smem + C::kQ + st * C::kTileBytes);
           // dK += dS^T Q
           if (!mbar_wait(&ds_ready, g & 1, &abort_flag)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
-          for (int kk = 0; kk < kBlk / 16; ++kk)
-            mma_ts(tmem + C::tDK, tmem + C::tDP + a_col(kk), sdesc_sw128(q_addr + kk * 2048, C::kSubBytes, 1024),
-                   id_kv, (t > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(&qd_empty[st]);  // dP^T_t completed before dS_t existed; dK_t read Q_t
-          if (t + 1 < n_tiles) {      // over the columns dK_t has just read
+          for (int kk = 0; kk < kBlk / 16; ++kk) {
+            const uint64_t bdesc = sdesc_sw128(q_addr + kk * 2048, C::kSubBytes, 1024);
+            if constexpr (PAIR)
+              mma_ts_pair(tmem + C::tDK, tmem + C::tDP + a_col(kk), bdesc, id_kv, (t > 0 || kk > 0) ? 1u : 0u);
+            else
+              mma_ts(tmem + C::tDK, tmem + C::tDP + a_col(kk), bdesc, id_kv, (t > 0 || kk > 0) ? 1u : 0u);
+          }
+          commit(&qd_empty[st]);  // dP^T_t completed before dS_t existed; dK_t read Q_t
+          if (t + 1 < n_tiles) {  // over the columns dK_t has just read
             if (!issue_dp(g + 1)) { ok = false; break; }
-            if (t + 2 == n_tiles) mma_commit(&v_empty);  // the block's last dP^T
+            if (t + 2 == n_tiles) commit(&v_empty);  // the block's last dP^T
           }
         }
         if (!ok) break;
-        mma_commit(&done);
+        commit(&done);
         ++it;
       }
-      mma_commit(&drain_kv);
+      if constexpr (PAIR) mma_commit_pair_local(&drain_kv);
+      else mma_commit(&drain_kv);
       mbar_wait_drain(&drain_kv, 0);
     }
   } else if (warp >= 4) {
@@ -366,12 +468,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_addr = static_cast<uint32_t>(wq * 32) << 16;
     const uint64_t cc = f2_pack(scale_log2, scale_log2);
     bool ok = true;
-    int g = 0, it = 0, kb, bh;
+    int g = 0, it = 0, rank, bh;
     for (int k = 0; ok; ++k) {
-      const int step = sched_item(sched, blockIdx.x, k, kb, bh);
+      const int step = sched_item(sched, cta, k, rank, bh);
       if (step == kDone) break;
       if (step == kSkip) continue;
-      const int i_first = first_tile(kb), n_tiles = n_tiles_all - i_first;
+      const int kb = block_of(rank);
+      const int i_first = first_tile(rank), n_tiles = n_tiles_all - i_first;
       const int key = kb * kBlk + kr;
       // queries below qmin see nothing of this key (causal); keys past Nk see nothing
       const int qmin0 = causal ? key - off : 0;
@@ -382,7 +485,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int qmin = (key >= Nk) ? (q0 + 64) : qmin0;
         uint32_t keep[2];  // dropout: keep bits of this key for the 64 queries, drawn while S^T is in flight
         if constexpr (DROP) dropout_col_bits<2>(drop, static_cast<uint32_t>(bh), key, q0, keep);
-        if (!mbar_wait_warp(&qd_full[st], (g / NST) & 1, &abort_flag)) { ok = false; break; }
+        if (!mbar_wait_warp(PAIR ? &ld_full[st] : &qd_full[st], (g / NST) & 1, &abort_flag)) {
+          ok = false;
+          break;
+        }
         const float4 *L4 = reinterpret_cast<const float4 *>(Lst[st] + h * 64);
         const float4 *D4 = reinterpret_cast<const float4 *>(Dst[st] + h * 64);
         if (!mbar_wait_warp(&s_full, ph, &abort_flag)) { ok = false; break; }
@@ -433,7 +539,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         tc_fence_before();
-        mbar_arrive(&p_ready);
+        if constexpr (PAIR) {  // one arrival per warp, on rank 0's barrier
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cl(cluster_addr(&p_ready, 0));
+        } else {
+          mbar_arrive(&p_ready);
+        }
         // dS^T = P^T o (dP^T - D); written in 16 bits
         // pairs over the dP^T columns this warpgroup has just read
         if (!mbar_wait_warp(&dp_full, ph, &abort_flag)) { ok = false; break; }
@@ -464,7 +575,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_st32(tmem + lane_addr + C::tDP + h * 64, ds);
         }
         tc_fence_before();
-        mbar_arrive(&ds_ready);
+        if constexpr (PAIR) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cl(cluster_addr(&ds_ready, 0));
+        } else {
+          mbar_arrive(&ds_ready);
+        }
       }
       // epilogue: warpgroup 0 stores dV, warpgroup 1 stores dK (times scale).
       // Each warp stages 32 rows x 16 columns at a time in shared memory (the
@@ -515,10 +631,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   // the staged dK / dV stores complete before the CTA's shared memory goes
   if (warp >= 4 && lane == 0) bulk_wait_all();
   tc_fence_before();
-  __syncthreads();
+  if constexpr (PAIR)
+    cluster_sync_all();  // rank 0 has drained every copy and MMA that touches either CTA
+  else
+    __syncthreads();
   if (warp == 2) {
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    if constexpr (PAIR) tmem_dealloc_pair(tmem, 512);
+    else tmem_dealloc(tmem, 512);
   }
   if (threadIdx.x == 0 && abort_flag) atomicExch(status, kErrTimeout);
 }
@@ -527,30 +647,44 @@ __global__ void __launch_bounds__(kThreads, 1)
 // K_j is needed until dQ_j, V_j only until dP_j, so they have rings of their
 // own (K one deeper) and loaders of their own: the next K blocks can be in
 // flight while dQ of the current one runs.
-template <int D>
+//
+// PAIR (d = 128, no dropout): a two-CTA cluster runs query tiles 2u and 2u + 1
+// with M = 256 MMAs, and each CTA holds half of each key block's operands:
+// for S = Q K^T its keys 64r..64r+63 (rank r; K-major, two 8 KB sub-tiles),
+// for dQ += dS K all 128 keys of head columns 64r..64r+63 (MN-major, one
+// 16 KB sub-tile) -- a K stage holds both, 32 KB -- and for dP = dO V^T the
+// value rows 64r..64r+63 (16 KB).
+template <int D, bool PAIR = false>
 struct DqCfg {
+  static_assert(!PAIR || D == 128, "the pair kernel covers d = 128");
   static constexpr int kDP = (D + 63) / 64 * 64;  // whole 64-column TMA boxes per row
   static constexpr int kKStages = (kDP == 128) ? 3 : 4;
-  static constexpr int kVStages = (kDP == 128) ? 2 : 3;
+  static constexpr int kVStages = PAIR ? 3 : ((kDP == 128) ? 2 : 3);
   static constexpr int kTileBytes = kBlk * kDP * 2;
   static constexpr int kSubBytes = kBlk * 128;
+  static constexpr int kHalfSub = kSubBytes / 2;           // 64 rows x 64 columns
+  static constexpr int kKRowsBytes = PAIR ? kTileBytes / 2 : kTileBytes;  // keys 64r.. (or the whole tile)
+  static constexpr int kKStageBytes = PAIR ? kTileBytes : kTileBytes;     // pair: rows half + columns half
+  static constexpr int kVStageBytes = PAIR ? kTileBytes / 2 : kTileBytes;
   static constexpr int kQ = 0;
   static constexpr int kDO = kQ + kTileBytes;
   static constexpr int kK = kDO + kTileBytes;
-  static constexpr int kV = kK + kKStages * kTileBytes;
-  static constexpr int kBytes = kV + kVStages * kTileBytes;
+  static constexpr int kV = kK + kKStages * kKStageBytes;
+  static constexpr int kBytes = kV + kVStages * kVStageBytes;
   static constexpr int kAlloc = kBytes + 1024;
   static constexpr uint32_t tS = 0, tDP = 256, tDQ = 384;  // S buffers at 0 and 128
 };
 
-template <int D, bool F16, bool DROP>
+template <int D, bool F16, bool DROP, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                  const __grid_constant__ CUtensorMap tmKh, const __grid_constant__ CUtensorMap tmVh,
                   const float *__restrict__ Lp, const float *__restrict__ Dp,
                   uint16_t *__restrict__ dq, int N, int Nk, const __grid_constant__ TileSched sched, float scale,
                   float scale_log2, int causal, const Dropout drop, int *status) {
-  using C = DqCfg<D>;
+  static_assert(!(PAIR && DROP), "the pair kernel has no dropout");
+  using C = DqCfg<D, PAIR>;
   using E = Elt<F16>;
   constexpr int KS = C::kKStages, VS = C::kVStages;
   extern __shared__ uint8_t smem_raw[];
@@ -566,12 +700,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int Np = n_tiles * kBlk;
   const int off = Nk - N;  // bottom-right causal alignment, as in the forward
   const int n_kb_all = (Nk + kBlk - 1) / kBlk;
-  // schedule rank 0 is a head's most expensive query tile (the last one
-  // under the causal mask)
-  auto qtile_of = [&](int rank) { return causal ? n_tiles - 1 - rank : rank; };
-  auto kblocks = [&](int qt) {
+  // A schedule unit is a query tile, or with PAIR a tile pair whose tile
+  // 2u + r runs on cluster rank r (both CTAs walk the same units). Schedule
+  // rank 0 is a head's most expensive unit (the last one under the causal
+  // mask).
+  const uint32_t crank = PAIR ? cluster_rank() : 0u;
+  const int cta = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  auto unit_of = [&](int rank) { return causal ? sched.nt - 1 - rank : rank; };
+  auto qtile_of = [&](int rank) { return PAIR ? 2 * unit_of(rank) + static_cast<int>(crank) : unit_of(rank); };
+  auto kblocks_q = [&](int qt) {
     return causal ? min(n_kb_all, (qt * kBlk + kBlk - 1 + off) / kBlk + 1) : n_kb_all;
   };
+  // key blocks of a unit: a pair walks those of its upper tile (the rows of
+  // the lower tile see the extra block fully masked: p = 0 there)
+  auto kblocks = [&](int rank) { return kblocks_q(PAIR ? 2 * unit_of(rank) + 1 : unit_of(rank)); };
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
@@ -591,7 +733,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&s_full[1], 1);
     mbar_init(&dp_full, 1);
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&ds_ready[b], 256);
+      mbar_init(&ds_ready[b], PAIR ? 2 * 8 : 256);  // pair: one arrival per elementwise warp of each CTA
       mbar_init(&sfree[b], 1);
     }
     mbar_init(&done, 1);
@@ -600,13 +742,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_mbar_init();
   }
   if (warp == 2) {
-    tmem_alloc(&tmem_base_s, 512);
-    tmem_relinquish();
+    if constexpr (PAIR) {
+      tmem_alloc_pair(&tmem_base_s, 512);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(&tmem_base_s, 512);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
-  __syncthreads();
+  if constexpr (PAIR)
+    cluster_sync_all();  // the other CTA arrives on this one's barriers only once they exist
+  else
+    __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base_s;
+  // a pair's copies complete on rank 0's barriers, which only rank 0 drains
+  const bool drains = !PAIR || crank == 0;
+  // this CTA's rows tile: Q or dO of `row` into smem + dst, counted on `bar`
+  auto load_tile = [&](uint32_t dst, const CUtensorMap *map, uint64_t *bar, int row, int bh) {
+    if constexpr (PAIR) {
+      if (crank == 0) mbar_arrive_expect_tx(bar, 2 * C::kTileBytes);
+      const uint32_t b0 = cluster_addr(bar, 0);
+      for (int x = 0; x < D; x += 64) tma_load_3d_pair(smem + dst + (x / 64) * C::kSubBytes, map, b0, x, row, bh);
+    } else {
+      mbar_arrive_expect_tx(bar, C::kTileBytes);
+      load_rows(smem + dst, map, bar, D, row, bh);
+    }
+  };
 
   // Every role walks the same items (query tiles); key blocks are counted
   // across items (g) for the K/V rings, the S buffers and the per-block
@@ -623,13 +786,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       int g = 0, nq = 0, ndo = 0, rank, bh;  // K blocks, Q tiles, dO tiles issued
       for (int k = 0; ok; ++k) {
-        const int step = sched_item(sched, blockIdx.x, k, rank, bh);
+        const int step = sched_item(sched, cta, k, rank, bh);
         if (step == kDone) break;
         if (step == kSkip) continue;
-        const int qt = qtile_of(rank), n_kb = kblocks(qt);
+        const int qt = qtile_of(rank), n_kb = kblocks(rank);
         {  // the next tile's Q and dO are read once: start them towards L2 now
           int nr, nbh, ns, k2 = k + 1;
-          while ((ns = sched_item(sched, blockIdx.x, k2, nr, nbh)) == kSkip) ++k2;
+          while ((ns = sched_item(sched, cta, k2, nr, nbh)) == kSkip) ++k2;
           if (ns == kItem)
             for (int x = 0; x < D; x += 64) {
               tma_prefetch_l2_3d(&tmQ, x, qtile_of(nr) * kBlk, nbh);
@@ -637,26 +800,38 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         if (nq > 0 && !mbar_wait(&q_empty, (nq - 1) & 1, &abort_flag)) break;
-        mbar_arrive_expect_tx(&q_full, C::kTileBytes);
-        load_rows(smem + C::kQ, &tmQ, &q_full, D, qt * kBlk, bh);
+        load_tile(C::kQ, &tmQ, &q_full, qt * kBlk, bh);
         ++nq;
         for (int j = 0; j < n_kb; ++j, ++g) {
           const int st = g % KS;
           if (g >= KS && !mbar_wait(&k_empty[st], ((g / KS) & 1) ^ 1, &abort_flag)) { ok = false; break; }
-          mbar_arrive_expect_tx(&k_full[st], C::kTileBytes);
-          load_rows(smem + C::kK + st * C::kTileBytes, &tmK, &k_full[st], D, j * kBlk, bh);
+          if constexpr (PAIR) {
+            // keys 64r..64r+63 (for S) and head columns 64r..64r+63 of all
+            // the block's keys (for dQ), both on rank 0's barrier
+            if (crank == 0) mbar_arrive_expect_tx(&k_full[st], 2 * C::kKStageBytes);
+            const uint32_t b0 = cluster_addr(&k_full[st], 0);
+            uint8_t *dst = smem + C::kK + st * C::kKStageBytes;
+            for (int x = 0; x < D; x += 64)
+              tma_load_3d_pair(dst + (x / 64) * C::kHalfSub, &tmKh, b0, x, j * kBlk + 64 * static_cast<int>(crank),
+                               bh);
+            tma_load_3d_pair(dst + C::kKRowsBytes, &tmK, b0, 64 * static_cast<int>(crank), j * kBlk, bh);
+          } else {
+            mbar_arrive_expect_tx(&k_full[st], C::kTileBytes);
+            load_rows(smem + C::kK + st * C::kKStageBytes, &tmK, &k_full[st], D, j * kBlk, bh);
+          }
           if (j == 0) {  // dO after the first K block: S_0 needs Q and K_0 first
             if (ndo > 0 && !mbar_wait(&do_empty, (ndo - 1) & 1, &abort_flag)) { ok = false; ++g; break; }
-            mbar_arrive_expect_tx(&do_full, C::kTileBytes);
-            load_rows(smem + C::kDO, &tmdO, &do_full, D, qt * kBlk, bh);
+            load_tile(C::kDO, &tmdO, &do_full, qt * kBlk, bh);
             ++ndo;
           }
         }
       }
       // teardown: every issued copy must land before the CTA's memory is released
-      if (nq > 0) mbar_wait_drain(&q_full, (nq - 1) & 1);
-      if (ndo > 0) mbar_wait_drain(&do_full, (ndo - 1) & 1);
-      for (int j = max(0, g - KS); j < g; ++j) mbar_wait_drain(&k_full[j % KS], (j / KS) & 1);
+      if (drains) {
+        if (nq > 0) mbar_wait_drain(&q_full, (nq - 1) & 1);
+        if (ndo > 0) mbar_wait_drain(&do_full, (ndo - 1) & 1);
+        for (int j = max(0, g - KS); j < g; ++j) mbar_wait_drain(&k_full[j % KS], (j / KS) & 1);
+      }
     }
   } else if (warp == 3) {
     // ---------------------------------------------------------------- loader: V
@@ -665,18 +840,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       int g = 0, rank, bh;
       for (int k = 0; ok; ++k) {
-        const int step = sched_item(sched, blockIdx.x, k, rank, bh);
+        const int step = sched_item(sched, cta, k, rank, bh);
         if (step == kDone) break;
         if (step == kSkip) continue;
-        const int n_kb = kblocks(qtile_of(rank));
+        const int n_kb = kblocks(rank);
         for (int j = 0; j < n_kb; ++j, ++g) {
           const int st = g % VS;
           if (g >= VS && !mbar_wait(&v_empty[st], ((g / VS) & 1) ^ 1, &abort_flag)) { ok = false; break; }
-          mbar_arrive_expect_tx(&v_full[st], C::kTileBytes);
-          load_rows(smem + C::kV + st * C::kTileBytes, &tmV, &v_full[st], D, j * kBlk, bh);
+          if constexpr (PAIR) {  // value rows 64r..64r+63, on rank 0's barrier
+            if (crank == 0) mbar_arrive_expect_tx(&v_full[st], 2 * C::kVStageBytes);
+            const uint32_t b0 = cluster_addr(&v_full[st], 0);
+            for (int x = 0; x < D; x += 64)
+              tma_load_3d_pair(smem + C::kV + st * C::kVStageBytes + (x / 64) * C::kHalfSub, &tmVh, b0, x,
+                               j * kBlk + 64 * static_cast<int>(crank), bh);
+          } else {
+            mbar_arrive_expect_tx(&v_full[st], C::kTileBytes);
+            load_rows(smem + C::kV + st * C::kVStageBytes, &tmV, &v_full[st], D, j * kBlk, bh);
+          }
         }
       }
-      for (int j = max(0, g - VS); j < g; ++j) mbar_wait_drain(&v_full[j % VS], (j / VS) & 1);
+      if (drains)
+        for (int j = max(0, g - VS); j < g; ++j) mbar_wait_drain(&v_full[j % VS], (j / VS) & 1);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------ MMA issuer: S, dP
@@ -686,70 +870,82 @@ __global__ void __launch_bounds__(kThreads, 1)
     // MMAs: S_{g+2} reuses the buffer of dS_g and so waits for dQ_g to
     // complete (sfree), and dP_{g+1} reuses the dP columns, which the
     // elementwise warps have read once dS_g is ready.
-    if (lane == 0) {
-      constexpr uint32_t id_s = idesc_16(kBlk, kBlk, false, false, F16);  // S, dP
+    // With PAIR only rank 0 issues (M = 256 over both CTAs), and commits
+    // arrive on the barrier of that name in both CTAs.
+    if (lane == 0 && (!PAIR || crank == 0)) {
+      constexpr uint32_t id_s = idesc_16(PAIR ? 2 * kBlk : kBlk, kBlk, false, false, F16);  // S, dP
+      constexpr int kBSub = PAIR ? C::kHalfSub : C::kSubBytes;  // B operand sub-tile stride
       const uint32_t q_addr = smem_u32(smem + C::kQ), do_addr = smem_u32(smem + C::kDO);
+      auto commit = [](uint64_t *bar) {
+        if constexpr (PAIR) mma_commit_pair_both(bar);
+        else mma_commit(bar);
+      };
+      auto mma = [](uint32_t d, uint64_t a, uint64_t b, uint32_t id, uint32_t acc) {
+        if constexpr (PAIR) mma_ss_pair(d, a, b, id, acc);
+        else mma_ss(d, a, b, id, acc);
+      };
       auto issue_s = [&](int gj) -> bool {  // S of global block gj = Q K^T into buffer gj&1
         if (gj >= 2 && !mbar_wait(&sfree[gj & 1], ((gj >> 1) - 1) & 1, &abort_flag)) return false;
         const int st = gj % KS;
         if (!mbar_wait(&k_full[st], (gj / KS) & 1, &abort_flag)) return false;
         tc_fence_after();
-        const uint32_t k_addr = smem_u32(smem + C::kK + st * C::kTileBytes);
+        const uint32_t k_addr = smem_u32(smem + C::kK + st * C::kKStageBytes);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk / 4) * C::kSubBytes + (kk % 4) * 32;
-          mma_ss(tmem + C::tS + (gj & 1) * 128, sdesc_sw128(q_addr + off, 16, 1024),
-                 sdesc_sw128(k_addr + off, 16, 1024), id_s, kk > 0);
+          const uint32_t aoff = (kk / 4) * C::kSubBytes + (kk % 4) * 32, boff = (kk / 4) * kBSub + (kk % 4) * 32;
+          mma(tmem + C::tS + (gj & 1) * 128, sdesc_sw128(q_addr + aoff, 16, 1024),
+              sdesc_sw128(k_addr + boff, 16, 1024), id_s, kk > 0);
         }
-        mma_commit(&s_full[gj & 1]);
+        commit(&s_full[gj & 1]);
         return true;
       };
       auto issue_dp = [&](int gj) -> bool {  // dP = dO V^T
         const int st = gj % VS;
         if (!mbar_wait(&v_full[st], (gj / VS) & 1, &abort_flag)) return false;
         tc_fence_after();
-        const uint32_t v_addr = smem_u32(smem + C::kV + st * C::kTileBytes);
+        const uint32_t v_addr = smem_u32(smem + C::kV + st * C::kVStageBytes);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk / 4) * C::kSubBytes + (kk % 4) * 32;
-          mma_ss(tmem + C::tDP, sdesc_sw128(do_addr + off, 16, 1024), sdesc_sw128(v_addr + off, 16, 1024),
-                 id_s, kk > 0);
+          const uint32_t aoff = (kk / 4) * C::kSubBytes + (kk % 4) * 32, boff = (kk / 4) * kBSub + (kk % 4) * 32;
+          mma(tmem + C::tDP, sdesc_sw128(do_addr + aoff, 16, 1024), sdesc_sw128(v_addr + boff, 16, 1024), id_s,
+              kk > 0);
         }
-        mma_commit(&dp_full);
-        mma_commit(&v_empty[st]);
+        commit(&dp_full);
+        commit(&v_empty[st]);
         return true;
       };
       bool ok = true;
       int g = 0, it = 0, rank, bh;
       for (int k = 0; ok; ++k) {
-        const int step = sched_item(sched, blockIdx.x, k, rank, bh);
+        const int step = sched_item(sched, cta, k, rank, bh);
         if (step == kDone) break;
         if (step == kSkip) continue;
-        const int n_kb = kblocks(qtile_of(rank));
+        const int n_kb = kblocks(rank);
         if (!mbar_wait(&q_full, it & 1, &abort_flag) || !issue_s(g)) break;
-        if (n_kb == 1) mma_commit(&q_empty);
+        if (n_kb == 1) commit(&q_empty);
         if (!mbar_wait(&do_full, it & 1, &abort_flag) || !issue_dp(g)) break;
-        if (n_kb == 1) mma_commit(&do_empty);
+        if (n_kb == 1) commit(&do_empty);
         if (n_kb > 1) {
           if (!issue_s(g + 1)) break;
-          if (n_kb == 2) mma_commit(&q_empty);
+          if (n_kb == 2) commit(&q_empty);
         }
         for (int j = 0; j < n_kb; ++j, ++g) {
           if (!mbar_wait(&ds_ready[g & 1], (g >> 1) & 1, &abort_flag)) { ok = false; break; }
           if (j + 1 < n_kb) {  // dP_j has been read into dS_j
             tc_fence_after();
             if (!issue_dp(g + 1)) { ok = false; break; }
-            if (j + 2 == n_kb) mma_commit(&do_empty);  // the tile's last dP
+            if (j + 2 == n_kb) commit(&do_empty);  // the tile's last dP
           }
           if (j + 2 < n_kb) {
             if (!issue_s(g + 2)) { ok = false; break; }
-            if (j + 3 == n_kb) mma_commit(&q_empty);  // the tile's last S
+            if (j + 3 == n_kb) commit(&q_empty);  // the tile's last S
           }
         }
         if (!ok) break;
         ++it;
       }
-      mma_commit(&drain);
+      if constexpr (PAIR) mma_commit_pair_local(&drain);
+      else mma_commit(&drain);
       mbar_wait_drain(&drain, 0);
     }
   } else if (warp == 2) {
@@ -758,32 +954,46 @@ __global__ void __launch_bounds__(kThreads, 1)
     // MN-major). The first of a tile overwrites the accumulator: it waits for
     // dS_0, which the elementwise warps only produce after storing the
     // previous tile's dQ.
-    if (lane == 0) {
-      constexpr uint32_t id_q = idesc_16(kBlk, D, false, true, F16);
+    if (lane == 0 && (!PAIR || crank == 0)) {
+      constexpr uint32_t id_q = idesc_16(PAIR ? 2 * kBlk : kBlk, D, false, true, F16);
       bool ok = true;
       int g = 0, rank, bh;
       for (int k = 0; ok; ++k) {
-        const int step = sched_item(sched, blockIdx.x, k, rank, bh);
+        const int step = sched_item(sched, cta, k, rank, bh);
         if (step == kDone) break;
         if (step == kSkip) continue;
-        const int n_kb = kblocks(qtile_of(rank));
+        const int n_kb = kblocks(rank);
         for (int j = 0; j < n_kb; ++j, ++g) {
           const int st = g % KS;
           if (!mbar_wait(&ds_ready[g & 1], (g >> 1) & 1, &abort_flag)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t k_addr = smem_u32(smem + C::kK + st * C::kTileBytes);
+          // the pair's B: this CTA's head columns of all the block's keys (MN-major)
+          const uint32_t k_addr = smem_u32(smem + C::kK + st * C::kKStageBytes) + (PAIR ? C::kKRowsBytes : 0);
 #pragma unroll
-          for (int kk = 0; kk < kBlk / 16; ++kk)
-            mma_ts(tmem + C::tDQ, tmem + C::tS + (g & 1) * 128 + a_col(kk),
-                   sdesc_sw128(k_addr + kk * 2048, C::kSubBytes, 1024), id_q, (j > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < kBlk / 16; ++kk) {
+            const uint64_t bdesc = sdesc_sw128(k_addr + kk * 2048, C::kSubBytes, 1024);
+            if constexpr (PAIR)
+              mma_ts_pair(tmem + C::tDQ, tmem + C::tS + (g & 1) * 128 + a_col(kk), bdesc, id_q,
+                          (j > 0 || kk > 0) ? 1u : 0u);
+            else
+              mma_ts(tmem + C::tDQ, tmem + C::tS + (g & 1) * 128 + a_col(kk), bdesc, id_q,
+                     (j > 0 || kk > 0) ? 1u : 0u);
+          }
           // S_g completed before dS_g existed, so K_g is free once dQ_g is
-          mma_commit(&k_empty[st]);
-          mma_commit(&sfree[g & 1]);
+          if constexpr (PAIR) {
+            mma_commit_pair_both(&k_empty[st]);
+            mma_commit_pair_local(&sfree[g & 1]);  // only rank 0's S issuer waits on it
+          } else {
+            mma_commit(&k_empty[st]);
+            mma_commit(&sfree[g & 1]);
+          }
         }
         if (!ok) break;
-        mma_commit(&done);
+        if constexpr (PAIR) mma_commit_pair_both(&done);
+        else mma_commit(&done);
       }
-      mma_commit(&drain_q);
+      if constexpr (PAIR) mma_commit_pair_local(&drain_q);
+      else mma_commit(&drain_q);
       mbar_wait_drain(&drain_q, 0);
     }
   } else if (warp >= 4) {
@@ -797,9 +1007,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     // loaded one item ahead so the epilogue hides their latency
     auto row_terms = [&](int k, float &nl, float &drow) {
       int rk, hb, st;
-      while ((st = sched_item(sched, blockIdx.x, k, rk, hb)) == kSkip) ++k;
+      while ((st = sched_item(sched, cta, k, rk, hb)) == kSkip) ++k;
       if (st == kDone) return;
-      const size_t prow = static_cast<size_t>(hb) * Np + qtile_of(rk) * kBlk + r;
+      const int qt = qtile_of(rk);
+      if (qt >= n_tiles) {  // a pair's second tile past the last one: no rows
+        nl = -INFINITY;
+        drow = 0.f;
+        return;
+      }
+      const size_t prow = static_cast<size_t>(hb) * Np + qt * kBlk + r;
       nl = Lp[prow];
       drow = Dp[prow];
     };
@@ -808,10 +1024,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     int g = 0, it = 0, rank, bh;
     for (int k = 0; ok; ++k) {
-      const int step = sched_item(sched, blockIdx.x, k, rank, bh);
+      const int step = sched_item(sched, cta, k, rank, bh);
       if (step == kDone) break;
       if (step == kSkip) continue;
-      const int qt = qtile_of(rank), n_kb = kblocks(qt);
+      const int qt = qtile_of(rank), n_kb = kblocks(rank);
       const int q = qt * kBlk + r;
       const float nl = nl_next, drow = drow_next;
       const uint64_t nn = f2_pack(nl, nl), dd2 = f2_pack(drow, drow);
@@ -862,7 +1078,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_st32(tmem + lane_addr + sb, ds);  // over scores already read
         }
         tc_fence_before();
-        mbar_arrive(&ds_ready[g & 1]);
+        if constexpr (PAIR) {  // one arrival per warp, on rank 0's barrier
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cl(cluster_addr(&ds_ready[g & 1], 0));
+        } else {
+          mbar_arrive(&ds_ready[g & 1]);
+        }
       }
       if (ok) row_terms(k + 1, nl_next, drow_next);
       // epilogue: dQ = scale * accumulator; warpgroup h stores head columns
@@ -879,20 +1100,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   tc_fence_before();
-  __syncthreads();
+  if constexpr (PAIR)
+    cluster_sync_all();  // rank 0 has drained every copy and MMA that touches either CTA
+  else
+    __syncthreads();
   if (warp == 2) {
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    if constexpr (PAIR) tmem_dealloc_pair(tmem, 512);
+    else tmem_dealloc(tmem, 512);
   }
   if (threadIdx.x == 0 && abort_flag) atomicExch(status, kErrTimeout);
 }
 
 template <int D, bool F16, bool DROP>
 cudaError_t launch(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtensorMap &tmV,
-                   const CUtensorMap &tmdO, const CUtensorMap &tmdK, const CUtensorMap &tmdV, const void *o,
-                   const void *dO, const float *lse, void *dq,
-                   void *dk, void *dv, float *Lp, float *Dp, int B, int H, int N, int Nk, float scale,
-                   int causal, const Dropout &drop, int *status, int num_sms, cudaStream_t stream) {
+                   const CUtensorMap &tmdO, const CUtensorMap &tmdK, const CUtensorMap &tmdV, const HalfMaps *half,
+                   const void *o, const void *dO, const float *lse, void *dq, void *dk, void *dv, float *Lp,
+                   float *Dp, int B, int H, int N, int Nk, float scale, int causal, const Dropout &drop, int *status,
+                   int num_sms, cudaStream_t stream) {
   const int n_tiles = (N + kBlk - 1) / kBlk;
   const int Np = n_tiles * kBlk;
   const float scale_log2 = scale * kLog2e;
@@ -909,28 +1134,85 @@ cudaError_t launch(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtenso
   // key blocks (dK/dV pass) or query tiles (dQ pass); an item costs the tiles
   // it visits plus about one for its epilogue
   const int BH = B * H, off = Nk - N, n_kb_all = (Nk + kBlk - 1) / kBlk;
-  const TileSched sched_kv = sched_cached(1, BH, N, Nk, causal != 0, n_kb_all, num_sms, [&](int kb) {
-    const int i_first = causal ? std::max(0, kb * kBlk - off) / kBlk : 0;
-    return static_cast<long long>(n_tiles - i_first) + 1;
-  });
+  auto kblocks_q = [&](int qt) {
+    return causal ? std::min(n_kb_all, (qt * kBlk + kBlk - 1 + off) / kBlk + 1) : n_kb_all;
+  };
+  auto first_tile = [&](int kb) { return causal ? std::max(0, kb * kBlk - off) / kBlk : 0; };
+  bool kv_done = false;
+  if constexpr (D == 128 && !DROP && FA_PAIR_KERNELS) {
+    // dK/dV pass on two-CTA clusters (key block pairs, M = 256 MMAs) when
+    // the heads have at least two key blocks
+    auto kpair = bwd_dkdv_kernel<D, F16, false, true>;
+    static SmemOnce smem_kvp;
+    if (half && n_kb_all >= 2) {
+      if ((e = set_smem_once(reinterpret_cast<const void *>(kpair), DkdvCfg<D, true>::kAlloc, &smem_kvp)) !=
+          cudaSuccess)
+        return e;
+      const int clusters = pair_grid(reinterpret_cast<const void *>(kpair), DkdvCfg<D, true>::kAlloc, kThreads, num_sms);
+      if (clusters >= 1) {
+        const int np = (n_kb_all + 1) / 2;
+        // a pair visits the query tiles of its lower block
+        const TileSched sched_kvp = sched_cached(5, BH, N, Nk, causal != 0, np, clusters, [&](int r) {
+          return static_cast<long long>(n_tiles - first_tile(2 * r)) + 1;
+        });
+        timing_begin(stream);
+        e = launch_pair_grid(kpair, sched_kvp.G, kThreads, DkdvCfg<D, true>::kAlloc, stream, tmQ, tmK, tmV, tmdO,
+                             tmdK, tmdV, half->q, half->dO, Lp, Dp, N, Nk, sched_kvp, scale, scale_log2, causal,
+                             drop, status);
+        timing_end(stream);
+        if (e != cudaSuccess || (e = cudaGetLastError()) != cudaSuccess) return e;
+        kv_done = true;
+      }
+    }
+  }
+  if (!kv_done) {
+    const TileSched sched_kv = sched_cached(1, BH, N, Nk, causal != 0, n_kb_all, num_sms, [&](int kb) {
+      return static_cast<long long>(n_tiles - first_tile(kb)) + 1;
+    });
+    auto kdkdv = bwd_dkdv_kernel<D, F16, DROP, false>;
+    static SmemOnce smem_kv;
+    if ((e = set_smem_once(reinterpret_cast<const void *>(kdkdv), DkdvCfg<D>::kAlloc, &smem_kv)) != cudaSuccess)
+      return e;
+    timing_begin(stream);
+    kdkdv<<<sched_kv.G, kThreads, DkdvCfg<D>::kAlloc, stream>>>(tmQ, tmK, tmV, tmdO, tmdK, tmdV, tmQ, tmdO, Lp, Dp,
+                                                                 N, Nk, sched_kv, scale, scale_log2, causal, drop,
+                                                                 status);
+    timing_end(stream);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  if constexpr (D == 128 && !DROP && FA_PAIR_KERNELS) {
+    // dQ pass on two-CTA clusters (tile pairs, M = 256 MMAs) when the heads
+    // have at least two query tiles
+    auto kpair = bwd_dq_kernel<D, F16, false, true>;
+    static SmemOnce smem_qp;
+    if (half && n_tiles >= 2) {
+      if ((e = set_smem_once(reinterpret_cast<const void *>(kpair), DqCfg<D, true>::kAlloc, &smem_qp)) !=
+          cudaSuccess)
+        return e;
+      const int clusters = pair_grid(reinterpret_cast<const void *>(kpair), DqCfg<D, true>::kAlloc, kThreads, num_sms);
+      if (clusters >= 1) {
+        const int np = (n_tiles + 1) / 2;
+        const TileSched sched_qp = sched_cached(4, BH, N, Nk, causal != 0, np, clusters, [&](int rank) {
+          return static_cast<long long>(kblocks_q(2 * (np - 1 - rank) + 1)) + 1;
+        });
+        timing_begin(stream);
+        e = launch_pair_grid(kpair, sched_qp.G, kThreads, DqCfg<D, true>::kAlloc, stream, tmQ, tmK, tmV, tmdO,
+                             half->k, half->v, Lp, Dp, static_cast<uint16_t *>(dq), N, Nk, sched_qp, scale,
+                             scale_log2, causal, drop, status);
+        timing_end(stream);
+        if (e != cudaSuccess) return e;
+        return cudaGetLastError();
+      }
+    }
+  }
   const TileSched sched_q = sched_cached(2, BH, N, Nk, causal != 0, n_tiles, num_sms, [&](int rank) {
-    const int qt = n_tiles - 1 - rank;
-    const int nkb = causal ? std::min(n_kb_all, (qt * kBlk + kBlk - 1 + off) / kBlk + 1) : n_kb_all;
-    return static_cast<long long>(nkb) + 1;
+    return static_cast<long long>(kblocks_q(n_tiles - 1 - rank)) + 1;
   });
-  auto kdkdv = bwd_dkdv_kernel<D, F16, DROP>;
-  auto kdq = bwd_dq_kernel<D, F16, DROP>;
-  static SmemOnce smem_kv, smem_q;
-  if ((e = set_smem_once(reinterpret_cast<const void *>(kdkdv), DkdvCfg<D>::kAlloc, &smem_kv)) != cudaSuccess ||
-      (e = set_smem_once(reinterpret_cast<const void *>(kdq), DqCfg<D>::kAlloc, &smem_q)) != cudaSuccess)
-    return e;
+  auto kdq = bwd_dq_kernel<D, F16, DROP, false>;
+  static SmemOnce smem_q;
+  if ((e = set_smem_once(reinterpret_cast<const void *>(kdq), DqCfg<D>::kAlloc, &smem_q)) != cudaSuccess) return e;
   timing_begin(stream);
-  kdkdv<<<sched_kv.G, kThreads, DkdvCfg<D>::kAlloc, stream>>>(tmQ, tmK, tmV, tmdO, tmdK, tmdV, Lp, Dp, N, Nk,
-                                                               sched_kv, scale, scale_log2, causal, drop, status);
-  timing_end(stream);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  timing_begin(stream);
-  kdq<<<sched_q.G, kThreads, DqCfg<D>::kAlloc, stream>>>(tmQ, tmK, tmV, tmdO, Lp, Dp,
+  kdq<<<sched_q.G, kThreads, DqCfg<D>::kAlloc, stream>>>(tmQ, tmK, tmV, tmdO, tmK, tmV, Lp, Dp,
                                                           static_cast<uint16_t *>(dq), N, Nk, sched_q, scale,
                                                           scale_log2, causal, drop, status);
   timing_end(stream);
@@ -939,13 +1221,13 @@ cudaError_t launch(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtenso
 
 template <bool DROP>
 cudaError_t dispatch(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtensorMap &tmV,
-                     const CUtensorMap &tmdO, const CUtensorMap &tmdK, const CUtensorMap &tmdV, const void *o,
-                     const void *dO, const float *lse, void *dq, void *dk, void *dv, float *Lp, float *Dp, int B,
-                     int H, int N, int Nk, int d, float scale, int causal, bool f16, const Dropout &drop,
-                     int *status, int num_sms, cudaStream_t stream) {
+                     const CUtensorMap &tmdO, const CUtensorMap &tmdK, const CUtensorMap &tmdV, const HalfMaps *half,
+                     const void *o, const void *dO, const float *lse, void *dq, void *dk, void *dv, float *Lp,
+                     float *Dp, int B, int H, int N, int Nk, int d, float scale, int causal, bool f16,
+                     const Dropout &drop, int *status, int num_sms, cudaStream_t stream) {
 #define FA_BWD_LAUNCH(DD, FF)                                                                                  \
-  return launch<DD, FF, DROP>(tmQ, tmK, tmV, tmdO, tmdK, tmdV, o, dO, lse, dq, dk, dv, Lp, Dp, B, H, N, Nk,  \
-                              scale, causal, drop, status, num_sms, stream)
+  return launch<DD, FF, DROP>(tmQ, tmK, tmV, tmdO, tmdK, tmdV, half, o, dO, lse, dq, dk, dv, Lp, Dp, B, H, N,  \
+                              Nk, scale, causal, drop, status, num_sms, stream)
   if (f16) {
     if (d == 64) FA_BWD_LAUNCH(64, true);
     if (d == 96) FA_BWD_LAUNCH(96, true);
@@ -961,16 +1243,16 @@ cudaError_t dispatch(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUten
 
 cudaError_t launch_bwd_16(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtensorMap &tmV,
                           const CUtensorMap &tmdO, const CUtensorMap &tmdK, const CUtensorMap &tmdV,
-                          const void *o, const void *dO, const float *lse,
-                          void *dq, void *dk, void *dv, float *Lp, float *Dp, int B, int H, int N, int Nk, int d,
-                          float scale, int causal, bool f16, const Dropout *drop, int *status, int num_sms,
-                          cudaStream_t stream, int *launches) {
+                          const HalfMaps *half, const void *o, const void *dO, const float *lse, void *dq, void *dk,
+                          void *dv, float *Lp, float *Dp, int B, int H, int N, int Nk, int d, float scale, int causal,
+                          bool f16, const Dropout *drop, int *status, int num_sms, cudaStream_t stream,
+                          int *launches) {
   *launches += 3;
   if (drop)
-    return dispatch<true>(tmQ, tmK, tmV, tmdO, tmdK, tmdV, o, dO, lse, dq, dk, dv, Lp, Dp, B, H, N, Nk, d, scale,
-                          causal, f16, *drop, status, num_sms, stream);
-  return dispatch<false>(tmQ, tmK, tmV, tmdO, tmdK, tmdV, o, dO, lse, dq, dk, dv, Lp, Dp, B, H, N, Nk, d, scale,
-                         causal, f16, Dropout{}, status, num_sms, stream);
+    return dispatch<true>(tmQ, tmK, tmV, tmdO, tmdK, tmdV, half, o, dO, lse, dq, dk, dv, Lp, Dp, B, H, N, Nk, d,
+                          scale, causal, f16, *drop, status, num_sms, stream);
+  return dispatch<false>(tmQ, tmK, tmV, tmdO, tmdK, tmdV, half, o, dO, lse, dq, dk, dv, Lp, Dp, B, H, N, Nk, d,
+                         scale, causal, f16, Dropout{}, status, num_sms, stream);
 }
 
 }  // namespace fa

@@ -76,26 +76,37 @@ constexpr float kLn2 = 0.69314718055994531f;
 // ring and the V ring, under the 227 KB limit: at d = 96 and 128, 2 Q + 3 K +
 // 2 V tiles; at d = 256, 1 Q tile + 3 K + 2 V units. Tensor memory holds
 // kSBuf score buffers of 128 columns and O after them (512 columns).
-template <int D, bool DROP = false>
+//
+// PAIR (d = 128, no dropout): a cluster of two CTAs runs the two query tiles
+// of a tile pair with M = 256 MMAs. Each CTA then holds only its half of each
+// key tile's operands: for S = Q K^T the keys 64r..64r+63 (rank r; K-major,
+// two 8 KB sub-tiles of 64 rows), for O += P V the head columns 64r..64r+63
+// of all 128 keys (MN-major, one 16 KB sub-tile). Both rings hold 16 KB
+// stages, four of each.
+template <int D, bool DROP = false, bool PAIR = false>
 struct FwdSmem {
+  static_assert(!PAIR || (D == 128 && !DROP), "the pair kernel covers d = 128 without dropout");
   static constexpr int kDP = (D + 63) / 64 * 64;
   static constexpr int kUnits = kDP > 128 ? kDP / 128 : 1;  // K / V ring units per key tile
   static constexpr int kUnitCols = kDP / kUnits;
   static constexpr int kUnitBytes = kBlockN * kUnitCols * 2;
+  static constexpr int kKBytes = PAIR ? kUnitBytes / 2 : kUnitBytes;  // one K ring stage
+  static constexpr int kVBytes = PAIR ? kUnitBytes / 2 : kUnitBytes;  // one V ring stage
+  static constexpr int kKSub = PAIR ? (kBlockN / 2) * 128 : kBlockN * 128;  // bytes of one K sub-tile
   static constexpr int kQBytes = kBlockM * kDP * 2;
   static constexpr int kSK = (kUnits == 1 ? D : kUnitCols) / 16;  // k-steps of S per unit
   static constexpr int kPVN = kUnits == 1 ? D : kUnitCols;         // N of one P V product
   static constexpr int kSBuf = kDP > 128 ? 2 : 3;
   // with dropout the keep-mask ring needs 6 KB: one Q buffer, and at d = 256
   // a K ring of two units
-  static constexpr int kQBuf = (kDP > 128 || DROP) ? 1 : FA_FWD_QBUF;
-  static constexpr int kKStages = (kDP > 128 && DROP) ? 2 : 3;
-  static constexpr int kVStages = kDP > 128 ? 2 : ((kDP == 128 && (kQBuf == 2 || DROP)) ? 2 : 3);
+  static constexpr int kQBuf = PAIR ? 2 : ((kDP > 128 || DROP) ? 1 : FA_FWD_QBUF);
+  static constexpr int kKStages = PAIR ? 4 : ((kDP > 128 && DROP) ? 2 : 3);
+  static constexpr int kVStages = PAIR ? 4 : (kDP > 128 ? 2 : ((kDP == 128 && (kQBuf == 2 || DROP)) ? 2 : 3));
   static constexpr int kSubBytes = kBlockN * 128;  // one 128-row x 64-column sub-tile
   static constexpr int kQ = 0;
   static constexpr int kK = kQ + kQBuf * kQBytes;
-  static constexpr int kV = kK + kKStages * kUnitBytes;
-  static constexpr int kMask = kV + kVStages * kUnitBytes;
+  static constexpr int kV = kK + kKStages * kKBytes;
+  static constexpr int kMask = kV + kVStages * kVBytes;
   static constexpr int kMaskBytes = DROP ? kMaskSlots * kBlockM * 16 : 0;
   static constexpr int kBytes = kMask + kMaskBytes;
   static constexpr int kAlloc = kBytes + 1024;  // slack for 1024-byte alignment
@@ -108,14 +119,14 @@ __device__ __forceinline__ void load_cols(uint8_t *dst, const CUtensorMap *map, 
   for (int x = c0; x < c1; x += 64) tma_load_3d(dst + ((x - c0) / 64) * (kBlockN * 128), map, bar, x, row, bh);
 }
 
-template <int D, bool F16, bool DROP>
+template <int D, bool F16, bool DROP, bool PAIR>
 __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ,
                     const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, uint16_t *__restrict__ o,
                     float *__restrict__ lse, int N, int Nk, const __grid_constant__ TileSched sched, float scale,
                     float scale_log2, int causal, const Dropout drop, int *status) {
-  using L = FwdSmem<D, DROP>;
+  using L = FwdSmem<D, DROP, PAIR>;
   using E = Elt<F16>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -129,17 +140,24 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
   __shared__ int abort_flag;
 
   const int warp = warp_id(), lane = lane_id();
-  const int n_qtiles = sched.nt;
-  // schedule rank 0 is a head's most expensive query tile (the last one
-  // under the causal mask)
-  auto qtile_of = [&](int rank) { return causal ? n_qtiles - 1 - rank : rank; };
+  // A schedule unit is a query tile, or with PAIR a tile pair (2u, 2u + 1)
+  // whose tile 2u + r runs on cluster rank r; both CTAs of a pair walk the
+  // same units. Schedule rank 0 is a head's most expensive unit (the last one
+  // under the causal mask).
+  const uint32_t crank = PAIR ? cluster_rank() : 0u;
+  const int cta = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  auto unit_of = [&](int rank) { return causal ? sched.nt - 1 - rank : rank; };
+  auto qtile_of = [&](int rank) { return PAIR ? 2 * unit_of(rank) + static_cast<int>(crank) : unit_of(rank); };
   // N query rows, Nk >= N keys under the causal mask; query i sees keys up to
   // i + (Nk - N) (bottom-right alignment; with Nk = N the usual triangle)
   const int off = Nk - N;
   const int n_ktiles_all = (Nk + kBlockN - 1) / kBlockN;
-  auto ktiles = [&](int qtile) {
+  auto ktiles_q = [&](int qtile) {
     return causal ? min(n_ktiles_all, (qtile * kBlockM + kBlockM - 1 + off) / kBlockN + 1) : n_ktiles_all;
   };
+  // key tiles of a unit: a pair walks those of its upper tile (the lower
+  // tile's softmax masks the extra one out entirely)
+  auto ktiles = [&](int rank) { return ktiles_q(PAIR ? 2 * unit_of(rank) + 1 : unit_of(rank)); };
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
@@ -157,7 +175,7 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
     }
     for (int b = 0; b < kSBuf; ++b) {
       mbar_init(&s_full[b], 1);
-      mbar_init(&p_ready[b], 4 * 32);
+      mbar_init(&p_ready[b], PAIR ? 2 * 4 : 4 * 32);  // pair: one arrival per softmax warp of each CTA
       mbar_init(&pv_done[b], 1);
     }
     mbar_init(&drain_s, 1);
@@ -171,11 +189,19 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
     fence_mbar_init();
   }
   if (warp == 2) {
-    tmem_alloc(&tmem_base_s, 512);
-    tmem_relinquish();
+    if constexpr (PAIR) {
+      tmem_alloc_pair(&tmem_base_s, 512);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(&tmem_base_s, 512);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
-  __syncthreads();
+  if constexpr (PAIR)
+    cluster_sync_all();  // the other CTA arrives on this one's barriers only once they exist
+  else
+    __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base_s;
   const uint32_t tmem_O = tmem + kSBuf * 128;
@@ -195,36 +221,57 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
       bool ok = true;
       int kt = 0, it = 0, rank, bh;
       for (int k = 0; ok; ++k) {
-        const int step = sched_item(sched, blockIdx.x, k, rank, bh);
+        const int step = sched_item(sched, cta, k, rank, bh);
         if (step == kDone) break;
         if (step == kSkip) continue;
         const int qtile = qtile_of(rank);
         {  // L2 prefetch of the next item's Q
           int nr, nbh, ns, k2 = k + 1;
-          while ((ns = sched_item(sched, blockIdx.x, k2, nr, nbh)) == kSkip) ++k2;
+          while ((ns = sched_item(sched, cta, k2, nr, nbh)) == kSkip) ++k2;
           if (ns == kItem)
             for (int x = 0; x < D; x += 64) tma_prefetch_l2_3d(&tmQ, x, qtile_of(nr) * kBlockM, nbh);
         }
         const int qb = it % kQBuf;
         if (it >= kQBuf && !mbar_wait(&q_empty[qb], ((it / kQBuf) & 1) ^ 1, &abort_flag)) { ok = false; break; }
-        mbar_arrive_expect_tx(&q_full[qb], L::kQBytes);
-        load_cols(smem + L::kQ + qb * L::kQBytes, &tmQ, &q_full[qb], 0, D, qtile * kBlockM, bh);
-        const int nk = ktiles(qtile) * kUnits;  // K units of this item
+        if constexpr (PAIR) {  // both CTAs' Q tiles complete on rank 0's barrier
+          if (crank == 0) mbar_arrive_expect_tx(&q_full[qb], 2 * L::kQBytes);
+          const uint32_t bar = cluster_addr(&q_full[qb], 0);
+          for (int x = 0; x < D; x += 64)
+            tma_load_3d_pair(smem + L::kQ + qb * L::kQBytes + (x / 64) * L::kSubBytes, &tmQ, bar, x,
+                             qtile * kBlockM, bh);
+        } else {
+          mbar_arrive_expect_tx(&q_full[qb], L::kQBytes);
+          load_cols(smem + L::kQ + qb * L::kQBytes, &tmQ, &q_full[qb], 0, D, qtile * kBlockM, bh);
+        }
+        const int nk = ktiles(rank) * kUnits;  // K units of this item
         for (int j = 0; j < nk; ++j, ++kt) {
           const int st = kt % kStages, c0 = (j % kUnits) * kUC;
           if (kt >= kStages && !mbar_wait(&k_empty[st], ((kt / kStages) & 1) ^ 1, &abort_flag)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&k_full[st], L::kUnitBytes);
-          load_cols(smem + L::kK + st * L::kUnitBytes, &tmK, &k_full[st], c0, min(D, c0 + kUC),
-                    (j / kUnits) * kBlockN, bh);
+          if constexpr (PAIR) {  // keys 64r..64r+63 of the tile (tmK has 64-row boxes)
+            if (crank == 0) mbar_arrive_expect_tx(&k_full[st], 2 * L::kKBytes);
+            const uint32_t bar = cluster_addr(&k_full[st], 0);
+            for (int x = 0; x < D; x += 64)
+              tma_load_3d_pair(smem + L::kK + st * L::kKBytes + (x / 64) * L::kKSub, &tmK, bar, x,
+                               j * kBlockN + 64 * static_cast<int>(crank), bh);
+          } else {
+            mbar_arrive_expect_tx(&k_full[st], L::kKBytes);
+            load_cols(smem + L::kK + st * L::kKBytes, &tmK, &k_full[st], c0, min(D, c0 + kUC),
+                      (j / kUnits) * kBlockN, bh);
+          }
         }
         ++it;  // this item's Q load was issued
       }
-      // teardown: every issued copy must land before the CTA's memory is released
-      for (int i = max(0, it - kQBuf); i < it; ++i) mbar_wait_drain(&q_full[i % kQBuf], (i / kQBuf) & 1);
-      for (int j = max(0, kt - kStages); j < kt; ++j) mbar_wait_drain(&k_full[j % kStages], (j / kStages) & 1);
+      // teardown: every issued copy must land before the CTA's memory is
+      // released (a pair's copies all complete on rank 0's barriers, which
+      // rank 0 drains before the pair's closing cluster barrier)
+      if (!PAIR || crank == 0) {
+        for (int i = max(0, it - kQBuf); i < it; ++i) mbar_wait_drain(&q_full[i % kQBuf], (i / kQBuf) & 1);
+        for (int j = max(0, kt - kStages); j < kt; ++j)
+          mbar_wait_drain(&k_full[j % kStages], (j / kStages) & 1);
+      }
     }
   };
   auto role_v_loader = [&]() {
@@ -234,22 +281,30 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
       bool ok = true;
       int kt = 0, rank, bh;
       for (int k = 0; ok; ++k) {
-        const int step = sched_item(sched, blockIdx.x, k, rank, bh);
+        const int step = sched_item(sched, cta, k, rank, bh);
         if (step == kDone) break;
         if (step == kSkip) continue;
-        const int nk = ktiles(qtile_of(rank)) * kUnits;  // V units of this item
+        const int nk = ktiles(rank) * kUnits;  // V units of this item
         for (int j = 0; j < nk; ++j, ++kt) {
           const int st = kt % kVStages, c0 = (j % kUnits) * kUC;
           if (kt >= kVStages && !mbar_wait(&v_empty[st], ((kt / kVStages) & 1) ^ 1, &abort_flag)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&v_full[st], L::kUnitBytes);
-          load_cols(smem + L::kV + st * L::kUnitBytes, &tmV, &v_full[st], c0, min(D, c0 + kUC),
-                    (j / kUnits) * kBlockN, bh);
+          if constexpr (PAIR) {  // head columns 64r..64r+63 of all the tile's keys
+            if (crank == 0) mbar_arrive_expect_tx(&v_full[st], 2 * L::kVBytes);
+            tma_load_3d_pair(smem + L::kV + st * L::kVBytes, &tmV, cluster_addr(&v_full[st], 0),
+                             64 * static_cast<int>(crank), j * kBlockN, bh);
+          } else {
+            mbar_arrive_expect_tx(&v_full[st], L::kVBytes);
+            load_cols(smem + L::kV + st * L::kVBytes, &tmV, &v_full[st], c0, min(D, c0 + kUC),
+                      (j / kUnits) * kBlockN, bh);
+          }
         }
       }
-      for (int j = max(0, kt - kVStages); j < kt; ++j) mbar_wait_drain(&v_full[j % kVStages], (j / kVStages) & 1);
+      if (!PAIR || crank == 0)
+        for (int j = max(0, kt - kVStages); j < kt; ++j)
+          mbar_wait_drain(&v_full[j % kVStages], (j / kVStages) & 1);
     }
   };
   auto role_s_issuer = [&]() {
@@ -257,45 +312,56 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
     // S of key tile kt goes to buffer kt % kSBuf once P V of tile kt - kSBuf
     // (which used that buffer) has completed; it accumulates over the tile's K
     // units (ring position ku).
-    if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_16(kBlockM, kBlockN, false, false, F16);
+    // With PAIR only rank 0 issues (M = 256 over both CTAs), and each commit
+    // arrives on the barrier of that name in both CTAs.
+    if (lane == 0 && (!PAIR || crank == 0)) {
+      constexpr uint32_t idesc_s = idesc_16(PAIR ? 2 * kBlockM : kBlockM, kBlockN, false, false, F16);
+      auto commit = [](uint64_t *bar) {
+        if constexpr (PAIR) mma_commit_pair_both(bar);
+        else mma_commit(bar);
+      };
       bool ok = true;
       int kt = 0, it = 0, ku = 0;
       int rank, bh;
       for (int k = 0; ok; ++k) {
-        const int step = sched_item(sched, blockIdx.x, k, rank, bh);
+        const int step = sched_item(sched, cta, k, rank, bh);
         if (step == kDone) break;
         if (step == kSkip) continue;
-        const int qtile = qtile_of(rank);
-        const int nk = ktiles(qtile);
+        const int nk = ktiles(rank);
         const int qb = it % kQBuf;
         const uint32_t q_addr = smem_u32(smem + L::kQ + qb * L::kQBytes);
         if (!mbar_wait(&q_full[qb], (it / kQBuf) & 1, &abort_flag)) { ok = false; break; }
         for (int j = 0; j < nk; ++j, ++kt) {
           const int sb = kt % kSBuf;
-          if (kt >= kSBuf && !mbar_wait(&pv_done[sb], ((kt / kSBuf) - 1) & 1, &abort_flag)) { ok = false; break; }
+          if (kt >= kSBuf && !mbar_wait(&pv_done[sb], ((kt / kSBuf) - 1) & 1, &abort_flag)) {
+            ok = false;
+            break;
+          }
           for (int u = 0; u < kUnits; ++u, ++ku) {
             const int st = ku % kStages;
             if (!mbar_wait(&k_full[st], (ku / kStages) & 1, &abort_flag)) { ok = false; break; }
             tc_fence_after();
-            const uint32_t k_addr = smem_u32(smem + L::kK + st * L::kUnitBytes);
+            const uint32_t k_addr = smem_u32(smem + L::kK + st * L::kKBytes);
             const uint32_t qu_addr = q_addr + u * (kUC / 64) * L::kSubBytes;
 #pragma unroll
             for (int kk = 0; kk < L::kSK; ++kk) {
-              const uint32_t off = (kk / 4) * L::kSubBytes + (kk % 4) * 32;
-              mma_ss(tmem + sb * 128, sdesc_sw128(qu_addr + off, 16, 1024), sdesc_sw128(k_addr + off, 16, 1024),
-                     idesc_s, (u > 0 || kk > 0) ? 1u : 0u);
+              const uint32_t qoff = (kk / 4) * L::kSubBytes + (kk % 4) * 32;
+              const uint32_t koff = (kk / 4) * L::kKSub + (kk % 4) * 32;
+              const uint64_t adesc = sdesc_sw128(qu_addr + qoff, 16, 1024), bdesc = sdesc_sw128(k_addr + koff, 16, 1024);
+              if constexpr (PAIR) mma_ss_pair(tmem + sb * 128, adesc, bdesc, idesc_s, (u > 0 || kk > 0) ? 1u : 0u);
+              else mma_ss(tmem + sb * 128, adesc, bdesc, idesc_s, (u > 0 || kk > 0) ? 1u : 0u);
             }
-            mma_commit(&k_empty[st]);
+            commit(&k_empty[st]);
           }
           if (!ok) break;
-          mma_commit(&s_full[sb]);
+          commit(&s_full[sb]);
         }
-        mma_commit(&q_empty[qb]);  // this Q buffer is free once the item's S MMAs are done
+        commit(&q_empty[qb]);  // this Q buffer is free once the item's S MMAs are done
         ++it;
       }
       // teardown: all issued MMAs finish before TMEM is released
-      mma_commit(&drain_s);
+      if constexpr (PAIR) mma_commit_pair_local(&drain_s);
+      else mma_commit(&drain_s);
       mbar_wait_drain(&drain_s, 0);
     }
   };
@@ -305,17 +371,20 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
     // streams queued while the other waits on its barriers. The first P V of
     // an item overwrites O: its P is only marked ready after the softmax warps
     // have read the previous item's O out of TMEM.
-    if (lane == 0) {
-      constexpr uint32_t idesc_o = idesc_16(kBlockM, L::kPVN, false, true, F16);
+    if (lane == 0 && (!PAIR || crank == 0)) {
+      constexpr uint32_t idesc_o = idesc_16(PAIR ? 2 * kBlockM : kBlockM, L::kPVN, false, true, F16);
+      auto commit = [](uint64_t *bar) {
+        if constexpr (PAIR) mma_commit_pair_both(bar);
+        else mma_commit(bar);
+      };
       bool ok = true;
       int kt = 0, vu = 0;
       int rank, bh;
       for (int k = 0; ok; ++k) {
-        const int step = sched_item(sched, blockIdx.x, k, rank, bh);
+        const int step = sched_item(sched, cta, k, rank, bh);
         if (step == kDone) break;
         if (step == kSkip) continue;
-        const int qtile = qtile_of(rank);
-        const int nk = ktiles(qtile);
+        const int nk = ktiles(rank);
         for (int j = 0; j < nk; ++j, ++kt) {
           const int sb = kt % kSBuf;
           if (!mbar_wait(&p_ready[sb], (kt / kSBuf) & 1, &abort_flag)) { ok = false; break; }
@@ -323,18 +392,23 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
             const int st = vu % kVStages;
             if (!mbar_wait(&v_full[st], (vu / kVStages) & 1, &abort_flag)) { ok = false; break; }
             tc_fence_after();
-            const uint32_t v_addr = smem_u32(smem + L::kV + st * L::kUnitBytes);
+            const uint32_t v_addr = smem_u32(smem + L::kV + st * L::kVBytes);
 #pragma unroll
-            for (int kk = 0; kk < kBlockN / 16; ++kk)
-              mma_ts(tmem_O + u * kUC, tmem + sb * 128 + kk * 8,
-                     sdesc_sw128(v_addr + kk * 2048, L::kSubBytes, 1024), idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
-            mma_commit(&v_empty[st]);
+            for (int kk = 0; kk < kBlockN / 16; ++kk) {
+              const uint64_t bdesc = sdesc_sw128(v_addr + kk * 2048, L::kSubBytes, 1024);
+              if constexpr (PAIR)
+                mma_ts_pair(tmem_O + u * kUC, tmem + sb * 128 + kk * 8, bdesc, idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+              else
+                mma_ts(tmem_O + u * kUC, tmem + sb * 128 + kk * 8, bdesc, idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+            }
+            commit(&v_empty[st]);
           }
           if (!ok) break;
-          mma_commit(&pv_done[sb]);
+          commit(&pv_done[sb]);
         }
       }
-      mma_commit(&drain_pv);
+      if constexpr (PAIR) mma_commit_pair_local(&drain_pv);
+      else mma_commit(&drain_pv);
       mbar_wait_drain(&drain_pv, 0);
     }
   };
@@ -347,11 +421,11 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
     int kt = 0;
     int rank, bh;
     for (int k = 0; ok; ++k) {
-      const int step = sched_item(sched, blockIdx.x, k, rank, bh);
+      const int step = sched_item(sched, cta, k, rank, bh);
       if (step == kDone) break;
       if (step == kSkip) continue;
       const int qtile = qtile_of(rank);
-      const int nk = ktiles(qtile);
+      const int nk = ktiles(rank);
       const int row = qtile * kBlockM + r_local;
       float m_used = -INFINITY, l_sum = 0.f;
       for (int j = 0; j < nk; ++j, ++kt) {
@@ -462,7 +536,12 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
         }
         l_sum += rs;
         tc_fence_before();
-        mbar_arrive(&p_ready[sb]);
+        if constexpr (PAIR) {  // one arrival per warp, on rank 0's barrier
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cl(cluster_addr(&p_ready[sb], 0));
+        } else {
+          mbar_arrive(&p_ready[sb]);
+        }
       }
       // -------------------------------------------------------------- epilogue
       // the item's last P V (and, issued in order before it, every other
@@ -488,11 +567,11 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
       bool ok = true;
       int kt = 0, rank, bh;
       for (int k = 0; ok; ++k) {
-        const int step = sched_item(sched, blockIdx.x, k, rank, bh);
+        const int step = sched_item(sched, cta, k, rank, bh);
         if (step == kDone) break;
         if (step == kSkip) continue;
         const int qtile = qtile_of(rank);
-        const int nk = ktiles(qtile), row = qtile * kBlockM + r_local;
+        const int nk = ktiles(rank), row = qtile * kBlockM + r_local;
         for (int j = 0; j < nk; ++j, ++kt) {
           const int ms = kt % kMaskSlots;
           if (kt >= kMaskSlots &&
@@ -534,47 +613,79 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
   }
 
   tc_fence_before();
-  __syncthreads();
+  if constexpr (PAIR)
+    cluster_sync_all();  // rank 0 has drained every copy and MMA that touches either CTA
+  else
+    __syncthreads();
   if (warp == 2) {
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    if constexpr (PAIR) tmem_dealloc_pair(tmem, 512);
+    else tmem_dealloc(tmem, 512);
   }
   if (threadIdx.x == 0 && abort_flag) atomicExch(status, kErrTimeout);
 }
 
 template <int D, bool F16, bool DROP>
-cudaError_t launch(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtensorMap &tmV, void *o,
-                   float *lse, int B, int H, int N, int Nk, float scale, int causal, const Dropout &drop,
-                   int *status, int num_sms, cudaStream_t stream) {
+cudaError_t launch(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtensorMap *tmKhalf,
+                   const CUtensorMap &tmV, void *o, float *lse, int B, int H, int N, int Nk, float scale,
+                   int causal, const Dropout &drop, int *status, int num_sms, cudaStream_t stream) {
+  const int BH = B * H, nt = (N + kBlockM - 1) / kBlockM;
+  const int n_ktiles_all = (Nk + kBlockN - 1) / kBlockN, off = Nk - N;
+  auto ktiles_q = [&](int qtile) {
+    return causal ? std::min(n_ktiles_all, (qtile * kBlockM + kBlockM - 1 + off) / kBlockN + 1) : n_ktiles_all;
+  };
+  const float scale_log2 = scale * 1.4426950408889634f;
+  cudaError_t e;
+  if constexpr (D == 128 && !DROP && FA_PAIR_KERNELS) {
+    // pairs of query tiles on two-CTA clusters with M = 256 MMAs, when the
+    // heads have at least two tiles (a lone tile would waste half the pair)
+    using LP = FwdSmem<D, false, true>;
+    auto kpair = fwd_kernel<D, F16, false, true>;
+    static SmemOnce smem_pair;
+    if (tmKhalf && nt >= 2) {
+      if ((e = set_smem_once(reinterpret_cast<const void *>(kpair), LP::kAlloc, &smem_pair)) != cudaSuccess)
+        return e;
+      const int clusters =
+          pair_grid(reinterpret_cast<const void *>(kpair), LP::kAlloc, kThreads, num_sms);
+      if (clusters >= 1) {
+        const int np = (nt + 1) / 2;
+        // a pair costs the key tiles of its upper tile plus about one for the epilogues
+        const TileSched sched = sched_cached(3, BH, N, Nk, causal != 0, np, clusters, [&](int rank) {
+          return static_cast<long long>(ktiles_q(2 * (np - 1 - rank) + 1)) + 1;
+        });
+        timing_begin(stream);
+        e = launch_pair_grid(kpair, sched.G, kThreads, LP::kAlloc, stream, tmQ, *tmKhalf, tmV,
+                             static_cast<uint16_t *>(o), lse, N, Nk, sched, scale, scale_log2, causal, drop, status);
+        timing_end(stream);
+        if (e != cudaSuccess) return e;
+        return cudaGetLastError();
+      }
+    }
+  }
   using L = FwdSmem<D, DROP>;
-  auto kern = fwd_kernel<D, F16, DROP>;
+  auto kern = fwd_kernel<D, F16, DROP, false>;
   static SmemOnce smem_set;
-  cudaError_t e = set_smem_once(reinterpret_cast<const void *>(kern), L::kAlloc, &smem_set);
+  e = set_smem_once(reinterpret_cast<const void *>(kern), L::kAlloc, &smem_set);
   if (e != cudaSuccess) return e;
   // persistent grid: at most one CTA per SM, each walking its static list of
   // query tiles; a tile costs its key tiles plus about one for its epilogue
-  const int BH = B * H, nt = (N + kBlockM - 1) / kBlockM;
-  const int n_ktiles_all = (Nk + kBlockN - 1) / kBlockN, off = Nk - N;
   const TileSched sched = sched_cached(0, BH, N, Nk, causal != 0, nt, num_sms, [&](int rank) {
-    const int qtile = nt - 1 - rank;
-    const int nk = causal ? std::min(n_ktiles_all, (qtile * kBlockM + kBlockM - 1 + off) / kBlockN + 1)
-                          : n_ktiles_all;
-    return static_cast<long long>(nk) + 1;
+    return static_cast<long long>(ktiles_q(nt - 1 - rank)) + 1;
   });
   timing_begin(stream);
   kern<<<sched.G, DROP ? kThreadsDrop : kThreads, L::kAlloc, stream>>>(tmQ, tmK, tmV, static_cast<uint16_t *>(o), lse,
-                                                  N, Nk, sched, scale, scale * 1.4426950408889634f, causal,
-                                                  drop, status);
+                                                  N, Nk, sched, scale, scale_log2, causal, drop, status);
   timing_end(stream);
   return cudaGetLastError();
 }
 
 template <bool DROP>
-cudaError_t dispatch(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtensorMap &tmV, void *o, float *lse,
-                     int B, int H, int N, int Nk, int d, float scale, int causal, bool f16, const Dropout &drop,
-                     int *status, int num_sms, cudaStream_t stream) {
-#define FA_FWD_LAUNCH(DD, FF) \
-  return launch<DD, FF, DROP>(tmQ, tmK, tmV, o, lse, B, H, N, Nk, scale, causal, drop, status, num_sms, stream)
+cudaError_t dispatch(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtensorMap *tmKhalf,
+                     const CUtensorMap &tmV, void *o, float *lse, int B, int H, int N, int Nk, int d, float scale,
+                     int causal, bool f16, const Dropout &drop, int *status, int num_sms, cudaStream_t stream) {
+#define FA_FWD_LAUNCH(DD, FF)                                                                                  \
+  return launch<DD, FF, DROP>(tmQ, tmK, tmKhalf, tmV, o, lse, B, H, N, Nk, scale, causal, drop, status, num_sms, \
+                              stream)
   if (f16) {
     if (d == 64) FA_FWD_LAUNCH(64, true);
     if (d == 96) FA_FWD_LAUNCH(96, true);
@@ -590,16 +701,16 @@ cudaError_t dispatch(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUten
 
 }  // namespace
 
-cudaError_t launch_fwd_16(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtensorMap &tmV,
-                          void *o, float *lse, int B, int H, int N, int Nk, int d, float scale, int causal,
-                          bool f16, const Dropout *drop, int *status, int num_sms, cudaStream_t stream,
-                          int *launches) {
+cudaError_t launch_fwd_16(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtensorMap *tmKhalf,
+                          const CUtensorMap &tmV, void *o, float *lse, int B, int H, int N, int Nk, int d,
+                          float scale, int causal, bool f16, const Dropout *drop, int *status, int num_sms,
+                          cudaStream_t stream, int *launches) {
   *launches += 1;
   if (drop)
-    return dispatch<true>(tmQ, tmK, tmV, o, lse, B, H, N, Nk, d, scale, causal, f16, *drop, status, num_sms,
-                          stream);
-  return dispatch<false>(tmQ, tmK, tmV, o, lse, B, H, N, Nk, d, scale, causal, f16, Dropout{}, status, num_sms,
-                         stream);
+    return dispatch<true>(tmQ, tmK, tmKhalf, tmV, o, lse, B, H, N, Nk, d, scale, causal, f16, *drop, status,
+                          num_sms, stream);
+  return dispatch<false>(tmQ, tmK, tmKhalf, tmV, o, lse, B, H, N, Nk, d, scale, causal, f16, Dropout{}, status,
+                         num_sms, stream);
 }
 
 }  // namespace fa

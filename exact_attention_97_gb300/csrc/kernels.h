@@ -6,6 +6,7 @@
 #include <stdint.h>
 
 #include <atomic>
+#include <utility>
 
 namespace fa {
 
@@ -54,6 +55,49 @@ struct SmemOnce {
 // looked up its device (the epoch comes from that lookup).
 cudaError_t set_smem_once(const void *kernel, int bytes, SmemOnce *done);
 
+// ----------------------------------------------------------- CTA-pair grids
+// Largest number of two-CTA clusters of `kernel` (threads per CTA, dynamic
+// shared memory per CTA) that fit on the current device at once; 0 if none.
+// Looked up once per kernel and device (the kernel's shared-memory attribute
+// must already be set).
+int max_pair_clusters(const void *kernel, int smem_bytes, int threads);
+
+// The two-CTA (pair) kernels of d = 128 -- the forward and both backward
+// passes with M = 256 MMAs split over the two SMs of a cluster -- are built
+// only with FA_PAIR_KERNELS=1. On GB300 they run at the per-SM rate of the
+// one-CTA kernels (the products keep N = 128, and that instruction rate, not
+// operand traffic, bounds these kernels), so the default build leaves them out.
+#ifndef FA_PAIR_KERNELS
+#define FA_PAIR_KERNELS 0
+#endif
+
+// Clusters of a persistent pair kernel's grid: one per two SMs, at most as
+// many as fit at once.
+inline int pair_grid(const void *kernel, int smem_bytes, int threads, int num_sms) {
+  const int fit = max_pair_clusters(kernel, smem_bytes, threads);
+  const int want = num_sms / 2;
+  return fit < want ? fit : want;
+}
+
+// Launches `kern` on `clusters` two-CTA clusters (grid 2 * clusters).
+template <class Kern, class... Args>
+cudaError_t launch_pair_grid(Kern kern, int clusters, int threads, int smem_bytes, cudaStream_t stream,
+                             Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(2 * clusters, 1, 1);
+  cfg.blockDim = dim3(threads, 1, 1);
+  cfg.dynamicSmemBytes = smem_bytes;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
 cudaError_t launch_fwd_f32(const float *q, const float *k, const float *v, float *o, float *lse,
                            int B, int H, int N, int d, float scale, int causal,
                            cudaStream_t stream, int *launches);
@@ -66,21 +110,28 @@ cudaError_t launch_bwd_f32(const float *q, const float *k, const float *v, const
 // N query rows and Nk key rows per head (causal: bottom-right aligned, Nk >= N).
 // 16-bit tensor-core forward (bf16, or f16 when `f16`). tmQ/tmK/tmV are 3-D
 // tensor maps {d, N, B*H} of that element type with a {64, 128, 1} box and
-// 128-byte swizzle.
-cudaError_t launch_fwd_16(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtensorMap &tmV,
-                          void *o, float *lse, int B, int H, int N, int Nk, int d, float scale, int causal,
-                          bool f16, const Dropout *drop, int *status, int num_sms, cudaStream_t stream,
-                          int *launches);
+// 128-byte swizzle; tmKhalf (may be null) is K's map with a {64, 64, 1} box,
+// which the two-CTA (pair) kernel of d = 128 needs.
+cudaError_t launch_fwd_16(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtensorMap *tmKhalf,
+                          const CUtensorMap &tmV, void *o, float *lse, int B, int H, int N, int Nk, int d,
+                          float scale, int causal, bool f16, const Dropout *drop, int *status, int num_sms,
+                          cudaStream_t stream, int *launches);
+
+// Load maps with {64, 64, 1} boxes (half tiles) of the backward's inputs, for
+// the two-CTA (pair) kernels of d = 128.
+struct HalfMaps {
+  CUtensorMap q, k, v, dO;
+};
 
 // 16-bit tensor-core backward (three kernels: row terms, dK/dV pass, dQ
 // pass). Lp and Dp are [B*H][Np] fp32 with Np = 128*ceil(N/128), in the
 // caller's workspace. tmdK / tmdV are store maps {d, Nk, B*H} of dk / dv with
-// a {16, 32, 1} box and 32-byte swizzle.
+// a {16, 32, 1} box and 32-byte swizzle. `half` may be null (no pair kernels).
 cudaError_t launch_bwd_16(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtensorMap &tmV,
                           const CUtensorMap &tmdO, const CUtensorMap &tmdK, const CUtensorMap &tmdV,
-                          const void *o, const void *dO, const float *lse,
-                          void *dq, void *dk, void *dv, float *Lp, float *Dp, int B, int H, int N, int Nk, int d,
-                          float scale, int causal, bool f16, const Dropout *drop, int *status, int num_sms,
-                          cudaStream_t stream, int *launches);
+                          const HalfMaps *half, const void *o, const void *dO, const float *lse, void *dq, void *dk,
+                          void *dv, float *Lp, float *Dp, int B, int H, int N, int Nk, int d, float scale, int causal,
+                          bool f16, const Dropout *drop, int *status, int num_sms, cudaStream_t stream,
+                          int *launches);
 
 }  // namespace fa

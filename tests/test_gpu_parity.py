@@ -178,6 +178,25 @@ def test_causal_schedules_with_several_items_per_cta(B, H, Nq, Nk, d):
     check(f"sched_B{B}_H{H}_Nq{Nq}_Nk{Nk}_d{d}", "bf16", got, {"o": o, "lse": lse, "dq": dq, "dk": dk, "dv": dv})
 
 
+@pytest.mark.parametrize("B,H,Nq,Nk,causal", [
+    (2, 24, 2048, 2048, True),   # 8 tile pairs / key-block pairs per head, several per cluster
+    (2, 12, 1100, 1300, True),   # 9 query tiles and 11 key blocks: each head's last pair has one tile
+    (3, 5, 1100, 1300, False),   # the same without the mask
+])
+def test_d128_several_items_per_cta(B, H, Nq, Nk, causal):
+    """Head size 128 with several items per persistent CTA and odd tile and
+    block counts (the two-CTA variant of these kernels runs the same shapes
+    in test_gpu_pair_kernels.py)."""
+    q, _, _, dO = make_qkv_do(B, H, Nq, 128, seed=800 + Nq + B, dtype=torch.bfloat16)
+    _, k, v, _ = make_qkv_do(B, H, Nk, 128, seed=900 + Nk + B, dtype=torch.bfloat16)
+    scale = 1.0 / math.sqrt(128)
+    got = _run_gpu_kv(q, k, v, dO, scale, causal)
+    o, lse = oracle.attention_fwd_kv(_np(q), _np(k), _np(v), scale, causal)
+    dq, dk, dv = oracle.attention_bwd_kv(_np(q), _np(k), _np(v), _np(dO), scale, causal)
+    check(f"pair_B{B}_H{H}_Nq{Nq}_Nk{Nk}_c{int(causal)}", "bf16", got,
+          {"o": o, "lse": lse, "dq": dq, "dk": dk, "dv": dv})
+
+
 # ------------------------------------------------------------ host-resident training step
 
 @pytest.mark.parametrize("case", ["bf16_causal", "f16_kv", "dropout", "one_chunk"])
