@@ -108,6 +108,35 @@ int current_device(DeviceInfo **out) {
   return kOk;
 }
 
+// A side stream and a fork / join event pair per host thread and device
+// (and context): the backward runs its two passes concurrently on the
+// caller's stream and this one when both grids fit on the GPU together.
+// Per thread, so that concurrent callers never share the events.
+struct SideStream {
+  CUcontext ctx = nullptr;
+  cudaStream_t stream = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+thread_local SideStream t_side[kMaxDevices];
+
+// This thread's side stream on the current device, created on first use
+// (nullptr members if creation fails: the passes then run one after the other).
+const SideStream *side_stream(int dev, CUcontext ctx) {
+  if (dev < 0 || dev >= kMaxDevices) return nullptr;
+  SideStream &s = t_side[dev];
+  if (s.stream && s.ctx == ctx) return &s;
+  s = SideStream{};  // a replaced context took the old handles with it
+  if (cudaStreamCreateWithFlags(&s.stream, cudaStreamNonBlocking) != cudaSuccess ||
+      cudaEventCreateWithFlags(&s.fork, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&s.join, cudaEventDisableTiming) != cudaSuccess) {
+    cudaGetLastError();
+    s = SideStream{};
+    return nullptr;
+  }
+  s.ctx = ctx;
+  return &s;
+}
+
 int get_encoder() {
   std::call_once(g_encode_once, [] {
     void *fn = nullptr;
@@ -459,11 +488,15 @@ int bwd16(const void *q, const void *k, const void *v, const void *o, const floa
     return st;
   const BwdWorkspace w = ws_layout(B, H, N, d, FA_BF16);
   char *ws = static_cast<char *>(workspace);
+  int cur = 0;
+  if (cudaGetDevice(&cur) != cudaSuccess) return record(cudaGetLastError());
+  const SideStream *side = side_stream(cur, dev->ctx);
+  const BwdSide bs{side ? side->stream : nullptr, side ? side->fork : nullptr, side ? side->join : nullptr};
   int launches = 0;
   cudaError_t e = launch_bwd_16(tq, tk, tv, tdo, tdk, tdv, pair ? &half : nullptr, o, dO, lse, dq, dk, dv,
                                 reinterpret_cast<float *>(ws + w.lp), reinterpret_cast<float *>(ws + w.dp), B, H, N,
                                 Nk, d, scale, causal ? 1 : 0, f16, drop, dev->status, dev->num_sms,
-                                reinterpret_cast<cudaStream_t>(stream), &launches);
+                                reinterpret_cast<cudaStream_t>(stream), bs, &launches);
   if (e != cudaSuccess) return record(e);
   t_last_launches = launches;
   return FA_OK;

@@ -1117,7 +1117,7 @@ cudaError_t launch(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtenso
                    const CUtensorMap &tmdO, const CUtensorMap &tmdK, const CUtensorMap &tmdV, const HalfMaps *half,
                    const void *o, const void *dO, const float *lse, void *dq, void *dk, void *dv, float *Lp,
                    float *Dp, int B, int H, int N, int Nk, float scale, int causal, const Dropout &drop, int *status,
-                   int num_sms, cudaStream_t stream) {
+                   int num_sms, cudaStream_t stream, const BwdSide &side) {
   const int n_tiles = (N + kBlk - 1) / kBlk;
   const int Np = n_tiles * kBlk;
   const float scale_log2 = scale * kLog2e;
@@ -1138,85 +1138,119 @@ cudaError_t launch(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtenso
     return causal ? std::min(n_kb_all, (qt * kBlk + kBlk - 1 + off) / kBlk + 1) : n_kb_all;
   };
   auto first_tile = [&](int kb) { return causal ? std::max(0, kb * kBlk - off) / kBlk : 0; };
-  bool kv_done = false;
+
+  // Each pass as a launch on a given stream; `ctas` tells how many SMs its
+  // grid takes.
+  struct Pass {
+    int ctas = 0;
+    bool pair = false;
+    TileSched sched{};
+  };
+  Pass kv, q;
+  int clusters_kv = 0, clusters_q = 0;
   if constexpr (D == 128 && !DROP && FA_PAIR_KERNELS) {
-    // dK/dV pass on two-CTA clusters (key block pairs, M = 256 MMAs) when
-    // the heads have at least two key blocks
-    auto kpair = bwd_dkdv_kernel<D, F16, false, true>;
-    static SmemOnce smem_kvp;
+    // two-CTA clusters (block / tile pairs, M = 256 MMAs) when the heads have
+    // at least two key blocks / query tiles
+    static SmemOnce smem_kvp, smem_qp;
+    auto kpk = bwd_dkdv_kernel<D, F16, false, true>;
+    auto kpq = bwd_dq_kernel<D, F16, false, true>;
     if (half && n_kb_all >= 2) {
-      if ((e = set_smem_once(reinterpret_cast<const void *>(kpair), DkdvCfg<D, true>::kAlloc, &smem_kvp)) !=
+      if ((e = set_smem_once(reinterpret_cast<const void *>(kpk), DkdvCfg<D, true>::kAlloc, &smem_kvp)) !=
           cudaSuccess)
         return e;
-      const int clusters = pair_grid(reinterpret_cast<const void *>(kpair), DkdvCfg<D, true>::kAlloc, kThreads, num_sms);
-      if (clusters >= 1) {
-        const int np = (n_kb_all + 1) / 2;
-        // a pair visits the query tiles of its lower block
-        const TileSched sched_kvp = sched_cached(5, BH, N, Nk, causal != 0, np, clusters, [&](int r) {
-          return static_cast<long long>(n_tiles - first_tile(2 * r)) + 1;
-        });
-        timing_begin(stream);
-        e = launch_pair_grid(kpair, sched_kvp.G, kThreads, DkdvCfg<D, true>::kAlloc, stream, tmQ, tmK, tmV, tmdO,
-                             tmdK, tmdV, half->q, half->dO, Lp, Dp, N, Nk, sched_kvp, scale, scale_log2, causal,
-                             drop, status);
-        timing_end(stream);
-        if (e != cudaSuccess || (e = cudaGetLastError()) != cudaSuccess) return e;
-        kv_done = true;
-      }
+      clusters_kv = pair_grid(reinterpret_cast<const void *>(kpk), DkdvCfg<D, true>::kAlloc, kThreads, num_sms);
+    }
+    if (half && n_tiles >= 2) {
+      if ((e = set_smem_once(reinterpret_cast<const void *>(kpq), DqCfg<D, true>::kAlloc, &smem_qp)) != cudaSuccess)
+        return e;
+      clusters_q = pair_grid(reinterpret_cast<const void *>(kpq), DqCfg<D, true>::kAlloc, kThreads, num_sms);
     }
   }
-  if (!kv_done) {
-    const TileSched sched_kv = sched_cached(1, BH, N, Nk, causal != 0, n_kb_all, num_sms, [&](int kb) {
+  if (clusters_kv >= 1) {
+    const int np = (n_kb_all + 1) / 2;  // a pair visits the query tiles of its lower block
+    kv.sched = sched_cached(5, BH, N, Nk, causal != 0, np, clusters_kv, [&](int r) {
+      return static_cast<long long>(n_tiles - first_tile(2 * r)) + 1;
+    });
+    kv.pair = true;
+    kv.ctas = 2 * kv.sched.G;
+  } else {
+    kv.sched = sched_cached(1, BH, N, Nk, causal != 0, n_kb_all, num_sms, [&](int kb) {
       return static_cast<long long>(n_tiles - first_tile(kb)) + 1;
     });
-    auto kdkdv = bwd_dkdv_kernel<D, F16, DROP, false>;
-    static SmemOnce smem_kv;
-    if ((e = set_smem_once(reinterpret_cast<const void *>(kdkdv), DkdvCfg<D>::kAlloc, &smem_kv)) != cudaSuccess)
-      return e;
-    timing_begin(stream);
-    kdkdv<<<sched_kv.G, kThreads, DkdvCfg<D>::kAlloc, stream>>>(tmQ, tmK, tmV, tmdO, tmdK, tmdV, tmQ, tmdO, Lp, Dp,
-                                                                 N, Nk, sched_kv, scale, scale_log2, causal, drop,
-                                                                 status);
-    timing_end(stream);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    kv.ctas = kv.sched.G;
   }
-  if constexpr (D == 128 && !DROP && FA_PAIR_KERNELS) {
-    // dQ pass on two-CTA clusters (tile pairs, M = 256 MMAs) when the heads
-    // have at least two query tiles
-    auto kpair = bwd_dq_kernel<D, F16, false, true>;
-    static SmemOnce smem_qp;
-    if (half && n_tiles >= 2) {
-      if ((e = set_smem_once(reinterpret_cast<const void *>(kpair), DqCfg<D, true>::kAlloc, &smem_qp)) !=
-          cudaSuccess)
-        return e;
-      const int clusters = pair_grid(reinterpret_cast<const void *>(kpair), DqCfg<D, true>::kAlloc, kThreads, num_sms);
-      if (clusters >= 1) {
-        const int np = (n_tiles + 1) / 2;
-        const TileSched sched_qp = sched_cached(4, BH, N, Nk, causal != 0, np, clusters, [&](int rank) {
-          return static_cast<long long>(kblocks_q(2 * (np - 1 - rank) + 1)) + 1;
-        });
-        timing_begin(stream);
-        e = launch_pair_grid(kpair, sched_qp.G, kThreads, DqCfg<D, true>::kAlloc, stream, tmQ, tmK, tmV, tmdO,
-                             half->k, half->v, Lp, Dp, static_cast<uint16_t *>(dq), N, Nk, sched_qp, scale,
-                             scale_log2, causal, drop, status);
-        timing_end(stream);
-        if (e != cudaSuccess) return e;
-        return cudaGetLastError();
+  if (clusters_q >= 1) {
+    const int np = (n_tiles + 1) / 2;
+    q.sched = sched_cached(4, BH, N, Nk, causal != 0, np, clusters_q, [&](int rank) {
+      return static_cast<long long>(kblocks_q(2 * (np - 1 - rank) + 1)) + 1;
+    });
+    q.pair = true;
+    q.ctas = 2 * q.sched.G;
+  } else {
+    q.sched = sched_cached(2, BH, N, Nk, causal != 0, n_tiles, num_sms, [&](int rank) {
+      return static_cast<long long>(kblocks_q(n_tiles - 1 - rank)) + 1;
+    });
+    q.ctas = q.sched.G;
+  }
+
+  auto run_kv = [&](cudaStream_t st) -> cudaError_t {
+    timing_begin(st);
+    if constexpr (D == 128 && !DROP && FA_PAIR_KERNELS) {
+      if (kv.pair) {
+        cudaError_t r = launch_pair_grid(bwd_dkdv_kernel<D, F16, false, true>, kv.sched.G, kThreads,
+                                         DkdvCfg<D, true>::kAlloc, st, tmQ, tmK, tmV, tmdO, tmdK, tmdV, half->q,
+                                         half->dO, Lp, Dp, N, Nk, kv.sched, scale, scale_log2, causal, drop, status);
+        timing_end(st);
+        return r != cudaSuccess ? r : cudaGetLastError();
       }
     }
+    static SmemOnce smem_kv;
+    auto kern = bwd_dkdv_kernel<D, F16, DROP, false>;
+    cudaError_t r = set_smem_once(reinterpret_cast<const void *>(kern), DkdvCfg<D>::kAlloc, &smem_kv);
+    if (r != cudaSuccess) return r;
+    kern<<<kv.sched.G, kThreads, DkdvCfg<D>::kAlloc, st>>>(tmQ, tmK, tmV, tmdO, tmdK, tmdV, tmQ, tmdO, Lp, Dp, N, Nk,
+                                                           kv.sched, scale, scale_log2, causal, drop, status);
+    timing_end(st);
+    return cudaGetLastError();
+  };
+  auto run_q = [&](cudaStream_t st) -> cudaError_t {
+    timing_begin(st);
+    if constexpr (D == 128 && !DROP && FA_PAIR_KERNELS) {
+      if (q.pair) {
+        cudaError_t r = launch_pair_grid(bwd_dq_kernel<D, F16, false, true>, q.sched.G, kThreads,
+                                         DqCfg<D, true>::kAlloc, st, tmQ, tmK, tmV, tmdO, half->k, half->v, Lp, Dp,
+                                         static_cast<uint16_t *>(dq), N, Nk, q.sched, scale, scale_log2, causal, drop,
+                                         status);
+        timing_end(st);
+        return r != cudaSuccess ? r : cudaGetLastError();
+      }
+    }
+    static SmemOnce smem_q;
+    auto kern = bwd_dq_kernel<D, F16, DROP, false>;
+    cudaError_t r = set_smem_once(reinterpret_cast<const void *>(kern), DqCfg<D>::kAlloc, &smem_q);
+    if (r != cudaSuccess) return r;
+    kern<<<q.sched.G, kThreads, DqCfg<D>::kAlloc, st>>>(tmQ, tmK, tmV, tmdO, tmK, tmV, Lp, Dp,
+                                                        static_cast<uint16_t *>(dq), N, Nk, q.sched, scale,
+                                                        scale_log2, causal, drop, status);
+    timing_end(st);
+    return cudaGetLastError();
+  };
+
+  // Both passes only read what the row-term kernel and the forward wrote, so
+  // when their grids fit on the GPU together (small problems, where each
+  // leaves SMs idle) the dQ pass runs on the side stream alongside the dK/dV
+  // pass; otherwise one after the other (each persistent grid fills the GPU).
+  if (side.stream && kv.ctas + q.ctas <= num_sms) {
+    if ((e = cudaEventRecord(side.fork, stream)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(side.stream, side.fork, 0)) != cudaSuccess)
+      return e;
+    if ((e = run_kv(stream)) != cudaSuccess) return e;
+    if ((e = run_q(side.stream)) != cudaSuccess) return e;
+    if ((e = cudaEventRecord(side.join, side.stream)) != cudaSuccess) return e;
+    return cudaStreamWaitEvent(stream, side.join, 0);
   }
-  const TileSched sched_q = sched_cached(2, BH, N, Nk, causal != 0, n_tiles, num_sms, [&](int rank) {
-    return static_cast<long long>(kblocks_q(n_tiles - 1 - rank)) + 1;
-  });
-  auto kdq = bwd_dq_kernel<D, F16, DROP, false>;
-  static SmemOnce smem_q;
-  if ((e = set_smem_once(reinterpret_cast<const void *>(kdq), DqCfg<D>::kAlloc, &smem_q)) != cudaSuccess) return e;
-  timing_begin(stream);
-  kdq<<<sched_q.G, kThreads, DqCfg<D>::kAlloc, stream>>>(tmQ, tmK, tmV, tmdO, tmK, tmV, Lp, Dp,
-                                                          static_cast<uint16_t *>(dq), N, Nk, sched_q, scale,
-                                                          scale_log2, causal, drop, status);
-  timing_end(stream);
-  return cudaGetLastError();
+  if ((e = run_kv(stream)) != cudaSuccess) return e;
+  return run_q(stream);
 }
 
 template <bool DROP>
@@ -1224,10 +1258,10 @@ cudaError_t dispatch(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUten
                      const CUtensorMap &tmdO, const CUtensorMap &tmdK, const CUtensorMap &tmdV, const HalfMaps *half,
                      const void *o, const void *dO, const float *lse, void *dq, void *dk, void *dv, float *Lp,
                      float *Dp, int B, int H, int N, int Nk, int d, float scale, int causal, bool f16,
-                     const Dropout &drop, int *status, int num_sms, cudaStream_t stream) {
+                     const Dropout &drop, int *status, int num_sms, cudaStream_t stream, const BwdSide &side) {
 #define FA_BWD_LAUNCH(DD, FF)                                                                                  \
   return launch<DD, FF, DROP>(tmQ, tmK, tmV, tmdO, tmdK, tmdV, half, o, dO, lse, dq, dk, dv, Lp, Dp, B, H, N,  \
-                              Nk, scale, causal, drop, status, num_sms, stream)
+                              Nk, scale, causal, drop, status, num_sms, stream, side)
   if (f16) {
     if (d == 64) FA_BWD_LAUNCH(64, true);
     if (d == 96) FA_BWD_LAUNCH(96, true);
@@ -1246,13 +1280,13 @@ cudaError_t launch_bwd_16(const CUtensorMap &tmQ, const CUtensorMap &tmK, const 
                           const HalfMaps *half, const void *o, const void *dO, const float *lse, void *dq, void *dk,
                           void *dv, float *Lp, float *Dp, int B, int H, int N, int Nk, int d, float scale, int causal,
                           bool f16, const Dropout *drop, int *status, int num_sms, cudaStream_t stream,
-                          int *launches) {
+                          const BwdSide &side, int *launches) {
   *launches += 3;
   if (drop)
     return dispatch<true>(tmQ, tmK, tmV, tmdO, tmdK, tmdV, half, o, dO, lse, dq, dk, dv, Lp, Dp, B, H, N, Nk, d,
-                          scale, causal, f16, *drop, status, num_sms, stream);
+                          scale, causal, f16, *drop, status, num_sms, stream, side);
   return dispatch<false>(tmQ, tmK, tmV, tmdO, tmdK, tmdV, half, o, dO, lse, dq, dk, dv, Lp, Dp, B, H, N, Nk, d,
-                         scale, causal, f16, Dropout{}, status, num_sms, stream);
+                         scale, causal, f16, Dropout{}, status, num_sms, stream, side);
 }
 
 }  // namespace fa

@@ -127,11 +127,19 @@ struct HalfMaps {
 // pass). Lp and Dp are [B*H][Np] fp32 with Np = 128*ceil(N/128), in the
 // caller's workspace. tmdK / tmdV are store maps {d, Nk, B*H} of dk / dv with
 // a {16, 32, 1} box and 32-byte swizzle. `half` may be null (no pair kernels).
+// Optional second stream for the backward: when the dK/dV and dQ grids fit
+// on the GPU together, the dQ pass runs on `stream` forked from the caller's
+// stream after the row-term kernel (event `fork`) and joins it back (`join`).
+struct BwdSide {
+  cudaStream_t stream;
+  cudaEvent_t fork, join;
+};
+
 cudaError_t launch_bwd_16(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtensorMap &tmV,
                           const CUtensorMap &tmdO, const CUtensorMap &tmdK, const CUtensorMap &tmdV,
                           const HalfMaps *half, const void *o, const void *dO, const float *lse, void *dq, void *dk,
                           void *dv, float *Lp, float *Dp, int B, int H, int N, int Nk, int d, float scale, int causal,
                           bool f16, const Dropout *drop, int *status, int num_sms, cudaStream_t stream,
-                          int *launches);
+                          const BwdSide &side, int *launches);
 
 }  // namespace fa
