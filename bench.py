@@ -272,6 +272,11 @@ def run_ours(args, w):
     stream = torch.cuda.current_stream()
 
     drop = {"dropout_p": args.dropout, "seed": 1234, "offset": 0} if args.dropout else {}
+    drop_bwd = dict(drop)
+    if args.dropout and args.dropout_saved:  # the forward saves its keep bits, the backward reads them
+        mask = fa.dropout_mask_buffer(w.B, w.H, w.N, w.n_keys, dev)
+        drop["dropout_mask"] = mask
+        drop_bwd = {"dropout_p": args.dropout, "dropout_mask": mask}
     launches = [0]
     marks = []  # (fwd start, bwd start, bwd end) events per timed step, on the launch stream
 
@@ -284,7 +289,8 @@ def run_ours(args, w):
         if mark:
             m[1].record(stream)
         if not args.fwd_only:
-            fa.attention_backward(q, k, v, o, lse, dO, w.scale, w.causal, workspace=ws, grads=(dq, dk, dv), **drop)
+            fa.attention_backward(q, k, v, o, lse, dO, w.scale, w.causal, workspace=ws, grads=(dq, dk, dv),
+                                  **drop_bwd)
         if mark:
             m[2].record(stream)
             marks.append(m)
@@ -438,14 +444,16 @@ def run_ours(args, w):
                      torch.empty_like(q_h).pin_memory(), torch.empty_like(k_h).pin_memory(),
                      torch.empty_like(v_h).pin_memory()]
 
+        drop_e2e = {k_: v_ for k_, v_ in drop.items() if k_ != "dropout_mask"}  # chunks draw their bits
+
         def e2e_step():
             if args.fwd_only:
                 qd, kd, vd = (t.to(dev, non_blocking=True) for t in (q_h, k_h, v_h))
-                od, ld = fa.attention_forward(qd, kd, vd, w.scale, w.causal, **drop)
+                od, ld = fa.attention_forward(qd, kd, vd, w.scale, w.causal, **drop_e2e)
                 for dst, src in zip(out_h, (od, ld)):
                     dst.copy_(src, non_blocking=True)
             else:
-                fa.attention_step_host(q_h, k_h, v_h, do_h, w.scale, w.causal, out=tuple(out_h), **drop)
+                fa.attention_step_host(q_h, k_h, v_h, do_h, w.scale, w.causal, out=tuple(out_h), **drop_e2e)
 
         for _ in range(2):
             e2e_step()
@@ -536,6 +544,8 @@ def run_ours(args, w):
             "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
             "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "Nk": w.n_keys, "d": w.d,
                        "causal": w.causal, "dropout": args.dropout,
+                       "dropout_bits": ("saved by the forward" if args.dropout_saved else "drawn in every pass")
+                       if args.dropout else None,
                        "inputs": "i.i.d. N(0,1), seeds Q=0 K=1 V=2 dO=3",
                        "l2": "inputs larger than L2 (each of Q, K, V, dO is "
                              f"{q.numel() * 2 / 1e6:.0f} MB vs 129 MB L2)",
@@ -578,6 +588,8 @@ def main():
                     help="time the forward alone (head sizes with no backward kernel, e.g. d = 256)")
     ap.add_argument("--dropout", type=float, default=0.0,
                     help="dropout probability on the attention probabilities (Philox mask, seed 1234)")
+    ap.add_argument("--dropout-saved", action="store_true",
+                    help="with --dropout: the forward saves its keep bits and the backward reads them")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--graph", action="store_true",
                     help="also time the step replayed from a CUDA graph (host launch cost off the critical path)")

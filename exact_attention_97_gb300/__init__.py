@@ -17,16 +17,17 @@ import math
 
 import threading
 
-from ._lib import (FA_BF16, FA_F16, FA_F32, FAError, fa_bwd, fa_bwd_dropout, fa_bwd_f16, fa_bwd_f32, fa_bwd_kv,
-                   fa_bwd_workspace_size, fa_device_status, fa_fwd, fa_fwd_dropout, fa_fwd_f16, fa_fwd_f32,
-                   fa_fwd_kv, fa_last_launch_count, fa_set_kernel_timing, fa_status_async, fa_status_string,
-                   fa_status_word, lib_path, load)
+from ._lib import (FA_BF16, FA_F16, FA_F32, FAError, fa_bwd, fa_bwd_dropout, fa_bwd_dropout_mask, fa_bwd_f16,
+                   fa_bwd_f32, fa_bwd_kv, fa_bwd_workspace_size, fa_device_status, fa_dropout_mask_size, fa_fwd,
+                   fa_fwd_dropout, fa_fwd_dropout_mask, fa_fwd_f16, fa_fwd_f32, fa_fwd_kv, fa_last_launch_count,
+                   fa_set_kernel_timing, fa_status_async, fa_status_string, fa_status_word, lib_path, load)
 
 __all__ = [
     "FA_BF16", "FA_F16", "FA_F32", "FAError", "fa_fwd", "fa_bwd", "fa_fwd_f16", "fa_bwd_f16",
     "fa_fwd_f32", "fa_bwd_f32", "fa_fwd_kv", "fa_bwd_kv", "fa_fwd_dropout", "fa_bwd_dropout",
     "fa_bwd_workspace_size", "fa_status_string", "fa_device_status", "fa_last_launch_count",
-    "fa_set_kernel_timing", "fa_status_async", "fa_status_word",
+    "fa_set_kernel_timing", "fa_status_async", "fa_status_word", "fa_dropout_mask_size", "fa_fwd_dropout_mask",
+    "fa_bwd_dropout_mask", "dropout_mask_buffer",
     "attention_forward", "attention_backward", "attention_step_host", "lib_path", "load",
 ]
 
@@ -53,6 +54,21 @@ def _stream_handle(stream):
     return s.cuda_stream
 
 
+def dropout_mask_buffer(B, H, Nq, Nk, device=None):
+    """A device buffer for the saved dropout keep bits of a [B, H, Nq, Nk]
+    problem (fa_dropout_mask_size bytes), to pass as `dropout_mask` to
+    attention_forward and then attention_backward."""
+    torch = _torch()
+    return torch.empty(fa_dropout_mask_size(B, H, Nq, Nk), dtype=torch.uint8,
+                       device=device if device is not None else torch.device("cuda"))
+
+
+def _mask_arg(mask):
+    if not mask.is_cuda or not mask.is_contiguous():
+        raise ValueError("dropout_mask must be a contiguous CUDA tensor")
+    return mask.data_ptr(), mask.numel() * mask.element_size()
+
+
 _status_buf = threading.local()
 
 
@@ -72,7 +88,7 @@ def _check_status(fn, stream):
 
 
 def attention_forward(q, k, v, scale=None, causal=False, out=None, lse=None, stream=None,
-                      dropout_p=0.0, seed=0, offset=0, head_base=0, check=False):
+                      dropout_p=0.0, seed=0, offset=0, head_base=0, check=False, dropout_mask=None):
     """(O, L) for CUDA tensors q [B, H, Nq, d] and k, v [B, H, Nk, d] (all bf16, all f16 or all float32).
 
     bf16 and f16 need d in {64, 96, 128} (or 256 for the forward); float32 takes 1 <= d <= 128 and Nk == Nq. L is
@@ -82,6 +98,9 @@ def attention_forward(q, k, v, scale=None, causal=False, out=None, lse=None, str
     Philox mask of fa_fwd_dropout, keyed by (seed, offset) and the heads'
     global index (head_base + b * H + h); pass the same values to
     attention_backward.
+    dropout_mask (a buffer from dropout_mask_buffer) makes the forward also
+    save the keep bits it draws, for attention_backward to read instead of
+    drawing them again.
     check=True waits for the call's stream and raises FAError (status
     FA_ERR_TIMEOUT) if a kernel of the library on this device gave up on a
     pipeline wait since the status was last read; the results of such a call
@@ -106,9 +125,13 @@ def attention_forward(q, k, v, scale=None, causal=False, out=None, lse=None, str
         if dropout_p:
             if dt == torch.float32:
                 raise ValueError("dropout needs bfloat16 or float16 inputs")
-            fa_fwd_dropout(*ptrs, B, H, N, Nk, d, scale, int(bool(causal)),
-                           FA_F16 if dt == torch.float16 else FA_BF16, dropout_p, seed, offset, head_base,
-                           _stream_handle(stream))
+            kind = FA_F16 if dt == torch.float16 else FA_BF16
+            if dropout_mask is not None:
+                fa_fwd_dropout_mask(*ptrs, B, H, N, Nk, d, scale, int(bool(causal)), kind, dropout_p, seed, offset,
+                                    head_base, *_mask_arg(dropout_mask), _stream_handle(stream))
+            else:
+                fa_fwd_dropout(*ptrs, B, H, N, Nk, d, scale, int(bool(causal)), kind, dropout_p, seed, offset,
+                               head_base, _stream_handle(stream))
         elif Nk != N:
             if dt == torch.float32:
                 raise ValueError("float32 needs k and v with as many rows as q")
@@ -123,10 +146,10 @@ def attention_forward(q, k, v, scale=None, causal=False, out=None, lse=None, str
 
 
 def attention_backward(q, k, v, o, lse, dO, scale=None, causal=False, workspace=None, stream=None,
-                       grads=None, dropout_p=0.0, seed=0, offset=0, head_base=0, check=False):
+                       grads=None, dropout_p=0.0, seed=0, offset=0, head_base=0, check=False, dropout_mask=None):
     """(dQ, dK, dV) for upstream gradient dO, given the forward's O and L (and
-    the forward's dropout_p, seed and offset). check=True as for
-    attention_forward."""
+    the forward's dropout_p, seed and offset, or dropout_p and the
+    dropout_mask the forward saved). check=True as for attention_forward."""
     torch = _torch()
     B, H, N, d = q.shape
     Nk = k.shape[2]
@@ -152,8 +175,12 @@ def attention_backward(q, k, v, o, lse, dO, scale=None, causal=False, workspace=
         if dropout_p:
             if kind == FA_F32:
                 raise ValueError("dropout needs bfloat16 or float16 inputs")
-            fa_bwd_dropout(*ptrs, B, H, N, Nk, d, scale, int(bool(causal)), kind, dropout_p, seed, offset, head_base,
-                           *ws)
+            if dropout_mask is not None:
+                fa_bwd_dropout_mask(*ptrs, B, H, N, Nk, d, scale, int(bool(causal)), kind, dropout_p,
+                                    *_mask_arg(dropout_mask), *ws)
+            else:
+                fa_bwd_dropout(*ptrs, B, H, N, Nk, d, scale, int(bool(causal)), kind, dropout_p, seed, offset,
+                               head_base, *ws)
         elif Nk != N:
             if kind == FA_F32:
                 raise ValueError("float32 needs k and v with as many rows as q")

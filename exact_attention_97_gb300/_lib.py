@@ -28,6 +28,12 @@ _SIGNATURES = {
     "fa_bwd_dropout": (c_int, [c_void_p] * 9 + [c_int] * 5 + [c_float, c_int, c_int, c_float, ctypes.c_ulonglong,
                                                                ctypes.c_uint, ctypes.c_uint, c_void_p, c_size_t,
                                                                c_void_p]),
+    "fa_dropout_mask_size": (c_size_t, [c_int] * 4),
+    "fa_fwd_dropout_mask": (c_int, [c_void_p] * 5 + [c_int] * 5 + [c_float, c_int, c_int, c_float,
+                                                                    ctypes.c_ulonglong, ctypes.c_uint, ctypes.c_uint,
+                                                                    c_void_p, c_size_t, c_void_p]),
+    "fa_bwd_dropout_mask": (c_int, [c_void_p] * 9 + [c_int] * 5 + [c_float, c_int, c_int, c_float, c_void_p,
+                                                                    c_size_t, c_void_p, c_size_t, c_void_p]),
     "fa_fwd_f32": (c_int, [c_void_p] * 5 + [c_int] * 4 + [c_float, c_int, c_void_p]),
     "fa_bwd_f32": (c_int, [c_void_p] * 9 + [c_int] * 4 + [c_float, c_int, c_void_p, c_size_t, c_void_p]),
     "fa_bwd_workspace_size": (c_size_t, [c_int] * 5),
@@ -123,6 +129,22 @@ def fa_bwd_dropout(q, k, v, o, lse, dO, dq, dk, dv, B, H, Nq, Nk, d, scale, caus
     return _call("fa_bwd_dropout", q, k, v, o, lse, dO, dq, dk, dv, B, H, Nq, Nk, d, float(scale), int(causal),
                  int(dtype), float(p_drop), int(seed), int(offset), int(head_base), workspace, workspace_bytes,
                  stream)
+
+
+def fa_dropout_mask_size(B, H, Nq, Nk) -> int:
+    return int(load().fa_dropout_mask_size(B, H, Nq, Nk))
+
+
+def fa_fwd_dropout_mask(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, dtype, p_drop, seed, offset, head_base,
+                        mask, mask_bytes, stream):
+    return _call("fa_fwd_dropout_mask", q, k, v, o, lse, B, H, Nq, Nk, d, float(scale), int(causal), int(dtype),
+                 float(p_drop), int(seed), int(offset), int(head_base), mask, mask_bytes, stream)
+
+
+def fa_bwd_dropout_mask(q, k, v, o, lse, dO, dq, dk, dv, B, H, Nq, Nk, d, scale, causal, dtype, p_drop, mask,
+                        mask_bytes, workspace, workspace_bytes, stream):
+    return _call("fa_bwd_dropout_mask", q, k, v, o, lse, dO, dq, dk, dv, B, H, Nq, Nk, d, float(scale),
+                 int(causal), int(dtype), float(p_drop), mask, mask_bytes, workspace, workspace_bytes, stream)
 
 
 def fa_fwd_f32(q, k, v, o, lse, B, H, N, d, scale, causal, stream):

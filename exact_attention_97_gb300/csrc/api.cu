@@ -556,7 +556,57 @@ static int make_dropout(float p, unsigned long long seed, unsigned int offset, u
   dr->head_base = head_base;
   dr->t = static_cast<uint32_t>(t);
   dr->inv_keep = static_cast<float>(256.0 / (256.0 - t));
+  dr->mask = nullptr;
+  dr->n_qt = dr->n_kt = 0;
   return FA_OK;
+}
+
+// Bytes of saved keep bits for the shape (0 if a size is not positive): a 2 KB
+// block per (head, query tile, key tile).
+static size_t mask_bytes_for(int B, int H, int Nq, int Nk) {
+  if (B < 1 || H < 1 || Nq < 1 || Nk < 1) return 0;
+  return static_cast<size_t>(B) * H * ((static_cast<size_t>(Nq) + 127) / 128) * ((static_cast<size_t>(Nk) + 127) / 128) *
+         2048;
+}
+
+// Attaches the caller's saved-bits buffer to the dropout parameters.
+static int attach_mask(Dropout *dr, const void *mask, size_t mask_bytes, int B, int H, int Nq, int Nk) {
+  const size_t need = mask_bytes_for(B, H, Nq, Nk);
+  if (need == 0) return FA_ERR_SHAPE;
+  if (!mask) return FA_ERR_NULL;
+  if (!aligned(mask, 16)) return FA_ERR_ALIGN;
+  if (mask_bytes < need) return FA_ERR_WORKSPACE;
+  dr->mask = static_cast<uint32_t *>(const_cast<void *>(mask));
+  dr->n_qt = (Nq + 127) / 128;
+  dr->n_kt = (Nk + 127) / 128;
+  return FA_OK;
+}
+
+size_t fa_dropout_mask_size(int B, int H, int Nq, int Nk) { return mask_bytes_for(B, H, Nq, Nk); }
+
+int fa_fwd_dropout_mask(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int Nq,
+                        int Nk, int d, float scale, int causal, int dtype, float p_drop, unsigned long long seed,
+                        unsigned int offset, unsigned int head_base, void *mask, size_t mask_bytes,
+                        fa_stream_t stream) {
+  if (dtype != FA_BF16 && dtype != FA_F16) return dtype == FA_F32 ? FA_ERR_UNSUPPORTED : FA_ERR_ARG;
+  Dropout dr;
+  int st = make_dropout(p_drop, seed, offset, head_base, &dr);
+  if (st == FA_OK) st = attach_mask(&dr, mask, mask_bytes, B, H, Nq, Nk);
+  if (st != FA_OK) return st;
+  return fwd16(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, stream, dtype == FA_F16, &dr);
+}
+
+int fa_bwd_dropout_mask(const void *q, const void *k, const void *v, const void *o, const float *lse,
+                        const void *dO, void *dq, void *dk, void *dv, int B, int H, int Nq, int Nk, int d,
+                        float scale, int causal, int dtype, float p_drop, const void *mask, size_t mask_bytes,
+                        void *workspace, size_t workspace_bytes, fa_stream_t stream) {
+  if (dtype != FA_BF16 && dtype != FA_F16) return dtype == FA_F32 ? FA_ERR_UNSUPPORTED : FA_ERR_ARG;
+  Dropout dr;
+  int st = make_dropout(p_drop, 0, 0, 0, &dr);  // the bits come from `mask`, not the generator
+  if (st == FA_OK) st = attach_mask(&dr, mask, mask_bytes, B, H, Nq, Nk);
+  if (st != FA_OK) return st;
+  return bwd16(q, k, v, o, lse, dO, dq, dk, dv, B, H, Nq, Nk, d, scale, causal, workspace, workspace_bytes,
+               stream, dtype == FA_F16, &dr);
 }
 
 int fa_fwd_dropout(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int Nq,

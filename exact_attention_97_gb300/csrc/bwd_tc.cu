@@ -164,6 +164,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_flag;
   __shared__ __align__(16) float Lst[NST][kBlk], Dst[NST][kBlk];  // per stage, by bulk copy
+  // with saved dropout bits: the stage's 2 KB block (128 query rows x 4 words)
+  __shared__ __align__(16) uint32_t Mst[DROP ? NST : 1][DROP ? kBlk * 4 : 4];
 
   const int warp = warp_id(), lane = lane_id();
   const int n_tiles_all = (N + kBlk - 1) / kBlk;
@@ -247,7 +249,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tmV);
       tma_prefetch_desc(&tmdO);
       bool ok = true;
-      int g = 0, it = 0, rank, bh;
+      int g = 0, it = 0, rank, bh, kb = 0;
       auto load_qd = [&](int row) -> bool {
         const int st = g % NST;
         if (g >= NST && !mbar_wait(&qd_empty[st], ((g / NST) & 1) ^ 1, &abort_flag)) return false;
@@ -269,12 +271,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           bulk_load(Lst[st], Lp + prow, kBlk * 4, &ld_full[st]);
           bulk_load(Dst[st], Dp + prow, kBlk * 4, &ld_full[st]);
         } else {
-          mbar_arrive_expect_tx(&qd_full[st], 2 * C::kTileBytes + 2 * kBlk * 4);
+          const bool saved = DROP && drop.mask;
+          mbar_arrive_expect_tx(&qd_full[st], 2 * C::kTileBytes + 2 * kBlk * 4 + (saved ? kBlk * 16 : 0));
           load_rows(smem + C::kQ + st * C::kTileBytes, &tmQ, &qd_full[st], D, row, bh);
           load_rows(smem + C::kDO + st * C::kTileBytes, &tmdO, &qd_full[st], D, row, bh);
           const size_t prow = static_cast<size_t>(bh) * Np + row;
           bulk_load(Lst[st], Lp + prow, kBlk * 4, &qd_full[st]);
           bulk_load(Dst[st], Dp + prow, kBlk * 4, &qd_full[st]);
+          if (saved)  // the keep bits of query tile row / 128 against this key block
+            bulk_load(Mst[st], reinterpret_cast<const uint8_t *>(drop.mask) + dropout_block(drop, bh, row / kBlk, kb),
+                      kBlk * 16, &qd_full[st]);
         }
         ++g;
         return true;
@@ -284,7 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int step = sched_item(sched, cta, k, rank, bh);
         if (step == kDone) break;
         if (step == kSkip) continue;
-        const int kb = block_of(rank);
+        kb = block_of(rank);
         const int i_first = first_tile(rank), n_tiles = n_tiles_all - i_first;
         {  // the next block's K and V are read once: start them towards L2 now
           int nr, nbh, ns, k2 = k + 1;
@@ -484,10 +490,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int q0 = (i_first + t) * kBlk + h * 64;  // first query of this warpgroup's columns
         const int qmin = (key >= Nk) ? (q0 + 64) : qmin0;
         uint32_t keep[2];  // dropout: keep bits of this key for the 64 queries, drawn while S^T is in flight
-        if constexpr (DROP) dropout_col_bits<2>(drop, static_cast<uint32_t>(bh), key, q0, keep);
+        if constexpr (DROP)
+          if (!drop.mask) dropout_col_bits<2>(drop, static_cast<uint32_t>(bh), key, q0, keep);
         if (!mbar_wait_warp(PAIR ? &ld_full[st] : &qd_full[st], (g / NST) & 1, &abort_flag)) {
           ok = false;
           break;
+        }
+        if constexpr (DROP) {
+          if (drop.mask) {
+            // saved bits are stored by query row: this key's bit is bit
+            // `lane` of word wq of each row, and the words wq of the
+            // warpgroup's 64 rows are consecutive (the same for the whole
+            // warp: broadcast loads)
+            keep[0] = keep[1] = 0u;
+            const uint4 *col = reinterpret_cast<const uint4 *>(&Mst[st][wq * kBlk + 64 * h]);
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+              const uint4 w4 = col[c];
+              const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int i = 4 * c + e;
+                keep[i >> 5] |= ((w[e] >> lane) & 1u) << (i & 31);
+              }
+            }
+          }
         }
         const float4 *L4 = reinterpret_cast<const float4 *>(Lst[st] + h * 64);
         const float4 *D4 = reinterpret_cast<const float4 *>(Dst[st] + h * 64);
@@ -530,8 +557,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int u = 0; u < 32; ++u) {
               const uint32_t kb = keep[u >> 4] >> ((2 * u) & 31);
-              pk[u] = E::pack((kb & 1u) ? pf[2 * u] * drop.inv_keep : 0.f,
-                              (kb & 2u) ? pf[2 * u + 1] * drop.inv_keep : 0.f);
+              // P o Z; the 1 / (1 - p) of dV is applied once, in the epilogue
+              pk[u] = E::pack((kb & 1u) ? pf[2 * u] : 0.f, (kb & 2u) ? pf[2 * u + 1] : 0.f);
             }
             tmem_st32(tmem + lane_addr + C::tS + h * 64, pk);
           } else {
@@ -594,7 +621,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       {
         const uint32_t col = h ? C::tDK : C::tDV;
-        const float mul = h ? scale : 1.f;
+        const float mul = h ? scale : (DROP ? drop.inv_keep : 1.f);  // dV takes the dropout's 1 / (1 - p) here
         const CUtensorMap *map = h ? &tmdK : &tmdV;
         uint8_t *stg = smem + C::kStg + (warp - 4) * 2 * C::kStgBuf;
         const int row0 = kb * kBlk + wq * 32;
@@ -1030,13 +1057,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int qt = qtile_of(rank), n_kb = kblocks(rank);
       const int q = qt * kBlk + r;
       const float nl = nl_next, drow = drow_next;
-      const uint64_t nn = f2_pack(nl, nl), dd2 = f2_pack(drow, drow);
+      const uint64_t nn = f2_pack(nl, nl), dd2 = f2_pack(drow, drow), ndd2 = f2_pack(-drow, -drow);
       const int kvis = causal ? min(Nk, q + 1 + off) : Nk;  // keys below kvis are visible
       for (int j = 0; j < n_kb; ++j, ++g) {
         const uint32_t sb = C::tS + (g & 1) * 128 + h * 64;
         const int limit = kvis - (j * kBlk + h * 64);  // columns at or past limit are masked
         uint32_t keep[2];  // dropout: keep bits of this row for the 64 keys, drawn while S is in flight
-        if constexpr (DROP) dropout_row_bits<2>(drop, static_cast<uint32_t>(bh), q, j * kBlk + h * 64, keep);
+        if constexpr (DROP) {
+          if (drop.mask) {  // saved by the forward: words 2h, 2h + 1 of this row in block (qt, j)
+            const uint32_t *blk = drop.mask + dropout_block(drop, bh, qt, j) / 4 + r;
+            keep[0] = __ldg(blk + (2 * h) * kBlk);
+            keep[1] = __ldg(blk + (2 * h + 1) * kBlk);
+          } else {
+            dropout_row_bits<2>(drop, static_cast<uint32_t>(bh), q, j * kBlk + h * 64, keep);
+          }
+        }
         if (!mbar_wait_warp(&s_full[g & 1], (g >> 1) & 1, &abort_flag)) { ok = false; break; }
         tc_fence_after();
         float p[64];
@@ -1065,14 +1100,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t ds[32];
 #pragma unroll
           for (int u = 0; u < 32; ++u) {
-            float dp0 = __uint_as_float(rr[2 * u]), dp1 = __uint_as_float(rr[2 * u + 1]);
-            if constexpr (DROP) {  // dP = (dO V^T) o Z / (1 - p)
-              const uint32_t kb = keep[u >> 4] >> ((2 * u) & 31);
-              dp0 = (kb & 1u) ? dp0 * drop.inv_keep : 0.f;
-              dp1 = (kb & 2u) ? dp1 * drop.inv_keep : 0.f;
-            }
+            const float dp0 = __uint_as_float(rr[2 * u]), dp1 = __uint_as_float(rr[2 * u + 1]);
             float d0, d1;  // p (dP - D), two lanes at a time
-            f2_unpack(f2_mul(f2_pack(p[2 * u], p[2 * u + 1]), f2_sub(f2_pack(dp0, dp1), dd2)), d0, d1);
+            if constexpr (DROP) {  // dP = (dO V^T) o Z / (1 - p): dP m - D with m = Z / (1 - p)
+              const uint32_t kb = keep[u >> 4] >> ((2 * u) & 31);
+              const uint64_t m2 = f2_pack((kb & 1u) ? drop.inv_keep : 0.f, (kb & 2u) ? drop.inv_keep : 0.f);
+              f2_unpack(f2_mul(f2_pack(p[2 * u], p[2 * u + 1]), f2_fma(f2_pack(dp0, dp1), m2, ndd2)), d0, d1);
+            } else {
+              f2_unpack(f2_mul(f2_pack(p[2 * u], p[2 * u + 1]), f2_sub(f2_pack(dp0, dp1), dd2)), d0, d1);
+            }
             ds[u] = E::pack(d0, d1);
           }
           tmem_st32(tmem + lane_addr + sb, ds);  // over scores already read

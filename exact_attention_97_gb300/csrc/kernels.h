@@ -14,13 +14,28 @@ namespace fa {
 // iff byte j mod 4 of word i mod 4 of Philox4x32-10 with counter
 // (j/4, i/4, head_base + h, offset) and key (k0, k1) is >= t; kept
 // probabilities are scaled by inv_keep = 256 / (256 - t).
+//
+// Saved keep bits (mask != nullptr): the forward also writes every visited
+// tile's bits there, and the backward passes read them instead of drawing
+// them again. Layout: for head bh, query tile qt, key tile kt, a 2 KB block
+// at ((bh * n_qt + qt) * n_kt + kt) * 2048 bytes of 512 words, word-major:
+// word w * 128 + r holds bit b = the keep bit of (query 128 qt + r,
+// key 128 kt + 32 w + b). A row owner reads one word per 32 keys (coalesced
+// across rows); a key owner gathers its bit from 128 consecutive words.
 struct Dropout {
   uint32_t k0, k1;  // the 64-bit seed, low word first
   uint32_t offset;
   uint32_t head_base;  // index of the call's first head in a larger problem
   uint32_t t;       // byte threshold, 0..255
   float inv_keep;
+  uint32_t *mask;   // saved keep bits, or nullptr (draw them)
+  int n_qt, n_kt;   // query and key tiles per head of the saved layout
 };
+
+// Byte offset of the saved keep bits of tile (qt, kt) of head bh.
+__host__ __device__ inline size_t dropout_block(const Dropout &d, size_t bh, int qt, int kt) {
+  return ((bh * static_cast<size_t>(d.n_qt) + qt) * static_cast<size_t>(d.n_kt) + kt) * 2048;
+}
 
 // Error codes shared with include/fa.h (kept numerically identical).
 enum : int {

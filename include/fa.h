@@ -180,6 +180,45 @@ int fa_bwd_dropout(const void *q, const void *k, const void *v, const void *o,
                    unsigned int head_base, void *workspace,
                    size_t workspace_bytes, fa_stream_t stream);
 
+/*
+ * Dropout with saved keep bits: the same method, results and arguments as
+ * fa_fwd_dropout / fa_bwd_dropout, but the forward also writes every keep
+ * bit it draws into `mask`, and the backward reads them from there instead
+ * of drawing them again with Philox4x32-10 (which costs each backward pass
+ * about as much as the forward's drawing). The trade is memory: one bit per
+ * (query, key) pair, fa_dropout_mask_size(B, H, Nq, Nk) bytes, e.g. 512 MiB
+ * for B 8, H 32, Nq = Nk = 4096.
+ *   mask    device memory owned by the caller, 16-byte aligned, at least
+ *           fa_dropout_mask_size(...) bytes (FA_ERR_NULL / FA_ERR_ALIGN /
+ *           FA_ERR_WORKSPACE otherwise). Layout: for head bh = b*H + h (the
+ *           call's own heads), query tile qt < ceil(Nq/128) and key tile
+ *           kt < ceil(Nk/128), a 2048-byte block at byte offset
+ *           ((bh * ceil(Nq/128) + qt) * ceil(Nk/128) + kt) * 2048 of 512
+ *           32-bit words, word-major: bit b of word w * 128 + r = the keep
+ *           bit of query 128 qt + r and key 128 kt + 32 w + b (the Philox
+ *           mask of fa_fwd_dropout with the given seed, offset and
+ *           head_base).
+ *           Blocks of tiles the causal mask hides entirely, and bits past Nq
+ *           or Nk, are left unspecified.
+ *   backward  takes the forward's p_drop and the mask it wrote (no seed:
+ *           the bits are given); its results equal fa_bwd_dropout's with the
+ *           forward's seed, offset and head_base, bit for bit.
+ */
+size_t fa_dropout_mask_size(int B, int H, int Nq, int Nk);
+int fa_fwd_dropout_mask(const void *q, const void *k, const void *v, void *o,
+                        float *lse, int B, int H, int Nq, int Nk, int d,
+                        float scale, int causal, int dtype, float p_drop,
+                        unsigned long long seed, unsigned int offset,
+                        unsigned int head_base, void *mask, size_t mask_bytes,
+                        fa_stream_t stream);
+int fa_bwd_dropout_mask(const void *q, const void *k, const void *v,
+                        const void *o, const float *lse, const void *dO,
+                        void *dq, void *dk, void *dv, int B, int H, int Nq,
+                        int Nk, int d, float scale, int causal, int dtype,
+                        float p_drop, const void *mask, size_t mask_bytes,
+                        void *workspace, size_t workspace_bytes,
+                        fa_stream_t stream);
+
 /* Forward with float tensors (all fp32 arithmetic, exact expf). Same
  * arguments and layout as fa_fwd with float element type. */
 int fa_fwd_f32(const float *q, const float *k, const float *v, float *o,

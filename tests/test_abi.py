@@ -154,6 +154,26 @@ def test_f32_argument_errors(lib):
     assert lib.fa_bwd_f32(*ptrs, 1, 1, 4, 2, 1.0, 0, None, 0, None) == 5
 
 
+def test_dropout_mask_size_and_argument_errors(lib):
+    assert fa.fa_dropout_mask_size(8, 32, 4096, 4096) == 8 * 32 * 32 * 32 * 2048
+    assert fa.fa_dropout_mask_size(1, 2, 300, 129) == 2 * 3 * 2 * 2048
+    assert fa.fa_dropout_mask_size(0, 1, 1, 1) == 0
+    need = fa.fa_dropout_mask_size(1, 1, 128, 128)
+    args = [P] * 5
+    fwd = lambda mask, nbytes, p=0.1, Nq=128: lib.fa_fwd_dropout_mask(  # noqa: E731
+        *args, 1, 1, Nq, 128, 64, 0.125, 0, fa.FA_BF16, p, 1, 0, 0, mask, nbytes, None)
+    assert fwd(None, need) == 1
+    assert fwd(P + 8, need) == 4
+    assert fwd(P, need - 16) == 5
+    assert fwd(P, need, p=1.0) == 9
+    assert fwd(P, need, Nq=0) == 2
+    ptrs = [P] * 9
+    bwd = lambda mask, nbytes: lib.fa_bwd_dropout_mask(  # noqa: E731
+        *ptrs, 1, 1, 128, 128, 64, 0.125, 0, fa.FA_BF16, 0.1, mask, nbytes, P, 1 << 30, None)
+    assert bwd(None, need) == 1
+    assert bwd(P, need - 1) == 5
+
+
 def test_status_read_argument_errors(lib):
     assert lib.fa_status_async(None, None) == 1
     assert lib.fa_status_async(P + 2, None) == 4

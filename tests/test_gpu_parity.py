@@ -336,6 +336,68 @@ def test_dropout_kv_f16_and_d256():
     check("dropout_fwd_d256", "bf16", got, _drop_ref(q, k, v, None, 1.0 / 16, True, 42, 0, 0.2))
 
 
+def _saved_bits(buf, B, H, Nq, Nk):
+    """Unpack a saved-keep-bits buffer into a [B, H, Nq, Nk] bool array (its
+    documented layout: per head, query tile and key tile a block of 512
+    words, bit b of word w * 128 + r = the bit of row r and key 32 w + b)."""
+    nqt, nkt = (Nq + 127) // 128, (Nk + 127) // 128
+    words = buf.cpu().numpy()[: B * H * nqt * nkt * 2048].view(np.uint32).reshape(B * H, nqt, nkt, 4, 128)
+    rows = np.ascontiguousarray(words.transpose(0, 1, 2, 4, 3)).view(np.uint8)  # [BH, qt, kt, row, 16 bytes]
+    bits = np.unpackbits(rows, axis=-1, bitorder="little")  # [BH, qt, kt, row, 128 keys]
+    bits = bits.transpose(0, 1, 3, 2, 4).reshape(B * H, nqt * 128, nkt * 128)[:, :Nq, :Nk]
+    return bits.reshape(B, H, Nq, Nk).astype(bool)
+
+
+@pytest.mark.parametrize("Nq,Nk,causal", [(300, 513, False), (300, 513, True), (128, 128, False)])
+def test_dropout_saved_bits_are_the_oracle_mask(Nq, Nk, causal):
+    """The forward's saved keep bits equal the oracle's Philox mask bit for
+    bit on every visible (query, key) pair."""
+    import exact_attention_97_gb300 as fa
+    seed, offset, p, B, H = 0xABCDEF0123, 9, 0.3, 1, 3
+    q, _, _, _ = make_qkv_do(B, H, Nq, 64, seed=31, dtype=torch.bfloat16)
+    _, k, v, _ = make_qkv_do(B, H, Nk, 64, seed=32, dtype=torch.bfloat16)
+    dev = torch.device("cuda")
+    mask = fa.dropout_mask_buffer(B, H, Nq, Nk, dev)
+    fa.attention_forward(q.to(dev), k.to(dev), v.to(dev), 0.125, causal, dropout_p=p, seed=seed, offset=offset,
+                         head_base=5, dropout_mask=mask)
+    torch.cuda.synchronize()
+    assert fa.fa_device_status() == 0
+    got = _saved_bits(mask, B, H, Nq, Nk)
+    t = oracle.dropout_threshold(p)
+    want = np.stack([oracle.dropout_mask(seed, offset, t, 5 + h, Nq, Nk) for h in range(B * H)]).reshape(
+        B, H, Nq, Nk).astype(bool)
+    visible = np.ones((Nq, Nk), dtype=bool)
+    if causal:
+        visible = np.arange(Nk)[None, :] <= np.arange(Nq)[:, None] + (Nk - Nq)
+    assert np.array_equal(got[..., visible], want[..., visible])
+
+
+@pytest.mark.parametrize("d,Nq,Nk,causal,dtype", [(64, 300, 300, True, torch.bfloat16),
+                                                  (96, 257, 700, True, torch.bfloat16),
+                                                  (128, 1000, 1000, False, torch.bfloat16),
+                                                  (128, 200, 777, True, torch.float16)])
+def test_dropout_saved_bits_give_the_regenerated_results(d, Nq, Nk, causal, dtype):
+    """Backward from the saved bits equals the backward that draws them again,
+    bit for bit (same keep decisions, same arithmetic); both forwards agree too."""
+    import exact_attention_97_gb300 as fa
+    seed, offset, p, B, H = 314159, 2, 0.2, 2, 2
+    q, _, _, dO = make_qkv_do(B, H, Nq, d, seed=40 + d, dtype=dtype)
+    _, k, v, _ = make_qkv_do(B, H, Nk, d, seed=41 + d, dtype=dtype)
+    dev = torch.device("cuda")
+    q, k, v, dO = (x.to(dev) for x in (q, k, v, dO))
+    scale = 1.0 / math.sqrt(d)
+    kw = dict(dropout_p=p, seed=seed, offset=offset)
+    o1, l1 = fa.attention_forward(q, k, v, scale, causal, **kw)
+    g1 = fa.attention_backward(q, k, v, o1, l1, dO, scale, causal, **kw)
+    mask = fa.dropout_mask_buffer(B, H, Nq, Nk, dev)
+    o2, l2 = fa.attention_forward(q, k, v, scale, causal, dropout_mask=mask, **kw)
+    g2 = fa.attention_backward(q, k, v, o2, l2, dO, scale, causal, dropout_p=p, dropout_mask=mask)
+    torch.cuda.synchronize()
+    assert fa.fa_device_status() == 0
+    for a, b in zip((o1, l1, *g1), (o2, l2, *g2)):
+        assert torch.equal(a, b)
+
+
 def test_dropout_zero_is_the_plain_path():
     import exact_attention_97_gb300 as fa
     q, k, v, dO = (x.cuda() for x in make_qkv_do(1, 2, 260, 128, seed=8, dtype=torch.bfloat16))
