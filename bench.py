@@ -38,8 +38,8 @@ METRIC_FWD = "attention forward TFLOP/s (forward-only run of the workload in con
 # with the number of heads). Only valid for the kernel source it was measured
 # on: reported as null once that file changes.
 MEASURED_TRAFFIC = {"workload": "bf16_B8_H32_N4096_d128", "kernel": "bwd_dkdv_kernel<128>",
-                    "bytes": 4 * (270.937088e6 + 103.252480e6),
-                    "source": "exact_attention_97_gb300/csrc/bwd_tc.cu", "sha256_16": "90c6224de6860c6d"}
+                    "bytes": 4 * (270.790144e6 + 104.232960e6),
+                    "source": "exact_attention_97_gb300/csrc/bwd_tc.cu", "sha256_16": "8bd5852cb4cac89d"}
 
 
 def _measured_traffic(kernel: str, workload: str):

@@ -38,20 +38,46 @@ def _torch():
 
 
 def _check(name, t, shape, dtype):
+    if t.is_cuda and t.dtype is dtype and t.shape == shape and t.is_contiguous():
+        return  # the common case, tested in one expression (these calls sit on small problems' critical path)
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
     if tuple(t.shape) != tuple(shape):
         raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
     if t.dtype != dtype:
         raise ValueError(f"{name} has dtype {t.dtype}, expected {dtype}")
-    if not t.is_contiguous():
-        raise ValueError(f"{name} must be contiguous")
+    raise ValueError(f"{name} must be contiguous")
 
 
-def _stream_handle(stream):
+def _stream_handle(stream, device=None):
+    """The raw cudaStream_t of `stream`, or of the current stream of `device`
+    (torch's raw-handle query when it has one: creating a Stream object costs
+    microseconds per call)."""
     torch = _torch()
-    s = stream if stream is not None else torch.cuda.current_stream()
-    return s.cuda_stream
+    if stream is not None:
+        return stream.cuda_stream
+    raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+    if raw is not None:
+        return raw(torch.cuda.current_device() if device is None else device)
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+class _Nothing:
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        return False
+
+
+_NOTHING = _Nothing()
+
+
+def _device_of(t):
+    """A context that makes t's device current, entered only when it is not already."""
+    torch = _torch()
+    dev = t.get_device()
+    return _NOTHING if dev == torch.cuda.current_device() else torch.cuda.device(dev)
 
 
 def dropout_mask_buffer(B, H, Nq, Nk, device=None):
@@ -116,7 +142,8 @@ def attention_forward(q, k, v, scale=None, causal=False, out=None, lse=None, str
     for name, t in (("k", k), ("v", v)):
         _check(name, t, (B, H, Nk, d), dt)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    with torch.cuda.device(q.device):
+    with _device_of(q):
+        dev = q.get_device()
         o = torch.empty_like(q) if out is None else out
         lse = torch.empty((B, H, N), device=q.device, dtype=torch.float32) if lse is None else lse
         _check("out", o, (B, H, N, d), dt)
@@ -128,18 +155,18 @@ def attention_forward(q, k, v, scale=None, causal=False, out=None, lse=None, str
             kind = FA_F16 if dt == torch.float16 else FA_BF16
             if dropout_mask is not None:
                 fa_fwd_dropout_mask(*ptrs, B, H, N, Nk, d, scale, int(bool(causal)), kind, dropout_p, seed, offset,
-                                    head_base, *_mask_arg(dropout_mask), _stream_handle(stream))
+                                    head_base, *_mask_arg(dropout_mask), _stream_handle(stream, dev))
             else:
                 fa_fwd_dropout(*ptrs, B, H, N, Nk, d, scale, int(bool(causal)), kind, dropout_p, seed, offset,
-                               head_base, _stream_handle(stream))
+                               head_base, _stream_handle(stream, dev))
         elif Nk != N:
             if dt == torch.float32:
                 raise ValueError("float32 needs k and v with as many rows as q")
             fa_fwd_kv(*ptrs, B, H, N, Nk, d, scale, int(bool(causal)),
-                      FA_F16 if dt == torch.float16 else FA_BF16, _stream_handle(stream))
+                      FA_F16 if dt == torch.float16 else FA_BF16, _stream_handle(stream, dev))
         else:
             fn = {torch.bfloat16: fa_fwd, torch.float16: fa_fwd_f16, torch.float32: fa_fwd_f32}[dt]
-            fn(*ptrs, B, H, N, d, scale, int(bool(causal)), _stream_handle(stream))
+            fn(*ptrs, B, H, N, d, scale, int(bool(causal)), _stream_handle(stream, dev))
         if check:
             _check_status("attention_forward", stream)
     return o, lse
@@ -162,7 +189,8 @@ def attention_backward(q, k, v, o, lse, dO, scale=None, causal=False, workspace=
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     kind = {torch.bfloat16: FA_BF16, torch.float16: FA_F16, torch.float32: FA_F32}[dt]
     need = fa_bwd_workspace_size(B, H, N, d, kind)
-    with torch.cuda.device(q.device):
+    with _device_of(q):
+        dev = q.get_device()
         if workspace is None:
             workspace = torch.empty(need, device=q.device, dtype=torch.uint8)
         if workspace.numel() * workspace.element_size() < need:
@@ -171,7 +199,7 @@ def attention_backward(q, k, v, o, lse, dO, scale=None, causal=False, workspace=
                                                       torch.empty_like(v))
         ptrs = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), dO.data_ptr(),
                 dq.data_ptr(), dk.data_ptr(), dv.data_ptr())
-        ws = (workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream_handle(stream))
+        ws = (workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream_handle(stream, dev))
         if dropout_p:
             if kind == FA_F32:
                 raise ValueError("dropout needs bfloat16 or float16 inputs")

@@ -67,6 +67,8 @@ def lib_path() -> str:
 def load(build_if_missing: bool = True):
     """Load libfa.so (building it first when asked and nvcc is present)."""
     global _lib
+    if _lib is not None:  # loaded: no lock on the per-call path
+        return _lib
     with _lock:
         if _lib is None:
             path = _build.LIB

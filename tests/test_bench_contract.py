@@ -36,7 +36,8 @@ def test_reference_arm_json_line():
 
 @pytest.mark.gpu
 def test_our_arm_json_line():
-    d = _run(["--shape", "2,8,1024,128,1", "--steps", "3", "--warmup", "3", "--no-cpu-baseline"], timeout=600)
+    d = _run(["--shape", "2,8,1024,128,1", "--steps", "3", "--warmup", "3", "--no-cpu-baseline", "--graph"],
+             timeout=600)
     for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
                 "scaling", "vs_baseline", "dtype", "data", "config", "roofline", "e2e", "gpu_launches", "clocks",
                 "hbm", "kernels"):
@@ -50,3 +51,14 @@ def test_our_arm_json_line():
     assert e["value"] < d["value"]  # host copies are inside its timed region
     assert {"sm_mhz", "sm_max_mhz", "reasons"} <= set(d["clocks"])
     assert d["config"]["causal"] is True and d["dtype"] == "bf16"
+    # median and spread over the timed steps, peak allocated memory
+    sp = d["spread"]
+    assert sp["ms_p10"] <= sp["ms_median"] <= sp["ms_p90"]
+    assert sp["value_p10"] <= sp["value_median"] <= sp["value_p90"]
+    assert d["peak_mem_bytes"] > 0
+    # the end-to-end line explains itself: copy bandwidths and the floor they set
+    assert e["h2d_gbs_alone"] > 0 and e["d2h_gbs_alone"] > 0
+    assert e["floor_ms"] >= e["copy_ms_both_directions_at_once"] and e["floor_ms"] > 0
+    # the same step replayed from a CUDA graph
+    g = d["graph"]
+    assert g["ms_per_step"] > 0 and g["value"] > 0
