@@ -459,15 +459,20 @@ def run_ours(args, w):
             e2e_step()
         torch.cuda.synchronize()
         e2e_steps = max(3, min(args.steps, 10))
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        # every step bracketed by its own events on the caller's stream (the
+        # step's streams join it): the median step is the value, so a single
+        # host stall does not stand for the run
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps + 1)]
         if world > 1:
             dist.barrier()
-        a.record(stream)
-        for _ in range(e2e_steps):
+        ev[0].record(stream)
+        for i in range(e2e_steps):
             e2e_step()
-        b.record(stream)
+            ev[i + 1].record(stream)
         torch.cuda.synchronize()
-        ems = a.elapsed_time(b)
+        per_step = sorted(ev[i].elapsed_time(ev[i + 1]) for i in range(e2e_steps))
+        e2e_mean = ev[0].elapsed_time(ev[-1]) / e2e_steps
+        ems = statistics.median(per_step) * e2e_steps
         ems = max_over_ranks(ems, dev)
         bytes_in = sum(t.numel() * t.element_size() for t in ((q_h, k_h, v_h) if args.fwd_only else
                                                                 (q_h, k_h, v_h, do_h)))
@@ -521,6 +526,8 @@ def run_ours(args, w):
         e2e = {"value": flops_step * world * e2e_steps / (ems * 1e-3) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": bytes_in, "d2h_bytes_per_step": bytes_out,
                "ms_per_step": ems / e2e_steps,
+               "ms_per_step_min_median_max_mean": [per_step[0], statistics.median(per_step), per_step[-1],
+                                                   e2e_mean],
                "h2d_gbs_alone": h2d_gbs, "d2h_gbs_alone": d2h_gbs,
                "copy_ms_alone": {"h2d": h2d_ms, "d2h": d2h_ms},
                "copy_ms_both_directions_at_once": both_ms,
