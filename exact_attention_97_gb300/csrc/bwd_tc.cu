@@ -38,8 +38,10 @@
 // last products and its epilogue. The dK/dV pass writes its results through
 // per-warp shared-memory boxes and TMA stores, the dQ pass with whole-line
 // row-segment stores. Head sizes 64, 96 and 128.
-// With dropout (DROP instances) both passes draw the keep bits of each tile
-// (Philox4x32-10, sm103.cuh) before its scores arrive: dV takes
+// With dropout both passes take the keep bits of each tile before its scores
+// arrive: DROP = kDrawn instances draw them (Philox4x32-10, sm103.cuh),
+// DROP = kSaved instances read the ones the forward saved (separate
+// instances, so that each is compiled for its own path). dV takes
 // P o Z / (1 - p), and dP is scaled by Z / (1 - p) before dS.
 #include <cuda_runtime.h>
 #include <math.h>
@@ -56,6 +58,7 @@ namespace fa {
 namespace {
 
 constexpr int kBlk = 128;       // keys per block and query rows per tile
+constexpr int kNoDrop = 0, kDrawn = 1, kSaved = 2;  // DROP: no dropout, keep bits drawn, keep bits saved
 constexpr int kThreads = 384;   // 12 warps
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -142,7 +145,7 @@ struct DkdvCfg {
   static constexpr uint32_t tS = 0, tDP = 128, tDV = 256, tDK = 256 + D;  // TMEM columns
 };
 
-template <int D, bool F16, bool DROP, bool PAIR>
+template <int D, bool F16, int DROP, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -165,7 +168,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ int abort_flag;
   __shared__ __align__(16) float Lst[NST][kBlk], Dst[NST][kBlk];  // per stage, by bulk copy
   // with saved dropout bits: the stage's 2 KB block (128 query rows x 4 words)
-  __shared__ __align__(16) uint32_t Mst[DROP ? NST : 1][DROP ? kBlk * 4 : 4];
+  __shared__ __align__(16) uint32_t Mst[DROP == kSaved ? NST : 1][DROP == kSaved ? kBlk * 4 : 4];
 
   const int warp = warp_id(), lane = lane_id();
   const int n_tiles_all = (N + kBlk - 1) / kBlk;
@@ -271,14 +274,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           bulk_load(Lst[st], Lp + prow, kBlk * 4, &ld_full[st]);
           bulk_load(Dst[st], Dp + prow, kBlk * 4, &ld_full[st]);
         } else {
-          const bool saved = DROP && drop.mask;
+          constexpr bool saved = DROP == kSaved;
           mbar_arrive_expect_tx(&qd_full[st], 2 * C::kTileBytes + 2 * kBlk * 4 + (saved ? kBlk * 16 : 0));
           load_rows(smem + C::kQ + st * C::kTileBytes, &tmQ, &qd_full[st], D, row, bh);
           load_rows(smem + C::kDO + st * C::kTileBytes, &tmdO, &qd_full[st], D, row, bh);
           const size_t prow = static_cast<size_t>(bh) * Np + row;
           bulk_load(Lst[st], Lp + prow, kBlk * 4, &qd_full[st]);
           bulk_load(Dst[st], Dp + prow, kBlk * 4, &qd_full[st]);
-          if (saved)  // the keep bits of query tile row / 128 against this key block
+          if constexpr (saved)  // the keep bits of query tile row / 128 against this key block
             bulk_load(Mst[st], reinterpret_cast<const uint8_t *>(drop.mask) + dropout_block(drop, bh, row / kBlk, kb),
                       kBlk * 16, &qd_full[st]);
         }
@@ -490,31 +493,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int q0 = (i_first + t) * kBlk + h * 64;  // first query of this warpgroup's columns
         const int qmin = (key >= Nk) ? (q0 + 64) : qmin0;
         uint32_t keep[2];  // dropout: keep bits of this key for the 64 queries, drawn while S^T is in flight
-        if constexpr (DROP)
-          if (!drop.mask) dropout_col_bits<2>(drop, static_cast<uint32_t>(bh), key, q0, keep);
+        if constexpr (DROP == kDrawn) dropout_col_bits<2>(drop, static_cast<uint32_t>(bh), key, q0, keep);
         if (!mbar_wait_warp(PAIR ? &ld_full[st] : &qd_full[st], (g / NST) & 1, &abort_flag)) {
           ok = false;
           break;
         }
-        if constexpr (DROP) {
-          if (drop.mask) {
-            // saved bits are stored by query row: this key's bit is bit
-            // `lane` of word wq of each row, and the words wq of the
-            // warpgroup's 64 rows are consecutive (the same for the whole
-            // warp: broadcast loads)
-            keep[0] = keep[1] = 0u;
-            const uint4 *col = reinterpret_cast<const uint4 *>(&Mst[st][wq * kBlk + 64 * h]);
+        if constexpr (DROP == kSaved) {
+          // saved bits are stored by query row, 32 keys a word: the warp's
+          // keys are word wq of each row, and the words wq of the
+          // warpgroup's 64 rows are consecutive. Lane r takes rows r and
+          // 32 + r, a transpose gives lane c the bits of bit position c,
+          // and the key of bit position keep_bit(lane) is this lane's.
+          const uint32_t *rows = &Mst[st][wq * kBlk + 64 * h];
 #pragma unroll
-            for (int c = 0; c < 16; ++c) {
-              const uint4 w4 = col[c];
-              const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const int i = 4 * c + e;
-                keep[i >> 5] |= ((w[e] >> lane) & 1u) << (i & 31);
-              }
-            }
-          }
+          for (int w = 0; w < 2; ++w)
+            keep[w] = __shfl_sync(0xffffffffu, warp_transpose_bits(rows[32 * w + lane]), keep_bit(lane));
         }
         const float4 *L4 = reinterpret_cast<const float4 *>(Lst[st] + h * 64);
         const float4 *D4 = reinterpret_cast<const float4 *>(Dst[st] + h * 64);
@@ -545,7 +538,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 pf[2 * u] = p0;
                 pf[2 * u + 1] = p1;
-                if constexpr (!DROP) pk[u] = E::pack(p0, p1);
+                if constexpr (DROP == kNoDrop) pk[u] = E::pack(p0, p1);
               }
             }
           };
@@ -553,7 +546,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             p_pairs(std::true_type{});
           else
             p_pairs(std::false_type{});
-          if constexpr (DROP) {  // dV takes P o Z / (1 - p); dS takes P
+          if constexpr (DROP != kNoDrop) {  // dV takes P o Z / (1 - p); dS takes P
 #pragma unroll
             for (int u = 0; u < 32; ++u) {
               const uint32_t kb = keep[u >> 4] >> ((2 * u) & 31);
@@ -587,7 +580,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int e = 0; e < 2; ++e) {
               const int u = 2 * u2 + e;
               float dp0 = __uint_as_float(r[2 * u]), dp1 = __uint_as_float(r[2 * u + 1]);
-              if constexpr (DROP) {  // dP = (dO V^T) o Z / (1 - p)
+              if constexpr (DROP != kNoDrop) {  // dP = (dO V^T) o Z / (1 - p)
                 const uint32_t kb = keep[u >> 4] >> ((2 * u) & 31);
                 dp0 = (kb & 1u) ? dp0 * drop.inv_keep : 0.f;
                 dp1 = (kb & 2u) ? dp1 * drop.inv_keep : 0.f;
@@ -621,7 +614,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       {
         const uint32_t col = h ? C::tDK : C::tDV;
-        const float mul = h ? scale : (DROP ? drop.inv_keep : 1.f);  // dV takes the dropout's 1 / (1 - p) here
+        const float mul = h ? scale : (DROP != kNoDrop ? drop.inv_keep : 1.f);  // dV takes the dropout's 1 / (1 - p) here
         const CUtensorMap *map = h ? &tmdK : &tmdV;
         uint8_t *stg = smem + C::kStg + (warp - 4) * 2 * C::kStgBuf;
         const int row0 = kb * kBlk + wq * 32;
@@ -702,7 +695,7 @@ struct DqCfg {
   static constexpr uint32_t tS = 0, tDP = 256, tDQ = 384;  // S buffers at 0 and 128
 };
 
-template <int D, bool F16, bool DROP, bool PAIR>
+template <int D, bool F16, int DROP, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -1063,14 +1056,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t sb = C::tS + (g & 1) * 128 + h * 64;
         const int limit = kvis - (j * kBlk + h * 64);  // columns at or past limit are masked
         uint32_t keep[2];  // dropout: keep bits of this row for the 64 keys, drawn while S is in flight
-        if constexpr (DROP) {
-          if (drop.mask) {  // saved by the forward: words 2h, 2h + 1 of this row in block (qt, j)
-            const uint32_t *blk = drop.mask + dropout_block(drop, bh, qt, j) / 4 + r;
-            keep[0] = __ldg(blk + (2 * h) * kBlk);
-            keep[1] = __ldg(blk + (2 * h + 1) * kBlk);
-          } else {
-            dropout_row_bits<2>(drop, static_cast<uint32_t>(bh), q, j * kBlk + h * 64, keep);
-          }
+        // (bit keep_bit(b) of keep[w]: key j * 128 + 64 h + 32 w + b)
+        if constexpr (DROP == kSaved) {  // saved by the forward: words 2h, 2h + 1 of this row in block (qt, j)
+          const uint32_t *blk = drop.mask + dropout_block(drop, bh, qt, j) / 4 + r;
+          keep[0] = __ldg(blk + (2 * h) * kBlk);
+          keep[1] = __ldg(blk + (2 * h + 1) * kBlk);
+        } else if constexpr (DROP == kDrawn) {
+          dropout_row_bits<2>(drop, static_cast<uint32_t>(bh), q, j * kBlk + h * 64, keep);
         }
         if (!mbar_wait_warp(&s_full[g & 1], (g >> 1) & 1, &abort_flag)) { ok = false; break; }
         tc_fence_after();
@@ -1102,9 +1094,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int u = 0; u < 32; ++u) {
             const float dp0 = __uint_as_float(rr[2 * u]), dp1 = __uint_as_float(rr[2 * u + 1]);
             float d0, d1;  // p (dP - D), two lanes at a time
-            if constexpr (DROP) {  // dP = (dO V^T) o Z / (1 - p): dP m - D with m = Z / (1 - p)
-              const uint32_t kb = keep[u >> 4] >> ((2 * u) & 31);
-              const uint64_t m2 = f2_pack((kb & 1u) ? drop.inv_keep : 0.f, (kb & 2u) ? drop.inv_keep : 0.f);
+            if constexpr (DROP != kNoDrop) {  // dP = (dO V^T) o Z / (1 - p): dP m - D with m = Z / (1 - p)
+              // keys 2u, 2u + 1 (bytes e, e + 1 of the word, bit c): shifted
+              // left by 7 - c they are byte tops, and prmt makes each a
+              // 32-bit mask for the bits of 1 / (1 - p)
+              const int b = (2 * u) & 31, c = b >> 2, e = b & 3;
+              const uint32_t y = keep[u >> 4] << (7 - c), ik = __float_as_uint(drop.inv_keep);
+              const uint64_t m2 = f2_pack(__uint_as_float(byte_signs(y, (8 + e) * 0x1111u) & ik),
+                                          __uint_as_float(byte_signs(y, (9 + e) * 0x1111u) & ik));
               f2_unpack(f2_mul(f2_pack(p[2 * u], p[2 * u + 1]), f2_fma(f2_pack(dp0, dp1), m2, ndd2)), d0, d1);
             } else {
               f2_unpack(f2_mul(f2_pack(p[2 * u], p[2 * u + 1]), f2_sub(f2_pack(dp0, dp1), dd2)), d0, d1);
@@ -1148,7 +1145,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0 && abort_flag) atomicExch(status, kErrTimeout);
 }
 
-template <int D, bool F16, bool DROP>
+template <int D, bool F16, int DROP>
 cudaError_t launch(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtensorMap &tmV,
                    const CUtensorMap &tmdO, const CUtensorMap &tmdK, const CUtensorMap &tmdV, const HalfMaps *half,
                    const void *o, const void *dO, const float *lse, void *dq, void *dk, void *dv, float *Lp,
@@ -1184,12 +1181,12 @@ cudaError_t launch(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtenso
   };
   Pass kv, q;
   int clusters_kv = 0, clusters_q = 0;
-  if constexpr (D == 128 && !DROP && FA_PAIR_KERNELS) {
+  if constexpr (D == 128 && DROP == kNoDrop && FA_PAIR_KERNELS) {
     // two-CTA clusters (block / tile pairs, M = 256 MMAs) when the heads have
     // at least two key blocks / query tiles
     static SmemOnce smem_kvp, smem_qp;
-    auto kpk = bwd_dkdv_kernel<D, F16, false, true>;
-    auto kpq = bwd_dq_kernel<D, F16, false, true>;
+    auto kpk = bwd_dkdv_kernel<D, F16, kNoDrop, true>;
+    auto kpq = bwd_dq_kernel<D, F16, kNoDrop, true>;
     if (half && n_kb_all >= 2) {
       if ((e = set_smem_once(reinterpret_cast<const void *>(kpk), DkdvCfg<D, true>::kAlloc, &smem_kvp)) !=
           cudaSuccess)
@@ -1231,9 +1228,9 @@ cudaError_t launch(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtenso
 
   auto run_kv = [&](cudaStream_t st) -> cudaError_t {
     timing_begin(st);
-    if constexpr (D == 128 && !DROP && FA_PAIR_KERNELS) {
+    if constexpr (D == 128 && DROP == kNoDrop && FA_PAIR_KERNELS) {
       if (kv.pair) {
-        cudaError_t r = launch_pair_grid(bwd_dkdv_kernel<D, F16, false, true>, kv.sched.G, kThreads,
+        cudaError_t r = launch_pair_grid(bwd_dkdv_kernel<D, F16, kNoDrop, true>, kv.sched.G, kThreads,
                                          DkdvCfg<D, true>::kAlloc, st, tmQ, tmK, tmV, tmdO, tmdK, tmdV, half->q,
                                          half->dO, Lp, Dp, N, Nk, kv.sched, scale, scale_log2, causal, drop, status);
         timing_end(st);
@@ -1251,9 +1248,9 @@ cudaError_t launch(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtenso
   };
   auto run_q = [&](cudaStream_t st) -> cudaError_t {
     timing_begin(st);
-    if constexpr (D == 128 && !DROP && FA_PAIR_KERNELS) {
+    if constexpr (D == 128 && DROP == kNoDrop && FA_PAIR_KERNELS) {
       if (q.pair) {
-        cudaError_t r = launch_pair_grid(bwd_dq_kernel<D, F16, false, true>, q.sched.G, kThreads,
+        cudaError_t r = launch_pair_grid(bwd_dq_kernel<D, F16, kNoDrop, true>, q.sched.G, kThreads,
                                          DqCfg<D, true>::kAlloc, st, tmQ, tmK, tmV, tmdO, half->k, half->v, Lp, Dp,
                                          static_cast<uint16_t *>(dq), N, Nk, q.sched, scale, scale_log2, causal, drop,
                                          status);
@@ -1289,7 +1286,7 @@ cudaError_t launch(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtenso
   return run_q(stream);
 }
 
-template <bool DROP>
+template <int DROP>
 cudaError_t dispatch(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtensorMap &tmV,
                      const CUtensorMap &tmdO, const CUtensorMap &tmdK, const CUtensorMap &tmdV, const HalfMaps *half,
                      const void *o, const void *dO, const float *lse, void *dq, void *dk, void *dv, float *Lp,
@@ -1318,10 +1315,13 @@ cudaError_t launch_bwd_16(const CUtensorMap &tmQ, const CUtensorMap &tmK, const 
                           bool f16, const Dropout *drop, int *status, int num_sms, cudaStream_t stream,
                           const BwdSide &side, int *launches) {
   *launches += 3;
+  if (drop && drop->mask)
+    return dispatch<kSaved>(tmQ, tmK, tmV, tmdO, tmdK, tmdV, half, o, dO, lse, dq, dk, dv, Lp, Dp, B, H, N, Nk, d,
+                            scale, causal, f16, *drop, status, num_sms, stream, side);
   if (drop)
-    return dispatch<true>(tmQ, tmK, tmV, tmdO, tmdK, tmdV, half, o, dO, lse, dq, dk, dv, Lp, Dp, B, H, N, Nk, d,
+    return dispatch<kDrawn>(tmQ, tmK, tmV, tmdO, tmdK, tmdV, half, o, dO, lse, dq, dk, dv, Lp, Dp, B, H, N, Nk, d,
                           scale, causal, f16, *drop, status, num_sms, stream, side);
-  return dispatch<false>(tmQ, tmK, tmV, tmdO, tmdK, tmdV, half, o, dO, lse, dq, dk, dv, Lp, Dp, B, H, N, Nk, d,
+  return dispatch<kNoDrop>(tmQ, tmK, tmV, tmdO, tmdK, tmdV, half, o, dO, lse, dq, dk, dv, Lp, Dp, B, H, N, Nk, d,
                          scale, causal, f16, Dropout{}, status, num_sms, stream, side);
 }
 

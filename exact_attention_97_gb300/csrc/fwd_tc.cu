@@ -58,9 +58,14 @@ namespace {
 constexpr int kBlockM = 128;   // query rows per tile (= TMEM lanes)
 constexpr int kBlockN = 128;   // keys per tile
 constexpr int kThreads = 256;      // 8 warps
-constexpr int kMaskWarps = 4;  // with dropout, warps 8-11 draw the keep masks (a whole row each)
+constexpr int kMaskWarps = 4;  // with dropout, warps 8-11 draw the keep masks (32 keys of each tile each)
 constexpr int kThreadsDrop = 256 + 32 * kMaskWarps;
 constexpr int kMaskSlots = 3;      // keep-mask ring (128 rows x 128 keys of bits each)
+constexpr int kMaskSlotBytes = 128 * 128 / 8;
+template <bool B>
+struct BoolTag {
+  static constexpr bool value = B;
+};
 constexpr float kRescaleLog2 = 8.0f;  // move the running max only past 2^8
 constexpr float kLn2 = 0.69314718055994531f;
 
@@ -108,7 +113,7 @@ struct FwdSmem {
   static constexpr int kK = kQ + kQBuf * kQBytes;
   static constexpr int kV = kK + kKStages * kKBytes;
   static constexpr int kMask = kV + kVStages * kVBytes;
-  static constexpr int kMaskBytes = DROP ? kMaskSlots * kBlockM * 16 : 0;
+  static constexpr int kMaskBytes = DROP ? kMaskSlots * kMaskSlotBytes : 0;
   static constexpr int kBytes = kMask + kMaskBytes;
   static constexpr int kAlloc = kBytes + 1024;  // slack for 1024-byte alignment
 };
@@ -438,11 +443,9 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
             ok = false;
             break;
           }
-          const uint4 mv = *reinterpret_cast<const uint4 *>(smem + L::kMask + (ms * kBlockM + r_local) * 16);
-          keep[0] = mv.x;
-          keep[1] = mv.y;
-          keep[2] = mv.z;
-          keep[3] = mv.w;
+          const uint32_t *mw = reinterpret_cast<const uint32_t *>(smem + L::kMask + ms * kMaskSlotBytes) + r_local;
+#pragma unroll
+          for (int w = 0; w < 4; ++w) keep[w] = mw[w * kBlockM];
           mbar_arrive(&mask_empty[ms]);
         }
         if (!mbar_wait_warp(&s_full[sb], (kt / kSBuf) & 1, &abort_flag)) {
@@ -521,12 +524,13 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
           }
           float p0, p1;
           f2_unpack(p2, p0, p1);
-          if constexpr (DROP) {  // l keeps the undropped sum; P V gets P o Z (1 / (1 - p) in the epilogue)
-            const uint32_t kb = keep[w >> 4] >> ((2 * w) & 31);
-            p0 = (kb & 1u) ? p0 : 0.f;
-            p1 = (kb & 2u) ? p1 : 0.f;
-          }
           pk[w] = E::pack(p0, p1);
+          if constexpr (DROP) {  // l keeps the undropped sum; P V gets P o Z (1 / (1 - p) in the epilogue)
+            // keys 2w, 2w + 1 are bits c + 8 e, c + 8 (e + 1) of their word (c = (2w mod 32) / 4,
+            // e = 2w mod 4); shifted left by 7 - c they are the top bits of bytes e, e + 1
+            const int b = (2 * w) & 31, c = b >> 2;
+            pk[w] &= byte_signs(keep[w >> 4] << (7 - c), (b & 3) ? 0xBBAAu : 0x9988u);
+          }
         }
         tmem_st64(tmem + lane_addr + sb * 128, pk);
         float rs;
@@ -559,13 +563,17 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
       if (row < N) lse[static_cast<size_t>(bh) * N + row] = (m_used * scale_log2 + log2f(l_sum)) * kLn2;
     }
   };
-  auto role_masks = [&]() {
+  auto role_masks = [&](auto high) {
       // ---------------------------------------------------------- keep masks
-      // Row r_local of every key tile, one tile ahead of the softmax warps at
-      // most kMaskSlots: the bits of Philox4x32-10 bytes >= t, in the layout
-      // the softmax reads (bit b of word w = key 32 w + b of the tile).
-      constexpr int kWords = 4 * 4 / kMaskWarps;  // words of a row this thread draws (4 or 2)
-      const int r_local = ((warp - 8) & 3) * 32 + lane, w0 = ((warp - 8) >> 2) * kWords;
+      // Warp 8 + c draws keys 32c .. 32c + 31 of every key tile for rows
+      // 4 lane .. 4 lane + 3 (no exchange between lanes), one tile ahead of
+      // the softmax warps at most kMaskSlots, into a slot laid out word-major
+      // (word c * 128 + r = keys 32c .. 32c + 31 of row r, bit keep_bit(b)
+      // key 32c + b): one 16-byte store per lane, 512 contiguous bytes per
+      // warp, in the same layout as the saved keep bits.
+      static_assert(kMaskWarps * 32 == kBlockN && 4 * 32 == kBlockM, "one 4 x 32 block of bits per mask lane");
+      constexpr bool kHigh = decltype(high)::value;
+      const int wc = warp - 8;
       bool ok = true;
       int kt = 0, rank, bh;
       for (int k = 0; ok; ++k) {
@@ -573,7 +581,7 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
         if (step == kDone) break;
         if (step == kSkip) continue;
         const int qtile = qtile_of(rank);
-        const int nk = ktiles(rank), row = qtile * kBlockM + r_local;
+        const int nk = ktiles(rank), row0 = qtile * kBlockM + 4 * lane;
         for (int j = 0; j < nk; ++j, ++kt) {
           const int ms = kt % kMaskSlots;
           if (kt >= kMaskSlots &&
@@ -581,19 +589,11 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
             ok = false;
             break;
           }
-          uint32_t bits[kWords];
-          // the word loop stays rolled (two Philox chains in flight): unrolled
-          // to eight, the forward measured 43 % slower
-          dropout_row_bits<kWords>(drop, static_cast<uint32_t>(bh), row, j * kBlockN + 32 * w0, bits);
-          uint32_t *slot = reinterpret_cast<uint32_t *>(smem + L::kMask + (ms * kBlockM + r_local) * 16) + w0;
-#pragma unroll
-          for (int w = 0; w < kWords; ++w) slot[w] = bits[w];
+          const uint4 bits = dropout_block_bits<kHigh>(drop, static_cast<uint32_t>(bh), row0, j * kBlockN + 32 * wc);
+          *reinterpret_cast<uint4 *>(smem + L::kMask + ms * kMaskSlotBytes + wc * 512 + 16 * lane) = bits;
           mbar_arrive(&mask_full[ms]);
-          if (drop.mask) {  // saved for the backward: row r_local of this tile's block, word-major
-            uint32_t *blk = drop.mask + dropout_block(drop, bh, qtile, j) / 4 + r_local;
-#pragma unroll
-            for (int w = 0; w < kWords; ++w) blk[(w0 + w) * 128] = bits[w];
-          }
+          if (drop.mask)  // saved for the backward
+            *reinterpret_cast<uint4 *>(drop.mask + dropout_block(drop, bh, qtile, j) / 4 + wc * 128 + 4 * lane) = bits;
         }
       }
   };
@@ -613,7 +613,8 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
       role_softmax();
     } else {
       setmaxnreg_dec<96>();
-      role_masks();
+      if (drop.t >= 128) role_masks(BoolTag<true>{});
+      else role_masks(BoolTag<false>{});
     }
   } else {
     if (warp == 0) role_k_loader();

@@ -19,9 +19,10 @@ namespace fa {
 // tile's bits there, and the backward passes read them instead of drawing
 // them again. Layout: for head bh, query tile qt, key tile kt, a 2 KB block
 // at ((bh * n_qt + qt) * n_kt + kt) * 2048 bytes of 512 words, word-major:
-// word w * 128 + r holds bit b = the keep bit of (query 128 qt + r,
-// key 128 kt + 32 w + b). A row owner reads one word per 32 keys (coalesced
-// across rows); a key owner gathers its bit from 128 consecutive words.
+// bit 8 (b mod 4) + b / 4 (keep_bit(b), sm103.cuh) of word w * 128 + r is the
+// keep bit of (query 128 qt + r, key 128 kt + 32 w + b). A row owner reads
+// one word per 32 keys (coalesced across rows); the key owners of a warp
+// take 32 consecutive words at once and transpose them.
 struct Dropout {
   uint32_t k0, k1;  // the 64-bit seed, low word first
   uint32_t offset;

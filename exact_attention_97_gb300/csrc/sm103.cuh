@@ -518,10 +518,55 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1
 // element (i, j) of head h (query i, key j) is kept iff byte j mod 4 of word
 // i mod 4 of philox4x32_10((j/4, i/4, head_base + h, offset), seed) is >= t.
 
-// Bits (>= t) of the four bytes of w, as a 4-bit value (byte b -> bit b).
-__device__ __forceinline__ uint32_t keep_nibble(uint32_t w, uint32_t t4) {
-  const uint32_t ge = __vcmpgeu4(w, t4);  // 0xFF in each byte that is >= t
-  return ((ge >> 7) & 1u) | ((ge >> 14) & 2u) | ((ge >> 21) & 4u) | ((ge >> 28) & 8u);
+// Bit order inside a 32-key keep word (rows drawn here, blocks saved for the
+// backward): key b of the word is bit keep_bit(b) = 8 (b mod 4) + b / 4, so
+// byte i holds keys i, 4 + i, ..., 28 + i. A 4 x 4 Philox group (keys
+// 4c .. 4c + 3) then fills bit c of every byte with one shift, and a left
+// shift of the word by 7 - c brings that group's bits to the top bits of the
+// four bytes, where prmt's sign replication turns them into byte masks.
+__host__ __device__ constexpr int keep_bit(int b) { return 8 * (b & 3) + (b >> 2); }
+
+// 32 x 32 bit-matrix transpose across a warp: lane r passes row r (bit c =
+// element (r, c)) and gets column `lane` back (bit r = element (r, lane)).
+// Stage s swaps the off-diagonal s x s blocks of every 2s x 2s block: each
+// lane sends its partner (lane ^ s) the half it gives up, already shifted
+// into place, and keeps the other half.
+__device__ __forceinline__ uint32_t warp_transpose_bits(uint32_t x) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int s = 16; s >= 1; s >>= 1) {
+    const uint32_t m = s == 16 ? 0x0000FFFFu : s == 8 ? 0x00FF00FFu : s == 4 ? 0x0F0F0F0Fu
+                                                     : s == 2 ? 0x33333333u : 0x55555555u;
+    const bool hi = lane & s;
+    const uint32_t recv = __shfl_xor_sync(0xffffffffu, hi ? x << s : x >> s, s);
+    const uint32_t keep = hi ? ~m : m;
+    x = (x & keep) | (recv & ~keep);
+  }
+  return x;
+}
+
+// Top bit of each byte of the result: byte of x >= t (the other bits are
+// zero). t7 = (t mod 128) replicated in the four bytes, HIGH: t >= 128.
+// In d = (x | 0x80) - (t mod 128) no byte borrows from the next, and the top
+// bit of a byte of d says whether the low seven bits of x reach those of t;
+// x >= t is then (top bit of x) or that bit when t < 128, and when t >= 128.
+template <bool HIGH>
+__device__ __forceinline__ uint32_t keep_top_bits(uint32_t x, uint32_t t7) {
+  const uint32_t d = (x | 0x80808080u) - t7;
+  return (HIGH ? (x & d) : (x | d)) & 0x80808080u;
+}
+// The same with t >= 128 given at run time: low_t = 0 if it is, ~0 if not.
+__device__ __forceinline__ uint32_t keep_top_bits(uint32_t x, uint32_t t7, uint32_t low_t) {
+  const uint32_t d = (x | 0x80808080u) - t7;
+  return ((x & d) | ((x | d) & low_t)) & 0x80808080u;
+}
+
+// 0xFF in byte n of the result where bit 7 of byte (nibble n of sel) & 7 of
+// x is set, else 0 (prmt with sign replication, every selector nibble >= 8).
+__device__ __forceinline__ uint32_t byte_signs(uint32_t x, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(x), "r"(0u), "r"(sel));
+  return r;
 }
 
 // The mask helpers below are warp-collective: the four lanes of a quad own
@@ -530,12 +575,13 @@ __device__ __forceinline__ uint32_t keep_nibble(uint32_t w, uint32_t t4) {
 // shuffle.
 
 // Keep bits of query row i (i mod 4 == lane mod 4) for the 32 * NW keys
-// starting at j0 (a multiple of 4): bit b of bits[w] is key j0 + 32 w + b.
+// starting at j0 (a multiple of 4): bit keep_bit(b) of bits[w] is key
+// j0 + 32 w + b.
 template <int NW>
 __device__ __forceinline__ void dropout_row_bits(const Dropout &dr, uint32_t h, int i, int j0, uint32_t (&bits)[NW]) {
-  const uint32_t t4 = dr.t * 0x01010101u;
+  const uint32_t t7 = (dr.t & 0x7Fu) * 0x01010101u, low_t = dr.t >= 128u ? 0u : ~0u;
   const int lane = threadIdx.x & 31, quad = lane & ~3, me = lane & 3;
-#pragma unroll(NW > 2 ? 1 : NW)  // the four-word (forward) case stays rolled: its body is long
+#pragma unroll(NW > 2 ? 1 : NW)  // the four-word case stays rolled: its body is long
   for (int w = 0; w < NW; ++w) {
     uint32_t m = 0;
 #pragma unroll
@@ -543,13 +589,13 @@ __device__ __forceinline__ void dropout_row_bits(const Dropout &dr, uint32_t h, 
       const uint4 r = philox4x32_10(make_uint4(static_cast<uint32_t>(j0 / 4 + 8 * w + 4 * blk + me),
                                                static_cast<uint32_t>(i / 4), dr.head_base + h, dr.offset),
                                     dr.k0, dr.k1);
-      // nibble r of `packed`: keep bits of row 4 (i/4) + r for this lane's 4 keys
-      const uint32_t packed = keep_nibble(r.x, t4) | (keep_nibble(r.y, t4) << 4) | (keep_nibble(r.z, t4) << 8) |
-                              (keep_nibble(r.w, t4) << 12);
+      // bit 8 b + q of `packed`: keep bit of row 4 (i/4) + q for key b of this lane's call
+      const uint32_t packed = (keep_top_bits(r.x, t7, low_t) >> 7) + (keep_top_bits(r.y, t7, low_t) >> 6) +
+                              (keep_top_bits(r.z, t7, low_t) >> 5) + (keep_top_bits(r.w, t7, low_t) >> 4);
 #pragma unroll
-      for (int src = 0; src < 4; ++src) {
+      for (int src = 0; src < 4; ++src) {  // call 4 blk + src of the word: bit 8 b + call
         const uint32_t v = __shfl_sync(0xffffffffu, packed, quad | src);
-        m |= ((v >> (4 * me)) & 0xFu) << (4 * (4 * blk + src));
+        m += ((v >> me) & 0x01010101u) << (4 * blk + src);
       }
     }
     bits[w] = m;
@@ -560,7 +606,7 @@ __device__ __forceinline__ void dropout_row_bits(const Dropout &dr, uint32_t h, 
 // starting at i0 (a multiple of 4): bit b of bits[w] is row i0 + 32 w + b.
 template <int NW>
 __device__ __forceinline__ void dropout_col_bits(const Dropout &dr, uint32_t h, int j, int i0, uint32_t (&bits)[NW]) {
-  const uint32_t t4 = dr.t * 0x01010101u;
+  const uint32_t t7 = (dr.t & 0x7Fu) * 0x01010101u, low_t = dr.t >= 128u ? 0u : ~0u;
   const int lane = threadIdx.x & 31, quad = lane & ~3, me = lane & 3;
 #pragma unroll(NW > 2 ? 1 : NW)  // the four-word (forward) case stays rolled: its body is long
   for (int w = 0; w < NW; ++w) {
@@ -572,14 +618,12 @@ __device__ __forceinline__ void dropout_col_bits(const Dropout &dr, uint32_t h, 
                                                dr.head_base + h, dr.offset),
                                     dr.k0, dr.k1);
       // nibble b of `packed`: keep bits of this call's 4 rows for key 4 (j/4) + b
-      const uint32_t g0 = __vcmpgeu4(r.x, t4), g1 = __vcmpgeu4(r.y, t4), g2 = __vcmpgeu4(r.z, t4),
-                     g3 = __vcmpgeu4(r.w, t4);
+      // (bit 8 b + 4 + q of s is row q)
+      const uint32_t s = (keep_top_bits(r.x, t7, low_t) >> 3) + (keep_top_bits(r.y, t7, low_t) >> 2) +
+                         (keep_top_bits(r.z, t7, low_t) >> 1) + keep_top_bits(r.w, t7, low_t);
       uint32_t packed = 0;
 #pragma unroll
-      for (int b = 0; b < 4; ++b)
-        packed |= (((g0 >> (8 * b + 7)) & 1u) | (((g1 >> (8 * b + 7)) & 1u) << 1) |
-                   (((g2 >> (8 * b + 7)) & 1u) << 2) | (((g3 >> (8 * b + 7)) & 1u) << 3))
-                  << (4 * b);
+      for (int b = 0; b < 4; ++b) packed |= ((s >> (8 * b + 4)) & 0xFu) << (4 * b);
 #pragma unroll
       for (int src = 0; src < 4; ++src) {
         const uint32_t v = __shfl_sync(0xffffffffu, packed, quad | src);
@@ -588,6 +632,26 @@ __device__ __forceinline__ void dropout_col_bits(const Dropout &dr, uint32_t h, 
     }
     bits[w] = m;
   }
+}
+
+// Keep bits of the 4 x 32 block of rows i0..i0+3 (i0 a multiple of 4) and
+// keys j0..j0+31 (j0 a multiple of 4), drawn by one thread with no exchange:
+// eight Philox calls, one per 4 x 4 group of the block. Component k of the
+// result is row i0 + k, bit keep_bit(b) key j0 + b. HIGH says t >= 128.
+template <bool HIGH>
+__device__ __forceinline__ uint4 dropout_block_bits(const Dropout &dr, uint32_t h, int i0, int j0) {
+  const uint32_t t7 = (dr.t & 0x7Fu) * 0x01010101u;
+  uint32_t acc[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const uint4 r = philox4x32_10(make_uint4(static_cast<uint32_t>(j0 / 4 + c), static_cast<uint32_t>(i0 / 4),
+                                             dr.head_base + h, dr.offset),
+                                  dr.k0, dr.k1);
+    const uint32_t x[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) acc[k] += keep_top_bits<HIGH>(x[k], t7) >> (7 - c);  // bit 8 b + c: key 4 c + b
+  }
+  return make_uint4(acc[0], acc[1], acc[2], acc[3]);
 }
 
 // Register rebalancing between warpgroups (all four warps of a warpgroup

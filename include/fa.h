@@ -194,10 +194,12 @@ int fa_bwd_dropout(const void *q, const void *k, const void *v, const void *o,
  *           call's own heads), query tile qt < ceil(Nq/128) and key tile
  *           kt < ceil(Nk/128), a 2048-byte block at byte offset
  *           ((bh * ceil(Nq/128) + qt) * ceil(Nk/128) + kt) * 2048 of 512
- *           32-bit words, word-major: bit b of word w * 128 + r = the keep
- *           bit of query 128 qt + r and key 128 kt + 32 w + b (the Philox
- *           mask of fa_fwd_dropout with the given seed, offset and
- *           head_base).
+ *           32-bit words, word-major: bit 8 (b mod 4) + floor(b / 4) of
+ *           word w * 128 + r (b = 0..31) = the keep bit of query 128 qt + r
+ *           and key 128 kt + 32 w + b (the Philox mask of fa_fwd_dropout
+ *           with the given seed, offset and head_base). Byte i of a word
+ *           thus holds keys i, i + 4, ..., i + 28 of its 32, one bit per
+ *           4-key Philox group.
  *           Blocks of tiles the causal mask hides entirely, and bits past Nq
  *           or Nk, are left unspecified.
  *   backward  takes the forward's p_drop and the mask it wrote (no seed:

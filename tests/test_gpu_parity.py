@@ -339,21 +339,25 @@ def test_dropout_kv_f16_and_d256():
 def _saved_bits(buf, B, H, Nq, Nk):
     """Unpack a saved-keep-bits buffer into a [B, H, Nq, Nk] bool array (its
     documented layout: per head, query tile and key tile a block of 512
-    words, bit b of word w * 128 + r = the bit of row r and key 32 w + b)."""
+    words, bit 8 (b mod 4) + b // 4 of word w * 128 + r = the bit of row r
+    and key 32 w + b)."""
     nqt, nkt = (Nq + 127) // 128, (Nk + 127) // 128
     words = buf.cpu().numpy()[: B * H * nqt * nkt * 2048].view(np.uint32).reshape(B * H, nqt, nkt, 4, 128)
     rows = np.ascontiguousarray(words.transpose(0, 1, 2, 4, 3)).view(np.uint8)  # [BH, qt, kt, row, 16 bytes]
-    bits = np.unpackbits(rows, axis=-1, bitorder="little")  # [BH, qt, kt, row, 128 keys]
+    bits = np.unpackbits(rows, axis=-1, bitorder="little")  # [BH, qt, kt, row, 4 words x 32 bit positions]
+    pos = np.array([8 * (b % 4) + b // 4 for b in range(32)])
+    bits = bits.reshape(*bits.shape[:-1], 4, 32)[..., pos].reshape(*bits.shape)  # bit positions -> keys
     bits = bits.transpose(0, 1, 3, 2, 4).reshape(B * H, nqt * 128, nkt * 128)[:, :Nq, :Nk]
     return bits.reshape(B, H, Nq, Nk).astype(bool)
 
 
-@pytest.mark.parametrize("Nq,Nk,causal", [(300, 513, False), (300, 513, True), (128, 128, False)])
-def test_dropout_saved_bits_are_the_oracle_mask(Nq, Nk, causal):
+@pytest.mark.parametrize("Nq,Nk,causal,p", [(300, 513, False, 0.3), (300, 513, True, 0.3), (128, 128, False, 0.3),
+                                            (300, 513, False, 0.7)])
+def test_dropout_saved_bits_are_the_oracle_mask(Nq, Nk, causal, p):
     """The forward's saved keep bits equal the oracle's Philox mask bit for
-    bit on every visible (query, key) pair."""
+    bit on every visible (query, key) pair (thresholds below and above 128)."""
     import exact_attention_97_gb300 as fa
-    seed, offset, p, B, H = 0xABCDEF0123, 9, 0.3, 1, 3
+    seed, offset, B, H = 0xABCDEF0123, 9, 1, 3
     q, _, _, _ = make_qkv_do(B, H, Nq, 64, seed=31, dtype=torch.bfloat16)
     _, k, v, _ = make_qkv_do(B, H, Nk, 64, seed=32, dtype=torch.bfloat16)
     dev = torch.device("cuda")
