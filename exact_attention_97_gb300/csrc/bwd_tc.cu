@@ -60,6 +60,7 @@ namespace {
 constexpr int kBlk = 128;       // keys per block and query rows per tile
 constexpr int kNoDrop = 0, kDrawn = 1, kSaved = 2;  // DROP: no dropout, keep bits drawn, keep bits saved
 constexpr int kThreads = 384;   // 12 warps
+constexpr int kThreadsMask = 512;  // dK/dV pass with drawn keep bits: warps 12-15 draw them
 constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ __forceinline__ void load_rows(uint8_t *dst, const CUtensorMap *map, uint64_t *bar,
@@ -146,7 +147,7 @@ struct DkdvCfg {
 };
 
 template <int D, bool F16, int DROP, bool PAIR>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(DROP == kDrawn ? kThreadsMask : kThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                     const __grid_constant__ CUtensorMap tmdK, const __grid_constant__ CUtensorMap tmdV,
@@ -167,8 +168,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_flag;
   __shared__ __align__(16) float Lst[NST][kBlk], Dst[NST][kBlk];  // per stage, by bulk copy
-  // with saved dropout bits: the stage's 2 KB block (128 query rows x 4 words)
-  __shared__ __align__(16) uint32_t Mst[DROP == kSaved ? NST : 1][DROP == kSaved ? kBlk * 4 : 4];
+  // with dropout: the stage's 2 KB block of keep bits (128 query rows x 4
+  // words), saved ones by bulk copy with the stage, drawn ones by the mask
+  // warps (mk_full: written, mk_empty: the elementwise warps have read it)
+  __shared__ __align__(16) uint32_t Mst[DROP != kNoDrop ? NST : 1][DROP != kNoDrop ? kBlk * 4 : 4];
+  __shared__ uint64_t mk_full[DROP == kDrawn ? NST : 1], mk_empty[DROP == kDrawn ? NST : 1];
 
   const int warp = warp_id(), lane = lane_id();
   const int n_tiles_all = (N + kBlk - 1) / kBlk;
@@ -206,6 +210,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&done, 2);  // dV and dK, from the two issuing threads
     mbar_init(&drain, 1);
     mbar_init(&drain_kv, 1);
+    if constexpr (DROP == kDrawn) {
+      for (int s = 0; s < NST; ++s) {
+        mbar_init(&mk_full[s], 4 * 32);
+        mbar_init(&mk_empty[s], 8 * 32);
+      }
+    }
     fence_mbar_init();
   }
   if (warp == 2) {
@@ -241,6 +251,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Every role walks the same items (key blocks); query tiles are counted
   // across items (g) for the ring and the per-tile barriers, items (it) for
   // the K, V and `done` barriers.
+  // With drawn keep bits the block has 512 threads at 128 registers, and each
+  // warpgroup resizes its share at the top of its branch: 56 for warps 0-3
+  // (one producer and two issuing lanes), 168 for the elementwise warps, 112
+  // for the mask warps (64512 of the 65536).
+  if (warp < 4) {
+  if constexpr (DROP == kDrawn) setmaxnreg_dec<56>();
   if (warp == 0) {
     // ---------------------------------------------------------------- producer
     // K of the next block loads as soon as the last S^T MMA of the current
@@ -469,7 +485,41 @@ __global__ void __launch_bounds__(kThreads, 1)
       else mma_commit(&drain_kv);
       mbar_wait_drain(&drain_kv, 0);
     }
+  }
+  } else if (DROP == kDrawn && warp >= 12) {
+    setmaxnreg_dec<112>();
+    // -------------------------------------------------------------- keep bits
+    // Warp 12 + c draws keys 32c..32c+31 of the block for query rows
+    // 4 lane..4 lane + 3 of every query tile, into the slot of that tile's
+    // Q/dO stage, in the layout of the saved keep bits.
+    auto draw = [&](auto high) {
+      constexpr bool kHigh = decltype(high)::value;
+      const int wc = warp - 12;
+      bool ok = true;
+      int g = 0, rank, bh;
+      for (int k = 0; ok; ++k) {
+        const int step = sched_item(sched, cta, k, rank, bh);
+        if (step == kDone) break;
+        if (step == kSkip) continue;
+        const int kb = block_of(rank);
+        const int i_first = first_tile(rank), n_tiles = n_tiles_all - i_first;
+        for (int t = 0; t < n_tiles; ++t, ++g) {
+          const int st = g % NST;
+          if (g >= NST && !mbar_wait_warp(&mk_empty[st], ((g / NST) & 1) ^ 1, &abort_flag)) {
+            ok = false;
+            break;
+          }
+          const uint4 bits = dropout_block_bits<kHigh>(drop, static_cast<uint32_t>(bh), (i_first + t) * kBlk + 4 * lane,
+                                                       kb * kBlk + 32 * wc);
+          *reinterpret_cast<uint4 *>(&Mst[st][wc * kBlk + 4 * lane]) = bits;
+          mbar_arrive(&mk_full[st]);
+        }
+      }
+    };
+    if (drop.t >= 128u) draw(std::true_type{});
+    else draw(std::false_type{});
   } else if (warp >= 4) {
+    if constexpr (DROP == kDrawn) setmaxnreg_inc<168>();
     // -------------------------------------------- P, dS (warpgroup h: queries 64h..64h+63)
     const int h = (warp >= 8) ? 1 : 0;
     const int wq = warp & 3;
@@ -492,15 +542,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int st = g % NST;
         const int q0 = (i_first + t) * kBlk + h * 64;  // first query of this warpgroup's columns
         const int qmin = (key >= Nk) ? (q0 + 64) : qmin0;
-        uint32_t keep[2];  // dropout: keep bits of this key for the 64 queries, drawn while S^T is in flight
-        if constexpr (DROP == kDrawn) dropout_col_bits<2>(drop, static_cast<uint32_t>(bh), key, q0, keep);
+        uint32_t keep[2];  // dropout: keep bits of this key for the 64 queries
         if (!mbar_wait_warp(PAIR ? &ld_full[st] : &qd_full[st], (g / NST) & 1, &abort_flag)) {
           ok = false;
           break;
         }
-        if constexpr (DROP == kSaved) {
-          // saved bits are stored by query row, 32 keys a word: the warp's
-          // keys are word wq of each row, and the words wq of the
+        if constexpr (DROP == kDrawn) {
+          if (!mbar_wait_warp(&mk_full[st], (g / NST) & 1, &abort_flag)) {
+            ok = false;
+            break;
+          }
+        }
+        if constexpr (DROP != kNoDrop) {
+          // the block's bits are stored by query row, 32 keys a word: the
+          // warp's keys are word wq of each row, and the words wq of the
           // warpgroup's 64 rows are consecutive. Lane r takes rows r and
           // 32 + r, a transpose gives lane c the bits of bit position c,
           // and the key of bit position keep_bit(lane) is this lane's.
@@ -508,6 +563,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int w = 0; w < 2; ++w)
             keep[w] = __shfl_sync(0xffffffffu, warp_transpose_bits(rows[32 * w + lane]), keep_bit(lane));
+          if constexpr (DROP == kDrawn) mbar_arrive(&mk_empty[st]);
         }
         const float4 *L4 = reinterpret_cast<const float4 *>(Lst[st] + h * 64);
         const float4 *D4 = reinterpret_cast<const float4 *>(Dst[st] + h * 64);
@@ -1241,7 +1297,7 @@ cudaError_t launch(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtenso
     auto kern = bwd_dkdv_kernel<D, F16, DROP, false>;
     cudaError_t r = set_smem_once(reinterpret_cast<const void *>(kern), DkdvCfg<D>::kAlloc, &smem_kv);
     if (r != cudaSuccess) return r;
-    kern<<<kv.sched.G, kThreads, DkdvCfg<D>::kAlloc, st>>>(tmQ, tmK, tmV, tmdO, tmdK, tmdV, tmQ, tmdO, Lp, Dp, N, Nk,
+    kern<<<kv.sched.G, DROP == kDrawn ? kThreadsMask : kThreads, DkdvCfg<D>::kAlloc, st>>>(tmQ, tmK, tmV, tmdO, tmdK, tmdV, tmQ, tmdO, Lp, Dp, N, Nk,
                                                            kv.sched, scale, scale_log2, causal, drop, status);
     timing_end(st);
     return cudaGetLastError();

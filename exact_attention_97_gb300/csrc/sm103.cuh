@@ -602,38 +602,6 @@ __device__ __forceinline__ void dropout_row_bits(const Dropout &dr, uint32_t h, 
   }
 }
 
-// Keep bits of key j (j mod 4 == lane mod 4) for the 32 * NW query rows
-// starting at i0 (a multiple of 4): bit b of bits[w] is row i0 + 32 w + b.
-template <int NW>
-__device__ __forceinline__ void dropout_col_bits(const Dropout &dr, uint32_t h, int j, int i0, uint32_t (&bits)[NW]) {
-  const uint32_t t7 = (dr.t & 0x7Fu) * 0x01010101u, low_t = dr.t >= 128u ? 0u : ~0u;
-  const int lane = threadIdx.x & 31, quad = lane & ~3, me = lane & 3;
-#pragma unroll(NW > 2 ? 1 : NW)  // the four-word (forward) case stays rolled: its body is long
-  for (int w = 0; w < NW; ++w) {
-    uint32_t m = 0;
-#pragma unroll
-    for (int blk = 0; blk < 2; ++blk) {  // 16 rows: 4 calls, one per lane of the quad
-      const uint4 r = philox4x32_10(make_uint4(static_cast<uint32_t>(j / 4),
-                                               static_cast<uint32_t>(i0 / 4 + 8 * w + 4 * blk + me),
-                                               dr.head_base + h, dr.offset),
-                                    dr.k0, dr.k1);
-      // nibble b of `packed`: keep bits of this call's 4 rows for key 4 (j/4) + b
-      // (bit 8 b + 4 + q of s is row q)
-      const uint32_t s = (keep_top_bits(r.x, t7, low_t) >> 3) + (keep_top_bits(r.y, t7, low_t) >> 2) +
-                         (keep_top_bits(r.z, t7, low_t) >> 1) + keep_top_bits(r.w, t7, low_t);
-      uint32_t packed = 0;
-#pragma unroll
-      for (int b = 0; b < 4; ++b) packed |= ((s >> (8 * b + 4)) & 0xFu) << (4 * b);
-#pragma unroll
-      for (int src = 0; src < 4; ++src) {
-        const uint32_t v = __shfl_sync(0xffffffffu, packed, quad | src);
-        m |= ((v >> (4 * me)) & 0xFu) << (4 * (4 * blk + src));
-      }
-    }
-    bits[w] = m;
-  }
-}
-
 // Keep bits of the 4 x 32 block of rows i0..i0+3 (i0 a multiple of 4) and
 // keys j0..j0+31 (j0 a multiple of 4), drawn by one thread with no exchange:
 // eight Philox calls, one per 4 x 4 group of the block. Component k of the
