@@ -730,11 +730,13 @@ __global__ void __launch_bounds__(DROP == kDrawn ? kThreadsMask : kThreads, 1)
 // for dQ += dS K all 128 keys of head columns 64r..64r+63 (MN-major, one
 // 16 KB sub-tile) -- a K stage holds both, 32 KB -- and for dP = dO V^T the
 // value rows 64r..64r+63 (16 KB).
-template <int D, bool PAIR = false>
+// DRAWN (dropout with drawn keep bits): at 128 columns the K ring is one
+// stage shorter, which leaves room for the mask warps' ring of keep bits.
+template <int D, bool PAIR = false, bool DRAWN = false>
 struct DqCfg {
   static_assert(!PAIR || D == 128, "the pair kernel covers d = 128");
   static constexpr int kDP = (D + 63) / 64 * 64;  // whole 64-column TMA boxes per row
-  static constexpr int kKStages = (kDP == 128) ? 3 : 4;
+  static constexpr int kKStages = (kDP == 128) ? (DRAWN ? 2 : 3) : 4;
   static constexpr int kVStages = PAIR ? 3 : ((kDP == 128) ? 2 : 3);
   static constexpr int kTileBytes = kBlk * kDP * 2;
   static constexpr int kSubBytes = kBlk * 128;
@@ -752,7 +754,7 @@ struct DqCfg {
 };
 
 template <int D, bool F16, int DROP, bool PAIR>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(DROP == kDrawn ? kThreadsMask : kThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                   const __grid_constant__ CUtensorMap tmKh, const __grid_constant__ CUtensorMap tmVh,
@@ -760,9 +762,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                   uint16_t *__restrict__ dq, int N, int Nk, const __grid_constant__ TileSched sched, float scale,
                   float scale_log2, int causal, const Dropout drop, int *status) {
   static_assert(!(PAIR && DROP), "the pair kernel has no dropout");
-  using C = DqCfg<D, PAIR>;
+  using C = DqCfg<D, PAIR, DROP == kDrawn>;
   using E = Elt<F16>;
   constexpr int KS = C::kKStages, VS = C::kVStages;
+  // drawn keep bits: a ring of (query tile, key block) blocks from the mask
+  // warps, in the layout of the saved bits (mk_full: written, mk_empty: read)
+  constexpr int kMSlots = 4;
+  __shared__ __align__(16) uint32_t Mst[DROP == kDrawn ? kMSlots : 1][DROP == kDrawn ? kBlk * 4 : 4];
+  __shared__ uint64_t mk_full[DROP == kDrawn ? kMSlots : 1], mk_empty[DROP == kDrawn ? kMSlots : 1];
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
@@ -815,6 +822,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&done, 1);
     mbar_init(&drain, 1);
     mbar_init(&drain_q, 1);
+    if constexpr (DROP == kDrawn) {
+      for (int s = 0; s < kMSlots; ++s) {
+        mbar_init(&mk_full[s], 4 * 32);
+        mbar_init(&mk_empty[s], 8 * 32);
+      }
+    }
     fence_mbar_init();
   }
   if (warp == 2) {
@@ -850,6 +863,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Every role walks the same items (query tiles); key blocks are counted
   // across items (g) for the K/V rings, the S buffers and the per-block
   // barriers, items (it) for the Q, dO and `done` barriers.
+  // With drawn keep bits the block has 512 threads at 128 registers, split as
+  // in the dK/dV pass: 56 for warps 0-3, 168 for the elementwise warps, 112 for
+  // the mask warps.
+  if (warp < 4) {
+  if constexpr (DROP == kDrawn) setmaxnreg_dec<56>();
   if (warp == 0) {
     // ------------------------------------------------------- loader: Q, dO, K
     // Q of the next tile loads once the last S MMA of the current one has
@@ -1072,7 +1090,39 @@ __global__ void __launch_bounds__(kThreads, 1)
       else mma_commit(&drain_q);
       mbar_wait_drain(&drain_q, 0);
     }
+  }
+  } else if (DROP == kDrawn && warp >= 12) {
+    setmaxnreg_dec<112>();
+    // -------------------------------------------------------------- keep bits
+    // Warp 12 + c draws keys 32c..32c+31 of every key block for rows
+    // 4 lane..4 lane + 3 of the query tile, into ring slot g mod kMSlots.
+    auto draw = [&](auto high) {
+      constexpr bool kHigh = decltype(high)::value;
+      const int wc = warp - 12;
+      bool ok = true;
+      int g = 0, rank, bh;
+      for (int k = 0; ok; ++k) {
+        const int step = sched_item(sched, cta, k, rank, bh);
+        if (step == kDone) break;
+        if (step == kSkip) continue;
+        const int qt = qtile_of(rank), n_kb = kblocks(rank);
+        for (int j = 0; j < n_kb; ++j, ++g) {
+          const int m = g % kMSlots;
+          if (g >= kMSlots && !mbar_wait_warp(&mk_empty[m], ((g / kMSlots) & 1) ^ 1, &abort_flag)) {
+            ok = false;
+            break;
+          }
+          const uint4 bits = dropout_block_bits<kHigh>(drop, static_cast<uint32_t>(bh), qt * kBlk + 4 * lane,
+                                                       j * kBlk + 32 * wc);
+          *reinterpret_cast<uint4 *>(&Mst[m][wc * kBlk + 4 * lane]) = bits;
+          mbar_arrive(&mk_full[m]);
+        }
+      }
+    };
+    if (drop.t >= 128u) draw(std::true_type{});
+    else draw(std::false_type{});
   } else if (warp >= 4) {
+    if constexpr (DROP == kDrawn) setmaxnreg_inc<168>();
     // ------------------------------------------ P, dS (warpgroup h: keys 64h..64h+63 of a block)
     const int h = (warp >= 8) ? 1 : 0;
     const int wq = warp & 3;
@@ -1111,14 +1161,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < n_kb; ++j, ++g) {
         const uint32_t sb = C::tS + (g & 1) * 128 + h * 64;
         const int limit = kvis - (j * kBlk + h * 64);  // columns at or past limit are masked
-        uint32_t keep[2];  // dropout: keep bits of this row for the 64 keys, drawn while S is in flight
+        uint32_t keep[2];  // dropout: keep bits of this row for the 64 keys, read while S is in flight
         // (bit keep_bit(b) of keep[w]: key j * 128 + 64 h + 32 w + b)
         if constexpr (DROP == kSaved) {  // saved by the forward: words 2h, 2h + 1 of this row in block (qt, j)
           const uint32_t *blk = drop.mask + dropout_block(drop, bh, qt, j) / 4 + r;
           keep[0] = __ldg(blk + (2 * h) * kBlk);
           keep[1] = __ldg(blk + (2 * h + 1) * kBlk);
-        } else if constexpr (DROP == kDrawn) {
-          dropout_row_bits<2>(drop, static_cast<uint32_t>(bh), q, j * kBlk + h * 64, keep);
+        } else if constexpr (DROP == kDrawn) {  // from the mask warps: the same words of ring slot g mod kMSlots
+          const int m = g % kMSlots;
+          if (!mbar_wait_warp(&mk_full[m], (g / kMSlots) & 1, &abort_flag)) { ok = false; break; }
+          keep[0] = Mst[m][(2 * h) * kBlk + r];
+          keep[1] = Mst[m][(2 * h + 1) * kBlk + r];
+          mbar_arrive(&mk_empty[m]);
         }
         if (!mbar_wait_warp(&s_full[g & 1], (g >> 1) & 1, &abort_flag)) { ok = false; break; }
         tc_fence_after();
@@ -1316,9 +1370,10 @@ cudaError_t launch(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtenso
     }
     static SmemOnce smem_q;
     auto kern = bwd_dq_kernel<D, F16, DROP, false>;
-    cudaError_t r = set_smem_once(reinterpret_cast<const void *>(kern), DqCfg<D>::kAlloc, &smem_q);
+    using CQ = DqCfg<D, false, DROP == kDrawn>;
+    cudaError_t r = set_smem_once(reinterpret_cast<const void *>(kern), CQ::kAlloc, &smem_q);
     if (r != cudaSuccess) return r;
-    kern<<<q.sched.G, kThreads, DqCfg<D>::kAlloc, st>>>(tmQ, tmK, tmV, tmdO, tmK, tmV, Lp, Dp,
+    kern<<<q.sched.G, DROP == kDrawn ? kThreadsMask : kThreads, CQ::kAlloc, st>>>(tmQ, tmK, tmV, tmdO, tmK, tmV, Lp, Dp,
                                                         static_cast<uint16_t *>(dq), N, Nk, q.sched, scale,
                                                         scale_log2, causal, drop, status);
     timing_end(st);

@@ -518,8 +518,8 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1
 // element (i, j) of head h (query i, key j) is kept iff byte j mod 4 of word
 // i mod 4 of philox4x32_10((j/4, i/4, head_base + h, offset), seed) is >= t.
 
-// Bit order inside a 32-key keep word (rows drawn here, blocks saved for the
-// backward): key b of the word is bit keep_bit(b) = 8 (b mod 4) + b / 4, so
+// Bit order inside a 32-key keep word (in the shared keep-bit rings and in the
+// saved buffer): key b of the word is bit keep_bit(b) = 8 (b mod 4) + b / 4, so
 // byte i holds keys i, 4 + i, ..., 28 + i. A 4 x 4 Philox group (keys
 // 4c .. 4c + 3) then fills bit c of every byte with one shift, and a left
 // shift of the word by 7 - c brings that group's bits to the top bits of the
@@ -555,11 +555,6 @@ __device__ __forceinline__ uint32_t keep_top_bits(uint32_t x, uint32_t t7) {
   const uint32_t d = (x | 0x80808080u) - t7;
   return (HIGH ? (x & d) : (x | d)) & 0x80808080u;
 }
-// The same with t >= 128 given at run time: low_t = 0 if it is, ~0 if not.
-__device__ __forceinline__ uint32_t keep_top_bits(uint32_t x, uint32_t t7, uint32_t low_t) {
-  const uint32_t d = (x | 0x80808080u) - t7;
-  return ((x & d) | ((x | d) & low_t)) & 0x80808080u;
-}
 
 // 0xFF in byte n of the result where bit 7 of byte (nibble n of sel) & 7 of
 // x is set, else 0 (prmt with sign replication, every selector nibble >= 8).
@@ -567,39 +562,6 @@ __device__ __forceinline__ uint32_t byte_signs(uint32_t x, uint32_t sel) {
   uint32_t r;
   asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(x), "r"(0u), "r"(sel));
   return r;
-}
-
-// The mask helpers below are warp-collective: the four lanes of a quad own
-// four consecutive rows (or keys) that share every Philox counter, so each
-// lane draws a quarter of the calls and the quad swaps 4-bit keep nibbles by
-// shuffle.
-
-// Keep bits of query row i (i mod 4 == lane mod 4) for the 32 * NW keys
-// starting at j0 (a multiple of 4): bit keep_bit(b) of bits[w] is key
-// j0 + 32 w + b.
-template <int NW>
-__device__ __forceinline__ void dropout_row_bits(const Dropout &dr, uint32_t h, int i, int j0, uint32_t (&bits)[NW]) {
-  const uint32_t t7 = (dr.t & 0x7Fu) * 0x01010101u, low_t = dr.t >= 128u ? 0u : ~0u;
-  const int lane = threadIdx.x & 31, quad = lane & ~3, me = lane & 3;
-#pragma unroll(NW > 2 ? 1 : NW)  // the four-word case stays rolled: its body is long
-  for (int w = 0; w < NW; ++w) {
-    uint32_t m = 0;
-#pragma unroll
-    for (int blk = 0; blk < 2; ++blk) {  // 16 keys: 4 calls, one per lane of the quad
-      const uint4 r = philox4x32_10(make_uint4(static_cast<uint32_t>(j0 / 4 + 8 * w + 4 * blk + me),
-                                               static_cast<uint32_t>(i / 4), dr.head_base + h, dr.offset),
-                                    dr.k0, dr.k1);
-      // bit 8 b + q of `packed`: keep bit of row 4 (i/4) + q for key b of this lane's call
-      const uint32_t packed = (keep_top_bits(r.x, t7, low_t) >> 7) + (keep_top_bits(r.y, t7, low_t) >> 6) +
-                              (keep_top_bits(r.z, t7, low_t) >> 5) + (keep_top_bits(r.w, t7, low_t) >> 4);
-#pragma unroll
-      for (int src = 0; src < 4; ++src) {  // call 4 blk + src of the word: bit 8 b + call
-        const uint32_t v = __shfl_sync(0xffffffffu, packed, quad | src);
-        m += ((v >> me) & 0x01010101u) << (4 * blk + src);
-      }
-    }
-    bits[w] = m;
-  }
 }
 
 // Keep bits of the 4 x 32 block of rows i0..i0+3 (i0 a multiple of 4) and
