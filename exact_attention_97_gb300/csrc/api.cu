@@ -366,6 +366,7 @@ const char *fa_status_string(int status) {
     case FA_ERR_TIMEOUT: return "a kernel gave up waiting on a pipeline barrier";
     case FA_ERR_ARCH: return "current device is not sm_103";
     case FA_ERR_ARG: return "invalid argument";
+    case FA_ERR_CHECK: return "a device-side check of the checked build failed";
     default: return "unknown status";
   }
 }

@@ -717,6 +717,7 @@ __global__ void __launch_bounds__(DROP == kDrawn ? kThreadsMask : kThreads, 1)
     else tmem_dealloc(tmem, 512);
   }
   if (threadIdx.x == 0 && abort_flag) atomicExch(status, kErrTimeout);
+  report_checks(status);
 }
 
 // ------------------------------------------------------------------ kernel 3
@@ -1253,6 +1254,7 @@ __global__ void __launch_bounds__(DROP == kDrawn ? kThreadsMask : kThreads, 1)
     else tmem_dealloc(tmem, 512);
   }
   if (threadIdx.x == 0 && abort_flag) atomicExch(status, kErrTimeout);
+  report_checks(status);
 }
 
 template <int D, bool F16, int DROP>

@@ -635,6 +635,7 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
     else tmem_dealloc(tmem, 512);
   }
   if (threadIdx.x == 0 && abort_flag) atomicExch(status, kErrTimeout);
+  report_checks(status);
 }
 
 template <int D, bool F16, bool DROP>

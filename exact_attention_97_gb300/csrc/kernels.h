@@ -49,7 +49,8 @@ enum : int {
   kErrLaunch = 6,
   kErrTimeout = 7,
   kErrArch = 8,
-  kErrArg = 9
+  kErrArg = 9,
+  kErrCheck = 10  // only with FA_CHECKED: a device-side argument check failed
 };
 
 // Benchmark timing hook: records the next free event pair (if any) around a

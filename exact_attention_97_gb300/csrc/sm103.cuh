@@ -12,6 +12,7 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include "checks.h"
 #include "kernels.h"
 
 #ifndef FA_WAIT_LIMIT_CYCLES
@@ -19,6 +20,56 @@
 #endif
 
 namespace fa {
+
+// Checked build (FA_CHECKED): the TMA, bulk-copy and TMEM wrappers below test
+// their arguments against the rules of their instruction first. A failed test
+// sets a bit in this translation unit's check word and skips the instruction
+// (nothing traps); every kernel copies a non-zero word into the status word
+// (kErrCheck) at its end. Without FA_CHECKED the tests compile to nothing.
+// The rules are the predicates of checks.h.
+enum : uint32_t { kCheckTmaLoad = 1, kCheckTmaStore = 2, kCheckBulk = 4, kCheckTmem = 8 };
+#ifdef FA_CHECKED
+static __device__ uint32_t g_check_word;
+#define FA_CHECK(cond, bit)              \
+  do {                                   \
+    if (!(cond)) {                       \
+      atomicOr(&::fa::g_check_word, (bit)); \
+      return;                            \
+    }                                    \
+  } while (0)
+// For loads into a register array: the skipped load leaves zeros, so that
+// the registers' earlier values need not stay live across the test.
+#define FA_CHECK_LD(cond, bit, r, n)         \
+  do {                                       \
+    if (!(cond)) {                           \
+      atomicOr(&::fa::g_check_word, (bit)); \
+      _Pragma("unroll") for (int i_ = 0; i_ < (n); ++i_) r[i_] = 0u; \
+      return;                                \
+    }                                        \
+  } while (0)
+#else
+#define FA_CHECK(cond, bit) \
+  do {                      \
+  } while (0)
+#define FA_CHECK_LD(cond, bit, r, n) \
+  do {                               \
+  } while (0)
+#endif
+
+// The end of every kernel (after its closing barrier): a tripped check becomes
+// the caller-visible status.
+__device__ __forceinline__ void report_checks(int *status) {
+#ifdef FA_CHECKED
+  if (threadIdx.x == 0 && *reinterpret_cast<volatile uint32_t *>(&g_check_word) != 0u) atomicExch(status, kErrCheck);
+#else
+  (void)status;
+#endif
+}
+
+// A 32x32b TMEM access of `cols` columns at taddr by the calling warp.
+__device__ __forceinline__ bool tmem_access_ok(uint32_t taddr, uint32_t cols) {
+  return tmem_ok(taddr, cols, threadIdx.x >> 5);
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -132,6 +183,7 @@ __device__ __forceinline__ void mbar_arrive_cl(uint32_t cl_addr) {
 // a barrier of either CTA of the pair (shared::cluster address).
 __device__ __forceinline__ void tma_load_3d_pair(void *dst, const CUtensorMap *map, uint32_t bar_cl, int x, int y,
                                                  int z) {
+  FA_CHECK(tma_load_ok(x, smem_u32(dst)), kCheckTmaLoad);
   asm volatile(
       "cp.async.bulk.tensor.3d.shared::cta.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
       " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
@@ -201,6 +253,7 @@ __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map) {
 // 3-D tiled load global -> shared, completion counted in bytes on `bar`.
 __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, uint64_t *bar,
                                             int x, int y, int z) {
+  FA_CHECK(tma_load_ok(x, smem_u32(dst)), kCheckTmaLoad);
   asm volatile(
       "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
@@ -211,6 +264,7 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, u
 // 3-D tiled store shared -> global, tracked as a bulk group of the issuing
 // thread. Box elements outside the tensor are not written.
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, const void *src, int x, int y, int z) {
+  FA_CHECK(tma_store_ok(x, y, z, smem_u32(src)), kCheckTmaStore);
   asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
                    reinterpret_cast<uint64_t>(map)),
                "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
@@ -229,6 +283,7 @@ __device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap *map, int x
 // 1-D bulk copy global -> shared (16-byte aligned addresses, size a multiple
 // of 16), completion counted in bytes on `bar`.
 __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+  FA_CHECK(bulk_ok(smem_u32(dst), reinterpret_cast<uintptr_t>(src), bytes), kCheckBulk);
   asm volatile(
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
           smem_u32(dst)),
@@ -279,6 +334,7 @@ __device__ __forceinline__ void tc_fence_after() {
 // 32 lanes x 32 consecutive columns of 32 bits: lane i of the warp receives
 // row (lane base + i), columns [col, col+32). Waits for completion.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  FA_CHECK_LD(tmem_access_ok(taddr, 32), kCheckTmem, r, 32);
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
       "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
@@ -296,6 +352,7 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
 
 // 16 columns per lane; waits for completion.
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  FA_CHECK_LD(tmem_access_ok(taddr, 16), kCheckTmem, r, 16);
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
       "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
@@ -309,6 +366,7 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
 
 // Store 32 columns (32 x 32 bit per lane) and wait for completion.
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  FA_CHECK(tmem_access_ok(taddr, 32), kCheckTmem);
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
       "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
@@ -324,6 +382,7 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 
 // 64 consecutive columns per lane in one instruction; waits for completion.
 __device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
+  FA_CHECK_LD(tmem_access_ok(taddr, 64), kCheckTmem, r, 64);
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];\n\t"
       "tcgen05.wait::ld.sync.aligned;"
@@ -334,6 +393,7 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
 
 // 128 consecutive columns per lane in one instruction; waits for completion.
 __device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t (&r)[128]) {
+  FA_CHECK_LD(tmem_access_ok(taddr, 128), kCheckTmem, r, 128);
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x128.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63,%64,%65,%66,%67,%68,%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79,%80,%81,%82,%83,%84,%85,%86,%87,%88,%89,%90,%91,%92,%93,%94,%95,%96,%97,%98,%99,%100,%101,%102,%103,%104,%105,%106,%107,%108,%109,%110,%111,%112,%113,%114,%115,%116,%117,%118,%119,%120,%121,%122,%123,%124,%125,%126,%127}, [%128];\n\t"
       "tcgen05.wait::ld.sync.aligned;"
@@ -344,6 +404,7 @@ __device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t (&r)[128]) {
 
 // Store 64 consecutive columns per lane in one instruction and wait.
 __device__ __forceinline__ void tmem_st64(uint32_t taddr, const uint32_t (&r)[64]) {
+  FA_CHECK(tmem_access_ok(taddr, 64), kCheckTmem);
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x64.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63,%64};\n\t"
       "tcgen05.wait::st.sync.aligned;" ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31]), "r"(r[32]), "r"(r[33]), "r"(r[34]), "r"(r[35]), "r"(r[36]), "r"(r[37]), "r"(r[38]), "r"(r[39]), "r"(r[40]), "r"(r[41]), "r"(r[42]), "r"(r[43]), "r"(r[44]), "r"(r[45]), "r"(r[46]), "r"(r[47]), "r"(r[48]), "r"(r[49]), "r"(r[50]), "r"(r[51]), "r"(r[52]), "r"(r[53]), "r"(r[54]), "r"(r[55]), "r"(r[56]), "r"(r[57]), "r"(r[58]), "r"(r[59]), "r"(r[60]), "r"(r[61]), "r"(r[62]), "r"(r[63])

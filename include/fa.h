@@ -73,7 +73,11 @@ typedef enum {
   FA_ERR_LAUNCH = 6,      /* a CUDA launch or tensor-map call failed */
   FA_ERR_TIMEOUT = 7,     /* a kernel gave up waiting on a pipeline barrier */
   FA_ERR_ARCH = 8,        /* current device is not sm_103 */
-  FA_ERR_ARG = 9          /* other invalid argument (non-finite scale, dtype) */
+  FA_ERR_ARG = 9,         /* other invalid argument (non-finite scale, dtype) */
+  FA_ERR_CHECK = 10       /* only in a library built with FA_CHECKED: a kernel's
+                             own check rejected a TMA coordinate or address, a
+                             bulk-copy address or size, or a TMEM address, and
+                             skipped that access; the results are not valid */
 } fa_status;
 
 typedef enum { FA_BF16 = 0, FA_F32 = 1, FA_F16 = 2 } fa_dtype;
