@@ -199,7 +199,7 @@ def test_d128_several_items_per_cta(B, H, Nq, Nk, causal):
 
 # ------------------------------------------------------------ host-resident training step
 
-@pytest.mark.parametrize("case", ["bf16_causal", "f16_kv", "dropout", "one_chunk"])
+@pytest.mark.parametrize("case", ["bf16_causal", "f16_kv", "dropout", "one_chunk", "sizes"])
 def test_host_step_equals_device_path(case):
     """attention_step_host streams chunks of heads through the GPU on three
     streams; its results must equal the device-side calls bit for bit."""
@@ -209,7 +209,7 @@ def test_host_step_equals_device_path(case):
     q, _, _, dO = make_qkv_do(2, 5, 300, 128, seed=77, dtype=dt)
     _, k, v, _ = make_qkv_do(2, 5, Nk, 128, seed=78, dtype=dt)
     kw = {"dropout_p": 0.2, "seed": 5, "offset": 1} if case == "dropout" else {}
-    chunks = 1 if case == "one_chunk" else 4
+    chunks = {"one_chunk": 1, "sizes": [1, 3, 4, 2]}.get(case, 4)
     pin = [t.pin_memory() for t in (q, k, v, dO)]
     res = fa.attention_step_host(*pin, None, True, chunks=chunks, **kw)
     torch.cuda.current_stream().synchronize()
