@@ -28,7 +28,7 @@ __all__ = [
     "fa_bwd_workspace_size", "fa_status_string", "fa_device_status", "fa_last_launch_count",
     "fa_set_kernel_timing", "fa_status_async", "fa_status_word", "fa_dropout_mask_size", "fa_fwd_dropout_mask",
     "fa_bwd_dropout_mask", "dropout_mask_buffer",
-    "attention_forward", "attention_backward", "attention_step_host", "lib_path", "load",
+    "attention_forward", "attention_backward", "attention", "attention_step_host", "lib_path", "load",
 ]
 
 
@@ -219,6 +219,58 @@ def attention_backward(q, k, v, o, lse, dO, scale=None, causal=False, workspace=
         if check:
             _check_status("attention_backward", stream)
     return dq, dk, dv
+
+
+class _Attention:
+    """torch.autograd.Function over attention_forward / attention_backward,
+    built on first use (the module imports torch lazily)."""
+    fn = None
+
+    @classmethod
+    def get(cls):
+        if cls.fn is None:
+            torch = _torch()
+
+            class AttentionFn(torch.autograd.Function):
+                @staticmethod
+                def forward(ctx, q, k, v, scale, causal, dropout_p, seed, offset, head_base, save_mask):
+                    mask = None
+                    if dropout_p and save_mask:
+                        B, H, Nq, _ = q.shape
+                        mask = dropout_mask_buffer(B, H, Nq, k.shape[2], q.device)
+                    o, lse = attention_forward(q, k, v, scale, causal, dropout_p=dropout_p, seed=seed, offset=offset,
+                                               head_base=head_base, dropout_mask=mask)
+                    ctx.save_for_backward(q, k, v, o, lse)
+                    ctx.args = (scale, causal, dropout_p, seed, offset, head_base, mask)
+                    ctx.mark_non_differentiable(lse)
+                    return o, lse
+
+                @staticmethod
+                def backward(ctx, dO, _dlse):
+                    q, k, v, o, lse = ctx.saved_tensors
+                    scale, causal, dropout_p, seed, offset, head_base, mask = ctx.args
+                    dq, dk, dv = attention_backward(q, k, v, o, lse, dO.contiguous(), scale, causal,
+                                                    dropout_p=dropout_p, seed=seed, offset=offset,
+                                                    head_base=head_base, dropout_mask=mask)
+                    return dq, dk, dv, None, None, None, None, None, None, None
+
+            cls.fn = AttentionFn
+        return cls.fn
+
+
+def attention(q, k, v, scale=None, causal=False, dropout_p=0.0, seed=0, offset=0, head_base=0,
+              save_dropout_mask=False, return_lse=False):
+    """O for CUDA tensors q [B, H, Nq, d] and k, v [B, H, Nk, d], differentiable
+    in q, k and v through torch.autograd: the forward runs attention_forward
+    and keeps O and L, the backward runs attention_backward on the incoming
+    dO (made contiguous if it is not). Same dtypes, shapes and dropout
+    arguments as attention_forward; save_dropout_mask=True keeps the
+    forward's keep bits (one bit per query-key pair) for the backward instead
+    of drawing them again. return_lse=True also returns L (no gradient)."""
+    scale = 1.0 / math.sqrt(q.shape[-1]) if scale is None else float(scale)
+    o, lse = _Attention.get().apply(q, k, v, scale, bool(causal), float(dropout_p), int(seed), int(offset),
+                                    int(head_base), bool(save_dropout_mask))
+    return (o, lse) if return_lse else o
 
 
 from .pipeline import attention_step_host  # noqa: E402  (uses the functions above)

@@ -222,6 +222,37 @@ def test_host_step_equals_device_path(case):
         assert torch.equal(a, b.cpu())
 
 
+@pytest.mark.parametrize("case", ["bf16_causal", "f16_kv", "dropout_saved", "f32"])
+def test_autograd_attention_equals_the_direct_calls(case):
+    """fa.attention through torch.autograd: O and the gradients that
+    .backward() produces equal attention_forward / attention_backward on the
+    same dO, bit for bit (same kernels, same arguments). The fp32 backward
+    sums dK and dV with atomic adds, whose order varies from run to run, so
+    its gradients are compared to 1e-5 of their largest magnitude."""
+    import exact_attention_97_gb300 as fa
+    dt = {"f16_kv": torch.float16, "f32": torch.float32}.get(case, torch.bfloat16)
+    Nk = 700 if case == "f16_kv" else 300
+    d = 64 if case == "f32" else 128
+    q, _, _, dO = make_qkv_do(2, 3, 300, d, seed=91, dtype=dt)
+    _, k, v, _ = make_qkv_do(2, 3, Nk, d, seed=92, dtype=dt)
+    q, k, v, dO = (t.cuda() for t in (q, k, v, dO))
+    kw = dict(dropout_p=0.2, seed=9, offset=1) if case == "dropout_saved" else {}
+    qa, ka, va = (t.clone().requires_grad_() for t in (q, k, v))
+    o, lse = fa.attention(qa, ka, va, None, True, save_dropout_mask=case == "dropout_saved", return_lse=True, **kw)
+    assert not lse.requires_grad
+    o.backward(dO)
+    o2, lse2 = fa.attention_forward(q, k, v, None, True, **kw)
+    g2 = fa.attention_backward(q, k, v, o2, lse2, dO, None, True, **kw)
+    torch.cuda.synchronize()
+    assert fa.fa_device_status() == 0
+    assert torch.equal(o.detach(), o2) and torch.equal(lse, lse2)
+    for a, b in zip((qa.grad, ka.grad, va.grad), g2):
+        if case == "f32":
+            assert float((a - b).abs().max()) <= 1e-5 * float(b.abs().max())
+        else:
+            assert torch.equal(a, b)
+
+
 # ------------------------------------------------------------ dropout
 
 def _drop_ref(q, k, v, dO, scale, causal, seed, offset, p):
