@@ -27,9 +27,9 @@
 //                  S = Q K^T (double-buffered), dP = dO V^T   (TMEM)
 //                  dQ += dS K     (dS read from TMEM in 16 bits)
 // In both passes two warpgroups split the 128 columns of S and dP (64 each)
-// for the elementwise work and one warp loads. Two threads issue the MMAs,
-// so that the barrier waits of either leave the tensor pipe fed by the
-// other: in the dK/dV pass one per chain of products that reuse TMEM columns
+// for the elementwise work, one warp loads (two in the dQ pass), and two
+// threads issue the MMAs, so that the barrier waits of either leave the
+// tensor pipe fed by the other: in the dK/dV pass one per chain of products that reuse TMEM columns
 // (S^T and dV; dP^T and dK), in the dQ pass one for S and dP and one for dQ,
 // where S_{j+2} waits for dQ_j to complete before overwriting dS_j. Both
 // passes are persistent: at most one CTA per SM walks a static list of items
@@ -39,10 +39,11 @@
 // per-warp shared-memory boxes and TMA stores, the dQ pass with whole-line
 // row-segment stores. Head sizes 64, 96 and 128.
 // With dropout both passes take the keep bits of each tile before its scores
-// arrive: DROP = kDrawn instances draw them (Philox4x32-10, sm103.cuh),
-// DROP = kSaved instances read the ones the forward saved (separate
-// instances, so that each is compiled for its own path). dV takes
-// P o Z / (1 - p), and dP is scaled by Z / (1 - p) before dS.
+// arrive: in DROP = kDrawn instances four more warps draw them
+// (Philox4x32-10, sm103.cuh) into shared slots, DROP = kSaved instances read
+// the ones the forward saved (separate instances, so that each is compiled
+// for its own path). dV takes P o Z / (1 - p), and dP is scaled by
+// Z / (1 - p) before dS.
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
