@@ -60,6 +60,16 @@ constexpr int kBlockN = 128;   // keys per tile
 constexpr int kThreads = 256;      // 8 warps
 constexpr int kMaskWarps = 4;  // with dropout, warps 8-11 draw the keep masks (32 keys of each tile each)
 constexpr int kThreadsDrop = 256 + 32 * kMaskWarps;
+// The one-CTA forward without dropout: warps 8-11 write each item's O and L
+// (the epilogue warps), so the softmax warps start the next item at once.
+template <bool DROP, bool PAIR>
+__host__ __device__ constexpr bool fwd_epi_warps() {
+  return !DROP && !PAIR;
+}
+template <bool DROP, bool PAIR>
+__host__ __device__ constexpr int fwd_threads() {
+  return DROP ? kThreadsDrop : (fwd_epi_warps<DROP, PAIR>() ? 384 : kThreads);
+}
 constexpr int kMaskSlots = 3;      // keep-mask ring (128 rows x 128 keys of bits each)
 constexpr int kMaskSlotBytes = 128 * 128 / 8;
 template <bool B>
@@ -126,7 +136,7 @@ __device__ __forceinline__ void load_cols(uint8_t *dst, const CUtensorMap *map, 
 }
 
 template <int D, bool F16, bool DROP, bool PAIR>
-__global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
+__global__ void __launch_bounds__(fwd_threads<DROP, PAIR>(), 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ,
                     const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, uint16_t *__restrict__ o,
@@ -144,6 +154,12 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
       mask_full[DROP ? kMaskSlots : 1], mask_empty[DROP ? kMaskSlots : 1];
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_flag;
+  // epilogue warps: each row's sum l and max m of the item just finished
+  // (stat_full: written by the softmax warps, stat_empty: read), and o_free:
+  // O has been read out of TMEM, so the next item's first P V may overwrite it
+  constexpr bool EPI = fwd_epi_warps<DROP, PAIR>();
+  __shared__ float st_l[EPI ? kBlockM : 1], st_m[EPI ? kBlockM : 1];
+  __shared__ uint64_t stat_full, stat_empty, o_free;
 
   const int warp = warp_id(), lane = lane_id();
   // A schedule unit is a query tile, or with PAIR a tile pair (2u, 2u + 1)
@@ -186,6 +202,11 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
     }
     mbar_init(&drain_s, 1);
     mbar_init(&drain_pv, 1);
+    if constexpr (EPI) {
+      mbar_init(&stat_full, 4 * 32);
+      mbar_init(&stat_empty, 4 * 32);
+      mbar_init(&o_free, 4 * 32);
+    }
     if constexpr (DROP) {
       for (int b = 0; b < kMaskSlots; ++b) {
         mbar_init(&mask_full[b], kMaskWarps * 32);
@@ -375,8 +396,9 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
     // ---------------------------------------------------- MMA issuer: O += P V
     // A second issuing thread, so the tensor pipe always has one of the two
     // streams queued while the other waits on its barriers. The first P V of
-    // an item overwrites O: its P is only marked ready after the softmax warps
-    // have read the previous item's O out of TMEM.
+    // an item overwrites O: with epilogue warps it waits for them to have read
+    // the previous item's O out of TMEM (o_free); otherwise its P is only
+    // marked ready after the softmax warps have done so.
     if (lane == 0 && (!PAIR || crank == 0)) {
       constexpr uint32_t idesc_o = idesc_16(PAIR ? 2 * kBlockM : kBlockM, L::kPVN, false, true, F16);
       auto commit = [](uint64_t *bar) {
@@ -384,13 +406,17 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
         else mma_commit(bar);
       };
       bool ok = true;
-      int kt = 0, vu = 0;
+      int kt = 0, vu = 0, it = 0;
       int rank, bh;
       for (int k = 0; ok; ++k) {
         const int step = sched_item(sched, cta, k, rank, bh);
         if (step == kDone) break;
         if (step == kSkip) continue;
         const int nk = ktiles(rank);
+        if constexpr (EPI) {
+          if (it > 0 && !mbar_wait(&o_free, (it - 1) & 1, &abort_flag)) break;
+        }
+        ++it;
         for (int j = 0; j < nk; ++j, ++kt) {
           const int sb = kt % kSBuf;
           if (!mbar_wait(&p_ready[sb], (kt / kSBuf) & 1, &abort_flag)) { ok = false; break; }
@@ -424,7 +450,7 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
     const int r_local = wq * 32 + lane;      // row within the tile
     const uint32_t lane_addr = static_cast<uint32_t>(wq * 32) << 16;
     bool ok = true;
-    int kt = 0;
+    int kt = 0, it = 0;
     int rank, bh;
     for (int k = 0; ok; ++k) {
       const int step = sched_item(sched, cta, k, rank, bh);
@@ -549,18 +575,67 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
         }
       }
       // -------------------------------------------------------------- epilogue
-      // the item's last P V (and, issued in order before it, every other
-      // one) is done; the next item's first P V waits for this warp's next
-      // p_ready arrival, which comes after these TMEM reads
-      if (!ok || !mbar_wait_warp(&pv_done[(kt - 1) % kSBuf], ((kt - 1) / kSBuf) & 1, &abort_flag)) {
+      if constexpr (EPI) {
+        // this row's l and m go to the epilogue warps; the next item starts now
+        if (!ok) break;
+        if (it > 0 && !mbar_wait_warp(&stat_empty, (it - 1) & 1, &abort_flag)) {
+          ok = false;
+          break;
+        }
+        st_l[r_local] = l_sum;
+        st_m[r_local] = m_used;
+        mbar_arrive(&stat_full);
+        ++it;
+      } else {
+        // the item's last P V (and, issued in order before it, every other
+        // one) is done; the next item's first P V waits for this warp's next
+        // p_ready arrival, which comes after these TMEM reads
+        if (!ok || !mbar_wait_warp(&pv_done[(kt - 1) % kSBuf], ((kt - 1) / kSBuf) & 1, &abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const float inv_l = DROP ? drop.inv_keep / l_sum : 1.f / l_sum;
+        // O = accumulator / l, whole-line row-segment stores
+        store_tmem_rows<E, D>(tmem_O + lane_addr, inv_l, o + (static_cast<size_t>(bh) * N + row) * D, D, N - row);
+        if (row < N) lse[static_cast<size_t>(bh) * N + row] = (m_used * scale_log2 + log2f(l_sum)) * kLn2;
+      }
+    }
+  };
+  auto role_epilogue = [&]() {
+    // ------------------------------------------------------- O and L (EPI)
+    // Warp 8 + q writes rows 32q..32q+31 of each item once its last P V is
+    // done, from the l and m the softmax warps handed over, then frees O for
+    // the next item's first P V. That wait cannot meet a later phase of the
+    // buffer: the next use of it is a P V of the next item, issued after o_free.
+    const int wq = warp & 3;
+    const int r_local = wq * 32 + lane;
+    const uint32_t lane_addr = static_cast<uint32_t>(wq * 32) << 16;
+    bool ok = true;
+    int kt = 0, it = 0, rank, bh;
+    for (int k = 0; ok; ++k) {
+      const int step = sched_item(sched, cta, k, rank, bh);
+      if (step == kDone) break;
+      if (step == kSkip) continue;
+      const int row = qtile_of(rank) * kBlockM + r_local;
+      kt += ktiles(rank);
+      if (!mbar_wait_warp(&stat_full, it & 1, &abort_flag)) {
+        ok = false;
+        break;
+      }
+      const float l_sum = st_l[r_local], m_used = st_m[r_local];
+      mbar_arrive(&stat_empty);
+      if (!mbar_wait_warp(&pv_done[(kt - 1) % kSBuf], ((kt - 1) / kSBuf) & 1, &abort_flag)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const float inv_l = DROP ? drop.inv_keep / l_sum : 1.f / l_sum;
       // O = accumulator / l, whole-line row-segment stores
-      store_tmem_rows<E, D>(tmem_O + lane_addr, inv_l, o + (static_cast<size_t>(bh) * N + row) * D, D, N - row);
+      store_tmem_rows<E, D>(tmem_O + lane_addr, 1.f / l_sum, o + (static_cast<size_t>(bh) * N + row) * D, D, N - row);
       if (row < N) lse[static_cast<size_t>(bh) * N + row] = (m_used * scale_log2 + log2f(l_sum)) * kLn2;
+      tc_fence_before();
+      mbar_arrive(&o_free);
+      ++it;
     }
   };
   auto role_masks = [&](auto high) {
@@ -615,6 +690,22 @@ __global__ void __launch_bounds__(DROP ? kThreadsDrop : kThreads, 1)
       setmaxnreg_dec<96>();
       if (drop.t >= 128) role_masks(BoolTag<true>{});
       else role_masks(BoolTag<false>{});
+    }
+  } else if constexpr (EPI) {
+    // 384 x 168 registers, resized as with dropout: loaders and issuers 56,
+    // softmax 232, epilogue warps 96 (49152 of the 64512)
+    if (warp < 4) {
+      setmaxnreg_dec<56>();
+      if (warp == 0) role_k_loader();
+      else if (warp == 2) role_v_loader();
+      else if (warp == 1) role_s_issuer();
+      else role_pv_issuer();
+    } else if (warp < 8) {
+      setmaxnreg_inc<232>();
+      role_softmax();
+    } else {
+      setmaxnreg_dec<96>();
+      role_epilogue();
     }
   } else {
     if (warp == 0) role_k_loader();
@@ -686,7 +777,7 @@ cudaError_t launch(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtenso
     return static_cast<long long>(ktiles_q(nt - 1 - rank)) + 1;
   });
   timing_begin(stream);
-  kern<<<sched.G, DROP ? kThreadsDrop : kThreads, L::kAlloc, stream>>>(tmQ, tmK, tmV, static_cast<uint16_t *>(o), lse,
+  kern<<<sched.G, fwd_threads<DROP, false>(), L::kAlloc, stream>>>(tmQ, tmK, tmV, static_cast<uint16_t *>(o), lse,
                                                   N, Nk, sched, scale, scale_log2, causal, drop, status);
   timing_end(stream);
   return cudaGetLastError();
