@@ -31,13 +31,18 @@
 //               pairs over the S columns, and keeps l. The running max is only
 //               moved when it grows by more than 2^8: any common base leaves
 //               u/l unchanged (tutorial section 02), so the O rescale in TMEM
-//               (ld, multiply, st) is skipped on most tiles. The epilogue
-//               divides by l and stores O with whole-line row-segment stores
-//               (store_tmem_rows, sm103.cuh), then L = m*scale + ln l.
-//   warps 8-11  (dropout instances only) draw each tile's keep bits
-//               (Philox4x32-10, sm103.cuh) into a shared ring one tile ahead;
-//               the softmax warps scale the kept P by 1 / (1 - p) for P V
-//               and keep the undropped l.
+//               (ld, multiply, st) is skipped on most tiles. At the end of
+//               a tile the epilogue divides by l and stores O with
+//               whole-line row-segment stores (store_tmem_rows, sm103.cuh),
+//               then L = m*scale + ln l.
+//   warps 8-11  without dropout (one-CTA kernels): the epilogue warps. The
+//               softmax warps hand l and m over in shared memory and start
+//               the next tile; these write O and L once its last P V is done,
+//               and free O for the next tile's first P V.
+//               With dropout: draw each tile's keep bits (Philox4x32-10,
+//               sm103.cuh) into a shared ring one tile ahead; the softmax
+//               warps then zero the dropped P for P V, keep the undropped l
+//               and write the epilogue themselves (1 / (1 - p) folded in).
 //
 // Head sizes 64, 96 and 128 use one K/V unit per key tile; 256 uses two
 // (FwdSmem). TMEM columns: score buffers of 128 columns, then O.
