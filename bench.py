@@ -38,8 +38,8 @@ METRIC_FWD = "attention forward TFLOP/s (forward-only run of the workload in con
 # with the number of heads). Only valid for the kernel source it was measured
 # on: reported as null once that file changes.
 MEASURED_TRAFFIC = {"workload": "bf16_B8_H32_N4096_d128", "kernel": "bwd_dkdv_kernel<128>",
-                    "bytes": 4 * (271.330816e6 + 103.760640e6),
-                    "source": "exact_attention_97_gb300/csrc/bwd_tc.cu", "sha256_16": "b1e7a3c3c5794708"}
+                    "bytes": 4 * (270.785280e6 + 103.033600e6),
+                    "source": "exact_attention_97_gb300/csrc/bwd_tc.cu", "sha256_16": "ada841523632de83"}
 
 
 def _measured_traffic(kernel: str, workload: str):
