@@ -38,8 +38,8 @@ METRIC_FWD = "attention forward TFLOP/s (forward-only run of the workload in con
 # with the number of heads). Only valid for the kernel source it was measured
 # on: reported as null once that file changes.
 MEASURED_TRAFFIC = {"workload": "bf16_B8_H32_N4096_d128", "kernel": "bwd_dkdv_kernel<128>",
-                    "bytes": 4 * (270.785280e6 + 103.033600e6),
-                    "source": "exact_attention_97_gb300/csrc/bwd_tc.cu", "sha256_16": "ada841523632de83"}
+                    "bytes": 4 * (270.915072e6 + 103.886592e6),
+                    "source": "exact_attention_97_gb300/csrc/bwd_tc.cu", "sha256_16": "567d2c49096803e5"}
 
 
 def _measured_traffic(kernel: str, workload: str):
@@ -268,6 +268,8 @@ def run_ours(args, w):
     lse = torch.empty((w.B, w.H, w.N), device=dev, dtype=torch.float32)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     need = fa.fa_bwd_workspace_size(w.B, w.H, w.N, w.d, fa.FA_BF16)
+    if args.dropout and not args.dropout_saved:  # room for the keep bits the dK/dV pass hands to the dQ pass
+        need = fa.fa_bwd_dropout_workspace_size(w.B, w.H, w.N, w.n_keys, w.d, fa.FA_BF16)
     ws = torch.empty(need, device=dev, dtype=torch.uint8)
     stream = torch.cuda.current_stream()
 

@@ -17,8 +17,9 @@ import math
 
 import threading
 
-from ._lib import (FA_BF16, FA_F16, FA_F32, FAError, fa_bwd, fa_bwd_dropout, fa_bwd_dropout_mask, fa_bwd_f16,
-                   fa_bwd_f32, fa_bwd_kv, fa_bwd_workspace_size, fa_device_status, fa_dropout_mask_size, fa_fwd,
+from ._lib import (FA_BF16, FA_F16, FA_F32, FAError, fa_bwd, fa_bwd_dropout, fa_bwd_dropout_mask,
+                   fa_bwd_dropout_workspace_size, fa_bwd_f16, fa_bwd_f32, fa_bwd_kv, fa_bwd_workspace_size,
+                   fa_device_status, fa_dropout_mask_size, fa_fwd,
                    fa_fwd_dropout, fa_fwd_dropout_mask, fa_fwd_f16, fa_fwd_f32, fa_fwd_kv, fa_last_launch_count,
                    fa_set_kernel_timing, fa_status_async, fa_status_string, fa_status_word, lib_path, load)
 
@@ -27,7 +28,7 @@ __all__ = [
     "fa_fwd_f32", "fa_bwd_f32", "fa_fwd_kv", "fa_bwd_kv", "fa_fwd_dropout", "fa_bwd_dropout",
     "fa_bwd_workspace_size", "fa_status_string", "fa_device_status", "fa_last_launch_count",
     "fa_set_kernel_timing", "fa_status_async", "fa_status_word", "fa_dropout_mask_size", "fa_fwd_dropout_mask",
-    "fa_bwd_dropout_mask", "dropout_mask_buffer",
+    "fa_bwd_dropout_mask", "fa_bwd_dropout_workspace_size", "dropout_mask_buffer",
     "attention_forward", "attention_backward", "attention", "attention_step_host", "lib_path", "load",
 ]
 
@@ -176,7 +177,13 @@ def attention_backward(q, k, v, o, lse, dO, scale=None, causal=False, workspace=
                        grads=None, dropout_p=0.0, seed=0, offset=0, head_base=0, check=False, dropout_mask=None):
     """(dQ, dK, dV) for upstream gradient dO, given the forward's O and L (and
     the forward's dropout_p, seed and offset, or dropout_p and the
-    dropout_mask the forward saved). check=True as for attention_forward."""
+    dropout_mask the forward saved). check=True as for attention_forward.
+
+    With dropout and no saved mask, a workspace allocated here has room for
+    the keep bits (fa_bwd_dropout_workspace_size: one bit per (query, key)
+    pair), so the dQ pass reads the bits the dK/dV pass draws instead of
+    drawing them again; a caller's workspace of only fa_bwd_workspace_size
+    bytes makes both passes draw them (same results)."""
     torch = _torch()
     B, H, N, d = q.shape
     Nk = k.shape[2]
@@ -192,7 +199,9 @@ def attention_backward(q, k, v, o, lse, dO, scale=None, causal=False, workspace=
     with _device_of(q):
         dev = q.get_device()
         if workspace is None:
-            workspace = torch.empty(need, device=q.device, dtype=torch.uint8)
+            shared_bits = dropout_p and dropout_mask is None and kind != FA_F32
+            size = fa_bwd_dropout_workspace_size(B, H, N, Nk, d, kind) if shared_bits else 0
+            workspace = torch.empty(size or need, device=q.device, dtype=torch.uint8)
         if workspace.numel() * workspace.element_size() < need:
             raise ValueError(f"workspace needs {need} bytes")
         dq, dk, dv = grads if grads is not None else (torch.empty_like(q), torch.empty_like(k),

@@ -29,6 +29,7 @@ _SIGNATURES = {
                                                                ctypes.c_uint, ctypes.c_uint, c_void_p, c_size_t,
                                                                c_void_p]),
     "fa_dropout_mask_size": (c_size_t, [c_int] * 4),
+    "fa_bwd_dropout_workspace_size": (c_size_t, [c_int] * 6),
     "fa_fwd_dropout_mask": (c_int, [c_void_p] * 5 + [c_int] * 5 + [c_float, c_int, c_int, c_float,
                                                                     ctypes.c_ulonglong, ctypes.c_uint, ctypes.c_uint,
                                                                     c_void_p, c_size_t, c_void_p]),
@@ -135,6 +136,10 @@ def fa_bwd_dropout(q, k, v, o, lse, dO, dq, dk, dv, B, H, Nq, Nk, d, scale, caus
 
 def fa_dropout_mask_size(B, H, Nq, Nk) -> int:
     return int(load().fa_dropout_mask_size(B, H, Nq, Nk))
+
+
+def fa_bwd_dropout_workspace_size(B, H, Nq, Nk, d, dtype) -> int:
+    return int(load().fa_bwd_dropout_workspace_size(B, H, Nq, Nk, d, dtype))
 
 
 def fa_fwd_dropout_mask(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, dtype, p_drop, seed, offset, head_base,

@@ -559,6 +559,7 @@ static int make_dropout(float p, unsigned long long seed, unsigned int offset, u
   dr->inv_keep = static_cast<float>(256.0 / (256.0 - t));
   dr->mask = nullptr;
   dr->n_qt = dr->n_kt = 0;
+  dr->dkdv_writes_mask = 0;
   return FA_OK;
 }
 
@@ -584,6 +585,23 @@ static int attach_mask(Dropout *dr, const void *mask, size_t mask_bytes, int B, 
 }
 
 size_t fa_dropout_mask_size(int B, int H, int Nq, int Nk) { return mask_bytes_for(B, H, Nq, Nk); }
+
+// fa_bwd_dropout's workspace with room for the keep bits its dK/dV pass hands
+// to its dQ pass: the plain workspace (a multiple of 256 bytes), then the
+// saved-bits layout at *bits_at. 0 for a shape or dtype the call rejects.
+static size_t bwd_dropout_ws_bytes(int B, int H, int Nq, int Nk, int d, int dtype, size_t *bits_at) {
+  if (dtype != FA_BF16 && dtype != FA_F16) return 0;
+  if (d != 64 && d != 96 && d != 128) return 0;
+  const size_t base = ws_bytes(B, H, Nq, d, FA_BF16);
+  const size_t bits = mask_bytes_for(B, H, Nq, Nk);
+  if (base == 0 || bits == 0) return 0;
+  if (bits_at) *bits_at = round_up(base, 256);
+  return round_up(base, 256) + bits;
+}
+
+size_t fa_bwd_dropout_workspace_size(int B, int H, int Nq, int Nk, int d, int dtype) {
+  return bwd_dropout_ws_bytes(B, H, Nq, Nk, d, dtype, nullptr);
+}
 
 int fa_fwd_dropout_mask(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int Nq,
                         int Nk, int d, float scale, int causal, int dtype, float p_drop, unsigned long long seed,
@@ -628,6 +646,15 @@ int fa_bwd_dropout(const void *q, const void *k, const void *v, const void *o, c
   Dropout dr;
   const int st = make_dropout(p_drop, seed, offset, head_base, &dr);
   if (st != FA_OK) return st;
+  // room for the keep bits: the dK/dV pass writes what it draws, the dQ pass reads it
+  size_t bits_at = 0;
+  const size_t with_bits = bwd_dropout_ws_bytes(B, H, Nq, Nk, d, dtype, &bits_at);
+  if (with_bits != 0 && workspace && aligned(workspace, 256) && workspace_bytes >= with_bits) {
+    dr.mask = reinterpret_cast<uint32_t *>(static_cast<char *>(workspace) + bits_at);
+    dr.n_qt = (Nq + 127) / 128;
+    dr.n_kt = (Nk + 127) / 128;
+    dr.dkdv_writes_mask = 1;
+  }
   return bwd16(q, k, v, o, lse, dO, dq, dk, dv, B, H, Nq, Nk, d, scale, causal, workspace, workspace_bytes,
                stream, dtype == FA_F16, &dr);
 }

@@ -42,7 +42,8 @@
 // arrive: in DROP = kDrawn instances four more warps draw them
 // (Philox4x32-10, sm103.cuh) into shared slots, DROP = kSaved instances read
 // the ones the forward saved (separate instances, so that each is compiled
-// for its own path). dV takes P o Z / (1 - p), and dP is scaled by
+// for its own path). Given room in the workspace, the drawn dK/dV pass also
+// writes its bits there in the saved layout, and a kSaved dQ pass reads them. dV takes P o Z / (1 - p), and dP is scaled by
 // Z / (1 - p) before dS.
 #include <cuda_runtime.h>
 #include <math.h>
@@ -492,7 +493,8 @@ __global__ void __launch_bounds__(DROP == kDrawn ? kThreadsMask : kThreads, 1)
     // -------------------------------------------------------------- keep bits
     // Warp 12 + c draws keys 32c..32c+31 of the block for query rows
     // 4 lane..4 lane + 3 of every query tile, into the slot of that tile's
-    // Q/dO stage, in the layout of the saved keep bits.
+    // Q/dO stage, in the layout of the saved keep bits; given drop.mask, it
+    // also writes them there for the dQ pass.
     auto draw = [&](auto high) {
       constexpr bool kHigh = decltype(high)::value;
       const int wc = warp - 12;
@@ -514,6 +516,9 @@ __global__ void __launch_bounds__(DROP == kDrawn ? kThreadsMask : kThreads, 1)
                                                        kb * kBlk + 32 * wc);
           *reinterpret_cast<uint4 *>(&Mst[st][wc * kBlk + 4 * lane]) = bits;
           mbar_arrive(&mk_full[st]);
+          if (drop.mask)  // for the dQ pass, in the saved layout
+            *reinterpret_cast<uint4 *>(drop.mask + dropout_block(drop, bh, i_first + t, kb) / 4 + wc * kBlk + 4 * lane) =
+                bits;
         }
       }
     };
@@ -1258,7 +1263,10 @@ __global__ void __launch_bounds__(DROP == kDrawn ? kThreadsMask : kThreads, 1)
   report_checks(status);
 }
 
-template <int D, bool F16, int DROP>
+// DROP is the dK/dV pass's dropout mode, DROPQ the dQ pass's: they differ
+// (kDrawn, kSaved) when the dK/dV pass writes the bits it draws to
+// drop.mask for the dQ pass to read.
+template <int D, bool F16, int DROP, int DROPQ>
 cudaError_t launch(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtensorMap &tmV,
                    const CUtensorMap &tmdO, const CUtensorMap &tmdK, const CUtensorMap &tmdV, const HalfMaps *half,
                    const void *o, const void *dO, const float *lse, void *dq, void *dk, void *dv, float *Lp,
@@ -1372,22 +1380,23 @@ cudaError_t launch(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtenso
       }
     }
     static SmemOnce smem_q;
-    auto kern = bwd_dq_kernel<D, F16, DROP, false>;
-    using CQ = DqCfg<D, false, DROP == kDrawn>;
+    auto kern = bwd_dq_kernel<D, F16, DROPQ, false>;
+    using CQ = DqCfg<D, false, DROPQ == kDrawn>;
     cudaError_t r = set_smem_once(reinterpret_cast<const void *>(kern), CQ::kAlloc, &smem_q);
     if (r != cudaSuccess) return r;
-    kern<<<q.sched.G, DROP == kDrawn ? kThreadsMask : kThreads, CQ::kAlloc, st>>>(tmQ, tmK, tmV, tmdO, tmK, tmV, Lp, Dp,
+    kern<<<q.sched.G, DROPQ == kDrawn ? kThreadsMask : kThreads, CQ::kAlloc, st>>>(tmQ, tmK, tmV, tmdO, tmK, tmV, Lp, Dp,
                                                         static_cast<uint16_t *>(dq), N, Nk, q.sched, scale,
                                                         scale_log2, causal, drop, status);
     timing_end(st);
     return cudaGetLastError();
   };
 
-  // Both passes only read what the row-term kernel and the forward wrote, so
-  // when their grids fit on the GPU together (small problems, where each
-  // leaves SMs idle) the dQ pass runs on the side stream alongside the dK/dV
-  // pass; otherwise one after the other (each persistent grid fills the GPU).
-  if (side.stream && kv.ctas + q.ctas <= num_sms) {
+  // Both passes only read what the row-term kernel and the forward wrote
+  // (unless the dK/dV pass hands the keep bits on), so when their grids fit
+  // on the GPU together (small problems, where each leaves SMs idle) the dQ
+  // pass runs on the side stream alongside the dK/dV pass; otherwise one
+  // after the other (each persistent grid fills the GPU).
+  if (DROP == DROPQ && side.stream && kv.ctas + q.ctas <= num_sms) {
     if ((e = cudaEventRecord(side.fork, stream)) != cudaSuccess ||
         (e = cudaStreamWaitEvent(side.stream, side.fork, 0)) != cudaSuccess)
       return e;
@@ -1400,14 +1409,14 @@ cudaError_t launch(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtenso
   return run_q(stream);
 }
 
-template <int DROP>
+template <int DROP, int DROPQ>
 cudaError_t dispatch(const CUtensorMap &tmQ, const CUtensorMap &tmK, const CUtensorMap &tmV,
                      const CUtensorMap &tmdO, const CUtensorMap &tmdK, const CUtensorMap &tmdV, const HalfMaps *half,
                      const void *o, const void *dO, const float *lse, void *dq, void *dk, void *dv, float *Lp,
                      float *Dp, int B, int H, int N, int Nk, int d, float scale, int causal, bool f16,
                      const Dropout &drop, int *status, int num_sms, cudaStream_t stream, const BwdSide &side) {
 #define FA_BWD_LAUNCH(DD, FF)                                                                                  \
-  return launch<DD, FF, DROP>(tmQ, tmK, tmV, tmdO, tmdK, tmdV, half, o, dO, lse, dq, dk, dv, Lp, Dp, B, H, N,  \
+  return launch<DD, FF, DROP, DROPQ>(tmQ, tmK, tmV, tmdO, tmdK, tmdV, half, o, dO, lse, dq, dk, dv, Lp, Dp, B, H, N,  \
                               Nk, scale, causal, drop, status, num_sms, stream, side)
   if (f16) {
     if (d == 64) FA_BWD_LAUNCH(64, true);
@@ -1429,14 +1438,14 @@ cudaError_t launch_bwd_16(const CUtensorMap &tmQ, const CUtensorMap &tmK, const 
                           bool f16, const Dropout *drop, int *status, int num_sms, cudaStream_t stream,
                           const BwdSide &side, int *launches) {
   *launches += 3;
-  if (drop && drop->mask)
-    return dispatch<kSaved>(tmQ, tmK, tmV, tmdO, tmdK, tmdV, half, o, dO, lse, dq, dk, dv, Lp, Dp, B, H, N, Nk, d,
-                            scale, causal, f16, *drop, status, num_sms, stream, side);
-  if (drop)
-    return dispatch<kDrawn>(tmQ, tmK, tmV, tmdO, tmdK, tmdV, half, o, dO, lse, dq, dk, dv, Lp, Dp, B, H, N, Nk, d,
-                          scale, causal, f16, *drop, status, num_sms, stream, side);
-  return dispatch<kNoDrop>(tmQ, tmK, tmV, tmdO, tmdK, tmdV, half, o, dO, lse, dq, dk, dv, Lp, Dp, B, H, N, Nk, d,
-                         scale, causal, f16, Dropout{}, status, num_sms, stream, side);
+#define FA_BWD_DISPATCH(M, MQ, DR)                                                                              \
+  return dispatch<M, MQ>(tmQ, tmK, tmV, tmdO, tmdK, tmdV, half, o, dO, lse, dq, dk, dv, Lp, Dp, B, H, N, Nk, d, \
+                         scale, causal, f16, DR, status, num_sms, stream, side)
+  if (drop && drop->mask && drop->dkdv_writes_mask) FA_BWD_DISPATCH(kDrawn, kSaved, *drop);
+  if (drop && drop->mask) FA_BWD_DISPATCH(kSaved, kSaved, *drop);
+  if (drop) FA_BWD_DISPATCH(kDrawn, kDrawn, *drop);
+  FA_BWD_DISPATCH(kNoDrop, kNoDrop, Dropout{});
+#undef FA_BWD_DISPATCH
 }
 
 }  // namespace fa

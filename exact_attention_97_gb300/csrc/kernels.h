@@ -31,6 +31,9 @@ struct Dropout {
   float inv_keep;
   uint32_t *mask;   // saved keep bits, or nullptr (draw them)
   int n_qt, n_kt;   // query and key tiles per head of the saved layout
+  // backward only: the dK/dV pass draws the bits and writes them to `mask`,
+  // and the dQ pass reads them there (0: both passes read `mask` if given)
+  int dkdv_writes_mask;
 };
 
 // Byte offset of the saved keep bits of tile (qt, kt) of head bh.

@@ -14,7 +14,7 @@ from __future__ import annotations
 
 import math
 
-from ._lib import FA_BF16, FA_F16, fa_bwd_workspace_size
+from ._lib import FA_BF16, FA_F16, fa_bwd_dropout_workspace_size, fa_bwd_workspace_size
 
 
 def _torch():
@@ -103,7 +103,9 @@ def attention_step_host(q, k, v, dO, scale=None, causal=False, chunks=None, out=
 
     dev = torch.device("cuda", torch.cuda.current_device())
     kind = FA_F16 if dt == torch.float16 else FA_BF16
-    ws_bytes = fa_bwd_workspace_size(1, hmax, Nq, d, kind)
+    # with dropout, room for the keep bits the dK/dV pass hands to the dQ pass
+    ws_bytes = (fa_bwd_dropout_workspace_size(1, hmax, Nq, Nk, d, kind) if dropout_p
+                else fa_bwd_workspace_size(1, hmax, Nq, d, kind))
 
     def make_buffers():
         return {"in": [torch.empty((hmax, r, d), dtype=dt, device=dev) for r in (Nq, Nk, Nk, Nq)],

@@ -154,6 +154,21 @@ def test_f32_argument_errors(lib):
     assert lib.fa_bwd_f32(*ptrs, 1, 1, 4, 2, 1.0, 0, None, 0, None) == 5
 
 
+def test_dropout_workspace_size():
+    """The shared-bits workspace is the plain one followed by the saved-bits
+    layout; shapes and types the dropout backward rejects give 0."""
+    for B, H, Nq, Nk, d in [(1, 1, 1, 1, 64), (2, 3, 300, 513, 96), (8, 32, 4096, 4096, 128), (64, 32, 128, 8192, 128)]:
+        for kind in (fa.FA_BF16, fa.FA_F16):
+            want = fa.fa_bwd_workspace_size(B, H, Nq, d, kind) + fa.fa_dropout_mask_size(B, H, Nq, Nk)
+            assert fa.fa_bwd_dropout_workspace_size(B, H, Nq, Nk, d, kind) == want
+    assert fa.fa_bwd_workspace_size(2, 3, 300, 96, fa.FA_BF16) % 256 == 0  # the bits start 256-byte aligned
+    assert fa.fa_bwd_dropout_workspace_size(1, 1, 128, 128, 64, fa.FA_F32) == 0
+    assert fa.fa_bwd_dropout_workspace_size(1, 1, 128, 128, 256, fa.FA_BF16) == 0
+    assert fa.fa_bwd_dropout_workspace_size(1, 1, 128, 128, 80, fa.FA_BF16) == 0
+    assert fa.fa_bwd_dropout_workspace_size(0, 1, 128, 128, 64, fa.FA_BF16) == 0
+    assert fa.fa_bwd_dropout_workspace_size(1, 1, 128, 0, 64, fa.FA_BF16) == 0
+
+
 def test_dropout_mask_size_and_argument_errors(lib):
     assert fa.fa_dropout_mask_size(8, 32, 4096, 4096) == 8 * 32 * 32 * 32 * 2048
     assert fa.fa_dropout_mask_size(1, 2, 300, 129) == 2 * 3 * 2 * 2048

@@ -9,7 +9,8 @@ and makes the kernel end with status FA_ERR_CHECK; nothing traps.
 
 These tests build the checked library in a temporary directory and
   * run every kernel family (head sizes 64, 96, 128 and 256, f16, ragged and
-    causal tiles, Nq != Nk, dropout with drawn and saved bits) through it and
+    causal tiles, Nq != Nk, dropout with drawn bits, saved bits and bits the
+    dK/dV pass hands to the dQ pass) through it and
     through the default library on the same inputs: no check may fire, and
     the results must be bit for bit those of the default build;
   * show the reporting path with a test kernel whose rejected call stands in
@@ -61,7 +62,7 @@ def _run(lib, q, k, v, dO, causal, kind, mode, p):
     mask = None
     if mode == "plain":
         st = lib.fa_fwd_kv(*ptrs, B, H, Nq, Nk, d, ctypes.c_float(scale), int(causal), kind, stream)
-    elif mode == "drawn":
+    elif mode in ("drawn", "handed"):
         st = lib.fa_fwd_dropout(*ptrs, B, H, Nq, Nk, d, ctypes.c_float(scale), int(causal), kind,
                                 ctypes.c_float(p), seed, offset, head_base, stream)
     else:
@@ -73,12 +74,14 @@ def _run(lib, q, k, v, dO, causal, kind, mode, p):
     out = {"o": o, "lse": lse}
     if d <= 128:
         dq, dk, dv = torch.full_like(q, nan), torch.full_like(k, nan), torch.full_like(v, nan)
-        ws = torch.empty(lib.fa_bwd_workspace_size(B, H, Nq, d, kind), device=dev, dtype=torch.uint8)
+        ws_bytes = (lib.fa_bwd_dropout_workspace_size(B, H, Nq, Nk, d, kind) if mode == "handed"
+                    else lib.fa_bwd_workspace_size(B, H, Nq, d, kind))
+        ws = torch.empty(ws_bytes, device=dev, dtype=torch.uint8)
         bp = ptrs[:4] + (lse.data_ptr(), dO.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr())
         if mode == "plain":
             st = lib.fa_bwd_kv(*bp, B, H, Nq, Nk, d, ctypes.c_float(scale), int(causal), kind, ws.data_ptr(),
                                ws.numel(), stream)
-        elif mode == "drawn":
+        elif mode in ("drawn", "handed"):  # handed: the dK/dV pass hands its bits to the dQ pass
             st = lib.fa_bwd_dropout(*bp, B, H, Nq, Nk, d, ctypes.c_float(scale), int(causal), kind,
                                     ctypes.c_float(p), seed, offset, head_base, ws.data_ptr(), ws.numel(), stream)
         else:
@@ -100,6 +103,7 @@ def _run(lib, q, k, v, dO, causal, kind, mode, p):
     (1, 2, 300, 513, 128, True, torch.bfloat16, "drawn", 0.2),
     (2, 2, 700, 700, 64, True, torch.bfloat16, "drawn", 0.3),
     (1, 2, 300, 513, 128, False, torch.bfloat16, "saved", 0.6),
+    (2, 2, 300, 513, 96, True, torch.float16, "handed", 0.3),
     (1, 2, 333, 333, 256, False, torch.float16, "drawn", 0.1),     # forward only
 ])
 def test_checked_build_trips_nothing_and_matches_the_default(checked_lib, B, H, Nq, Nk, d, causal, dtype, mode, p):

@@ -265,15 +265,23 @@ def _drop_ref(q, k, v, dO, scale, causal, seed, offset, p):
     return ref
 
 
-def _run_drop(q, k, v, dO, scale, causal, seed, offset, p):
+def _run_drop(q, k, v, dO, scale, causal, seed, offset, p, plain_workspace=False):
+    """Forward (and backward) with drawn keep bits. By default the backward's
+    workspace has room for the bits, so its dQ pass reads those its dK/dV
+    pass drew; plain_workspace=True makes the dQ pass draw them itself."""
     import exact_attention_97_gb300 as fa
     dev = torch.device("cuda")
     qd, kd, vd = (x.to(dev) for x in (q, k, v))
     o, lse = fa.attention_forward(qd, kd, vd, scale, causal, dropout_p=p, seed=seed, offset=offset)
     got = {"o": o, "lse": lse}
     if dO is not None:
+        ws = None
+        if plain_workspace:
+            B, H, Nq, d = q.shape
+            kind = fa.FA_F16 if q.dtype == torch.float16 else fa.FA_BF16
+            ws = torch.empty(fa.fa_bwd_workspace_size(B, H, Nq, d, kind), device=dev, dtype=torch.uint8)
         dq, dk, dv = fa.attention_backward(qd, kd, vd, o, lse, dO.to(dev), scale, causal, dropout_p=p, seed=seed,
-                                           offset=offset)
+                                           offset=offset, workspace=ws)
         got.update(dq=dq, dk=dk, dv=dv)
     torch.cuda.synchronize()
     assert fa.fa_device_status() == 0
@@ -327,10 +335,12 @@ def test_dropout_dkdv_mask_is_exact(Nk):
           _drop_ref(q, k, v, dO, 1.0 / math.sqrt(128), False, seed, offset, p))
 
 
-def test_dropout_dq_mask_is_exact():
+@pytest.mark.parametrize("plain_workspace", [False, True])
+def test_dropout_dq_mask_is_exact(plain_workspace):
     """With K the identity (Nk = d = 128), every value and every dO row equal
     to unit vector 0: dP = dO V^T = 1, D_i = sum_j Pd_ij, and dQ[i, j] =
-    scale P_ij (Z_ij / (1 - p) - D_i), positive exactly where Z_ij = 1."""
+    scale P_ij (Z_ij / (1 - p) - D_i), positive exactly where Z_ij = 1. Once
+    with the bits the dK/dV pass hands on, once drawn in the dQ pass itself."""
     seed, offset, p = 2024, 0, 0.3
     q, _, _, _ = make_qkv_do(1, 2, 300, 128, seed=12, dtype=torch.float32)
     q = (0.2 * q).to(torch.bfloat16)
@@ -340,7 +350,7 @@ def test_dropout_dq_mask_is_exact():
     dO = torch.zeros(1, 2, 300, 128)
     dO[..., 0] = 1.0
     v, dO = v.to(torch.bfloat16), dO.to(torch.bfloat16)
-    got = _run_drop(q, k, v, dO, 1.0 / math.sqrt(128), False, seed, offset, p)
+    got = _run_drop(q, k, v, dO, 1.0 / math.sqrt(128), False, seed, offset, p, plain_workspace)
     want = _mask(seed, offset, p, 1, 2, 300, 128, False)
     assert np.array_equal(got["dq"] > 0, want)
     check("dropout_dq_identity", "bf16", got, _drop_ref(q, k, v, dO, 1.0 / math.sqrt(128), False, seed, offset, p))
@@ -433,6 +443,44 @@ def test_dropout_saved_bits_give_the_regenerated_results(d, Nq, Nk, causal, dtyp
     assert fa.fa_device_status() == 0
     for a, b in zip((o1, l1, *g1), (o2, l2, *g2)):
         assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("d,Nq,Nk,causal,dtype,p", [(64, 300, 300, True, torch.bfloat16, 0.2),
+                                                    (96, 257, 700, True, torch.bfloat16, 0.2),
+                                                    (128, 1000, 1000, False, torch.bfloat16, 0.2),
+                                                    (128, 200, 777, True, torch.float16, 0.6),
+                                                    (128, 513, 300, False, torch.bfloat16, 0.6)])
+def test_dropout_bits_handed_from_dkdv_to_dq(d, Nq, Nk, causal, dtype, p):
+    """Given a workspace with room for the keep bits, the dropout backward's
+    dK/dV pass writes the bits it draws there and its dQ pass reads them: the
+    gradients equal, bit for bit, those of the backward whose passes both
+    draw, and the bits left in the workspace are the forward's saved ones on
+    every visible (query, key) pair."""
+    import exact_attention_97_gb300 as fa
+    seed, offset, head_base, B, H = 271828, 4, 3, 2, 2
+    q, _, _, dO = make_qkv_do(B, H, Nq, d, seed=50 + d, dtype=dtype)
+    _, k, v, _ = make_qkv_do(B, H, Nk, d, seed=51 + d, dtype=dtype)
+    dev = torch.device("cuda")
+    q, k, v, dO = (x.to(dev) for x in (q, k, v, dO))
+    scale = 1.0 / math.sqrt(d)
+    kw = dict(dropout_p=p, seed=seed, offset=offset, head_base=head_base)
+    kind = fa.FA_F16 if dtype == torch.float16 else fa.FA_BF16
+    mask = fa.dropout_mask_buffer(B, H, Nq, Nk, dev)
+    o, lse = fa.attention_forward(q, k, v, scale, causal, dropout_mask=mask, **kw)
+    plain = torch.empty(fa.fa_bwd_workspace_size(B, H, Nq, d, kind), device=dev, dtype=torch.uint8)
+    shared = torch.zeros(fa.fa_bwd_dropout_workspace_size(B, H, Nq, Nk, d, kind), device=dev, dtype=torch.uint8)
+    g_drawn = fa.attention_backward(q, k, v, o, lse, dO, scale, causal, workspace=plain, **kw)
+    g_handed = fa.attention_backward(q, k, v, o, lse, dO, scale, causal, workspace=shared, **kw)
+    torch.cuda.synchronize()
+    assert fa.fa_device_status() == 0
+    for a, b in zip(g_drawn, g_handed):
+        assert torch.equal(a, b)
+    got = _saved_bits(shared[plain.numel():], B, H, Nq, Nk)  # the bits follow the plain workspace
+    want = _saved_bits(mask, B, H, Nq, Nk)
+    visible = np.ones((Nq, Nk), dtype=bool)
+    if causal:
+        visible = np.arange(Nk)[None, :] <= np.arange(Nq)[:, None] + (Nk - Nq)
+    assert np.array_equal(got[..., visible], want[..., visible])
 
 
 def test_dropout_zero_is_the_plain_path():
