@@ -187,13 +187,13 @@ int fa_bwd_dropout(const void *q, const void *k, const void *v, const void *o,
 /*
  * Workspace of fa_bwd_dropout in which its two passes share the keep bits:
  * fa_bwd_workspace_size(B, H, Nq, d, dtype) plus fa_dropout_mask_size(B, H,
- * Nq, Nk) bytes (0 for a shape or dtype fa_bwd_dropout rejects). Given at
- * least this many bytes, fa_bwd_dropout's dK/dV pass writes the keep bits it
- * draws into the rest of the workspace (the saved-bits layout below) and its
- * dQ pass reads them there instead of drawing them again; with less (but at
- * least fa_bwd_workspace_size bytes) both passes draw them. The results are
- * the same, bit for bit; the larger workspace trades that memory for about a
- * quarter of the dQ pass's time.
+ * Nq, Nk) bytes (0 unless B, H, Nq, Nk >= 1, d is 64, 96 or 128 and dtype
+ * is FA_BF16 or FA_F16). Given at least this many bytes, fa_bwd_dropout's
+ * dK/dV pass writes the keep bits it draws into the rest of the workspace
+ * (the saved-bits layout below) and its dQ pass reads them there instead of
+ * drawing them again; with less (but at least fa_bwd_workspace_size bytes)
+ * both passes draw them. The results are the same, bit for bit; the larger
+ * workspace trades that memory for about a fifth of the dQ pass's time.
  */
 size_t fa_bwd_dropout_workspace_size(int B, int H, int Nq, int Nk, int d,
                                      int dtype);
