@@ -483,6 +483,30 @@ def test_dropout_bits_handed_from_dkdv_to_dq(d, Nq, Nk, causal, dtype, p):
     assert np.array_equal(got[..., visible], want[..., visible])
 
 
+def test_dropout_bits_handed_at_full_size():
+    """The same at B8 H32 N4096 d128 (32 x 32 blocks per head, every one
+    visited): the gradients with and without the handoff are bit-identical,
+    and the workspace's bits are byte for byte the forward's saved ones."""
+    import exact_attention_97_gb300 as fa
+    B, H, N, d, p = 8, 32, 4096, 128, 0.1
+    kw = dict(dropout_p=p, seed=0x5151, offset=6)
+    dev = torch.device("cuda")
+    q, k, v, dO = (x.to(dev) for x in make_qkv_do(B, H, N, d, seed=77, dtype=torch.bfloat16))
+    scale = 1.0 / math.sqrt(d)
+    mask = fa.dropout_mask_buffer(B, H, N, N, dev)
+    o, lse = fa.attention_forward(q, k, v, scale, False, dropout_mask=mask, **kw)
+    plain = torch.empty(fa.fa_bwd_workspace_size(B, H, N, d, fa.FA_BF16), device=dev, dtype=torch.uint8)
+    shared = torch.zeros(fa.fa_bwd_dropout_workspace_size(B, H, N, N, d, fa.FA_BF16), device=dev,
+                         dtype=torch.uint8)
+    g_drawn = fa.attention_backward(q, k, v, o, lse, dO, scale, False, workspace=plain, **kw)
+    g_handed = fa.attention_backward(q, k, v, o, lse, dO, scale, False, workspace=shared, **kw)
+    torch.cuda.synchronize()
+    assert fa.fa_device_status() == 0
+    for a, b in zip(g_drawn, g_handed):
+        assert torch.equal(a, b)
+    assert torch.equal(shared[plain.numel():], mask)
+
+
 def test_dropout_zero_is_the_plain_path():
     import exact_attention_97_gb300 as fa
     q, k, v, dO = (x.cuda() for x in make_qkv_do(1, 2, 260, 128, seed=8, dtype=torch.bfloat16))
